@@ -1,0 +1,444 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises ``AssertionError``
+when the oracle disagrees with a closed form, a stated invariant, a hand-worked
+golden case or brute force.  None of them re-types the oracle's own loops: they
+use exact small-integer arithmetic, special cases whose answer is known without
+running the method, and properties that characterise the unique answer.
+
+``tests/test_oracle_pins.py`` runs every pin on the oracle; ``tests/test_oracle_mutants.py``
+plants plausible mistakes in copies of the oracle source and checks that each one
+fails at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import zlib
+
+import numpy as np
+
+from workloads import bf16_bits_to_f32, f32_to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bf(a):
+    """Exact-in-bf16 floats -> bf16 bits (asserts exactness)."""
+    a = np.asarray(a, np.float32)
+    b = f32_to_bf16_bits(a)
+    assert np.array_equal(bf16_bits_to_f32(b), a), "fixture value not exact in bf16"
+    return b
+
+
+def _rng(tag):
+    return np.random.default_rng(zlib.crc32(tag.encode()))
+
+
+# ------------------------------------------------------------- logits (o1) --
+
+def pin_logits_one_hot(o):
+    """h = e_d selects column d of W_lm exactly: U[v] = W_lm[v, d]."""
+    rng = _rng("one_hot")
+    V, D = 37, 24
+    W = f32_to_bf16_bits(rng.standard_normal((V, D)).astype(np.float32))
+    h = np.zeros((D, D), np.float32)
+    np.fill_diagonal(h, 1.0)
+    U = o.logits(bf(h), W)
+    assert np.array_equal(U, bf16_bits_to_f32(W).T)
+
+
+def pin_logits_permutation(o):
+    """W_lm a permuted identity: U[p, v] = h[p, perm[v]] exactly."""
+    rng = _rng("perm")
+    D = 16
+    perm = rng.permutation(D)
+    W = np.zeros((D, D), np.float32)
+    W[np.arange(D), perm] = 1.0
+    h = f32_to_bf16_bits(rng.standard_normal((3, D)).astype(np.float32))
+    U = o.logits(h, bf(W))
+    assert np.array_equal(U, bf16_bits_to_f32(h)[:, perm])
+
+
+def pin_logits_integer_exact(o):
+    """Small-integer operands: every sum is an exact integer (brute force with Python ints)."""
+    rng = _rng("int")
+    P, V, D = 3, 11, 29
+    h = rng.integers(-8, 9, size=(P, D))
+    W = rng.integers(-8, 9, size=(V, D))
+    U = o.logits(bf(h), bf(W))
+    for p in range(P):
+        for v in range(V):
+            exact = sum(int(h[p, d]) * int(W[v, d]) for d in range(D))
+            assert U[p, v] == exact, (p, v, U[p, v], exact)
+
+
+def pin_logits_within_rounding(o):
+    """Random bf16 operands, D = 4096: the result is within one fp32 ulp of the
+    exactly rounded sum (products of bf16 values are exact; math.fsum sums exactly)."""
+    rng = _rng("fsum")
+    D = 4096
+    h = f32_to_bf16_bits(rng.standard_normal((2, D)).astype(np.float32))
+    W = f32_to_bf16_bits((rng.standard_normal((5, D)) * 0.02).astype(np.float32))
+    U = o.logits(h, W)
+    hf, Wf = bf16_bits_to_f32(h).astype(np.float64), bf16_bits_to_f32(W).astype(np.float64)
+    for p in range(2):
+        for v in range(5):
+            exact = np.float32(math.fsum(hf[p] * Wf[v]))
+            assert abs(float(U[p, v]) - float(exact)) <= float(np.spacing(np.abs(exact))), (U[p, v], exact)
+
+
+# -------------------------------------------------------------- top-K (o2) --
+
+def pin_topk_golden(o):
+    g = _golden("topk_ties.json")
+    h, W = bf(g["h"]), bf(g["W_lm"])
+    for case in g["cases"]:
+        ids, vals, margin, _ = o.unary_topk(h, W, case["K"])
+        assert ids[0].tolist() == case["ids"], (ids, case)
+        assert vals[0].tolist() == case["vals"]
+        want = math.inf if case["margin"] == "inf" else case["margin"]
+        assert margin[0] == want
+
+
+def _check_topk_properties(U, ids, vals, margin, K):
+    """The unique top-K: distinct ids; every kept (value, id) ranks above every
+    dropped one; listed in rank order; vals are the kept logits; margin is the gap
+    between the K-th kept and the best dropped value."""
+    V = U.shape[0]
+    assert len(set(ids.tolist())) == K and ids.min() >= 0 and ids.max() < V
+    assert np.array_equal(vals, U[ids])
+    keys = [(-float(U[i]), int(i)) for i in ids]
+    assert keys == sorted(keys)
+    kept = set(ids.tolist())
+    worst = keys[-1]
+    dropped = [(-float(U[i]), i) for i in range(V) if i not in kept]
+    assert all(worst < d for d in dropped)
+    if dropped:
+        assert margin == float(vals[-1]) - max(-d[0] for d in dropped)
+    else:
+        assert margin == math.inf
+
+
+def pin_topk_brute_force(o):
+    """Tiny vocabularies with many exact ties (small-integer logits, duplicate rows)."""
+    rng = _rng("topk")
+    for V, D, K in [(12, 3, 5), (40, 4, 7), (64, 2, 64), (9, 1, 1), (33, 5, 32)]:
+        h = rng.integers(-2, 3, size=(4, D))
+        W = rng.integers(-2, 3, size=(V, D))
+        W[V // 2] = W[1]  # exact duplicate rows
+        U = h @ W.T  # small integers: exact, independent of the oracle
+        ids, vals, margin, _ = o.unary_topk(bf(h), bf(W), K)
+        for p in range(4):
+            _check_topk_properties(U[p].astype(np.float32), ids[p], vals[p], margin[p], K)
+
+
+def pin_topk_k_equals_v(o):
+    rng = _rng("kv")
+    V, D = 50, 8
+    h = f32_to_bf16_bits(rng.standard_normal((2, D)).astype(np.float32))
+    W = f32_to_bf16_bits(rng.standard_normal((V, D)).astype(np.float32))
+    ids, vals, margin, _ = o.unary_topk(h, W, V)
+    for p in range(2):
+        assert sorted(ids[p].tolist()) == list(range(V))
+        assert margin[p] == math.inf
+        assert np.all(np.diff(vals[p]) <= 0)
+
+
+def pin_topk_hidden_projection(o):
+    """G = H(h): with W_H = I (r = D) G equals h; with integer operands it is exact."""
+    rng = _rng("G")
+    D = 12
+    h = rng.integers(-4, 5, size=(3, D))
+    WH = rng.integers(-3, 4, size=(5, D))
+    W = rng.integers(-3, 4, size=(7, D))
+    _, _, _, G = o.unary_topk(bf(h), bf(W), 2, W_H=bf(WH))
+    assert np.array_equal(G, (h @ WH.T).astype(np.float32))
+    _, _, _, G2 = o.unary_topk(bf(h), bf(W), 2, W_H=bf(np.eye(D)))
+    assert np.array_equal(G2, h.astype(np.float32))
+
+
+# ------------------------------------------------------------ walk (o3/o4) --
+
+def _walk_fixture(o, name):
+    g = _golden(name)
+    K, r, B = g["K"], g["r"], g["block"]
+    ids = np.asarray(g["ids"], np.int32)
+    vals = np.asarray(g["vals"], np.float32)
+    G = np.asarray(g["G"], np.float32)
+    A, Bc = bf(g["A"]), bf(g["Bc"])
+    anchors = np.asarray([g["anchor"]], np.int32)
+    path, score, margin, status = o.selector_walk(anchors, ids, vals, G, A, Bc, B)
+    return g, (ids, vals, G, A, Bc), (path, score, margin, status)
+
+
+def pin_walk_golden(o):
+    g, _, (path, score, margin, status) = _walk_fixture(o, "walk_r1_k2.json")
+    assert status == 0
+    assert path[0].tolist() == g["path"]
+    assert score[0].tolist() == g["path_score"]
+    assert margin[0].tolist() == g["margin"]
+
+
+def pin_walk_tie_lower_id(o):
+    g, _, (path, score, margin, status) = _walk_fixture(o, "walk_tie.json")
+    assert path[0].tolist() == g["path"] and score[0].tolist() == g["path_score"]
+    assert margin[0].tolist() == g["margin"]
+
+
+def pin_pair_scores_golden(o):
+    g, (ids, vals, G, A, Bc), _ = _walk_fixture(o, "walk_r1_k2.json")
+    pred = np.asarray(g["teacher_forced_pred"], np.int32)
+    scores, status = o.pair_scores(pred, ids, vals, G, A, Bc)
+    assert status == 0
+    assert scores.tolist() == g["teacher_forced_scores"]
+
+
+def _random_lattice(tag, R, B, K, V, r, cb_std=1.0, G_std=1.0):
+    rng = _rng(tag)
+    ids = np.stack([np.stack([rng.choice(V, size=K, replace=False) for _ in range(B)]) for _ in range(R)])
+    vals = -np.sort(-rng.standard_normal((R, B, K)).astype(np.float32), axis=-1)
+    G = (rng.standard_normal((R, B, r)) * G_std).astype(np.float32)
+    A = f32_to_bf16_bits((rng.standard_normal((V, r)) * cb_std).astype(np.float32))
+    Bc = f32_to_bf16_bits((rng.standard_normal((V, r)) * cb_std).astype(np.float32))
+    anchors = rng.integers(0, V, size=R).astype(np.int32)
+    return (anchors, ids.reshape(R * B, K).astype(np.int32), vals.reshape(R * B, K), G.reshape(R * B, r),
+            A, Bc)
+
+
+def pin_walk_zero_successor_is_unary(o):
+    """A zero successor codebook leaves the unary scores (SpecForge DFlash2 concept doc,
+    'Architecture'): the path is each row's unary argmax (lower id on ties) and the
+    path score its unary logit."""
+    anchors, ids, vals, G, A, _ = _random_lattice("zeroB", 5, 6, 8, 97, 16)
+    Bc = np.zeros_like(A)
+    vals[3, 2] = vals[3, 0]  # an exact unary tie
+    path, score, _, _ = o.selector_walk(anchors, ids, vals, G, A, Bc, 6)
+    for q in range(5):
+        for t in range(1, 6):
+            row = q * 6 + t
+            best = max(range(8), key=lambda j: (vals[row, j], -ids[row, j]))
+            assert path[q, t - 1] == ids[row, best]
+            assert score[q, t - 1] == vals[row, best]
+
+
+def pin_walk_k1_is_top1(o):
+    anchors, ids, vals, G, A, Bc = _random_lattice("k1", 4, 5, 1, 60, 8)
+    path, score, margin, _ = o.selector_walk(anchors, ids, vals, G, A, Bc, 5)
+    assert np.array_equal(path, ids.reshape(4, 5)[:, 1:])
+    assert np.all(np.isinf(margin))
+
+
+def pin_walk_unit_codebooks_closed_form(o):
+    """A = B = 1: S_t(a, b) = U_t(b) + sum_i G_t[i] for every predecessor; integer
+    G and unary values keep every score exact."""
+    rng = _rng("ones")
+    R, B, K, V, r = 3, 5, 4, 30, 6
+    anchors, ids, _, _, _, _ = _random_lattice("ones", R, B, K, V, r)
+    vals = rng.integers(-6, 7, size=(R * B, K)).astype(np.float32)
+    G = rng.integers(-3, 4, size=(R * B, r)).astype(np.float32)
+    one = bf(np.ones((V, r)))
+    path, score, _, _ = o.selector_walk(anchors, ids, vals, G, one, one, B)
+    scores, _ = o.pair_scores(np.zeros(R * B, np.int32), ids, vals, G, one, one)
+    want = vals + G.sum(axis=1, keepdims=True)
+    assert np.array_equal(scores, want)
+    for q in range(R):
+        for t in range(1, B):
+            row = q * B + t
+            best = max(range(K), key=lambda j: (want[row, j], -ids[row, j]))
+            assert path[q, t - 1] == ids[row, best] and score[q, t - 1] == want[row, best]
+
+
+def pin_walk_replay_matches_teacher_forced(o):
+    """Replaying the walk's own predecessors through the teacher-forced scorer gives
+    back the same path and scores (verl-SpeCo PR #62, 'Selector training objective')."""
+    R, B, K, V, r = 6, 8, 5, 80, 12
+    anchors, ids, vals, G, A, Bc = _random_lattice("replay", R, B, K, V, r)
+    path, score, _, _ = o.selector_walk(anchors, ids, vals, G, A, Bc, B)
+    pred = np.concatenate([anchors[:, None], anchors[:, None], path[:, :-1]], axis=1).reshape(-1)
+    scores, _ = o.pair_scores(pred.astype(np.int32), ids, vals, G, A, Bc)
+    scores = scores.reshape(R, B, K)
+    idsr = ids.reshape(R, B, K)
+    for q in range(R):
+        for t in range(1, B):
+            j = max(range(K), key=lambda jj: (scores[q, t, jj], -idsr[q, t, jj]))
+            assert idsr[q, t, j] == path[q, t - 1]
+            assert scores[q, t, j] == score[q, t - 1]
+
+
+def pin_walk_feeds_back_choice(o):
+    """The predecessor at row t is the token chosen at row t-1: changing only the
+    row-1 unary values so that a different token is picked changes row 2's scores
+    as the pair-score formula says (checked with the fixture's exact numbers)."""
+    g = _golden("walk_r1_k2.json")
+    ids = np.asarray(g["ids"], np.int32)
+    vals = np.asarray(g["vals"], np.float32).copy()
+    vals[1] = [10.0, 0.5]  # now token 0 wins row 1: S(1,0) = 12.0 > S(1,2) = 4.5
+    path, score, _, _ = o.selector_walk(np.asarray([g["anchor"]], np.int32), ids, vals,
+                                        np.asarray(g["G"], np.float32), bf(g["A"]), bf(g["Bc"]), 3)
+    assert path[0].tolist() == [0, 3] and score[0].tolist() == [12.0, 0.5]
+
+
+def pin_walk_rejects_bad_ids(o):
+    anchors, ids, vals, G, A, Bc = _random_lattice("bad", 3, 4, 3, 20, 4)
+    anchors = anchors.copy()
+    anchors[1] = 20
+    path, score, _, status = o.selector_walk(anchors, ids, vals, G, A, Bc, 4)
+    assert status == 1 and np.all(path[1] == -1) and np.all(np.isnan(score[1]))
+    assert np.all(path[0] >= 0) and np.all(path[2] >= 0)
+    pred = np.zeros(12, np.int32)
+    pred[5] = -1
+    s, st = o.pair_scores(pred, ids, vals, G, A, Bc)
+    assert st == 1 and np.all(np.isnan(s[5])) and not np.any(np.isnan(np.delete(s, 5, axis=0)))
+
+
+# ---------------------------------------------------------------- conv (o5) --
+
+def pin_conv_golden(o):
+    g = _golden("conv_2tap_1group.json")
+    x = np.asarray(g["x"], np.float32)
+    y, dyn = o.conv_prepare(x, g["block"], g["taps"], g["group"], bf(g["W_proj"]),
+                            np.asarray(g["base"], np.float32))
+    assert y.tolist() == g["y"] and dyn.tolist() == g["dyn_out"]
+    z = np.asarray(g["z"], np.float32)
+    yf = o.conv_finish(z, g["block"], g["taps"], g["group"], dyn, np.asarray(g["base"], np.float32))
+    assert yf.tolist() == g["y_finish"]
+    # the same case through bf16 activations (all values exact in bf16)
+    yb, dynb = o.conv_prepare(bf(x), g["block"], g["taps"], g["group"], bf(g["W_proj"]),
+                              np.asarray(g["base"], np.float32))
+    assert bf16_bits_to_f32(yb).tolist() == g["y"] and dynb.tolist() == g["dyn_out"]
+
+
+def _identity_base(taps, C):
+    base = np.zeros((2, taps, C), np.float32)
+    base[:, 0, :] = 1.0
+    return base
+
+
+def pin_conv_identity_at_init(o):
+    """Base tap 0 = 1, later taps 0, projection 0: an exact no-op (verl-SpeCo PR #62,
+    'Two deltas', item 2; SpecForge DFlash2 concept doc, 'Architecture')."""
+    rng = _rng("ident")
+    for taps, B in [(2, 8), (4, 4), (1, 3)]:
+        P, C, g = 3 * B, 48, 16
+        Wp = np.zeros((2 * taps * (C // g), C), np.uint16)
+        base = _identity_base(taps, C)
+        xf = rng.standard_normal((P, C)).astype(np.float32)
+        xb = f32_to_bf16_bits(xf)
+        for x in (xf, xb):
+            y, dyn = o.conv_prepare(x, B, taps, g, Wp, base)
+            assert np.array_equal(y, x) and not np.any(dyn)
+            yf = o.conv_finish(x, B, taps, g, dyn, base)
+            assert np.array_equal(yf, x)
+
+
+def pin_conv_block_locality(o):
+    """Changing the last row of block n leaves every row of block n+1 bit-identical
+    (verl-SpeCo PR #62, 'Two deltas', item 1; vLLM guide, 'Local Convolution')."""
+    rng = _rng("local")
+    B, taps, C, g, nb = 4, 3, 32, 8, 3
+    P = B * nb
+    x = f32_to_bf16_bits(rng.standard_normal((P, C)).astype(np.float32))
+    Wp = f32_to_bf16_bits((rng.standard_normal((2 * taps * (C // g), C)) * 0.1).astype(np.float32))
+    base = rng.standard_normal((2, taps, C)).astype(np.float32)
+    y0, d0 = o.conv_prepare(x, B, taps, g, Wp, base)
+    f0 = o.conv_finish(x, B, taps, g, d0, base)
+    x2 = x.copy()
+    x2[B - 1] = f32_to_bf16_bits(rng.standard_normal(C).astype(np.float32) * 50)
+    y1, d1 = o.conv_prepare(x2, B, taps, g, Wp, base)
+    f1 = o.conv_finish(x2, B, taps, g, d0, base)
+    assert np.array_equal(y0[B:], y1[B:]) and np.array_equal(d0[B:], d1[B:])
+    assert np.array_equal(f0[B:], f1[B:])
+    assert not np.array_equal(y0[B - 1], y1[B - 1])
+
+
+def pin_conv_static_kernel_closed_form(o):
+    """Zero projection: y_t = sum_{j<=t} base[j] * x_{t-j}, exact for small integers;
+    taps = block makes the last position read the whole block."""
+    rng = _rng("static")
+    for taps, B in [(2, 4), (4, 4), (3, 5)]:
+        P, C, g = 2 * B, 8, 4
+        x = rng.integers(-5, 6, size=(P, C)).astype(np.float32)
+        base = rng.integers(-3, 4, size=(2, taps, C)).astype(np.float32)
+        Wp = np.zeros((2 * taps * (C // g), C), np.uint16)
+        y, _ = o.conv_prepare(x, B, taps, g, Wp, base)
+        yf = o.conv_finish(x, B, taps, g, np.zeros((P, taps, C // g), np.float32), base)
+        for p in range(P):
+            t = p % B
+            want = sum(base[0, j] * x[p - j] for j in range(taps) if t - j >= 0)
+            wantf = sum(base[1, j] * x[p - j] for j in range(taps) if t - j >= 0)
+            assert np.array_equal(y[p], want) and np.array_equal(yf[p], wantf), (taps, B, p)
+
+
+def pin_conv_group_sharing(o):
+    """One non-zero projection row (input side, tap j, group gi) changes only the g
+    channels of group gi, only through tap j, and leaves dyn_out at zero; a row on
+    the output side changes only dyn_out[., j, gi] = W_proj row . x_p."""
+    rng = _rng("group")
+    B, taps, C, g = 4, 2, 24, 8
+    G = C // g
+    P = 2 * B
+    x = rng.integers(-4, 5, size=(P, C)).astype(np.float32)
+    base = rng.integers(-2, 3, size=(2, taps, C)).astype(np.float32)
+    zero = np.zeros((2 * taps * G, C), np.float32)
+    y0, _ = o.conv_prepare(x, B, taps, g, bf(zero), base)
+    for j in range(taps):
+        for gi in range(G):
+            Wp = zero.copy()
+            Wp[(0 * taps + j) * G + gi] = rng.integers(-2, 3, size=C)
+            y, dyn = o.conv_prepare(x, B, taps, g, bf(Wp), base)
+            assert not np.any(dyn)
+            d = x @ Wp[(0 * taps + j) * G + gi]
+            for p in range(P):
+                t = p % B
+                delta = np.zeros(C, np.float32)
+                if t - j >= 0:
+                    delta[gi * g:(gi + 1) * g] = d[p] * x[p - j, gi * g:(gi + 1) * g]
+                assert np.array_equal(y[p], y0[p] + delta), (j, gi, p)
+            Wo = zero.copy()
+            Wo[(1 * taps + j) * G + gi] = rng.integers(-2, 3, size=C)
+            y2, dyn2 = o.conv_prepare(x, B, taps, g, bf(Wo), base)
+            assert np.array_equal(y2, y0)
+            want = np.zeros((P, taps, G), np.float32)
+            want[:, j, gi] = x @ Wo[(1 * taps + j) * G + gi]
+            assert np.array_equal(dyn2, want)
+
+
+def pin_conv_bf16_rounding(o):
+    """bf16 output is the exact result rounded once to nearest-even: a value just
+    above a bf16 midpoint by less than an fp32 ulp must round up (rounding through
+    fp32 first would land on the midpoint and round to even, i.e. down)."""
+    C, g, B, taps = 2, 2, 1, 1
+    x = bf(np.ones((1, C)))
+    base = np.zeros((2, taps, C), np.float32)
+    base[0, 0, :] = np.float32(1 + 2.0**-8)
+    Wp = np.zeros((2, C), np.float32)
+    Wp[0, 0] = 2.0**-40   # d = 2^-40 for the single group
+    y, _ = o.conv_prepare(x, B, taps, g, bf(Wp), base)
+    assert bf16_bits_to_f32(y).tolist() == [[1 + 2.0**-7, 1 + 2.0**-7]]
+    y2, _ = o.conv_prepare(x, B, taps, g, bf(np.zeros((2, C))), base)
+    assert bf16_bits_to_f32(y2).tolist() == [[1.0, 1.0]]  # exact midpoint: ties to even
+    base[0, 0, :] = np.float32(1 + 2.0**-8 + 2.0**-23)
+    y3, _ = o.conv_prepare(x, B, taps, g, bf(np.zeros((2, C))), base)
+    assert bf16_bits_to_f32(y3).tolist() == [[1 + 2.0**-7, 1 + 2.0**-7]]
+
+
+def pin_conv_rejects_bad_shapes(o):
+    x = np.zeros((6, 8), np.float32)
+    base = np.zeros((2, 2, 8), np.float32)
+    Wp = np.zeros((2 * 2 * 2, 8), np.uint16)
+    for B, taps, g in [(4, 2, 4), (3, 4, 4), (3, 2, 3)]:  # P % B, taps > B, C % g
+        try:
+            o.conv_prepare(x, B, taps, g, Wp, base)
+        except ValueError:
+            continue
+        raise AssertionError(f"accepted block={B} taps={taps} group={g}")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

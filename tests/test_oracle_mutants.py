@@ -1,0 +1,77 @@
+"""Plant plausible mistakes in copies of the oracle source; each must fail a pin.
+
+This is how the pins are shown to pin something: a dropped term, a wrong sign or
+index, a transposed operand or a reversed tie rule anywhere in the oracle has to
+be caught.  The mutants are compiled from text substitutions into a temporary
+directory; the oracle itself is never modified."""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, original text, replacement).  Every original must occur exactly once.
+MUTANTS = [
+    ("topk_tie_toward_higher_id",
+     "return (a->id > b->id) - (a->id < b->id);", "return (a->id < b->id) - (a->id > b->id);"),
+    ("topk_margin_from_top1",
+     "(double)c[K - 1].val - (double)c[K].val", "(double)c[0].val - (double)c[K].val"),
+    ("logits_reversed_operand",
+     "acc += bf16_value(h[p * D + d]) * bf16_value(W_lm[v * D + d]);",
+     "acc += bf16_value(h[p * D + d]) * bf16_value(W_lm[v * D + (D - 1 - d)]);"),
+    ("logits_dropped_last_term",
+     "            for (int64_t d = 0; d < D; ++d)\n                acc += bf16_value(h[p * D + d]) * bf16_value(W[v * D + d]);",
+     "            for (int64_t d = 0; d + 1 < D; ++d)\n                acc += bf16_value(h[p * D + d]) * bf16_value(W[v * D + d]);"),
+    ("G_wrong_row",
+     "bf16_value(W_H[(int64_t)i * D + d])", "bf16_value(W_H[(int64_t)(r - 1 - i) * D + d])"),
+    ("walk_no_feedback", "            a = best_id;", "            a = anchors[q];"),
+    ("walk_tie_toward_higher_id", "(s == best && b < best_id)", "(s == best && b > best_id)"),
+    ("pair_drops_context_gate", "* (double)Grow[i] *", "*"),
+    ("pair_sign_flip", "        s += bf16_value(A[", "        s -= bf16_value(A["),
+    ("walk_gate_from_previous_row",
+     "float s = pair_score(vals[row * K + j], a, b, G + row * r, A, Bc, r);",
+     "float s = pair_score(vals[row * K + j], a, b, G + (row - 1) * r, A, Bc, r);"),
+    ("pair_wrong_predecessor", "        int32_t a = pred[p];", "        int32_t a = ids[p * K];"),
+    ("walk_margin_unflagged_ties", "                } else if (s > second) {", "                } else if (s > second && s < best) {"),
+    ("conv_crosses_block",
+     "                if (t - j < 0) continue;\n                double k = (double)base[((int64_t)0",
+     "                if (p - j < 0) continue;\n                double k = (double)base[((int64_t)0"),
+    ("conv_group_strided",
+     "d[((int64_t)0 * taps + j) * G + c / g];", "d[((int64_t)0 * taps + j) * G + c % G];"),
+    ("conv_proj_io_j_swapped",
+     "d[((int64_t)0 * taps + j) * G + c / g];", "d[((int64_t)j * 2 + 0) * G + c / g];"),
+    ("conv_tap_reads_current_row",
+     "acc += k * act_value(x, x_is_f32, (p - j) * C + c);", "acc += k * act_value(x, x_is_f32, p * C + c);"),
+    ("conv_finish_uses_input_base",
+     "double k = (double)base[((int64_t)1 * taps + j) * C + c] +",
+     "double k = (double)base[((int64_t)0 * taps + j) * C + c] +"),
+    ("conv_finish_ignores_dynamic",
+     "(double)dyn_out[(p * taps + j) * G + c / g];", "0.0 * (double)dyn_out[(p * taps + j) * G + c / g];"),
+    ("conv_dyn_out_from_input_side",
+     "(float)d[((int64_t)1 * taps + j) * G + gi];", "(float)d[((int64_t)0 * taps + j) * G + gi];"),
+    ("bf16_double_rounding", "    if (lo == 0x8000u) {", "    if (0) {"),
+    ("conv_no_validation", "P % Bsz == 0;", "1;"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle.SOURCE) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name,orig,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, source, name, orig, repl):
+    assert source.count(orig) == 1, f"mutation site for {name} not unique/found"
+    src = tmp_path / f"{name}.c"
+    src.write_text(source.replace(orig, repl))
+    lib = oracle.build(str(src), str(tmp_path / f"lib{name}.so"), force=True)
+    o = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
