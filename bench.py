@@ -1,0 +1,437 @@
+"""Benchmark of the DFlash2 draft-block head on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one pass of the whole head over one draft batch of the workload:
+conv_prepare -> conv_finish (one sublayer's conv pair) -> unary_topk (logits,
+top-K, hidden projection) -> selector_walk -> selector_pair_scores.  Inputs are
+seeded synthetic tensors (see workloads/), resident in HBM before timing; the
+step streams the whole LM head (1.25 GB for the default batch-1 workload, larger
+than the 129 MB L2), so no separate L2 flush is needed for the default workload;
+other workloads flush L2 with a 256 MB write between steps.
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica on its own GPU (the head shards by requests with no exchange: "weak"
+scaling); the time is the max over ranks.  --impl reference times the CPU oracle
+on the host cores on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+import workloads as W  # noqa: E402
+
+METRIC = "draft positions/s (topK+selector walk) and conv GB/s, % of HBM/TC roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def head_bytes(w):
+    """Algorithmic bytes of unary_topk: W_lm + W_H + h read once, ids/vals/G written."""
+    return (w.V * w.D * 2 + w.r * w.D * 2 + w.P * w.D * 2 + w.P * w.K * 8 + w.P * w.r * 4)
+
+
+def conv_bytes(w, which):
+    C, P, G = w.C, w.P, w.G
+    act = 2 if w.act == "bf16" else 4
+    if which == "prepare":  # x read, y written, W_proj read, dyn_out written, base read
+        return P * C * act * 2 + 2 * w.taps * G * C * 2 + P * w.taps * G * 4 + 2 * w.taps * C * 4
+    return P * C * act * 2 + P * w.taps * G * 4 + 2 * w.taps * C * 4  # finish
+
+
+def config_of(w):
+    return {"workload": f"{w.name}: V={w.V} D={w.D} r={w.r} K={w.K} block={w.B} requests={w.R} "
+                        f"(P={w.P} positions) conv taps={w.taps} group={w.g}",
+            "positions_per_step": w.P, "drafted_positions_per_step": w.R * (w.B - 1),
+            "l2": ("inputs larger than L2: the 1.25+ GB LM head is streamed every step"
+                   if w.V * w.D * 2 > 256 << 20 else "L2 flushed between steps (256 MB write)")}
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [l.split(",") for l in (self.out or "").strip().splitlines() if l.count(",") >= 8]
+        if not rows:
+            try:
+                one = subprocess.run(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits", "-i", str(self.dev)],
+                                     capture_output=True, text=True, timeout=10).stdout
+                rows = [l.split(",") for l in one.strip().splitlines() if l.count(",") >= 8]
+            except (OSError, subprocess.TimeoutExpired):
+                rows = []
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm = []
+        smax = None
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                pass
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# -------------------------------------------------------------- GPU arm --
+
+class Step:
+    """Device-resident inputs/outputs of one workload and the five calls."""
+
+    def __init__(self, w, device, torch, df2):
+        self.w, self.torch, self.df2 = w, torch, df2
+        inp = W.head_inputs(w)
+        conv = W.conv_inputs(w)
+
+        def bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+        def dv(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+        self.host = {"h": inp["h"], "x": conv["x"], "z": conv["z"], "anchors": inp["anchors"],
+                     "pred": inp["pred"]}
+        self.h, self.W_lm, self.W_H = bf(inp["h"]), bf(inp["W_lm"]), bf(inp["W_H"])
+        self.A, self.Bc = bf(inp["A"]), bf(inp["Bc"])
+        self.anchors, self.pred = dv(inp["anchors"]), dv(inp["pred"])
+        act = bf if w.act == "bf16" else dv
+        self.x, self.z = act(conv["x"]), act(conv["z"])
+        self.W_proj, self.base = bf(conv["W_proj"]), dv(conv["base"])
+        P, K, r, G = w.P, w.K, w.r, w.G
+        e = torch.empty
+        self.ids = e((P, K), dtype=torch.int32, device=device)
+        self.vals = e((P, K), dtype=torch.float32, device=device)
+        self.Gt = e((P, r), dtype=torch.float32, device=device)
+        self.path = e((w.R, w.B - 1), dtype=torch.int32, device=device)
+        self.pscore = e((w.R, w.B - 1), dtype=torch.float32, device=device)
+        self.scores = e((P, K), dtype=torch.float32, device=device)
+        self.y = torch.empty_like(self.x)
+        self.y2 = torch.empty_like(self.z)
+        self.dyn = e((P, w.taps, G), dtype=torch.float32, device=device)
+        self.ws_head = e(max(1, df2.unary_topk_workspace_size(P, w.D, w.V, K, r)), dtype=torch.uint8,
+                         device=device)
+        dt = df2.DF2_DTYPE_BF16 if w.act == "bf16" else df2.DF2_DTYPE_F32
+        self.ws_conv = e(max(1, df2.conv_prepare_workspace_size(P, w.C, w.taps, w.g, dt)),
+                         dtype=torch.uint8, device=device)
+        self.flush = None
+        if w.V * w.D * 2 <= 256 << 20:
+            self.flush = e(256 << 20, dtype=torch.uint8, device=device)
+
+    def run(self, events=None):
+        d, w = self.df2, self.w
+        ev = events or [None] * 6
+        self._rec(ev[0])
+        d.conv_prepare(self.x, w.B, w.taps, w.g, self.W_proj, self.base, workspace=self.ws_conv,
+                       out=(self.y, self.dyn))
+        self._rec(ev[1])
+        d.conv_finish(self.z, w.B, w.taps, w.g, self.dyn, self.base, out=self.y2)
+        self._rec(ev[2])
+        d.unary_topk(self.h, self.W_lm, w.K, self.W_H, workspace=self.ws_head,
+                     out=(self.ids, self.vals, self.Gt))
+        self._rec(ev[3])
+        d.selector_walk(self.anchors, self.ids, self.vals, self.Gt, self.A, self.Bc, w.B,
+                        out=(self.path, self.pscore))
+        self._rec(ev[4])
+        d.selector_pair_scores(self.pred, self.ids, self.vals, self.Gt, self.A, self.Bc,
+                               out=self.scores)
+        self._rec(ev[5])
+
+    @staticmethod
+    def _rec(e):
+        if e is not None:
+            e.record()
+
+    def outputs(self):
+        return [self.ids, self.vals, self.path, self.pscore, self.scores, self.y, self.y2, self.dyn]
+
+
+def count_launches(step, torch):
+    """Kernels one step launches, counted by the profiler (CUPTI)."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step.run()
+            torch.cuda.synchronize()
+        names = []
+        for e in prof.events():
+            dt = str(getattr(e, "device_type", ""))
+            if "CUDA" in dt and not e.name.lower().startswith(("memcpy", "memset")):
+                names.append(e.name)
+        return len(names), sorted(set(names))
+    except Exception as exc:  # profiler unavailable: report it rather than guess
+        return None, [f"profiler unavailable: {exc}"]
+
+
+def gpu_arm(args, w, rank, world, torch):
+    import dflash2_draft_block_gb300 as df2
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    step = Step(w, device, torch, df2)
+    for _ in range(args.warmup):
+        step.run()
+        if step.flush is not None:
+            step.flush.zero_()
+    torch.cuda.synchronize()
+    n_launch, kernel_names = count_launches(step, torch)
+
+    # ---- device-resident timing (W warm-up done above), per-call events
+    nev = 6
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush_ms = 0.0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record()
+        for s in range(args.steps):
+            step.run(evs[s])
+            if step.flush is not None:
+                step.flush.zero_()
+        t1.record()
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    per_call = np.zeros(nev - 1)
+    for s in range(args.steps):
+        for i in range(nev - 1):
+            per_call[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+    if step.flush is not None:
+        # the flush runs between timed steps; its time is subtracted
+        fe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        fe[0].record()
+        for _ in range(5):
+            step.flush.zero_()
+        fe[1].record()
+        torch.cuda.synchronize()
+        flush_ms = fe[0].elapsed_time(fe[1]) / 5 * args.steps
+    step_ms = (total_ms - flush_ms) / args.steps
+    if dist is not None:
+        t = torch.tensor([step_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    per_call_us = (per_call / args.steps * 1e3).tolist()
+
+    # ---- end to end through the public API with host buffers
+    pinned_in = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v))
+                 .pin_memory() for k, v in step.host.items()}
+    dev_in = {"h": step.h, "x": step.x, "z": step.z, "anchors": step.anchors, "pred": step.pred}
+    outs = step.outputs()
+    pinned_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in pinned_in.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def e2e_step():
+        for k, v in pinned_in.items():
+            dst = dev_in[k]
+            dst.view(torch.uint8).reshape(-1).copy_(v.view(torch.uint8).reshape(-1), non_blocking=True)
+        step.run()
+        for o, po in zip(outs, pinned_out):
+            po.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+        if step.flush is not None:
+            step.flush.zero_()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+        if step.flush is not None:
+            step.flush.zero_()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = (e0.elapsed_time(e1) - flush_ms) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    clocks = clk.summary()
+    out = None
+    if rank == 0:
+        peaks, src = load_peaks()
+        hb = head_bytes(w)
+        head_us = per_call_us[2]
+        achieved = hb / (head_us * 1e-6) / 1e9
+        out = {
+            "metric": METRIC,
+            "value": w.P * world / (step_ms * 1e-3),
+            "unit": "positions/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": step_ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and scales of the workload, no dataset or checkpoint)",
+            "config": config_of(w),
+            "drafted_positions_per_s": w.R * (w.B - 1) * world / (step_ms * 1e-3),
+            "per_call_us": dict(zip(["conv_prepare", "conv_finish", "unary_topk", "selector_walk",
+                                     "selector_pair_scores"], per_call_us)),
+            "conv_gbs": {"prepare": conv_bytes(w, "prepare") / (per_call_us[0] * 1e-6) / 1e9,
+                         "finish": conv_bytes(w, "finish") / (per_call_us[1] * 1e-6) / 1e9},
+            "roofline": {"kernel": "dflash2_unary_topk (all its launches)", "bound": "hbm",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "peak_source": src,
+                         "traffic": None, "algorithmic_bytes": hb},
+            "e2e": {"value": w.P * world / (e2e_ms * 1e-3), "unit": "positions/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": None if n_launch is None else n_launch * args.steps,
+            "kernels_per_step": n_launch,
+            "kernel_names": kernel_names,
+            "clocks": clocks,
+        }
+    if dist is not None:
+        dist.destroy_process_group()
+    return out
+
+
+# ------------------------------------------------------------ oracle arm --
+
+def oracle_step(orc, w, inp, conv):
+    """The whole head on the CPU oracle for one draft batch (all P rows)."""
+    y, dyn = orc.conv_prepare(conv["x"], w.B, w.taps, w.g, conv["W_proj"], conv["base"])
+    orc.conv_finish(conv["z"], w.B, w.taps, w.g, dyn, conv["base"])
+    ids, vals, _, G = orc.unary_topk(inp["h"], inp["W_lm"], w.K, W_H=inp["W_H"])
+    orc.selector_walk(inp["anchors"], ids, vals, G, inp["A"], inp["Bc"], w.B)
+    orc.pair_scores(inp["pred"], ids, vals, G, inp["A"], inp["Bc"])
+
+
+def oracle_sample(w):
+    """A bounded slice of the workload for the CPU oracle: the first requests, so one
+    oracle step costs at most ~8 LM-head rows of work."""
+    rows_budget = 8
+    R = max(1, min(w.R, rows_budget // w.B if w.B <= rows_budget else 1))
+    return w.scaled(R=R), R
+
+
+def cpu_arm(w, steps, warmup):
+    import oracle
+    orc = oracle.default()
+    ws, R = oracle_sample(w)
+    inp = W.head_inputs(ws)
+    conv = W.conv_inputs(ws)
+    for _ in range(warmup):
+        oracle_step(orc, ws, inp, conv)
+    t = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(orc, ws, inp, conv)
+    dt = (time.perf_counter() - t) / max(1, steps)
+    sample = (f"{R} of {w.R} requests ({ws.P} positions) per step: the full head on them "
+              f"(conv pair, {ws.P} x {w.V} logits, full-sort top-{w.K}, walk, pair scores)")
+    return ws.P / dt, orc.num_threads(), sample, dt
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="batch1", choices=[c.name for c in W.CONFIGS if not c.conv_only])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    w = W.BY_NAME[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        value, cores, sample, dt = cpu_arm(w, args.steps, max(0, args.warmup))
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w),
+                "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    # the oracle runs before the first CUDA call (its threads, not a forked pool)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        value, cores, sample, dt = cpu_arm(w, steps=2, warmup=0)
+        cpu = {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
+               "sample": sample}
+    import torch
+    out = gpu_arm(args, w, rank, world, torch)
+    if rank == 0:
+        out["cpu_baseline"] = cpu
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+// The C-ABI of libdflash2: argument validation, workspace sizing and dispatch.
+// Every rule checked here is stated beside the call in include/dflash2.h.
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "head_tc.h"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+int num_sms_current() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? DF2_OK : DF2_ERR_CUDA; }
+
+size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+}  // namespace
+
+DF2_API const char* dflash2_status_string(int status) {
+    switch (status) {
+        case DF2_OK: return "DF2_OK";
+        case DF2_ERR_INVALID_ARGUMENT: return "DF2_ERR_INVALID_ARGUMENT";
+        case DF2_ERR_UNSUPPORTED: return "DF2_ERR_UNSUPPORTED";
+        case DF2_ERR_CUDA: return "DF2_ERR_CUDA";
+        case DF2_ERR_WORKSPACE_TOO_SMALL: return "DF2_ERR_WORKSPACE_TOO_SMALL";
+        case DF2_ERR_TIMEOUT: return "DF2_ERR_TIMEOUT";
+        default: return "DF2_ERR_UNKNOWN";
+    }
+}
+
+DF2_API int dflash2_abi_version(void) { return kAbiVersion; }
+
+// ------------------------------------------------------------ unary_topk --
+
+namespace {
+
+int check_head(int64_t P, int64_t D, int64_t V, int K, int r, bool has_wh) {
+    if (P < 0 || D < 1 || V < 1 || K < 1 || K > V) return DF2_ERR_INVALID_ARGUMENT;
+    if (has_wh && r < 1) return DF2_ERR_INVALID_ARGUMENT;
+    if (D % 8 != 0 || K > DF2_MAX_TOPK || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (has_wh && (r > DF2_MAX_RANK || r % 8 != 0)) return DF2_ERR_UNSUPPORTED;
+    if (!df2::head_simple_supported(D, K)) return DF2_ERR_UNSUPPORTED;
+    return DF2_OK;
+}
+
+}  // namespace
+
+DF2_API size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V, int K, int r) {
+    (void)r;
+    if (check_head(P, D, V, K, 0, false) != DF2_OK || P == 0) return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0) return 0;
+    size_t need = 0;
+    if (df2::head_tc_supported(P, D, V, K)) need = df2::head_tc_workspace(P, D, V, K, sms);
+    else need = df2::head_simple_workspace(P, D, V, K, sms);
+    return round_up(need, 256);
+}
+
+DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,
+                               int64_t V, int K, const uint16_t* W_H, int r, float* G,
+                               int32_t* topk_ids, float* topk_vals, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    const bool has_wh = W_H != nullptr;
+    int rc = check_head(P, D, V, K, r, has_wh);
+    if (rc != DF2_OK) return rc;
+    if (P == 0) return DF2_OK;
+    if (!h || !W_lm || !topk_ids || !topk_vals || (has_wh && !G)) return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(h) || !aligned16(W_lm) || !aligned16(topk_ids) || !aligned16(topk_vals) ||
+        (has_wh && (!aligned16(W_H) || !aligned16(G))) || !aligned16(workspace))
+        return DF2_ERR_UNSUPPORTED;
+    const int sms = num_sms_current();
+    if (sms <= 0) return DF2_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool tc = df2::head_tc_supported(P, D, V, K);
+    const size_t need = round_up(tc ? df2::head_tc_workspace(P, D, V, K, sms)
+                                    : df2::head_simple_workspace(P, D, V, K, sms), 256);
+    if (workspace_bytes < need || (need > 0 && !workspace)) return DF2_ERR_WORKSPACE_TOO_SMALL;
+    if (tc) {
+        rc = df2::head_tc_launch(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
+                                 dev_status, sms, st);
+        return rc;
+    }
+    cudaError_t e = df2::head_simple_launch(h, P, D, W_lm, V, K, topk_ids, topk_vals, workspace,
+                                            sms, st);
+    if (e != cudaSuccess) return DF2_ERR_CUDA;
+    if (has_wh) {
+        e = df2::gemm_simple_launch(h, false, W_H, P, r, D, G, r, r, G, r, st);
+        if (e != cudaSuccess) return DF2_ERR_CUDA;
+    }
+    return DF2_OK;
+}
+
+// -------------------------------------------------------------- selector --
+
+namespace {
+
+int check_selector(int64_t V, int K, int r) {
+    if (V < 1 || K < 1 || r < 1) return DF2_ERR_INVALID_ARGUMENT;
+    if (K > DF2_MAX_TOPK || r > DF2_MAX_RANK || r % 8 != 0 || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    return DF2_OK;
+}
+
+}  // namespace
+
+DF2_API int dflash2_selector_walk(const int32_t* anchors, int R, int B, const int32_t* topk_ids,
+                                  const float* topk_vals, const float* G, const uint16_t* A,
+                                  const uint16_t* Bc, int64_t V, int K, int r, int32_t* path,
+                                  float* path_scores, int32_t* dev_status, void* stream) {
+    if (R < 0 || B < 2 || K > V) return DF2_ERR_INVALID_ARGUMENT;
+    int rc = check_selector(V, K, r);
+    if (rc != DF2_OK) return rc;
+    if (R == 0) return DF2_OK;
+    if (!anchors || !topk_ids || !topk_vals || !G || !A || !Bc || !path || !path_scores)
+        return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(G) || !aligned16(A) || !aligned16(Bc)) return DF2_ERR_UNSUPPORTED;
+    return from_cuda(df2::walk_launch(anchors, R, B, topk_ids, topk_vals, G, A, Bc, V, K, r, path,
+                                      path_scores, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+DF2_API int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* topk_ids,
+                                         const float* topk_vals, const float* G, const uint16_t* A,
+                                         const uint16_t* Bc, int64_t V, int K, int r, float* scores,
+                                         int32_t* dev_status, void* stream) {
+    if (P < 0) return DF2_ERR_INVALID_ARGUMENT;
+    int rc = check_selector(V, K, r);
+    if (rc != DF2_OK) return rc;
+    if (P == 0) return DF2_OK;
+    if (!pred || !topk_ids || !topk_vals || !G || !A || !Bc || !scores)
+        return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(G) || !aligned16(A) || !aligned16(Bc)) return DF2_ERR_UNSUPPORTED;
+    if ((P + 7) / 8 > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    return from_cuda(df2::pair_scores_launch(pred, P, topk_ids, topk_vals, G, A, Bc, V, K, r,
+                                             scores, dev_status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------ conv --
+
+namespace {
+
+int check_conv(int dtype, int64_t P, int C, int B, int taps, int g) {
+    if (dtype != DF2_DTYPE_BF16 && dtype != DF2_DTYPE_F32) return DF2_ERR_INVALID_ARGUMENT;
+    if (P < 0 || C < 1 || B < 1 || g < 1 || taps < 1 || taps > B) return DF2_ERR_INVALID_ARGUMENT;
+    if (C % g != 0 || P % B != 0) return DF2_ERR_INVALID_ARGUMENT;
+    if (C % 8 != 0) return DF2_ERR_UNSUPPORTED;
+    if ((P + 63) / 64 > 65535) return DF2_ERR_UNSUPPORTED;
+    return DF2_OK;
+}
+
+}  // namespace
+
+DF2_API size_t dflash2_conv_prepare_workspace_size(int64_t P, int C, int taps, int g, int dtype) {
+    if (P <= 0 || C < 1 || g < 1 || taps < 1 || C % g != 0) return 0;
+    (void)dtype;
+    return round_up(size_t(P) * taps * (C / g) * sizeof(float), 256);
+}
+
+DF2_API int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int B, int taps, int g,
+                                 const uint16_t* W_proj, const float* base, void* y, float* dyn_out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_conv(dtype, P, C, B, taps, g);
+    if (rc != DF2_OK) return rc;
+    if (P == 0) return DF2_OK;
+    if (!x || !W_proj || !base || !y || !dyn_out || x == y) return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(base) || !aligned16(W_proj) ||
+        !aligned16(dyn_out) || !aligned16(workspace))
+        return DF2_ERR_UNSUPPORTED;
+    const size_t need = dflash2_conv_prepare_workspace_size(P, C, taps, g, dtype);
+    if (workspace_bytes < need || !workspace) return DF2_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int G = C / g;
+    const int64_t half = int64_t(taps) * G;
+    float* d_in = static_cast<float*>(workspace);
+    cudaError_t e = df2::gemm_simple_launch(x, dtype == DF2_DTYPE_F32, W_proj, P, 2 * half, C, d_in,
+                                            half, half, dyn_out, half, st);
+    if (e != cudaSuccess) return DF2_ERR_CUDA;
+    e = df2::conv_apply_launch(x, dtype == DF2_DTYPE_F32, P, C, B, taps, g, base, d_in, half, y, st);
+    return from_cuda(e);
+}
+
+DF2_API int dflash2_conv_finish(const void* z, int dtype, int64_t P, int C, int B, int taps, int g,
+                                const float* dyn_out, const float* base, void* y, void* stream) {
+    int rc = check_conv(dtype, P, C, B, taps, g);
+    if (rc != DF2_OK) return rc;
+    if (P == 0) return DF2_OK;
+    if (!z || !dyn_out || !base || !y || z == y) return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(z) || !aligned16(y) || !aligned16(base) || !aligned16(dyn_out))
+        return DF2_ERR_UNSUPPORTED;
+    const int G = C / g;
+    return from_cuda(df2::conv_apply_launch(z, dtype == DF2_DTYPE_F32, P, C, B, taps, g,
+                                            base + int64_t(taps) * C, dyn_out, int64_t(taps) * G, y,
+                                            static_cast<cudaStream_t>(stream)));
+}

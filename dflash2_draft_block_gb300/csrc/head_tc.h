@@ -1,0 +1,16 @@
+// Tensor-core (tcgen05/TMEM, TMA-fed) unary logits + top-K + hidden projection.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace df2 {
+
+bool head_tc_supported(int64_t P, int64_t D, int64_t V, int K);
+size_t head_tc_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms);
+int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V, int K,
+                   const uint16_t* W_H, int r, float* G, int32_t* ids, float* vals, void* ws,
+                   int32_t* dev_status, int num_sms, cudaStream_t stream);
+
+}  // namespace df2

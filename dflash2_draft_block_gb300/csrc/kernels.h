@@ -1,0 +1,37 @@
+// Internal launchers of libdflash2 (not part of the C-ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace df2 {
+
+// ---- unary logits + top-K on the CUDA cores (any D % 8 == 0, K <= DF2_MAX_TOPK)
+bool head_simple_supported(int64_t D, int K);
+size_t head_simple_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms);
+cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V,
+                               int K, int32_t* ids, float* vals, void* ws, int num_sms,
+                               cudaStream_t stream);
+
+// ---- out = X . W^T on the CUDA cores, columns split between two outputs
+cudaError_t gemm_simple_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
+                               int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,
+                               int64_t ld1, cudaStream_t stream);
+
+// ---- selector
+cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,
+                        const float* G, const uint16_t* A, const uint16_t* Bc, int64_t V, int K,
+                        int r, int32_t* path, float* scores, int32_t* dev_status,
+                        cudaStream_t stream);
+cudaError_t pair_scores_launch(const int32_t* pred, int64_t P, const int32_t* ids,
+                               const float* vals, const float* G, const uint16_t* A,
+                               const uint16_t* Bc, int64_t V, int K, int r, float* scores,
+                               int32_t* dev_status, cudaStream_t stream);
+
+// ---- conv: y = sum_{j<taps, t-j>=0} (base[j] + dyn[p, j, c/g]) * x[p-j]
+cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
+                              const float* base_io, const float* dyn, int64_t dyn_ld, void* y,
+                              cudaStream_t stream);
+
+}  // namespace df2

@@ -1,0 +1,206 @@
+/*
+ * libdflash2 — the DFlash2 draft-block head on one GB300 (sm_103a).
+ *
+ * Five calls cover the data-parallel part of one DFlash2 draft cycle:
+ *
+ *   dflash2_unary_topk            unary logits over the full verifier vocabulary,
+ *                                 the per-position top-K, and the hidden projection H
+ *   dflash2_selector_walk         the candidate selector's greedy walk
+ *   dflash2_selector_pair_scores  the selector scores with teacher-forced predecessors
+ *   dflash2_conv_prepare          the grouped dynamic causal conv before a sublayer
+ *   dflash2_conv_finish           the same conv after the sublayer
+ *
+ * Sources (web pages, cited by title and section):
+ *   [vLLM]  "DFlash2", vLLM Speculators user guide: "Local Convolution",
+ *           "Candidate Selector", "Key Parameters".
+ *   [SF]    "DFlash2", SpecForge concept doc: "Architecture" and the dflash_config
+ *           validity rules under it.
+ *   [PR62]  verl-SpeCo PR #62 "feat: add DFlash2 drafter training backend":
+ *           "What DFlash2 adds" (conv and selector equations), "Two deltas over the
+ *           upstream inference implementation", "Selector training objective".
+ *   [KB]    "DFlash 2 Explanation": "Component Breakdown", "Draft-Verify Cycle",
+ *           "Problem 1" (pair score), "Problem 2" (two-tap conv).
+ *
+ * Conventions shared by every call
+ * ---------------------------------
+ * - Every pointer argument except the documented host ones is a DEVICE pointer
+ *   on the current CUDA device.  Tensors are dense and row-major with the shapes
+ *   given; the caller owns every buffer, the library allocates nothing per call.
+ * - bf16 tensors are passed as uint16_t: raw IEEE bfloat16 bit patterns.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream) and does not synchronise the host.  Host-side validation
+ *   happens before any launch; on any non-zero return nothing was launched
+ *   (DF2_ERR_CUDA: a launch was attempted and failed).
+ * - Workspace: calls that need scratch take (workspace, workspace_bytes), a device
+ *   buffer the caller allocates; the matching *_workspace_size() query returns the
+ *   bytes needed for those shapes on the current device (0 = none).  The
+ *   workspace must be 256-byte aligned and must not be used concurrently by
+ *   another call.  Its contents on entry do not matter.
+ * - dev_status (nullable): a device int32 that kernels OR DF2_STATUS_* bits into.
+ *   The library never clears it; the caller zeroes it when it wants a fresh read.
+ * - Inputs must be finite; NaN/Inf inputs give unspecified ids.
+ * - Alignment: every tensor pointer must be 16-byte aligned.
+ */
+#ifndef DFLASH2_H
+#define DFLASH2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define DF2_OK 0
+#define DF2_ERR_INVALID_ARGUMENT 1   /* a shape or value rule below is broken */
+#define DF2_ERR_UNSUPPORTED 2        /* valid for the method but outside this build's limits */
+#define DF2_ERR_CUDA 3               /* a CUDA runtime call failed (launch, attribute, ...) */
+#define DF2_ERR_WORKSPACE_TOO_SMALL 4
+#define DF2_ERR_TIMEOUT 5            /* reserved: a bounded device wait gave up */
+
+/* Activation dtypes for the conv calls. */
+#define DF2_DTYPE_BF16 0
+#define DF2_DTYPE_F32 1
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define DF2_STATUS_ID_OUT_OF_RANGE 0x1  /* a token id outside [0, V) was read */
+#define DF2_STATUS_WAIT_TIMEOUT 0x2     /* a bounded in-kernel wait gave up; outputs invalid */
+
+/* Limits of this build (DF2_ERR_UNSUPPORTED beyond them). */
+#define DF2_MAX_TOPK 1024
+#define DF2_MAX_RANK 4096
+
+/* Name of a return code ("DF2_OK", ...); never NULL. */
+const char* dflash2_status_string(int status);
+
+/* ABI version of this library (bumped on any signature change). */
+int dflash2_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * dflash2_unary_topk — unary logits, per-position top-K, hidden projection.
+ *
+ * For every row p of the draft hidden state (P = requests x block_size rows;
+ * row 0 of each block is the anchor position):
+ *   U[p, v] = sum_d h[p, d] * W_lm[v, d]        for all v in [0, V)   ([vLLM]
+ *             "Candidate Selector": the unary draft logits; [KB] "Draft-Verify
+ *             Cycle": the shared lm_head gives logits and top-K per position;
+ *             the full verifier vocabulary, [vLLM] "Candidate Selector")
+ *   topk_ids[p, :], topk_vals[p, :] = the K largest U[p, .], ordered by value
+ *             descending, equal values by token id ascending
+ *   G[p, i]  = sum_d h[p, d] * W_H[i, d]         the hidden projection H(h_t) of
+ *             the pair score ([PR62] "What DFlash2 adds"; [KB] "Problem 1"), read
+ *             as linear with no bias
+ * U never leaves the chip; products are of the bf16 inputs, sums in fp32.
+ *
+ *   h         [P, D]  bf16        draft hidden state
+ *   W_lm      [V, D]  bf16        LM head (the verifier's, shared)
+ *   K                              selector_top_k, 1 <= K <= min(V, DF2_MAX_TOPK)
+ *   W_H       [r, D]  bf16        hidden projection, or NULL (then G is not written
+ *                                  and r is ignored)
+ *   G         [P, r]  fp32        out (when W_H != NULL); 1 <= r <= DF2_MAX_RANK
+ *   topk_ids  [P, K]  int32       out
+ *   topk_vals [P, K]  fp32        out
+ *   workspace                      >= dflash2_unary_topk_workspace_size(P, D, V, K, r)
+ * Rules: P >= 0 (P = 0 launches nothing), D >= 1, D % 8 == 0, V >= 1.
+ * ---------------------------------------------------------------------- */
+size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V, int K, int r);
+int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm, int64_t V,
+                       int K, const uint16_t* W_H, int r, float* G, int32_t* topk_ids,
+                       float* topk_vals, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_selector_walk — the candidate selector's greedy walk.
+ *
+ * Per request q (R requests, blocks of B rows, T = B - 1 drafted positions):
+ *   a_0 = anchors[q]                            (the last verified token)
+ *   for t = 1 .. B-1, row = q*B + t:
+ *     s_j = topk_vals[row, j] + sum_i A[a_{t-1}, i] * G[row, i] * Bc[topk_ids[row, j], i]
+ *     j*  = argmax_j s_j   (equal scores: the lower token id)
+ *     a_t = topk_ids[row, j*];  path[q, t-1] = a_t;  path_scores[q, t-1] = s_{j*}
+ * ([vLLM] "Candidate Selector": start at the anchor, condition each position on the
+ * token selected at the one before; [PR62] "What DFlash2 adds": S_t(a, b) =
+ * U_t(b) + <A(a) * H(h_t), B(b)>; [KB] "Problem 1": greedy follows the best
+ * successor.)  Rows t = 0 (the anchor rows) are not read.  Scores are fp32.
+ *
+ *   anchors     [R]        int32   device
+ *   topk_ids    [R*B, K]   int32   candidates (as written by dflash2_unary_topk)
+ *   topk_vals   [R*B, K]   fp32    their unary logits
+ *   G           [R*B, r]   fp32    H(h_t)
+ *   A, Bc       [V, r]     bf16    predecessor / successor codebooks
+ *   path        [R, B-1]   int32   out
+ *   path_scores [R, B-1]   fp32    out
+ * Rules: R >= 0, B >= 2, 1 <= K <= min(V, DF2_MAX_TOPK), 1 <= r <= DF2_MAX_RANK.
+ * An anchor or candidate id outside [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and
+ * writes -1 / NaN over that request's whole path.
+ * ---------------------------------------------------------------------- */
+int dflash2_selector_walk(const int32_t* anchors, int R, int B, const int32_t* topk_ids,
+                          const float* topk_vals, const float* G, const uint16_t* A,
+                          const uint16_t* Bc, int64_t V, int K, int r, int32_t* path,
+                          float* path_scores, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_selector_pair_scores — teacher-forced selector scores.
+ *
+ *   scores[p, j] = topk_vals[p, j] + sum_i A[pred[p], i] * G[p, i] * Bc[topk_ids[p, j], i]
+ * for all P rows at once: the predecessor is given (the previous ground-truth
+ * token) instead of walked ([PR62] "Selector training objective").  Replaying a
+ * walk's own predecessors through this call reproduces the walk.
+ *
+ *   pred [P] int32; topk_ids/topk_vals [P, K]; G [P, r]; A, Bc [V, r] bf16;
+ *   scores [P, K] fp32 out.
+ * Rules: P >= 0, 1 <= K <= DF2_MAX_TOPK, 1 <= r <= DF2_MAX_RANK, V >= 1.
+ * A pred or candidate id outside [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and
+ * writes NaN for the affected scores.
+ * ---------------------------------------------------------------------- */
+int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* topk_ids,
+                                 const float* topk_vals, const float* G, const uint16_t* A,
+                                 const uint16_t* Bc, int64_t V, int K, int r, float* scores,
+                                 int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_conv_prepare — grouped dynamic causal conv before a sublayer.
+ *
+ * Rows are packed anchor blocks: row p has in-block position t = p mod B, and no
+ * tap reads across a block boundary ([PR62] "Two deltas", item 1; [vLLM] "Local
+ * Convolution").  With G = C / g groups of g contiguous channels:
+ *   d[p, io, j, gi] = sum_c W_proj[(io*taps + j)*G + gi, c] * x[p, c]
+ *   y[p, c]         = sum_{j < taps, t-j >= 0} (base[0, j, c] + d[p, 0, j, c/g]) * x[p-j, c]
+ *   dyn_out[p, j, gi] = d[p, 1, j, gi]
+ * ([PR62] "What DFlash2 adds": Conv_k(x)_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}, a
+ * static per-channel kernel plus a correction shared by conv_group_size channels;
+ * prepare also emits the kernel finish applies; [vLLM] "Local Convolution": a
+ * projection of the current hidden state gives both kernels.)  io = 0 is the
+ * kernel applied here, io = 1 the one dflash2_conv_finish applies.
+ *
+ *   x       [P, C]            dtype (DF2_DTYPE_BF16 or DF2_DTYPE_F32)
+ *   W_proj  [2*taps*G, C]     bf16
+ *   base    [2, taps, C]      fp32
+ *   y       [P, C]            dtype, out (must not alias x)
+ *   dyn_out [P, taps, G]      fp32, out
+ *   workspace                  >= dflash2_conv_prepare_workspace_size(P, C, taps, g, dtype)
+ * Rules ([SF] dflash_config rules and [PR62] item 1): P >= 0, P % B == 0,
+ * 1 <= taps <= B, g >= 1, C % g == 0, C % 8 == 0.
+ * ---------------------------------------------------------------------- */
+size_t dflash2_conv_prepare_workspace_size(int64_t P, int C, int taps, int g, int dtype);
+int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int B, int taps, int g,
+                         const uint16_t* W_proj, const float* base, void* y, float* dyn_out,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_conv_finish — the same conv after the sublayer, with the dynamic
+ * kernel correction dflash2_conv_prepare emitted:
+ *   y[p, c] = sum_{j < taps, t-j >= 0} (base[1, j, c] + dyn_out[p, j, c/g]) * z[p-j, c]
+ *
+ *   z [P, C] dtype; dyn_out [P, taps, G] fp32; base [2, taps, C] fp32 (uses base[1]);
+ *   y [P, C] dtype out (must not alias z).  Rules as for dflash2_conv_prepare.
+ * ---------------------------------------------------------------------- */
+int dflash2_conv_finish(const void* z, int dtype, int64_t P, int C, int B, int taps, int g,
+                        const float* dyn_out, const float* base, void* y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H */

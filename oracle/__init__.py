@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import ctypes as ct
 import os
+import platform
 import subprocess
 import threading
 
@@ -25,7 +26,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "dflash2_oracle.c")
 BUILD_DIR = os.path.join(_HERE, "_build")
-DEFAULT_LIB = os.path.join(BUILD_DIR, "libdflash2_oracle.so")
+# one build per host architecture (x86 and aarch64 hosts share this tree)
+DEFAULT_LIB = os.path.join(BUILD_DIR, f"libdflash2_oracle.{platform.machine()}.so")
 
 # Flags: no fast-math and no FMA contraction, so x86 and Arm hosts produce the
 # same doubles from the same loops.
