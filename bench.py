@@ -202,19 +202,22 @@ class Step:
 
 
 def count_launches(step, torch):
-    """Kernels one step launches, counted by the profiler (CUPTI)."""
+    """Kernels one step launches, counted from a profiler (CUPTI) trace."""
+    import tempfile
     try:
         from torch.profiler import ProfilerActivity, profile
         torch.cuda.synchronize()
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
             step.run()
             torch.cuda.synchronize()
-        names = []
-        for e in prof.events():
-            dt = str(getattr(e, "device_type", ""))
-            if "CUDA" in dt and not e.name.lower().startswith(("memcpy", "memset")):
-                names.append(e.name)
-        return len(names), sorted(set(names))
+        with tempfile.TemporaryDirectory() as d:
+            path = os.path.join(d, "trace.json")
+            prof.export_chrome_trace(path)
+            with open(path) as f:
+                trace = json.load(f)
+        evs = trace["traceEvents"] if isinstance(trace, dict) else trace
+        names = [e.get("name", "") for e in evs if e.get("cat") == "kernel"]
+        return len(names), sorted(set(n[:80] for n in names))
     except Exception as exc:  # profiler unavailable: report it rather than guess
         return None, [f"profiler unavailable: {exc}"]
 

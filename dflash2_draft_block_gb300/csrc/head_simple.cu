@@ -212,12 +212,16 @@ cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const ui
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    return topk_merge_launch(part_v, part_id, pl.S, P, K, ids, vals, stream);
+}
+
+cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
+                              int32_t* ids, float* vals, cudaStream_t stream) {
     const size_t msmem = size_t(8) * K * 8 + 64;
-    e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(msmem));
+    cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(msmem));
     if (e != cudaSuccess) return e;
-    topk_merge_kernel<<<unsigned(P), kThreads, msmem, stream>>>(part_v, part_id, pl.S, P, K, ids,
-                                                                vals);
+    topk_merge_kernel<<<unsigned(P), kThreads, msmem, stream>>>(part_v, part_id, S, P, K, ids, vals);
     return cudaGetLastError();
 }
 

@@ -14,6 +14,10 @@ cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const ui
                                int K, int32_t* ids, float* vals, void* ws, int num_sms,
                                cudaStream_t stream);
 
+// ---- S unsorted partial lists [S][P][K] (id -1 = empty slot) -> sorted top-K [P][K]
+cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
+                              int32_t* ids, float* vals, cudaStream_t stream);
+
 // ---- out = X . W^T on the CUDA cores, columns split between two outputs
 cudaError_t gemm_simple_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
                                int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,
