@@ -106,6 +106,27 @@ def unary_topk(h, W_lm, K, W_H=None, *, workspace=None, dev_status=None, out=Non
     return ids, vals, G
 
 
+def unary_topk_noalloc(h, W_lm, K, W_H=None, *, dev_status=None, out=None, stream=None):
+    """unary_topk without a workspace: for callers that may not allocate device
+    memory during a call.  Scratch comes from a fixed array inside the library
+    (DF2_NOALLOC_SCRATCH_BYTES per GPU), shared by every call, so calls must not
+    overlap on the GPU.  Outputs are allocated here unless `out` is given."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W_lm, "W_lm", torch.bfloat16, 2)
+    P, D = h.shape
+    r = 0 if W_H is None else W_H.shape[0]
+    if out is None:
+        ids = torch.empty((P, K), dtype=torch.int32, device=h.device)
+        vals = torch.empty((P, K), dtype=torch.float32, device=h.device)
+        G = torch.empty((P, r), dtype=torch.float32, device=h.device) if r else None
+    else:
+        ids, vals, G = out
+    rc = lib().dflash2_unary_topk_noalloc(_p(h), P, D, _p(W_lm), W_lm.shape[0], int(K), _p(W_H), r,
+                                          _p(G), _p(ids), _p(vals), _p(dev_status), _stream(stream))
+    _check("dflash2_unary_topk_noalloc", rc)
+    return ids, vals, G
+
+
 def selector_walk(anchors, topk_ids, topk_vals, G, A, Bc, block_size, *, dev_status=None,
                   out=None, stream=None):
     """Greedy walk per request.  Returns (path [R, B-1] int32, path_scores [R, B-1] f32)."""

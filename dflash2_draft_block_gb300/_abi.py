@@ -19,6 +19,8 @@ SIGNATURES = {
     "dflash2_unary_topk_workspace_size": (_sz, [_i64, _i64, _i64, _int, _int]),
     "dflash2_unary_topk": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp,
                                   _sz, _vp, _vp]),
+    "dflash2_unary_topk_noalloc": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _vp, _int, _vp, _vp,
+                                          _vp, _vp, _vp]),
     "dflash2_selector_walk": (_int, [_vp, _int, _int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _vp,
                                      _vp, _vp, _vp]),
     "dflash2_selector_pair_scores": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int,

@@ -111,6 +111,34 @@ int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* 
                        int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dflash2_unary_topk_noalloc — dflash2_unary_topk without a caller workspace.
+ *
+ * No counterpart in the pages: this is a convenience of the library.  It is for
+ * callers that cannot allocate device memory at call time, such as code running
+ * inside a host framework that owns all device allocations and forbids new ones
+ * during a step, or a latency-critical path where a cudaMalloc (which may
+ * synchronise the device) is not acceptable.  Same arguments, results and rules
+ * as dflash2_unary_topk, minus (workspace, workspace_bytes).
+ *
+ * Scratch: a DF2_NOALLOC_SCRATCH_BYTES array inside the library, one per GPU,
+ * held by every GPU that loads the library until the process exits.  Shapes
+ * whose dflash2_unary_topk_workspace_size() exceeds it return
+ * DF2_ERR_UNSUPPORTED (use dflash2_unary_topk with your own workspace then).
+ * Allocates nothing: no cudaMalloc / cudaFree or allocating library call.
+ * The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress, with the device current); make that first call before
+ * any stream capture.  All calls share the one array: calls that may overlap on
+ * the GPU (different streams, no ordering between them) race and give wrong
+ * results.  The array keeps the last call's contents; none of it needs to start
+ * at zero.
+ * ---------------------------------------------------------------------- */
+#define DF2_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,
+                               int64_t V, int K, const uint16_t* W_H, int r, float* G,
+                               int32_t* topk_ids, float* topk_vals, int32_t* dev_status,
+                               void* stream);
+
+/* ------------------------------------------------------------------------
  * dflash2_selector_walk — the candidate selector's greedy walk.
  *
  * Per request q (R requests, blocks of B rows, T = B - 1 drafted positions):

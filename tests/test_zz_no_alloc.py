@@ -1,0 +1,98 @@
+"""dflash2_unary_topk_noalloc against dflash2_unary_topk, through the C-ABI.
+
+The no-allocation entry point serves callers that may not allocate device memory
+during a call (a host framework that owns all device memory, a latency-critical
+path where cudaMalloc's possible device synchronisation is not acceptable).  It
+must give the same top-K ids, values and G as the workspace entry point, on two
+calls in a row: the second call finds the first call's leftovers in the shared
+scratch array.  This file is collected last on purpose."""
+import ctypes as ct
+
+import numpy as np
+import pytest
+
+from parity import close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _p(t):
+    return ct.c_void_p(0 if t is None else t.data_ptr())
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dflash2_draft_block_gb300 import _abi, build
+    build.build()
+    return _abi.load()
+
+
+def _inputs(seed, P, D, V, r):
+    g = torch.Generator().manual_seed(seed)
+    h = torch.randn((P, D), generator=g).to(torch.bfloat16).cuda()
+    W = (torch.randn((V, D), generator=g) * 0.02).to(torch.bfloat16).cuda()
+    WH = (torch.randn((r, D), generator=g) * 0.02).to(torch.bfloat16).cuda()
+    return h, W, WH
+
+
+def _with_workspace(lib, h, W, K, WH, stream):
+    P, D = h.shape
+    V, r = W.shape[0], WH.shape[0]
+    ids = torch.empty((P, K), dtype=torch.int32, device="cuda")
+    vals = torch.empty((P, K), dtype=torch.float32, device="cuda")
+    G = torch.empty((P, r), dtype=torch.float32, device="cuda")
+    nbytes = lib.dflash2_unary_topk_workspace_size(P, D, V, K, r)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+    rc = lib.dflash2_unary_topk(_p(h), P, D, _p(W), V, K, _p(WH), r, _p(G), _p(ids), _p(vals), _p(ws),
+                                nbytes, None, stream)
+    assert rc == 0, lib.dflash2_status_string(rc)
+    return ids, vals, G
+
+
+def _no_alloc(lib, h, W, K, WH, stream):
+    P, D = h.shape
+    V, r = W.shape[0], WH.shape[0]
+    ids = torch.full((P, K), -7, dtype=torch.int32, device="cuda")
+    vals = torch.zeros((P, K), dtype=torch.float32, device="cuda")
+    G = torch.zeros((P, r), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.dflash2_unary_topk_noalloc(_p(h), P, D, _p(W), V, K, _p(WH), r, _p(G), _p(ids), _p(vals),
+                                        _p(status), stream)
+    assert rc == 0, lib.dflash2_status_string(rc)
+    return ids, vals, G, status
+
+
+@pytest.mark.parametrize("shape", [
+    [(8, 4096, 151936, 16, 256), (8, 4096, 151936, 16, 256)],   # batch-1 head, twice
+    [(8, 512, 30011, 16, 64), (24, 256, 5000, 64, 32)],         # different shapes back to back
+    [(40, 256, 3000, 8, 32), (5, 1024, 7777, 32, 128)],         # CUDA-core path, then tensor-core path
+])
+def test_no_alloc_matches_workspace_entry_point(lib, shape):
+    stream = ct.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for i, (P, D, V, K, r) in enumerate(shape):
+        h, W, WH = _inputs(100 * i + P, P, D, V, r)
+        ref_ids, ref_vals, ref_G = _with_workspace(lib, h, W, K, WH, stream)
+        ids, vals, G, status = _no_alloc(lib, h, W, K, WH, stream)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(ids, ref_ids)
+        close(vals.cpu().numpy(), ref_vals.cpu().numpy(), what="no-alloc vals")
+        close(G.cpu().numpy(), ref_G.cpu().numpy(), what="no-alloc G")
+
+
+def test_no_alloc_rejects_oversized_shapes(lib):
+    P, D, V, K = 32, 4096, 151936, 64
+    need = lib.dflash2_unary_topk_workspace_size(P, D, V, K, 0)
+    limit = 8 << 20
+    if need <= limit:
+        pytest.skip("this GPU's plan for the shape fits the scratch array")
+    h = torch.zeros((P, D), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((V, D), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((P, K), dtype=torch.int32, device="cuda")
+    vals = torch.empty((P, K), dtype=torch.float32, device="cuda")
+    rc = lib.dflash2_unary_topk_noalloc(_p(h), P, D, _p(W), V, K, None, 0, None, _p(ids), _p(vals),
+                                        None, ct.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 2 and lib.dflash2_status_string(rc) == b"DF2_ERR_UNSUPPORTED"
