@@ -181,8 +181,16 @@ DF2_API int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int
     const int G = C / g;
     const int64_t half = int64_t(taps) * G;
     float* d_in = static_cast<float*>(workspace);
-    cudaError_t e = df2::gemm_simple_launch(x, dtype == DF2_DTYPE_F32, W_proj, P, 2 * half, C, d_in,
-                                            half, half, dyn_out, half, st);
+    cudaError_t e;
+    if (P <= 64) {
+        const int sms = num_sms_current();
+        if (sms <= 0) return DF2_ERR_CUDA;
+        e = df2::gemm_rows_launch(x, dtype == DF2_DTYPE_F32, W_proj, P, 2 * half, C, d_in, half, half,
+                                  dyn_out, half, sms, st);
+    } else {
+        e = df2::gemm_simple_launch(x, dtype == DF2_DTYPE_F32, W_proj, P, 2 * half, C, d_in, half,
+                                    half, dyn_out, half, st);
+    }
     if (e != cudaSuccess) return DF2_ERR_CUDA;
     e = df2::conv_apply_launch(x, dtype == DF2_DTYPE_F32, P, C, B, taps, g, base, d_in, half, y, st);
     return from_cuda(e);

@@ -126,14 +126,51 @@ conv_apply_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, int ta
     }
 }
 
+// Few rows: one thread per (row, 16-byte channel chunk); the taps re-read the
+// previous rows (from L1/L2) so every thread has at most `taps` independent loads.
+template <typename T>
+__global__ void __launch_bounds__(256)
+conv_apply_rows_kernel(const T* __restrict__ x, int64_t P, int C, int B, int taps, int g, int G,
+                       const float* __restrict__ base, const float* __restrict__ dyn, int64_t dyn_ld,
+                       T* __restrict__ y) {
+    constexpr int N = Vec<T>::N;
+    const int chunks = C / N;
+    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= P * chunks) return;
+    const int64_t p = idx / chunks;
+    const int c0 = int(idx % chunks) * N;
+    const int t = int(p % B);
+    const float* drow = dyn + p * dyn_ld;
+    float acc[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc[e] = 0.f;
+    for (int j = 0; j < taps && j <= t; ++j) {
+        float xv[N];
+        Vec<T>::load(x + (p - j) * C + c0, xv);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            const float k = __ldg(base + int64_t(j) * C + c0 + e) + __ldg(drow + j * G + (c0 + e) / g);
+            acc[e] = fmaf(k, xv[e], acc[e]);
+        }
+    }
+    Vec<T>::store(y + p * C + c0, acc);
+}
+
 template <typename T>
 cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const float* base,
                      const float* dyn, int64_t dyn_ld, T* y, cudaStream_t stream) {
     const int64_t nblocks = P / B;
     const int64_t total = nblocks * (C / Vec<T>::N);
     if (total == 0) return cudaSuccess;
-    const unsigned grid = unsigned((total + 255) / 256);
     const int G = C / g;
+    if (total < 32768) {
+        // too few (block, chunk) pairs to fill the GPU: spread the rows instead
+        const int64_t rows_total = P * (C / Vec<T>::N);
+        conv_apply_rows_kernel<T><<<unsigned((rows_total + 255) / 256), 256, 0, stream>>>(
+            x, P, C, B, taps, g, G, base, dyn, dyn_ld, y);
+        return cudaGetLastError();
+    }
+    const unsigned grid = unsigned((total + 255) / 256);
 #define DF2_CONV(TP)                                                                               \
     conv_apply_kernel<T, TP><<<grid, 256, 0, stream>>>(x, nblocks, C, B, taps, g, G, base, dyn,    \
                                                        dyn_ld, y)

@@ -73,7 +73,87 @@ gemm_nt_simple(const TX* __restrict__ X, const uint16_t* __restrict__ W, int64_t
     }
 }
 
+// Few rows of X: one warp per output column n (one row of W, read once with
+// 16-byte loads), the PG rows of X staged in shared memory as fp32.  Used when M
+// is small, where the tiled kernel above would leave most SMs idle.
+template <int PG, typename TX>
+__global__ void __launch_bounds__(256)
+gemm_rows_kernel(const TX* __restrict__ X, const uint16_t* __restrict__ W, int64_t M, int64_t N,
+                 int64_t Kd, float* __restrict__ out0, int64_t ld0, int64_t n_split,
+                 float* __restrict__ out1, int64_t ld1) {
+    extern __shared__ __align__(16) float xs[];  // [PG][Kd]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = int64_t(blockIdx.y) * PG;
+    const int nm = int(dmin<int64_t>(PG, M - m0));
+    for (int64_t i = threadIdx.x; i < PG * Kd; i += 256) {
+        const int p = int(i / Kd);
+        xs[i] = p < nm ? load_x<TX>(X + (m0 + p) * Kd + (i - int64_t(p) * Kd)) : 0.f;
+    }
+    __syncthreads();
+    const int64_t k8 = Kd / 8;
+    for (int64_t n = int64_t(blockIdx.x) * 8 + warp; n < N; n += int64_t(gridDim.x) * 8) {
+        float acc[PG];
+#pragma unroll
+        for (int p = 0; p < PG; ++p) acc[p] = 0.f;
+        const uint4* wrow = reinterpret_cast<const uint4*>(W + n * Kd);
+        for (int64_t c = lane; c < k8; c += 32) {
+            float wf[8];
+            unpack8(__ldg(wrow + c), wf);
+#pragma unroll
+            for (int p = 0; p < PG; ++p) {
+                const float4 x0 = *reinterpret_cast<const float4*>(xs + p * Kd + c * 8);
+                const float4 x1 = *reinterpret_cast<const float4*>(xs + p * Kd + c * 8 + 4);
+                acc[p] = fmaf(wf[0], x0.x, acc[p]); acc[p] = fmaf(wf[1], x0.y, acc[p]);
+                acc[p] = fmaf(wf[2], x0.z, acc[p]); acc[p] = fmaf(wf[3], x0.w, acc[p]);
+                acc[p] = fmaf(wf[4], x1.x, acc[p]); acc[p] = fmaf(wf[5], x1.y, acc[p]);
+                acc[p] = fmaf(wf[6], x1.z, acc[p]); acc[p] = fmaf(wf[7], x1.w, acc[p]);
+            }
+        }
+        float mine = 0.f;
+#pragma unroll
+        for (int p = 0; p < PG; ++p) {
+            const float s = warp_sum(acc[p]);
+            if (lane == p) mine = s;
+        }
+        if (lane < nm) {
+            const int64_t gm = m0 + lane;
+            if (n < n_split) out0[gm * ld0 + n] = mine;
+            else out1[gm * ld1 + (n - n_split)] = mine;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t gemm_rows_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
+                             int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,
+                             int64_t ld1, int num_sms, cudaStream_t stream) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    int pg = 8;
+    while (pg > 1 && size_t(pg) * Kd * 4 > 160 * 1024) pg /= 2;
+    const size_t smem = size_t(pg) * Kd * 4;
+    const int64_t groups = (M + pg - 1) / pg;
+    int64_t gx = (N + 7) / 8;
+    const int64_t want = (4LL * num_sms + groups - 1) / groups;
+    if (gx > want) gx = want < 1 ? 1 : want;
+    const dim3 grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(groups));
+    cudaError_t e = cudaSuccess;
+#define DF2_ROWS(PGV, T)                                                                            \
+    e = cudaFuncSetAttribute(gemm_rows_kernel<PGV, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             int(smem));                                                            \
+    if (e != cudaSuccess) return e;                                                                 \
+    gemm_rows_kernel<PGV, T><<<grid, 256, smem, stream>>>(static_cast<const T*>(X), W, M, N, Kd,    \
+                                                           out0, ld0, n_split, out1, ld1)
+    if (x_f32) {
+        if (pg == 8) { DF2_ROWS(8, float); } else if (pg == 4) { DF2_ROWS(4, float); }
+        else if (pg == 2) { DF2_ROWS(2, float); } else { DF2_ROWS(1, float); }
+    } else {
+        if (pg == 8) { DF2_ROWS(8, uint16_t); } else if (pg == 4) { DF2_ROWS(4, uint16_t); }
+        else if (pg == 2) { DF2_ROWS(2, uint16_t); } else { DF2_ROWS(1, uint16_t); }
+    }
+#undef DF2_ROWS
+    return cudaGetLastError();
+}
 
 cudaError_t gemm_simple_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
                                int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,

@@ -101,32 +101,44 @@ head_simple_kernel(const uint16_t* __restrict__ h, int64_t P, int64_t D,
 }
 
 // One CTA per position: fold the S partial lists into the final sorted top-K.
+// Candidates are staged through shared memory in chunks with independent,
+// coalesced loads (all 256 threads), so the selection never waits on a global
+// load; each warp then keeps its own list over its share of a chunk, and warp 0
+// folds the 8 lists together at the end.
+constexpr int kMergeChunk = 4096;
+
 __global__ void __launch_bounds__(kThreads)
 topk_merge_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id, int S,
                   int64_t P, int K, int32_t* __restrict__ out_ids, float* __restrict__ out_vals) {
     extern __shared__ __align__(16) uint8_t smem[];
-    float* lv = reinterpret_cast<float*>(smem);                  // [8][K]
-    int* lid = reinterpret_cast<int*>(lv + 8 * K);               // [8][K]
-    int* counts = lid + 8 * K;                                   // [8]
+    float* cv_s = reinterpret_cast<float*>(smem);                       // [kMergeChunk]
+    int* ci_s = reinterpret_cast<int*>(cv_s + kMergeChunk);             // [kMergeChunk]
+    float* lv = reinterpret_cast<float*>(ci_s + kMergeChunk);           // [8][K]
+    int* lid = reinterpret_cast<int*>(lv + 8 * K);                      // [8][K]
+    int* counts = lid + 8 * K;                                          // [8]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t p = blockIdx.x;
 
     WarpTopK list;
     list.init(lv + warp * K, lid + warp * K, K);
     const int64_t total = int64_t(S) * K;
-    for (int64_t base = int64_t(warp) * 32; base < total; base += kThreads) {
-        const int64_t idx = base + lane;
-        bool valid = idx < total;
-        float cv = -INFINITY;
-        int cid = -1;
-        if (valid) {
-            const int64_t s = idx / K, k = idx % K;
+    for (int64_t c0 = 0; c0 < total; c0 += kMergeChunk) {
+        const int n = int(dmin<int64_t>(kMergeChunk, total - c0));
+        for (int i = threadIdx.x; i < n; i += kThreads) {
+            const int64_t idx = c0 + i;
+            const int64_t s = idx / K, k = idx - s * K;
             const int64_t at = (s * P + p) * K + k;
-            cv = part_v[at];
-            cid = part_id[at];
-            valid = cid >= 0;
+            cv_s[i] = part_v[at];
+            ci_s[i] = part_id[at];
         }
-        list.offer(valid, cv, cid, lane);
+        __syncthreads();
+        for (int b = warp * 32; b < n; b += kThreads) {
+            const int i = b + lane;
+            const bool in = i < n;
+            const int cid = in ? ci_s[i] : -1;
+            list.offer(cid >= 0, in ? cv_s[i] : 0.f, cid, lane);
+        }
+        __syncthreads();
     }
     if (lane == 0) counts[warp] = list.n;
     __syncthreads();
@@ -217,7 +229,7 @@ cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const ui
 
 cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
                               int32_t* ids, float* vals, cudaStream_t stream) {
-    const size_t msmem = size_t(8) * K * 8 + 64;
+    const size_t msmem = size_t(kMergeChunk) * 8 + size_t(8) * K * 8 + 64;
     cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(msmem));
     if (e != cudaSuccess) return e;

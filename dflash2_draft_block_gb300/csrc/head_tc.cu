@@ -9,24 +9,29 @@
 // kernel is built around that stream:
 //   * the vocabulary is cut into 128-row tiles (plus ceil(r/128) tiles of W_H);
 //     one persistent CTA per SM walks tiles blockIdx.x, +gridDim.x, ...
-//   * warp 0 (one lane) streams [128 x 64] bf16 boxes of the tile with TMA,
-//     128-byte swizzled, evict-first in L2, into a ring of `nstages` slots,
-//     together with the matching [N x 64] box of h (rows past P read as zero);
+//   * warp 0 (one lane) streams each tile with TMA in stages of `kbox` [128 x 64]
+//     bf16 boxes (so every W row contributes 64*kbox contiguous elements per
+//     stage), 128-byte swizzled, evict-first in L2, into a ring of `nstages`
+//     slots, together with the matching [N x 64] boxes of h (rows past P read 0);
 //   * warp 1 (one lane) issues tcgen05.mma M=128 (vocab rows) x N (positions,
-//     16 or 32) x K=16, accumulating the tile's logits in TMEM; the two TMEM
-//     accumulators alternate so the next tile's MMAs overlap the epilogue;
-//   * warps 2-5 read the accumulator (warp w owns TMEM lanes 32*(w%4)..+31,
-//     i.e. 32 vocab rows) and fold each position's 32 logits into a per-warp
-//     top-K list in shared memory (a ballot against the list's worst entry
-//     rejects nearly everything once the list is full), or store G for W_H tiles.
-// The logits never reach global memory.  Each epilogue warp's lists go to the
-// workspace and topk_merge_kernel reduces them to the sorted top-K.
+//     16 or 32) x K=16 into TMEM; two tile accumulators alternate so the next
+//     tile's MMAs overlap the epilogue of this one;
+//   * warps 2-5 read the accumulator (warp w owns TMEM lanes 32*(w%4)..+31, i.e.
+//     32 vocab rows) and keep, per position, a top-K list in registers across
+//     their 32 lanes (topk_warp.cuh): a ballot against the list's K-th entry
+//     drops a tile's 32 candidates unless one of them enters the list, so after
+//     the first tiles almost every tile costs one compare per position; W_H
+//     tiles store G instead.
+// The logits never reach global memory.  At the end the four warps' lists of a
+// position are folded into one, written to the workspace in rank order, and
+// topk_merge_sorted_kernel folds the CTAs' lists into the final top-K.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "head_tc.h"
 #include "kernels.h"
 #include "tc_ptx.cuh"
+#include "topk_warp.cuh"
 
 namespace df2 {
 
@@ -40,90 +45,42 @@ constexpr uint32_t kWBytes = BM * BK * 2;
 constexpr int kMaxK = 64;
 constexpr int kMaxStages = 16;
 
-// Top-K list state kept in shared memory; operated on by one warp.
-struct ListState {
-    int n;
-    float wv;
-    int wid;
-    int wpos;
-};
-
-__device__ __forceinline__ void list_find_worst(ListState* st, const float* v, const int* id, int K,
-                                                int lane) {
-    float bv = 0.f;
-    int bi = 0, bp = -1;
-    for (int i = lane; i < K; i += 32) {
-        const float vv = v[i];
-        const int ii = id[i];
-        if (bp < 0 || ranks_before(bv, bi, vv, ii)) { bv = vv; bi = ii; bp = i; }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, o);
-        const int oi = __shfl_xor_sync(kFull, bi, o);
-        const int op = __shfl_xor_sync(kFull, bp, o);
-        if (op >= 0 && (bp < 0 || ranks_before(bv, bi, ov, oi))) { bv = ov; bi = oi; bp = op; }
-    }
-    if (lane == 0) { st->wv = bv; st->wid = bi; st->wpos = bp; }
-    __syncwarp();
-}
-
-// Offer one candidate per lane to the list.
-__device__ __forceinline__ void list_offer(ListState* st, float* v, int* id, int K, bool valid,
-                                           float cv, int cid, int lane) {
-    int n = st->n;
-    float wv = st->wv;
-    int wid = st->wid;
-    unsigned m = __ballot_sync(kFull, valid && (n < K || ranks_before(cv, cid, wv, wid)));
-    while (m) {
-        const int src = __ffs(m) - 1;
-        m &= m - 1;
-        const float sv = __shfl_sync(kFull, cv, src);
-        const int si = __shfl_sync(kFull, cid, src);
-        if (n < K) {
-            if (lane == 0) { v[n] = sv; id[n] = si; st->n = n + 1; }
-            ++n;
-            __syncwarp();
-            if (n == K) list_find_worst(st, v, id, K, lane);
-        } else if (ranks_before(sv, si, wv, wid)) {
-            if (lane == 0) { v[st->wpos] = sv; id[st->wpos] = si; }
-            __syncwarp();
-            list_find_worst(st, v, id, K, lane);
-        }
-        wv = st->wv;
-        wid = st->wid;
-    }
-}
-
 struct SmemLayout {
-    uint32_t w_off, h_off, bar_off, misc_off, state_off, lv_off, lid_off, total;
+    uint32_t w_off, h_off, bar_off, misc_off, xch_off, total, stage_w, stage_h;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int N, int K, int nstages) {
+// xch: the four epilogue warps' lists, exchanged through shared memory at the end.
+__host__ __device__ inline SmemLayout smem_layout(int N, int R, int nstages, int kbox) {
     SmemLayout L;
-    const uint32_t h_bytes = uint32_t(N) * BK * 2;
+    L.stage_w = uint32_t(kbox) * kWBytes;
+    L.stage_h = uint32_t(kbox) * uint32_t(N) * BK * 2;
     L.w_off = 0;
-    L.h_off = L.w_off + uint32_t(nstages) * kWBytes;
-    L.bar_off = L.h_off + uint32_t(nstages) * h_bytes;                 // 1024-aligned
+    L.h_off = L.w_off + uint32_t(nstages) * L.stage_w;
+    L.bar_off = L.h_off + uint32_t(nstages) * L.stage_h;               // 1024-aligned
     L.misc_off = L.bar_off + uint32_t(2 * nstages + 5) * 8;
-    L.state_off = (L.misc_off + 16 + 15) / 16 * 16;
-    L.lv_off = L.state_off + uint32_t(kEpiWarps * N) * sizeof(ListState);
-    L.lid_off = L.lv_off + uint32_t(kEpiWarps * N * K) * 4;
-    L.total = L.lid_off + uint32_t(kEpiWarps * N * K) * 4;
+    L.xch_off = (L.misc_off + 16 + 15) / 16 * 16;
+    L.total = L.xch_off + uint32_t(kEpiWarps * N * R * 32) * 8;
     return L;
 }
 
-template <int N>
+template <int N, int R>
 __global__ void __launch_bounds__(kThreads, 1)
 head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
                    const __grid_constant__ CUtensorMap tm_wh, int P, int D, int V, int K, int r,
-                   int n_vtiles, int n_tiles, int nstages, float* __restrict__ part_v,
-                   int* __restrict__ part_id, float* __restrict__ G, int32_t* __restrict__ dev_status) {
-    constexpr uint32_t kHBytes = N * BK * 2;
-    constexpr uint32_t kTmemCols = 2 * N;  // 32 or 64: two accumulators
+                   int n_vtiles, int n_tiles, int nstages, int kbox, int pf_stages, int nacc,
+                   float* __restrict__ part_v, int* __restrict__ part_id, float* __restrict__ G,
+                   int32_t* __restrict__ dev_status) {
+    // TMEM: two tile buffers (the epilogue drains one while the MMAs fill the
+    // other), each holding nacc partial accumulators of N columns.  Successive
+    // k-steps of a tile rotate over the partial accumulators, so consecutive MMAs
+    // do not depend on each other and the tensor core can overlap them; the
+    // epilogue adds the partials.
+    const uint32_t buf_cols = uint32_t(nacc) * N;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < 2 * buf_cols) tmem_cols *= 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout L = smem_layout(N, K, nstages);
+    const SmemLayout L = smem_layout(N, R, nstages, kbox);
     uint8_t* sW = smem + L.w_off;
     uint8_t* sH = smem + L.h_off;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
@@ -133,12 +90,13 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     uint64_t* mma_done = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
-    ListState* states = reinterpret_cast<ListState*>(smem + L.state_off);
-    float* lv = reinterpret_cast<float*>(smem + L.lv_off);
-    int* lid = reinterpret_cast<int*>(smem + L.lid_off);
+    float* xch_v = reinterpret_cast<float*>(smem + L.xch_off);                 // [4][N][R*32]
+    int* xch_id = reinterpret_cast<int*>(xch_v + kEpiWarps * N * R * 32);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nk = (D + BK - 1) / BK;
+    const int nbox = (D + BK - 1) / BK;            // 64-wide boxes along D
+    const int nk = (nbox + kbox - 1) / kbox;       // stages per tile
+    const uint32_t h_box_bytes = uint32_t(N) * BK * 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
@@ -150,18 +108,11 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             tc::mbar_init(&tempty[b], kEpiWarps);
         }
         tc::mbar_init(mma_done, 1);
-        *abort_flag = 0;
+        abort_flag[0] = 0;
         tc::fence_mbar_init();
     }
-    if (warp >= 2) {
-        const int e = warp - 2;
-        for (int i = lane; i < N; i += 32) {
-            ListState* st = &states[e * N + i];
-            st->n = 0; st->wv = -INFINITY; st->wid = INT_MAX; st->wpos = 0;
-        }
-    }
     if (warp == 1) {
-        tc::tmem_alloc(tmem_holder, kTmemCols);
+        tc::tmem_alloc(tmem_holder, tmem_cols);
         tc::tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -179,22 +130,47 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             // ---------------------------------------------------- TMA producer
             const uint64_t pol_w = tc::l2_policy_evict_first();
             const uint64_t pol_h = tc::l2_policy_evict_last();
+            const int my_tiles = n_tiles > int(blockIdx.x) ? (n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+            const int total = my_tiles * nk;
+            // L2 prefetch of the first pf_stages stages of this CTA's stream
+            for (int g = 0; g < pf_stages && g < total; ++g) {
+                const int t = int(blockIdx.x) + (g / nk) * int(gridDim.x);
+                const int kb = g % nk;
+                const bool is_wh = t >= n_vtiles;
+                const int row0 = (is_wh ? t - n_vtiles : t) * BM;
+                for (int j = 0; j < kbox && kb * kbox + j < nbox; ++j)
+                    tc::tma_prefetch_2d(is_wh ? &tm_wh : &tm_w, (kb * kbox + j) * BK, row0);
+            }
             int stage = 0;
             uint32_t phase = 0;
             int8_t armed[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) armed[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            for (int g = 0; g < total && ok; ++g) {
+                const int t = int(blockIdx.x) + (g / nk) * int(gridDim.x);
+                const int kb = g % nk;
                 const bool is_wh = t >= n_vtiles;
                 const CUtensorMap* mw = is_wh ? &tm_wh : &tm_w;
                 const int row0 = (is_wh ? t - n_vtiles : t) * BM;
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&full[stage], kWBytes + kHBytes);
-                    tc::tma_load_2d(sW + size_t(stage) * kWBytes, mw, &full[stage], kb * BK, row0, pol_w);
-                    tc::tma_load_2d(sH + size_t(stage) * kHBytes, &tm_h, &full[stage], kb * BK, 0, pol_h);
-                    armed[stage] = int8_t(phase);
-                    if (++stage == nstages) { stage = 0; phase ^= 1; }
+                const int nb = min(kbox, nbox - kb * kbox);
+                if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                tc::mbar_arrive_expect_tx(&full[stage], uint32_t(nb) * (kWBytes + h_box_bytes));
+                for (int j = 0; j < nb; ++j) {
+                    tc::tma_load_2d(sW + size_t(stage) * L.stage_w + size_t(j) * kWBytes, mw, &full[stage],
+                                    (kb * kbox + j) * BK, row0, pol_w);
+                    tc::tma_load_2d(sH + size_t(stage) * L.stage_h + size_t(j) * h_box_bytes, &tm_h,
+                                    &full[stage], (kb * kbox + j) * BK, 0, pol_h);
+                }
+                armed[stage] = int8_t(phase);
+                if (++stage == nstages) { stage = 0; phase ^= 1; }
+                const int gp = g + pf_stages;
+                if (pf_stages > 0 && gp < total) {
+                    const int tp = int(blockIdx.x) + (gp / nk) * int(gridDim.x);
+                    const int kbp = gp % nk;
+                    const bool wh_p = tp >= n_vtiles;
+                    const int rowp = (wh_p ? tp - n_vtiles : tp) * BM;
+                    for (int j = 0; j < kbox && kbp * kbox + j < nbox; ++j)
+                        tc::tma_prefetch_2d(wh_p ? &tm_wh : &tm_w, (kbp * kbox + j) * BK, rowp);
                 }
             }
             if (!ok) {
@@ -217,17 +193,23 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 const uint32_t tph = (it >> 1) & 1;
                 if (!tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag)) break;
                 tc::fence_after_sync();
-                const uint32_t d_tmem = tmem_base + uint32_t(b * N);
+                const uint32_t d_tmem = tmem_base + uint32_t(b) * buf_cols;
+                int ks = 0;  // k-step (16 elements of D) within the tile
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!tc::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     tc::fence_after_sync();
-                    const uint32_t a0 = tc::smem_u32(sW + size_t(stage) * kWBytes);
-                    const uint32_t b0 = tc::smem_u32(sH + size_t(stage) * kHBytes);
+                    const int nb = min(kbox, nbox - kb * kbox);
+                    for (int j = 0; j < nb; ++j) {
+                        const uint32_t a0 = tc::smem_u32(sW + size_t(stage) * L.stage_w + size_t(j) * kWBytes);
+                        const uint32_t b0 = tc::smem_u32(sH + size_t(stage) * L.stage_h + size_t(j) * h_box_bytes);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        tc::mma_bf16(d_tmem, tc::sw128_kmajor_desc(a0 + 32 * k),
-                                     tc::sw128_kmajor_desc(b0 + 32 * k), idesc,
-                                     (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < BK / 16; ++k, ++ks) {
+                            const int a = ks % nacc;
+                            tc::mma_bf16(d_tmem + uint32_t(a * N), tc::sw128_kmajor_desc(a0 + 32 * k),
+                                         tc::sw128_kmajor_desc(b0 + 32 * k), idesc,
+                                         ks >= nacc ? 1u : 0u);
+                        }
+                    }
                     tc::mma_commit(&empty[stage]);
                     if (++stage == nstages) { stage = 0; phase ^= 1; }
                 }
@@ -242,6 +224,10 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         // ---------------------------------------------------------- epilogue
         const int e = warp - 2;
         const int quarter = warp & 3;
+        const int nacc_used = min(nacc, 4 * nbox);  // partials a tile actually wrote
+        wtk::List<R> lists[N];
+#pragma unroll
+        for (int p = 0; p < N; ++p) lists[p].clear();
         int it = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
             const int b = it & 1;
@@ -250,9 +236,16 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             if (!__all_sync(kFull, got)) break;
             tc::fence_after_sync();
             float acc[N];
-            const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(b * N);
+            const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(b) * buf_cols;
             tc::tmem_ld16(taddr, acc);
             if constexpr (N == 32) tc::tmem_ld16(taddr + 16, acc + 16);
+            for (int a = 1; a < nacc_used; ++a) {
+                float part[N];
+                tc::tmem_ld16(taddr + uint32_t(a * N), part);
+                if constexpr (N == 32) tc::tmem_ld16(taddr + uint32_t(a * N) + 16, part + 16);
+#pragma unroll
+                for (int p = 0; p < N; ++p) acc[p] += part[p];
+            }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&tempty[b]);
@@ -268,24 +261,45 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             } else {
                 const bool valid = row < V;
 #pragma unroll
-                for (int p = 0; p < N; ++p) {
-                    if (p < P) {
-                        const int li = e * N + p;
-                        list_offer(&states[li], lv + size_t(li) * K, lid + size_t(li) * K, K, valid,
-                                   acc[p], row, lane);
-                    }
+                for (int p = 0; p < N; ++p)
+                    if (p < P) lists[p].offer(acc[p], valid ? row : wtk::kEmptyId, K, lane);
+            }
+        }
+        // the four warps' lists of a position -> one list -> workspace (partial blockIdx.x)
+#pragma unroll
+        for (int p = 0; p < N; ++p) {
+            if (p < P) {
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr) {
+                    const int at = ((e * N + p) * R + rr) * 32 + lane;
+                    xch_v[at] = lists[p].v[rr];
+                    xch_id[at] = lists[p].id[rr];
                 }
             }
         }
-        // this warp's lists -> workspace partial (blockIdx.x * 4 + e)
-        const size_t s = size_t(blockIdx.x) * kEpiWarps + e;
-        for (int p = 0; p < P; ++p) {
-            const int li = e * N + p;
-            const int n = states[li].n;
-            for (int k = lane; k < K; k += 32) {
-                const size_t at = (s * P + p) * K + k;
-                part_v[at] = k < n ? lv[size_t(li) * K + k] : -INFINITY;
-                part_id[at] = k < n ? lid[size_t(li) * K + k] : -1;
+        tc::named_barrier(1, 32 * kEpiWarps);
+        for (int p = e; p < P; p += kEpiWarps) {
+            wtk::List<R> m;
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                m.v[rr] = xch_v[((0 * N + p) * R + rr) * 32 + lane];
+                m.id[rr] = xch_id[((0 * N + p) * R + rr) * 32 + lane];
+            }
+            for (int src = 1; src < kEpiWarps; ++src) {
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr) {
+                    const int at = ((src * N + p) * R + rr) * 32 + lane;
+                    m.offer_sorted(xch_v[at], xch_id[at], K, lane);
+                }
+            }
+            const size_t base = (size_t(blockIdx.x) * P + p) * K;
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                const int k = rr * 32 + lane;
+                if (k < K) {
+                    part_v[base + k] = m.id[rr] != wtk::kEmptyId ? m.v[rr] : -INFINITY;
+                    part_id[base + k] = m.id[rr] != wtk::kEmptyId ? m.id[rr] : -1;
+                }
             }
         }
     }
@@ -295,7 +309,7 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     if (threadIdx.x == 0 && *abort_flag && dev_status) atomicOr(dev_status, DF2_STATUS_WAIT_TIMEOUT);
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem_base, kTmemCols);
+        tc::tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 
@@ -330,32 +344,53 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
 
 int pick_n(int64_t P) { return P <= 16 ? 16 : 32; }
 
-int pick_stages(int N, int K) {
+#ifndef DF2_HEAD_KBOX
+#define DF2_HEAD_KBOX 4  // 64-wide boxes per pipeline stage: 512 contiguous bytes per W row
+#endif
+#ifndef DF2_HEAD_PF
+#define DF2_HEAD_PF 0    // stages prefetched into L2 ahead of the TMA loads
+#endif
+#ifndef DF2_HEAD_NACC
+#define DF2_HEAD_NACC 1  // independent partial accumulators per tile
+#endif
+
+struct Plan {
+    int N, R, nstages, kbox;
+};
+
+Plan pick_plan(int64_t P, int K) {
+    Plan pl{pick_n(P), K <= 32 ? 1 : 2, 0, DF2_HEAD_KBOX};
     const int budget = 227 * 1024 - 1024;
-    for (int s = kMaxStages; s >= 2; --s)
-        if (int(smem_layout(N, K, s).total) <= budget) return s;
-    return 0;
+    for (int kb = pl.kbox; kb >= 1; kb /= 2) {
+        for (int s = kMaxStages; s >= 2; --s)
+            if (int(smem_layout(pl.N, pl.R, s, kb).total) <= budget && s * kb <= 4 * kMaxStages) {
+                if (s * kb >= 6 || kb == 1) { pl.nstages = s; pl.kbox = kb; return pl; }
+                break;
+            }
+    }
+    return pl;
 }
 
 }  // namespace
 
 bool head_tc_supported(int64_t P, int64_t D, int64_t V, int K) {
-    return P >= 1 && P <= 32 && K <= kMaxK && D % 8 == 0 && D <= (int64_t(1) << 30) &&
-           V <= INT32_MAX && pick_stages(pick_n(P), K) >= 2;
+    // register lists: N positions x R rows per epilogue lane; 32 x 2 would not fit
+    return P >= 1 && P <= 32 && K <= kMaxK && (P <= 16 || K <= 32) && D % 8 == 0 &&
+           D <= (int64_t(1) << 30) && V <= INT32_MAX && pick_plan(P, K).nstages >= 2;
 }
 
 size_t head_tc_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms) {
     (void)D;
     const int64_t n_tiles = (V + BM - 1) / BM;
     const int64_t grid = n_tiles < num_sms ? n_tiles : num_sms;
-    return size_t(grid) * kEpiWarps * size_t(P) * size_t(K) * 8;
+    return size_t(grid) * size_t(P) * size_t(K) * 8;
 }
 
 int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V, int K,
                    const uint16_t* W_H, int r, float* G, int32_t* ids, float* vals, void* ws,
                    int32_t* dev_status, int num_sms, cudaStream_t stream) {
-    const int N = pick_n(P);
-    const int nstages = pick_stages(N, K);
+    const Plan pl = pick_plan(P, K);
+    const int N = pl.N;
     CUtensorMap tm_w, tm_h, tm_wh;
     if (!make_map(&tm_w, W, V, D, BM) || !make_map(&tm_h, h, P, D, N)) return DF2_ERR_CUDA;
     const bool has_wh = W_H != nullptr;
@@ -367,28 +402,26 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
     const int n_vtiles = int((V + BM - 1) / BM);
     const int n_tiles = n_vtiles + (has_wh ? (r + BM - 1) / BM : 0);
     const int grid = n_vtiles < num_sms ? n_vtiles : num_sms;
-    const size_t parts = size_t(grid) * kEpiWarps;
+    const size_t parts = size_t(grid);
     float* part_v = static_cast<float*>(ws);
     int* part_id = reinterpret_cast<int*>(part_v + parts * P * K);
-    const size_t smem = smem_layout(N, K, nstages).total + 1024;
-    cudaError_t e;
-    if (N == 16) {
-        e = cudaFuncSetAttribute(head_skinny_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem));
-        if (e != cudaSuccess) return DF2_ERR_CUDA;
-        head_skinny_kernel<16><<<grid, kThreads, smem, stream>>>(
-            tm_w, tm_h, tm_wh, int(P), int(D), int(V), K, r, n_vtiles, n_tiles, nstages, part_v,
-            part_id, G, dev_status);
-    } else {
-        e = cudaFuncSetAttribute(head_skinny_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem));
-        if (e != cudaSuccess) return DF2_ERR_CUDA;
-        head_skinny_kernel<32><<<grid, kThreads, smem, stream>>>(
-            tm_w, tm_h, tm_wh, int(P), int(D), int(V), K, r, n_vtiles, n_tiles, nstages, part_v,
-            part_id, G, dev_status);
-    }
+    const size_t smem = smem_layout(N, pl.R, pl.nstages, pl.kbox).total + 1024;
+    cudaError_t e = cudaSuccess;
+#define DF2_HEAD(NV, RV)                                                                          \
+    do {                                                                                          \
+        e = cudaFuncSetAttribute(head_skinny_kernel<NV, RV>,                                      \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));         \
+        if (e != cudaSuccess) return DF2_ERR_CUDA;                                                \
+        head_skinny_kernel<NV, RV><<<grid, kThreads, smem, stream>>>(                             \
+            tm_w, tm_h, tm_wh, int(P), int(D), int(V), K, r, n_vtiles, n_tiles, pl.nstages,       \
+            pl.kbox, DF2_HEAD_PF, DF2_HEAD_NACC, part_v, part_id, G, dev_status);                 \
+    } while (0)
+    if (N == 16 && pl.R == 1) DF2_HEAD(16, 1);
+    else if (N == 16) DF2_HEAD(16, 2);
+    else DF2_HEAD(32, 1);
+#undef DF2_HEAD
     if (cudaGetLastError() != cudaSuccess) return DF2_ERR_CUDA;
-    e = topk_merge_launch(part_v, part_id, int(parts), P, K, ids, vals, stream);
+    e = topk_merge_sorted_launch(part_v, part_id, int(parts), P, K, ids, vals, stream);
     return e == cudaSuccess ? DF2_OK : DF2_ERR_CUDA;
 }
 

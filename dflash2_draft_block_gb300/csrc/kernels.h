@@ -18,10 +18,20 @@ cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const ui
 cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
                               int32_t* ids, float* vals, cudaStream_t stream);
 
+// ---- S partial lists [S][P][K], each in rank order (id -1 = empty), K <= 64 -> top-K [P][K]
+cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
+                                     int32_t* ids, float* vals, cudaStream_t stream);
+
 // ---- out = X . W^T on the CUDA cores, columns split between two outputs
 cudaError_t gemm_simple_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
                                int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,
                                int64_t ld1, cudaStream_t stream);
+
+// ---- the same for few rows of X (one warp per output column, X in shared memory);
+//      needs Kd % 8 == 0
+cudaError_t gemm_rows_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
+                             int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,
+                             int64_t ld1, int num_sms, cudaStream_t stream);
 
 // ---- selector
 cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,

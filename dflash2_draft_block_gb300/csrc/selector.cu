@@ -173,14 +173,156 @@ pair_scores_kernel(const int32_t* __restrict__ pred, int64_t P, const int32_t* _
     if (bad && lane == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src)
+                 : "memory");
+}
+
+// Walk with everything it can read gathered into shared memory first: the B rows
+// of every candidate of rows 1..B-1, the A rows of the anchor and of every
+// candidate of rows 1..B-2 (the only possible predecessors), and the G rows.
+// The gathers are independent, so they are all in flight at once; the B-1
+// sequential steps then touch shared memory only.  One CTA (8 warps) per request.
+constexpr int kWalkThreads = 256;
+
+__host__ __device__ inline size_t walk_cta_smem(int B, int K, int r) {
+    const size_t T = size_t(B) - 1;
+    return T * K * r * 2 + ((T - 1) * K + 1) * r * 2 + T * r * 4 + size_t(r) * 4 + size_t(K) * 4 + 64;
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kWalkThreads)
+walk_cta_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __restrict__ ids,
+                const float* __restrict__ vals, const float* __restrict__ G,
+                const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K,
+                int r, int32_t* __restrict__ path, float* __restrict__ path_scores,
+                int32_t* __restrict__ dev_status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int T = B - 1;
+    const int q = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint16_t* Bs = reinterpret_cast<uint16_t*>(smem);                     // [T*K][r]
+    uint16_t* As = Bs + size_t(T) * K * r;                                // [(T-1)*K + 1][r]
+    float* Gs = reinterpret_cast<float*>(As + (size_t(T - 1) * K + 1) * r);  // [T][r]
+    float* gate = Gs + size_t(T) * r;                                     // [r]
+    float* sc = gate + r;                                                 // [K]
+    int* misc = reinterpret_cast<int*>(sc + K);                           // bad, jstar
+
+    const int64_t row1 = int64_t(q) * B + 1;  // first drafted row of the request
+    const int32_t a0 = __ldg(anchors + q);
+    if (tid == 0) misc[0] = (a0 < 0 || a0 >= V) ? 1 : 0;
+    __syncthreads();
+    for (int e = tid; e < T * K; e += kWalkThreads) {
+        const int32_t b = __ldg(ids + row1 * K + e);
+        if (b < 0 || b >= V) misc[0] = 1;
+    }
+    __syncthreads();
+    if (misc[0]) {
+        for (int t = tid; t < T; t += kWalkThreads) {
+            path[int64_t(q) * T + t] = -1;
+            path_scores[int64_t(q) * T + t] = __int_as_float(0x7fc00000);
+        }
+        if (tid == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+        return;
+    }
+
+    const int cpr = r / 8;  // 16-byte chunks per bf16 row
+    for (int i = tid; i < T * K * cpr; i += kWalkThreads) {
+        const int row = i / cpr, c = i - row * cpr;
+        const int64_t b = __ldg(ids + row1 * K + row);
+        cp_async16(Bs + size_t(row) * r + c * 8, Bc + b * r + c * 8);
+    }
+    const int na = (T - 1) * K + 1;
+    for (int i = tid; i < na * cpr; i += kWalkThreads) {
+        const int arow = i / cpr, c = i - arow * cpr;
+        const int64_t a = arow == 0 ? a0 : __ldg(ids + row1 * K + (arow - 1));
+        cp_async16(As + size_t(arow) * r + c * 8, A + a * r + c * 8);
+    }
+    const int gpr = r / 4;  // 16-byte chunks per fp32 row
+    for (int i = tid; i < T * gpr; i += kWalkThreads) {
+        const int t = i / gpr, c = i - t * gpr;
+        cp_async16(Gs + size_t(t) * r + c * 4, G + (row1 + t) * r + c * 4);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+    __syncthreads();
+
+    int arow = 0;  // As row of the current predecessor
+    for (int t = 1; t <= T; ++t) {
+        for (int i = tid; i < r; i += kWalkThreads)
+            gate[i] = bf16_to_f32(As[size_t(arow) * r + i]) * Gs[size_t(t - 1) * r + i];
+        __syncthreads();
+        for (int j = warp; j < K; j += kWalkThreads / 32) {
+            const uint16_t* brow = Bs + (size_t(t - 1) * K + j) * r;
+            float part = 0.f;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                const int i0 = c * 256 + lane * 8;
+                if (i0 < r) {
+                    float bf[8];
+                    unpack8(*reinterpret_cast<const uint4*>(brow + i0), bf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) part = fmaf(gate[i0 + e], bf[e], part);
+                }
+            }
+            const float d = warp_sum(part);
+            if (lane == 0) sc[j] = __ldg(vals + (row1 + t - 1) * K + j) + d;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float bv = -INFINITY;
+            int bi = INT_MAX, bj = -1;
+            for (int j = lane; j < K; j += 32) {
+                const float v = sc[j];
+                const int id = __ldg(ids + (row1 + t - 1) * K + j);
+                if (bj < 0 || ranks_before(v, id, bv, bi)) { bv = v; bi = id; bj = j; }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float ov = __shfl_xor_sync(kFull, bv, o);
+                const int oi = __shfl_xor_sync(kFull, bi, o);
+                const int oj = __shfl_xor_sync(kFull, bj, o);
+                if (oj >= 0 && (bj < 0 || ranks_before(ov, oi, bv, bi))) { bv = ov; bi = oi; bj = oj; }
+            }
+            if (lane == 0) {
+                path[int64_t(q) * T + (t - 1)] = bi;
+                path_scores[int64_t(q) * T + (t - 1)] = bv;
+                misc[1] = bj;
+            }
+        }
+        __syncthreads();
+        arow = 1 + (t - 1) * K + misc[1];
+    }
+}
+
 }  // namespace
 
 cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,
                         const float* G, const uint16_t* A, const uint16_t* Bc, int64_t V, int K,
                         int r, int32_t* path, float* scores, int32_t* dev_status,
                         cudaStream_t stream) {
-    const unsigned grid = unsigned((R + kWarpsPerBlock - 1) / kWarpsPerBlock);
     const int nch = (r + 255) / 256;
+    const size_t smem = walk_cta_smem(B, K, r);
+    if (smem <= 200 * 1024) {
+#define DF2_WALK_CTA(N)                                                                             \
+    do {                                                                                            \
+        cudaError_t e = cudaFuncSetAttribute(walk_cta_kernel<N>,                                    \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)); \
+        if (e != cudaSuccess) return e;                                                             \
+        walk_cta_kernel<N><<<unsigned(R), kWalkThreads, smem, stream>>>(anchors, B, ids, vals, G, A,  \
+                                                                        Bc, V, K, r, path, scores,   \
+                                                                        dev_status);                 \
+    } while (0)
+        if (nch <= 1) DF2_WALK_CTA(1);
+        else if (nch <= 2) DF2_WALK_CTA(2);
+        else if (nch <= 4) DF2_WALK_CTA(4);
+        else if (nch <= 8) DF2_WALK_CTA(8);
+        else DF2_WALK_CTA(16);
+#undef DF2_WALK_CTA
+        return cudaGetLastError();
+    }
+    const unsigned grid = unsigned((R + kWarpsPerBlock - 1) / kWarpsPerBlock);
 #define DF2_WALK(N)                                                                            \
     walk_kernel<N><<<grid, kWarpsPerBlock * 32, 0, stream>>>(anchors, R, B, ids, vals, G, A,  \
                                                              Bc, V, K, r, path, scores,       \

@@ -1,0 +1,80 @@
+// Cross-CTA merge of sorted per-CTA top-K lists (K <= 64) into the final top-K.
+//
+// One CTA per position.  Each of its 8 warps folds every 8th CTA list into a
+// register-resident list (topk_warp.cuh): a list row is a batch already in rank
+// order, and one ballot against the running K-th entry drops it unless it
+// improves the list.  Warp 0 then folds the other warps' lists and writes the
+// K best in rank order.
+#include "common.cuh"
+#include "kernels.h"
+#include "topk_warp.cuh"
+
+namespace df2 {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+template <int R>
+__global__ void __launch_bounds__(kWarps * 32)
+topk_merge_sorted_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id, int S,
+                         int64_t P, int K, int32_t* __restrict__ out_ids,
+                         float* __restrict__ out_vals) {
+    __shared__ float xv[kWarps][R * 32];
+    __shared__ int xi[kWarps][R * 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t p = blockIdx.x;
+    wtk::List<R> m;
+    m.clear();
+    for (int s = warp; s < S; s += kWarps) {
+        const size_t base = (size_t(s) * P + p) * K;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const int k = rr * 32 + lane;
+            float v = -INFINITY;
+            int id = wtk::kEmptyId;
+            if (k < K) {
+                const int i = __ldg(part_id + base + k);
+                if (i >= 0) {
+                    v = __ldg(part_v + base + k);
+                    id = i;
+                }
+            }
+            m.offer_sorted(v, id, K, lane);
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        xv[warp][rr * 32 + lane] = m.v[rr];
+        xi[warp][rr * 32 + lane] = m.id[rr];
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    for (int w = 1; w < kWarps; ++w)
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) m.offer_sorted(xv[w][rr * 32 + lane], xi[w][rr * 32 + lane], K, lane);
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        const int k = rr * 32 + lane;
+        if (k < K) {
+            const bool ok = m.id[rr] != wtk::kEmptyId;
+            out_ids[p * K + k] = ok ? m.id[rr] : -1;
+            out_vals[p * K + k] = ok ? m.v[rr] : -INFINITY;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
+                                     int32_t* ids, float* vals, cudaStream_t stream) {
+    if (K <= 32)
+        topk_merge_sorted_kernel<1><<<unsigned(P), kWarps * 32, 0, stream>>>(part_v, part_id, S, P, K,
+                                                                             ids, vals);
+    else
+        topk_merge_sorted_kernel<2><<<unsigned(P), kWarps * 32, 0, stream>>>(part_v, part_id, S, P, K,
+                                                                             ids, vals);
+    return cudaGetLastError();
+}
+
+}  // namespace df2
