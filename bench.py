@@ -201,25 +201,13 @@ class Step:
         return [self.ids, self.vals, self.path, self.pscore, self.scores, self.y, self.y2, self.dyn]
 
 
-def count_launches(step, torch):
-    """Kernels one step launches, counted from a profiler (CUPTI) trace."""
-    import tempfile
-    try:
-        from torch.profiler import ProfilerActivity, profile
-        torch.cuda.synchronize()
-        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-            step.run()
-            torch.cuda.synchronize()
-        with tempfile.TemporaryDirectory() as d:
-            path = os.path.join(d, "trace.json")
-            prof.export_chrome_trace(path)
-            with open(path) as f:
-                trace = json.load(f)
-        evs = trace["traceEvents"] if isinstance(trace, dict) else trace
-        names = [e.get("name", "") for e in evs if e.get("cat") == "kernel"]
-        return len(names), sorted(set(n[:80] for n in names))
-    except Exception as exc:  # profiler unavailable: report it rather than guess
-        return None, [f"profiler unavailable: {exc}"]
+def count_launches(step, torch, df2):
+    """Kernels one step launches, from the library's own launch counter."""
+    torch.cuda.synchronize()
+    before = df2.kernels_launched()
+    step.run()
+    torch.cuda.synchronize()
+    return df2.kernels_launched() - before
 
 
 def gpu_arm(args, w, rank, world, torch):
@@ -238,7 +226,7 @@ def gpu_arm(args, w, rank, world, torch):
         if step.flush is not None:
             step.flush.zero_()
     torch.cuda.synchronize()
-    n_launch, kernel_names = count_launches(step, torch)
+    n_launch = count_launches(step, torch, df2)
 
     # ---- device-resident timing (W warm-up done above), per-call events
     nev = 6
@@ -248,6 +236,7 @@ def gpu_arm(args, w, rank, world, torch):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    launched0 = df2.kernels_launched()
     with ClockSampler(local) as clk:
         t0.record()
         for s in range(args.steps):
@@ -256,6 +245,7 @@ def gpu_arm(args, w, rank, world, torch):
                 step.flush.zero_()
         t1.record()
         torch.cuda.synchronize()
+    timed_launches = df2.kernels_launched() - launched0
     if dist is not None:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
@@ -349,9 +339,8 @@ def gpu_arm(args, w, rank, world, torch):
                          "traffic": None, "algorithmic_bytes": hb},
             "e2e": {"value": w.P * world / (e2e_ms * 1e-3), "unit": "positions/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": None if n_launch is None else n_launch * args.steps,
+            "gpu_launches": timed_launches,
             "kernels_per_step": n_launch,
-            "kernel_names": kernel_names,
             "clocks": clocks,
         }
     if dist is not None:

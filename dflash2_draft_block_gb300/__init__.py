@@ -34,6 +34,11 @@ def lib():
     return _abi.load()
 
 
+def kernels_launched() -> int:
+    """Kernels this library has launched in this process so far."""
+    return int(lib().dflash2_kernels_launched())
+
+
 def status_string(code: int) -> str:
     return lib().dflash2_status_string(int(code)).decode()
 

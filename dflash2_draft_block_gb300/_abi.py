@@ -16,6 +16,7 @@ _i64, _i32, _int, _vp, _sz = ct.c_int64, ct.c_int32, ct.c_int, ct.c_void_p, ct.c
 SIGNATURES = {
     "dflash2_status_string": (ct.c_char_p, [_int]),
     "dflash2_abi_version": (_int, []),
+    "dflash2_kernels_launched": (ct.c_longlong, []),
     "dflash2_unary_topk_workspace_size": (_sz, [_i64, _i64, _i64, _int, _int]),
     "dflash2_unary_topk": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp,
                                   _sz, _vp, _vp]),

@@ -1,5 +1,6 @@
 // The C-ABI of libdflash2: argument validation, workspace sizing and dispatch.
 // Every rule checked here is stated beside the call in include/dflash2.h.
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -39,6 +40,14 @@ DF2_API const char* dflash2_status_string(int status) {
 }
 
 DF2_API int dflash2_abi_version(void) { return kAbiVersion; }
+
+namespace {
+std::atomic<long long> g_launches{0};
+}  // namespace
+
+void df2::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+DF2_API long long dflash2_kernels_launched(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // ------------------------------------------------------------ unary_topk --
 
@@ -138,7 +147,7 @@ DF2_API int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const i
     if (!pred || !topk_ids || !topk_vals || !G || !A || !Bc || !scores)
         return DF2_ERR_INVALID_ARGUMENT;
     if (!aligned16(G) || !aligned16(A) || !aligned16(Bc)) return DF2_ERR_UNSUPPORTED;
-    if ((P + 7) / 8 > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (P * ((K + 7) / 8) / 8 + 1 > INT32_MAX) return DF2_ERR_UNSUPPORTED;
     return from_cuda(df2::pair_scores_launch(pred, P, topk_ids, topk_vals, G, A, Bc, V, K, r,
                                              scores, dev_status,
                                              static_cast<cudaStream_t>(stream)));

@@ -13,6 +13,10 @@
 
 namespace df2 {
 
+// Host side: count one kernel launch by this library (read back through
+// dflash2_kernels_launched).
+void note_launch();
+
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 template <class T>

@@ -168,6 +168,7 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
         const int64_t rows_total = P * (C / Vec<T>::N);
         conv_apply_rows_kernel<T><<<unsigned((rows_total + 255) / 256), 256, 0, stream>>>(
             x, P, C, B, taps, g, G, base, dyn, dyn_ld, y);
+        note_launch();
         return cudaGetLastError();
     }
     const unsigned grid = unsigned((total + 255) / 256);
@@ -182,6 +183,7 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
         default: DF2_CONV(0); break;
     }
 #undef DF2_CONV
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -85,17 +85,36 @@ gemm_rows_kernel(const TX* __restrict__ X, const uint16_t* __restrict__ W, int64
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t m0 = int64_t(blockIdx.y) * PG;
     const int nm = int(dmin<int64_t>(PG, M - m0));
-    for (int64_t i = threadIdx.x; i < PG * Kd; i += 256) {
-        const int p = int(i / Kd);
-        xs[i] = p < nm ? load_x<TX>(X + (m0 + p) * Kd + (i - int64_t(p) * Kd)) : 0.f;
+    const int64_t k8 = Kd / 8;
+    // stage the rows with 16-byte loads, widened to fp32 (rows past M are zero)
+    for (int p = 0; p < PG; ++p) {
+        float* dst = xs + size_t(p) * Kd;
+        for (int64_t c = threadIdx.x; c < k8; c += 256) {
+            float f[8];
+            if (p < nm) {
+                if constexpr (sizeof(TX) == 2) {
+                    unpack8(__ldg(reinterpret_cast<const uint4*>(X + (m0 + p) * Kd) + c), f);
+                } else {
+                    const float4 a = __ldg(reinterpret_cast<const float4*>(X + (m0 + p) * Kd) + 2 * c);
+                    const float4 b = __ldg(reinterpret_cast<const float4*>(X + (m0 + p) * Kd) + 2 * c + 1);
+                    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+                    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            }
+            reinterpret_cast<float4*>(dst)[2 * c] = make_float4(f[0], f[1], f[2], f[3]);
+            reinterpret_cast<float4*>(dst)[2 * c + 1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
     }
     __syncthreads();
-    const int64_t k8 = Kd / 8;
     for (int64_t n = int64_t(blockIdx.x) * 8 + warp; n < N; n += int64_t(gridDim.x) * 8) {
         float acc[PG];
 #pragma unroll
         for (int p = 0; p < PG; ++p) acc[p] = 0.f;
         const uint4* wrow = reinterpret_cast<const uint4*>(W + n * Kd);
+#pragma unroll 4
         for (int64_t c = lane; c < k8; c += 32) {
             float wf[8];
             unpack8(__ldg(wrow + c), wf);
@@ -152,6 +171,7 @@ cudaError_t gemm_rows_launch(const void* X, bool x_f32, const uint16_t* W, int64
         else if (pg == 2) { DF2_ROWS(2, uint16_t); } else { DF2_ROWS(1, uint16_t); }
     }
 #undef DF2_ROWS
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -166,6 +186,7 @@ cudaError_t gemm_simple_launch(const void* X, bool x_f32, const uint16_t* W, int
     else
         gemm_nt_simple<uint16_t><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(X), W, M, N,
                                                            Kd, out0, ld0, n_split, out1, ld1);
+    note_launch();
     return cudaGetLastError();
 }
 

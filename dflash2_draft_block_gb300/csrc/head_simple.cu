@@ -222,6 +222,7 @@ cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const ui
         DF2_CASE(1)
 #undef DF2_CASE
     }
+    note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return topk_merge_launch(part_v, part_id, pl.S, P, K, ids, vals, stream);
@@ -234,6 +235,7 @@ cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, in
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(msmem));
     if (e != cudaSuccess) return e;
     topk_merge_kernel<<<unsigned(P), kThreads, msmem, stream>>>(part_v, part_id, S, P, K, ids, vals);
+    note_launch();
     return cudaGetLastError();
 }
 

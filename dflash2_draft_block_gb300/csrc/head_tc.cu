@@ -420,6 +420,7 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
     else if (N == 16) DF2_HEAD(16, 2);
     else DF2_HEAD(32, 1);
 #undef DF2_HEAD
+    note_launch();
     if (cudaGetLastError() != cudaSuccess) return DF2_ERR_CUDA;
     e = topk_merge_sorted_launch(part_v, part_id, int(parts), P, K, ids, vals, stream);
     return e == cudaSuccess ? DF2_OK : DF2_ERR_CUDA;

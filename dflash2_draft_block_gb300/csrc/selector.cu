@@ -132,6 +132,10 @@ walk_kernel(const int32_t* __restrict__ anchors, int R, int B, const int32_t* __
     }
 }
 
+// One warp per (row, group of kPairGroup candidates): the gate and the group's
+// B rows are independent loads, so a warp waits for about two memory latencies.
+constexpr int kPairGroup = 8;
+
 template <int NCH>
 __global__ void __launch_bounds__(256)
 pair_scores_kernel(const int32_t* __restrict__ pred, int64_t P, const int32_t* __restrict__ ids,
@@ -139,35 +143,35 @@ pair_scores_kernel(const int32_t* __restrict__ pred, int64_t P, const int32_t* _
                    const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K,
                    int r, float* __restrict__ scores, int32_t* __restrict__ dev_status) {
     const int lane = threadIdx.x & 31;
-    const int64_t p = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (p >= P) return;
+    const int ngroups = (K + kPairGroup - 1) / kPairGroup;
+    const int64_t w = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (w >= P * ngroups) return;
+    const int64_t p = w / ngroups;
+    const int j0 = int(w - p * ngroups) * kPairGroup;
     const float nan = __int_as_float(0x7fc00000);
     const int32_t a = __ldg(pred + p);
     bool bad = false;
     if (a < 0 || a >= V) {
-        for (int j = lane; j < K; j += 32) scores[p * K + j] = nan;
+        if (lane < kPairGroup && j0 + lane < K) scores[p * K + j0 + lane] = nan;
         bad = true;
     } else {
         float qv[NCH][8];
         load_gate<NCH>(A, a, r, G + p * r, lane, qv);
-        for (int j0 = 0; j0 < K; j0 += 4) {
-            float part[4];
-            int32_t b[4];
-            bool inr[4];
+        float part[kPairGroup];
+        int32_t b[kPairGroup];
+        bool inr[kPairGroup];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                b[u] = (j0 + u < K) ? __ldg(ids + p * K + j0 + u) : 0;
-                inr[u] = b[u] >= 0 && b[u] < V;
-                part[u] = (j0 + u < K && inr[u]) ? dot_lane<NCH>(Bc, b[u], r, lane, qv) : 0.f;
-            }
+        for (int u = 0; u < kPairGroup; ++u) {
+            b[u] = (j0 + u < K) ? __ldg(ids + p * K + j0 + u) : 0;
+            inr[u] = b[u] >= 0 && b[u] < V;
+            part[u] = (j0 + u < K && inr[u]) ? dot_lane<NCH>(Bc, b[u], r, lane, qv) : 0.f;
+        }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float d = warp_sum(part[u]);
-                if (j0 + u < K && lane == 0) {
-                    scores[p * K + j0 + u] = inr[u] ? __ldg(vals + p * K + j0 + u) + d : nan;
-                }
-                bad = bad || (j0 + u < K && !inr[u]);
-            }
+        for (int u = 0; u < kPairGroup; ++u) {
+            const float d = warp_sum(part[u]);
+            if (j0 + u < K && lane == 0)
+                scores[p * K + j0 + u] = inr[u] ? __ldg(vals + p * K + j0 + u) + d : nan;
+            bad = bad || (j0 + u < K && !inr[u]);
         }
     }
     if (bad && lane == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
@@ -320,6 +324,7 @@ cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids
         else if (nch <= 8) DF2_WALK_CTA(8);
         else DF2_WALK_CTA(16);
 #undef DF2_WALK_CTA
+        note_launch();
         return cudaGetLastError();
     }
     const unsigned grid = unsigned((R + kWarpsPerBlock - 1) / kWarpsPerBlock);
@@ -333,6 +338,7 @@ cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids
     else if (nch <= 8) DF2_WALK(8);
     else DF2_WALK(16);
 #undef DF2_WALK
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -340,7 +346,8 @@ cudaError_t pair_scores_launch(const int32_t* pred, int64_t P, const int32_t* id
                                const float* vals, const float* G, const uint16_t* A,
                                const uint16_t* Bc, int64_t V, int K, int r, float* scores,
                                int32_t* dev_status, cudaStream_t stream) {
-    const unsigned grid = unsigned((P + 7) / 8);
+    const int64_t warps = P * ((K + kPairGroup - 1) / kPairGroup);
+    const unsigned grid = unsigned((warps + 7) / 8);
     const int nch = (r + 255) / 256;
 #define DF2_PAIR(N)                                                                            \
     pair_scores_kernel<N><<<grid, 256, 0, stream>>>(pred, P, ids, vals, G, A, Bc, V, K, r,    \
@@ -351,6 +358,7 @@ cudaError_t pair_scores_launch(const int32_t* pred, int64_t P, const int32_t* id
     else if (nch <= 8) DF2_PAIR(8);
     else DF2_PAIR(16);
 #undef DF2_PAIR
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -74,6 +74,7 @@ cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, in
     else
         topk_merge_sorted_kernel<2><<<unsigned(P), kWarps * 32, 0, stream>>>(part_v, part_id, S, P, K,
                                                                              ids, vals);
+    note_launch();
     return cudaGetLastError();
 }
 

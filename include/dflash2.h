@@ -77,6 +77,11 @@ const char* dflash2_status_string(int status);
 /* ABI version of this library (bumped on any signature change). */
 int dflash2_abi_version(void);
 
+/* Diagnostics: how many CUDA kernels this library has launched in this process
+ * so far (every device and call; a launch that failed is counted too).  Read it
+ * before and after a region to count the region's kernels. */
+long long dflash2_kernels_launched(void);
+
 /* ------------------------------------------------------------------------
  * dflash2_unary_topk — unary logits, per-position top-K, hidden projection.
  *

@@ -84,15 +84,20 @@ def test_no_alloc_matches_workspace_entry_point(lib, shape):
 
 
 def test_no_alloc_rejects_oversized_shapes(lib):
-    P, D, V, K = 32, 4096, 151936, 64
+    """A shape whose workspace exceeds the fixed scratch array is refused with
+    DF2_ERR_UNSUPPORTED and nothing runs.  The buffers are real and full-sized, so
+    even a call that wrongly went ahead would stay in bounds."""
+    P, D, V, K = 4096, 256, 2048, 1024
     need = lib.dflash2_unary_topk_workspace_size(P, D, V, K, 0)
-    limit = 8 << 20
-    if need <= limit:
-        pytest.skip("this GPU's plan for the shape fits the scratch array")
+    assert need > (8 << 20), need
     h = torch.zeros((P, D), dtype=torch.bfloat16, device="cuda")
     W = torch.zeros((V, D), dtype=torch.bfloat16, device="cuda")
-    ids = torch.empty((P, K), dtype=torch.int32, device="cuda")
+    ids = torch.full((P, K), -7, dtype=torch.int32, device="cuda")
     vals = torch.empty((P, K), dtype=torch.float32, device="cuda")
+    before = lib.dflash2_kernels_launched()
     rc = lib.dflash2_unary_topk_noalloc(_p(h), P, D, _p(W), V, K, None, 0, None, _p(ids), _p(vals),
                                         None, ct.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 2 and lib.dflash2_status_string(rc) == b"DF2_ERR_UNSUPPORTED"
+    assert lib.dflash2_kernels_launched() == before
+    torch.cuda.synchronize()
+    assert int(ids[0, 0].item()) == -7
