@@ -74,58 +74,63 @@ gemm_nt_simple(const TX* __restrict__ X, const uint16_t* __restrict__ W, int64_t
 }
 
 // Few rows of X: one warp per output column n (one row of W, read once with
-// 16-byte loads), the PG rows of X staged in shared memory as fp32.  Used when M
-// is small, where the tiled kernel above would leave most SMs idle.
+// 16-byte loads), the PG rows of X copied to shared memory in their own dtype
+// with one round of cp.async (every copy in flight at once).  Used when M is
+// small, where the tiled kernel above would leave most SMs idle.
+__device__ __forceinline__ void cp_async16_g(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void load8(const uint16_t* p, float f[8]) {
+    unpack8(*reinterpret_cast<const uint4*>(p), f);
+}
+__device__ __forceinline__ void load8(const float* p, float f[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
 template <int PG, typename TX>
 __global__ void __launch_bounds__(256)
 gemm_rows_kernel(const TX* __restrict__ X, const uint16_t* __restrict__ W, int64_t M, int64_t N,
                  int64_t Kd, float* __restrict__ out0, int64_t ld0, int64_t n_split,
                  float* __restrict__ out1, int64_t ld1) {
-    extern __shared__ __align__(16) float xs[];  // [PG][Kd]
+    extern __shared__ __align__(16) uint8_t xs_raw[];
+    TX* xs = reinterpret_cast<TX*>(xs_raw);  // [PG][Kd]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t m0 = int64_t(blockIdx.y) * PG;
     const int nm = int(dmin<int64_t>(PG, M - m0));
-    const int64_t k8 = Kd / 8;
-    // stage the rows with 16-byte loads, widened to fp32 (rows past M are zero)
-    for (int p = 0; p < PG; ++p) {
-        float* dst = xs + size_t(p) * Kd;
-        for (int64_t c = threadIdx.x; c < k8; c += 256) {
-            float f[8];
-            if (p < nm) {
-                if constexpr (sizeof(TX) == 2) {
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(X + (m0 + p) * Kd) + c), f);
-                } else {
-                    const float4 a = __ldg(reinterpret_cast<const float4*>(X + (m0 + p) * Kd) + 2 * c);
-                    const float4 b = __ldg(reinterpret_cast<const float4*>(X + (m0 + p) * Kd) + 2 * c + 1);
-                    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-                    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = 0.f;
-            }
-            reinterpret_cast<float4*>(dst)[2 * c] = make_float4(f[0], f[1], f[2], f[3]);
-            reinterpret_cast<float4*>(dst)[2 * c + 1] = make_float4(f[4], f[5], f[6], f[7]);
-        }
+    constexpr int kPer16 = 16 / int(sizeof(TX));  // elements per 16-byte chunk
+    const int64_t cpr = Kd / kPer16;               // chunks per row
+    for (int64_t i = threadIdx.x; i < int64_t(nm) * cpr; i += 256) {
+        const int p = int(i / cpr);
+        const int64_t c = i - int64_t(p) * cpr;
+        cp_async16_g(xs + size_t(p) * Kd + c * kPer16, X + (m0 + p) * Kd + c * kPer16);
     }
+    for (int64_t i = int64_t(nm) * cpr + threadIdx.x; i < int64_t(PG) * cpr; i += 256)
+        reinterpret_cast<uint4*>(xs)[i] = make_uint4(0, 0, 0, 0);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     __syncthreads();
+    const int64_t k8 = Kd / 8;
     for (int64_t n = int64_t(blockIdx.x) * 8 + warp; n < N; n += int64_t(gridDim.x) * 8) {
         float acc[PG];
 #pragma unroll
         for (int p = 0; p < PG; ++p) acc[p] = 0.f;
         const uint4* wrow = reinterpret_cast<const uint4*>(W + n * Kd);
-#pragma unroll 4
+#pragma unroll 8
         for (int64_t c = lane; c < k8; c += 32) {
             float wf[8];
             unpack8(__ldg(wrow + c), wf);
 #pragma unroll
             for (int p = 0; p < PG; ++p) {
-                const float4 x0 = *reinterpret_cast<const float4*>(xs + p * Kd + c * 8);
-                const float4 x1 = *reinterpret_cast<const float4*>(xs + p * Kd + c * 8 + 4);
-                acc[p] = fmaf(wf[0], x0.x, acc[p]); acc[p] = fmaf(wf[1], x0.y, acc[p]);
-                acc[p] = fmaf(wf[2], x0.z, acc[p]); acc[p] = fmaf(wf[3], x0.w, acc[p]);
-                acc[p] = fmaf(wf[4], x1.x, acc[p]); acc[p] = fmaf(wf[5], x1.y, acc[p]);
-                acc[p] = fmaf(wf[6], x1.z, acc[p]); acc[p] = fmaf(wf[7], x1.w, acc[p]);
+                float xf[8];
+                load8(xs + size_t(p) * Kd + c * 8, xf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[p] = fmaf(wf[e], xf[e], acc[p]);
             }
         }
         float mine = 0.f;
@@ -148,9 +153,10 @@ cudaError_t gemm_rows_launch(const void* X, bool x_f32, const uint16_t* W, int64
                              int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,
                              int64_t ld1, int num_sms, cudaStream_t stream) {
     if (M <= 0 || N <= 0) return cudaSuccess;
+    const size_t esz = x_f32 ? 4 : 2;
     int pg = 8;
-    while (pg > 1 && size_t(pg) * Kd * 4 > 160 * 1024) pg /= 2;
-    const size_t smem = size_t(pg) * Kd * 4;
+    while (pg > 1 && size_t(pg) * Kd * esz > 160 * 1024) pg /= 2;
+    const size_t smem = size_t(pg) * Kd * esz;
     const int64_t groups = (M + pg - 1) / pg;
     int64_t gx = (N + 7) / 8;
     const int64_t want = (4LL * num_sms + groups - 1) / groups;

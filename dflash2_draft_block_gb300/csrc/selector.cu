@@ -188,12 +188,32 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 // of every candidate of rows 1..B-1, the A rows of the anchor and of every
 // candidate of rows 1..B-2 (the only possible predecessors), and the G rows.
 // The gathers are independent, so they are all in flight at once; the B-1
-// sequential steps then touch shared memory only.  One CTA (8 warps) per request.
+// sequential steps then touch shared memory only and are run by one warp with
+// no block-wide barrier.  One CTA per request (8 warps issue the gathers).
 constexpr int kWalkThreads = 256;
+
+// Sum 16 per-lane values over the warp at once: at each butterfly level a lane
+// keeps half of its values and adds its partner's copy of them, so 16 shuffles in
+// 5 levels replace 16 separate 5-level reductions.  Returns u = (lane >> 1) & 15:
+// on return v[0] of this lane is the warp-wide sum of the lanes' v[u].
+__device__ __forceinline__ int reduce16_transpose(float v[16], int lane) {
+#pragma unroll
+    for (int m = 16, h = 8; m >= 2; m >>= 1, h >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? v[i] : v[i + h];
+            const float keep = upper ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, m);
+        }
+    }
+    v[0] += __shfl_xor_sync(kFull, v[0], 1);
+    return (lane >> 1) & 15;
+}
 
 __host__ __device__ inline size_t walk_cta_smem(int B, int K, int r) {
     const size_t T = size_t(B) - 1;
-    return T * K * r * 2 + ((T - 1) * K + 1) * r * 2 + T * r * 4 + size_t(r) * 4 + size_t(K) * 4 + 64;
+    return T * K * r * 2 + ((T - 1) * K + 1) * r * 2 + T * r * 4 + T * K * 8 + 64;
 }
 
 template <int NCH>
@@ -210,20 +230,22 @@ walk_cta_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __res
     uint16_t* Bs = reinterpret_cast<uint16_t*>(smem);                     // [T*K][r]
     uint16_t* As = Bs + size_t(T) * K * r;                                // [(T-1)*K + 1][r]
     float* Gs = reinterpret_cast<float*>(As + (size_t(T - 1) * K + 1) * r);  // [T][r]
-    float* gate = Gs + size_t(T) * r;                                     // [r]
-    float* sc = gate + r;                                                 // [K]
-    int* misc = reinterpret_cast<int*>(sc + K);                           // bad, jstar
+    float* vs = Gs + size_t(T) * r;                                       // [T*K]
+    int* is = reinterpret_cast<int*>(vs + size_t(T) * K);                 // [T*K]
+    int* bad = is + size_t(T) * K;
 
     const int64_t row1 = int64_t(q) * B + 1;  // first drafted row of the request
     const int32_t a0 = __ldg(anchors + q);
-    if (tid == 0) misc[0] = (a0 < 0 || a0 >= V) ? 1 : 0;
+    if (tid == 0) *bad = (a0 < 0 || a0 >= V) ? 1 : 0;
     __syncthreads();
     for (int e = tid; e < T * K; e += kWalkThreads) {
         const int32_t b = __ldg(ids + row1 * K + e);
-        if (b < 0 || b >= V) misc[0] = 1;
+        is[e] = b;
+        vs[e] = __ldg(vals + row1 * K + e);
+        if (b < 0 || b >= V) *bad = 1;
     }
     __syncthreads();
-    if (misc[0]) {
+    if (*bad) {
         for (int t = tid; t < T; t += kWalkThreads) {
             path[int64_t(q) * T + t] = -1;
             path_scores[int64_t(q) * T + t] = __int_as_float(0x7fc00000);
@@ -235,13 +257,12 @@ walk_cta_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __res
     const int cpr = r / 8;  // 16-byte chunks per bf16 row
     for (int i = tid; i < T * K * cpr; i += kWalkThreads) {
         const int row = i / cpr, c = i - row * cpr;
-        const int64_t b = __ldg(ids + row1 * K + row);
-        cp_async16(Bs + size_t(row) * r + c * 8, Bc + b * r + c * 8);
+        cp_async16(Bs + size_t(row) * r + c * 8, Bc + int64_t(is[row]) * r + c * 8);
     }
     const int na = (T - 1) * K + 1;
     for (int i = tid; i < na * cpr; i += kWalkThreads) {
         const int arow = i / cpr, c = i - arow * cpr;
-        const int64_t a = arow == 0 ? a0 : __ldg(ids + row1 * K + (arow - 1));
+        const int64_t a = arow == 0 ? a0 : is[arow - 1];
         cp_async16(As + size_t(arow) * r + c * 8, A + a * r + c * 8);
     }
     const int gpr = r / 4;  // 16-byte chunks per fp32 row
@@ -251,52 +272,76 @@ walk_cta_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __res
     }
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
     __syncthreads();
+    if (warp != 0) return;
 
+    // The sequential part, one warp, shared memory only.  Lane l owns rank
+    // elements [256c + 8l, 256c + 8l + 8) of the gate and of every B row.
     int arow = 0;  // As row of the current predecessor
     for (int t = 1; t <= T; ++t) {
-        for (int i = tid; i < r; i += kWalkThreads)
-            gate[i] = bf16_to_f32(As[size_t(arow) * r + i]) * Gs[size_t(t - 1) * r + i];
-        __syncthreads();
-        for (int j = warp; j < K; j += kWalkThreads / 32) {
-            const uint16_t* brow = Bs + (size_t(t - 1) * K + j) * r;
-            float part = 0.f;
+        float qv[NCH][8];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                const int i0 = c * 256 + lane * 8;
-                if (i0 < r) {
-                    float bf[8];
-                    unpack8(*reinterpret_cast<const uint4*>(brow + i0), bf);
+        for (int c = 0; c < NCH; ++c) {
+            const int i0 = c * 256 + lane * 8;
+            if (i0 < r) {
+                float af[8];
+                unpack8(*reinterpret_cast<const uint4*>(As + size_t(arow) * r + i0), af);
+                const float* g = Gs + size_t(t - 1) * r + i0;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) part = fmaf(gate[i0 + e], bf[e], part);
+                for (int e = 0; e < 8; ++e) qv[c][e] = af[e] * g[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qv[c][e] = 0.f;
+            }
+        }
+        float best = -INFINITY;
+        int best_id = -1, best_j = 0;
+        for (int j0 = 0; j0 < K; j0 += 16) {
+            // 16 candidates' lane partials, summed across the warp together
+            float part[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                part[u] = 0.f;
+                if (j0 + u < K) {
+                    const uint16_t* brow = Bs + (size_t(t - 1) * K + j0 + u) * r;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        const int i0 = c * 256 + lane * 8;
+                        if (i0 < r) {
+                            float bf[8];
+                            unpack8(*reinterpret_cast<const uint4*>(brow + i0), bf);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) part[u] = fmaf(qv[c][e], bf[e], part[u]);
+                        }
+                    }
                 }
             }
-            const float d = warp_sum(part);
-            if (lane == 0) sc[j] = __ldg(vals + (row1 + t - 1) * K + j) + d;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            float bv = -INFINITY;
-            int bi = INT_MAX, bj = -1;
-            for (int j = lane; j < K; j += 32) {
-                const float v = sc[j];
-                const int id = __ldg(ids + (row1 + t - 1) * K + j);
-                if (bj < 0 || ranks_before(v, id, bv, bi)) { bv = v; bi = id; bj = j; }
+            // lanes 2u and 2u+1 end up holding candidate j0+u's full sum
+            const int u = reduce16_transpose(part, lane);
+            float sj = -INFINITY;
+            int idj = INT_MAX, jj = -1;
+            if (j0 + u < K) {
+                sj = vs[(t - 1) * K + j0 + u] + part[0];
+                idj = is[(t - 1) * K + j0 + u];
+                jj = j0 + u;
             }
 #pragma unroll
             for (int o = 16; o; o >>= 1) {
-                const float ov = __shfl_xor_sync(kFull, bv, o);
-                const int oi = __shfl_xor_sync(kFull, bi, o);
-                const int oj = __shfl_xor_sync(kFull, bj, o);
-                if (oj >= 0 && (bj < 0 || ranks_before(ov, oi, bv, bi))) { bv = ov; bi = oi; bj = oj; }
+                const float ov = __shfl_xor_sync(kFull, sj, o);
+                const int oi = __shfl_xor_sync(kFull, idj, o);
+                const int oj = __shfl_xor_sync(kFull, jj, o);
+                if (oj >= 0 && (jj < 0 || ranks_before(ov, oi, sj, idj))) { sj = ov; idj = oi; jj = oj; }
             }
-            if (lane == 0) {
-                path[int64_t(q) * T + (t - 1)] = bi;
-                path_scores[int64_t(q) * T + (t - 1)] = bv;
-                misc[1] = bj;
+            if (jj >= 0 && (best_id < 0 || ranks_before(sj, idj, best, best_id))) {
+                best = sj;
+                best_id = idj;
+                best_j = jj;
             }
         }
-        __syncthreads();
-        arow = 1 + (t - 1) * K + misc[1];
+        if (lane == 0) {
+            path[int64_t(q) * T + (t - 1)] = best_id;
+            path_scores[int64_t(q) * T + (t - 1)] = best;
+        }
+        arow = 1 + (t - 1) * K + best_j;
     }
 }
 
