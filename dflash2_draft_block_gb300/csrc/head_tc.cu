@@ -49,7 +49,10 @@ struct SmemLayout {
     uint32_t w_off, h_off, bar_off, misc_off, xch_off, total, stage_w, stage_h;
 };
 
-// xch: the four epilogue warps' lists, exchanged through shared memory at the end.
+// xch: the four epilogue warps' lists, exchanged through shared memory at the
+// end.  It aliases the start of the W stage ring: the epilogue only uses it after
+// the last tile's accumulator is complete, i.e. after every MMA has read its
+// operands and every TMA load has landed.
 __host__ __device__ inline SmemLayout smem_layout(int N, int R, int nstages, int kbox) {
     SmemLayout L;
     L.stage_w = uint32_t(kbox) * kWBytes;
@@ -58,8 +61,10 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int R, int nstages, int
     L.h_off = L.w_off + uint32_t(nstages) * L.stage_w;
     L.bar_off = L.h_off + uint32_t(nstages) * L.stage_h;               // 1024-aligned
     L.misc_off = L.bar_off + uint32_t(2 * nstages + 5) * 8;
-    L.xch_off = (L.misc_off + 16 + 15) / 16 * 16;
-    L.total = L.xch_off + uint32_t(kEpiWarps * N * R * 32) * 8;
+    L.xch_off = 0;
+    const uint32_t xch_bytes = uint32_t(kEpiWarps * N * R * 32) * 8;
+    const uint32_t end = L.misc_off + 16;
+    L.total = end > xch_bytes ? end : xch_bytes;
     return L;
 }
 
