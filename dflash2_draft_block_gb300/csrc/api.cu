@@ -62,6 +62,25 @@ int check_head(int64_t P, int64_t D, int64_t V, int K, int r, bool has_wh) {
     return DF2_OK;
 }
 
+
+enum class HeadPath { Skinny, Wide, Simple };
+
+// Few positions: the HBM-streaming swap-AB kernel; many: the tensor-core GEMM with
+// a per-position top-K epilogue; anything else (K > 64): the CUDA-core path.
+HeadPath pick_head(int64_t P, int64_t D, int64_t V, int K) {
+    if (df2::head_tc_supported(P, D, V, K)) return HeadPath::Skinny;
+    if (df2::wide_supported(P, V, D, K)) return HeadPath::Wide;
+    return HeadPath::Simple;
+}
+
+size_t head_workspace(HeadPath path, int64_t P, int64_t D, int64_t V, int K, int sms) {
+    switch (path) {
+        case HeadPath::Skinny: return df2::head_tc_workspace(P, D, V, K, sms);
+        case HeadPath::Wide: return df2::wide_topk_workspace(P, V, K, sms);
+        default: return df2::head_simple_workspace(P, D, V, K, sms);
+    }
+}
+
 }  // namespace
 
 DF2_API size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V, int K, int r) {
@@ -69,10 +88,7 @@ DF2_API size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V
     if (check_head(P, D, V, K, 0, false) != DF2_OK || P == 0) return 0;
     const int sms = num_sms_current();
     if (sms <= 0) return 0;
-    size_t need = 0;
-    if (df2::head_tc_supported(P, D, V, K)) need = df2::head_tc_workspace(P, D, V, K, sms);
-    else need = df2::head_simple_workspace(P, D, V, K, sms);
-    return round_up(need, 256);
+    return round_up(head_workspace(pick_head(P, D, V, K), P, D, V, K, sms), 256);
 }
 
 DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,
@@ -90,14 +106,23 @@ DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const ui
     const int sms = num_sms_current();
     if (sms <= 0) return DF2_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool tc = df2::head_tc_supported(P, D, V, K);
-    const size_t need = round_up(tc ? df2::head_tc_workspace(P, D, V, K, sms)
-                                    : df2::head_simple_workspace(P, D, V, K, sms), 256);
+    const HeadPath path = pick_head(P, D, V, K);
+    const size_t need = round_up(head_workspace(path, P, D, V, K, sms), 256);
     if (workspace_bytes < need || (need > 0 && !workspace)) return DF2_ERR_WORKSPACE_TOO_SMALL;
-    if (tc) {
+    if (path == HeadPath::Skinny) {
         rc = df2::head_tc_launch(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
                                  dev_status, sms, st);
         return rc;
+    }
+    if (path == HeadPath::Wide) {
+        cudaError_t e = df2::wide_topk_launch(h, P, W_lm, V, D, K, topk_ids, topk_vals, workspace,
+                                              dev_status, sms, st);
+        if (e != cudaSuccess) return DF2_ERR_CUDA;
+        if (has_wh) {
+            e = df2::wide_store_launch(h, P, W_H, r, D, G, r, r, G, r, dev_status, st);
+            if (e != cudaSuccess) return DF2_ERR_CUDA;
+        }
+        return DF2_OK;
     }
     cudaError_t e = df2::head_simple_launch(h, P, D, W_lm, V, K, topk_ids, topk_vals, workspace,
                                             sms, st);
@@ -196,6 +221,9 @@ DF2_API int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int
         if (sms <= 0) return DF2_ERR_CUDA;
         e = df2::gemm_rows_launch(x, dtype == DF2_DTYPE_F32, W_proj, P, 2 * half, C, d_in, half, half,
                                   dyn_out, half, sms, st);
+    } else if (dtype == DF2_DTYPE_BF16 && df2::wide_supported(P, 2 * half, C, 1)) {
+        e = df2::wide_store_launch(static_cast<const uint16_t*>(x), P, W_proj, 2 * half, C, d_in, half,
+                                   half, dyn_out, half, nullptr, st);
     } else {
         e = df2::gemm_simple_launch(x, dtype == DF2_DTYPE_F32, W_proj, P, 2 * half, C, d_in, half,
                                     half, dyn_out, half, st);

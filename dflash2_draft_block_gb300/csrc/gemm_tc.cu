@@ -1,0 +1,437 @@
+// Many-row GEMM on the tensor cores: out[m, n] = sum_k A[m, k] * B[n, k] with
+// A = positions (h, or conv activations x) and B = the weight rows (W_lm, W_H,
+// W_proj), bf16 in, fp32 accumulate in TMEM (tcgen05.mma, M = 128, N = 256).
+//
+// Two epilogues share one TMA/MMA pipeline:
+//   * STORE: fp32 tile to global, columns split between two outputs (the conv
+//     projection's input-side and output-side kernels; G = H(h)).
+//   * TOPK: the unary logits of the head never leave the chip.  TMEM lane m of the
+//     accumulator is position m, so each epilogue thread owns one position and
+//     streams its 256 logits per tile against the K-th best so far; survivors go
+//     into a per-thread min-heap of the K best (root = the current K-th), kept in
+//     shared memory with a [slot][thread] layout so every lane hits its own bank.
+//     A CTA owns 128 positions and a contiguous vocabulary range; its per-position
+//     lists go to the workspace in rank order and topk_merge_sorted_kernel folds
+//     the ranges.
+//
+// Roles (192 threads): warp 0 lane 0 issues the TMA loads (stages of kbox
+// [128 x 64] A boxes and [256 x 64] B boxes, 128-byte swizzle), warp 1 lane 0
+// issues tcgen05.mma into one of two TMEM accumulators (2 x 256 columns), warps
+// 2-5 drain the other accumulator with tcgen05.ld.  All waits are bounded.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace df2 {
+
+namespace {
+
+constexpr int WM = 128;  // rows of A per tile (MMA M, TMEM lanes)
+constexpr int WN = 256;  // rows of B per tile (MMA N, TMEM columns)
+constexpr int WK = 64;   // K elements per box (one 128-byte swizzle row)
+constexpr int kWideThreads = 192;
+constexpr uint32_t kABox = WM * WK * 2;  // 16 KB
+constexpr uint32_t kBBox = WN * WK * 2;  // 32 KB
+constexpr int kWideMaxStages = 8;
+
+enum { EPI_STORE = 0, EPI_TOPK = 1 };
+
+struct WideArgs {
+    int M, N, Kd;           // A rows, B rows, reduction length
+    int n_mt;               // M tiles
+    int n_nt;               // N tiles
+    int tiles_per_cta;      // consecutive N tiles per CTA
+    int m_major;            // 1: consecutive CTAs share an M tile; 0: share an N range
+    int nstages, kbox;
+    // STORE
+    float* out0;
+    int64_t ld0;
+    int n_split;
+    float* out1;
+    int64_t ld1;
+    // TOPK
+    int K;
+    float* part_v;          // [n_groups][M][K]
+    int* part_id;
+    int32_t* dev_status;
+};
+
+__host__ __device__ inline uint32_t wide_stage_bytes(int kbox) { return uint32_t(kbox) * (kABox + kBBox); }
+
+__host__ __device__ inline uint32_t wide_smem(int nstages, int kbox, int epi, int K) {
+    uint32_t off = uint32_t(nstages) * wide_stage_bytes(kbox);
+    off += uint32_t(2 * nstages + 5) * 8 + 16;  // barriers, TMEM address, abort flag
+    off = (off + 15) / 16 * 16;
+    if (epi == EPI_TOPK) off += uint32_t(K) * 128 * 8;  // heaps [K][128] (value, id)
+    return off;
+}
+
+// Min-heap by rank order kept by one thread in [slot][thread] shared arrays: the
+// root is the worst of the kept entries.  (v, i) replaces the root and sifts down.
+__device__ __forceinline__ void heap_replace_root(float* hv, int* hi, int K, int tt, float v, int i) {
+    int pos = 0;
+    while (true) {
+        const int c1 = 2 * pos + 1;
+        if (c1 >= K) break;
+        int c = c1;
+        float cv = hv[c1 * 128 + tt];
+        int ci = hi[c1 * 128 + tt];
+        if (c1 + 1 < K) {
+            const float c2v = hv[(c1 + 1) * 128 + tt];
+            const int c2i = hi[(c1 + 1) * 128 + tt];
+            if (ranks_before(cv, ci, c2v, c2i)) { c = c1 + 1; cv = c2v; ci = c2i; }  // the worse child
+        }
+        if (!ranks_before(v, i, cv, ci)) break;  // new entry is not better than the worse child
+        hv[pos * 128 + tt] = cv;
+        hi[pos * 128 + tt] = ci;
+        pos = c;
+    }
+    hv[pos * 128 + tt] = v;
+    hi[pos * 128 + tt] = i;
+}
+
+}  // namespace
+
+namespace {
+
+template <int EPI>
+__global__ void __launch_bounds__(kWideThreads, 1)
+gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                 const WideArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int nstages = args.nstages, kbox = args.kbox;
+    const uint32_t stage_bytes = wide_stage_bytes(kbox);
+    uint8_t* stages = smem;  // stage s: kbox A boxes, then kbox B boxes
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(nstages) * stage_bytes);
+    uint64_t* empty = full + nstages;
+    uint64_t* tfull = empty + nstages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* mma_done = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    uint32_t heap_off = uint32_t(nstages) * stage_bytes + uint32_t(2 * nstages + 5) * 8 + 16;
+    heap_off = (heap_off + 15) / 16 * 16;
+    float* hv = reinterpret_cast<float*>(smem + heap_off);      // [K][128]
+    int* hi = reinterpret_cast<int*>(hv + size_t(args.K) * 128);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bid = int(blockIdx.x);
+    const int n_groups = (args.n_nt + args.tiles_per_cta - 1) / args.tiles_per_cta;
+    const int mt = args.m_major ? bid / n_groups : bid % args.n_mt;
+    const int grp = args.m_major ? bid % n_groups : bid / args.n_mt;
+    const int nt0 = grp * args.tiles_per_cta;
+    const int nt1 = min(args.n_nt, nt0 + args.tiles_per_cta);
+    const int nbox = (args.Kd + WK - 1) / WK;
+    const int nk = (nbox + kbox - 1) / kbox;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nstages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tempty[b], 4);
+        }
+        tc::mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (EPI == EPI_TOPK && warp >= 2) {
+        const int tt = (warp - 2) * 32 + lane;
+        for (int k = 0; k < args.K; ++k) {
+            hv[k * 128 + tt] = -INFINITY;
+            hi[k * 128 + tt] = INT_MAX;
+        }
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_holder, 512);
+        tc::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tm_a);
+        tc::prefetch_tmap(&tm_b);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            const uint64_t pol_a = tc::l2_policy_evict_last();
+            const uint64_t pol_b = EPI == EPI_TOPK ? tc::l2_policy_evict_first() : tc::l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            int8_t armed[kWideMaxStages];
+            for (int s = 0; s < kWideMaxStages; ++s) armed[s] = -1;
+            bool ok = true;
+            for (int nt = nt0; nt < nt1 && ok; ++nt) {
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int nb = min(kbox, nbox - kb * kbox);
+                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                    tc::mbar_arrive_expect_tx(&full[stage], uint32_t(nb) * (kABox + kBBox));
+                    uint8_t* st = stages + size_t(stage) * stage_bytes;
+                    for (int j = 0; j < nb; ++j) {
+                        const int x = (kb * kbox + j) * WK;
+                        tc::tma_load_2d(st + size_t(j) * kABox, &tm_a, &full[stage], x, mt * WM, pol_a);
+                        tc::tma_load_2d(st + size_t(kbox) * kABox + size_t(j) * kBBox, &tm_b, &full[stage], x,
+                                        nt * WN, pol_b);
+                    }
+                    armed[stage] = int8_t(phase);
+                    if (++stage == nstages) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int s = 0; s < nstages; ++s)
+                    if (armed[s] >= 0) tc::mbar_wait(&full[s], uint32_t(armed[s]), &never);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(WM, WN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int nt = nt0; nt < nt1 && ok; ++nt, ++it) {
+                const int b = it & 1;
+                const uint32_t tph = (it >> 1) & 1;
+                if (!tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag)) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem_base + uint32_t(b * WN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!tc::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    const int nb = min(kbox, nbox - kb * kbox);
+                    uint8_t* st = stages + size_t(stage) * stage_bytes;
+                    for (int j = 0; j < nb; ++j) {
+                        const uint32_t a0 = tc::smem_u32(st + size_t(j) * kABox);
+                        const uint32_t b0 = tc::smem_u32(st + size_t(kbox) * kABox + size_t(j) * kBBox);
+#pragma unroll
+                        for (int k = 0; k < WK / 16; ++k)
+                            tc::mma_bf16(d_tmem, tc::sw128_kmajor_desc(a0 + 32 * k),
+                                         tc::sw128_kmajor_desc(b0 + 32 * k), idesc, (kb | j | k) != 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&empty[stage]);
+                    if (++stage == nstages) { stage = 0; phase ^= 1; }
+                }
+                if (ok) tc::mma_commit(&tfull[b]);
+            }
+            tc::mma_commit(mma_done);
+            volatile int never = 0;
+            tc::mbar_wait(mma_done, 0, &never);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int tt = (warp - 2) * 32 + lane;      // heap column
+        const int m = mt * WM + quarter * 32 + lane;  // A row (position) of this thread
+        const bool row_ok = m < args.M;
+        float tv = -INFINITY;                       // heap root: the K-th best so far
+        int tid = INT_MAX;
+        int it = 0;
+        for (int nt = nt0; nt < nt1; ++nt, ++it) {
+            const int b = it & 1;
+            const uint32_t tph = (it >> 1) & 1;
+            const bool got = tc::mbar_wait(&tfull[b], tph, abort_flag);
+            if (!__all_sync(kFull, got)) break;
+            tc::fence_after_sync();
+            const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(b * WN);
+            for (int c0 = 0; c0 < WN; c0 += 16) {
+                float v[16];
+                tc::tmem_ld16(taddr + uint32_t(c0), v);
+                const int n0 = nt * WN + c0;
+                if (EPI == EPI_STORE) {
+                    if (row_ok) {
+                        const bool whole = n0 + 16 <= args.N;
+                        const bool side0 = n0 + 16 <= args.n_split, side1 = n0 >= args.n_split;
+                        float* dst = nullptr;
+                        if (side0) dst = args.out0 + int64_t(m) * args.ld0 + n0;
+                        else if (side1) dst = args.out1 + int64_t(m) * args.ld1 + (n0 - args.n_split);
+                        if (whole && dst && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                reinterpret_cast<float4*>(dst)[q] =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int n = n0 + e;
+                                if (n >= args.N) break;
+                                if (n < args.n_split) args.out0[int64_t(m) * args.ld0 + n] = v[e];
+                                else args.out1[int64_t(m) * args.ld1 + (n - args.n_split)] = v[e];
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int n = n0 + e;
+                        if (row_ok && n < args.N && ranks_before(v[e], n, tv, tid)) {
+                            heap_replace_root(hv, hi, args.K, tt, v[e], n);
+                            tv = hv[tt];
+                            tid = hi[tt];
+                        }
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&tempty[b]);
+        }
+        if (EPI == EPI_TOPK && row_ok) {
+            // heap -> rank order (repeatedly move the worst to the end), then write
+            const int K = args.K;
+            for (int end = K - 1; end > 0; --end) {
+                const float rv = hv[tt], ev = hv[end * 128 + tt];
+                const int ri = hi[tt], ei = hi[end * 128 + tt];
+                hv[end * 128 + tt] = rv;
+                hi[end * 128 + tt] = ri;
+                heap_replace_root(hv, hi, end, tt, ev, ei);
+            }
+            const size_t base = (size_t(grp) * args.M + m) * K;
+            for (int k = 0; k < K; ++k) {
+                const int id = hi[k * 128 + tt];
+                args.part_v[base + k] = id != INT_MAX ? hv[k * 128 + tt] : -INFINITY;
+                args.part_id[base + k] = id != INT_MAX ? id : -1;
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag && args.dev_status) atomicOr(args.dev_status, DF2_STATUS_WAIT_TIMEOUT);
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- host --
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 wide_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool wide_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = wide_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    cuuint32_t box[2] = {cuuint32_t(WK), cuuint32_t(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int wide_stages(int epi, int K) {
+    const uint32_t budget = 227 * 1024 - 1024;
+    for (int s = 4; s >= 2; --s)
+        if (wide_smem(s, 1, epi, K) <= budget) return s;
+    return 0;
+}
+
+// Vocabulary ranges per M tile for the top-K epilogue: enough CTAs to fill whole
+// waves of the SMs (at least 90% of the last wave busy).
+int wide_groups(int n_mt, int n_nt, int num_sms) {
+    for (int w = 1; w <= 16; ++w) {
+        int S = (w * num_sms) / n_mt;
+        if (S < 1) continue;
+        if (S > n_nt) S = n_nt;
+        if (double(n_mt) * S >= 0.9 * w * num_sms || S == n_nt) {
+            const int tpc = (n_nt + S - 1) / S;
+            return (n_nt + tpc - 1) / tpc;
+        }
+    }
+    return n_nt < num_sms ? n_nt : num_sms;
+}
+
+template <int EPI>
+cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const WideArgs& a, int grid,
+                        cudaStream_t stream) {
+    const size_t smem = wide_smem(a.nstages, a.kbox, EPI, a.K) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(gemm_wide_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    gemm_wide_kernel<EPI><<<grid, kWideThreads, smem, stream>>>(ta, tb, a);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool wide_supported(int64_t M, int64_t N, int64_t Kd, int K) {
+    return M >= 1 && N >= 1 && Kd >= 1 && Kd % 8 == 0 && M <= INT32_MAX && N <= INT32_MAX &&
+           Kd <= INT32_MAX && K <= 64 && wide_stages(EPI_TOPK, K < 1 ? 1 : K) >= 2;
+}
+
+size_t wide_topk_workspace(int64_t M, int64_t N, int K, int num_sms) {
+    const int n_mt = int((M + WM - 1) / WM), n_nt = int((N + WN - 1) / WN);
+    return size_t(wide_groups(n_mt, n_nt, num_sms)) * size_t(M) * size_t(K) * 8;
+}
+
+cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd,
+                              float* out0, int64_t ld0, int64_t n_split, float* out1, int64_t ld1,
+                              int32_t* dev_status, cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, WN)) return cudaErrorInvalidValue;
+    WideArgs a{};
+    a.M = int(M); a.N = int(N); a.Kd = int(Kd);
+    a.n_mt = int((M + WM - 1) / WM);
+    a.n_nt = int((N + WN - 1) / WN);
+    a.tiles_per_cta = 1;
+    a.m_major = 1;
+    a.nstages = wide_stages(EPI_STORE, 0);
+    a.kbox = 1;
+    a.out0 = out0; a.ld0 = ld0; a.n_split = int(n_split); a.out1 = out1; a.ld1 = ld1;
+    a.K = 0;
+    a.dev_status = dev_status;
+    return launch_wide<EPI_STORE>(ta, tb, a, a.n_mt * a.n_nt, stream);
+}
+
+cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
+                             int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
+                             cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, WN)) return cudaErrorInvalidValue;
+    WideArgs a{};
+    a.M = int(M); a.N = int(N); a.Kd = int(Kd);
+    a.n_mt = int((M + WM - 1) / WM);
+    a.n_nt = int((N + WN - 1) / WN);
+    const int groups = wide_groups(a.n_mt, a.n_nt, num_sms);
+    a.tiles_per_cta = (a.n_nt + groups - 1) / groups;
+    const int n_groups = (a.n_nt + a.tiles_per_cta - 1) / a.tiles_per_cta;
+    a.m_major = 0;
+    a.nstages = wide_stages(EPI_TOPK, K);
+    a.kbox = 1;
+    a.K = K;
+    a.part_v = static_cast<float*>(ws);
+    a.part_id = reinterpret_cast<int*>(a.part_v + size_t(groups) * M * K);
+    a.dev_status = dev_status;
+    cudaError_t e = launch_wide<EPI_TOPK>(ta, tb, a, a.n_mt * n_groups, stream);
+    if (e != cudaSuccess) return e;
+    return topk_merge_sorted_launch(a.part_v, a.part_id, n_groups, M, K, ids, vals, stream);
+}
+
+}  // namespace df2

@@ -33,6 +33,18 @@ cudaError_t gemm_rows_launch(const void* X, bool x_f32, const uint16_t* W, int64
                              int64_t Kd, float* out0, int64_t ld0, int64_t n_split, float* out1,
                              int64_t ld1, int num_sms, cudaStream_t stream);
 
+// ---- many-row tensor-core GEMM (gemm_tc.cu): A [M, Kd] x B [N, Kd]^T, bf16
+bool wide_supported(int64_t M, int64_t N, int64_t Kd, int K);
+size_t wide_topk_workspace(int64_t M, int64_t N, int K, int num_sms);
+// fp32 out, columns n < n_split to out0 (row stride ld0), the rest to out1
+cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd,
+                              float* out0, int64_t ld0, int64_t n_split, float* out1, int64_t ld1,
+                              int32_t* dev_status, cudaStream_t stream);
+// per-row top-K of A B^T (ids = B row indices), merged into ids/vals [M][K]
+cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
+                             int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
+                             cudaStream_t stream);
+
 // ---- selector
 cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,
                         const float* G, const uint16_t* A, const uint16_t* Bc, int64_t V, int K,

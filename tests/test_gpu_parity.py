@@ -90,6 +90,33 @@ def test_head_shapes(orc, df2, P, D, V, K):
     check_head(orc, df2, h, Wlm, K, WH, f"head{P}x{D}x{V}k{K}")
 
 
+@pytest.mark.parametrize("P,D,V,K", [
+    (129, 256, 1000, 16),     # many-position tensor-core path: ragged M tile, V % 256 != 0
+    (200, 320, 777, 64),      # D not a multiple of 64, K = 64
+    (130, 128, 513, 1),       # K = 1
+    (257, 64, 300, 33),       # three M tiles, K just above one register row
+    (48, 512, 5000, 16),      # just above the few-position path
+])
+def test_head_many_positions(orc, df2, P, D, V, K):
+    rng = _rng(P * 131 + D + V * 7 + K)
+    h = rand_bf16(rng, (P, D))
+    Wlm = rand_bf16(rng, (V, D), 0.02)
+    WH = rand_bf16(rng, (16 * (1 + P % 3), D), 0.02)
+    check_head(orc, df2, h, Wlm, K, WH, f"wide{P}x{D}x{V}k{K}")
+
+
+def test_head_many_positions_exact_ties(orc, df2):
+    rng = _rng(77)
+    P, D, V, K = 140, 128, 3000, 16
+    Wlm = rand_bf16(rng, (V, D), 0.02)
+    Wlm[1500:2400] = Wlm[0:900]          # duplicates in other CTA ranges and tiles
+    Wlm[2999] = Wlm[5]
+    h = rand_bf16(rng, (P, D))
+    gi, gv, _ = run_head(df2, h, Wlm, K)
+    oi, ov, om, _ = orc.unary_topk(h, Wlm, K)
+    assert np.array_equal(gi, oi)
+
+
 def test_head_exact_ties_break_to_lower_id(orc, df2):
     rng = _rng(5)
     P, D, V, K = 6, 128, 2000, 16
@@ -276,6 +303,9 @@ def test_tiny_conv(orc, df2):
     (27, 40, 9, 3, 2, "f32"),       # groups narrower than a 16-byte chunk
     (64, 512, 8, 6, 64, "bf16"),    # generic-taps path
     (8, 8, 8, 8, 8, "f32"),
+    (136, 264, 8, 3, 8, "bf16"),    # many rows: tensor-core projection, column split not /16
+    (80, 512, 16, 4, 16, "bf16"),   # many rows, taps 4
+    (72, 40, 9, 2, 4, "f32"),       # many fp32 rows: CUDA-core projection
 ])
 def test_conv_shapes(orc, df2, P, C, B, taps, g, dt):
     rng = _rng(P * 13 + C + taps * 7 + g)
