@@ -29,11 +29,11 @@ namespace df2 {
 namespace {
 
 constexpr int WM = 128;  // rows of A per tile (MMA M, TMEM lanes)
-constexpr int WN = 256;  // rows of B per tile (MMA N, TMEM columns)
 constexpr int WK = 64;   // K elements per box (one 128-byte swizzle row)
 constexpr int kWideThreads = 192;
 constexpr uint32_t kABox = WM * WK * 2;  // 16 KB
-constexpr uint32_t kBBox = WN * WK * 2;  // 32 KB
+// rows of B per tile (MMA N, TMEM columns): 256, or 192 to leave room for
+// 64-entry heaps next to four pipeline stages
 constexpr int kWideMaxStages = 8;
 
 enum { EPI_STORE = 0, EPI_TOPK = 1 };
@@ -55,55 +55,69 @@ struct WideArgs {
     int K;
     float* part_v;          // [n_groups][M][K]
     int* part_id;
+    unsigned* thr_g;        // [M] best K-th value so far over all ranges (ordered key), or null
     int32_t* dev_status;
 };
 
-__host__ __device__ inline uint32_t wide_stage_bytes(int kbox) { return uint32_t(kbox) * (kABox + kBBox); }
+__host__ __device__ inline uint32_t wide_stage_bytes(int kbox, int bn) {
+    return uint32_t(kbox) * (kABox + uint32_t(bn) * WK * 2);
+}
 
-__host__ __device__ inline uint32_t wide_smem(int nstages, int kbox, int epi, int K) {
-    uint32_t off = uint32_t(nstages) * wide_stage_bytes(kbox);
+__host__ __device__ inline uint32_t wide_smem(int nstages, int kbox, int epi, int K, int bn) {
+    uint32_t off = uint32_t(nstages) * wide_stage_bytes(kbox, bn);
     off += uint32_t(2 * nstages + 5) * 8 + 16;  // barriers, TMEM address, abort flag
     off = (off + 15) / 16 * 16;
     if (epi == EPI_TOPK) off += uint32_t(K) * 128 * 8;  // heaps [K][128] (value, id)
     return off;
 }
 
-// Min-heap by rank order kept by one thread in [slot][thread] shared arrays: the
-// root is the worst of the kept entries.  (v, i) replaces the root and sifts down.
-__device__ __forceinline__ void heap_replace_root(float* hv, int* hi, int K, int tt, float v, int i) {
+// Min-heap by rank order kept by one thread in a [slot][thread] shared array of
+// packed (value bits, id) pairs: the root is the worst of the kept entries.
+// (v, i) replaces the root and sifts down.
+__device__ __forceinline__ void heap_replace_root(uint2* hp, int K, int tt, float v, int i) {
     int pos = 0;
     while (true) {
         const int c1 = 2 * pos + 1;
         if (c1 >= K) break;
         int c = c1;
-        float cv = hv[c1 * 128 + tt];
-        int ci = hi[c1 * 128 + tt];
+        uint2 ce = hp[c1 * 128 + tt];
         if (c1 + 1 < K) {
-            const float c2v = hv[(c1 + 1) * 128 + tt];
-            const int c2i = hi[(c1 + 1) * 128 + tt];
-            if (ranks_before(cv, ci, c2v, c2i)) { c = c1 + 1; cv = c2v; ci = c2i; }  // the worse child
+            const uint2 c2 = hp[(c1 + 1) * 128 + tt];
+            if (ranks_before(__uint_as_float(ce.x), int(ce.y), __uint_as_float(c2.x), int(c2.y))) {
+                c = c1 + 1;  // the worse child
+                ce = c2;
+            }
         }
-        if (!ranks_before(v, i, cv, ci)) break;  // new entry is not better than the worse child
-        hv[pos * 128 + tt] = cv;
-        hi[pos * 128 + tt] = ci;
+        if (!ranks_before(v, i, __uint_as_float(ce.x), int(ce.y))) break;
+        hp[pos * 128 + tt] = ce;
         pos = c;
     }
-    hv[pos * 128 + tt] = v;
-    hi[pos * 128 + tt] = i;
+    hp[pos * 128 + tt] = make_uint2(__float_as_uint(v), unsigned(i));
+}
+
+// Order-preserving map of finite floats to unsigned keys (0 = below everything).
+__device__ __forceinline__ unsigned order_key(float v) {
+    const unsigned u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+    if (k < 0x00800000u) return -INFINITY;  // below the key of -inf: nothing published yet
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 }  // namespace
 
 namespace {
 
-template <int EPI>
+template <int EPI, int WN>
 __global__ void __launch_bounds__(kWideThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const WideArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr uint32_t kBBox = WN * WK * 2;
     const int nstages = args.nstages, kbox = args.kbox;
-    const uint32_t stage_bytes = wide_stage_bytes(kbox);
+    const uint32_t stage_bytes = wide_stage_bytes(kbox, WN);
     uint8_t* stages = smem;  // stage s: kbox A boxes, then kbox B boxes
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(nstages) * stage_bytes);
     uint64_t* empty = full + nstages;
@@ -114,8 +128,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     uint32_t heap_off = uint32_t(nstages) * stage_bytes + uint32_t(2 * nstages + 5) * 8 + 16;
     heap_off = (heap_off + 15) / 16 * 16;
-    float* hv = reinterpret_cast<float*>(smem + heap_off);      // [K][128]
-    int* hi = reinterpret_cast<int*>(hv + size_t(args.K) * 128);
+    uint2* hp = reinterpret_cast<uint2*>(smem + heap_off);      // [K][128] (value bits, id)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bid = int(blockIdx.x);
@@ -142,10 +155,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     }
     if (EPI == EPI_TOPK && warp >= 2) {
         const int tt = (warp - 2) * 32 + lane;
-        for (int k = 0; k < args.K; ++k) {
-            hv[k * 128 + tt] = -INFINITY;
-            hi[k * 128 + tt] = INT_MAX;
-        }
+        for (int k = 0; k < args.K; ++k) hp[k * 128 + tt] = make_uint2(__float_as_uint(-INFINITY), unsigned(INT_MAX));
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_holder, 512);
@@ -236,6 +246,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         const bool row_ok = m < args.M;
         float tv = -INFINITY;                       // heap root: the K-th best so far
         int tid = INT_MAX;
+        // Best K-th value any vocabulary range has reached for this position: a
+        // logit strictly below it cannot be in the global top-K.
+        float gthr = -INFINITY;
         int it = 0;
         for (int nt = nt0; nt < nt1; ++nt, ++it) {
             const int b = it & 1;
@@ -271,13 +284,30 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                         }
                     }
                 } else {
+                    // the chunk's candidates that beat the current K-th, as a bit mask;
+                    // the warp then inserts them in rounds, one per lane per round, so
+                    // the cost is the largest per-lane count, not one round per column
+                    unsigned mask = 0;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int n = n0 + e;
-                        if (row_ok && n < args.N && ranks_before(v[e], n, tv, tid)) {
-                            heap_replace_root(hv, hi, args.K, tt, v[e], n);
-                            tv = hv[tt];
-                            tid = hi[tt];
+                        if (row_ok && n < args.N && v[e] >= gthr && ranks_before(v[e], n, tv, tid))
+                            mask |= 1u << e;
+                    }
+                    while (__any_sync(kFull, mask != 0)) {
+                        if (mask) {
+                            const int j = __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            float cv = v[0];
+#pragma unroll
+                            for (int e = 1; e < 16; ++e) cv = (j == e) ? v[e] : cv;
+                            const int n = n0 + j;
+                            if (ranks_before(cv, n, tv, tid)) {
+                                heap_replace_root(hp, args.K, tt, cv, n);
+                                const uint2 root = hp[tt];
+                                tv = __uint_as_float(root.x);
+                                tid = int(root.y);
+                            }
                         }
                     }
                 }
@@ -285,22 +315,27 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&tempty[b]);
+            if (EPI == EPI_TOPK && args.thr_g && row_ok) {
+                unsigned k = 0;
+                if (tid != INT_MAX) k = order_key(tv);  // heap full: publish its K-th value
+                const unsigned old = atomicMax(args.thr_g + m, k);
+                gthr = key_value(old > k ? old : k);
+            }
         }
         if (EPI == EPI_TOPK && row_ok) {
             // heap -> rank order (repeatedly move the worst to the end), then write
             const int K = args.K;
             for (int end = K - 1; end > 0; --end) {
-                const float rv = hv[tt], ev = hv[end * 128 + tt];
-                const int ri = hi[tt], ei = hi[end * 128 + tt];
-                hv[end * 128 + tt] = rv;
-                hi[end * 128 + tt] = ri;
-                heap_replace_root(hv, hi, end, tt, ev, ei);
+                const uint2 root = hp[tt], last = hp[end * 128 + tt];
+                hp[end * 128 + tt] = root;
+                heap_replace_root(hp, end, tt, __uint_as_float(last.x), int(last.y));
             }
             const size_t base = (size_t(grp) * args.M + m) * K;
             for (int k = 0; k < K; ++k) {
-                const int id = hi[k * 128 + tt];
-                args.part_v[base + k] = id != INT_MAX ? hv[k * 128 + tt] : -INFINITY;
-                args.part_id[base + k] = id != INT_MAX ? id : -1;
+                const uint2 en = hp[k * 128 + tt];
+                const bool ok_k = int(en.y) != INT_MAX;
+                args.part_v[base + k] = ok_k ? __uint_as_float(en.x) : -INFINITY;
+                args.part_id[base + k] = ok_k ? int(en.y) : -1;
             }
         }
     }
@@ -345,10 +380,12 @@ bool wide_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int wide_bn(int epi, int K) { return (epi == EPI_TOPK && K > 32) ? 192 : 256; }
+
 int wide_stages(int epi, int K) {
     const uint32_t budget = 227 * 1024 - 1024;
     for (int s = 4; s >= 2; --s)
-        if (wide_smem(s, 1, epi, K) <= budget) return s;
+        if (wide_smem(s, 1, epi, K, wide_bn(epi, K)) <= budget) return s;
     return 0;
 }
 
@@ -367,14 +404,14 @@ int wide_groups(int n_mt, int n_nt, int num_sms) {
     return n_nt < num_sms ? n_nt : num_sms;
 }
 
-template <int EPI>
+template <int EPI, int BN>
 cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const WideArgs& a, int grid,
                         cudaStream_t stream) {
-    const size_t smem = wide_smem(a.nstages, a.kbox, EPI, a.K) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(gemm_wide_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem));
+    const size_t smem = wide_smem(a.nstages, a.kbox, EPI, a.K, BN) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(gemm_wide_kernel<EPI, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    gemm_wide_kernel<EPI><<<grid, kWideThreads, smem, stream>>>(ta, tb, a);
+    gemm_wide_kernel<EPI, BN><<<grid, kWideThreads, smem, stream>>>(ta, tb, a);
     note_launch();
     return cudaGetLastError();
 }
@@ -387,19 +424,20 @@ bool wide_supported(int64_t M, int64_t N, int64_t Kd, int K) {
 }
 
 size_t wide_topk_workspace(int64_t M, int64_t N, int K, int num_sms) {
-    const int n_mt = int((M + WM - 1) / WM), n_nt = int((N + WN - 1) / WN);
-    return size_t(wide_groups(n_mt, n_nt, num_sms)) * size_t(M) * size_t(K) * 8;
+    const int bn = wide_bn(EPI_TOPK, K);
+    const int n_mt = int((M + WM - 1) / WM), n_nt = int((N + bn - 1) / bn);
+    return size_t(wide_groups(n_mt, n_nt, num_sms)) * size_t(M) * size_t(K) * 8 + size_t(M) * 4;
 }
 
 cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd,
                               float* out0, int64_t ld0, int64_t n_split, float* out1, int64_t ld1,
                               int32_t* dev_status, cudaStream_t stream) {
     CUtensorMap ta, tb;
-    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, WN)) return cudaErrorInvalidValue;
+    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, 256)) return cudaErrorInvalidValue;
     WideArgs a{};
     a.M = int(M); a.N = int(N); a.Kd = int(Kd);
     a.n_mt = int((M + WM - 1) / WM);
-    a.n_nt = int((N + WN - 1) / WN);
+    a.n_nt = int((N + 256 - 1) / 256);
     a.tiles_per_cta = 1;
     a.m_major = 1;
     a.nstages = wide_stages(EPI_STORE, 0);
@@ -407,18 +445,19 @@ cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, i
     a.out0 = out0; a.ld0 = ld0; a.n_split = int(n_split); a.out1 = out1; a.ld1 = ld1;
     a.K = 0;
     a.dev_status = dev_status;
-    return launch_wide<EPI_STORE>(ta, tb, a, a.n_mt * a.n_nt, stream);
+    return launch_wide<EPI_STORE, 256>(ta, tb, a, a.n_mt * a.n_nt, stream);
 }
 
 cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
                              int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
                              cudaStream_t stream) {
+    const int bn = wide_bn(EPI_TOPK, K);
     CUtensorMap ta, tb;
-    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, WN)) return cudaErrorInvalidValue;
+    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, bn)) return cudaErrorInvalidValue;
     WideArgs a{};
     a.M = int(M); a.N = int(N); a.Kd = int(Kd);
     a.n_mt = int((M + WM - 1) / WM);
-    a.n_nt = int((N + WN - 1) / WN);
+    a.n_nt = int((N + bn - 1) / bn);
     const int groups = wide_groups(a.n_mt, a.n_nt, num_sms);
     a.tiles_per_cta = (a.n_nt + groups - 1) / groups;
     const int n_groups = (a.n_nt + a.tiles_per_cta - 1) / a.tiles_per_cta;
@@ -428,8 +467,12 @@ cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, in
     a.K = K;
     a.part_v = static_cast<float*>(ws);
     a.part_id = reinterpret_cast<int*>(a.part_v + size_t(groups) * M * K);
+    a.thr_g = reinterpret_cast<unsigned*>(a.part_id + size_t(groups) * M * K);
     a.dev_status = dev_status;
-    cudaError_t e = launch_wide<EPI_TOPK>(ta, tb, a, a.n_mt * n_groups, stream);
+    cudaError_t e = cudaMemsetAsync(a.thr_g, 0, size_t(M) * 4, stream);
+    if (e != cudaSuccess) return e;
+    e = bn == 192 ? launch_wide<EPI_TOPK, 192>(ta, tb, a, a.n_mt * n_groups, stream)
+                  : launch_wide<EPI_TOPK, 256>(ta, tb, a, a.n_mt * n_groups, stream);
     if (e != cudaSuccess) return e;
     return topk_merge_sorted_launch(a.part_v, a.part_id, n_groups, M, K, ids, vals, stream);
 }
