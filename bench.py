@@ -47,19 +47,27 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-HEAD_SOURCES = ["head_tc.cu", "topk_warp.cuh", "tc_ptx.cuh", "common.cuh"]
+# The dominant kernel per workload, the committed ncu summary of it, and the
+# sources whose hash the summary records.
+PROFILES = {
+    "batch1": ("head_skinny_kernel_batch1.md", ["head_tc.cu", "topk_warp.cuh", "tc_ptx.cuh", "common.cuh"]),
+    "batched": ("gemm_wide_topk_batched.md", ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh"]),
+}
 
 
-def head_traffic():
-    """DRAM traffic per launch of the head kernel from the committed ncu summary,
-    or None when the kernel's sources changed since that capture."""
+def head_traffic(workload="batch1"):
+    """DRAM traffic per launch of the workload's dominant kernel from the committed
+    ncu summary, or None when there is none or the kernel's sources changed since."""
     import hashlib
     import re
-    path = os.path.join(ROOT, "profiles", "head_skinny_kernel_batch1.md")
+    if workload not in PROFILES:
+        return None, "no capture for this workload"
+    fname, sources = PROFILES[workload]
+    path = os.path.join(ROOT, "profiles", fname)
     try:
         text = open(path).read()
         h = hashlib.sha256()
-        for f in HEAD_SOURCES:
+        for f in sources:
             with open(os.path.join(ROOT, "dflash2_draft_block_gb300", "csrc", f), "rb") as fh:
                 h.update(fh.read())
         sha = re.search(r"source_sha256_16 = ([0-9a-f]{16})", text).group(1)
@@ -68,7 +76,23 @@ def head_traffic():
         return None, "no capture"
     if h.hexdigest()[:16] != sha:
         return None, "kernel changed since the capture"
-    return traffic, "profiles/head_skinny_kernel_batch1.md"
+    return traffic, "profiles/" + fname
+
+
+def slowest_rank_ms(ms, dist, device):
+    """Max of a per-rank time over all ranks (the job is as slow as its slowest
+    replica); unchanged when not distributed."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job rate: every rank processed units_per_rank in the (max) time ms."""
+    return units_per_rank * world / (ms * 1e-3)
 
 
 def head_bytes(w):
@@ -286,11 +310,7 @@ def gpu_arm(args, w, rank, world, torch):
         fe[1].record()
         torch.cuda.synchronize()
         flush_ms = fe[0].elapsed_time(fe[1]) / 5 * args.steps
-    step_ms = (total_ms - flush_ms) / args.steps
-    if dist is not None:
-        t = torch.tensor([step_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = slowest_rank_ms((total_ms - flush_ms) / args.steps, dist, device)
     per_call_us = (per_call / args.steps * 1e3).tolist()
 
     # ---- end to end through the public API with host buffers
@@ -325,23 +345,34 @@ def gpu_arm(args, w, rank, world, torch):
             step.flush.zero_()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = (e0.elapsed_time(e1) - flush_ms) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_rank_ms((e0.elapsed_time(e1) - flush_ms) / args.steps, dist, device)
 
     clocks = clk.summary()
     out = None
     if rank == 0:
         peaks, src = load_peaks()
-        traffic, traffic_src = head_traffic()
         hb = head_bytes(w)
         head_us = per_call_us[2]
-        achieved = hb / (head_us * 1e-6) / 1e9
+        traffic, traffic_src = head_traffic(w.name)
+        if w.P <= 32:
+            # few positions: the head streams the LM head from HBM
+            roof = {"kernel": "dflash2_unary_topk call (head_skinny_kernel + top-K merge)", "bound": "hbm",
+                    "achieved": hb / (head_us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "algorithmic_bytes": hb}
+        else:
+            # many positions: the logits GEMM (plus G) is tensor-core bound
+            flops = 2.0 * w.P * w.D * (w.V + w.r)
+            pk = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+            roof = {"kernel": "dflash2_unary_topk call (gemm_wide_kernel top-K + G + merge)",
+                    "bound": "tensor", "achieved": flops / (head_us * 1e-6) / 1e12, "peak": pk,
+                    "unit": "TFLOP/s", "algorithmic_flops": flops}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["peak_source"] = src
+        roof["traffic"] = traffic
+        roof["traffic_source"] = traffic_src
         out = {
             "metric": METRIC,
-            "value": w.P * world / (step_ms * 1e-3),
+            "value": job_throughput(w.P, world, step_ms),
             "unit": "positions/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -353,17 +384,13 @@ def gpu_arm(args, w, rank, world, torch):
             "dtype": "bf16",
             "data": "synthetic (seeded; shapes and scales of the workload, no dataset or checkpoint)",
             "config": config_of(w),
-            "drafted_positions_per_s": w.R * (w.B - 1) * world / (step_ms * 1e-3),
+            "drafted_positions_per_s": job_throughput(w.R * (w.B - 1), world, step_ms),
             "per_call_us": dict(zip(["conv_prepare", "conv_finish", "unary_topk", "selector_walk",
                                      "selector_pair_scores"], per_call_us)),
             "conv_gbs": {"prepare": conv_bytes(w, "prepare") / (per_call_us[0] * 1e-6) / 1e9,
                          "finish": conv_bytes(w, "finish") / (per_call_us[1] * 1e-6) / 1e9},
-            "roofline": {"kernel": "dflash2_unary_topk call (head_skinny_kernel + top-K merge)",
-                         "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "peak_source": src, "traffic": traffic if w.name == "batch1" else None,
-                         "traffic_source": traffic_src, "algorithmic_bytes": hb},
-            "e2e": {"value": w.P * world / (e2e_ms * 1e-3), "unit": "positions/s",
+            "roofline": roof,
+            "e2e": {"value": job_throughput(w.P, world, e2e_ms), "unit": "positions/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": timed_launches,
             "kernels_per_step": n_launch,

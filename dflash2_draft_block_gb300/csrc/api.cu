@@ -246,3 +246,21 @@ DF2_API int dflash2_conv_finish(const void* z, int dtype, int64_t P, int C, int 
                                             base + int64_t(taps) * C, dyn_out, int64_t(taps) * G, y,
                                             static_cast<cudaStream_t>(stream)));
 }
+
+// ---------------------------------------------------------------- self-test --
+
+DF2_API int dflash2_selftest_wait_timeout(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,
+                                          int64_t V, int K, int32_t* topk_ids, float* topk_vals,
+                                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                          void* stream) {
+    int rc = check_head(P, D, V, K, 0, false);
+    if (rc != DF2_OK) return rc;
+    if (P == 0 || !df2::head_tc_supported(P, D, V, K) || !dev_status) return DF2_ERR_UNSUPPORTED;
+    if (!h || !W_lm || !topk_ids || !topk_vals) return DF2_ERR_INVALID_ARGUMENT;
+    const int sms = num_sms_current();
+    if (sms <= 0) return DF2_ERR_CUDA;
+    const size_t need = round_up(df2::head_tc_workspace(P, D, V, K, sms), 256);
+    if (workspace_bytes < need || !workspace) return DF2_ERR_WORKSPACE_TOO_SMALL;
+    return df2::head_tc_launch(h, P, D, W_lm, V, K, nullptr, 0, nullptr, topk_ids, topk_vals, workspace,
+                               dev_status, sms, static_cast<cudaStream_t>(stream), /*stall_stage=*/0);
+}

@@ -74,7 +74,7 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_wh, int P, int D, int V, int K, int r,
                    int n_vtiles, int n_tiles, int nstages, int kbox, int pf_stages, int nacc,
                    float* __restrict__ part_v, int* __restrict__ part_id, float* __restrict__ G,
-                   int32_t* __restrict__ dev_status) {
+                   int32_t* __restrict__ dev_status, int stall_stage) {
     // TMEM: two tile buffers (the epilogue drains one while the MMAs fill the
     // other), each holding nacc partial accumulators of N columns.  Successive
     // k-steps of a tile rotate over the partial accumulators, so consecutive MMAs
@@ -160,7 +160,9 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 const int nb = min(kbox, nbox - kb * kbox);
                 if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
                 tc::mbar_arrive_expect_tx(&full[stage], uint32_t(nb) * (kWBytes + h_box_bytes));
-                for (int j = 0; j < nb; ++j) {
+                // self-test only: a stage whose copies are never issued, so the
+                // consumer's bounded wait must give up and report a timeout
+                for (int j = 0; j < nb && g != stall_stage; ++j) {
                     tc::tma_load_2d(sW + size_t(stage) * L.stage_w + size_t(j) * kWBytes, mw, &full[stage],
                                     (kb * kbox + j) * BK, row0, pol_w);
                     tc::tma_load_2d(sH + size_t(stage) * L.stage_h + size_t(j) * h_box_bytes, &tm_h,
@@ -393,7 +395,7 @@ size_t head_tc_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms) {
 
 int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V, int K,
                    const uint16_t* W_H, int r, float* G, int32_t* ids, float* vals, void* ws,
-                   int32_t* dev_status, int num_sms, cudaStream_t stream) {
+                   int32_t* dev_status, int num_sms, cudaStream_t stream, int stall_stage) {
     const Plan pl = pick_plan(P, K);
     const int N = pl.N;
     CUtensorMap tm_w, tm_h, tm_wh;
@@ -419,7 +421,7 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
         if (e != cudaSuccess) return DF2_ERR_CUDA;                                                \
         head_skinny_kernel<NV, RV><<<grid, kThreads, smem, stream>>>(                             \
             tm_w, tm_h, tm_wh, int(P), int(D), int(V), K, r, n_vtiles, n_tiles, pl.nstages,       \
-            pl.kbox, DF2_HEAD_PF, DF2_HEAD_NACC, part_v, part_id, G, dev_status);                 \
+            pl.kbox, DF2_HEAD_PF, DF2_HEAD_NACC, part_v, part_id, G, dev_status, stall_stage);    \
     } while (0)
     if (N == 16 && pl.R == 1) DF2_HEAD(16, 1);
     else if (N == 16) DF2_HEAD(16, 2);

@@ -9,8 +9,10 @@ namespace df2 {
 
 bool head_tc_supported(int64_t P, int64_t D, int64_t V, int K);
 size_t head_tc_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms);
+// stall_stage >= 0 (self-test only): that pipeline stage's copies are never
+// issued, so the kernel's bounded waits time out and report it in dev_status.
 int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V, int K,
                    const uint16_t* W_H, int r, float* G, int32_t* ids, float* vals, void* ws,
-                   int32_t* dev_status, int num_sms, cudaStream_t stream);
+                   int32_t* dev_status, int num_sms, cudaStream_t stream, int stall_stage = -1);
 
 }  // namespace df2

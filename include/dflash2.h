@@ -232,6 +232,23 @@ int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int B, int 
 int dflash2_conv_finish(const void* z, int dtype, int64_t P, int C, int B, int taps, int g,
                         const float* dyn_out, const float* base, void* y, void* stream);
 
+/* ------------------------------------------------------------------------
+ * dflash2_selftest_wait_timeout — exercises the in-kernel timeout path.
+ *
+ * No counterpart in the pages: a diagnostic.  Runs the tensor-core head of
+ * dflash2_unary_topk (same arguments, no W_H; shapes must take that path:
+ * P <= 32, K <= 64) with the copies of its first pipeline stage never issued.
+ * The kernel's bounded waits give up after about one second, every role drains
+ * its own work, frees its tensor memory and exits, and DF2_STATUS_WAIT_TIMEOUT is
+ * OR-ed into *dev_status (required, not NULL).  The outputs are meaningless; the
+ * device and context stay usable.  Returns DF2_ERR_UNSUPPORTED for shapes that
+ * do not take the tensor-core head.
+ * ---------------------------------------------------------------------- */
+int dflash2_selftest_wait_timeout(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,
+                                  int64_t V, int K, int32_t* topk_ids, float* topk_vals,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -393,3 +393,36 @@ def test_full_size_conv(orc, df2, name):
     close_bf16(gy[rows], oy, what=name + " y")
     oy2 = orc.conv_finish(z, w.B, w.taps, w.g, od, c["base"])
     close_bf16(gy2[rows], oy2, what=name + " finish")
+
+
+# ------------------------------------------------------- failure detection ----
+
+def test_bounded_wait_reports_timeout_and_device_stays_usable(df2):
+    """A pipeline stage whose copies are never issued: the tensor-core head's
+    bounded waits must give up, report DF2_STATUS_WAIT_TIMEOUT and leave the
+    device usable for the next call (no trap, no fault)."""
+    import ctypes as ct
+    lib = df2.lib()
+    P, D, V, K = 8, 256, 4096, 16
+    h = torch.randn(P, D, device="cuda").to(torch.bfloat16)
+    Wlm = (torch.randn(V, D, device="cuda") * 0.02).to(torch.bfloat16)
+    ids = torch.empty(P, K, dtype=torch.int32, device="cuda")
+    vals = torch.empty(P, K, dtype=torch.float32, device="cuda")
+    nb = df2.unary_topk_workspace_size(P, D, V, K)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = ct.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.dflash2_selftest_wait_timeout(ct.c_void_p(h.data_ptr()), P, D, ct.c_void_p(Wlm.data_ptr()), V, K,
+                                           ct.c_void_p(ids.data_ptr()), ct.c_void_p(vals.data_ptr()),
+                                           ct.c_void_p(ws.data_ptr()), nb, ct.c_void_p(status.data_ptr()),
+                                           stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) & df2.DF2_STATUS_WAIT_TIMEOUT
+    # the same call without the stall works right after, with no timeout
+    status.zero_()
+    ids2, vals2, _ = df2.unary_topk(h, Wlm, K, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = torch.topk((h.float() @ Wlm.float().T), K, dim=1)
+    assert (ids2.long() == ref.indices).float().mean() > 0.9
