@@ -73,6 +73,8 @@ class Oracle:
         L.df2o_unary_topk.argtypes = [vp, i64, i64, vp, i64, i32, vp, i32, vp, vp, vp, vp]
         L.df2o_selector_walk.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp, vp, vp]
         L.df2o_selector_pair_scores.argtypes = [vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp]
+        L.df2o_selector_lattice.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp]
+        L.df2o_lattice_walk.argtypes = [vp, vp, i32, i32, i32, i64, vp, ct.c_double, vp, vp, vp, vp]
         L.df2o_conv_prepare.argtypes = [vp, ct.c_int, i64, i32, i32, i32, i32, vp, vp, vp, vp]
         L.df2o_conv_finish.argtypes = [vp, ct.c_int, i64, i32, i32, i32, i32, vp, vp, vp]
         for f in ("df2o_logits", "df2o_unary_topk", "df2o_selector_walk",
@@ -150,6 +152,43 @@ class Oracle:
         self._check(self.lib.df2o_selector_pair_scores(_p(pred), P, _p(ids), _p(vals), _p(G), _p(A),
                                                        _p(Bc), V, K, r, _p(scores), _p(status)))
         return scores, int(status[0])
+
+    def lattice(self, anchors, ids, vals, G, A, Bc, block_size):
+        """ids/vals [R*B, K], G [R*B, r]; returns (lattice [R, B-1, K, K] f32, status)."""
+        anchors = _c(anchors, np.int32)
+        ids, vals, G = _c(ids, np.int32), _c(vals, np.float32), _c(G, np.float32)
+        A, Bc = _c(A, np.uint16), _c(Bc, np.uint16)
+        R = anchors.shape[0]
+        B = int(block_size)
+        K = ids.shape[-1]
+        V, r = A.shape
+        assert ids.size == R * B * K and G.size == R * B * r and Bc.shape == (V, r)
+        lat = np.empty((R, B - 1, K, K), np.float32)
+        status = np.zeros((1,), np.int32)
+        self._check(self.lib.df2o_selector_lattice(_p(anchors), R, B, _p(ids), _p(vals), _p(G), _p(A),
+                                                   _p(Bc), V, K, r, _p(lat), _p(status)))
+        return lat, int(status[0])
+
+    def lattice_walk(self, lattice, ids, block_size, V, uniforms=None, temperature=1.0):
+        """lattice [R, B-1, K, K], ids [R*B, K], uniforms [R, B-1] or None (greedy);
+        returns (path [R,B-1], score [R,B-1], margin [R,B-1], status)."""
+        lattice = _c(lattice, np.float32)
+        ids = _c(ids, np.int32)
+        R, T, K, K2 = lattice.shape
+        B = int(block_size)
+        assert K == K2 and T == B - 1 and ids.size == R * B * K
+        if uniforms is not None:
+            uniforms = _c(uniforms, np.float32)
+            assert uniforms.size == R * T
+        path = np.empty((R, T), np.int32)
+        score = np.empty((R, T), np.float32)
+        margin = np.empty((R, T), np.float64)
+        status = np.zeros((1,), np.int32)
+        self._check(self.lib.df2o_lattice_walk(_p(lattice), _p(ids), R, B, K, int(V),
+                                               _p(uniforms),
+                                               float(temperature), _p(path), _p(score), _p(margin),
+                                               _p(status)))
+        return path, score, margin, int(status[0])
 
     # -- conv -----------------------------------------------------------------
     def conv_prepare(self, x, block_size, taps, group, W_proj, base):

@@ -21,6 +21,9 @@
  *                   PR #62, "Selector training objective")
  *   teacher-forced  the same score with the predecessor given, all positions at
  *                   once (PR #62, "Selector training objective")
+ *   lattice         every adjacent candidate pair scored at once, then a greedy or
+ *                   sampling walk over the finished table ("DFlash 2 Explanation",
+ *                   "How It Works", Problem 1)
  *   conv            Conv_k(x)_t = k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1}, k = base +
  *                   a per-group correction projected from the hidden state; the
  *                   projection made before the sublayer also yields the kernel
@@ -34,6 +37,8 @@
  *   - top-K ranks by (value descending, token id ascending); the walk's argmax
  *     breaks equal scores toward the lower token id.  Both decisions are taken
  *     on fp32 values, the precision the kernels produce.
+ *   - sampling draws from softmax(S / temperature) over the K candidates by the
+ *     inverse CDF in candidate-list order, with one uniform per step passed in.
  *   - taps generalise the two-tap form: y_t = sum_{j < taps, t-j >= 0} k_{t,j} x_{t-j},
  *     with t the position inside its anchor block (zero padding inside a block).
  *   - projection row index (io*taps + j)*G + gi, io = 0 for the kernel applied
@@ -293,6 +298,179 @@ int df2o_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* ids
     }
     if (status) *status = bad;
     return DF2O_OK;
+}
+
+/* ------------------------------------------------------------- lattice -- */
+
+/* 1 when the anchor and every candidate id of rows 1 .. Bsz-1 of request q lie in [0, V). */
+static int request_ids_valid(const int32_t* anchors, int32_t q, int32_t Bsz, const int32_t* ids,
+                             int64_t V, int32_t K)
+{
+    if (anchors[q] < 0 || anchors[q] >= V) return 0;
+    for (int64_t t = 1; t < Bsz; ++t)
+        for (int32_t j = 0; j < K; ++j) {
+            int32_t b = ids[((int64_t)q * Bsz + t) * K + j];
+            if (b < 0 || b >= V) return 0;
+        }
+    return 1;
+}
+
+/*
+ * The lattice of pair scores ("DFlash 2 Explanation", "How It Works", Problem 1:
+ * every adjacent pair is scored in one parallel pass and only the final walk over
+ * the finished scores is sequential).  Table slot t-1 of request q, for drafted
+ * position t = 1 .. Bsz-1, holds
+ *     L[q][t-1][i][j] = S_t(a_i, b_j),   b_j = ids[q, t, j],
+ * where a_i is the i-th predecessor candidate: ids[q, t-1, i] for t >= 2, and for
+ * t = 1 the anchor alone in row i = 0 (rows 1 .. K-1 of slot 0 are NaN).
+ * Layout [R][Bsz-1][K][K] fp32.  A request with an id outside [0, V) gets an
+ * all-NaN table and sets bit 1 of *status.
+ */
+int df2o_selector_lattice(const int32_t* anchors, int32_t R, int32_t Bsz, const int32_t* ids,
+                          const float* vals, const float* G, const uint16_t* A, const uint16_t* Bc,
+                          int64_t V, int32_t K, int32_t r, float* lattice, int32_t* status)
+{
+    if (R < 0 || Bsz < 2 || K < 1 || r < 1 || V < 1 || K > V) return DF2O_INVALID;
+    const int64_t T = Bsz - 1;
+    const int64_t KK = (int64_t)K * K;
+    int32_t bad = 0;
+    int32_t q;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (q = 0; q < R; ++q) {
+        float* Lq = lattice + (int64_t)q * T * KK;
+        if (!request_ids_valid(anchors, q, Bsz, ids, V, K)) {
+            for (int64_t e = 0; e < T * KK; ++e) Lq[e] = NAN;
+            bad |= 1;
+            continue;
+        }
+        for (int64_t t = 1; t < Bsz; ++t) {
+            const int64_t row = (int64_t)q * Bsz + t;
+            float* Lt = Lq + (t - 1) * KK;
+            for (int32_t i = 0; i < K; ++i) {
+                int32_t a;
+                if (t == 1) {
+                    if (i > 0) {
+                        for (int32_t j = 0; j < K; ++j) Lt[(int64_t)i * K + j] = NAN;
+                        continue;
+                    }
+                    a = anchors[q];
+                } else {
+                    a = ids[(row - 1) * K + i];
+                }
+                for (int32_t j = 0; j < K; ++j)
+                    Lt[(int64_t)i * K + j] =
+                        pair_score(vals[row * K + j], a, ids[row * K + j], G + row * r, A, Bc, r);
+            }
+        }
+    }
+    if (status) *status = bad;
+    return DF2O_OK;
+}
+
+/*
+ * The walk over a finished lattice, request q.  The state is the row i of the
+ * current predecessor (i = 0, the anchor, at t = 1).  For t = 1 .. Bsz-1 the
+ * step reads row i of slot t-1 and picks a column j, which becomes the next row:
+ *   greedy (uniforms == NULL): the largest score, equal scores to the lower
+ *     token id; margin = best - second best (+inf when K == 1).
+ *   sampling: a draw from softmax(L[t-1][i][.] / temperature) by the inverse CDF
+ *     in candidate-list order with u = uniforms[q, t-1] in [0, 1): with
+ *     w_j = exp((L_j - max_j' L_j') / temperature), the smallest j whose running
+ *     sum w_0 + .. + w_j exceeds u * sum(w).  margin = distance of u to the nearer
+ *     end of the chosen interval, in probability units (the ends 0 and 1 do not
+ *     count; +inf when neither end counts).
+ * path = ids[q, t, j] and path_score = L[t-1][i][j].  A request with a candidate
+ * id outside [0, V) gets path -1, score NaN, margin NaN and sets bit 1 of *status.
+ */
+int df2o_lattice_walk(const float* lattice, const int32_t* ids, int32_t R, int32_t Bsz, int32_t K,
+                      int64_t V, const float* uniforms, double temperature, int32_t* path,
+                      float* path_score, double* margin, int32_t* status)
+{
+    if (R < 0 || Bsz < 2 || K < 1 || V < 1) return DF2O_INVALID;
+    if (uniforms && !(temperature > 0.0)) return DF2O_INVALID;
+    const int64_t T = Bsz - 1;
+    const int64_t KK = (int64_t)K * K;
+    int32_t bad = 0;
+    int failed = 0;
+    int32_t q;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (q = 0; q < R; ++q) {
+        int valid = 1;
+        for (int64_t t = 1; t < Bsz && valid; ++t)
+            for (int32_t j = 0; j < K; ++j) {
+                int32_t b = ids[((int64_t)q * Bsz + t) * K + j];
+                if (b < 0 || b >= V) valid = 0;
+            }
+        if (!valid) {
+            for (int64_t t = 0; t < T; ++t) {
+                path[q * T + t] = -1;
+                path_score[q * T + t] = NAN;
+                if (margin) margin[q * T + t] = NAN;
+            }
+            bad |= 1;
+            continue;
+        }
+        double* w = uniforms ? (double*)malloc((size_t)K * sizeof(double)) : NULL;
+        if (uniforms && !w) {
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        int32_t i = 0;
+        for (int64_t t = 1; t < Bsz; ++t) {
+            const int32_t* cand = ids + ((int64_t)q * Bsz + t) * K;
+            const float* Lrow = lattice + ((int64_t)q * T + (t - 1)) * KK + (int64_t)i * K;
+            int32_t pick = -1;
+            double mg;
+            if (!uniforms) {
+                float best = -INFINITY, second = -INFINITY;
+                for (int32_t j = 0; j < K; ++j) {
+                    float s = Lrow[j];
+                    if (pick < 0 || s > best || (s == best && cand[j] < cand[pick])) {
+                        if (pick >= 0) second = best;
+                        best = s;
+                        pick = j;
+                    } else if (second < s) {
+                        second = s;
+                    }
+                }
+                mg = (K > 1) ? (double)best - (double)second : INFINITY;
+            } else {
+                double mx = -INFINITY, total = 0.0;
+                for (int32_t j = 0; j < K; ++j)
+                    if ((double)Lrow[j] > mx) mx = (double)Lrow[j];
+                for (int32_t j = 0; j < K; ++j) {
+                    w[j] = exp(((double)Lrow[j] - mx) / temperature);
+                    total += w[j];
+                }
+                const double u = (double)uniforms[q * T + (t - 1)];
+                double below = 0.0;  /* running sum of the weights before j */
+                for (int32_t j = 0; j < K; ++j) {
+                    if (below + w[j] > u * total) {
+                        pick = j;
+                        break;
+                    }
+                    below += w[j];
+                }
+                if (pick < 0) /* u * total rounded up to the full sum: the last nonzero weight */
+                    for (int32_t j = K - 1; j >= 0 && pick < 0; --j)
+                        if (w[j] > 0.0) pick = j;
+                double lo = 0.0;
+                for (int32_t j = 0; j < pick; ++j) lo += w[j];
+                const double hi = lo + w[pick];
+                mg = INFINITY;
+                if (pick > 0) mg = u - lo / total;
+                if (pick < K - 1 && hi / total - u < mg) mg = hi / total - u;
+            }
+            path[q * T + (t - 1)] = cand[pick];
+            path_score[q * T + (t - 1)] = Lrow[pick];
+            if (margin) margin[q * T + (t - 1)] = mg;
+            i = pick;
+        }
+        free(w);
+    }
+    if (status) *status = bad;
+    return failed ? DF2O_NOMEM : DF2O_OK;
 }
 
 /* ---------------------------------------------------------------- conv -- */

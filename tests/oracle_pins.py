@@ -298,6 +298,184 @@ def pin_walk_rejects_bad_ids(o):
     assert st == 1 and np.all(np.isnan(s[5])) and not np.any(np.isnan(np.delete(s, 5, axis=0)))
 
 
+# --------------------------------------------------------- lattice (next 1-2) --
+
+def pin_lattice_golden(o):
+    """Hand-worked table for the walk_r1_k2 inputs (tests/golden/lattice_r1_k2.json)."""
+    want = _golden("lattice_r1_k2.json")
+    g = _golden(want["inputs"])
+    ids = np.asarray(g["ids"], np.int32)
+    lat, status = o.lattice(np.asarray([g["anchor"]], np.int32), ids, np.asarray(g["vals"], np.float32),
+                            np.asarray(g["G"], np.float32), bf(g["A"]), bf(g["Bc"]), g["block"])
+    assert status == 0
+    exp = np.asarray([[[np.nan if v is None else v for v in row] for row in slot] for slot in want["lattice"]],
+                     np.float64)
+    assert np.array_equal(np.isnan(lat[0]), np.isnan(exp))
+    assert np.array_equal(np.nan_to_num(lat[0]), np.nan_to_num(exp))
+    path, score, _, _ = o.lattice_walk(lat, ids, g["block"], g["V"])
+    assert path[0].tolist() == want["greedy_path"] and score[0].tolist() == want["greedy_score"]
+
+
+def pin_lattice_tie_lower_id(o):
+    """The hand-worked tie case (walk_tie.json) walked over its table: equal scores go
+    to the lower token id and report a zero margin."""
+    g = _golden("walk_tie.json")
+    ids = np.asarray(g["ids"], np.int32)
+    lat, _ = o.lattice(np.asarray([g["anchor"]], np.int32), ids, np.asarray(g["vals"], np.float32),
+                       np.asarray(g["G"], np.float32), bf(g["A"]), bf(g["Bc"]), g["block"])
+    path, score, margin, _ = o.lattice_walk(lat, ids, g["block"], g["V"])
+    assert path[0].tolist() == g["path"] and score[0].tolist() == g["path_score"]
+    assert margin[0].tolist() == g["margin"]
+
+
+def pin_lattice_greedy_is_the_walk(o):
+    """'Greedy follows the best successor' over the precomputed table: the greedy
+    lattice walk gives the sequential walk's path, scores and margins exactly."""
+    R, B, K, V, r = 5, 7, 6, 90, 10
+    anchors, ids, vals, G, A, Bc = _random_lattice("lat_greedy", R, B, K, V, r)
+    vals[4, 1] = vals[4, 0]  # exact unary tie somewhere
+    lat, st = o.lattice(anchors, ids, vals, G, A, Bc, B)
+    p1, s1, m1, _ = o.selector_walk(anchors, ids, vals, G, A, Bc, B)
+    p2, s2, m2, st2 = o.lattice_walk(lat, ids, B, V)
+    assert st == 0 and st2 == 0
+    assert np.array_equal(p1, p2) and np.array_equal(s1, s2) and np.array_equal(m1, m2)
+
+
+def pin_lattice_rows_are_teacher_forced(o):
+    """Row i of slot t-1 scores position t's candidates after predecessor
+    ids[t-1, i]: the teacher-forced scorer with that predecessor gives the same row."""
+    R, B, K, V, r = 3, 5, 4, 50, 8
+    anchors, ids, vals, G, A, Bc = _random_lattice("lat_rows", R, B, K, V, r)
+    lat, _ = o.lattice(anchors, ids, vals, G, A, Bc, B)
+    for i in range(K):
+        pred = np.empty(R * B, np.int32)
+        for q in range(R):
+            pred[q * B] = anchors[q]
+            pred[q * B + 1] = anchors[q]
+            for t in range(2, B):
+                pred[q * B + t] = ids[q * B + t - 1, i]
+        sc, _ = o.pair_scores(pred, ids, vals, G, A, Bc)
+        sc = sc.reshape(R, B, K)
+        for q in range(R):
+            if i == 0:
+                assert np.array_equal(lat[q, 0, 0], sc[q, 1])
+            else:
+                assert np.all(np.isnan(lat[q, 0, i]))
+            for t in range(2, B):
+                assert np.array_equal(lat[q, t - 1, i], sc[q, t])
+
+
+def pin_lattice_unit_codebooks_closed_form(o):
+    """A = B = 1 makes every row of slot t-1 equal U_t(b) + sum_i G_t[i] (exact with
+    small integers), whatever the predecessor."""
+    rng = _rng("lat_ones")
+    R, B, K, V, r = 2, 4, 3, 25, 5
+    anchors, ids, _, _, _, _ = _random_lattice("lat_ones", R, B, K, V, r)
+    vals = rng.integers(-6, 7, size=(R * B, K)).astype(np.float32)
+    G = rng.integers(-3, 4, size=(R * B, r)).astype(np.float32)
+    one = bf(np.ones((V, r)))
+    lat, _ = o.lattice(anchors, ids, vals, G, one, one, B)
+    want = (vals + G.sum(axis=1, keepdims=True)).reshape(R, B, K)
+    for q in range(R):
+        assert np.array_equal(lat[q, 0, 0], want[q, 1])
+        for t in range(2, B):
+            for i in range(K):
+                assert np.array_equal(lat[q, t - 1, i], want[q, t])
+    # small integers tie often: the greedy table walk breaks them like the walk
+    p1, s1, _, _ = o.selector_walk(anchors, ids, vals, G, one, one, B)
+    p2, s2, _, _ = o.lattice_walk(lat, ids, B, V)
+    assert np.array_equal(p1, p2) and np.array_equal(s1, s2)
+
+
+def pin_lattice_rejects_bad_ids(o):
+    anchors, ids, vals, G, A, Bc = _random_lattice("lat_bad", 3, 4, 3, 20, 4)
+    ids = ids.copy()
+    ids[2 * 4 + 3, 1] = 20  # request 2, last row
+    lat, st = o.lattice(anchors, ids, vals, G, A, Bc, 4)
+    assert st == 1 and np.all(np.isnan(lat[2])) and not np.any(np.isnan(lat[:2, 1:]))
+    path, score, _, st2 = o.lattice_walk(lat, ids, 4, 20)
+    assert st2 == 1 and np.all(path[2] == -1) and np.all(np.isnan(score[2])) and np.all(path[:2] >= 0)
+
+
+def _sampling_fixture():
+    g = _golden("lattice_sampling.json")
+    lat = np.asarray(g["lattice"], np.float32)[None]
+    ids = np.asarray(g["ids"], np.int32)
+    return g, lat, ids
+
+
+def pin_sampling_golden(o):
+    """Hand-worked draws (tests/golden/lattice_sampling.json), including one where
+    the sampled column, not the greedy one, selects the next row."""
+    g, lat, ids = _sampling_fixture()
+    for case in g["cases"]:
+        u = np.asarray([case["u"]], np.float32)
+        path, score, _, st = o.lattice_walk(lat, ids, g["block"], g["V"], uniforms=u,
+                                            temperature=1.0 / math.log(2.0))
+        assert st == 0
+        assert path[0].tolist() == case["path"], case["work"]
+        assert score[0].tolist() == case["score"]
+
+
+def pin_sampling_two_candidates_closed_form(o):
+    """K = 2: column 0 is drawn exactly when u < sigmoid((S_0 - S_1) / temperature),
+    and the margin is the distance of u to that boundary."""
+    rng = _rng("samp2")
+    R, B, K = 400, 2, 2
+    lat = np.full((R, 1, K, K), np.nan, np.float32)
+    lat[:, 0, 0, :] = rng.standard_normal((R, K)).astype(np.float32) * 2
+    ids = np.tile(np.asarray([[0, 0], [3, 5]], np.int32), (R, 1))
+    u = rng.random((R, 1)).astype(np.float32)
+    tau = 0.7
+    path, score, margin, _ = o.lattice_walk(lat, ids, B, 8, uniforms=u, temperature=tau)
+    for q in range(R):
+        s0, s1 = float(lat[q, 0, 0, 0]), float(lat[q, 0, 0, 1])
+        p0 = 1.0 / (1.0 + math.exp(-(s0 - s1) / tau))
+        uq = float(u[q, 0])
+        if abs(uq - p0) < 1e-12:
+            continue
+        assert path[q, 0] == (3 if uq < p0 else 5)
+        assert abs(margin[q, 0] - abs(uq - p0)) < 1e-12
+
+
+def pin_sampling_frequencies(o):
+    """Draws with independent uniforms follow softmax(S / temperature): the count of
+    every column stays within 5 binomial standard deviations of n * p_j."""
+    rng = _rng("sampfreq")
+    n, K = 20000, 5
+    row = np.asarray([1.0, -0.5, 2.0, 0.25, 1.5], np.float32)
+    tau = 1.3
+    lat = np.broadcast_to(row, (n, 1, K, K)).astype(np.float32).copy()
+    ids = np.tile(np.asarray([[0] * K, [10, 11, 12, 13, 14]], np.int32), (n, 1))
+    u = rng.random((n, 1)).astype(np.float32)
+    path, _, _, _ = o.lattice_walk(lat, ids, 2, 20, uniforms=u, temperature=tau)
+    w = np.exp((row.astype(np.float64) - row.max()) / tau)
+    p = w / w.sum()
+    counts = np.bincount(path[:, 0] - 10, minlength=K)
+    assert np.all(np.abs(counts - n * p) <= 5 * np.sqrt(n * p * (1 - p))), (counts, n * p)
+
+
+def pin_sampling_cold_is_greedy(o):
+    """As the temperature goes to zero the draw becomes the greedy pick: with every
+    score gap >= 0.1 and temperature 1e-3, any u in [0.01, 0.99] gives the greedy path."""
+    rng = _rng("cold")
+    R, B, K, V, r = 6, 6, 5, 70, 8
+    anchors, ids, vals, G, A, Bc = _random_lattice("cold", R, B, K, V, r)
+    lat, _ = o.lattice(anchors, ids, vals, G, A, Bc, B)
+    for q in range(R):  # keep each used row's order but space its scores 0.1 apart
+        for t in range(B - 1):
+            for i in range(K):
+                row = lat[q, t, i]
+                if np.isnan(row[0]):
+                    continue
+                order = np.argsort(-row, kind="stable")
+                row[order] = row[order[0]] - np.float32(0.1) * np.arange(K, dtype=np.float32)
+    gp, gs, _, _ = o.lattice_walk(lat, ids, B, V)
+    u = rng.uniform(0.01, 0.99, size=(R, B - 1)).astype(np.float32)
+    sp, ss, _, _ = o.lattice_walk(lat, ids, B, V, uniforms=u, temperature=1e-3)
+    assert np.array_equal(gp, sp) and np.array_equal(gs, ss)
+
+
 # ---------------------------------------------------------------- conv (o5) --
 
 def pin_conv_golden(o):

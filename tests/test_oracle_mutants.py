@@ -52,6 +52,23 @@ MUTANTS = [
      "(float)d[((int64_t)1 * taps + j) * G + gi];", "(float)d[((int64_t)0 * taps + j) * G + gi];"),
     ("bf16_double_rounding", "    if (lo == 0x8000u) {", "    if (0) {"),
     ("conv_no_validation", "P % Bsz == 0;", "1;"),
+    ("lattice_predecessor_from_same_row",
+     "a = ids[(row - 1) * K + i];", "a = ids[row * K + i];"),
+    ("lattice_first_slot_reads_anchor_row",
+     "a = anchors[q];\n                } else {", "a = ids[(row - 1) * K];\n                } else {"),
+    ("lattice_gate_from_previous_row",
+     "ids[row * K + j], G + row * r", "ids[row * K + j], G + (row - 1) * r"),
+    ("lattice_walk_no_feedback", "            i = pick;", "            i = 0;"),
+    ("lattice_walk_tie_toward_higher_id",
+     "(s == best && cand[j] < cand[pick])", "(s == best && cand[j] > cand[pick])"),
+    ("lattice_walk_margin_unflagged_ties",
+     "} else if (second < s) {", "} else if (second < s && s < best) {"),
+    ("sampling_ignores_temperature",
+     "w[j] = exp(((double)Lrow[j] - mx) / temperature);", "w[j] = exp(((double)Lrow[j] - mx));"),
+    ("sampling_reflected_uniform",
+     "if (below + w[j] > u * total) {", "if (below + w[j] > (1.0 - u) * total) {"),
+    ("sampling_margin_wrong_end",
+     "if (pick > 0) mg = u - lo / total;", "if (pick > 0) mg = u - hi / total;"),
 ]
 
 
