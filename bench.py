@@ -108,6 +108,51 @@ def conv_bytes(w, which):
     return P * C * act * 2 + P * w.taps * G * 4 + 2 * w.taps * C * 4  # finish
 
 
+def lattice_bytes(w):
+    """Algorithmic bytes of selector_lattice: per request the anchor's A row and the K
+    predecessor candidates' A rows of every slot after the first, the K successor
+    B rows of every slot, G and the unary values of the drafted rows, and the table
+    written."""
+    T = w.B - 1
+    rows = w.R * ((1 + (T - 1) * w.K) + T * w.K)
+    return (rows * w.r * 2 + w.R * T * (w.r * 4 + w.K * 8) + w.R * T * w.K * w.K * 4)
+
+
+def lattice_flops(w):
+    T = w.B - 1
+    return 2.0 * w.R * (w.K + (T - 1) * w.K * w.K) * w.r
+
+
+def time_next_rows(step, torch, df2, iters=20):
+    """Per-call times of the lattice schedule on the step's own candidates: the table,
+    then the greedy and the sampling walk over it (not part of the timed step)."""
+    w = step.w
+    lat = torch.empty((w.R, w.B - 1, w.K, w.K), dtype=torch.float32, device=step.ids.device)
+    gen = torch.Generator(device=step.ids.device)
+    gen.manual_seed(w.seed)
+    u = torch.rand((w.R, w.B - 1), generator=gen, device=step.ids.device)
+    path = torch.empty((w.R, w.B - 1), dtype=torch.int32, device=step.ids.device)
+    sc = torch.empty((w.R, w.B - 1), dtype=torch.float32, device=step.ids.device)
+    calls = [
+        lambda: df2.selector_lattice(step.anchors, step.ids, step.vals, step.Gt, step.A, step.Bc, w.B, out=lat),
+        lambda: df2.lattice_walk(lat, step.ids, w.B, w.V, out=(path, sc)),
+        lambda: df2.lattice_walk(lat, step.ids, w.B, w.V, uniforms=u, temperature=1.0, out=(path, sc)),
+    ]
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    out = []
+    for c in calls:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(iters):
+            c()
+        ev[1].record()
+        torch.cuda.synchronize()
+        out.append(ev[0].elapsed_time(ev[1]) / iters * 1e3)
+    return out
+
+
 def config_of(w):
     return {"workload": f"{w.name}: V={w.V} D={w.D} r={w.r} K={w.K} block={w.B} requests={w.R} "
                         f"(P={w.P} positions) conv taps={w.taps} group={w.g}",
@@ -312,6 +357,7 @@ def gpu_arm(args, w, rank, world, torch):
         flush_ms = fe[0].elapsed_time(fe[1]) / 5 * args.steps
     step_ms = slowest_rank_ms((total_ms - flush_ms) / args.steps, dist, device)
     per_call_us = (per_call / args.steps * 1e3).tolist()
+    next_us = time_next_rows(step, torch, df2)
 
     # ---- end to end through the public API with host buffers
     pinned_in = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v))
@@ -390,6 +436,14 @@ def gpu_arm(args, w, rank, world, torch):
             "conv_gbs": {"prepare": conv_bytes(w, "prepare") / (per_call_us[0] * 1e-6) / 1e9,
                          "finish": conv_bytes(w, "finish") / (per_call_us[1] * 1e-6) / 1e9},
             "roofline": roof,
+            "next_rows": {
+                "note": "the lattice schedule, timed on the step's candidates outside the timed step",
+                "selector_lattice_us": next_us[0],
+                "lattice_walk_greedy_us": next_us[1],
+                "lattice_walk_sampling_us": next_us[2],
+                "lattice_gbs": lattice_bytes(w) / (next_us[0] * 1e-6) / 1e9,
+                "lattice_tflops": lattice_flops(w) / (next_us[0] * 1e-6) / 1e12,
+            },
             "e2e": {"value": job_throughput(w.P, world, e2e_ms), "unit": "positions/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": timed_launches,

@@ -183,6 +183,60 @@ def selector_pair_scores(pred, topk_ids, topk_vals, G, A, Bc, *, dev_status=None
     return scores
 
 
+def selector_lattice(anchors, topk_ids, topk_vals, G, A, Bc, block_size, *, dev_status=None,
+                     out=None, stream=None):
+    """Every adjacent candidate pair scored at once: lattice [R, B-1, K, K] f32."""
+    _need(anchors, "anchors", torch.int32, 1)
+    _need(topk_ids, "topk_ids", torch.int32)
+    _need(topk_vals, "topk_vals", torch.float32)
+    _need(G, "G", torch.float32)
+    _need(A, "A", torch.bfloat16, 2)
+    _need(Bc, "Bc", torch.bfloat16, 2)
+    R = anchors.shape[0]
+    B = int(block_size)
+    K = topk_ids.shape[-1]
+    V, r = A.shape
+    if topk_ids.numel() != R * B * K or topk_vals.numel() != R * B * K or G.numel() != R * B * r:
+        raise ValueError("candidate / gate shapes do not match [R*B, K] / [R*B, r]")
+    if tuple(Bc.shape) != (V, r):
+        raise ValueError("Bc must be [V, r] like A")
+    lat = out if out is not None else torch.empty((R, B - 1, K, K), dtype=torch.float32,
+                                                  device=anchors.device)
+    _need(lat, "lattice", torch.float32)
+    if lat.numel() != R * (B - 1) * K * K:
+        raise ValueError("lattice must hold [R, B-1, K, K]")
+    rc = lib().dflash2_selector_lattice(_p(anchors), R, B, _p(topk_ids), _p(topk_vals), _p(G), _p(A),
+                                        _p(Bc), V, K, r, _p(lat), _p(dev_status), _stream(stream))
+    _check("dflash2_selector_lattice", rc)
+    return lat
+
+
+def lattice_walk(lattice, topk_ids, block_size, vocab_size, *, uniforms=None, temperature=1.0,
+                 dev_status=None, out=None, stream=None):
+    """Greedy (uniforms None) or sampling walk over a lattice.  Returns (path [R, B-1]
+    int32, path_scores [R, B-1] f32)."""
+    _need(lattice, "lattice", torch.float32, 4)
+    _need(topk_ids, "topk_ids", torch.int32)
+    R, T, K, K2 = lattice.shape
+    B = int(block_size)
+    if K2 != K or T != B - 1 or topk_ids.numel() != R * B * K:
+        raise ValueError("lattice must be [R, B-1, K, K] over topk_ids [R*B, K]")
+    if uniforms is not None:
+        _need(uniforms, "uniforms", torch.float32)
+        if uniforms.numel() != R * T:
+            raise ValueError("uniforms must be [R, B-1]")
+    if out is None:
+        path = torch.empty((R, T), dtype=torch.int32, device=lattice.device)
+        scores = torch.empty((R, T), dtype=torch.float32, device=lattice.device)
+    else:
+        path, scores = out
+    rc = lib().dflash2_lattice_walk(_p(lattice), _p(topk_ids), R, B, K, int(vocab_size), _p(uniforms),
+                                    float(temperature), _p(path), _p(scores), _p(dev_status),
+                                    _stream(stream))
+    _check("dflash2_lattice_walk", rc)
+    return path, scores
+
+
 def _act_dtype(x):
     if x.dtype == torch.bfloat16:
         return DF2_DTYPE_BF16

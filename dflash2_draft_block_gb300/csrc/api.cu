@@ -1,6 +1,7 @@
 // The C-ABI of libdflash2: argument validation, workspace sizing and dispatch.
 // Every rule checked here is stated beside the call in include/dflash2.h.
 #include <atomic>
+#include <cfloat>
 #include <cstring>
 
 #include "common.cuh"
@@ -176,6 +177,39 @@ DF2_API int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const i
     return from_cuda(df2::pair_scores_launch(pred, P, topk_ids, topk_vals, G, A, Bc, V, K, r,
                                              scores, dev_status,
                                              static_cast<cudaStream_t>(stream)));
+}
+
+// --------------------------------------------------------------- lattice --
+
+DF2_API int dflash2_selector_lattice(const int32_t* anchors, int R, int B, const int32_t* topk_ids,
+                                     const float* topk_vals, const float* G, const uint16_t* A,
+                                     const uint16_t* Bc, int64_t V, int K, int r, float* lattice,
+                                     int32_t* dev_status, void* stream) {
+    if (R < 0 || B < 2 || K > V) return DF2_ERR_INVALID_ARGUMENT;
+    int rc = check_selector(V, K, r);
+    if (rc != DF2_OK) return rc;
+    if (R == 0) return DF2_OK;
+    if (!anchors || !topk_ids || !topk_vals || !G || !A || !Bc || !lattice)
+        return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(G) || !aligned16(A) || !aligned16(Bc)) return DF2_ERR_UNSUPPORTED;
+    const int64_t tile = K <= 16 ? 16 : (K <= 32 ? 32 : 64);
+    const int64_t tiles = (K + tile - 1) / tile;
+    if (int64_t(R) * (B - 1) * tiles * tiles > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    return from_cuda(df2::lattice_launch(anchors, R, B, topk_ids, topk_vals, G, A, Bc, V, K, r, lattice,
+                                         dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+DF2_API int dflash2_lattice_walk(const float* lattice, const int32_t* topk_ids, int R, int B, int K,
+                                 int64_t V, const float* uniforms, float temperature, int32_t* path,
+                                 float* path_scores, int32_t* dev_status, void* stream) {
+    if (R < 0 || B < 2 || K < 1 || V < 1 || K > V) return DF2_ERR_INVALID_ARGUMENT;
+    if (K > DF2_MAX_TOPK || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (uniforms && !(temperature > 0.f && temperature <= FLT_MAX)) return DF2_ERR_INVALID_ARGUMENT;
+    if (R == 0) return DF2_OK;
+    if (!lattice || !topk_ids || !path || !path_scores) return DF2_ERR_INVALID_ARGUMENT;
+    return from_cuda(df2::lattice_walk_launch(lattice, topk_ids, R, B, K, V, uniforms, temperature, path,
+                                              path_scores, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 // ------------------------------------------------------------------ conv --

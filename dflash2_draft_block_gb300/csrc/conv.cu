@@ -186,8 +186,10 @@ __device__ __forceinline__ void cp_async4_c(void* smem_dst, const void* gmem_src
 // group, of its B x taps dynamic corrections) into its own shared-memory slots,
 // then waits for them: the whole block's loads are in flight at once without
 // holding registers.  A thread reads back only what it copied, so no barrier
-// is needed.  Shared memory per CTA: B x 256 x (16 + taps x 4) bytes.
+// is needed.  Shared memory per CTA: B x threads x (16 + taps x 4) bytes; long
+// blocks launch fewer threads per CTA so that several CTAs still fit on an SM.
 constexpr int kAsyncThreads = 256;
+constexpr size_t kAsyncSmemMax = 96 * 1024;
 
 template <typename T, int TAPS>
 __global__ void __launch_bounds__(kAsyncThreads)
@@ -196,22 +198,23 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
                         T* __restrict__ y) {
     constexpr int N = Vec<T>::N;
     extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t* xs = smem;                                                          // [B][256][16 B]
-    float* ds = reinterpret_cast<float*>(smem + size_t(B) * kAsyncThreads * 16);  // [B][TAPS][256]
+    const int nt = blockDim.x;
+    uint8_t* xs = smem;                                                // [B][nt][16 B]
+    float* ds = reinterpret_cast<float*>(smem + size_t(B) * nt * 16);  // [B][TAPS][nt]
     const int tid = threadIdx.x;
     const int64_t nb = blockIdx.x / strips;
     const int strip = int(blockIdx.x % strips);
-    const int c0 = (strip * kAsyncThreads + tid) * N;
+    const int c0 = (strip * nt + tid) * N;
     if (nb >= nblocks || c0 >= C) return;
     const bool shared_group = (g % N) == 0;
     const int grp0 = c0 / g;
     for (int t = 0; t < B; ++t) {
         const int64_t p = nb * B + t;
-        cp_async16_c(xs + (size_t(t) * kAsyncThreads + tid) * 16, x + p * C + c0);
+        cp_async16_c(xs + (size_t(t) * nt + tid) * 16, x + p * C + c0);
         if (shared_group) {
 #pragma unroll
             for (int j = 0; j < TAPS; ++j)
-                cp_async4_c(ds + (size_t(t) * TAPS + j) * kAsyncThreads + tid, dyn + p * dyn_ld + j * G + grp0);
+                cp_async4_c(ds + (size_t(t) * TAPS + j) * nt + tid, dyn + p * dyn_ld + j * G + grp0);
         }
     }
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
@@ -230,8 +233,7 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
         for (int j = TAPS - 1; j > 0; --j)
 #pragma unroll
             for (int e = 0; e < N; ++e) hist[j][e] = hist[j - 1][e];
-        Vec<T>::widen(*reinterpret_cast<const typename Vec<T>::Raw*>(xs + (size_t(t) * kAsyncThreads + tid) * 16),
-                      hist[0]);
+        Vec<T>::widen(*reinterpret_cast<const typename Vec<T>::Raw*>(xs + (size_t(t) * nt + tid) * 16), hist[0]);
         float acc[N];
 #pragma unroll
         for (int e = 0; e < N; ++e) acc[e] = 0.f;
@@ -239,7 +241,7 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
         for (int j = 0; j < TAPS; ++j) {
             if (j > t) break;
             if (shared_group) {
-                const float d = ds[(size_t(t) * TAPS + j) * kAsyncThreads + tid];
+                const float d = ds[(size_t(t) * TAPS + j) * nt + tid];
 #pragma unroll
                 for (int e = 0; e < N; ++e) acc[e] = fmaf(kb[j][e] + d, hist[j][e], acc[e]);
             } else {
@@ -299,9 +301,12 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
         note_launch();
         return cudaGetLastError();
     }
-    const size_t async_smem = size_t(B) * kAsyncThreads * (16 + size_t(taps) * 4);
-    if (taps <= 4 && async_smem <= 96 * 1024) {
-        const int strips = (C / Vec<T>::N + kAsyncThreads - 1) / kAsyncThreads;
+    int nt = kAsyncThreads;
+    const size_t slot = size_t(B) * (16 + size_t(taps) * 4);  // bytes per thread
+    while (nt > 64 && slot * nt > kAsyncSmemMax) nt /= 2;
+    const size_t async_smem = slot * nt;
+    if (taps <= 4 && async_smem <= kAsyncSmemMax) {
+        const int strips = (C / Vec<T>::N + nt - 1) / nt;
         const unsigned agrid = unsigned(nblocks * strips);
         cudaError_t e = cudaSuccess;
 #define DF2_CONVA(TP)                                                                                       \
@@ -309,7 +314,7 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
         e = cudaFuncSetAttribute(conv_apply_async_kernel<T, TP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  int(async_smem));                                                         \
         if (e != cudaSuccess) return e;                                                                    \
-        conv_apply_async_kernel<T, TP><<<agrid, kAsyncThreads, async_smem, stream>>>(                       \
+        conv_apply_async_kernel<T, TP><<<agrid, nt, async_smem, stream>>>(                                  \
             x, nblocks, C, B, g, G, strips, base, dyn, dyn_ld, y);                                         \
     } while (0)
         switch (taps) {

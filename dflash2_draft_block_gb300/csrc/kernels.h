@@ -55,6 +55,14 @@ cudaError_t pair_scores_launch(const int32_t* pred, int64_t P, const int32_t* id
                                const uint16_t* Bc, int64_t V, int K, int r, float* scores,
                                int32_t* dev_status, cudaStream_t stream);
 
+// ---- lattice: L[q][t-1][i][j] = S_t(i-th predecessor, j-th candidate), then a walk over it
+cudaError_t lattice_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,
+                           const float* G, const uint16_t* A, const uint16_t* Bc, int64_t V, int K,
+                           int r, float* lattice, int32_t* dev_status, cudaStream_t stream);
+cudaError_t lattice_walk_launch(const float* lattice, const int32_t* ids, int R, int B, int K, int64_t V,
+                                const float* uniforms, float temperature, int32_t* path,
+                                float* path_scores, int32_t* dev_status, cudaStream_t stream);
+
 // ---- conv: y = sum_{j<taps, t-j>=0} (base[j] + dyn[p, j, c/g]) * x[p-j]
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
                               const float* base_io, const float* dyn, int64_t dyn_ld, void* y,

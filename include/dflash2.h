@@ -7,6 +7,8 @@
  *                                 the per-position top-K, and the hidden projection H
  *   dflash2_selector_walk         the candidate selector's greedy walk
  *   dflash2_selector_pair_scores  the selector scores with teacher-forced predecessors
+ *   dflash2_selector_lattice      every adjacent candidate pair scored at once
+ *   dflash2_lattice_walk          the greedy or sampling walk over that table
  *   dflash2_conv_prepare          the grouped dynamic causal conv before a sublayer
  *   dflash2_conv_finish           the same conv after the sublayer
  *
@@ -19,7 +21,8 @@
  *           "What DFlash2 adds" (conv and selector equations), "Two deltas over the
  *           upstream inference implementation", "Selector training objective".
  *   [KB]    "DFlash 2 Explanation": "Component Breakdown", "Draft-Verify Cycle",
- *           "Problem 1" (pair score), "Problem 2" (two-tap conv).
+ *           "Problem 1" (pair score; all pairs scored in one pass, then a greedy or
+ *           sampling walk over the scores), "Problem 2" (two-tap conv).
  *
  * Conventions shared by every call
  * ---------------------------------
@@ -191,6 +194,69 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
                                  const float* topk_vals, const float* G, const uint16_t* A,
                                  const uint16_t* Bc, int64_t V, int K, int r, float* scores,
                                  int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_selector_lattice — every adjacent candidate pair scored at once.
+ *
+ * [KB] "How It Works", Problem 1: all pairs of adjacent candidates are scored in
+ * one parallel pass, and only the final walk over those scores is sequential.
+ * For request q and drafted position t = 1 .. B-1 (table slot t-1), row = q*B + t:
+ *   lattice[q, t-1, i, j] = topk_vals[row, j]
+ *                         + sum_k A[a_i, k] * G[row, k] * Bc[topk_ids[row, j], k]
+ * where a_i = topk_ids[row - 1, i] (the i-th candidate of position t-1) for t >= 2,
+ * and for t = 1 the predecessor is the anchor alone: row i = 0 of slot 0 holds
+ * S_1(anchors[q], .) and rows 1 .. K-1 of slot 0 are NaN.
+ *
+ *   anchors     [R]               int32   device
+ *   topk_ids    [R*B, K]          int32   candidates (as written by dflash2_unary_topk)
+ *   topk_vals   [R*B, K]          fp32    their unary logits
+ *   G           [R*B, r]          fp32    H(h_t)
+ *   A, Bc       [V, r]            bf16    predecessor / successor codebooks
+ *   lattice     [R, B-1, K, K]    fp32    out (caller-allocated, fully written)
+ * Rules: as dflash2_selector_walk; G, A, Bc 16-byte aligned; r % 8 == 0;
+ * R * (B-1) * ceil(K/64)^2 (K > 32), ceil(K/32)^2 (16 < K <= 32) or 1 (K <= 16)
+ * below 2^31 (else DF2_ERR_UNSUPPORTED).  An anchor or candidate id outside
+ * [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and writes NaN over that request's table.
+ * Scores are fp32 sums of exact bf16 x fp32 products, summed in a different order
+ * than dflash2_selector_walk's, so the two agree to fp32 rounding.
+ * ---------------------------------------------------------------------- */
+int dflash2_selector_lattice(const int32_t* anchors, int R, int B, const int32_t* topk_ids,
+                             const float* topk_vals, const float* G, const uint16_t* A,
+                             const uint16_t* Bc, int64_t V, int K, int r, float* lattice,
+                             int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_lattice_walk — the walk over a finished lattice.
+ *
+ * [KB] "How It Works", Problem 1: greedy follows the best successor; sampling
+ * draws from the same scores.  Per request q the state is the row i of the
+ * current predecessor (i = 0, the anchor, at t = 1); step t reads row i of slot
+ * t-1 and picks a column j, which becomes the next row:
+ *   uniforms == NULL (greedy): the largest score, equal scores to the lower token id
+ *     (the same path as dflash2_selector_walk up to fp32 rounding of the scores);
+ *   uniforms != NULL (sampling): a draw from softmax(lattice[q, t-1, i, :] / temperature)
+ *     by the inverse CDF in candidate-list order with u = uniforms[q, t-1]: the
+ *     smallest j whose running sum w_0 + .. + w_j exceeds u * sum(w), with
+ *     w_j = exp((S_j - max S) / temperature); if rounding leaves no such j, the
+ *     last j with w_j > 0.  The pages name neither the scheme nor the
+ *     temperature: the caller supplies both, and the uniforms, so the draw is
+ *     reproducible.
+ *   path[q, t-1] = topk_ids[q*B + t, j];  path_scores[q, t-1] = lattice[q, t-1, i, j].
+ *
+ *   lattice     [R, B-1, K, K]  fp32   (as written by dflash2_selector_lattice)
+ *   topk_ids    [R*B, K]        int32  rows t = 0 are not read
+ *   uniforms    [R, B-1]        fp32   in [0, 1), nullable
+ *   temperature                 host float, > 0 and finite when uniforms is given
+ *   path        [R, B-1]        int32  out
+ *   path_scores [R, B-1]        fp32   out
+ * Rules: R >= 0, B >= 2, 1 <= K <= min(V, DF2_MAX_TOPK).  A candidate id outside
+ * [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and writes -1 / NaN over that request's
+ * path.  The sampling draw computes its weights and running sums in fp32, so a u
+ * that lies within rounding of an interval end may pick the neighbouring column.
+ * ---------------------------------------------------------------------- */
+int dflash2_lattice_walk(const float* lattice, const int32_t* topk_ids, int R, int B, int K,
+                         int64_t V, const float* uniforms, float temperature, int32_t* path,
+                         float* path_scores, int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * dflash2_conv_prepare — grouped dynamic causal conv before a sublayer.

@@ -69,6 +69,22 @@ def test_selector_validation(lib):
     assert w(fake, 2, 8, fake, fake, fake, fake, fake, 100, 101, 32, fake, fake, None, None) == 1  # K > V
     assert w(fake, 2, 8, fake, fake, fake, fake, fake, 100, 4, 12, fake, fake, None, None) == 2  # r % 8
     assert w(fake, 0, 8, fake, fake, fake, fake, fake, 100, 4, 32, fake, fake, None, None) == 0
+    lt = lib.dflash2_selector_lattice
+    assert lt(fake, 2, 1, fake, fake, fake, fake, fake, 100, 4, 32, fake, None, None) == 1  # B < 2
+    assert lt(fake, 2, 8, fake, fake, fake, fake, fake, 100, 101, 32, fake, None, None) == 1  # K > V
+    assert lt(fake, 2, 8, fake, fake, fake, fake, fake, 100, 4, 12, fake, None, None) == 2  # r % 8
+    assert lt(fake, 2, 8, fake, fake, fake, fake, fake, 5000, 2000, 32, fake, None, None) == 2  # K cap
+    assert lt(fake, 0, 8, fake, fake, fake, fake, fake, 100, 4, 32, fake, None, None) == 0
+    # more CTAs than one launch can address
+    assert lt(fake, 1 << 24, 8, fake, fake, fake, fake, fake, 5000, 1024, 32, fake, None, None) == 2
+    lw = lib.dflash2_lattice_walk
+    assert lw(fake, fake, 2, 1, 4, 100, None, 1.0, fake, fake, None, None) == 1  # B < 2
+    assert lw(fake, fake, 2, 8, 0, 100, None, 1.0, fake, fake, None, None) == 1  # K < 1
+    assert lw(fake, fake, 2, 8, 4, 100, fake, 0.0, fake, fake, None, None) == 1  # temperature 0
+    assert lw(fake, fake, 2, 8, 4, 100, fake, -1.0, fake, fake, None, None) == 1
+    assert lw(fake, fake, 2, 8, 4, 100, fake, float("inf"), fake, fake, None, None) == 1
+    assert lw(fake, fake, 2, 8, 4, 100, fake, float("nan"), fake, fake, None, None) == 1
+    assert lw(fake, fake, 0, 8, 4, 100, fake, 0.5, fake, fake, None, None) == 0
     ps = lib.dflash2_selector_pair_scores
     assert ps(fake, -1, fake, fake, fake, fake, fake, 100, 4, 32, fake, None, None) == 1
     assert ps(fake, 4, fake, fake, fake, fake, fake, 100, 0, 32, fake, None, None) == 1
