@@ -100,6 +100,17 @@ def head_bytes(w):
     return (w.V * w.D * 2 + w.r * w.D * 2 + w.P * w.D * 2 + w.P * w.K * 8 + w.P * w.r * 4)
 
 
+def draft_bytes(w):
+    """Algorithmic bytes of the draft head: the head's, plus the walk's gathered rows
+    (per request the anchor's and every predecessor candidate's A row, every
+    candidate's B row) and the teacher-forced scores' (per row one A row and K B
+    rows), the path and the scores written."""
+    T = w.B - 1
+    walk = w.R * ((1 + (T - 1) * w.K) + T * w.K) * w.r * 2 + w.R * T * 8
+    pair = w.P * (1 + w.K) * w.r * 2 + w.P * w.K * 4
+    return head_bytes(w) + walk + pair
+
+
 def conv_bytes(w, which):
     C, P, G = w.C, w.P, w.G
     act = 2 if w.act == "bf16" else 4
@@ -121,6 +132,30 @@ def lattice_bytes(w):
 def lattice_flops(w):
     T = w.B - 1
     return 2.0 * w.R * (w.K + (T - 1) * w.K * w.K) * w.r
+
+
+def time_per_call(step, torch, n):
+    """Per-call breakdown from separate loops with an event between consecutive calls
+    (outside the timed region): the step's three calls, then the draft head's three
+    separate equivalents."""
+    out = []
+    for runner, ncalls in ((step.run, 3), (step.run_separate, 3)):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)] for _ in range(n)]
+        for s in range(n):
+            if runner is step.run:
+                runner(evs[s])
+            else:
+                step.run(None)
+                runner(evs[s])
+            if step.flush is not None:
+                step.flush.zero_()
+        torch.cuda.synchronize()
+        per_call = np.zeros(ncalls)
+        for s in range(n):
+            for i in range(ncalls):
+                per_call[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+        out += (per_call / n * 1e3).tolist()
+    return out
 
 
 def time_next_rows(step, torch, df2, iters=20):
@@ -257,6 +292,8 @@ class Step:
         self.y = torch.empty_like(self.x)
         self.y2 = torch.empty_like(self.z)
         self.dyn = e((P, w.taps, G), dtype=torch.float32, device=device)
+        self.ws_draft = e(max(1, df2.draft_head_workspace_size(w.R, w.B, w.D, w.V, K, r)), dtype=torch.uint8,
+                          device=device)
         self.ws_head = e(max(1, df2.unary_topk_workspace_size(P, w.D, w.V, K, r)), dtype=torch.uint8,
                          device=device)
         dt = df2.DF2_DTYPE_BF16 if w.act == "bf16" else df2.DF2_DTYPE_F32
@@ -267,23 +304,38 @@ class Step:
             self.flush = e(256 << 20, dtype=torch.uint8, device=device)
 
     def run(self, events=None):
+        """One step: conv_prepare, conv_finish, then the fused draft head (unary
+        top-K + H, greedy walk, teacher-forced scores).  events: None, four events
+        (one between consecutive calls), or a pair (recorded around the draft head)."""
         d, w = self.df2, self.w
-        ev = events or [None] * 6
+        ev = events or [None] * 4
+        if len(ev) == 2:
+            ev = [None, None, ev[0], ev[1]]
         self._rec(ev[0])
         d.conv_prepare(self.x, w.B, w.taps, w.g, self.W_proj, self.base, workspace=self.ws_conv,
                        out=(self.y, self.dyn))
         self._rec(ev[1])
         d.conv_finish(self.z, w.B, w.taps, w.g, self.dyn, self.base, out=self.y2)
         self._rec(ev[2])
+        d.draft_head(self.h, self.W_lm, w.K, self.W_H, self.A, self.Bc, self.anchors, w.B, self.pred,
+                     workspace=self.ws_draft,
+                     out=(self.ids, self.vals, self.Gt, self.path, self.pscore, self.scores))
+        self._rec(ev[3])
+
+    def run_separate(self, events):
+        """The draft head as its three separate calls, an event between each (for the
+        per-call breakdown)."""
+        d, w = self.df2, self.w
+        self._rec(events[0])
         d.unary_topk(self.h, self.W_lm, w.K, self.W_H, workspace=self.ws_head,
                      out=(self.ids, self.vals, self.Gt))
-        self._rec(ev[3])
+        self._rec(events[1])
         d.selector_walk(self.anchors, self.ids, self.vals, self.Gt, self.A, self.Bc, w.B,
                         out=(self.path, self.pscore))
-        self._rec(ev[4])
+        self._rec(events[2])
         d.selector_pair_scores(self.pred, self.ids, self.vals, self.Gt, self.A, self.Bc,
                                out=self.scores)
-        self._rec(ev[5])
+        self._rec(events[3])
 
     @staticmethod
     def _rec(e):
@@ -321,9 +373,10 @@ def gpu_arm(args, w, rank, world, torch):
     torch.cuda.synchronize()
     n_launch = count_launches(step, torch, df2)
 
-    # ---- device-resident timing (W warm-up done above), per-call events
-    nev = 6
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    # ---- device-resident timing (W warm-up done above).  Inside the timed region
+    # only the head call is bracketed by events (every event between kernels
+    # drains the launch pipeline, so more of them would inflate the step).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     flush_ms = 0.0
     if dist is not None:
@@ -342,10 +395,7 @@ def gpu_arm(args, w, rank, world, torch):
     if dist is not None:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    per_call = np.zeros(nev - 1)
-    for s in range(args.steps):
-        for i in range(nev - 1):
-            per_call[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+    head_us_live = sum(evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)) / args.steps * 1e3
     if step.flush is not None:
         # the flush runs between timed steps; its time is subtracted
         fe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -356,7 +406,7 @@ def gpu_arm(args, w, rank, world, torch):
         torch.cuda.synchronize()
         flush_ms = fe[0].elapsed_time(fe[1]) / 5 * args.steps
     step_ms = slowest_rank_ms((total_ms - flush_ms) / args.steps, dist, device)
-    per_call_us = (per_call / args.steps * 1e3).tolist()
+    per_call_us = time_per_call(step, torch, min(args.steps, 50))
     next_us = time_next_rows(step, torch, df2)
 
     # ---- end to end through the public API with host buffers
@@ -397,25 +447,29 @@ def gpu_arm(args, w, rank, world, torch):
     out = None
     if rank == 0:
         peaks, src = load_peaks()
-        hb = head_bytes(w)
-        head_us = per_call_us[2]
+        hb = draft_bytes(w)
+        head_us = head_us_live
         traffic, traffic_src = head_traffic(w.name)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        tail = ("draft_tail_kernel (fold, walk, teacher-forced scores)" if w.P <= sms
+                else "top-K merge, walk and teacher-forced kernels")
         if w.P <= 32:
             # few positions: the head streams the LM head from HBM
-            roof = {"kernel": "dflash2_unary_topk call (head_skinny_kernel + top-K merge)", "bound": "hbm",
+            roof = {"kernel": "dflash2_draft_head call: head_skinny_kernel + " + tail, "bound": "hbm",
                     "achieved": hb / (head_us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "algorithmic_bytes": hb}
         else:
             # many positions: the logits GEMM (plus G) is tensor-core bound
             flops = 2.0 * w.P * w.D * (w.V + w.r)
             pk = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-            roof = {"kernel": "dflash2_unary_topk call (gemm_wide_kernel top-K + G + merge)",
+            roof = {"kernel": "dflash2_draft_head call: gemm_wide_kernel (top-K, G) + " + tail,
                     "bound": "tensor", "achieved": flops / (head_us * 1e-6) / 1e12, "peak": pk,
                     "unit": "TFLOP/s", "algorithmic_flops": flops}
         roof["frac"] = roof["achieved"] / roof["peak"]
         roof["peak_source"] = src
         roof["traffic"] = traffic
         roof["traffic_source"] = traffic_src
+        roof["traffic_note"] = "DRAM bytes per launch of the head kernel (ncu); the other kernels of the call move < 1%"
         out = {
             "metric": METRIC,
             "value": job_throughput(w.P, world, step_ms),
@@ -431,8 +485,12 @@ def gpu_arm(args, w, rank, world, torch):
             "data": "synthetic (seeded; shapes and scales of the workload, no dataset or checkpoint)",
             "config": config_of(w),
             "drafted_positions_per_s": job_throughput(w.R * (w.B - 1), world, step_ms),
-            "per_call_us": dict(zip(["conv_prepare", "conv_finish", "unary_topk", "selector_walk",
-                                     "selector_pair_scores"], per_call_us)),
+            "per_call_us": dict(zip(["conv_prepare", "conv_finish", "draft_head", "unary_topk",
+                                     "selector_walk", "selector_pair_scores"], per_call_us)),
+            "per_call_note": "per_call_us from separate loops with events between calls (the last three "
+                             "are the draft head's separate equivalents); roofline.achieved from the "
+                             "draft head call's events inside the timed region",
+            "draft_head_us_timed": head_us_live,
             "conv_gbs": {"prepare": conv_bytes(w, "prepare") / (per_call_us[0] * 1e-6) / 1e9,
                          "finish": conv_bytes(w, "finish") / (per_call_us[1] * 1e-6) / 1e9},
             "roofline": roof,

@@ -183,6 +183,52 @@ def selector_pair_scores(pred, topk_ids, topk_vals, G, A, Bc, *, dev_status=None
     return scores
 
 
+def draft_head_workspace_size(R, B, D, V, K, r) -> int:
+    return int(lib().dflash2_draft_head_workspace_size(R, B, D, V, K, r))
+
+
+def draft_head(h, W_lm, K, W_H, A, Bc, anchors, block_size, pred=None, *, workspace=None,
+               dev_status=None, out=None, stream=None):
+    """Unary top-K, G = H(h), the greedy walk and (pred given) the teacher-forced
+    scores of one draft block in one call.  Returns (ids, vals, G, path, path_scores,
+    pair_scores or None)."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W_lm, "W_lm", torch.bfloat16, 2)
+    _need(W_H, "W_H", torch.bfloat16, 2)
+    _need(A, "A", torch.bfloat16, 2)
+    _need(Bc, "Bc", torch.bfloat16, 2)
+    _need(anchors, "anchors", torch.int32, 1)
+    P, D = h.shape
+    V = W_lm.shape[0]
+    r = W_H.shape[0]
+    R = anchors.shape[0]
+    B = int(block_size)
+    if P != R * B or W_lm.shape[1] != D or W_H.shape[1] != D:
+        raise ValueError("h must be [R*B, D] with W_lm [V, D], W_H [r, D]")
+    if tuple(A.shape) != (V, r) or tuple(Bc.shape) != (V, r):
+        raise ValueError("A and Bc must be [V, r]")
+    if pred is not None:
+        _need(pred, "pred", torch.int32, 1)
+        if pred.shape[0] != P:
+            raise ValueError("pred must be [R*B]")
+    dev = h.device
+    if out is None:
+        e = torch.empty
+        out = (e((P, K), dtype=torch.int32, device=dev), e((P, K), dtype=torch.float32, device=dev),
+               e((P, r), dtype=torch.float32, device=dev), e((R, B - 1), dtype=torch.int32, device=dev),
+               e((R, B - 1), dtype=torch.float32, device=dev),
+               e((P, K), dtype=torch.float32, device=dev) if pred is not None else None)
+    ids, vals, G, path, ps, pair = out
+    need = draft_head_workspace_size(R, B, D, V, K, r)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    rc = lib().dflash2_draft_head(_p(h), R, B, D, _p(W_lm), V, K, _p(W_H), r, _p(A), _p(Bc), _p(anchors),
+                                  _p(pred), _p(ids), _p(vals), _p(G), _p(path), _p(ps), _p(pair),
+                                  _p(workspace), workspace.numel(), _p(dev_status), _stream(stream))
+    _check("dflash2_draft_head", rc)
+    return ids, vals, G, path, ps, pair
+
+
 def selector_lattice(anchors, topk_ids, topk_vals, G, A, Bc, block_size, *, dev_status=None,
                      out=None, stream=None):
     """Every adjacent candidate pair scored at once: lattice [R, B-1, K, K] f32."""

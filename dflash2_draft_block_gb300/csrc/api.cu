@@ -135,6 +135,92 @@ DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const ui
     return DF2_OK;
 }
 
+// ------------------------------------------------------------ draft head --
+
+namespace {
+
+// The fused path: the head kernel leaves its sorted lists in the workspace and one
+// tail launch folds them, scores the teacher-forced pairs and walks each request.
+bool draft_fused(HeadPath path, int64_t P, int B, int64_t D, int64_t V, int K, int r, int sms) {
+    if (path == HeadPath::Simple) return false;
+    int S = 0;
+    if (path == HeadPath::Skinny) S = int(df2::head_tc_workspace(P, D, V, K, sms) / (size_t(P) * K * 8));
+    else S = int((df2::wide_topk_workspace(P, V, K, sms) - size_t(P) * 4) / (size_t(P) * K * 8));
+    return df2::draft_tail_supported(P, B, K, r, S, sms);
+}
+
+size_t draft_workspace(int64_t P, int R, int B, int64_t D, int64_t V, int K, int r, int sms) {
+    const HeadPath path = pick_head(P, D, V, K);
+    size_t n = round_up(head_workspace(path, P, D, V, K, sms), 256);
+    if (draft_fused(path, P, B, D, V, K, r, sms)) n += round_up(size_t(R) * 4, 256);  // tickets
+    return n;
+}
+
+}  // namespace
+
+DF2_API size_t dflash2_draft_head_workspace_size(int R, int B, int64_t D, int64_t V, int K, int r) {
+    if (R < 1 || B < 2) return 0;
+    const int64_t P = int64_t(R) * B;
+    if (check_head(P, D, V, K, r, true) != DF2_OK) return 0;
+    const int sms = num_sms_current();
+    if (sms <= 0) return 0;
+    return draft_workspace(P, R, B, D, V, K, r, sms);
+}
+
+DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const uint16_t* W_lm,
+                               int64_t V, int K, const uint16_t* W_H, int r, const uint16_t* A,
+                               const uint16_t* Bc, const int32_t* anchors, const int32_t* pred,
+                               int32_t* topk_ids, float* topk_vals, float* G, int32_t* path,
+                               float* path_scores, float* pair_scores, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (R < 0 || B < 2) return DF2_ERR_INVALID_ARGUMENT;
+    const int64_t P = int64_t(R) * B;
+    int rc = check_head(P, D, V, K, r, true);
+    if (rc != DF2_OK) return rc;
+    if (r > DF2_MAX_RANK || r % 8 != 0) return DF2_ERR_UNSUPPORTED;
+    if (R == 0) return DF2_OK;
+    if (!h || !W_lm || !W_H || !A || !Bc || !anchors || !topk_ids || !topk_vals || !G || !path ||
+        !path_scores || (pred && !pair_scores))
+        return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(h) || !aligned16(W_lm) || !aligned16(W_H) || !aligned16(A) || !aligned16(Bc) ||
+        !aligned16(topk_ids) || !aligned16(topk_vals) || !aligned16(G) || !aligned16(workspace))
+        return DF2_ERR_UNSUPPORTED;
+    const int sms = num_sms_current();
+    if (sms <= 0) return DF2_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const HeadPath hp = pick_head(P, D, V, K);
+    const size_t need = draft_workspace(P, R, B, D, V, K, r, sms);
+    if (workspace_bytes < need || !workspace) return DF2_ERR_WORKSPACE_TOO_SMALL;
+    if (!draft_fused(hp, P, B, D, V, K, r, sms)) {
+        // the separate calls, in order
+        rc = dflash2_unary_topk(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
+                                workspace_bytes, dev_status, stream);
+        if (rc != DF2_OK) return rc;
+        rc = dflash2_selector_walk(anchors, R, B, topk_ids, topk_vals, G, A, Bc, V, K, r, path,
+                                   path_scores, dev_status, stream);
+        if (rc != DF2_OK || !pred) return rc;
+        return dflash2_selector_pair_scores(pred, P, topk_ids, topk_vals, G, A, Bc, V, K, r,
+                                            pair_scores, dev_status, stream);
+    }
+    unsigned* tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) +
+                                                    round_up(head_workspace(hp, P, D, V, K, sms), 256));
+    df2::TopkParts parts{};
+    if (hp == HeadPath::Skinny) {
+        rc = df2::head_tc_launch(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
+                                 dev_status, sms, st, -1, &parts, tickets, R);
+        if (rc != DF2_OK) return rc;
+    } else {
+        cudaError_t e = df2::wide_topk_launch(h, P, W_lm, V, D, K, topk_ids, topk_vals, workspace,
+                                              dev_status, sms, st, &parts, tickets, R);
+        if (e != cudaSuccess) return DF2_ERR_CUDA;
+        e = df2::wide_store_launch(h, P, W_H, r, D, G, r, r, G, r, dev_status, st);
+        if (e != cudaSuccess) return DF2_ERR_CUDA;
+    }
+    return from_cuda(df2::draft_tail_launch(parts, P, K, topk_ids, topk_vals, anchors, B, G, A, Bc, V,
+                                            r, path, path_scores, pred, pair_scores, tickets,
+                                            dev_status, st));
+}
+
 // -------------------------------------------------------------- selector --
 
 namespace {

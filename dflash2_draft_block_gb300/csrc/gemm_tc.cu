@@ -57,6 +57,8 @@ struct WideArgs {
     int* part_id;
     unsigned* thr_g;        // [M] best K-th value so far over all ranges (ordered key), or null
     int32_t* dev_status;
+    unsigned* zero_words;   // [n_zero] zeroed by CTA 0 for the next kernel in the stream
+    int n_zero;
 };
 
 __host__ __device__ inline uint32_t wide_stage_bytes(int kbox, int bn) {
@@ -132,6 +134,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bid = int(blockIdx.x);
+    if (bid == 0)
+        for (int i = threadIdx.x; i < args.n_zero; i += blockDim.x) args.zero_words[i] = 0u;
     const int n_groups = (args.n_nt + args.tiles_per_cta - 1) / args.tiles_per_cta;
     const int mt = args.m_major ? bid / n_groups : bid % args.n_mt;
     const int grp = args.m_major ? bid % n_groups : bid / args.n_mt;
@@ -450,7 +454,7 @@ cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, i
 
 cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
                              int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, TopkParts* parts_out, unsigned* zero_words, int n_zero) {
     const int bn = wide_bn(EPI_TOPK, K);
     CUtensorMap ta, tb;
     if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, bn)) return cudaErrorInvalidValue;
@@ -469,11 +473,17 @@ cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, in
     a.part_id = reinterpret_cast<int*>(a.part_v + size_t(groups) * M * K);
     a.thr_g = reinterpret_cast<unsigned*>(a.part_id + size_t(groups) * M * K);
     a.dev_status = dev_status;
+    a.zero_words = zero_words;
+    a.n_zero = n_zero;
     cudaError_t e = cudaMemsetAsync(a.thr_g, 0, size_t(M) * 4, stream);
     if (e != cudaSuccess) return e;
     e = bn == 192 ? launch_wide<EPI_TOPK, 192>(ta, tb, a, a.n_mt * n_groups, stream)
                   : launch_wide<EPI_TOPK, 256>(ta, tb, a, a.n_mt * n_groups, stream);
     if (e != cudaSuccess) return e;
+    if (parts_out) {  // the caller folds the per-range lists itself
+        *parts_out = TopkParts{a.part_v, a.part_id, n_groups};
+        return cudaSuccess;
+    }
     return topk_merge_sorted_launch(a.part_v, a.part_id, n_groups, M, K, ids, vals, stream);
 }
 

@@ -74,7 +74,8 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_wh, int P, int D, int V, int K, int r,
                    int n_vtiles, int n_tiles, int nstages, int kbox, int pf_stages, int nacc,
                    float* __restrict__ part_v, int* __restrict__ part_id, float* __restrict__ G,
-                   int32_t* __restrict__ dev_status, int stall_stage) {
+                   int32_t* __restrict__ dev_status, int stall_stage, unsigned* __restrict__ zero_words,
+                   int n_zero) {
     // TMEM: two tile buffers (the epilogue drains one while the MMAs fill the
     // other), each holding nacc partial accumulators of N columns.  Successive
     // k-steps of a tile rotate over the partial accumulators, so consecutive MMAs
@@ -100,6 +101,9 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nbox = (D + BK - 1) / BK;            // 64-wide boxes along D
+    // counters the kernel after this one expects to start at zero
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0u;
     const int nk = (nbox + kbox - 1) / kbox;       // stages per tile
     const uint32_t h_box_bytes = uint32_t(N) * BK * 2;
 
@@ -395,7 +399,8 @@ size_t head_tc_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms) {
 
 int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V, int K,
                    const uint16_t* W_H, int r, float* G, int32_t* ids, float* vals, void* ws,
-                   int32_t* dev_status, int num_sms, cudaStream_t stream, int stall_stage) {
+                   int32_t* dev_status, int num_sms, cudaStream_t stream, int stall_stage,
+                   TopkParts* parts_out, unsigned* zero_words, int n_zero) {
     const Plan pl = pick_plan(P, K);
     const int N = pl.N;
     CUtensorMap tm_w, tm_h, tm_wh;
@@ -421,7 +426,8 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
         if (e != cudaSuccess) return DF2_ERR_CUDA;                                                \
         head_skinny_kernel<NV, RV><<<grid, kThreads, smem, stream>>>(                             \
             tm_w, tm_h, tm_wh, int(P), int(D), int(V), K, r, n_vtiles, n_tiles, pl.nstages,       \
-            pl.kbox, DF2_HEAD_PF, DF2_HEAD_NACC, part_v, part_id, G, dev_status, stall_stage);    \
+            pl.kbox, DF2_HEAD_PF, DF2_HEAD_NACC, part_v, part_id, G, dev_status, stall_stage,     \
+            zero_words, n_zero);                                                                  \
     } while (0)
     if (N == 16 && pl.R == 1) DF2_HEAD(16, 1);
     else if (N == 16) DF2_HEAD(16, 2);
@@ -429,6 +435,10 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
 #undef DF2_HEAD
     note_launch();
     if (cudaGetLastError() != cudaSuccess) return DF2_ERR_CUDA;
+    if (parts_out) {  // the caller folds the per-CTA lists itself
+        *parts_out = TopkParts{part_v, part_id, int(parts)};
+        return DF2_OK;
+    }
     e = topk_merge_sorted_launch(part_v, part_id, int(parts), P, K, ids, vals, stream);
     return e == cudaSuccess ? DF2_OK : DF2_ERR_CUDA;
 }

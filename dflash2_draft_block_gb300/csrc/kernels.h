@@ -19,6 +19,11 @@ cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, in
                               int32_t* ids, float* vals, cudaStream_t stream);
 
 // ---- S partial lists [S][P][K], each in rank order (id -1 = empty), K <= 64 -> top-K [P][K]
+struct TopkParts {
+    const float* v;
+    const int* id;
+    int S;
+};
 cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
                                      int32_t* ids, float* vals, cudaStream_t stream);
 
@@ -40,10 +45,13 @@ size_t wide_topk_workspace(int64_t M, int64_t N, int K, int num_sms);
 cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd,
                               float* out0, int64_t ld0, int64_t n_split, float* out1, int64_t ld1,
                               int32_t* dev_status, cudaStream_t stream);
-// per-row top-K of A B^T (ids = B row indices), merged into ids/vals [M][K]
+// per-row top-K of A B^T (ids = B row indices), merged into ids/vals [M][K]; with
+// parts_out the sorted per-range lists are left for the caller to fold instead,
+// and zero_words[0 .. n_zero) are zeroed for the next kernel in the stream
 cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
                              int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
-                             cudaStream_t stream);
+                             cudaStream_t stream, TopkParts* parts_out = nullptr,
+                             unsigned* zero_words = nullptr, int n_zero = 0);
 
 // ---- selector
 cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,
@@ -62,6 +70,16 @@ cudaError_t lattice_launch(const int32_t* anchors, int R, int B, const int32_t* 
 cudaError_t lattice_walk_launch(const float* lattice, const int32_t* ids, int R, int B, int K, int64_t V,
                                 const float* uniforms, float temperature, int32_t* path,
                                 float* path_scores, int32_t* dev_status, cudaStream_t stream);
+
+// ---- the fused tail of the draft head: per position the fold of the sorted
+// lists, the teacher-forced scores (pred nullable), and per request the greedy
+// walk by the last of its positions' CTAs.  tickets [R] must be zero on entry.
+bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms);
+cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t* ids, float* vals,
+                              const int32_t* anchors, int B, const float* G, const uint16_t* A,
+                              const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
+                              const int32_t* pred, float* pair_scores, unsigned* tickets,
+                              int32_t* dev_status, cudaStream_t stream);
 
 // ---- conv: y = sum_{j<taps, t-j>=0} (base[j] + dyn[p, j, c/g]) * x[p-j]
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,

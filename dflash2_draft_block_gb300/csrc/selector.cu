@@ -7,58 +7,25 @@
 // teacher-forced scorer takes the predecessor as given (PR #62, "Selector
 // training objective").
 //
-// One warp per request (walk) or per row (pair scores).  Lane l owns rank
-// elements [8l, 8l+8) of every 256-wide chunk: the gate q = A[a] (.) G_t is
-// formed once per position in registers, each candidate's B row is read with one
-// 16-byte load per lane per chunk, and a shuffle tree sums the lanes.  The
-// candidate loop is unrolled by 4 so that four B-row gathers are in flight.
+// The walk runs one CTA per request with its gathers staged in shared memory
+// (walk_request_cta, selector_dev.cuh) when they fit, else one warp per request;
+// the teacher-forced scores run one warp per (row, group of 8 candidates).  Lane
+// l owns rank elements [8l, 8l+8) of every 256-wide chunk: the gate
+// q = A[a] (.) G_t is formed once per position in registers, each candidate's B
+// row is read with one 16-byte load per lane per chunk, and a shuffle tree sums
+// the lanes.  The warp walk's candidate loop is unrolled by 4 so that four B-row
+// gathers are in flight.
 #include "common.cuh"
 #include "kernels.h"
+#include "selector_dev.cuh"
 
 namespace df2 {
 
 namespace {
 
+using namespace sel;
+
 constexpr int kWarpsPerBlock = 4;
-
-// q[c][e] = A[a, 256c + 8l + e] * G[256c + 8l + e] for the lane's slice (NCH chunks).
-template <int NCH>
-__device__ __forceinline__ void load_gate(const uint16_t* __restrict__ A, int64_t a, int r,
-                                          const float* __restrict__ Grow, int lane,
-                                          float q[NCH][8]) {
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int i0 = c * 256 + lane * 8;
-        if (i0 < r) {
-            float af[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(A + a * r + i0)), af);
-            const float4 g0 = __ldg(reinterpret_cast<const float4*>(Grow + i0));
-            const float4 g1 = __ldg(reinterpret_cast<const float4*>(Grow + i0 + 4));
-            q[c][0] = af[0] * g0.x; q[c][1] = af[1] * g0.y; q[c][2] = af[2] * g0.z; q[c][3] = af[3] * g0.w;
-            q[c][4] = af[4] * g1.x; q[c][5] = af[5] * g1.y; q[c][6] = af[6] * g1.z; q[c][7] = af[7] * g1.w;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) q[c][e] = 0.f;
-        }
-    }
-}
-
-template <int NCH>
-__device__ __forceinline__ float dot_lane(const uint16_t* __restrict__ Bc, int64_t b, int r, int lane,
-                                          const float q[NCH][8]) {
-    float s = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const int i0 = c * 256 + lane * 8;
-        if (i0 < r) {
-            float bf[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(Bc + b * r + i0)), bf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s = fmaf(q[c][e], bf[e], s);
-        }
-    }
-    return s;
-}
 
 // Scores of candidates [j0, j0+4) of one row against gate q; ids are in range.
 template <int NCH>
@@ -177,172 +144,16 @@ pair_scores_kernel(const int32_t* __restrict__ pred, int64_t P, const int32_t* _
     if (bad && lane == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
 }
 
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-                 "l"(gmem_src)
-                 : "memory");
-}
-
-// Walk with everything it can read gathered into shared memory first: the B rows
-// of every candidate of rows 1..B-1, the A rows of the anchor and of every
-// candidate of rows 1..B-2 (the only possible predecessors), and the G rows.
-// The gathers are independent, so they are all in flight at once; the B-1
-// sequential steps then touch shared memory only and are run by one warp with
-// no block-wide barrier.  One CTA per request (8 warps issue the gathers).
-constexpr int kWalkThreads = 256;
-
-// Sum 16 per-lane values over the warp at once: at each butterfly level a lane
-// keeps half of its values and adds its partner's copy of them, so 16 shuffles in
-// 5 levels replace 16 separate 5-level reductions.  Returns u = (lane >> 1) & 15:
-// on return v[0] of this lane is the warp-wide sum of the lanes' v[u].
-__device__ __forceinline__ int reduce16_transpose(float v[16], int lane) {
-#pragma unroll
-    for (int m = 16, h = 8; m >= 2; m >>= 1, h >>= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < h; ++i) {
-            const float send = upper ? v[i] : v[i + h];
-            const float keep = upper ? v[i + h] : v[i];
-            v[i] = keep + __shfl_xor_sync(kFull, send, m);
-        }
-    }
-    v[0] += __shfl_xor_sync(kFull, v[0], 1);
-    return (lane >> 1) & 15;
-}
-
-__host__ __device__ inline size_t walk_cta_smem(int B, int K, int r) {
-    const size_t T = size_t(B) - 1;
-    return T * K * r * 2 + ((T - 1) * K + 1) * r * 2 + T * r * 4 + T * K * 8 + 64;
-}
-
 template <int NCH>
-__global__ void __launch_bounds__(kWalkThreads)
+__global__ void __launch_bounds__(kWalkThreads, 1)
 walk_cta_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __restrict__ ids,
                 const float* __restrict__ vals, const float* __restrict__ G,
                 const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K,
                 int r, int32_t* __restrict__ path, float* __restrict__ path_scores,
                 int32_t* __restrict__ dev_status) {
     extern __shared__ __align__(16) uint8_t smem[];
-    const int T = B - 1;
-    const int q = blockIdx.x;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint16_t* Bs = reinterpret_cast<uint16_t*>(smem);                     // [T*K][r]
-    uint16_t* As = Bs + size_t(T) * K * r;                                // [(T-1)*K + 1][r]
-    float* Gs = reinterpret_cast<float*>(As + (size_t(T - 1) * K + 1) * r);  // [T][r]
-    float* vs = Gs + size_t(T) * r;                                       // [T*K]
-    int* is = reinterpret_cast<int*>(vs + size_t(T) * K);                 // [T*K]
-    int* bad = is + size_t(T) * K;
-
-    const int64_t row1 = int64_t(q) * B + 1;  // first drafted row of the request
-    const int32_t a0 = __ldg(anchors + q);
-    if (tid == 0) *bad = (a0 < 0 || a0 >= V) ? 1 : 0;
-    __syncthreads();
-    for (int e = tid; e < T * K; e += kWalkThreads) {
-        const int32_t b = __ldg(ids + row1 * K + e);
-        is[e] = b;
-        vs[e] = __ldg(vals + row1 * K + e);
-        if (b < 0 || b >= V) *bad = 1;
-    }
-    __syncthreads();
-    if (*bad) {
-        for (int t = tid; t < T; t += kWalkThreads) {
-            path[int64_t(q) * T + t] = -1;
-            path_scores[int64_t(q) * T + t] = __int_as_float(0x7fc00000);
-        }
-        if (tid == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
-        return;
-    }
-
-    const int cpr = r / 8;  // 16-byte chunks per bf16 row
-    for (int i = tid; i < T * K * cpr; i += kWalkThreads) {
-        const int row = i / cpr, c = i - row * cpr;
-        cp_async16(Bs + size_t(row) * r + c * 8, Bc + int64_t(is[row]) * r + c * 8);
-    }
-    const int na = (T - 1) * K + 1;
-    for (int i = tid; i < na * cpr; i += kWalkThreads) {
-        const int arow = i / cpr, c = i - arow * cpr;
-        const int64_t a = arow == 0 ? a0 : is[arow - 1];
-        cp_async16(As + size_t(arow) * r + c * 8, A + a * r + c * 8);
-    }
-    const int gpr = r / 4;  // 16-byte chunks per fp32 row
-    for (int i = tid; i < T * gpr; i += kWalkThreads) {
-        const int t = i / gpr, c = i - t * gpr;
-        cp_async16(Gs + size_t(t) * r + c * 4, G + (row1 + t) * r + c * 4);
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (warp != 0) return;
-
-    // The sequential part, one warp, shared memory only.  Lane l owns rank
-    // elements [256c + 8l, 256c + 8l + 8) of the gate and of every B row.
-    int arow = 0;  // As row of the current predecessor
-    for (int t = 1; t <= T; ++t) {
-        float qv[NCH][8];
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int i0 = c * 256 + lane * 8;
-            if (i0 < r) {
-                float af[8];
-                unpack8(*reinterpret_cast<const uint4*>(As + size_t(arow) * r + i0), af);
-                const float* g = Gs + size_t(t - 1) * r + i0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qv[c][e] = af[e] * g[e];
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qv[c][e] = 0.f;
-            }
-        }
-        float best = -INFINITY;
-        int best_id = -1, best_j = 0;
-        for (int j0 = 0; j0 < K; j0 += 16) {
-            // 16 candidates' lane partials, summed across the warp together
-            float part[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                part[u] = 0.f;
-                if (j0 + u < K) {
-                    const uint16_t* brow = Bs + (size_t(t - 1) * K + j0 + u) * r;
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        const int i0 = c * 256 + lane * 8;
-                        if (i0 < r) {
-                            float bf[8];
-                            unpack8(*reinterpret_cast<const uint4*>(brow + i0), bf);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) part[u] = fmaf(qv[c][e], bf[e], part[u]);
-                        }
-                    }
-                }
-            }
-            // lanes 2u and 2u+1 end up holding candidate j0+u's full sum
-            const int u = reduce16_transpose(part, lane);
-            float sj = -INFINITY;
-            int idj = INT_MAX, jj = -1;
-            if (j0 + u < K) {
-                sj = vs[(t - 1) * K + j0 + u] + part[0];
-                idj = is[(t - 1) * K + j0 + u];
-                jj = j0 + u;
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                const float ov = __shfl_xor_sync(kFull, sj, o);
-                const int oi = __shfl_xor_sync(kFull, idj, o);
-                const int oj = __shfl_xor_sync(kFull, jj, o);
-                if (oj >= 0 && (jj < 0 || ranks_before(ov, oi, sj, idj))) { sj = ov; idj = oi; jj = oj; }
-            }
-            if (jj >= 0 && (best_id < 0 || ranks_before(sj, idj, best, best_id))) {
-                best = sj;
-                best_id = idj;
-                best_j = jj;
-            }
-        }
-        if (lane == 0) {
-            path[int64_t(q) * T + (t - 1)] = best_id;
-            path_scores[int64_t(q) * T + (t - 1)] = best;
-        }
-        arow = 1 + (t - 1) * K + best_j;
-    }
+    walk_request_cta<NCH, false>(blockIdx.x, anchors, B, ids, vals, G, A, Bc, V, K, r, path, path_scores,
+                                 dev_status, smem);
 }
 
 }  // namespace

@@ -1,0 +1,353 @@
+// Device-side building blocks of the candidate selector, shared by the selector
+// kernels and the fused draft-head kernel.
+//
+// Pair score S_t(a, b) = U_t(b) + < A(a) (.) H(h_t), B(b) > (verl-SpeCo PR #62,
+// "What DFlash2 adds"; "DFlash 2 Explanation", "Problem 1").  Every dot product
+// here uses one lane slicing -- lane l owns rank elements [256c + 8l, 256c + 8l + 8)
+// of the gate and of every B row, an fmaf chain over them -- and one shuffle tree
+// over the lanes, so the walk, the teacher-forced scores and the fused head give
+// bit-identical scores.
+#pragma once
+
+#include "common.cuh"
+
+namespace df2 {
+namespace sel {
+
+// q[c][e] = A[a, 256c + 8l + e] * G[256c + 8l + e] for the lane's slice (NCH chunks).
+template <int NCH>
+__device__ __forceinline__ void load_gate(const uint16_t* __restrict__ A, int64_t a, int r,
+                                          const float* __restrict__ Grow, int lane,
+                                          float q[NCH][8]) {
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int i0 = c * 256 + lane * 8;
+        if (i0 < r) {
+            float af[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(A + a * r + i0)), af);
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(Grow + i0));
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(Grow + i0 + 4));
+            q[c][0] = af[0] * g0.x; q[c][1] = af[1] * g0.y; q[c][2] = af[2] * g0.z; q[c][3] = af[3] * g0.w;
+            q[c][4] = af[4] * g1.x; q[c][5] = af[5] * g1.y; q[c][6] = af[6] * g1.z; q[c][7] = af[7] * g1.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[c][e] = 0.f;
+        }
+    }
+}
+
+template <int NCH>
+__device__ __forceinline__ float dot_lane(const uint16_t* __restrict__ Bc, int64_t b, int r, int lane,
+                                          const float q[NCH][8]) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int i0 = c * 256 + lane * 8;
+        if (i0 < r) {
+            float bf[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(Bc + b * r + i0)), bf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s = fmaf(q[c][e], bf[e], s);
+        }
+    }
+    return s;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src)
+                 : "memory");
+}
+
+// Walk with everything it can read gathered into shared memory: the B rows of
+// every candidate of rows 1..B-1, the A rows of the anchor and of every candidate
+// of rows 1..B-2 (the only possible predecessors), and the G rows.  The gathers
+// are issued up front in one cp.async group per step, in the order the steps
+// need them, so step t starts as soon as its own group has landed.  One CTA per
+// request; all 8 warps score each step's candidates.
+constexpr int kWalkThreads = 256;
+constexpr int kWalkWarps = kWalkThreads / 32;
+
+__host__ __device__ inline size_t walk_cta_smem(int B, int K, int r) {
+    const size_t T = size_t(B) - 1;
+    return T * K * r * 2 + ((T - 1) * K + 1) * r * 2 + T * r * 4 + T * K * 8 + 2 * size_t(K) * 4 + 64;
+}
+
+// A lane's slices [256c + 8l, 256c + 8l + 8) of a bf16 row and of an fp32 row in
+// shared memory (zeros past r, or everywhere when !valid).
+template <int NCH>
+__device__ __forceinline__ void load_bslice(const uint16_t* row, int r, int lane, bool valid,
+                                            float out[NCH][8]) {
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int i0 = c * 256 + lane * 8;
+        if (valid && i0 < r) {
+            unpack8(*reinterpret_cast<const uint4*>(row + i0), out[c]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) out[c][e] = 0.f;
+        }
+    }
+}
+
+template <int NCH>
+__device__ __forceinline__ void load_gslice(const float* row, int r, int lane, float out[NCH][8]) {
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int i0 = c * 256 + lane * 8;
+        if (i0 < r) {
+            const float4 x = *reinterpret_cast<const float4*>(row + i0);
+            const float4 y = *reinterpret_cast<const float4*>(row + i0 + 4);
+            out[c][0] = x.x; out[c][1] = x.y; out[c][2] = x.z; out[c][3] = x.w;
+            out[c][4] = y.x; out[c][5] = y.y; out[c][6] = y.z; out[c][7] = y.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) out[c][e] = 0.f;
+        }
+    }
+}
+
+// Wait until at most n of this thread's cp.async groups are pending (n > 7: 7).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
+
+// The greedy walk of one request by one CTA of kWalkThreads threads, with every
+// gather staged in shared memory (walk_cta_smem bytes at smem).  kFresh: the
+// candidate lists were written earlier in the same kernel, so they are read
+// through L2 rather than the read-only path.
+template <int NCH, bool kFresh>
+__device__ __forceinline__ void walk_request_cta(int q, const int32_t* __restrict__ anchors, int B,
+                                                 const int32_t* __restrict__ ids,
+                                                 const float* __restrict__ vals,
+                                                 const float* __restrict__ G,
+                                                 const uint16_t* __restrict__ A,
+                                                 const uint16_t* __restrict__ Bc, int64_t V, int K,
+                                                 int r, int32_t* __restrict__ path,
+                                                 float* __restrict__ path_scores,
+                                                 int32_t* __restrict__ dev_status, uint8_t* smem) {
+    const int T = B - 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint16_t* Bs = reinterpret_cast<uint16_t*>(smem);                     // [T*K][r]
+    uint16_t* As = Bs + size_t(T) * K * r;                                // [(T-1)*K + 1][r]
+    float* Gs = reinterpret_cast<float*>(As + (size_t(T - 1) * K + 1) * r);  // [T][r]
+    float* vs = Gs + size_t(T) * r;                                       // [T*K]
+    int* is = reinterpret_cast<int*>(vs + size_t(T) * K);                 // [T*K]
+    float* sc = reinterpret_cast<float*>(is + size_t(T) * K);             // [2][K] step scores
+    int* bad = reinterpret_cast<int*>(sc + 2 * size_t(K));
+
+    const int64_t row1 = int64_t(q) * B + 1;  // first drafted row of the request
+    const int32_t a0 = __ldg(anchors + q);
+    if (tid == 0) *bad = (a0 < 0 || a0 >= V) ? 1 : 0;
+    __syncthreads();
+    for (int e = tid; e < T * K; e += kWalkThreads) {
+        const int32_t b = kFresh ? __ldcg(ids + row1 * K + e) : __ldg(ids + row1 * K + e);
+        is[e] = b;
+        vs[e] = kFresh ? __ldcg(vals + row1 * K + e) : __ldg(vals + row1 * K + e);
+        if (b < 0 || b >= V) *bad = 1;
+    }
+    __syncthreads();
+    if (*bad) {
+        for (int t = tid; t < T; t += kWalkThreads) {
+            path[int64_t(q) * T + t] = -1;
+            path_scores[int64_t(q) * T + t] = __int_as_float(0x7fc00000);
+        }
+        if (tid == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+        return;
+    }
+
+    // group t: position t's B rows and G row, and the A rows of its possible
+    // predecessors (the anchor for t = 1, else position t-1's candidates).  Warp w
+    // copies rows w, w+8, ...; lane l copies 16-byte chunks l, l+32, ... of a row.
+    const int cpr = r / 8;  // 16-byte chunks per bf16 row
+    const int gpr = r / 4;  // 16-byte chunks per fp32 row
+    for (int t = 1; t <= T; ++t) {
+        for (int row = (t - 1) * K + warp; row < t * K; row += kWalkWarps) {
+            const uint16_t* src = Bc + int64_t(is[row]) * r;
+            for (int c = lane; c < cpr; c += 32) cp_async16(Bs + size_t(row) * r + c * 8, src + c * 8);
+        }
+        const int a_lo = (t == 1) ? 0 : 1 + (t - 2) * K;
+        const int a_hi = (t == 1) ? 1 : 1 + (t - 1) * K;
+        for (int arow = a_lo + warp; arow < a_hi; arow += kWalkWarps) {
+            const uint16_t* src = A + (arow == 0 ? int64_t(a0) : int64_t(is[arow - 1])) * r;
+            for (int c = lane; c < cpr; c += 32) cp_async16(As + size_t(arow) * r + c * 8, src + c * 8);
+        }
+        for (int i = tid; i < gpr; i += kWalkThreads)
+            cp_async16(Gs + size_t(t - 1) * r + i * 4, G + (row1 + t - 1) * r + i * 4);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+
+    // Step t scores position t's candidates against the gate A[a_{t-1}] (.) G_t.
+    // Warp w scores candidates w, w+8, ... in pairs; lane l owns rank elements
+    // [256c + 8l, 256c + 8l + 8) of the gate and of every B row, and a shuffle tree
+    // sums the lanes (the order of the other walk kernels, so the scores are
+    // bit-identical).  One barrier per step: after it, the step's gathers and the
+    // previous step's scores are visible to all warps, and every warp reduces those
+    // scores to the same argmax on its own.  The critical path of a step is that
+    // argmax, the predecessor's A row, one FMA chain and one shuffle tree: the B
+    // and G slices of a warp's first pair do not depend on the argmax and are read
+    // before it (for r <= 512).
+    constexpr bool kEarly = NCH <= 2;
+    int arow = 0;  // As row of the current predecessor
+    for (int t = 1; t <= T + 1; ++t) {
+        if (t <= T) cp_async_wait_pending(T - t);
+        __syncthreads();
+        const int ja = warp, jb = warp + kWalkWarps;
+        constexpr int NE = kEarly ? NCH : 1;  // slices held across the argmax
+        float gs[NE][8], b0[NE][8], b1[NE][8];
+        if constexpr (kEarly) {
+            if (t <= T) {
+                load_gslice<NE>(Gs + size_t(t - 1) * r, r, lane, gs);
+                load_bslice<NE>(Bs + (size_t(t - 1) * K + ja) * r, r, lane, ja < K, b0);
+                load_bslice<NE>(Bs + (size_t(t - 1) * K + jb) * r, r, lane, jb < K, b1);
+            }
+        }
+        if (t > 1) {
+            const float* sp = sc + ((t - 1) & 1) * K;
+            const int* ip = is + (t - 2) * K;
+            float bv = -INFINITY;
+            int bid = INT_MAX, bj = -1;
+            for (int j = lane; j < K; j += 32) {
+                const float v = sp[j];
+                const int id = ip[j];
+                if (bj < 0 || ranks_before(v, id, bv, bid)) {
+                    bv = v;
+                    bid = id;
+                    bj = j;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float ov = __shfl_xor_sync(kFull, bv, o);
+                const int oi = __shfl_xor_sync(kFull, bid, o);
+                const int oj = __shfl_xor_sync(kFull, bj, o);
+                if (oj >= 0 && (bj < 0 || ranks_before(ov, oi, bv, bid) ||
+                                (ov == bv && oi == bid && oj < bj))) {
+                    bv = ov;
+                    bid = oi;
+                    bj = oj;
+                }
+            }
+            if (tid == 0) {
+                path[int64_t(q) * T + (t - 2)] = bid;
+                path_scores[int64_t(q) * T + (t - 2)] = bv;
+            }
+            arow = 1 + (t - 2) * K + bj;
+        }
+        if (t > T) break;
+        float qv[NCH][8];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int i0 = c * 256 + lane * 8;
+            float af[8], gc[1][8];
+            if constexpr (kEarly) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gc[0][e] = gs[c][e];
+            } else {
+                load_gslice<1>(Gs + size_t(t - 1) * r + c * 256, r - c * 256, lane, gc);
+            }
+            if (i0 < r) {
+                unpack8(*reinterpret_cast<const uint4*>(As + size_t(arow) * r + i0), af);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) af[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qv[c][e] = af[e] * gc[0][e];
+        }
+        float* so = sc + (t & 1) * K;
+        const float* vrow = vs + (t - 1) * K;
+        for (int j = ja; j < K; j += 2 * kWalkWarps) {
+            const int j2 = j + kWalkWarps;
+            float pa = 0.f, pb = 0.f;
+            if constexpr (kEarly) {
+                if (j != ja) {
+                    load_bslice<NE>(Bs + (size_t(t - 1) * K + j) * r, r, lane, true, b0);
+                    load_bslice<NE>(Bs + (size_t(t - 1) * K + j2) * r, r, lane, j2 < K, b1);
+                }
+#pragma unroll
+                for (int c = 0; c < NE; ++c)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        pa = fmaf(qv[c][e], b0[c][e], pa);
+                        pb = fmaf(qv[c][e], b1[c][e], pb);
+                    }
+            } else {
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    float x[1][8], y[1][8];
+                    load_bslice<1>(Bs + (size_t(t - 1) * K + j) * r + c * 256, r - c * 256, lane, true, x);
+                    load_bslice<1>(Bs + (size_t(t - 1) * K + j2) * r + c * 256, r - c * 256, lane, j2 < K, y);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        pa = fmaf(qv[c][e], x[0][e], pa);
+                        pb = fmaf(qv[c][e], y[0][e], pb);
+                    }
+                }
+            }
+            if (j2 < K) {
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {  // two shuffle trees, interleaved
+                    pa += __shfl_xor_sync(kFull, pa, o);
+                    pb += __shfl_xor_sync(kFull, pb, o);
+                }
+                if (lane == 0) {
+                    so[j] = vrow[j] + pa;
+                    so[j2] = vrow[j2] + pb;
+                }
+            } else {
+                pa = warp_sum(pa);
+                if (lane == 0) so[j] = vrow[j] + pa;
+            }
+        }
+    }
+}
+
+// Teacher-forced scores of one row by one CTA: warp w scores candidates w, w+8, ...
+// with the lane slicing and shuffle tree of pair_scores_kernel (bit-identical).
+template <int NCH, bool kFresh>
+__device__ __forceinline__ void pair_row_cta(int64_t p, const int32_t* __restrict__ pred,
+                                             const int32_t* __restrict__ ids,
+                                             const float* __restrict__ vals,
+                                             const float* __restrict__ G,
+                                             const uint16_t* __restrict__ A,
+                                             const uint16_t* __restrict__ Bc, int64_t V, int K, int r,
+                                             float* __restrict__ scores,
+                                             int32_t* __restrict__ dev_status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float nan = __int_as_float(0x7fc00000);
+    const int32_t a = __ldg(pred + p);
+    bool bad = false;
+    if (a < 0 || a >= V) {
+        for (int j = threadIdx.x; j < K; j += blockDim.x) scores[p * K + j] = nan;
+        bad = threadIdx.x == 0;
+    } else {
+        float qv[NCH][8];
+        load_gate<NCH>(A, a, r, G + p * r, lane, qv);
+        for (int j = warp; j < K; j += kWalkWarps) {
+            const int32_t b = kFresh ? __ldcg(ids + p * K + j) : __ldg(ids + p * K + j);
+            const bool inr = b >= 0 && b < V;
+            const float part = inr ? dot_lane<NCH>(Bc, b, r, lane, qv) : 0.f;
+            const float d = warp_sum(part);
+            if (lane == 0) {
+                const float u = kFresh ? __ldcg(vals + p * K + j) : __ldg(vals + p * K + j);
+                scores[p * K + j] = inr ? u + d : nan;
+            }
+            bad = bad || (!inr && lane == 0);
+        }
+    }
+    if (bad && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+}
+
+}  // namespace sel
+}  // namespace df2

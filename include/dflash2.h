@@ -7,6 +7,7 @@
  *                                 the per-position top-K, and the hidden projection H
  *   dflash2_selector_walk         the candidate selector's greedy walk
  *   dflash2_selector_pair_scores  the selector scores with teacher-forced predecessors
+ *   dflash2_draft_head            the four steps above for one draft block, fused
  *   dflash2_selector_lattice      every adjacent candidate pair scored at once
  *   dflash2_lattice_walk          the greedy or sampling walk over that table
  *   dflash2_conv_prepare          the grouped dynamic causal conv before a sublayer
@@ -194,6 +195,35 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
                                  const float* topk_vals, const float* G, const uint16_t* A,
                                  const uint16_t* Bc, int64_t V, int K, int r, float* scores,
                                  int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_draft_head — unary top-K, H, greedy walk and teacher-forced scores of one
+ * draft block in one call.
+ *
+ * The same results as dflash2_unary_topk (with W_H), then dflash2_selector_walk,
+ * then (pred != NULL) dflash2_selector_pair_scores, on P = R*B rows: the same
+ * kernels' arithmetic in the same order, so every output is bit-identical to the
+ * three calls'.  Where the shapes allow (P <= the SM count, K <= 64, the walk's
+ * gathers within shared memory) the fold of the head's partial lists, the walk and
+ * the teacher-forced scores run in one launch after the head kernel; otherwise the
+ * three calls run in sequence.  There is no counterpart in the pages beyond their
+ * sum; the call exists to cut the launches of a batch-1 draft step.
+ *
+ *   h [R*B, D] bf16; W_lm [V, D] bf16; W_H [r, D] bf16 (required); A, Bc [V, r] bf16;
+ *   anchors [R] int32; pred [R*B] int32 (nullable);
+ *   topk_ids, topk_vals [R*B, K] out; G [R*B, r] fp32 out; path, path_scores [R, B-1]
+ *   out; pair_scores [R*B, K] fp32 out (required iff pred != NULL).
+ *   workspace: dflash2_draft_head_workspace_size(R, B, D, V, K, r) bytes, 256-byte
+ *   aligned (it holds the head's partial lists and per-request counters).
+ * Rules: the union of the three calls' rules; B >= 2.  Status bits as those calls.
+ * ---------------------------------------------------------------------- */
+size_t dflash2_draft_head_workspace_size(int R, int B, int64_t D, int64_t V, int K, int r);
+int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const uint16_t* W_lm, int64_t V,
+                       int K, const uint16_t* W_H, int r, const uint16_t* A, const uint16_t* Bc,
+                       const int32_t* anchors, const int32_t* pred, int32_t* topk_ids,
+                       float* topk_vals, float* G, int32_t* path, float* path_scores,
+                       float* pair_scores, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * dflash2_selector_lattice — every adjacent candidate pair scored at once.

@@ -69,6 +69,15 @@ def test_selector_validation(lib):
     assert w(fake, 2, 8, fake, fake, fake, fake, fake, 100, 101, 32, fake, fake, None, None) == 1  # K > V
     assert w(fake, 2, 8, fake, fake, fake, fake, fake, 100, 4, 12, fake, fake, None, None) == 2  # r % 8
     assert w(fake, 0, 8, fake, fake, fake, fake, fake, 100, 4, 32, fake, fake, None, None) == 0
+    dh = lib.dflash2_draft_head
+    f8 = [fake] * 8
+    # B < 2, K > V, r % 8, W_H missing, workspace too small
+    assert dh(fake, 1, 1, 64, fake, 100, 4, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
+    assert dh(fake, 1, 8, 64, fake, 100, 101, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
+    assert dh(fake, 1, 8, 64, fake, 100, 4, fake, 12, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 2
+    assert dh(fake, 1, 8, 64, fake, 100, 4, None, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
+    assert dh(fake, 0, 8, 64, fake, 100, 4, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 0, None, None) == 0
+    assert lib.dflash2_draft_head_workspace_size(1, 1, 64, 100, 4, 32) == 0
     lt = lib.dflash2_selector_lattice
     assert lt(fake, 2, 1, fake, fake, fake, fake, fake, 100, 4, 32, fake, None, None) == 1  # B < 2
     assert lt(fake, 2, 8, fake, fake, fake, fake, fake, 100, 101, 32, fake, None, None) == 1  # K > V
