@@ -140,7 +140,8 @@ DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const ui
 namespace {
 
 // The fused path: the head kernel leaves its sorted lists in the workspace and one
-// tail launch folds them, scores the teacher-forced pairs and walks each request.
+// tail launch (a thread-block cluster per request) folds them, scores the
+// teacher-forced pairs and the lattice, and walks each request.
 bool draft_fused(HeadPath path, int64_t P, int B, int64_t D, int64_t V, int K, int r, int sms) {
     if (path == HeadPath::Simple) return false;
     int S = 0;
@@ -151,9 +152,8 @@ bool draft_fused(HeadPath path, int64_t P, int B, int64_t D, int64_t V, int K, i
 
 size_t draft_workspace(int64_t P, int R, int B, int64_t D, int64_t V, int K, int r, int sms) {
     const HeadPath path = pick_head(P, D, V, K);
-    size_t n = round_up(head_workspace(path, P, D, V, K, sms), 256);
-    if (draft_fused(path, P, B, D, V, K, r, sms)) n += round_up(size_t(R) * 4, 256);  // tickets
-    return n;
+    (void)R;
+    return round_up(head_workspace(path, P, D, V, K, sms), 256);
 }
 
 }  // namespace
@@ -202,23 +202,20 @@ DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const
         return dflash2_selector_pair_scores(pred, P, topk_ids, topk_vals, G, A, Bc, V, K, r,
                                             pair_scores, dev_status, stream);
     }
-    unsigned* tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) +
-                                                    round_up(head_workspace(hp, P, D, V, K, sms), 256));
     df2::TopkParts parts{};
     if (hp == HeadPath::Skinny) {
         rc = df2::head_tc_launch(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
-                                 dev_status, sms, st, -1, &parts, tickets, R);
+                                 dev_status, sms, st, -1, &parts);
         if (rc != DF2_OK) return rc;
     } else {
         cudaError_t e = df2::wide_topk_launch(h, P, W_lm, V, D, K, topk_ids, topk_vals, workspace,
-                                              dev_status, sms, st, &parts, tickets, R);
+                                              dev_status, sms, st, &parts);
         if (e != cudaSuccess) return DF2_ERR_CUDA;
         e = df2::wide_store_launch(h, P, W_H, r, D, G, r, r, G, r, dev_status, st);
         if (e != cudaSuccess) return DF2_ERR_CUDA;
     }
     return from_cuda(df2::draft_tail_launch(parts, P, K, topk_ids, topk_vals, anchors, B, G, A, Bc, V,
-                                            r, path, path_scores, pred, pair_scores, tickets,
-                                            dev_status, st));
+                                            r, path, path_scores, pred, pair_scores, dev_status, st));
 }
 
 // -------------------------------------------------------------- selector --

@@ -50,6 +50,14 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// A 64-bit key whose unsigned order is the rank order below (for id >= 0, finite
+// values; -0 and +0 compare equal, as floats do).
+__device__ __forceinline__ unsigned long long rank_key(float v, int id) {
+    const unsigned u = __float_as_uint(v + 0.0f);  // -0 -> +0
+    const unsigned k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(k) << 32) | static_cast<unsigned>(0x7FFFFFFF - id);
+}
+
 // Rank order of (value, token id) pairs: larger value first, then lower id.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);

@@ -1,17 +1,34 @@
 // The fused tail of the draft head: after the head kernel has left its sorted
 // per-CTA (or per-range) top-K lists in the workspace, one launch finishes the
-// selector's part of the cycle.  CTA p
-//   1. folds position p's lists into its top-K (merge_position),
-//   2. scores position p's candidates after the teacher-forced predecessor
-//      pred[p] (pair_row_cta; verl-SpeCo PR #62, "Selector training objective"),
-//   3. takes a ticket for its request; the CTA that completes a request's block
-//      walks it (walk_request_cta; vLLM Speculators "DFlash2" guide, "Candidate
-//      Selector": start at the anchor, feed each best successor in as the next
+// selector's part of the cycle with the lattice schedule ("DFlash 2
+// Explanation", "How It Works", Problem 1: all adjacent pairs are scored in one
+// parallel pass, and only the final walk over the finished scores is sequential).
+//
+// Each request's B rows form one thread-block cluster; CTA t of the cluster owns
+// row t:
+//   1. every CTA folds its row's lists into the row's top-K (merge_position),
+//      then starts copying its candidates' B rows, its G row and its
+//      teacher-forced predecessor's A row, and prefetches its candidates' A rows
+//      into L2 for CTA t+1;
+//   -- cluster barrier: every row of the request is folded --
+//   2. CTA t >= 1 scores lattice slot t-1 (every candidate of row t after every
+//      candidate of row t-1, after the anchor for t = 1) with the walk's own
+//      arithmetic, reduces each predecessor's row to its best candidate, and
+//      writes those argmaxes into CTA 0's shared memory; every CTA then scores
+//      its row after its teacher-forced predecessor from the rows it staged
+//      (pair_row_staged; verl-SpeCo PR #62, "Selector training objective");
+//   -- cluster barrier --
+//   3. CTA 0 walks: from the anchor, each step follows the stored argmax of the
+//      current predecessor's row (vLLM Speculators "DFlash2" guide, "Candidate
+//      Selector": start at the anchor, feed the best successor in as the next
 //      predecessor).
-// The results are the ones the separate merge, walk and teacher-forced kernels
-// give (the same arithmetic, in the same order); only the launches and the
-// waiting between them go.  Every CTA must be resident at once for the tickets
-// to be taken in one wave, so the launch is used for P <= the SM count.
+// Every score uses the lane slicing, fmaf chains and shuffle-tree sums of the
+// separate walk and teacher-forced kernels, and every argmax the same order
+// (value, then the lower token id, then the lower column), so the outputs are
+// bit-identical to the separate calls'.  The cluster barriers are the hardware's;
+// nothing spins.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "selector_dev.cuh"
@@ -21,68 +38,153 @@ namespace df2 {
 
 namespace {
 
-constexpr int kTailThreads = 256;
-static_assert(kTailThreads == mrg::kMergeThreads && kTailThreads == sel::kWalkThreads,
-              "the three phases share one CTA shape");
+namespace cg = cooperative_groups;
 
-size_t tail_smem(int B, int K, int r, int S) {
-    const size_t a = mrg::merge_smem(S, K), b = sel::walk_cta_smem(B, K, r);
-    return a > b ? a : b;
+constexpr int kTailThreads = 256;
+static_assert(kTailThreads == mrg::kMergeThreads, "the phases share one CTA shape");
+constexpr int kMaxCluster = 16;
+
+// Dynamic shared memory: the merge's and the slot's layouts overlap at offset 0;
+// CTA 0's argmax table follows both.
+size_t tail_tab_off(int K, int r, int S) {
+    const size_t a = mrg::merge_smem(S, K), b = sel::lattice_slot_smem(K, r);
+    return ((a > b ? a : b) + 15) / 16 * 16;
 }
+size_t tail_smem(int B, int K, int r, int S) { return tail_tab_off(K, r, S) + size_t(B - 1) * K * 12 + 16; }
 
 template <int R, int NCH>
-__global__ void __launch_bounds__(kTailThreads, 1)
+__global__ void __launch_bounds__(kTailThreads)
 draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id, int S, int64_t P,
                   int K, int32_t* __restrict__ ids, float* __restrict__ vals,
                   const int32_t* __restrict__ anchors, int B, const float* __restrict__ G,
                   const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int r,
                   int32_t* __restrict__ path, float* __restrict__ path_scores,
                   const int32_t* __restrict__ pred, float* __restrict__ pair_scores,
-                  unsigned* __restrict__ tickets, int32_t* __restrict__ dev_status) {
+                  int32_t* __restrict__ dev_status, unsigned tab_off) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ int last;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int t = int(cluster.block_rank());
     const int64_t p = blockIdx.x;
-    const int q = int(p / B);
+    const int q = int(p / B), T = B - 1;
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    // CTA 0's table: for slot s and predecessor i, the best candidate's column,
+    // token id and score
+    int* tab_j = reinterpret_cast<int*>(smem + tab_off);
+    int* tab_id = tab_j + T * K;
+    float* tab_v = reinterpret_cast<float*>(tab_id + T * K);
+    int* tab_bad = reinterpret_cast<int*>(tab_v + T * K);
 
     mrg::merge_position<R>(part_v, part_id, S, P, K, p, ids, vals, smem);
-    __syncthreads();  // row p's list is written (by warp 0) before anyone reads it
-    if (pred) sel::pair_row_cta<NCH, true>(p, pred, ids, vals, G, A, Bc, V, K, r, pair_scores, dev_status);
-
-    // publish row p, then count it towards request q
+    __syncthreads();  // row p's list is written (by warp 0) and smem is free again
+    const int32_t pid = pred ? __ldg(pred + p) : -1;
+    const bool pred_ok = pid >= 0 && pid < V;
+    // row p's candidates' B rows, its G row and its teacher-forced predecessor's A row
+    const bool staged = sel::slot_stage_begin(p, ids, G, Bc, A, pid, V, K, r, smem);
+    if (t == 0 && threadIdx.x == 0) *tab_bad = 0;
+    if (t < T) {
+        // the next row's predecessors are this row's candidates: warm L2 with their A rows
+        const int lines = (r * 2 + 127) / 128;
+        for (int e = threadIdx.x; e < K * lines; e += blockDim.x) {
+            const int32_t a = __ldcg(ids + p * K + e / lines);
+            if (a >= 0 && a < V)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(A + int64_t(a) * r + (e % lines) * 64));
+        }
+    }
     __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(tickets + q, 1u) == unsigned(B - 1);
-    __syncthreads();
-    if (!last) return;
-    __threadfence();  // the other rows of request q, published before their tickets
-    sel::walk_request_cta<NCH, true>(q, anchors, B, ids, vals, G, A, Bc, V, K, r, path, path_scores,
-                                     dev_status, smem);
+    cluster.sync();
+
+    bool slot_ok = true;
+    if (t >= 1) {
+        int* rj = cluster.map_shared_rank(tab_j, 0) + size_t(t - 1) * K;
+        int* rid = cluster.map_shared_rank(tab_id, 0) + size_t(t - 1) * K;
+        float* rv = cluster.map_shared_rank(tab_v, 0) + size_t(t - 1) * K;
+        slot_ok = staged && sel::slot_finish<NCH>(p, t == 1 ? -1 : p - 1, __ldg(anchors + q), ids, vals, A, V,
+                                                  K, r, smem, rj, rv, rid);
+        if (!slot_ok && threadIdx.x == 0) *cluster.map_shared_rank(tab_bad, 0) = 1;
+    } else if (staged) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+    }
+    if (pred) {
+        // row p's teacher-forced scores: from the staged rows when they are all there
+        if (staged && (t == 0 || slot_ok)) {
+            sel::pair_row_staged<NCH>(p, pred_ok, vals, K, r, smem, pair_scores);
+            if (!pred_ok && threadIdx.x == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+        } else if (warp == 0) {
+            if (!sel::pair_row_warp<NCH, true>(p, pred, ids, vals, G, A, Bc, V, K, r, pair_scores) && dev_status &&
+                (threadIdx.x & 31) == 0)
+                atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+        }
+    }
+    cluster.sync();
+
+    if (t == 0 && threadIdx.x == 0) {
+        const int32_t a0 = __ldg(anchors + q);
+        if (*tab_bad || a0 < 0 || a0 >= V) {
+            for (int s = 0; s < T; ++s) {
+                path[int64_t(q) * T + s] = -1;
+                path_scores[int64_t(q) * T + s] = __int_as_float(0x7fc00000);
+            }
+            if (dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+        } else {
+            int i = 0;
+            for (int s = 0; s < T; ++s) {
+                const int at = s * K + i;
+                path[int64_t(q) * T + s] = tab_id[at];
+                path_scores[int64_t(q) * T + s] = tab_v[at];
+                i = tab_j[at];
+            }
+        }
+    }
 }
 
-}  // namespace
-
-bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
-    return P >= 1 && P <= num_sms && K <= 64 && r <= 4096 && P % B == 0 &&
-           tail_smem(B, K, r, S) <= 200 * 1024;
+template <int R, int N>
+cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, const TopkParts& parts, int K,
+                        int32_t* ids, float* vals, const int32_t* anchors, const float* G,
+                        const uint16_t* A, const uint16_t* Bc, int64_t V, int r, int32_t* path,
+                        float* path_scores, const int32_t* pred, float* pair_scores, int32_t* dev_status,
+                        bool probe_only, bool* fits) {
+    auto kernel = draft_tail_kernel<R, N>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    if (B > 8) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(P));
+    cfg.blockDim = dim3(kTailThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(B);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (probe_only) {
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+        *fits = e == cudaSuccess && clusters > 0;
+        return e;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, parts.v, parts.id, parts.S, P, K, ids, vals, anchors, B, G, A,
+                              Bc, V, r, path, path_scores, pred, pair_scores, dev_status,
+                              unsigned(tail_tab_off(K, r, parts.S)));
 }
 
-cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t* ids, float* vals,
-                              const int32_t* anchors, int B, const float* G, const uint16_t* A,
-                              const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
-                              const int32_t* pred, float* pair_scores, unsigned* tickets,
-                              int32_t* dev_status, cudaStream_t stream) {
+// Runs (or, probe_only, checks that the cluster shape can run) the right instance.
+cudaError_t dispatch_tail(bool probe_only, bool* fits, const TopkParts& parts, int64_t P, int K, int32_t* ids,
+                          float* vals, const int32_t* anchors, int B, const float* G, const uint16_t* A,
+                          const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
+                          const int32_t* pred, float* pair_scores, int32_t* dev_status, cudaStream_t stream) {
     const size_t smem = tail_smem(B, K, r, parts.S);
     const int nch = (r + 255) / 256;
     cudaError_t e = cudaSuccess;
-#define DF2_TAIL(RV, N)                                                                                 \
-    do {                                                                                                \
-        e = cudaFuncSetAttribute(draft_tail_kernel<RV, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
-                                 int(smem));                                                            \
-        if (e != cudaSuccess) return e;                                                                 \
-        draft_tail_kernel<RV, N><<<unsigned(P), kTailThreads, smem, stream>>>(                           \
-            parts.v, parts.id, parts.S, P, K, ids, vals, anchors, B, G, A, Bc, V, r, path, path_scores,  \
-            pred, pair_scores, tickets, dev_status);                                                    \
-    } while (0)
+#define DF2_TAIL(RV, N)                                                                                \
+    e = launch_tail<RV, N>(P, B, smem, stream, parts, K, ids, vals, anchors, G, A, Bc, V, r, path,     \
+                           path_scores, pred, pair_scores, dev_status, probe_only, fits)
 #define DF2_TAIL_N(RV)                        \
     do {                                      \
         if (nch <= 1) DF2_TAIL(RV, 1);        \
@@ -95,8 +197,33 @@ cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t*
     else DF2_TAIL_N(2);
 #undef DF2_TAIL_N
 #undef DF2_TAIL
+    return e;
+}
+
+}  // namespace
+
+bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
+    (void)num_sms;
+    if (P < 1 || B < 2 || B > kMaxCluster || K > 64 || r > 4096 || P % B != 0) return false;
+    if (tail_smem(B, K, r, S) > 200 * 1024) return false;
+    bool fits = false;
+    const TopkParts probe{nullptr, nullptr, S};
+    if (dispatch_tail(true, &fits, probe, P, K, nullptr, nullptr, nullptr, B, nullptr, nullptr, nullptr, 1, r,
+                      nullptr, nullptr, nullptr, nullptr, nullptr, nullptr) != cudaSuccess)
+        return false;
+    return fits;
+}
+
+cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t* ids, float* vals,
+                              const int32_t* anchors, int B, const float* G, const uint16_t* A,
+                              const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
+                              const int32_t* pred, float* pair_scores, int32_t* dev_status,
+                              cudaStream_t stream) {
+    bool unused = false;
+    const cudaError_t e = dispatch_tail(false, &unused, parts, P, K, ids, vals, anchors, B, G, A, Bc, V, r, path,
+                                        path_scores, pred, pair_scores, dev_status, stream);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace df2

@@ -71,15 +71,15 @@ cudaError_t lattice_walk_launch(const float* lattice, const int32_t* ids, int R,
                                 const float* uniforms, float temperature, int32_t* path,
                                 float* path_scores, int32_t* dev_status, cudaStream_t stream);
 
-// ---- the fused tail of the draft head: per position the fold of the sorted
-// lists, the teacher-forced scores (pred nullable), and per request the greedy
-// walk by the last of its positions' CTAs.  tickets [R] must be zero on entry.
+// ---- the fused tail of the draft head: one thread-block cluster per request
+// folds its rows' sorted lists, scores the teacher-forced pairs (pred nullable)
+// and the lattice slots, and walks the request
 bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms);
 cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t* ids, float* vals,
                               const int32_t* anchors, int B, const float* G, const uint16_t* A,
                               const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
-                              const int32_t* pred, float* pair_scores, unsigned* tickets,
-                              int32_t* dev_status, cudaStream_t stream);
+                              const int32_t* pred, float* pair_scores, int32_t* dev_status,
+                              cudaStream_t stream);
 
 // ---- conv: y = sum_{j<taps, t-j>=0} (base[j] + dyn[p, j, c/g]) * x[p-j]
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,

@@ -313,40 +313,264 @@ __device__ __forceinline__ void walk_request_cta(int q, const int32_t* __restric
     }
 }
 
-// Teacher-forced scores of one row by one CTA: warp w scores candidates w, w+8, ...
-// with the lane slicing and shuffle tree of pair_scores_kernel (bit-identical).
-template <int NCH, bool kFresh>
-__device__ __forceinline__ void pair_row_cta(int64_t p, const int32_t* __restrict__ pred,
-                                             const int32_t* __restrict__ ids,
-                                             const float* __restrict__ vals,
-                                             const float* __restrict__ G,
-                                             const uint16_t* __restrict__ A,
-                                             const uint16_t* __restrict__ Bc, int64_t V, int K, int r,
-                                             float* __restrict__ scores,
-                                             int32_t* __restrict__ dev_status) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float nan = __int_as_float(0x7fc00000);
-    const int32_t a = __ldg(pred + p);
-    bool bad = false;
-    if (a < 0 || a >= V) {
-        for (int j = threadIdx.x; j < K; j += blockDim.x) scores[p * K + j] = nan;
-        bad = threadIdx.x == 0;
-    } else {
-        float qv[NCH][8];
-        load_gate<NCH>(A, a, r, G + p * r, lane, qv);
-        for (int j = warp; j < K; j += kWalkWarps) {
-            const int32_t b = kFresh ? __ldcg(ids + p * K + j) : __ldg(ids + p * K + j);
-            const bool inr = b >= 0 && b < V;
-            const float part = inr ? dot_lane<NCH>(Bc, b, r, lane, qv) : 0.f;
-            const float d = warp_sum(part);
-            if (lane == 0) {
-                const float u = kFresh ? __ldcg(vals + p * K + j) : __ldg(vals + p * K + j);
-                scores[p * K + j] = inr ? u + d : nan;
-            }
-            bad = bad || (!inr && lane == 0);
+// Sum 16 per-lane values over the warp at once: at each butterfly level a lane
+// keeps half of its values and adds its partner's copy of them, so 16 shuffles in
+// 5 levels replace 16 separate 5-level reductions.  Each partial pairs the same
+// lanes as warp_sum at the same level, so the sums are bit-identical to
+// warp_sum's.  Returns u = (lane >> 1) & 15: on return v[0] of this lane is the
+// warp-wide sum of the lanes' v[u].
+__device__ __forceinline__ int reduce16_transpose(float v[16], int lane) {
+#pragma unroll
+    for (int m = 16, h = 8; m >= 2; m >>= 1, h >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? v[i] : v[i + h];
+            const float keep = upper ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, m);
         }
     }
-    if (bad && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+    v[0] += __shfl_xor_sync(kFull, v[0], 1);
+    return (lane >> 1) & 15;
+}
+
+__host__ __device__ inline size_t lattice_slot_smem(int K, int r) {
+    return size_t(K) * 2 * r * 2 + size_t(r) * 4 + size_t(K) * K * 4 + size_t(K) * 12 + size_t(r) * 2 + 80;
+}
+
+// Offset of the teacher-forced predecessor's A row [r] bf16 in the slot layout.
+__host__ __device__ inline size_t slot_pred_row_off(int K, int r) {
+    return (size_t(K) * 2 * r * 2 + size_t(r) * 4 + size_t(K) * K * 4 + size_t(K) * 12 + 15) / 16 * 16;
+}
+
+// Lattice slot t-1 of request q, in two halves so that the part that needs only
+// row t's own candidates can run before the CTA learns row t-1's: slot_stage_begin
+// starts the copies of row t's B rows and G row; slot_finish stages the
+// predecessors' A rows (the anchor alone for t = 1, else row t-1's K candidates),
+// scores every pair with the walk's arithmetic (gate slices, fmaf chains,
+// shuffle-tree sums: each entry bit-identical to the score the walk computes for
+// that pair) into shared memory, and reduces each predecessor's row to its best
+// candidate (value, then the lower token id, then the lower column).  Shared
+// memory layout (lattice_slot_smem bytes at smem): B rows [K][r] bf16, A rows
+// [K][r] bf16, G [r] fp32, slot [K][K] fp32, then row t's values and ids and the
+// predecessor ids.  slot_stage_begin returns false when a candidate id of row t is
+// out of range (nothing is copied).
+__device__ __forceinline__ bool slot_stage_begin(int64_t row, const int32_t* __restrict__ ids,
+                                                 const float* __restrict__ G,
+                                                 const uint16_t* __restrict__ Bc,
+                                                 const uint16_t* __restrict__ A, int32_t pred_id, int64_t V,
+                                                 int K, int r, uint8_t* smem) {
+    __shared__ int bad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+    uint16_t* Bs = reinterpret_cast<uint16_t*>(smem);
+    float* Gs = reinterpret_cast<float*>(Bs + size_t(2) * K * r);
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    for (int j = tid; j < K; j += blockDim.x) {
+        const int32_t b = __ldcg(ids + row * K + j);
+        if (b < 0 || b >= V) bad = 1;
+    }
+    __syncthreads();
+    if (bad) return false;
+    const int cpr = r / 8;
+    for (int j = warp; j < K; j += nwarps) {
+        const int32_t b = __ldcg(ids + row * K + j);
+        for (int c = lane; c < cpr; c += 32) cp_async16(Bs + size_t(j) * r + c * 8, Bc + int64_t(b) * r + c * 8);
+    }
+    for (int c = tid; c < r / 4; c += blockDim.x) cp_async16(Gs + c * 4, G + row * r + c * 4);
+    if (pred_id >= 0 && pred_id < V) {
+        uint16_t* Ap = reinterpret_cast<uint16_t*>(smem + slot_pred_row_off(K, r));
+        for (int c = tid; c < cpr; c += blockDim.x) cp_async16(Ap + c * 8, A + int64_t(pred_id) * r + c * 8);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    return true;
+}
+
+// Teacher-forced scores of row `row` from the rows slot_stage_begin staged (its
+// candidates' B rows, G and the predecessor's A row), every copy landed: warp w
+// scores candidates w, w+8, ... with the lane slicing and shuffle tree of
+// pair_scores_kernel (bit-identical).  The candidates' ids are in range.
+template <int NCH>
+__device__ __forceinline__ void pair_row_staged(int64_t row, bool pred_ok, const float* __restrict__ vals,
+                                                int K, int r, const uint8_t* smem,
+                                                float* __restrict__ scores) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    if (!pred_ok) {
+        for (int j = threadIdx.x; j < K; j += blockDim.x) scores[row * K + j] = __int_as_float(0x7fc00000);
+        return;
+    }
+    const uint16_t* Bs = reinterpret_cast<const uint16_t*>(smem);
+    const float* Gs = reinterpret_cast<const float*>(Bs + size_t(2) * K * r);
+    const uint16_t* Ap = reinterpret_cast<const uint16_t*>(smem + slot_pred_row_off(K, r));
+    float qv[NCH][8];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const int i0 = c * 256 + lane * 8;
+        float af[8], gc[1][8];
+        load_gslice<1>(Gs + c * 256, r - c * 256, lane, gc);
+        if (i0 < r) {
+            unpack8(*reinterpret_cast<const uint4*>(Ap + i0), af);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) af[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[c][e] = af[e] * gc[0][e];
+    }
+    for (int j = warp; j < K; j += nwarps) {
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            float bf[1][8];
+            load_bslice<1>(Bs + size_t(j) * r + c * 256, r - c * 256, lane, true, bf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) part = fmaf(qv[c][e], bf[0][e], part);
+        }
+        const float d = warp_sum(part);
+        if (lane == 0) scores[row * K + j] = __ldcg(vals + row * K + j) + d;
+    }
+}
+
+// Finishes the slot started by slot_stage_begin: best_j/best_v/best_id[i] for each
+// predecessor i < rows (rows = 1 and the anchor when pred_row < 0).  Returns false
+// when a predecessor id is out of range (the outputs are untouched).
+template <int NCH>
+__device__ __forceinline__ bool slot_finish(int64_t row, int64_t pred_row, int32_t anchor,
+                                            const int32_t* __restrict__ ids,
+                                            const float* __restrict__ vals,
+                                            const uint16_t* __restrict__ A, int64_t V, int K, int r,
+                                            uint8_t* smem, int* best_j, float* best_v, int* best_id) {
+    __shared__ int bad;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+    const int rows = pred_row < 0 ? 1 : K;
+    uint16_t* Bs = reinterpret_cast<uint16_t*>(smem);
+    uint16_t* As = Bs + size_t(K) * r;
+    float* Gs = reinterpret_cast<float*>(As + size_t(K) * r);
+    float* Ls = Gs + r;                        // [K][K]
+    float* vs = Ls + size_t(K) * K;            // [K] unary values of row t
+    int* cs = reinterpret_cast<int*>(vs + K);  // [K] candidate ids of row t
+    int* ps = cs + K;                          // [K] predecessor ids
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    for (int i = tid; i < K; i += blockDim.x) {
+        vs[i] = __ldcg(vals + row * K + i);
+        cs[i] = __ldcg(ids + row * K + i);
+        if (i < rows) {
+            const int32_t a = pred_row < 0 ? anchor : __ldcg(ids + pred_row * K + i);
+            ps[i] = a;
+            if (a < 0 || a >= V) bad = 1;
+        }
+    }
+    __syncthreads();
+    if (bad) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        return false;
+    }
+    const int cpr = r / 8;
+    for (int i = warp; i < rows; i += nwarps)
+        for (int c = lane; c < cpr; c += 32) cp_async16(As + size_t(i) * r + c * 8, A + int64_t(ps[i]) * r + c * 8);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    const int jblocks = (K + 15) / 16;
+    for (int item = warp; item < rows * jblocks; item += nwarps) {
+        const int i = item / jblocks, j0 = (item % jblocks) * 16;
+        float qv[NCH][8];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int i0 = c * 256 + lane * 8;
+            float af[8], gc[1][8];
+            load_gslice<1>(Gs + c * 256, r - c * 256, lane, gc);
+            if (i0 < r) {
+                unpack8(*reinterpret_cast<const uint4*>(As + size_t(i) * r + i0), af);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) af[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qv[c][e] = af[e] * gc[0][e];
+        }
+        float part[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            part[u] = 0.f;
+            if (j0 + u < K) {
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    float bf[1][8];
+                    load_bslice<1>(Bs + size_t(j0 + u) * r + c * 256, r - c * 256, lane, true, bf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) part[u] = fmaf(qv[c][e], bf[0][e], part[u]);
+                }
+            }
+        }
+        const int u = reduce16_transpose(part, lane);
+        if ((lane & 1) == 0 && j0 + u < K) Ls[size_t(i) * K + j0 + u] = vs[j0 + u] + part[0];
+    }
+    __syncthreads();
+    for (int i = tid; i < rows; i += blockDim.x) {
+        float bv = -INFINITY;
+        int bid = INT_MAX, bj = -1;
+        for (int j = 0; j < K; ++j) {
+            const float v = Ls[size_t(i) * K + j];
+            if (bj < 0 || ranks_before(v, cs[j], bv, bid)) {
+                bv = v;
+                bid = cs[j];
+                bj = j;
+            }
+        }
+        best_j[i] = bj;
+        best_v[i] = bv;
+        best_id[i] = bid;
+    }
+    return true;
+}
+
+// Teacher-forced scores of row p by one warp: every candidate with the lane
+// slicing and shuffle tree of pair_scores_kernel (bit-identical), four candidates
+// in flight.  kFresh: the row's list was written earlier in the same kernel.
+// Returns false when pred[p] or a candidate id is out of range (NaN written there).
+template <int NCH, bool kFresh>
+__device__ __forceinline__ bool pair_row_warp(int64_t p, const int32_t* __restrict__ pred,
+                                              const int32_t* __restrict__ ids,
+                                              const float* __restrict__ vals,
+                                              const float* __restrict__ G,
+                                              const uint16_t* __restrict__ A,
+                                              const uint16_t* __restrict__ Bc, int64_t V, int K, int r,
+                                              float* __restrict__ scores) {
+    const int lane = threadIdx.x & 31;
+    const float nan = __int_as_float(0x7fc00000);
+    const int32_t a = __ldg(pred + p);
+    if (a < 0 || a >= V) {
+        for (int j = lane; j < K; j += 32) scores[p * K + j] = nan;
+        return false;
+    }
+    float qv[NCH][8];
+    load_gate<NCH>(A, a, r, G + p * r, lane, qv);
+    bool ok = true;
+    for (int j0 = 0; j0 < K; j0 += 4) {
+        float part[4];
+        int32_t b[4];
+        bool inr[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const bool has = j0 + u < K;
+            b[u] = has ? (kFresh ? __ldcg(ids + p * K + j0 + u) : __ldg(ids + p * K + j0 + u)) : 0;
+            inr[u] = b[u] >= 0 && b[u] < V;
+            part[u] = (has && inr[u]) ? dot_lane<NCH>(Bc, b[u], r, lane, qv) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float d = warp_sum(part[u]);
+            if (j0 + u < K) {
+                if (lane == 0) {
+                    const float uv = kFresh ? __ldcg(vals + p * K + j0 + u) : __ldg(vals + p * K + j0 + u);
+                    scores[p * K + j0 + u] = inr[u] ? uv + d : nan;
+                }
+                ok = ok && inr[u];
+            }
+        }
+    }
+    return ok;
 }
 
 }  // namespace sel

@@ -23,7 +23,7 @@ constexpr int kWarps = 8;
 constexpr int kMergeThreads = kWarps * 32;
 constexpr int kOneWarpCands = 128;  // up to this many candidates one warp folds them alone
 
-__host__ __device__ inline size_t merge_smem(int S, int K) { return size_t(S) * K * 16; }
+__host__ __device__ inline size_t merge_smem(int S, int K) { return size_t(S) * K * 16 + size_t(S) * 12; }
 
 // The final top-K of position p from the S sorted lists part_[v|id][s][P][K], by
 // one CTA of kMergeThreads threads with merge_smem(S, K) bytes at smem.  Warp 0
@@ -55,25 +55,31 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
     }
     __syncthreads();
     // the K-th best head: the head that exactly K-1 other heads rank before.  The
-    // heads are first packed into the (still unused) candidate buffer.
+    // heads are packed as rank keys (larger = ranks before; 0 = empty list) into
+    // the still unused candidate buffer, and two threads count each head's rank.
+    unsigned long long* hk = reinterpret_cast<unsigned long long*>(smem + size_t(S) * K * 16);
+    int* rk = reinterpret_cast<int*>(hk + S);
     for (int s = tid; s < S; s += kWarps * 32) {
-        bv[s] = cv[s * K];
-        bi[s] = ci[s * K];
+        const int id = ci[s * K];
+        hk[s] = id < 0 ? 0ull : rank_key(cv[s * K], id);
+        rk[s] = 0;
+    }
+    __syncthreads();
+    const int half = (S + 1) / 2;
+    for (int it = tid; it < 2 * S; it += kWarps * 32) {
+        const int s = it >> 1, o0 = (it & 1) ? half : 0, o1 = (it & 1) ? S : half;
+        const unsigned long long mine = hk[s];
+        if (mine == 0ull) continue;
+        int n = 0;
+#pragma unroll 8
+        for (int o = o0; o < o1; ++o) n += hk[o] > mine ? 1 : 0;
+        atomicAdd(rk + s, n);
     }
     __syncthreads();
     for (int s = tid; s < S; s += kWarps * 32) {
-        const int hid = bi[s];
-        if (hid < 0) continue;
-        const float hv = bv[s];
-        int rank = 0;
-#pragma unroll 8
-        for (int o = 0; o < S; ++o) {
-            const int oid = bi[o];
-            rank += (oid >= 0 && ranks_before(bv[o], oid, hv, hid)) ? 1 : 0;
-        }
-        if (rank == K - 1) {
-            t_v = hv;
-            t_id = hid;
+        if (hk[s] != 0ull && rk[s] == K - 1) {
+            t_v = cv[s * K];
+            t_id = ci[s * K];
             have_t = 1;
         }
     }

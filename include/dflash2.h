@@ -203,18 +203,20 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
  * The same results as dflash2_unary_topk (with W_H), then dflash2_selector_walk,
  * then (pred != NULL) dflash2_selector_pair_scores, on P = R*B rows: the same
  * kernels' arithmetic in the same order, so every output is bit-identical to the
- * three calls'.  Where the shapes allow (P <= the SM count, K <= 64, the walk's
- * gathers within shared memory) the fold of the head's partial lists, the walk and
- * the teacher-forced scores run in one launch after the head kernel; otherwise the
- * three calls run in sequence.  There is no counterpart in the pages beyond their
- * sum; the call exists to cut the launches of a batch-1 draft step.
+ * three calls'.  Where the shapes allow (K <= 64 on a tensor-core head, B <= 16,
+ * a lattice slot's rows within shared memory) the fold of the head's partial
+ * lists, the walk and the teacher-forced scores run in one launch after the head
+ * kernel, one thread-block cluster per request, with the walk taken over the
+ * lattice of adjacent pair scores ([KB] "How It Works", Problem 1); otherwise the
+ * three calls run in sequence.  The pages describe the steps, not this fusion;
+ * the call exists to cut the launches and the serial latency of a draft step.
  *
  *   h [R*B, D] bf16; W_lm [V, D] bf16; W_H [r, D] bf16 (required); A, Bc [V, r] bf16;
  *   anchors [R] int32; pred [R*B] int32 (nullable);
  *   topk_ids, topk_vals [R*B, K] out; G [R*B, r] fp32 out; path, path_scores [R, B-1]
  *   out; pair_scores [R*B, K] fp32 out (required iff pred != NULL).
  *   workspace: dflash2_draft_head_workspace_size(R, B, D, V, K, r) bytes, 256-byte
- *   aligned (it holds the head's partial lists and per-request counters).
+ *   aligned (it holds the head's partial lists).
  * Rules: the union of the three calls' rules; B >= 2.  Status bits as those calls.
  * ---------------------------------------------------------------------- */
 size_t dflash2_draft_head_workspace_size(int R, int B, int64_t D, int64_t V, int K, int r);
