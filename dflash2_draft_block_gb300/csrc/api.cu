@@ -333,6 +333,9 @@ DF2_API int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int
     const int64_t half = int64_t(taps) * G;
     float* d_in = static_cast<float*>(workspace);
     cudaError_t e;
+    if (df2::conv_prepare_rows_supported(P, C, B, dtype == DF2_DTYPE_F32))
+        return from_cuda(df2::conv_prepare_rows_launch(x, dtype == DF2_DTYPE_F32, P, C, B, taps, g, W_proj,
+                                                       base, y, dyn_out, st));
     if (P <= 64) {
         const int sms = num_sms_current();
         if (sms <= 0) return DF2_ERR_CUDA;

@@ -343,6 +343,160 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
     return cudaGetLastError();
 }
 
+// Few rows (P <= 64): the projection and the apply in one kernel.  CTA (gx, gy)
+// owns channel groups [gx*gpc, gx*gpc + gpc) and rows [gy*PR, gy*PR + PR), PR a
+// multiple of the block size so that no tap reaches outside the CTA's rows.  It
+// stages its rows of x in shared memory, computes its groups' projection columns
+// -- (io*taps + j)*G + gi for both sides io -- one warp per column with the
+// arithmetic of gemm_rows_kernel (lane slices of 8 W elements, fmaf over the
+// rows, a shuffle tree), writes the output-side columns to dyn_out, keeps the
+// input-side ones in shared memory and applies the conv to its groups' channels
+// with the arithmetic of conv_apply_rows_kernel.  One launch instead of two, and
+// the input-side corrections never leave the chip.
+__device__ __forceinline__ void cp_async16_p(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void load8s(const uint16_t* p, float f[8]) {
+    unpack8(*reinterpret_cast<const uint4*>(p), f);
+}
+__device__ __forceinline__ void load8s(const float* p, float f[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ float to_f32(uint16_t v) { return bf16_to_f32(v); }
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ void store1(uint16_t* p, float v) { *p = f32_to_bf16_rn(v); }
+__device__ __forceinline__ void store1(float* p, float v) { *p = v; }
+
+constexpr int kPrepThreads = 256;
+
+template <int PG, typename T>
+__global__ void __launch_bounds__(kPrepThreads, 1)
+conv_prepare_rows_kernel(const T* __restrict__ x, int64_t P, int C, int B, int taps, int g, int G, int gpc,
+                         int PR, const uint16_t* __restrict__ W, const float* __restrict__ base,
+                         T* __restrict__ y, float* __restrict__ dyn_out) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    T* xs = reinterpret_cast<T*>(smem);                                          // [PR][C]
+    float* ds = reinterpret_cast<float*>(smem + size_t(PR) * C * sizeof(T));     // [PR][taps][gpc]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = kPrepThreads / 32;
+    const int g0 = int(blockIdx.x) * gpc;
+    const int ng = gpc < G - g0 ? gpc : G - g0;
+    const int64_t m0 = int64_t(blockIdx.y) * PR;
+    const int nm = int(P - m0 < PR ? P - m0 : PR);
+    constexpr int kPer16 = 16 / int(sizeof(T));
+    const int cpr = C / kPer16;
+    for (int r = warp; r < nm; r += nwarps)
+        for (int c = lane; c < cpr; c += 32)
+            cp_async16_p(xs + size_t(r) * C + c * kPer16, x + (m0 + r) * C + c * kPer16);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
+    const int k8 = C / 8;
+    const int ncols = 2 * taps * ng;
+    auto column = [&](int lc) {
+        const int io = lc / (taps * ng), rem = lc % (taps * ng), j = rem / ng, gl = rem % ng;
+        return int64_t(io * taps + j) * G + g0 + gl;
+    };
+    // the first kPre chunks of each lane's slice of the warp's first W row are loaded
+    // while x is still being staged
+    constexpr int kPre = 16;
+    uint4 wpre[kPre];
+    if (warp < ncols) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(W + column(warp) * C);
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int c = lane + 32 * k;
+            wpre[k] = c < k8 ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+
+    for (int lc = warp; lc < ncols; lc += nwarps) {
+        const int io = lc / (taps * ng), rem = lc % (taps * ng), j = rem / ng, gl = rem % ng;
+        const int64_t n = column(lc);
+        float acc[PG];
+#pragma unroll
+        for (int p = 0; p < PG; ++p) acc[p] = 0.f;
+        const uint4* wrow = reinterpret_cast<const uint4*>(W + n * C);
+        auto fold = [&](const uint4& wv, int c) {
+            float wf[8];
+            unpack8(wv, wf);
+#pragma unroll
+            for (int p = 0; p < PG; ++p) {
+                if (p < nm) {
+                    float xf[8];
+                    load8s(xs + size_t(p) * C + c * 8, xf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[p] = fmaf(wf[e], xf[e], acc[p]);
+                }
+            }
+        };
+        const bool first = lc == warp;
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int c = lane + 32 * k;
+            if (c < k8) fold(first ? wpre[k] : __ldg(wrow + c), c);
+        }
+#pragma unroll 8
+        for (int c = lane + 32 * kPre; c < k8; c += 32) fold(__ldg(wrow + c), c);
+        float mine = 0.f;
+#pragma unroll
+        for (int p = 0; p < PG; ++p) {
+            const float sum = warp_sum(acc[p]);
+            if (lane == p) mine = sum;
+        }
+        if (lane < nm) {
+            if (io == 0) ds[(lane * taps + j) * gpc + gl] = mine;
+            else dyn_out[(m0 + lane) * (int64_t(taps) * G) + int64_t(j) * G + g0 + gl] = mine;
+        }
+    }
+    __syncthreads();
+
+    const int c_lo = g0 * g, nch = ng * g;
+    for (int e = threadIdx.x; e < nm * nch; e += kPrepThreads) {
+        const int r = e / nch, c = c_lo + e % nch;
+        const int t = int((m0 + r) % B);
+        float acc = 0.f;
+        for (int j = 0; j < taps && j <= t; ++j) {
+            const float k = __ldg(base + int64_t(j) * C + c) + ds[(r * taps + j) * gpc + (c / g - g0)];
+            acc = fmaf(k, to_f32(xs[size_t(r - j) * C + c]), acc);
+        }
+        store1(y + (m0 + r) * C + c, acc);
+    }
+}
+
+template <int PG, typename T>
+cudaError_t launch_prepare_rows(const T* x, int64_t P, int C, int B, int taps, int g, int PR,
+                                const uint16_t* W, const float* base, T* y, float* dyn_out,
+                                cudaStream_t stream) {
+    const int G = C / g;
+    const int gpc = 2 * taps >= 8 ? 1 : 8 / (2 * taps);
+    const size_t smem = size_t(PR) * C * sizeof(T) + size_t(PR) * taps * gpc * 4;
+    cudaError_t e = cudaFuncSetAttribute(conv_prepare_rows_kernel<PG, T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    const dim3 grid = dim3(static_cast<unsigned>((G + gpc - 1) / gpc), static_cast<unsigned>((P + PR - 1) / PR));
+    conv_prepare_rows_kernel<PG, T><<<grid, kPrepThreads, smem, stream>>>(x, P, C, B, taps, g, G, gpc, PR, W,
+                                                                          base, y, dyn_out);
+    note_launch();
+    return cudaGetLastError();
+}
+
+// Rows per CTA for the fused few-row path (a multiple of B, at most 16, its x
+// rows within 160 KB of shared memory), or 0 when the path does not apply.
+int prepare_rows_per_cta(int64_t P, int C, int B, int esz) {
+    if (P > 64 || B > 16) return 0;
+    const int pg = B <= 8 ? 8 : 16;
+    const int pr = pg / B * B;
+    if (size_t(pr) * C * esz + 4096 > 160 * 1024) return 0;
+    return pr;
+}
+
 }  // namespace
 
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
@@ -353,6 +507,33 @@ cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, 
                                static_cast<float*>(y), stream);
     return launch_t<uint16_t>(static_cast<const uint16_t*>(x), P, C, B, taps, g, base_io, dyn,
                               dyn_ld, static_cast<uint16_t*>(y), stream);
+}
+
+}  // namespace df2
+
+namespace df2 {
+
+bool conv_prepare_rows_supported(int64_t P, int C, int B, bool f32) {
+    return prepare_rows_per_cta(P, C, B, f32 ? 4 : 2) > 0;
+}
+
+cudaError_t conv_prepare_rows_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
+                                     const uint16_t* W, const float* base, void* y, float* dyn_out,
+                                     cudaStream_t stream) {
+    const int pr = prepare_rows_per_cta(P, C, B, f32 ? 4 : 2);
+    if (pr == 0) return cudaErrorInvalidValue;
+    if (f32) {
+        if (pr <= 8)
+            return launch_prepare_rows<8, float>(static_cast<const float*>(x), P, C, B, taps, g, pr, W, base,
+                                                 static_cast<float*>(y), dyn_out, stream);
+        return launch_prepare_rows<16, float>(static_cast<const float*>(x), P, C, B, taps, g, pr, W, base,
+                                              static_cast<float*>(y), dyn_out, stream);
+    }
+    if (pr <= 8)
+        return launch_prepare_rows<8, uint16_t>(static_cast<const uint16_t*>(x), P, C, B, taps, g, pr, W, base,
+                                                static_cast<uint16_t*>(y), dyn_out, stream);
+    return launch_prepare_rows<16, uint16_t>(static_cast<const uint16_t*>(x), P, C, B, taps, g, pr, W, base,
+                                             static_cast<uint16_t*>(y), dyn_out, stream);
 }
 
 }  // namespace df2

@@ -43,6 +43,7 @@ namespace cg = cooperative_groups;
 constexpr int kTailThreads = 256;
 static_assert(kTailThreads == mrg::kMergeThreads, "the phases share one CTA shape");
 constexpr int kMaxCluster = 16;
+constexpr int kMaxLatticeK = 32;
 
 // Dynamic shared memory: the merge's and the slot's layouts overlap at offset 0;
 // CTA 0's argmax table follows both.
@@ -204,7 +205,9 @@ cudaError_t dispatch_tail(bool probe_only, bool* fits, const TopkParts& parts, i
 
 bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
     (void)num_sms;
-    if (P < 1 || B < 2 || B > kMaxCluster || K > 64 || r > 4096 || P % B != 0) return false;
+    // the lattice costs K times the greedy walk's products: worth its latency only
+    // for short candidate lists
+    if (P < 1 || B < 2 || B > kMaxCluster || K > kMaxLatticeK || r > 4096 || P % B != 0) return false;
     if (tail_smem(B, K, r, S) > 200 * 1024) return false;
     bool fits = false;
     const TopkParts probe{nullptr, nullptr, S};

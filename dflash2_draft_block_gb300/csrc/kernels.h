@@ -82,6 +82,11 @@ cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t*
                               cudaStream_t stream);
 
 // ---- conv: y = sum_{j<taps, t-j>=0} (base[j] + dyn[p, j, c/g]) * x[p-j]
+// ---- conv prepare for few rows (P <= 64, B <= 16): projection and apply fused
+bool conv_prepare_rows_supported(int64_t P, int C, int B, bool f32);
+cudaError_t conv_prepare_rows_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
+                                     const uint16_t* W, const float* base, void* y, float* dyn_out,
+                                     cudaStream_t stream);
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
                               const float* base_io, const float* dyn, int64_t dyn_ld, void* y,
                               cudaStream_t stream);

@@ -203,7 +203,7 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
  * The same results as dflash2_unary_topk (with W_H), then dflash2_selector_walk,
  * then (pred != NULL) dflash2_selector_pair_scores, on P = R*B rows: the same
  * kernels' arithmetic in the same order, so every output is bit-identical to the
- * three calls'.  Where the shapes allow (K <= 64 on a tensor-core head, B <= 16,
+ * three calls'.  Where the shapes allow (K <= 32 on a tensor-core head, B <= 16,
  * a lattice slot's rows within shared memory) the fold of the head's partial
  * lists, the walk and the teacher-forced scores run in one launch after the head
  * kernel, one thread-block cluster per request, with the walk taken over the

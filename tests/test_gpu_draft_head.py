@@ -59,7 +59,8 @@ def separate(df2, x, status=None):
 @pytest.mark.parametrize("R,B,D,V,K,r", [
     (1, 8, 4096, 151936, 16, 256),   # the batch-1 shape: skinny head + fused tail
     (2, 8, 256, 4096, 4, 32),        # the tiny shape
-    (1, 16, 512, 20000, 64, 512),    # K = 64 on the skinny head
+    (1, 16, 512, 20000, 64, 512),    # K = 64: the separate calls
+    (2, 16, 512, 20000, 32, 512),    # K = 32, a 16-CTA cluster
     (2, 8, 520, 9001, 17, 264),      # ragged K, D and r
     (16, 8, 256, 30000, 16, 256),    # 128 positions: the tensor-core GEMM head + fused tail
     (64, 8, 256, 20000, 16, 256),    # 512 positions: more than one wave, the separate calls
