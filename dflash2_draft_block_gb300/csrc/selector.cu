@@ -156,6 +156,160 @@ walk_cta_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __res
                                  dev_status, smem);
 }
 
+// Walk for requests whose gathers do not all fit in shared memory: one CTA per
+// request streams the steps.  The B rows and G row of step t+1 do not depend on
+// the choice at step t, so they are copied (cp.async, two buffers) while step t
+// runs, and the A rows of step t's candidates -- the possible predecessors at
+// step t+1 -- are prefetched into L2.  Warp w scores candidates w, w+8, ... with
+// the lane slicing and shuffle tree of the other walk kernels (bit-identical
+// scores); the warps' bests meet in shared memory.
+constexpr int kStreamThreads = 256;
+constexpr int kStreamWarps = kStreamThreads / 32;
+
+__host__ __device__ inline size_t walk_stream_smem(int K, int r) {
+    return 2 * (size_t(K) * r * 2 + size_t(r) * 4) + kStreamWarps * 16 + 64;
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+walk_stream_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __restrict__ ids,
+                   const float* __restrict__ vals, const float* __restrict__ G,
+                   const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K,
+                   int r, int32_t* __restrict__ path, float* __restrict__ path_scores,
+                   int32_t* __restrict__ dev_status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int bad;
+    const int T = B - 1;
+    const int q = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const size_t stage_bytes = size_t(K) * r * 2 + size_t(r) * 4;
+    float* wv = reinterpret_cast<float*>(smem + 2 * stage_bytes);  // [warps] best value
+    int* wi = reinterpret_cast<int*>(wv + kStreamWarps);           // [warps] best id
+    int* wj = wi + kStreamWarps;                                   // [warps] best column
+    const int64_t row1 = int64_t(q) * B + 1;
+    const int32_t a0 = __ldg(anchors + q);
+    if (tid == 0) bad = (a0 < 0 || a0 >= V) ? 1 : 0;
+    __syncthreads();
+    for (int e = tid; e < T * K; e += kStreamThreads) {
+        const int32_t b = __ldg(ids + row1 * K + e);
+        if (b < 0 || b >= V) bad = 1;
+    }
+    __syncthreads();
+    if (bad) {
+        for (int t = tid; t < T; t += kStreamThreads) {
+            path[int64_t(q) * T + t] = -1;
+            path_scores[int64_t(q) * T + t] = __int_as_float(0x7fc00000);
+        }
+        if (tid == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+        return;
+    }
+    const int cpr = r / 8;
+    // stage t (1-based) into buffer t & 1: position t's B rows [K][r] and G row [r]
+    auto issue = [&](int t) {
+        uint16_t* Bs = reinterpret_cast<uint16_t*>(smem + (t & 1) * stage_bytes);
+        float* Gs = reinterpret_cast<float*>(Bs + size_t(K) * r);
+        const int64_t row = row1 + t - 1;
+        for (int j = warp; j < K; j += kStreamWarps) {
+            const uint16_t* src = Bc + int64_t(__ldg(ids + row * K + j)) * r;
+            for (int c = lane; c < cpr; c += 32) cp_async16(Bs + size_t(j) * r + c * 8, src + c * 8);
+        }
+        for (int c = tid; c < r / 4; c += kStreamThreads) cp_async16(Gs + c * 4, G + row * r + c * 4);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (t < T) {  // position t's candidates are the predecessors at step t+1
+            const int lines = (r * 2 + 127) / 128;
+            for (int e = tid; e < K * lines; e += kStreamThreads)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(A + int64_t(__ldg(ids + row * K + e / lines)) * r +
+                                                              (e % lines) * 64));
+        }
+    };
+    issue(1);
+    int32_t a = a0;
+    for (int t = 1; t <= T; ++t) {
+        if (t < T) issue(t + 1);
+        // the gate A[a] (.) G_t: this warp's lane slices (A from L2, G once staged)
+        float af[NCH][8];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int i0 = c * 256 + lane * 8;
+            if (i0 < r) unpack8(__ldg(reinterpret_cast<const uint4*>(A + int64_t(a) * r + i0)), af[c]);
+            else
+#pragma unroll
+                for (int e = 0; e < 8; ++e) af[c][e] = 0.f;
+        }
+        if (t < T) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        const uint16_t* Bs = reinterpret_cast<const uint16_t*>(smem + (t & 1) * stage_bytes);
+        const float* Gs = reinterpret_cast<const float*>(Bs + size_t(K) * r);
+        float qv[NCH][8];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            float gc[1][8];
+            load_gslice<1>(Gs + c * 256, r - c * 256, lane, gc);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qv[c][e] = af[c][e] * gc[0][e];
+        }
+        const int64_t row = row1 + t - 1;
+        float bv = -INFINITY;
+        int bid = INT_MAX, bj = -1;
+        for (int j0 = warp; j0 < K; j0 += 4 * kStreamWarps) {
+            float part[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kStreamWarps;
+                part[u] = 0.f;
+                if (j < K) {
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        float bf[1][8];
+                        load_bslice<1>(Bs + size_t(j) * r + c * 256, r - c * 256, lane, true, bf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) part[u] = fmaf(qv[c][e], bf[0][e], part[u]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * kStreamWarps;
+                const float d = warp_sum(part[u]);
+                if (j < K) {
+                    const float sj = __ldg(vals + row * K + j) + d;
+                    const int idj = __ldg(ids + row * K + j);
+                    if (bj < 0 || ranks_before(sj, idj, bv, bid)) {
+                        bv = sj;
+                        bid = idj;
+                        bj = j;
+                    }
+                }
+            }
+        }
+        if (lane == 0) {
+            wv[warp] = bv;
+            wi[warp] = bid;
+            wj[warp] = bj;
+        }
+        __syncthreads();
+        // every thread reduces the warps' bests in the same order
+        float best = -INFINITY;
+        int best_id = INT_MAX, best_j = -1;
+        for (int w = 0; w < kStreamWarps; ++w) {
+            const int j = wj[w];
+            if (j >= 0 && (best_j < 0 || ranks_before(wv[w], wi[w], best, best_id) ||
+                           (wv[w] == best && wi[w] == best_id && j < best_j))) {
+                best = wv[w];
+                best_id = wi[w];
+                best_j = j;
+            }
+        }
+        if (tid == 0) {
+            path[int64_t(q) * T + (t - 1)] = best_id;
+            path_scores[int64_t(q) * T + (t - 1)] = best;
+        }
+        a = best_id;
+        __syncthreads();  // buffer t & 1 and the warps' bests are free again
+    }
+}
+
 }  // namespace
 
 cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,
@@ -180,6 +334,26 @@ cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids
         else if (nch <= 8) DF2_WALK_CTA(8);
         else DF2_WALK_CTA(16);
 #undef DF2_WALK_CTA
+        note_launch();
+        return cudaGetLastError();
+    }
+    const size_t ssmem = walk_stream_smem(K, r);
+    if (ssmem <= 200 * 1024) {
+#define DF2_WALK_STREAM(N)                                                                          \
+    do {                                                                                            \
+        cudaError_t e = cudaFuncSetAttribute(walk_stream_kernel<N>,                                 \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(ssmem)); \
+        if (e != cudaSuccess) return e;                                                             \
+        walk_stream_kernel<N><<<unsigned(R), kStreamThreads, ssmem, stream>>>(anchors, B, ids, vals, G, \
+                                                                              A, Bc, V, K, r, path,   \
+                                                                              scores, dev_status);    \
+    } while (0)
+        if (nch <= 1) DF2_WALK_STREAM(1);
+        else if (nch <= 2) DF2_WALK_STREAM(2);
+        else if (nch <= 4) DF2_WALK_STREAM(4);
+        else if (nch <= 8) DF2_WALK_STREAM(8);
+        else DF2_WALK_STREAM(16);
+#undef DF2_WALK_STREAM
         note_launch();
         return cudaGetLastError();
     }

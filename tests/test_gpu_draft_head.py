@@ -63,7 +63,7 @@ def separate(df2, x, status=None):
     (2, 16, 512, 20000, 32, 512),    # K = 32, a 16-CTA cluster
     (2, 8, 520, 9001, 17, 264),      # ragged K, D and r
     (16, 8, 256, 30000, 16, 256),    # 128 positions: the tensor-core GEMM head + fused tail
-    (64, 8, 256, 20000, 16, 256),    # 512 positions: more than one wave, the separate calls
+    (64, 8, 256, 20000, 16, 256),    # 512 positions: 64 clusters
 ])
 def test_fused_equals_separate_calls(df2, R, B, D, V, K, r):
     x = inputs(R * 7 + K + r, R, B, D, V, K, r)
@@ -104,7 +104,7 @@ def test_fused_bad_ids_flagged(df2):
 
 
 def test_fused_repeated_calls_reuse_the_workspace(df2):
-    """The per-request counters are reset by every call's head kernel."""
+    """Calls on a workspace that starts as garbage, repeated, give the same results."""
     x = inputs(7, 2, 8, 512, 8000, 16, 128)
     ws = torch.empty(df2.draft_head_workspace_size(2, 8, 512, 8000, 16, 128), dtype=torch.uint8, device="cuda")
     ws.fill_(0xAB)
