@@ -52,6 +52,7 @@ def load_peaks():
 PROFILES = {
     "batch1": ("head_skinny_kernel_batch1.md", ["head_tc.cu", "topk_warp.cuh", "tc_ptx.cuh", "common.cuh"]),
     "batched": ("gemm_wide_topk_batched.md", ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh"]),
+    "stress": ("gemm_wide_topk_stress.md", ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh"]),
 }
 
 
