@@ -32,8 +32,7 @@ constexpr int WM = 128;  // rows of A per tile (MMA M, TMEM lanes)
 constexpr int WK = 64;   // K elements per box (one 128-byte swizzle row)
 constexpr int kWideThreads = 192;
 constexpr uint32_t kABox = WM * WK * 2;  // 16 KB
-// rows of B per tile (MMA N, TMEM columns): 256, or 192 to leave room for
-// 64-entry heaps next to four pipeline stages
+// rows of B per tile (MMA N, TMEM columns): 256
 constexpr int kWideMaxStages = 8;
 
 enum { EPI_STORE = 0, EPI_TOPK = 1 };
@@ -384,7 +383,13 @@ bool wide_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int wide_bn(int epi, int K) { return (epi == EPI_TOPK && K > 32) ? 192 : 256; }
+// 256 columns for every K: an N = 192 MMA ran at ~79% of the N = 256 rate, which
+// cost more than the fourth pipeline stage the 64-entry heaps displace
+int wide_bn(int epi, int K) {
+    (void)epi;
+    (void)K;
+    return 256;
+}
 
 int wide_stages(int epi, int K) {
     const uint32_t budget = 227 * 1024 - 1024;
@@ -477,8 +482,7 @@ cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, in
     a.n_zero = n_zero;
     cudaError_t e = cudaMemsetAsync(a.thr_g, 0, size_t(M) * 4, stream);
     if (e != cudaSuccess) return e;
-    e = bn == 192 ? launch_wide<EPI_TOPK, 192>(ta, tb, a, a.n_mt * n_groups, stream)
-                  : launch_wide<EPI_TOPK, 256>(ta, tb, a, a.n_mt * n_groups, stream);
+    e = launch_wide<EPI_TOPK, 256>(ta, tb, a, a.n_mt * n_groups, stream);
     if (e != cudaSuccess) return e;
     if (parts_out) {  // the caller folds the per-range lists itself
         *parts_out = TopkParts{a.part_v, a.part_id, n_groups};
