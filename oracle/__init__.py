@@ -70,7 +70,8 @@ class Oracle:
         i64, i32, vp = ct.c_int64, ct.c_int32, ct.c_void_p
         L.df2o_num_threads.restype = ct.c_int
         L.df2o_logits.argtypes = [vp, i64, i64, vp, i64, vp]
-        L.df2o_unary_topk.argtypes = [vp, i64, i64, vp, i64, i32, vp, i32, vp, vp, vp, vp]
+        L.df2o_unary_topk.argtypes = [vp, i64, i64, vp, i64, i32, ct.c_double, ct.c_double, vp, i32, vp, vp,
+                                      vp, vp]
         L.df2o_selector_walk.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp, vp, vp]
         L.df2o_selector_pair_scores.argtypes = [vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp]
         L.df2o_selector_lattice.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp]
@@ -99,8 +100,12 @@ class Oracle:
         self._check(self.lib.df2o_logits(_p(h), P, D, _p(W), V, _p(U)))
         return U
 
-    def unary_topk(self, h, W_lm, K, W_H=None):
-        """Returns (ids [P,K] int32, vals [P,K] f32, margin [P] f64, G [P,r] f32 or None)."""
+    def unary_topk(self, h, W_lm, K, W_H=None, multiplier=1.0, softcap=0.0):
+        """Returns (ids [P,K] int32, vals [P,K] f32, margin [P] f64, G [P,r] f32 or None).
+
+        multiplier and softcap map every logit u to softcap*tanh(multiplier*u/softcap)
+        (multiplier*u when softcap is 0).  They are rounded to fp32 first, the
+        precision the library takes them in."""
         h, W_lm = _c(h, np.uint16), _c(W_lm, np.uint16)
         P, D = h.shape
         V = W_lm.shape[0]
@@ -114,7 +119,8 @@ class Oracle:
             r = W_H.shape[0]
             assert W_H.shape[1] == D
             G = np.empty((P, r), np.float32)
-        self._check(self.lib.df2o_unary_topk(_p(h), P, D, _p(W_lm), V, int(K), _p(W_H), r, _p(G),
+        mul, cap = float(np.float32(multiplier)), float(np.float32(softcap))
+        self._check(self.lib.df2o_unary_topk(_p(h), P, D, _p(W_lm), V, int(K), mul, cap, _p(W_H), r, _p(G),
                                              _p(ids), _p(vals), _p(margin)))
         return ids, vals, margin, G
 

@@ -153,15 +153,31 @@ static int cand_order(const void* pa, const void* pb)
 }
 
 /*
- * Per position p: U[p,.] over all V tokens, a full sort of the V (value, id)
- * pairs, the first K kept.  margin[p] = U_(K) - U_(K+1) (+inf when K == V).
- * When W_H is given, G[p,i] = sum_d h[p,d] * W_H[i,d] (the hidden projection H).
+ * The optional output multiplier and final logit softcap of the unary logits
+ * (SpecForge "DFlash2" concept doc, "Export and serve": both act on the unary
+ * logits; the page gives no formula).  Read as the common forms, the multiplier
+ * first and the cap last ("final"): u -> mul * u, then cap * tanh(u / cap);
+ * cap = 0 means no cap, and mul = 1, cap = 0 leaves the logits as they are.
+ */
+static double logit_map(double u, double mul, double cap)
+{
+    const double x = mul * u;
+    return cap > 0.0 ? cap * tanh(x / cap) : x;
+}
+
+/*
+ * Per position p: U[p,.] over all V tokens, each mapped by logit_map, a full
+ * sort of the V (value, id) pairs, the first K kept.  margin[p] = U_(K) -
+ * U_(K+1) of the mapped values (+inf when K == V).  When W_H is given,
+ * G[p,i] = sum_d h[p,d] * W_H[i,d] (the hidden projection H).  mul must be
+ * finite and > 0, cap finite and >= 0.
  */
 int df2o_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm, int64_t V,
-                    int32_t K, const uint16_t* W_H, int32_t r, float* G, int32_t* ids,
-                    float* vals, double* margin)
+                    int32_t K, double mul, double cap, const uint16_t* W_H, int32_t r, float* G,
+                    int32_t* ids, float* vals, double* margin)
 {
     if (P < 0 || D < 1 || V < 1 || K < 1 || K > V) return DF2O_INVALID;
+    if (!(mul > 0.0) || !isfinite(mul) || !(cap >= 0.0) || !isfinite(cap)) return DF2O_INVALID;
     if (W_H && (r < 1 || !G)) return DF2O_INVALID;
     int failed = 0;
     int64_t p;
@@ -177,7 +193,7 @@ int df2o_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_l
             double acc = 0.0;
             for (int64_t d = 0; d < D; ++d)
                 acc += bf16_value(h[p * D + d]) * bf16_value(W_lm[v * D + d]);
-            c[v].val = (float)acc;
+            c[v].val = (float)logit_map(acc, mul, cap);
             c[v].id = (int32_t)v;
         }
         qsort(c, (size_t)V, sizeof(cand_t), cand_order);

@@ -164,6 +164,91 @@ def pin_topk_hidden_projection(o):
     assert np.array_equal(G2, h.astype(np.float32))
 
 
+# ------------------------------------------- logit multiplier / softcap --
+# The pages name an optional output multiplier m and a final logit softcap c
+# applied to the unary logits; the reading pinned here is u -> c*tanh(m*u/c)
+# (m*u when c = 0), the multiplier first and the cap last.
+
+def pin_softcap_worked_values(o):
+    """tanh(ln(3)/2) = 1/2 exactly, so with m = ln 3 and c = 2 a logit of 1 maps to
+    1; halving the argument gives 2*(2 - sqrt 3); quartering it 2*(3^(1/4) - 1)/(3^(1/4) + 1);
+    the map is odd.  h = e_0 puts the chosen logits in column 0 of W_lm."""
+    col = [0.25, -1.0, 0.5, 0.0, -0.5, 1.0]
+    V, D = len(col), 4
+    W = np.zeros((V, D), np.float32)
+    W[:, 0] = col
+    h = np.zeros((1, D), np.float32)
+    h[0, 0] = 1.0
+    ids, vals, margin, _ = o.unary_topk(bf(h), bf(W), V, multiplier=math.log(3.0), softcap=2.0)
+    q = 3.0 ** 0.25
+    half, quarter = 4.0 - 2.0 * math.sqrt(3.0), 2.0 * (q - 1.0) / (q + 1.0)
+    assert ids[0].tolist() == [5, 2, 0, 3, 4, 1], ids
+    want = [1.0, half, quarter, 0.0, -half, -1.0]
+    assert np.allclose(vals[0].astype(np.float64), want, rtol=0, atol=1e-6), (vals, want)
+    assert margin[0] == math.inf
+
+
+def pin_softcap_saturates_before_selection(o):
+    """m*u/c >= 32 for every logit: tanh rounds to exactly 1 in double precision,
+    every mapped logit equals c, and the top-K falls to the tie rule: the K lowest
+    token ids, whatever their raw order; margin 0.  Shows the cap is applied to all
+    V logits before the selection, not to the K kept ones."""
+    rng = _rng("saturate")
+    V, D, K = 40, 4, 6
+    W = np.zeros((V, D), np.float32)
+    W[:, 1] = rng.integers(1, 9, size=V) * 0.25      # logits in [0.25, 2], exact in bf16
+    h = np.zeros((2, D), np.float32)
+    h[:, 1] = 1.0
+    ids, vals, margin, _ = o.unary_topk(bf(h), bf(W), K, multiplier=64.0, softcap=0.5)
+    for p in range(2):
+        assert ids[p].tolist() == list(range(K)), ids[p]
+        assert np.all(vals[p] == np.float32(0.5))
+        assert margin[p] == 0.0
+    assert np.argsort(-W[:, 1], kind="stable")[:K].tolist() != list(range(K))
+
+
+def _series_softcap(x, c):
+    """c*tanh(x/c) by its Taylor series in x/c (|x/c| <= 1/16 here: terms past the
+    fourth are below 1e-9 of x)."""
+    t = x / c
+    return c * (t - t ** 3 / 3.0 + 2.0 * t ** 5 / 15.0 - 17.0 * t ** 7 / 315.0)
+
+
+def pin_softcap_small_argument_series(o):
+    """Exact logits (multiples of 1/4, computed with integers) and m*|u| <= 3 under
+    a cap of 64: the values follow the tanh series, the ids follow the brute-force
+    order of the raw logits (the map is increasing and keeps ties), and with no
+    cap the values are m*u exactly."""
+    rng = _rng("series")
+    P, V, D, K = 3, 30, 8, 9
+    h = rng.integers(-2, 3, size=(P, D))
+    W = rng.integers(-2, 3, size=(V, D))
+    U = (h @ W.T) * 0.25 * 0.5                       # exact: h/2 and W/4 as bf16 operands
+    m, c = 0.375, 64.0
+    ids, vals, _, _ = o.unary_topk(bf(h * 0.5), bf(W * 0.25), K, multiplier=m, softcap=c)
+    ids0, vals0, _, _ = o.unary_topk(bf(h * 0.5), bf(W * 0.25), K, multiplier=m)
+    for p in range(P):
+        order = sorted(range(V), key=lambda v: (-U[p, v], v))[:K]
+        assert ids[p].tolist() == order and ids0[p].tolist() == order
+        x = m * U[p, order]
+        assert np.allclose(vals[p].astype(np.float64), _series_softcap(x, c), rtol=0, atol=1e-6)
+        assert np.array_equal(vals0[p], (x).astype(np.float32))
+        assert np.all(np.abs(vals[p]) <= c)
+
+
+def pin_softcap_rejects_bad_parameters(o):
+    """The multiplier must be finite and positive, the cap finite and >= 0."""
+    h = bf(np.eye(4)[:1])
+    W = bf(np.eye(4))
+    for m, c in [(0.0, 0.0), (-1.0, 0.0), (math.nan, 0.0), (math.inf, 1.0), (1.0, -1.0), (1.0, math.inf),
+                 (1.0, math.nan)]:
+        try:
+            o.unary_topk(h, W, 2, multiplier=m, softcap=c)
+        except ValueError:
+            continue
+        raise AssertionError(f"multiplier={m} softcap={c} accepted")
+
+
 # ------------------------------------------------------------ walk (o3/o4) --
 
 def _walk_fixture(o, name):

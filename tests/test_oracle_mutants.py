@@ -11,7 +11,8 @@ import pytest
 import oracle
 import oracle_pins
 
-# (name, original text, replacement).  Every original must occur exactly once.
+# (name, original text, replacement) or (name, [(original, replacement), ...]).
+# Every original must occur exactly once.
 MUTANTS = [
     ("topk_tie_toward_higher_id",
      "return (a->id > b->id) - (a->id < b->id);", "return (a->id < b->id) - (a->id > b->id);"),
@@ -69,6 +70,17 @@ MUTANTS = [
      "if (below + w[j] > u * total) {", "if (below + w[j] > (1.0 - u) * total) {"),
     ("sampling_margin_wrong_end",
      "if (pick > 0) mg = u - lo / total;", "if (pick > 0) mg = u - hi / total;"),
+    ("softcap_no_outer_cap",
+     "return cap > 0.0 ? cap * tanh(x / cap) : x;", "return cap > 0.0 ? tanh(x / cap) : x;"),
+    ("softcap_multiplier_after_cap",
+     "return cap > 0.0 ? cap * tanh(x / cap) : x;", "return cap > 0.0 ? mul * cap * tanh(u / cap) : x;"),
+    ("softcap_multiplier_dropped", "const double x = mul * u;", "const double x = u;"),
+    ("softcap_scaled_not_divided",
+     "return cap > 0.0 ? cap * tanh(x / cap) : x;", "return cap > 0.0 ? cap * tanh(x * cap) : x;"),
+    ("softcap_after_selection", [
+        ("c[v].val = (float)logit_map(acc, mul, cap);", "c[v].val = (float)acc;"),
+        ("vals[p * K + j] = c[j].val;", "vals[p * K + j] = (float)logit_map(c[j].val, mul, cap);")]),
+    ("softcap_accepts_negative_multiplier", "if (!(mul > 0.0) ||", "if (!(mul != 0.0) ||"),
 ]
 
 
@@ -78,11 +90,20 @@ def source():
         return f.read()
 
 
-@pytest.mark.parametrize("name,orig,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_mutant_is_caught(tmp_path, source, name, orig, repl):
-    assert source.count(orig) == 1, f"mutation site for {name} not unique/found"
+def _sites(m):
+    """A mutant's (original, replacement) pairs: one site, or a list of them."""
+    return m[1] if len(m) == 2 else [(m[1], m[2])]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, source, mutant):
+    name = mutant[0]
+    mutated = source
+    for orig, repl in _sites(mutant):
+        assert source.count(orig) == 1, f"mutation site for {name} not unique/found"
+        mutated = mutated.replace(orig, repl)
     src = tmp_path / f"{name}.c"
-    src.write_text(source.replace(orig, repl))
+    src.write_text(mutated)
     lib = oracle.build(str(src), str(tmp_path / f"lib{name}.so"), force=True)
     o = oracle.Oracle(lib)
     failed = []
