@@ -161,7 +161,8 @@ def time_per_call(step, torch, n):
 
 def time_next_rows(step, torch, df2, iters=20):
     """Per-call times of the lattice schedule on the step's own candidates: the table,
-    then the greedy and the sampling walk over it (not part of the timed step)."""
+    then the greedy and the sampling walk over it; then the draft head with capped
+    logits (multiplier 1, softcap 30).  None of it is part of the timed step."""
     w = step.w
     lat = torch.empty((w.R, w.B - 1, w.K, w.K), dtype=torch.float32, device=step.ids.device)
     gen = torch.Generator(device=step.ids.device)
@@ -173,6 +174,9 @@ def time_next_rows(step, torch, df2, iters=20):
         lambda: df2.selector_lattice(step.anchors, step.ids, step.vals, step.Gt, step.A, step.Bc, w.B, out=lat),
         lambda: df2.lattice_walk(lat, step.ids, w.B, w.V, out=(path, sc)),
         lambda: df2.lattice_walk(lat, step.ids, w.B, w.V, uniforms=u, temperature=1.0, out=(path, sc)),
+        lambda: df2.draft_head(step.h, step.W_lm, w.K, step.W_H, step.A, step.Bc, step.anchors, w.B, step.pred,
+                               output_multiplier=1.0, final_logit_softcapping=30.0, workspace=step.ws_draft,
+                               out=(step.ids, step.vals, step.Gt, step.path, step.pscore, step.scores)),
     ]
     for c in calls:
         c()
@@ -496,10 +500,11 @@ def gpu_arm(args, w, rank, world, torch):
                          "finish": conv_bytes(w, "finish") / (per_call_us[1] * 1e-6) / 1e9},
             "roofline": roof,
             "next_rows": {
-                "note": "the lattice schedule, timed on the step's candidates outside the timed step",
+                "note": "the lattice schedule and the capped-logit draft head, timed on the step's inputs outside the timed step",
                 "selector_lattice_us": next_us[0],
                 "lattice_walk_greedy_us": next_us[1],
                 "lattice_walk_sampling_us": next_us[2],
+                "draft_head_softcap_us": next_us[3],
                 "lattice_gbs": lattice_bytes(w) / (next_us[0] * 1e-6) / 1e9,
                 "lattice_tflops": lattice_flops(w) / (next_us[0] * 1e-6) / 1e12,
             },

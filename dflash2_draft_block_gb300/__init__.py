@@ -82,8 +82,12 @@ def unary_topk_workspace_size(P, D, V, K, r=0) -> int:
     return int(lib().dflash2_unary_topk_workspace_size(P, D, V, K, r))
 
 
-def unary_topk(h, W_lm, K, W_H=None, *, workspace=None, dev_status=None, out=None, stream=None):
-    """Top-K unary logits per row of h, and G = h W_H^T.  Returns (ids, vals, G)."""
+def unary_topk(h, W_lm, K, W_H=None, *, output_multiplier=1.0, final_logit_softcapping=0.0,
+               workspace=None, dev_status=None, out=None, stream=None):
+    """Top-K unary logits per row of h, and G = h W_H^T.  Returns (ids, vals, G).
+
+    output_multiplier m and final_logit_softcapping c map each logit u to
+    c*tanh(m*u/c) (m*u when c = 0) before the selection; the defaults leave it."""
     _need(h, "h", torch.bfloat16, 2)
     _need(W_lm, "W_lm", torch.bfloat16, 2)
     P, D = h.shape
@@ -104,14 +108,16 @@ def unary_topk(h, W_lm, K, W_H=None, *, workspace=None, dev_status=None, out=Non
     else:
         ids, vals, G = out
     ws = _workspace(unary_topk_workspace_size(P, D, V, K, r), workspace, dev)
-    rc = lib().dflash2_unary_topk(_p(h), P, D, _p(W_lm), V, int(K), _p(W_H), r, _p(G), _p(ids),
+    rc = lib().dflash2_unary_topk(_p(h), P, D, _p(W_lm), V, int(K), float(output_multiplier),
+                                  float(final_logit_softcapping), _p(W_H), r, _p(G), _p(ids),
                                   _p(vals), _p(ws), 0 if ws is None else ws.numel(),
                                   _p(dev_status), _stream(stream))
     _check("dflash2_unary_topk", rc)
     return ids, vals, G
 
 
-def unary_topk_noalloc(h, W_lm, K, W_H=None, *, dev_status=None, out=None, stream=None):
+def unary_topk_noalloc(h, W_lm, K, W_H=None, *, output_multiplier=1.0, final_logit_softcapping=0.0,
+                       dev_status=None, out=None, stream=None):
     """unary_topk without a workspace: for callers that may not allocate device
     memory during a call.  Scratch comes from a fixed array inside the library
     (DF2_NOALLOC_SCRATCH_BYTES per GPU), shared by every call, so calls must not
@@ -126,7 +132,8 @@ def unary_topk_noalloc(h, W_lm, K, W_H=None, *, dev_status=None, out=None, strea
         G = torch.empty((P, r), dtype=torch.float32, device=h.device) if r else None
     else:
         ids, vals, G = out
-    rc = lib().dflash2_unary_topk_noalloc(_p(h), P, D, _p(W_lm), W_lm.shape[0], int(K), _p(W_H), r,
+    rc = lib().dflash2_unary_topk_noalloc(_p(h), P, D, _p(W_lm), W_lm.shape[0], int(K),
+                                          float(output_multiplier), float(final_logit_softcapping), _p(W_H), r,
                                           _p(G), _p(ids), _p(vals), _p(dev_status), _stream(stream))
     _check("dflash2_unary_topk_noalloc", rc)
     return ids, vals, G
@@ -187,8 +194,8 @@ def draft_head_workspace_size(R, B, D, V, K, r) -> int:
     return int(lib().dflash2_draft_head_workspace_size(R, B, D, V, K, r))
 
 
-def draft_head(h, W_lm, K, W_H, A, Bc, anchors, block_size, pred=None, *, workspace=None,
-               dev_status=None, out=None, stream=None):
+def draft_head(h, W_lm, K, W_H, A, Bc, anchors, block_size, pred=None, *, output_multiplier=1.0,
+               final_logit_softcapping=0.0, workspace=None, dev_status=None, out=None, stream=None):
     """Unary top-K, G = H(h), the greedy walk and (pred given) the teacher-forced
     scores of one draft block in one call.  Returns (ids, vals, G, path, path_scores,
     pair_scores or None)."""
@@ -222,7 +229,8 @@ def draft_head(h, W_lm, K, W_H, A, Bc, anchors, block_size, pred=None, *, worksp
     need = draft_head_workspace_size(R, B, D, V, K, r)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    rc = lib().dflash2_draft_head(_p(h), R, B, D, _p(W_lm), V, K, _p(W_H), r, _p(A), _p(Bc), _p(anchors),
+    rc = lib().dflash2_draft_head(_p(h), R, B, D, _p(W_lm), V, K, float(output_multiplier),
+                                  float(final_logit_softcapping), _p(W_H), r, _p(A), _p(Bc), _p(anchors),
                                   _p(pred), _p(ids), _p(vals), _p(G), _p(path), _p(ps), _p(pair),
                                   _p(workspace), workspace.numel(), _p(dev_status), _stream(stream))
     _check("dflash2_draft_head", rc)

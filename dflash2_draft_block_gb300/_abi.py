@@ -11,23 +11,24 @@ import threading
 
 from .build import INCLUDE, LIB
 
-_i64, _i32, _int, _vp, _sz = ct.c_int64, ct.c_int32, ct.c_int, ct.c_void_p, ct.c_size_t
+_i64, _i32, _int, _vp, _sz, _f32 = ct.c_int64, ct.c_int32, ct.c_int, ct.c_void_p, ct.c_size_t, ct.c_float
 
 SIGNATURES = {
     "dflash2_status_string": (ct.c_char_p, [_int]),
     "dflash2_abi_version": (_int, []),
     "dflash2_kernels_launched": (ct.c_longlong, []),
     "dflash2_unary_topk_workspace_size": (_sz, [_i64, _i64, _i64, _int, _int]),
-    "dflash2_unary_topk": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp,
-                                  _sz, _vp, _vp]),
-    "dflash2_unary_topk_noalloc": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _vp, _int, _vp, _vp,
-                                          _vp, _vp, _vp]),
+    "dflash2_unary_topk": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _f32, _f32, _vp, _int, _vp, _vp, _vp,
+                                  _vp, _sz, _vp, _vp]),
+    "dflash2_unary_topk_noalloc": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _f32, _f32, _vp, _int, _vp,
+                                          _vp, _vp, _vp, _vp]),
     "dflash2_selector_walk": (_int, [_vp, _int, _int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _vp,
                                      _vp, _vp, _vp]),
     "dflash2_selector_pair_scores": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int,
                                             _vp, _vp, _vp]),
     "dflash2_draft_head_workspace_size": (_sz, [_int, _int, _i64, _i64, _int, _int]),
-    "dflash2_draft_head": (_int, [_vp, _int, _int, _i64, _vp, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp,
+    "dflash2_draft_head": (_int, [_vp, _int, _int, _i64, _vp, _i64, _int, _f32, _f32, _vp, _int, _vp, _vp,
+                                  _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "dflash2_selector_lattice": (_int, [_vp, _int, _int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int,
                                         _vp, _vp, _vp]),

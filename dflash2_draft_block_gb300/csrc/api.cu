@@ -10,7 +10,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 int num_sms_current() {
     int dev = 0;
@@ -25,6 +25,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? DF2_OK : DF2_ERR_CUDA; }
 
 size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+// The unary logits' output multiplier (finite, > 0) and final softcap (finite,
+// >= 0; 0 = none) as the map the top-K kernels apply to the values they keep.
+bool make_logit_map(float mul, float cap, df2::LogitMap* lm) {
+    if (!(mul > 0.f) || !(mul <= FLT_MAX) || !(cap >= 0.f) || !(cap <= FLT_MAX)) return false;
+    lm->mul = mul;
+    lm->cap = cap;
+    return true;
+}
 
 }  // namespace
 
@@ -93,12 +102,15 @@ DF2_API size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V
 }
 
 DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,
-                               int64_t V, int K, const uint16_t* W_H, int r, float* G,
+                               int64_t V, int K, float output_multiplier,
+                               float final_logit_softcapping, const uint16_t* W_H, int r, float* G,
                                int32_t* topk_ids, float* topk_vals, void* workspace,
                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
     const bool has_wh = W_H != nullptr;
     int rc = check_head(P, D, V, K, r, has_wh);
     if (rc != DF2_OK) return rc;
+    df2::LogitMap lm;
+    if (!make_logit_map(output_multiplier, final_logit_softcapping, &lm)) return DF2_ERR_INVALID_ARGUMENT;
     if (P == 0) return DF2_OK;
     if (!h || !W_lm || !topk_ids || !topk_vals || (has_wh && !G)) return DF2_ERR_INVALID_ARGUMENT;
     if (!aligned16(h) || !aligned16(W_lm) || !aligned16(topk_ids) || !aligned16(topk_vals) ||
@@ -110,23 +122,27 @@ DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const ui
     const HeadPath path = pick_head(P, D, V, K);
     const size_t need = round_up(head_workspace(path, P, D, V, K, sms), 256);
     if (workspace_bytes < need || (need > 0 && !workspace)) return DF2_ERR_WORKSPACE_TOO_SMALL;
-    if (path == HeadPath::Skinny) {
-        rc = df2::head_tc_launch(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
-                                 dev_status, sms, st);
-        return rc;
-    }
-    if (path == HeadPath::Wide) {
-        cudaError_t e = df2::wide_topk_launch(h, P, W_lm, V, D, K, topk_ids, topk_vals, workspace,
-                                              dev_status, sms, st);
-        if (e != cudaSuccess) return DF2_ERR_CUDA;
-        if (has_wh) {
-            e = df2::wide_store_launch(h, P, W_H, r, D, G, r, r, G, r, dev_status, st);
+    if (path == HeadPath::Skinny || path == HeadPath::Wide) {
+        // the head leaves its sorted per-CTA lists; the merge folds them and maps the kept values
+        df2::TopkParts parts{};
+        if (path == HeadPath::Skinny) {
+            rc = df2::head_tc_launch(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
+                                     dev_status, sms, st, -1, &parts);
+            if (rc != DF2_OK) return rc;
+        } else {
+            cudaError_t e = df2::wide_topk_launch(h, P, W_lm, V, D, K, topk_ids, topk_vals, workspace,
+                                                  dev_status, sms, st, &parts);
             if (e != cudaSuccess) return DF2_ERR_CUDA;
+            if (has_wh) {
+                e = df2::wide_store_launch(h, P, W_H, r, D, G, r, r, G, r, dev_status, st);
+                if (e != cudaSuccess) return DF2_ERR_CUDA;
+            }
         }
-        return DF2_OK;
+        return from_cuda(df2::topk_merge_sorted_launch(parts.v, parts.id, parts.S, P, K, topk_ids, topk_vals,
+                                                       st, lm));
     }
     cudaError_t e = df2::head_simple_launch(h, P, D, W_lm, V, K, topk_ids, topk_vals, workspace,
-                                            sms, st);
+                                            sms, st, lm);
     if (e != cudaSuccess) return DF2_ERR_CUDA;
     if (has_wh) {
         e = df2::gemm_simple_launch(h, false, W_H, P, r, D, G, r, r, G, r, st);
@@ -168,7 +184,8 @@ DF2_API size_t dflash2_draft_head_workspace_size(int R, int B, int64_t D, int64_
 }
 
 DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const uint16_t* W_lm,
-                               int64_t V, int K, const uint16_t* W_H, int r, const uint16_t* A,
+                               int64_t V, int K, float output_multiplier,
+                               float final_logit_softcapping, const uint16_t* W_H, int r, const uint16_t* A,
                                const uint16_t* Bc, const int32_t* anchors, const int32_t* pred,
                                int32_t* topk_ids, float* topk_vals, float* G, int32_t* path,
                                float* path_scores, float* pair_scores, void* workspace,
@@ -177,6 +194,8 @@ DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const
     const int64_t P = int64_t(R) * B;
     int rc = check_head(P, D, V, K, r, true);
     if (rc != DF2_OK) return rc;
+    df2::LogitMap lm;
+    if (!make_logit_map(output_multiplier, final_logit_softcapping, &lm)) return DF2_ERR_INVALID_ARGUMENT;
     if (r > DF2_MAX_RANK || r % 8 != 0) return DF2_ERR_UNSUPPORTED;
     if (R == 0) return DF2_OK;
     if (!h || !W_lm || !W_H || !A || !Bc || !anchors || !topk_ids || !topk_vals || !G || !path ||
@@ -193,8 +212,8 @@ DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const
     if (workspace_bytes < need || !workspace) return DF2_ERR_WORKSPACE_TOO_SMALL;
     if (!draft_fused(hp, P, B, D, V, K, r, sms)) {
         // the separate calls, in order
-        rc = dflash2_unary_topk(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, workspace,
-                                workspace_bytes, dev_status, stream);
+        rc = dflash2_unary_topk(h, P, D, W_lm, V, K, output_multiplier, final_logit_softcapping, W_H, r, G,
+                                topk_ids, topk_vals, workspace, workspace_bytes, dev_status, stream);
         if (rc != DF2_OK) return rc;
         rc = dflash2_selector_walk(anchors, R, B, topk_ids, topk_vals, G, A, Bc, V, K, r, path,
                                    path_scores, dev_status, stream);
@@ -215,7 +234,7 @@ DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const
         if (e != cudaSuccess) return DF2_ERR_CUDA;
     }
     return from_cuda(df2::draft_tail_launch(parts, P, K, topk_ids, topk_vals, anchors, B, G, A, Bc, V,
-                                            r, path, path_scores, pred, pair_scores, dev_status, st));
+                                            r, path, path_scores, pred, pair_scores, dev_status, st, lm));
 }
 
 // -------------------------------------------------------------- selector --

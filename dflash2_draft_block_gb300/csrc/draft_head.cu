@@ -61,7 +61,7 @@ draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part
                   const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int r,
                   int32_t* __restrict__ path, float* __restrict__ path_scores,
                   const int32_t* __restrict__ pred, float* __restrict__ pair_scores,
-                  int32_t* __restrict__ dev_status, unsigned tab_off) {
+                  int32_t* __restrict__ dev_status, unsigned tab_off, LogitMap lm) {
     extern __shared__ __align__(16) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
     const int t = int(cluster.block_rank());
@@ -75,7 +75,7 @@ draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part
     float* tab_v = reinterpret_cast<float*>(tab_id + T * K);
     int* tab_bad = reinterpret_cast<int*>(tab_v + T * K);
 
-    mrg::merge_position<R>(part_v, part_id, S, P, K, p, ids, vals, smem);
+    mrg::merge_position<R>(part_v, part_id, S, P, K, p, ids, vals, smem, lm);
     __syncthreads();  // row p's list is written (by warp 0) and smem is free again
     const int32_t pid = pred ? __ldg(pred + p) : -1;
     const bool pred_ok = pid >= 0 && pid < V;
@@ -144,7 +144,7 @@ cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, cons
                         int32_t* ids, float* vals, const int32_t* anchors, const float* G,
                         const uint16_t* A, const uint16_t* Bc, int64_t V, int r, int32_t* path,
                         float* path_scores, const int32_t* pred, float* pair_scores, int32_t* dev_status,
-                        bool probe_only, bool* fits) {
+                        LogitMap lm, bool probe_only, bool* fits) {
     auto kernel = draft_tail_kernel<R, N>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
@@ -172,20 +172,21 @@ cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, cons
     }
     return cudaLaunchKernelEx(&cfg, kernel, parts.v, parts.id, parts.S, P, K, ids, vals, anchors, B, G, A,
                               Bc, V, r, path, path_scores, pred, pair_scores, dev_status,
-                              unsigned(tail_tab_off(K, r, parts.S)));
+                              unsigned(tail_tab_off(K, r, parts.S)), lm);
 }
 
 // Runs (or, probe_only, checks that the cluster shape can run) the right instance.
 cudaError_t dispatch_tail(bool probe_only, bool* fits, const TopkParts& parts, int64_t P, int K, int32_t* ids,
                           float* vals, const int32_t* anchors, int B, const float* G, const uint16_t* A,
                           const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
-                          const int32_t* pred, float* pair_scores, int32_t* dev_status, cudaStream_t stream) {
+                          const int32_t* pred, float* pair_scores, int32_t* dev_status, LogitMap lm,
+                          cudaStream_t stream) {
     const size_t smem = tail_smem(B, K, r, parts.S);
     const int nch = (r + 255) / 256;
     cudaError_t e = cudaSuccess;
 #define DF2_TAIL(RV, N)                                                                                \
     e = launch_tail<RV, N>(P, B, smem, stream, parts, K, ids, vals, anchors, G, A, Bc, V, r, path,     \
-                           path_scores, pred, pair_scores, dev_status, probe_only, fits)
+                           path_scores, pred, pair_scores, dev_status, lm, probe_only, fits)
 #define DF2_TAIL_N(RV)                        \
     do {                                      \
         if (nch <= 1) DF2_TAIL(RV, 1);        \
@@ -212,7 +213,7 @@ bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
     bool fits = false;
     const TopkParts probe{nullptr, nullptr, S};
     if (dispatch_tail(true, &fits, probe, P, K, nullptr, nullptr, nullptr, B, nullptr, nullptr, nullptr, 1, r,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, nullptr) != cudaSuccess)
+                      nullptr, nullptr, nullptr, nullptr, nullptr, LogitMap{}, nullptr) != cudaSuccess)
         return false;
     return fits;
 }
@@ -221,10 +222,10 @@ cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t*
                               const int32_t* anchors, int B, const float* G, const uint16_t* A,
                               const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
                               const int32_t* pred, float* pair_scores, int32_t* dev_status,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, LogitMap lm) {
     bool unused = false;
     const cudaError_t e = dispatch_tail(false, &unused, parts, P, K, ids, vals, anchors, B, G, A, Bc, V, r, path,
-                                        path_scores, pred, pair_scores, dev_status, stream);
+                                        path_scores, pred, pair_scores, dev_status, lm, stream);
     note_launch();
     return e;
 }

@@ -109,7 +109,8 @@ constexpr int kMergeChunk = 4096;
 
 __global__ void __launch_bounds__(kThreads)
 topk_merge_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id, int S,
-                  int64_t P, int K, int32_t* __restrict__ out_ids, float* __restrict__ out_vals) {
+                  int64_t P, int K, int32_t* __restrict__ out_ids, float* __restrict__ out_vals,
+                  LogitMap lm) {
     extern __shared__ __align__(16) uint8_t smem[];
     float* cv_s = reinterpret_cast<float*>(smem);                       // [kMergeChunk]
     int* ci_s = reinterpret_cast<int*>(cv_s + kMergeChunk);             // [kMergeChunk]
@@ -154,7 +155,7 @@ topk_merge_kernel(const float* __restrict__ part_v, const int* __restrict__ part
         if (lane == 0) counts[0] = list.n;
     }
     __syncthreads();
-    write_sorted(lv, lid, counts[0], K, out_ids + p * K, out_vals + p * K, threadIdx.x, kThreads);
+    write_sorted(lv, lid, counts[0], K, out_ids + p * K, out_vals + p * K, threadIdx.x, kThreads, lm);
 }
 
 struct SimplePlan {
@@ -200,7 +201,7 @@ size_t head_simple_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms
 
 cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V,
                                int K, int32_t* ids, float* vals, void* ws, int num_sms,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, LogitMap lm) {
     SimplePlan pl = plan_simple(P, D, V, K, num_sms);
     float* part_v = reinterpret_cast<float*>(ws);
     int* part_id = reinterpret_cast<int*>(part_v + size_t(pl.S) * P * K);
@@ -225,16 +226,16 @@ cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const ui
     note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return topk_merge_launch(part_v, part_id, pl.S, P, K, ids, vals, stream);
+    return topk_merge_launch(part_v, part_id, pl.S, P, K, ids, vals, stream, lm);
 }
 
 cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
-                              int32_t* ids, float* vals, cudaStream_t stream) {
+                              int32_t* ids, float* vals, cudaStream_t stream, LogitMap lm) {
     const size_t msmem = size_t(kMergeChunk) * 8 + size_t(8) * K * 8 + 64;
     cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(msmem));
     if (e != cudaSuccess) return e;
-    topk_merge_kernel<<<unsigned(P), kThreads, msmem, stream>>>(part_v, part_id, S, P, K, ids, vals);
+    topk_merge_kernel<<<unsigned(P), kThreads, msmem, stream>>>(part_v, part_id, S, P, K, ids, vals, lm);
     note_launch();
     return cudaGetLastError();
 }

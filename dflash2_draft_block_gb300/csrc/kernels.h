@@ -7,16 +7,30 @@
 
 namespace df2 {
 
+// The unary logits' output multiplier and final softcap: u -> cap * tanh(mul * u / cap),
+// or mul * u when cap == 0 (the defaults leave every value bit for bit as it is).
+// With mul > 0 the map is increasing, so the kernels select on the raw logits
+// and map only the K values they keep.
+struct LogitMap {
+    float mul = 1.f;
+    float cap = 0.f;
+    __device__ __forceinline__ float operator()(float u) const {
+        const float x = mul * u;
+        return cap > 0.f ? cap * tanhf(x / cap) : x;
+    }
+};
+
 // ---- unary logits + top-K on the CUDA cores (any D % 8 == 0, K <= DF2_MAX_TOPK)
 bool head_simple_supported(int64_t D, int K);
 size_t head_simple_workspace(int64_t P, int64_t D, int64_t V, int K, int num_sms);
 cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, int64_t V,
                                int K, int32_t* ids, float* vals, void* ws, int num_sms,
-                               cudaStream_t stream);
+                               cudaStream_t stream, LogitMap lm = LogitMap{});
 
-// ---- S unsorted partial lists [S][P][K] (id -1 = empty slot) -> sorted top-K [P][K]
+// ---- S unsorted partial lists [S][P][K] (id -1 = empty slot) -> sorted top-K [P][K],
+//      the kept values mapped by lm
 cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
-                              int32_t* ids, float* vals, cudaStream_t stream);
+                              int32_t* ids, float* vals, cudaStream_t stream, LogitMap lm = LogitMap{});
 
 // ---- S partial lists [S][P][K], each in rank order (id -1 = empty), K <= 64 -> top-K [P][K]
 struct TopkParts {
@@ -25,7 +39,8 @@ struct TopkParts {
     int S;
 };
 cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
-                                     int32_t* ids, float* vals, cudaStream_t stream);
+                                     int32_t* ids, float* vals, cudaStream_t stream,
+                                     LogitMap lm = LogitMap{});
 
 // ---- out = X . W^T on the CUDA cores, columns split between two outputs
 cudaError_t gemm_simple_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
@@ -79,7 +94,7 @@ cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t*
                               const int32_t* anchors, int B, const float* G, const uint16_t* A,
                               const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
                               const int32_t* pred, float* pair_scores, int32_t* dev_status,
-                              cudaStream_t stream);
+                              cudaStream_t stream, LogitMap lm = LogitMap{});
 
 // ---- conv: y = sum_{j<taps, t-j>=0} (base[j] + dyn[p, j, c/g]) * x[p-j]
 // ---- conv prepare for few rows (P <= 64, B <= 16): projection and apply fused

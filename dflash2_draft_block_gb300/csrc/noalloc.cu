@@ -46,8 +46,9 @@ int scratch_for_current_device(void** out) {
 }  // namespace
 
 DF2_API int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D,
-                                       const uint16_t* W_lm, int64_t V, int K,
-                                       const uint16_t* W_H, int r, float* G, int32_t* topk_ids,
+                                       const uint16_t* W_lm, int64_t V, int K, float output_multiplier,
+                                       float final_logit_softcapping, const uint16_t* W_H, int r,
+                                       float* G, int32_t* topk_ids,
                                        float* topk_vals, int32_t* dev_status, void* stream) {
     const size_t need = dflash2_unary_topk_workspace_size(P, D, V, K, r);
     if (need > DF2_NOALLOC_SCRATCH_BYTES) return DF2_ERR_UNSUPPORTED;
@@ -56,6 +57,7 @@ DF2_API int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D,
         const int rc = scratch_for_current_device(&scratch);
         if (rc != DF2_OK) return rc;
     }
-    return dflash2_unary_topk(h, P, D, W_lm, V, K, W_H, r, G, topk_ids, topk_vals, scratch,
+    return dflash2_unary_topk(h, P, D, W_lm, V, K, output_multiplier, final_logit_softcapping, W_H, r, G,
+                              topk_ids, topk_vals, scratch,
                               scratch ? DF2_NOALLOC_SCRATCH_BYTES : 0, dev_status, stream);
 }

@@ -14,15 +14,15 @@ template <int R>
 __global__ void __launch_bounds__(kMergeThreads)
 topk_merge_sorted_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id, int S,
                          int64_t P, int K, int32_t* __restrict__ out_ids,
-                         float* __restrict__ out_vals) {
+                         float* __restrict__ out_vals, LogitMap lm) {
     extern __shared__ __align__(16) uint8_t smem[];
-    merge_position<R>(part_v, part_id, S, P, K, blockIdx.x, out_ids, out_vals, smem);
+    merge_position<R>(part_v, part_id, S, P, K, blockIdx.x, out_ids, out_vals, smem, lm);
 }
 
 }  // namespace
 
 cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
-                                     int32_t* ids, float* vals, cudaStream_t stream) {
+                                     int32_t* ids, float* vals, cudaStream_t stream, LogitMap lm) {
     const size_t smem = merge_smem(S, K);
     cudaError_t e;
     if (K <= 32) {
@@ -30,13 +30,13 @@ cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, in
                                  int(smem));
         if (e != cudaSuccess) return e;
         topk_merge_sorted_kernel<1><<<unsigned(P), kWarps * 32, smem, stream>>>(part_v, part_id, S, P, K,
-                                                                                ids, vals);
+                                                                                ids, vals, lm);
     } else {
         e = cudaFuncSetAttribute(topk_merge_sorted_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem));
         if (e != cudaSuccess) return e;
         topk_merge_sorted_kernel<2><<<unsigned(P), kWarps * 32, smem, stream>>>(part_v, part_id, S, P, K,
-                                                                                ids, vals);
+                                                                                ids, vals, lm);
     }
     note_launch();
     return cudaGetLastError();

@@ -27,12 +27,13 @@ __host__ __device__ inline size_t merge_smem(int S, int K) { return size_t(S) * 
 
 // The final top-K of position p from the S sorted lists part_[v|id][s][P][K], by
 // one CTA of kMergeThreads threads with merge_smem(S, K) bytes at smem.  Warp 0
-// writes out_ids/out_vals[p]; the other warps return without touching them.
-template <int R>
+// writes out_ids/out_vals[p], each kept value passed through map; the other
+// warps return without touching them.
+template <int R, class Map>
 __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
                                                const int* __restrict__ part_id, int S, int64_t P,
                                                int K, int64_t p, int32_t* __restrict__ out_ids,
-                                               float* __restrict__ out_vals, uint8_t* smem) {
+                                               float* __restrict__ out_vals, uint8_t* smem, Map map) {
     float* cv = reinterpret_cast<float*>(smem);        // [S*K] this position's lists
     int* ci = reinterpret_cast<int*>(cv + S * K);
     float* bv = reinterpret_cast<float*>(ci + S * K);  // [S*K] candidates
@@ -148,7 +149,7 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
         if (k < K) {
             const bool ok = m.id[rr] != wtk::kEmptyId;
             out_ids[p * K + k] = ok ? m.id[rr] : -1;
-            out_vals[p * K + k] = ok ? m.v[rr] : -INFINITY;
+            out_vals[p * K + k] = ok ? map(m.v[rr]) : -INFINITY;
         }
     }
 }

@@ -95,8 +95,16 @@ long long dflash2_kernels_launched(void);
  *             "Candidate Selector": the unary draft logits; [KB] "Draft-Verify
  *             Cycle": the shared lm_head gives logits and top-K per position;
  *             the full verifier vocabulary, [vLLM] "Candidate Selector")
- *   topk_ids[p, :], topk_vals[p, :] = the K largest U[p, .], ordered by value
- *             descending, equal values by token id ascending
+ *   U'[p, v] = c * tanh(m * U[p, v] / c)          (m * U[p, v] when c = 0)
+ *             the optional output multiplier m and final logit softcap c of the
+ *             unary logits ([SF] "Export and serve": both act on the unary
+ *             logits; no formula is given there, this is the common form with
+ *             the cap applied last).  m = 1, c = 0 leaves U as it is, bit for bit.
+ *   topk_ids[p, :], topk_vals[p, :] = the K largest U'[p, .], ordered by value
+ *             descending, equal values by token id ascending.  U' is increasing
+ *             in U, so the selection runs on U and only the K kept values are
+ *             mapped (fp32, tanhf); where fp32 rounding merges two mapped values
+ *             their order is U's, which can differ from the id rule
  *   G[p, i]  = sum_d h[p, d] * W_H[i, d]         the hidden projection H(h_t) of
  *             the pair score ([PR62] "What DFlash2 adds"; [KB] "Problem 1"), read
  *             as linear with no bias
@@ -105,6 +113,8 @@ long long dflash2_kernels_launched(void);
  *   h         [P, D]  bf16        draft hidden state
  *   W_lm      [V, D]  bf16        LM head (the verifier's, shared)
  *   K                              selector_top_k, 1 <= K <= min(V, DF2_MAX_TOPK)
+ *   output_multiplier              m: finite and > 0 (1 = none)
+ *   final_logit_softcapping        c: finite and >= 0 (0 = none)
  *   W_H       [r, D]  bf16        hidden projection, or NULL (then G is not written
  *                                  and r is ignored)
  *   G         [P, r]  fp32        out (when W_H != NULL); 1 <= r <= DF2_MAX_RANK
@@ -115,7 +125,8 @@ long long dflash2_kernels_launched(void);
  * ---------------------------------------------------------------------- */
 size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V, int K, int r);
 int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm, int64_t V,
-                       int K, const uint16_t* W_H, int r, float* G, int32_t* topk_ids,
+                       int K, float output_multiplier, float final_logit_softcapping,
+                       const uint16_t* W_H, int r, float* G, int32_t* topk_ids,
                        float* topk_vals, void* workspace, size_t workspace_bytes,
                        int32_t* dev_status, void* stream);
 
@@ -143,7 +154,8 @@ int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* 
  * ---------------------------------------------------------------------- */
 #define DF2_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,
-                               int64_t V, int K, const uint16_t* W_H, int r, float* G,
+                               int64_t V, int K, float output_multiplier,
+                               float final_logit_softcapping, const uint16_t* W_H, int r, float* G,
                                int32_t* topk_ids, float* topk_vals, int32_t* dev_status,
                                void* stream);
 
@@ -211,7 +223,8 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
  * three calls run in sequence.  The pages describe the steps, not this fusion;
  * the call exists to cut the launches and the serial latency of a draft step.
  *
- *   h [R*B, D] bf16; W_lm [V, D] bf16; W_H [r, D] bf16 (required); A, Bc [V, r] bf16;
+ *   h [R*B, D] bf16; W_lm [V, D] bf16; output_multiplier, final_logit_softcapping as
+ *   for dflash2_unary_topk; W_H [r, D] bf16 (required); A, Bc [V, r] bf16;
  *   anchors [R] int32; pred [R*B] int32 (nullable);
  *   topk_ids, topk_vals [R*B, K] out; G [R*B, r] fp32 out; path, path_scores [R, B-1]
  *   out; pair_scores [R*B, K] fp32 out (required iff pred != NULL).
@@ -221,7 +234,8 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
  * ---------------------------------------------------------------------- */
 size_t dflash2_draft_head_workspace_size(int R, int B, int64_t D, int64_t V, int K, int r);
 int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const uint16_t* W_lm, int64_t V,
-                       int K, const uint16_t* W_H, int r, const uint16_t* A, const uint16_t* Bc,
+                       int K, float output_multiplier, float final_logit_softcapping,
+                       const uint16_t* W_H, int r, const uint16_t* A, const uint16_t* Bc,
                        const int32_t* anchors, const int32_t* pred, int32_t* topk_ids,
                        float* topk_vals, float* G, int32_t* path, float* path_scores,
                        float* pair_scores, void* workspace, size_t workspace_bytes,

@@ -179,7 +179,8 @@ def pin_softcap_worked_values(o):
     W[:, 0] = col
     h = np.zeros((1, D), np.float32)
     h[0, 0] = 1.0
-    ids, vals, margin, _ = o.unary_topk(bf(h), bf(W), V, multiplier=math.log(3.0), softcap=2.0)
+    ids, vals, margin, _ = o.unary_topk(bf(h), bf(W), V, output_multiplier=math.log(3.0),
+                                        final_logit_softcapping=2.0)
     q = 3.0 ** 0.25
     half, quarter = 4.0 - 2.0 * math.sqrt(3.0), 2.0 * (q - 1.0) / (q + 1.0)
     assert ids[0].tolist() == [5, 2, 0, 3, 4, 1], ids
@@ -199,7 +200,7 @@ def pin_softcap_saturates_before_selection(o):
     W[:, 1] = rng.integers(1, 9, size=V) * 0.25      # logits in [0.25, 2], exact in bf16
     h = np.zeros((2, D), np.float32)
     h[:, 1] = 1.0
-    ids, vals, margin, _ = o.unary_topk(bf(h), bf(W), K, multiplier=64.0, softcap=0.5)
+    ids, vals, margin, _ = o.unary_topk(bf(h), bf(W), K, output_multiplier=64.0, final_logit_softcapping=0.5)
     for p in range(2):
         assert ids[p].tolist() == list(range(K)), ids[p]
         assert np.all(vals[p] == np.float32(0.5))
@@ -225,8 +226,9 @@ def pin_softcap_small_argument_series(o):
     W = rng.integers(-2, 3, size=(V, D))
     U = (h @ W.T) * 0.25 * 0.5                       # exact: h/2 and W/4 as bf16 operands
     m, c = 0.375, 64.0
-    ids, vals, _, _ = o.unary_topk(bf(h * 0.5), bf(W * 0.25), K, multiplier=m, softcap=c)
-    ids0, vals0, _, _ = o.unary_topk(bf(h * 0.5), bf(W * 0.25), K, multiplier=m)
+    ids, vals, _, _ = o.unary_topk(bf(h * 0.5), bf(W * 0.25), K, output_multiplier=m,
+                                   final_logit_softcapping=c)
+    ids0, vals0, _, _ = o.unary_topk(bf(h * 0.5), bf(W * 0.25), K, output_multiplier=m)
     for p in range(P):
         order = sorted(range(V), key=lambda v: (-U[p, v], v))[:K]
         assert ids[p].tolist() == order and ids0[p].tolist() == order
@@ -243,7 +245,7 @@ def pin_softcap_rejects_bad_parameters(o):
     for m, c in [(0.0, 0.0), (-1.0, 0.0), (math.nan, 0.0), (math.inf, 1.0), (1.0, -1.0), (1.0, math.inf),
                  (1.0, math.nan)]:
         try:
-            o.unary_topk(h, W, 2, multiplier=m, softcap=c)
+            o.unary_topk(h, W, 2, output_multiplier=m, final_logit_softcapping=c)
         except ValueError:
             continue
         raise AssertionError(f"multiplier={m} softcap={c} accepted")

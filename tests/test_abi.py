@@ -37,7 +37,7 @@ def test_status_strings(lib):
     assert names == ["DF2_OK", "DF2_ERR_INVALID_ARGUMENT", "DF2_ERR_UNSUPPORTED", "DF2_ERR_CUDA",
                      "DF2_ERR_WORKSPACE_TOO_SMALL", "DF2_ERR_TIMEOUT"]
     assert lib.dflash2_status_string(99).decode() == "DF2_ERR_UNKNOWN"
-    assert lib.dflash2_abi_version() == 1
+    assert lib.dflash2_abi_version() == 2
 
 
 def test_header_compiles_as_c(tmp_path):
@@ -51,15 +51,19 @@ def test_head_validation(lib):
     f = lib.dflash2_unary_topk
     fake = VP(0x1000)
     # K > V, K < 1, P < 0, D not multiple of 8, K above the build limit
-    assert f(fake, 4, 64, fake, 10, 11, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
-    assert f(fake, 4, 64, fake, 10, 0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
-    assert f(fake, -1, 64, fake, 10, 2, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
-    assert f(fake, 4, 60, fake, 10, 2, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 2
-    assert f(fake, 4, 64, fake, 5000, 2000, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 2
+    assert f(fake, 4, 64, fake, 10, 11, 1.0, 0.0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
+    assert f(fake, 4, 64, fake, 10, 0, 1.0, 0.0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
+    assert f(fake, -1, 64, fake, 10, 2, 1.0, 0.0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
+    assert f(fake, 4, 60, fake, 10, 2, 1.0, 0.0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 2
+    assert f(fake, 4, 64, fake, 5000, 2000, 1.0, 0.0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 2
     # W_H given with r < 1
-    assert f(fake, 4, 64, fake, 10, 2, fake, 0, fake, fake, fake, fake, 1 << 20, None, None) == 1
+    assert f(fake, 4, 64, fake, 10, 2, 1.0, 0.0, fake, 0, fake, fake, fake, fake, 1 << 20, None, None) == 1
     # P == 0 is a no-op
-    assert f(fake, 0, 64, fake, 10, 2, None, 0, None, fake, fake, fake, 0, None, None) == 0
+    assert f(fake, 0, 64, fake, 10, 2, 1.0, 0.0, None, 0, None, fake, fake, fake, 0, None, None) == 0
+    # output multiplier finite and > 0, final softcap finite and >= 0
+    inf, nan = float("inf"), float("nan")
+    for m, c in [(0.0, 0.0), (-1.0, 0.0), (nan, 0.0), (inf, 0.0), (1.0, -1.0), (1.0, inf), (1.0, nan)]:
+        assert f(fake, 4, 64, fake, 10, 2, m, c, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
 
 
 def test_selector_validation(lib):
@@ -72,11 +76,14 @@ def test_selector_validation(lib):
     dh = lib.dflash2_draft_head
     f8 = [fake] * 8
     # B < 2, K > V, r % 8, W_H missing, workspace too small
-    assert dh(fake, 1, 1, 64, fake, 100, 4, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
-    assert dh(fake, 1, 8, 64, fake, 100, 101, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
-    assert dh(fake, 1, 8, 64, fake, 100, 4, fake, 12, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 2
-    assert dh(fake, 1, 8, 64, fake, 100, 4, None, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
-    assert dh(fake, 0, 8, 64, fake, 100, 4, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 0, None, None) == 0
+    assert dh(fake, 1, 1, 64, fake, 100, 4, 1.0, 0.0, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
+    assert dh(fake, 1, 8, 64, fake, 100, 101, 1.0, 0.0, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
+    assert dh(fake, 1, 8, 64, fake, 100, 4, 1.0, 0.0, fake, 12, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 2
+    assert dh(fake, 1, 8, 64, fake, 100, 4, 1.0, 0.0, None, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
+    assert dh(fake, 0, 8, 64, fake, 100, 4, 1.0, 0.0, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 0, None, None) == 0
+    # a bad output multiplier or softcap
+    assert dh(fake, 1, 8, 64, fake, 100, 4, -2.0, 0.0, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
+    assert dh(fake, 1, 8, 64, fake, 100, 4, 1.0, -0.5, fake, 32, fake, fake, fake, None, *f8[:5], None, fake, 1 << 20, None, None) == 1
     assert lib.dflash2_draft_head_workspace_size(1, 1, 64, 100, 4, 32) == 0
     lt = lib.dflash2_selector_lattice
     assert lt(fake, 2, 1, fake, fake, fake, fake, fake, 100, 4, 32, fake, None, None) == 1  # B < 2

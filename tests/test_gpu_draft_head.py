@@ -42,14 +42,16 @@ def inputs(seed, R, B, D, V, K, r, cb_std=0.3):
 def fused(df2, x, with_pred=True, status=None):
     out = df2.draft_head(bf_dev(x["h"]), bf_dev(x["W_lm"]), x["K"], bf_dev(x["W_H"]), bf_dev(x["A"]),
                          bf_dev(x["Bc"]), dev(x["anchors"]), x["B"],
-                         dev(x["pred"]) if with_pred else None, dev_status=status)
+                         dev(x["pred"]) if with_pred else None, dev_status=status,
+                         output_multiplier=x.get("m", 1.0), final_logit_softcapping=x.get("c", 0.0))
     torch.cuda.synchronize()
     return [host(t) for t in out]
 
 
 def separate(df2, x, status=None):
     h, Wlm, WH, A, Bc = (bf_dev(x[k]) for k in ("h", "W_lm", "W_H", "A", "Bc"))
-    ids, vals, G = df2.unary_topk(h, Wlm, x["K"], WH, dev_status=status)
+    ids, vals, G = df2.unary_topk(h, Wlm, x["K"], WH, dev_status=status, output_multiplier=x.get("m", 1.0),
+                                  final_logit_softcapping=x.get("c", 0.0))
     path, ps = df2.selector_walk(dev(x["anchors"]), ids, vals, G, A, Bc, x["B"], dev_status=status)
     pair = df2.selector_pair_scores(dev(x["pred"]), ids, vals, G, A, Bc, dev_status=status)
     torch.cuda.synchronize()
@@ -73,11 +75,28 @@ def test_fused_equals_separate_calls(df2, R, B, D, V, K, r):
         assert np.array_equal(g, w, equal_nan=True), name
 
 
-def test_fused_against_the_oracle(orc, df2):
+@pytest.mark.parametrize("R,B,D,V,K,r,m,c", [
+    (1, 8, 4096, 151936, 16, 256, 1.25, 20.0),   # the batch-1 shape, capped logits
+    (16, 8, 256, 30000, 16, 256, 0.5, 2.0),      # the tensor-core GEMM head
+    (1, 16, 512, 20000, 64, 512, 2.0, 0.0),      # K = 64 (the separate calls), multiplier only
+])
+def test_fused_with_logit_map_equals_separate_calls(df2, R, B, D, V, K, r, m, c):
+    x = inputs(R * 5 + K + r, R, B, D, V, K, r)
+    x["m"], x["c"] = m, c
+    got = fused(df2, x)
+    want = separate(df2, x)
+    for name, g, w in zip(["ids", "vals", "G", "path", "path_scores", "pair_scores"], got, want):
+        assert np.array_equal(g, w, equal_nan=True), name
+
+
+@pytest.mark.parametrize("m,c", [(1.0, 0.0), (1.5, 3.0)])
+def test_fused_against_the_oracle(orc, df2, m, c):
     R, B, D, V, K, r = 3, 8, 256, 3000, 16, 64
     x = inputs(99, R, B, D, V, K, r)
+    x["m"], x["c"] = m, c
     ids, vals, G, path, ps, pair = fused(df2, x)
-    oi, ov, om, oG = orc.unary_topk(x["h"], x["W_lm"], K, W_H=x["W_H"])
+    oi, ov, om, oG = orc.unary_topk(x["h"], x["W_lm"], K, W_H=x["W_H"], output_multiplier=m,
+                                    final_logit_softcapping=c)
     compare_topk(ids, vals, oi, ov, om, "fused topk").check("fused topk")
     op, os_, omg, _ = orc.selector_walk(x["anchors"], oi, ov, oG, x["A"], x["Bc"], B)
     compare_walk(path, ps, op, os_, omg, "fused walk").check("fused walk")

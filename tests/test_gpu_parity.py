@@ -131,6 +131,47 @@ def test_head_exact_ties_break_to_lower_id(orc, df2):
     assert np.array_equal(gv, ov) or np.allclose(gv, ov, rtol=2e-3, atol=2e-3)
 
 
+# ------------------------------------------- logit multiplier / softcap ----
+
+@pytest.mark.parametrize("P,D,V,K,m,c", [
+    (8, 1024, 20011, 16, 1.0, 30.0),     # few positions (the streaming head), a cap only
+    (3, 264, 3000, 37, 0.5, 0.0),        # ragged shapes, a multiplier only
+    (140, 256, 5000, 16, 2.0, 0.75),     # many positions (the tensor-core GEMM), a tight cap
+    (20, 256, 3000, 100, 1.5, 4.0),      # K > 64: the CUDA-core path
+])
+def test_head_logit_map(orc, df2, P, D, V, K, m, c):
+    """Top-K of c*tanh(m*U/c) against the oracle, which maps all V logits before
+    selecting; the kernels select on U and map the K kept values, so their ids
+    equal the unmapped call's and their values are the map of its values."""
+    rng = _rng(P * 17 + D + V * 3 + K)
+    h = rand_bf16(rng, (P, D))
+    Wlm = rand_bf16(rng, (V, D), 0.02)
+    ids, vals, _ = df2.unary_topk(bf_dev(h), bf_dev(Wlm), K, output_multiplier=m, final_logit_softcapping=c)
+    ids0, vals0, _ = df2.unary_topk(bf_dev(h), bf_dev(Wlm), K)
+    torch.cuda.synchronize()
+    gi, gv, gi0, gv0 = host(ids), host(vals), host(ids0), host(vals0)
+    oi, ov, om, _ = orc.unary_topk(h, Wlm, K, output_multiplier=m, final_logit_softcapping=c)
+    what = f"map{P}x{D}x{V}k{K}"
+    compare_topk(gi, gv, oi, ov, om, what).check(what)
+    compare_topk_values(gi, gv, oi, ov, what + " vals")
+    assert np.array_equal(gi, gi0)
+    x = np.float32(m) * gv0.astype(np.float64)
+    want = np.float32(c) * np.tanh(x / np.float32(c)) if c > 0 else x
+    assert np.allclose(gv, want, rtol=1e-6, atol=1e-6 * max(c, 1.0)), np.abs(gv - want).max()
+    if c > 0:
+        assert np.all(np.abs(gv) <= np.float32(c))
+
+
+def test_head_logit_map_defaults_are_the_identity(df2):
+    """m = 1, c = 0 leaves every value bit for bit as the call without the map."""
+    rng = _rng(3)
+    h = bf_dev(rand_bf16(rng, (8, 512)))
+    Wlm = bf_dev(rand_bf16(rng, (9000, 512), 0.02))
+    a = df2.unary_topk(h, Wlm, 16, output_multiplier=1.0, final_logit_softcapping=0.0)
+    b = df2.unary_topk(h, Wlm, 16)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
 def test_head_empty(df2):
     h = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
     Wlm = torch.zeros((100, 64), dtype=torch.bfloat16, device="cuda")

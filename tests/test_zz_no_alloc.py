@@ -46,7 +46,7 @@ def _with_workspace(lib, h, W, K, WH, stream):
     G = torch.empty((P, r), dtype=torch.float32, device="cuda")
     nbytes = lib.dflash2_unary_topk_workspace_size(P, D, V, K, r)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
-    rc = lib.dflash2_unary_topk(_p(h), P, D, _p(W), V, K, _p(WH), r, _p(G), _p(ids), _p(vals), _p(ws),
+    rc = lib.dflash2_unary_topk(_p(h), P, D, _p(W), V, K, 1.0, 0.0, _p(WH), r, _p(G), _p(ids), _p(vals), _p(ws),
                                 nbytes, None, stream)
     assert rc == 0, lib.dflash2_status_string(rc)
     return ids, vals, G
@@ -59,7 +59,7 @@ def _no_alloc(lib, h, W, K, WH, stream):
     vals = torch.zeros((P, K), dtype=torch.float32, device="cuda")
     G = torch.zeros((P, r), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = lib.dflash2_unary_topk_noalloc(_p(h), P, D, _p(W), V, K, _p(WH), r, _p(G), _p(ids), _p(vals),
+    rc = lib.dflash2_unary_topk_noalloc(_p(h), P, D, _p(W), V, K, 1.0, 0.0, _p(WH), r, _p(G), _p(ids), _p(vals),
                                         _p(status), stream)
     assert rc == 0, lib.dflash2_status_string(rc)
     return ids, vals, G, status
@@ -95,7 +95,7 @@ def test_no_alloc_rejects_oversized_shapes(lib):
     ids = torch.full((P, K), -7, dtype=torch.int32, device="cuda")
     vals = torch.empty((P, K), dtype=torch.float32, device="cuda")
     before = lib.dflash2_kernels_launched()
-    rc = lib.dflash2_unary_topk_noalloc(_p(h), P, D, _p(W), V, K, None, 0, None, _p(ids), _p(vals),
+    rc = lib.dflash2_unary_topk_noalloc(_p(h), P, D, _p(W), V, K, 1.0, 0.0, None, 0, None, _p(ids), _p(vals),
                                         None, ct.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 2 and lib.dflash2_status_string(rc) == b"DF2_ERR_UNSUPPORTED"
     assert lib.dflash2_kernels_launched() == before
