@@ -110,15 +110,21 @@ __device__ __forceinline__ float key_value(unsigned k) {
 
 namespace {
 
-template <int EPI, int WN>
+// PAIR: a cluster of two CTAs shares each 256 x WN tile (cta_group::2).  CTA r
+// of the pair stages A rows [128 r, 128 r + 128) of the pair's 256 and B rows
+// [WN/2 r, WN/2 (r + 1)) of the tile's WN; CTA 0's MMA thread computes the whole
+// tile, and each CTA's TMEM receives its own 128 rows x WN columns.  Each CTA thus
+// stages half the B bytes per flop of the one-CTA tile.
+template <int EPI, int WN, bool PAIR>
 __global__ void __launch_bounds__(kWideThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const WideArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr uint32_t kBBox = WN * WK * 2;
+    constexpr int kBRows = PAIR ? WN / 2 : WN;  // B rows this CTA stages per tile
+    constexpr uint32_t kBBox = kBRows * WK * 2;
     const int nstages = args.nstages, kbox = args.kbox;
-    const uint32_t stage_bytes = wide_stage_bytes(kbox, WN);
+    const uint32_t stage_bytes = wide_stage_bytes(kbox, kBRows);
     uint8_t* stages = smem;  // stage s: kbox A boxes, then kbox B boxes
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(nstages) * stage_bytes);
     uint64_t* empty = full + nstages;
@@ -136,8 +142,14 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     if (bid == 0)
         for (int i = threadIdx.x; i < args.n_zero; i += blockDim.x) args.zero_words[i] = 0u;
     const int n_groups = (args.n_nt + args.tiles_per_cta - 1) / args.tiles_per_cta;
-    const int mt = args.m_major ? bid / n_groups : bid % args.n_mt;
-    const int grp = args.m_major ? bid % n_groups : bid / args.n_mt;
+    // the work unit: one M tile, or (PAIR) one pair of M tiles, times a range of N tiles
+    const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? bid >> 1 : bid;
+    const int n_mu = PAIR ? (args.n_mt + 1) / 2 : args.n_mt;
+    const int mu = args.m_major ? unit / n_groups : unit % n_mu;
+    const int mt = PAIR ? 2 * mu + int(rank) : mu;
+    const int grp = args.m_major ? unit % n_groups : unit / n_mu;
     const int nt0 = grp * args.tiles_per_cta;
     const int nt1 = min(args.n_nt, nt0 + args.tiles_per_cta);
     const int nbox = (args.Kd + WK - 1) / WK;
@@ -150,7 +162,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], 1);
-            tc::mbar_init(&tempty[b], 4);
+            tc::mbar_init(&tempty[b], PAIR ? 8 : 4);  // the epilogue warps of one CTA, or of both
         }
         tc::mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -161,8 +173,13 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         for (int k = 0; k < args.K; ++k) hp[k * 128 + tt] = make_uint2(__float_as_uint(-INFINITY), unsigned(INT_MAX));
     }
     if (warp == 1) {
-        tc::tmem_alloc(tmem_holder, 512);
-        tc::tmem_relinquish();
+        if (PAIR) {
+            tc::tmem_alloc_pair(tmem_holder, 512);
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc(tmem_holder, 512);
+            tc::tmem_relinquish();
+        }
     }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tm_a);
@@ -170,6 +187,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (PAIR) tc::cluster_sync_all();  // the peer's barriers are initialised before any remote use
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -187,28 +205,41 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                 for (int kb = 0; kb < nk; ++kb) {
                     const int nb = min(kbox, nbox - kb * kbox);
                     if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-                    tc::mbar_arrive_expect_tx(&full[stage], uint32_t(nb) * (kABox + kBBox));
+                    // PAIR: CTA 0's full barrier counts the bytes both CTAs stage
+                    if (leader)
+                        tc::mbar_arrive_expect_tx(&full[stage], uint32_t(nb) * (kABox + kBBox) * (PAIR ? 2u : 1u));
                     uint8_t* st = stages + size_t(stage) * stage_bytes;
+                    const int yb = nt * WN + int(rank) * kBRows;
                     for (int j = 0; j < nb; ++j) {
                         const int x = (kb * kbox + j) * WK;
-                        tc::tma_load_2d(st + size_t(j) * kABox, &tm_a, &full[stage], x, mt * WM, pol_a);
-                        tc::tma_load_2d(st + size_t(kbox) * kABox + size_t(j) * kBBox, &tm_b, &full[stage], x,
-                                        nt * WN, pol_b);
+                        uint8_t* da = st + size_t(j) * kABox;
+                        uint8_t* db = st + size_t(kbox) * kABox + size_t(j) * kBBox;
+                        if (PAIR) {
+                            const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
+                            tc::tma_load_2d_pair(da, &tm_a, fb, x, mt * WM, pol_a);
+                            tc::tma_load_2d_pair(db, &tm_b, fb, x, yb, pol_b);
+                        } else {
+                            tc::tma_load_2d(da, &tm_a, &full[stage], x, mt * WM, pol_a);
+                            tc::tma_load_2d(db, &tm_b, &full[stage], x, yb, pol_b);
+                        }
                     }
                     armed[stage] = int8_t(phase);
                     if (++stage == nstages) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
+                // wait (bounded) for the copies in flight; PAIR: CTA 1's copies complete on
+                // CTA 0's barriers too, and CTA 1 leaves only after the closing cluster
+                // barrier, which CTA 0 reaches after this
                 volatile int never = 0;
                 for (int s = 0; s < nstages; ++s)
                     if (armed[s] >= 0) tc::mbar_wait(&full[s], uint32_t(armed[s]), &never);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // -------------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(WM, WN);
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(PAIR ? 2 * WM : WM, WN);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -216,7 +247,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             for (int nt = nt0; nt < nt1 && ok; ++nt, ++it) {
                 const int b = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
-                if (!tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag)) break;
+                const bool drained = PAIR ? tc::mbar_wait_cluster(&tempty[b], tph ^ 1, abort_flag)
+                                          : tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag);
+                if (!drained) break;
                 tc::fence_after_sync();
                 const uint32_t d_tmem = tmem_base + uint32_t(b * WN);
                 for (int kb = 0; kb < nk; ++kb) {
@@ -228,16 +261,25 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                         const uint32_t a0 = tc::smem_u32(st + size_t(j) * kABox);
                         const uint32_t b0 = tc::smem_u32(st + size_t(kbox) * kABox + size_t(j) * kBBox);
 #pragma unroll
-                        for (int k = 0; k < WK / 16; ++k)
-                            tc::mma_bf16(d_tmem, tc::sw128_kmajor_desc(a0 + 32 * k),
-                                         tc::sw128_kmajor_desc(b0 + 32 * k), idesc, (kb | j | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < WK / 16; ++k) {
+                            const uint64_t ad = tc::sw128_kmajor_desc(a0 + 32 * k);
+                            const uint64_t bd = tc::sw128_kmajor_desc(b0 + 32 * k);
+                            const uint32_t acc = (kb | j | k) != 0 ? 1u : 0u;
+                            if (PAIR) tc::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                            else tc::mma_bf16(d_tmem, ad, bd, idesc, acc);
+                        }
                     }
-                    tc::mma_commit(&empty[stage]);
+                    if (PAIR) tc::mma_commit_pair(&empty[stage], 0x3);
+                    else tc::mma_commit(&empty[stage]);
                     if (++stage == nstages) { stage = 0; phase ^= 1; }
                 }
-                if (ok) tc::mma_commit(&tfull[b]);
+                if (ok) {
+                    if (PAIR) tc::mma_commit_pair(&tfull[b], 0x3);
+                    else tc::mma_commit(&tfull[b]);
+                }
             }
-            tc::mma_commit(mma_done);
+            if (PAIR) tc::mma_commit_pair(mma_done, 0x3);
+            else tc::mma_commit(mma_done);
             volatile int never = 0;
             tc::mbar_wait(mma_done, 0, &never);
         }
@@ -317,7 +359,11 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&tempty[b]);
+            if (lane == 0) {
+                // PAIR: CTA 0's MMA thread waits for both CTAs' epilogues
+                if (PAIR) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&tempty[b]), 0));
+                else tc::mbar_arrive(&tempty[b]);
+            }
             if (EPI == EPI_TOPK && args.thr_g && row_ok) {
                 unsigned k = 0;
                 if (tid != INT_MAX) k = order_key(tv);  // heap full: publish its K-th value
@@ -345,10 +391,14 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 
     tc::fence_before_sync();
     __syncthreads();
+    // PAIR: CTA 0's MMAs read this CTA's shared memory and write its TMEM; neither
+    // CTA frees TMEM or exits before both are done
+    if (PAIR) tc::cluster_sync_all();
     if (threadIdx.x == 0 && *abort_flag && args.dev_status) atomicOr(args.dev_status, DF2_STATUS_WAIT_TIMEOUT);
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem_base, 512);
+        if (PAIR) tc::tmem_dealloc_pair(tmem_base, 512);
+        else tc::tmem_dealloc(tmem_base, 512);
     }
 }
 
@@ -391,10 +441,13 @@ int wide_bn(int epi, int K) {
     return 256;
 }
 
-int wide_stages(int epi, int K) {
+// Pipeline stages that fit beside the epilogue's heaps: a stage holds one 64-wide
+// K slice of A (128 rows) and of the B rows the CTA stages (256, or 128 in a pair).
+int wide_stages(int epi, int K, bool pair) {
     const uint32_t budget = 227 * 1024 - 1024;
-    for (int s = 4; s >= 2; --s)
-        if (wide_smem(s, 1, epi, K, wide_bn(epi, K)) <= budget) return s;
+    const int brows = pair ? wide_bn(epi, K) / 2 : wide_bn(epi, K);
+    for (int s = pair ? 6 : 4; s >= 2; --s)
+        if (wide_smem(s, 1, epi, K, brows) <= budget) return s;
     return 0;
 }
 
@@ -413,76 +466,129 @@ int wide_groups(int n_mt, int n_nt, int num_sms) {
     return n_nt < num_sms ? n_nt : num_sms;
 }
 
-template <int EPI, int BN>
+// The tiling of one launch: a CTA per 128-row M tile, or, with two or more M
+// tiles, a CTA pair per two M tiles (the last pair's second tile may lie past M;
+// its CTA still stages its half of every B tile).
+struct WidePlan {
+    bool pair;
+    int n_mt, n_nt;     // 128-row M tiles, 256-row N tiles
+    int n_mu;           // work units along M: tiles, or pairs of tiles
+    int tiles_per_cta;  // consecutive N tiles per unit
+    int n_groups;       // N ranges per unit
+    int nstages;
+};
+
+WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persistent) {
+    WidePlan p{};
+    const int bn = wide_bn(epi, K);
+    p.n_mt = int((M + WM - 1) / WM);
+    p.n_nt = int((N + bn - 1) / bn);
+    p.pair = p.n_mt >= 2 && wide_stages(epi, K, true) >= 2;
+    p.n_mu = p.pair ? (p.n_mt + 1) / 2 : p.n_mt;
+    p.nstages = wide_stages(epi, K, p.pair);
+    if (persistent) {
+        const int groups = wide_groups(p.n_mu, p.n_nt, p.pair ? num_sms / 2 : num_sms);
+        p.tiles_per_cta = (p.n_nt + groups - 1) / groups;
+    } else {
+        p.tiles_per_cta = 1;
+    }
+    p.n_groups = (p.n_nt + p.tiles_per_cta - 1) / p.tiles_per_cta;
+    return p;
+}
+
+template <int EPI, int BN, bool PAIR>
 cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const WideArgs& a, int grid,
                         cudaStream_t stream) {
-    const size_t smem = wide_smem(a.nstages, a.kbox, EPI, a.K, BN) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(gemm_wide_kernel<EPI, BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    const int brows = PAIR ? BN / 2 : BN;
+    const size_t smem = wide_smem(a.nstages, a.kbox, EPI, a.K, brows) + 1024;
+    auto kernel = gemm_wide_kernel<EPI, BN, PAIR>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    gemm_wide_kernel<EPI, BN><<<grid, kWideThreads, smem, stream>>>(ta, tb, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kWideThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR ? 2u : 1u;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
+}
+
+template <int EPI>
+cudaError_t launch_plan(const WidePlan& p, const CUtensorMap& ta, const CUtensorMap& tb, const WideArgs& a,
+                        cudaStream_t stream) {
+    const int grid = (p.pair ? 2 : 1) * p.n_mu * p.n_groups;
+    return p.pair ? launch_wide<EPI, 256, true>(ta, tb, a, grid, stream)
+                  : launch_wide<EPI, 256, false>(ta, tb, a, grid, stream);
 }
 
 }  // namespace
 
 bool wide_supported(int64_t M, int64_t N, int64_t Kd, int K) {
     return M >= 1 && N >= 1 && Kd >= 1 && Kd % 8 == 0 && M <= INT32_MAX && N <= INT32_MAX &&
-           Kd <= INT32_MAX && K <= 64 && wide_stages(EPI_TOPK, K < 1 ? 1 : K) >= 2;
+           Kd <= INT32_MAX && K <= 64 && wide_stages(EPI_TOPK, K < 1 ? 1 : K, false) >= 2;
 }
 
 size_t wide_topk_workspace(int64_t M, int64_t N, int K, int num_sms) {
-    const int bn = wide_bn(EPI_TOPK, K);
-    const int n_mt = int((M + WM - 1) / WM), n_nt = int((N + bn - 1) / bn);
-    return size_t(wide_groups(n_mt, n_nt, num_sms)) * size_t(M) * size_t(K) * 8 + size_t(M) * 4;
+    const WidePlan p = wide_plan(EPI_TOPK, M, N, K, num_sms, true);
+    return size_t(p.n_groups) * size_t(M) * size_t(K) * 8 + size_t(M) * 4;
 }
 
 cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd,
                               float* out0, int64_t ld0, int64_t n_split, float* out1, int64_t ld1,
                               int32_t* dev_status, cudaStream_t stream) {
+    const WidePlan p = wide_plan(EPI_STORE, M, N, 0, 0, false);
     CUtensorMap ta, tb;
-    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, 256)) return cudaErrorInvalidValue;
+    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, p.pair ? 128 : 256))
+        return cudaErrorInvalidValue;
     WideArgs a{};
     a.M = int(M); a.N = int(N); a.Kd = int(Kd);
-    a.n_mt = int((M + WM - 1) / WM);
-    a.n_nt = int((N + 256 - 1) / 256);
-    a.tiles_per_cta = 1;
+    a.n_mt = p.n_mt;
+    a.n_nt = p.n_nt;
+    a.tiles_per_cta = p.tiles_per_cta;
     a.m_major = 1;
-    a.nstages = wide_stages(EPI_STORE, 0);
+    a.nstages = p.nstages;
     a.kbox = 1;
     a.out0 = out0; a.ld0 = ld0; a.n_split = int(n_split); a.out1 = out1; a.ld1 = ld1;
     a.K = 0;
     a.dev_status = dev_status;
-    return launch_wide<EPI_STORE, 256>(ta, tb, a, a.n_mt * a.n_nt, stream);
+    return launch_plan<EPI_STORE>(p, ta, tb, a, stream);
 }
 
 cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
                              int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
                              cudaStream_t stream, TopkParts* parts_out, unsigned* zero_words, int n_zero) {
+    const WidePlan p = wide_plan(EPI_TOPK, M, N, K, num_sms, true);
     const int bn = wide_bn(EPI_TOPK, K);
     CUtensorMap ta, tb;
-    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, bn)) return cudaErrorInvalidValue;
+    if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, p.pair ? bn / 2 : bn))
+        return cudaErrorInvalidValue;
     WideArgs a{};
     a.M = int(M); a.N = int(N); a.Kd = int(Kd);
-    a.n_mt = int((M + WM - 1) / WM);
-    a.n_nt = int((N + bn - 1) / bn);
-    const int groups = wide_groups(a.n_mt, a.n_nt, num_sms);
-    a.tiles_per_cta = (a.n_nt + groups - 1) / groups;
-    const int n_groups = (a.n_nt + a.tiles_per_cta - 1) / a.tiles_per_cta;
+    a.n_mt = p.n_mt;
+    a.n_nt = p.n_nt;
+    a.tiles_per_cta = p.tiles_per_cta;
+    const int n_groups = p.n_groups;
     a.m_major = 0;
-    a.nstages = wide_stages(EPI_TOPK, K);
+    a.nstages = p.nstages;
     a.kbox = 1;
     a.K = K;
     a.part_v = static_cast<float*>(ws);
-    a.part_id = reinterpret_cast<int*>(a.part_v + size_t(groups) * M * K);
-    a.thr_g = reinterpret_cast<unsigned*>(a.part_id + size_t(groups) * M * K);
+    a.part_id = reinterpret_cast<int*>(a.part_v + size_t(n_groups) * M * K);
+    a.thr_g = reinterpret_cast<unsigned*>(a.part_id + size_t(n_groups) * M * K);
     a.dev_status = dev_status;
     a.zero_words = zero_words;
     a.n_zero = n_zero;
     cudaError_t e = cudaMemsetAsync(a.thr_g, 0, size_t(M) * 4, stream);
     if (e != cudaSuccess) return e;
-    e = launch_wide<EPI_TOPK, 256>(ta, tb, a, a.n_mt * n_groups, stream);
+    e = launch_plan<EPI_TOPK>(p, ta, tb, a, stream);
     if (e != cudaSuccess) return e;
     if (parts_out) {  // the caller folds the per-range lists itself
         *parts_out = TopkParts{a.part_v, a.part_id, n_groups};
