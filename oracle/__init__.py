@@ -78,8 +78,11 @@ class Oracle:
         L.df2o_lattice_walk.argtypes = [vp, vp, i32, i32, i32, i64, vp, ct.c_double, vp, vp, vp, vp]
         L.df2o_conv_prepare.argtypes = [vp, ct.c_int, i64, i32, i32, i32, i32, vp, vp, vp, vp]
         L.df2o_conv_finish.argtypes = [vp, ct.c_int, i64, i32, i32, i32, i32, vp, vp, vp]
+        L.df2o_conv_finish_prepare.argtypes = [vp, ct.c_int, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                               vp, vp]
         for f in ("df2o_logits", "df2o_unary_topk", "df2o_selector_walk",
-                  "df2o_selector_pair_scores", "df2o_conv_prepare", "df2o_conv_finish"):
+                  "df2o_selector_pair_scores", "df2o_conv_prepare", "df2o_conv_finish",
+                  "df2o_conv_finish_prepare"):
             getattr(L, f).restype = ct.c_int
 
     def num_threads(self) -> int:
@@ -100,11 +103,11 @@ class Oracle:
         self._check(self.lib.df2o_logits(_p(h), P, D, _p(W), V, _p(U)))
         return U
 
-    def unary_topk(self, h, W_lm, K, W_H=None, multiplier=1.0, softcap=0.0):
+    def unary_topk(self, h, W_lm, K, W_H=None, output_multiplier=1.0, final_logit_softcapping=0.0):
         """Returns (ids [P,K] int32, vals [P,K] f32, margin [P] f64, G [P,r] f32 or None).
 
-        multiplier and softcap map every logit u to softcap*tanh(multiplier*u/softcap)
-        (multiplier*u when softcap is 0).  They are rounded to fp32 first, the
+        output_multiplier m and final_logit_softcapping c map every logit u to c*tanh(m*u/c)
+        (m*u when c is 0).  Both are rounded to fp32 first, the
         precision the library takes them in."""
         h, W_lm = _c(h, np.uint16), _c(W_lm, np.uint16)
         P, D = h.shape
@@ -119,7 +122,7 @@ class Oracle:
             r = W_H.shape[0]
             assert W_H.shape[1] == D
             G = np.empty((P, r), np.float32)
-        mul, cap = float(np.float32(multiplier)), float(np.float32(softcap))
+        mul, cap = float(np.float32(output_multiplier)), float(np.float32(final_logit_softcapping))
         self._check(self.lib.df2o_unary_topk(_p(h), P, D, _p(W_lm), V, int(K), mul, cap, _p(W_H), r, _p(G),
                                              _p(ids), _p(vals), _p(margin)))
         return ids, vals, margin, G
@@ -223,6 +226,26 @@ class Oracle:
         self._check(self.lib.df2o_conv_finish(_p(z), int(is_f32), P, C, int(block_size), int(taps),
                                               int(group), _p(dyn_out), _p(base), _p(y)))
         return y
+
+    def conv_finish_prepare(self, z, block_size, taps, group, dyn_out, base, W_proj, base_next,
+                            residual=None):
+        """finish(z) (+ residual), then the next prepare; returns (h, y_next, dyn_next [P,taps,G])."""
+        z = np.ascontiguousarray(z)
+        is_f32 = z.dtype == np.float32
+        z = _c(z, np.float32 if is_f32 else np.uint16)
+        if residual is not None:
+            residual = _c(residual, z.dtype)
+            assert residual.shape == z.shape
+        dyn_out, base = _c(dyn_out, np.float32), _c(base, np.float32)
+        W_proj, base_next = _c(W_proj, np.uint16), _c(base_next, np.float32)
+        P, C = z.shape
+        G = C // group
+        h, y = np.empty_like(z), np.empty_like(z)
+        dyn = np.empty((P, taps, G), np.float32)
+        self._check(self.lib.df2o_conv_finish_prepare(_p(z), int(is_f32), P, C, int(block_size), int(taps),
+                                                      int(group), _p(dyn_out), _p(base), _p(residual), _p(h),
+                                                      _p(W_proj), _p(base_next), _p(y), _p(dyn)))
+        return h, y, dyn
 
 
 def default() -> Oracle:

@@ -571,3 +571,27 @@ int df2o_conv_finish(const void* z, int z_is_f32, int64_t P, int32_t C, int32_t 
     }
     return DF2O_OK;
 }
+
+/*
+ * The two convs that meet between consecutive sublayers of a draft layer: the
+ * finish of one sublayer, then the prepare of the next (vLLM Speculators "DFlash2"
+ * guide, "Local Convolution": every attention and MLP sublayer is wrapped by a conv
+ * before and after it).  The pages do not state the residual wiring between the
+ * two.  Reading: h = finish(z), plus the residual stream when one is given (the sum
+ * rounded to the activation dtype, as a separate elementwise add would round it),
+ * then prepare(h) with the next sublayer's projection and base kernels.  Writes
+ * h, y_next and dyn_next.
+ */
+int df2o_conv_finish_prepare(const void* z, int is_f32, int64_t P, int32_t C, int32_t Bsz, int32_t taps,
+                             int32_t g, const float* dyn_out, const float* base, const void* residual,
+                             void* h, const uint16_t* W_proj, const float* base_next, void* y_next,
+                             float* dyn_next)
+{
+    int rc = df2o_conv_finish(z, is_f32, P, C, Bsz, taps, g, dyn_out, base, h);
+    if (rc != DF2O_OK) return rc;
+    if (residual) {
+        for (int64_t i = 0; i < P * (int64_t)C; ++i)
+            act_store(h, is_f32, i, act_value(h, is_f32, i) + act_value(residual, is_f32, i));
+    }
+    return df2o_conv_prepare(h, is_f32, P, C, Bsz, taps, g, W_proj, base_next, y_next, dyn_next);
+}

@@ -694,6 +694,71 @@ def pin_conv_bf16_rounding(o):
     assert bf16_bits_to_f32(y3).tolist() == [[1 + 2.0**-7, 1 + 2.0**-7]]
 
 
+def pin_conv_finish_prepare_identity(o):
+    """Identity convs on both sides and zero projections: h = z + residual and
+    y_next = h exactly, with dyn_next = 0 (quarter-integer values keep every sum
+    exact in bf16).  A nonzero residual separates h from z, so a prepare that read
+    z instead of h, or a dropped residual, shows."""
+    rng = _rng("fin_prep_id")
+    B, taps, C, g, nb = 4, 2, 32, 8, 2
+    P, G = B * nb, C // g
+    z = rng.integers(-4, 5, size=(P, C)) * 0.25
+    r = rng.integers(-4, 5, size=(P, C)) * 0.25
+    base = _identity_base(taps, C)
+    dyn = np.zeros((P, taps, G), np.float32)
+    Wp = np.zeros((2 * taps * G, C), np.uint16)
+    h, y, d = o.conv_finish_prepare(bf(z), B, taps, g, dyn, base, Wp, base, residual=bf(r))
+    assert np.array_equal(bf16_bits_to_f32(h), (z + r).astype(np.float32))
+    assert np.array_equal(y, h) and not np.any(d)
+    h0, y0, _ = o.conv_finish_prepare(bf(z), B, taps, g, dyn, base, Wp, base)
+    assert np.array_equal(bf16_bits_to_f32(h0), z.astype(np.float32)) and np.array_equal(y0, h0)
+
+
+def pin_conv_finish_prepare_static_closed_form(o):
+    """Static kernels (no projection, no dynamic part) on fp32 small-integer data,
+    so every value is exact: h_t = b1_0 z_t + b1_1 z_{t-1} + r_t with the finishing
+    conv's output-side base b1, then y_t = c0_0 h_t + c0_1 h_{t-1} with the next
+    conv's input-side base c0; no tap crosses a block (t-1 >= 0 inside the block)."""
+    rng = _rng("fin_prep_static")
+    B, taps, C, g, nb = 4, 2, 16, 4, 2
+    P, G = B * nb, C // g
+    z = rng.integers(-3, 4, size=(P, C)).astype(np.float32)
+    r = rng.integers(-3, 4, size=(P, C)).astype(np.float32)
+    base = rng.integers(-2, 3, size=(2, taps, C)).astype(np.float32)
+    base_next = rng.integers(-2, 3, size=(2, taps, C)).astype(np.float32)
+    dyn = np.zeros((P, taps, G), np.float32)
+    Wp = np.zeros((2 * taps * G, C), np.uint16)
+    h, y, d = o.conv_finish_prepare(z, B, taps, g, dyn, base, Wp, base_next, residual=r)
+    t = np.arange(P) % B
+    prev = lambda a: np.where((t >= 1)[:, None], np.roll(a, 1, axis=0), 0.0)
+    want_h = base[1, 0] * z + base[1, 1] * prev(z) + r
+    want_y = base_next[0, 0] * want_h + base_next[0, 1] * prev(want_h)
+    assert np.array_equal(h, want_h.astype(np.float32))
+    assert np.array_equal(y, want_y.astype(np.float32)) and not np.any(d)
+
+
+def pin_conv_finish_prepare_block_locality(o):
+    """Changing the last row of block n (z and the residual) leaves every output row
+    of block n+1 bit-identical through both convs."""
+    rng = _rng("fin_prep_local")
+    B, taps, C, g, nb = 4, 3, 32, 8, 3
+    P, G = B * nb, C // g
+    bfr = lambda shape, s: f32_to_bf16_bits((rng.standard_normal(shape) * s).astype(np.float32))
+    z, r = bfr((P, C), 1.0), bfr((P, C), 1.0)
+    dyn = (rng.standard_normal((P, taps, G)) * 0.1).astype(np.float32)
+    Wp = bfr((2 * taps * G, C), 0.1)
+    base = rng.standard_normal((2, taps, C)).astype(np.float32)
+    base_next = rng.standard_normal((2, taps, C)).astype(np.float32)
+    out0 = o.conv_finish_prepare(z, B, taps, g, dyn, base, Wp, base_next, residual=r)
+    z2, r2 = z.copy(), r.copy()
+    z2[B - 1] = bfr(C, 50.0)
+    r2[B - 1] = bfr(C, 50.0)
+    out1 = o.conv_finish_prepare(z2, B, taps, g, dyn, base, Wp, base_next, residual=r2)
+    for a, b in zip(out0, out1):
+        assert np.array_equal(a[B:], b[B:])
+        assert not np.array_equal(a[B - 1], b[B - 1])
+
+
 def pin_conv_rejects_bad_shapes(o):
     x = np.zeros((6, 8), np.float32)
     base = np.zeros((2, 2, 8), np.float32)

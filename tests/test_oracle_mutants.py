@@ -81,6 +81,11 @@ MUTANTS = [
         ("c[v].val = (float)logit_map(acc, mul, cap);", "c[v].val = (float)acc;"),
         ("vals[p * K + j] = c[j].val;", "vals[p * K + j] = (float)logit_map(c[j].val, mul, cap);")]),
     ("softcap_accepts_negative_multiplier", "if (!(mul > 0.0) ||", "if (!(mul != 0.0) ||"),
+    ("finish_prepare_drops_residual", "    if (residual) {\n", "    if (0) {\n"),
+    ("finish_prepare_next_reads_z",
+     "return df2o_conv_prepare(h, is_f32,", "return df2o_conv_prepare(z, is_f32,"),
+    ("finish_prepare_next_uses_same_base",
+     "W_proj, base_next, y_next, dyn_next);", "W_proj, base, y_next, dyn_next);"),
 ]
 
 
