@@ -159,10 +159,44 @@ def time_per_call(step, torch, n):
     return out
 
 
+def graph_time_us(torch, call, iters=20, reps=5):
+    """GPU time per call of a short call: `iters` calls captured in one CUDA graph and
+    the graph replayed, so the host's per-call cost (Python, argument checks) does
+    not show.  Returns (microseconds per call, how it was timed); falls back to a
+    plain loop, which then measures host-bound submission, if capture fails."""
+    call()
+    torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(iters):
+                call()
+        g.replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(reps):
+            g.replay()
+        ev[1].record()
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / (reps * iters) * 1e3, "graph"
+    except RuntimeError:
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(iters):
+            call()
+        ev[1].record()
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / iters * 1e3, "loop"
+
+
 def time_next_rows(step, torch, df2, iters=20):
     """Per-call times of the lattice schedule on the step's own candidates: the table,
     then the greedy and the sampling walk over it; then the draft head with capped
-    logits (multiplier 1, softcap 30).  None of it is part of the timed step."""
+    logits (multiplier 1, softcap 30); then the conv finish fused with the next
+    prepare (residual = the step's x), and the same as its separate calls with the
+    residual added by torch.  None of it is part of the timed step."""
     w = step.w
     lat = torch.empty((w.R, w.B - 1, w.K, w.K), dtype=torch.float32, device=step.ids.device)
     gen = torch.Generator(device=step.ids.device)
@@ -170,6 +204,14 @@ def time_next_rows(step, torch, df2, iters=20):
     u = torch.rand((w.R, w.B - 1), generator=gen, device=step.ids.device)
     path = torch.empty((w.R, w.B - 1), dtype=torch.int32, device=step.ids.device)
     sc = torch.empty((w.R, w.B - 1), dtype=torch.float32, device=step.ids.device)
+    h, y_next, dyn_next = torch.empty_like(step.z), torch.empty_like(step.z), torch.empty_like(step.dyn)
+    ws_conv = step.ws_conv
+
+    def finish_add_prepare():
+        hs = df2.conv_finish(step.z, w.B, w.taps, w.g, step.dyn, step.base, out=h)
+        hs.add_(step.x)
+        df2.conv_prepare(hs, w.B, w.taps, w.g, step.W_proj, step.base, workspace=ws_conv, out=(y_next, dyn_next))
+
     calls = [
         lambda: df2.selector_lattice(step.anchors, step.ids, step.vals, step.Gt, step.A, step.Bc, w.B, out=lat),
         lambda: df2.lattice_walk(lat, step.ids, w.B, w.V, out=(path, sc)),
@@ -177,20 +219,16 @@ def time_next_rows(step, torch, df2, iters=20):
         lambda: df2.draft_head(step.h, step.W_lm, w.K, step.W_H, step.A, step.Bc, step.anchors, w.B, step.pred,
                                output_multiplier=1.0, final_logit_softcapping=30.0, workspace=step.ws_draft,
                                out=(step.ids, step.vals, step.Gt, step.path, step.pscore, step.scores)),
+        lambda: df2.conv_finish_prepare(step.z, w.B, w.taps, w.g, step.dyn, step.base, step.W_proj, step.base,
+                                        step.x, workspace=ws_conv, out=(h, y_next, dyn_next)),
+        finish_add_prepare,
     ]
+    out, how = [], set()
     for c in calls:
-        c()
-    torch.cuda.synchronize()
-    out = []
-    for c in calls:
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        ev[0].record()
-        for _ in range(iters):
-            c()
-        ev[1].record()
-        torch.cuda.synchronize()
-        out.append(ev[0].elapsed_time(ev[1]) / iters * 1e3)
-    return out
+        us, kind = graph_time_us(torch, c, iters)
+        out.append(us)
+        how.add(kind)
+    return out, "+".join(sorted(how))
 
 
 def config_of(w):
@@ -412,7 +450,7 @@ def gpu_arm(args, w, rank, world, torch):
         flush_ms = fe[0].elapsed_time(fe[1]) / 5 * args.steps
     step_ms = slowest_rank_ms((total_ms - flush_ms) / args.steps, dist, device)
     per_call_us = time_per_call(step, torch, min(args.steps, 50))
-    next_us = time_next_rows(step, torch, df2)
+    next_us, next_how = time_next_rows(step, torch, df2)
 
     # ---- end to end through the public API with host buffers
     pinned_in = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v))
@@ -500,11 +538,15 @@ def gpu_arm(args, w, rank, world, torch):
                          "finish": conv_bytes(w, "finish") / (per_call_us[1] * 1e-6) / 1e9},
             "roofline": roof,
             "next_rows": {
-                "note": "the lattice schedule and the capped-logit draft head, timed on the step's inputs outside the timed step",
+                "note": "the lattice schedule, the capped-logit draft head and the fused conv finish -> prepare, timed on "
+                        "the step's inputs outside the timed step",
+                "timed_by": next_how + " (graph: the calls captured in a CUDA graph and replayed, GPU time only)",
                 "selector_lattice_us": next_us[0],
                 "lattice_walk_greedy_us": next_us[1],
                 "lattice_walk_sampling_us": next_us[2],
                 "draft_head_softcap_us": next_us[3],
+                "conv_finish_prepare_us": next_us[4],
+                "conv_finish_add_prepare_separate_us": next_us[5],
                 "lattice_gbs": lattice_bytes(w) / (next_us[0] * 1e-6) / 1e9,
                 "lattice_tflops": lattice_flops(w) / (next_us[0] * 1e-6) / 1e12,
             },

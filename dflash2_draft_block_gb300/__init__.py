@@ -336,3 +336,34 @@ def conv_finish(z, block_size, taps, group, dyn_out, base, *, out=None, stream=N
                                    _p(dyn_out), _p(base), _p(y), _stream(stream))
     _check("dflash2_conv_finish", rc)
     return y
+
+
+def conv_finish_prepare(z, block_size, taps, group, dyn_out, base, W_proj, base_next, residual=None, *,
+                        workspace=None, out=None, stream=None):
+    """A sublayer's conv finish, plus the residual stream when given, then the next
+    sublayer's conv prepare.  Returns (h like z, y_next like z, dyn_out_next
+    [P, taps, C/group] f32)."""
+    dt = _act_dtype(z)
+    _need(z, "z", z.dtype, 2)
+    _need(dyn_out, "dyn_out", torch.float32, 3)
+    _need(base, "base", torch.float32, 3)
+    _need(W_proj, "W_proj", torch.bfloat16, 2)
+    _need(base_next, "base_next", torch.float32, 3)
+    if residual is not None:
+        _need(residual, "residual", z.dtype, 2)
+        if residual.shape != z.shape:
+            raise ValueError("residual must have z's shape")
+    P, C = z.shape
+    G = C // group
+    if out is None:
+        h, y = torch.empty_like(z), torch.empty_like(z)
+        dyn = torch.empty((P, taps, G), dtype=torch.float32, device=z.device)
+    else:
+        h, y, dyn = out
+    ws = _workspace(int(lib().dflash2_conv_finish_prepare_workspace_size(P, C, taps, group, dt)), workspace,
+                    z.device)
+    rc = lib().dflash2_conv_finish_prepare(_p(z), dt, P, C, int(block_size), int(taps), int(group), _p(dyn_out),
+                                           _p(base), _p(residual), _p(h), _p(W_proj), _p(base_next), _p(y),
+                                           _p(dyn), _p(ws), 0 if ws is None else ws.numel(), _stream(stream))
+    _check("dflash2_conv_finish_prepare", rc)
+    return h, y, dyn

@@ -40,6 +40,9 @@ SIGNATURES = {
     "dflash2_selftest_wait_timeout": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp, _sz, _vp,
                                              _vp]),
     "dflash2_conv_finish": (_int, [_vp, _int, _i64, _int, _int, _int, _int, _vp, _vp, _vp, _vp]),
+    "dflash2_conv_finish_prepare_workspace_size": (_sz, [_i64, _int, _int, _int, _int]),
+    "dflash2_conv_finish_prepare": (_int, [_vp, _int, _i64, _int, _int, _int, _int, _vp, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
 _lock = threading.Lock()

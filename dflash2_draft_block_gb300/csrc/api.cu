@@ -386,6 +386,42 @@ DF2_API int dflash2_conv_finish(const void* z, int dtype, int64_t P, int C, int 
                                             static_cast<cudaStream_t>(stream)));
 }
 
+DF2_API size_t dflash2_conv_finish_prepare_workspace_size(int64_t P, int C, int taps, int g, int dtype) {
+    return dflash2_conv_prepare_workspace_size(P, C, taps, g, dtype);
+}
+
+DF2_API int dflash2_conv_finish_prepare(const void* z, int dtype, int64_t P, int C, int B, int taps, int g,
+                                        const float* dyn_out, const float* base, const void* residual, void* h,
+                                        const uint16_t* W_proj, const float* base_next, void* y_next,
+                                        float* dyn_out_next, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+    int rc = check_conv(dtype, P, C, B, taps, g);
+    if (rc != DF2_OK) return rc;
+    if (P == 0) return DF2_OK;
+    if (!z || !dyn_out || !base || !h || !W_proj || !base_next || !y_next || !dyn_out_next)
+        return DF2_ERR_INVALID_ARGUMENT;
+    // an output aliasing an input would be read and written by different threads
+    if (h == z || h == residual || y_next == z || y_next == residual || y_next == h ||
+        dyn_out_next == dyn_out)
+        return DF2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(z) || !aligned16(dyn_out) || !aligned16(base) || !aligned16(residual) || !aligned16(h) ||
+        !aligned16(W_proj) || !aligned16(base_next) || !aligned16(y_next) || !aligned16(dyn_out_next) ||
+        !aligned16(workspace))
+        return DF2_ERR_UNSUPPORTED;
+    const size_t need = dflash2_conv_finish_prepare_workspace_size(P, C, taps, g, dtype);
+    if (workspace_bytes < need || !workspace) return DF2_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool f32 = dtype == DF2_DTYPE_F32;
+    const int64_t half = int64_t(taps) * (C / g);
+    // the finish with the residual add in its store writes h, then the next prepare
+    // reads it (a kernel that recomputed h per CTA instead ran 2.7x longer at P = 8)
+    cudaError_t e = df2::conv_apply_launch(z, f32, P, C, B, taps, g, base + int64_t(taps) * C, dyn_out, half, h,
+                                           st, residual);
+    if (e != cudaSuccess) return DF2_ERR_CUDA;
+    return dflash2_conv_prepare(h, dtype, P, C, B, taps, g, W_proj, base_next, y_next, dyn_out_next, workspace,
+                                workspace_bytes, stream);
+}
+
 // ---------------------------------------------------------------- self-test --
 
 DF2_API int dflash2_selftest_wait_timeout(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,

@@ -32,6 +32,7 @@ struct Vec<uint16_t> {
     static __device__ __forceinline__ void load(const uint16_t* p, float f[8]) {
         unpack8(__ldg(reinterpret_cast<const uint4*>(p)), f);
     }
+    static __device__ __forceinline__ float round(float f) { return bf16_to_f32(f32_to_bf16_rn(f)); }
     static __device__ __forceinline__ void store(uint16_t* p, const float f[8]) {
         uint4 w;
         w.x = uint32_t(f32_to_bf16_rn(f[0])) | (uint32_t(f32_to_bf16_rn(f[1])) << 16);
@@ -55,10 +56,27 @@ struct Vec<float> {
         const float4 v = __ldg(reinterpret_cast<const float4*>(p));
         f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
     }
+    static __device__ __forceinline__ float round(float f) { return f; }
     static __device__ __forceinline__ void store(float* p, const float f[4]) {
         *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
     }
 };
+
+// The residual stream added to a conv output: the output rounded to T first, the
+// sum rounded again by the store, so the result equals the conv's stored output
+// followed by a separate elementwise add in T.
+template <typename T>
+__device__ __forceinline__ void add_residual_raw(float acc[], const typename Vec<T>::Raw& raw) {
+    constexpr int N = Vec<T>::N;
+    float rv[N];
+    Vec<T>::widen(raw, rv);
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc[e] = Vec<T>::round(acc[e]) + rv[e];
+}
+template <typename T>
+__device__ __forceinline__ void add_residual(float acc[], const T* __restrict__ res) {
+    add_residual_raw<T>(acc, Vec<T>::load_raw(res));
+}
 
 // TAPS > 0: taps known at compile time, history in registers.  TAPS == 0: any
 // taps; earlier rows are re-read through L1/L2.
@@ -66,7 +84,7 @@ template <typename T, int TAPS>
 __global__ void __launch_bounds__(256)
 conv_apply_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, int taps, int g, int G,
                   const float* __restrict__ base, const float* __restrict__ dyn, int64_t dyn_ld,
-                  T* __restrict__ y) {
+                  const T* __restrict__ res, T* __restrict__ y) {
     constexpr int N = Vec<T>::N;
     const int chunks = C / N;
     const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -136,6 +154,7 @@ conv_apply_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, int ta
                         }
                     }
                 }
+                if (res) add_residual<T>(acc, res + p * C + c0);
                 Vec<T>::store(y + p * C + c0, acc);
             }
         }
@@ -164,6 +183,7 @@ conv_apply_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, int ta
                 acc[e] = fmaf(k, xv[e], acc[e]);
             }
         }
+        if (res) add_residual<T>(acc, res + p * C + c0);
         Vec<T>::store(y + p * C + c0, acc);
     }
 }
@@ -191,16 +211,18 @@ __device__ __forceinline__ void cp_async4_c(void* smem_dst, const void* gmem_src
 constexpr int kAsyncThreads = 256;
 constexpr size_t kAsyncSmemMax = 96 * 1024;
 
-template <typename T, int TAPS>
+template <typename T, int TAPS, bool RES>
 __global__ void __launch_bounds__(kAsyncThreads)
 conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, int g, int G, int strips,
                         const float* __restrict__ base, const float* __restrict__ dyn, int64_t dyn_ld,
-                        T* __restrict__ y) {
+                        const T* __restrict__ res, T* __restrict__ y) {
     constexpr int N = Vec<T>::N;
+    using Raw = typename Vec<T>::Raw;
     extern __shared__ __align__(16) uint8_t smem[];
     const int nt = blockDim.x;
     uint8_t* xs = smem;                                                // [B][nt][16 B]
-    float* ds = reinterpret_cast<float*>(smem + size_t(B) * nt * 16);  // [B][TAPS][nt]
+    uint8_t* rs = smem + size_t(B) * nt * 16;                          // RES: [B][nt][16 B]
+    float* ds = reinterpret_cast<float*>(rs + (RES ? size_t(B) * nt * 16 : 0));  // [B][TAPS][nt]
     const int tid = threadIdx.x;
     const int64_t nb = blockIdx.x / strips;
     const int strip = int(blockIdx.x % strips);
@@ -211,6 +233,7 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
     for (int t = 0; t < B; ++t) {
         const int64_t p = nb * B + t;
         cp_async16_c(xs + (size_t(t) * nt + tid) * 16, x + p * C + c0);
+        if (RES) cp_async16_c(rs + (size_t(t) * nt + tid) * 16, res + p * C + c0);
         if (shared_group) {
 #pragma unroll
             for (int j = 0; j < TAPS; ++j)
@@ -233,7 +256,7 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
         for (int j = TAPS - 1; j > 0; --j)
 #pragma unroll
             for (int e = 0; e < N; ++e) hist[j][e] = hist[j - 1][e];
-        Vec<T>::widen(*reinterpret_cast<const typename Vec<T>::Raw*>(xs + (size_t(t) * nt + tid) * 16), hist[0]);
+        Vec<T>::widen(*reinterpret_cast<const Raw*>(xs + (size_t(t) * nt + tid) * 16), hist[0]);
         float acc[N];
 #pragma unroll
         for (int e = 0; e < N; ++e) acc[e] = 0.f;
@@ -252,6 +275,7 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
                 }
             }
         }
+        if (RES) add_residual_raw<T>(acc, *reinterpret_cast<const Raw*>(rs + (size_t(t) * nt + tid) * 16));
         Vec<T>::store(y + p * C + c0, acc);
     }
 }
@@ -262,7 +286,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 conv_apply_rows_kernel(const T* __restrict__ x, int64_t P, int C, int B, int taps, int g, int G,
                        const float* __restrict__ base, const float* __restrict__ dyn, int64_t dyn_ld,
-                       T* __restrict__ y) {
+                       const T* __restrict__ res, T* __restrict__ y) {
     constexpr int N = Vec<T>::N;
     const int chunks = C / N;
     const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -283,12 +307,13 @@ conv_apply_rows_kernel(const T* __restrict__ x, int64_t P, int C, int B, int tap
             acc[e] = fmaf(k, xv[e], acc[e]);
         }
     }
+    if (res) add_residual<T>(acc, res + p * C + c0);
     Vec<T>::store(y + p * C + c0, acc);
 }
 
 template <typename T>
 cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const float* base,
-                     const float* dyn, int64_t dyn_ld, T* y, cudaStream_t stream) {
+                     const float* dyn, int64_t dyn_ld, const T* res, T* y, cudaStream_t stream) {
     const int64_t nblocks = P / B;
     const int64_t total = nblocks * (C / Vec<T>::N);
     if (total == 0) return cudaSuccess;
@@ -297,25 +322,30 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
         // too few (block, chunk) pairs to fill the GPU: spread the rows instead
         const int64_t rows_total = P * (C / Vec<T>::N);
         conv_apply_rows_kernel<T><<<unsigned((rows_total + 255) / 256), 256, 0, stream>>>(
-            x, P, C, B, taps, g, G, base, dyn, dyn_ld, y);
+            x, P, C, B, taps, g, G, base, dyn, dyn_ld, res, y);
         note_launch();
         return cudaGetLastError();
     }
     int nt = kAsyncThreads;
-    const size_t slot = size_t(B) * (16 + size_t(taps) * 4);  // bytes per thread
+    const size_t slot = size_t(B) * ((res ? 32 : 16) + size_t(taps) * 4);  // bytes per thread
     while (nt > 64 && slot * nt > kAsyncSmemMax) nt /= 2;
     const size_t async_smem = slot * nt;
     if (taps <= 4 && async_smem <= kAsyncSmemMax) {
         const int strips = (C / Vec<T>::N + nt - 1) / nt;
         const unsigned agrid = unsigned(nblocks * strips);
         cudaError_t e = cudaSuccess;
-#define DF2_CONVA(TP)                                                                                       \
+#define DF2_CONVA_R(TP, R)                                                                                  \
     do {                                                                                                    \
-        e = cudaFuncSetAttribute(conv_apply_async_kernel<T, TP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 int(async_smem));                                                         \
+        e = cudaFuncSetAttribute(conv_apply_async_kernel<T, TP, R>,                                         \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(async_smem));            \
         if (e != cudaSuccess) return e;                                                                    \
-        conv_apply_async_kernel<T, TP><<<agrid, nt, async_smem, stream>>>(                                  \
-            x, nblocks, C, B, g, G, strips, base, dyn, dyn_ld, y);                                         \
+        conv_apply_async_kernel<T, TP, R><<<agrid, nt, async_smem, stream>>>(                               \
+            x, nblocks, C, B, g, G, strips, base, dyn, dyn_ld, res, y);                                    \
+    } while (0)
+#define DF2_CONVA(TP)                  \
+    do {                               \
+        if (res) DF2_CONVA_R(TP, true); \
+        else DF2_CONVA_R(TP, false);    \
     } while (0)
         switch (taps) {
             case 1: DF2_CONVA(1); break;
@@ -324,13 +354,14 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
             default: DF2_CONVA(4); break;
         }
 #undef DF2_CONVA
+#undef DF2_CONVA_R
         note_launch();
         return cudaGetLastError();
     }
     const unsigned grid = unsigned((total + 255) / 256);
 #define DF2_CONV(TP)                                                                               \
     conv_apply_kernel<T, TP><<<grid, 256, 0, stream>>>(x, nblocks, C, B, taps, g, G, base, dyn,    \
-                                                       dyn_ld, y)
+                                                       dyn_ld, res, y)
     switch (taps) {
         case 1: DF2_CONV(1); break;
         case 2: DF2_CONV(2); break;
@@ -501,12 +532,12 @@ int prepare_rows_per_cta(int64_t P, int C, int B, int esz) {
 
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
                               const float* base_io, const float* dyn, int64_t dyn_ld, void* y,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const void* res) {
     if (f32)
         return launch_t<float>(static_cast<const float*>(x), P, C, B, taps, g, base_io, dyn, dyn_ld,
-                               static_cast<float*>(y), stream);
+                               static_cast<const float*>(res), static_cast<float*>(y), stream);
     return launch_t<uint16_t>(static_cast<const uint16_t*>(x), P, C, B, taps, g, base_io, dyn,
-                              dyn_ld, static_cast<uint16_t*>(y), stream);
+                              dyn_ld, static_cast<const uint16_t*>(res), static_cast<uint16_t*>(y), stream);
 }
 
 }  // namespace df2

@@ -29,6 +29,9 @@
 // nothing spins.
 #include <cooperative_groups.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "selector_dev.cuh"
@@ -67,7 +70,7 @@ draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part
     const int t = int(cluster.block_rank());
     const int64_t p = blockIdx.x;
     const int q = int(p / B), T = B - 1;
-    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
     // CTA 0's table: for slot s and predecessor i, the best candidate's column,
     // token id and score
     int* tab_j = reinterpret_cast<int*>(smem + tab_off);
@@ -202,6 +205,9 @@ cudaError_t dispatch_tail(bool probe_only, bool* fits, const TopkParts& parts, i
     return e;
 }
 
+std::mutex g_fit_mu;
+std::unordered_map<uint64_t, bool> g_fit;  // cluster-shape probe results
+
 }  // namespace
 
 bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
@@ -210,11 +216,25 @@ bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
     // for short candidate lists
     if (P < 1 || B < 2 || B > kMaxCluster || K > kMaxLatticeK || r > 4096 || P % B != 0) return false;
     if (tail_smem(B, K, r, S) > 200 * 1024) return false;
+    // whether one cluster of this shape fits on an SM group depends on the cluster
+    // size, the instance and its shared memory, not on P: probe once per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const size_t smem = tail_smem(B, K, r, S);
+    const uint64_t key = (uint64_t(unsigned(dev)) << 48) ^ (uint64_t(B) << 40) ^ (uint64_t(K <= 32) << 39) ^
+                         (uint64_t((r + 255) / 256) << 32) ^ uint64_t(smem);
+    {
+        std::lock_guard<std::mutex> lock(g_fit_mu);
+        auto it = g_fit.find(key);
+        if (it != g_fit.end()) return it->second;
+    }
     bool fits = false;
     const TopkParts probe{nullptr, nullptr, S};
     if (dispatch_tail(true, &fits, probe, P, K, nullptr, nullptr, nullptr, B, nullptr, nullptr, nullptr, 1, r,
                       nullptr, nullptr, nullptr, nullptr, nullptr, LogitMap{}, nullptr) != cudaSuccess)
-        return false;
+        fits = false;
+    std::lock_guard<std::mutex> lock(g_fit_mu);
+    g_fit[key] = fits;
     return fits;
 }
 

@@ -104,6 +104,6 @@ cudaError_t conv_prepare_rows_launch(const void* x, bool f32, int64_t P, int C, 
                                      cudaStream_t stream);
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
                               const float* base_io, const float* dyn, int64_t dyn_ld, void* y,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const void* res = nullptr);
 
 }  // namespace df2

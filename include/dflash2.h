@@ -12,6 +12,7 @@
  *   dflash2_lattice_walk          the greedy or sampling walk over that table
  *   dflash2_conv_prepare          the grouped dynamic causal conv before a sublayer
  *   dflash2_conv_finish           the same conv after the sublayer
+ *   dflash2_conv_finish_prepare   a finish and the next sublayer's prepare in one call
  *
  * Sources (web pages, cited by title and section):
  *   [vLLM]  "DFlash2", vLLM Speculators user guide: "Local Convolution",
@@ -343,6 +344,36 @@ int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int B, int 
  * ---------------------------------------------------------------------- */
 int dflash2_conv_finish(const void* z, int dtype, int64_t P, int C, int B, int taps, int g,
                         const float* dyn_out, const float* base, void* y, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_conv_finish_prepare — the two convs between consecutive sublayers.
+ *
+ * ([vLLM] "Local Convolution": every attention and MLP sublayer is wrapped by a
+ * conv before and after it.)  The finish of one sublayer, then the prepare of the
+ * next, with the sum in between written out:
+ *   h        = dflash2_conv_finish(z; dyn_out, base)  (+ residual)
+ *   y_next, dyn_out_next = dflash2_conv_prepare(h; W_proj, base_next)
+ * The pages do not state the residual wiring between the two convs.  Here the
+ * caller passes the residual stream (or NULL for none), and the sum is rounded to
+ * dtype as a separate elementwise add in dtype would round it.  The results are
+ * bit-identical to dflash2_conv_finish, that add, and dflash2_conv_prepare.  The
+ * add happens in the finish kernel's store, so h is written once and never re-read
+ * for the add; the prepare then reads it.
+ *
+ *   z, residual (nullable), h        [P, C] dtype; h out
+ *   dyn_out [P, taps, G] fp32, base [2, taps, C] fp32   the finishing conv's (uses base[1])
+ *   W_proj [2*taps*G, C] bf16, base_next [2, taps, C]    the next conv's
+ *   y_next [P, C] dtype out; dyn_out_next [P, taps, G] fp32 out
+ *   workspace >= dflash2_conv_finish_prepare_workspace_size(P, C, taps, g, dtype)
+ * Rules as for dflash2_conv_prepare; no output may alias an input, and y_next
+ * must not alias h (DF2_ERR_INVALID_ARGUMENT).
+ * ---------------------------------------------------------------------- */
+size_t dflash2_conv_finish_prepare_workspace_size(int64_t P, int C, int taps, int g, int dtype);
+int dflash2_conv_finish_prepare(const void* z, int dtype, int64_t P, int C, int B, int taps, int g,
+                                const float* dyn_out, const float* base, const void* residual, void* h,
+                                const uint16_t* W_proj, const float* base_next, void* y_next,
+                                float* dyn_out_next, void* workspace, size_t workspace_bytes,
+                                void* stream);
 
 /* ------------------------------------------------------------------------
  * dflash2_selftest_wait_timeout — exercises the in-kernel timeout path.

@@ -124,6 +124,20 @@ def test_conv_validation(lib):
     assert fin(fake, 0, 12, 64, 8, 2, 16, fake, fake, fake2, None) == 1
     assert fin(fake, 0, 0, 64, 8, 2, 16, fake, fake, fake2, None) == 0
     assert lib.dflash2_conv_prepare_workspace_size(16, 64, 2, 16, 0) == 512
+    fp = lib.dflash2_conv_finish_prepare
+    f3, f4, f5, f6 = VP(0x3000), VP(0x4000), VP(0x5000), VP(0x6000)
+    ok = dict(z=fake, dyn=fake2, base=f3, res=None, h=f4, W=f5, bn=f3, y=f6, dn=VP(0x7000))
+    call = lambda d, P=16, B=8, ws=1 << 20: fp(d["z"], 0, P, 64, B, 2, 16, d["dyn"], d["base"], d["res"], d["h"],
+                                             d["W"], d["bn"], d["y"], d["dn"], fake, ws, None)
+    assert call(ok, P=12) == 1                                   # P % B != 0
+    assert call({**ok, "h": fake}) == 1                          # h aliases z
+    assert call({**ok, "res": f4}) == 1                          # h aliases the residual
+    assert call({**ok, "y": f4}) == 1                            # y_next aliases h
+    assert call({**ok, "y": fake}) == 1                          # y_next aliases z
+    assert call({**ok, "dn": fake2}) == 1                        # dyn_out_next aliases dyn_out
+    assert call(ok, ws=16) == 4                                  # workspace too small
+    assert call(ok, P=0) == 0
+    assert lib.dflash2_conv_finish_prepare_workspace_size(16, 64, 2, 16, 0) == 512
 
 
 def test_product_path_does_not_reach_the_oracle():
