@@ -3,8 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 One step = one pass of the whole head over one draft batch of the workload:
-conv_prepare -> conv_finish (one sublayer's conv pair) -> unary_topk (logits,
-top-K, hidden projection) -> selector_walk -> selector_pair_scores.  Inputs are
+conv_prepare -> conv_finish (one sublayer's conv pair) -> draft_head (unary
+logits, top-K and hidden projection, the selector walk and the teacher-forced
+scores in one call).  The timed steps replay those calls captured as two CUDA
+graphs; the end-to-end leg makes the calls directly with host buffers.  Inputs are
 seeded synthetic tensors (see workloads/), resident in HBM before timing; the
 step streams the whole LM head (1.25 GB for the default batch-1 workload, larger
 than the 129 MB L2), so no separate L2 flush is needed for the default workload;
@@ -51,8 +53,8 @@ def load_peaks():
 # sources whose hash the summary records.
 PROFILES = {
     "batch1": ("head_skinny_kernel_batch1.md", ["head_tc.cu", "topk_warp.cuh", "tc_ptx.cuh", "common.cuh"]),
-    "batched": ("gemm_wide_topk_batched.md", ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh"]),
-    "stress": ("gemm_wide_topk_stress.md", ["gemm_tc.cu", "tc_ptx.cuh", "common.cuh"]),
+    "batched": ("gemm_wide_topk_batched.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
+    "stress": ("gemm_wide_topk_stress.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
 }
 
 
@@ -342,6 +344,7 @@ class Step:
         dt = df2.DF2_DTYPE_BF16 if w.act == "bf16" else df2.DF2_DTYPE_F32
         self.ws_conv = e(max(1, df2.conv_prepare_workspace_size(P, w.C, w.taps, w.g, dt)),
                          dtype=torch.uint8, device=device)
+        self.torch = torch
         self.flush = None
         if w.V * w.D * 2 <= 256 << 20:
             self.flush = e(256 << 20, dtype=torch.uint8, device=device)
@@ -364,6 +367,28 @@ class Step:
                      workspace=self.ws_draft,
                      out=(self.ids, self.vals, self.Gt, self.path, self.pscore, self.scores))
         self._rec(ev[3])
+
+    def capture(self):
+        """The step as two CUDA graphs -- the conv calls, then the draft head call --
+        so that replaying them launches the same kernels without the host's per-call
+        work between them.  Returns None when capture is not possible here."""
+        torch = self.torch
+        try:
+            g_conv, g_head = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            d, w = self.df2, self.w
+            with torch.cuda.graph(g_conv):
+                d.conv_prepare(self.x, w.B, w.taps, w.g, self.W_proj, self.base, workspace=self.ws_conv,
+                               out=(self.y, self.dyn))
+                d.conv_finish(self.z, w.B, w.taps, w.g, self.dyn, self.base, out=self.y2)
+            with torch.cuda.graph(g_head):
+                d.draft_head(self.h, self.W_lm, w.K, self.W_H, self.A, self.Bc, self.anchors, w.B, self.pred,
+                             workspace=self.ws_draft,
+                             out=(self.ids, self.vals, self.Gt, self.path, self.pscore, self.scores))
+            torch.cuda.synchronize()
+            return g_conv, g_head
+        except RuntimeError:
+            torch.cuda.synchronize()
+            return None
 
     def run_separate(self, events):
         """The draft head as its three separate calls, an event between each (for the
@@ -415,10 +440,17 @@ def gpu_arm(args, w, rank, world, torch):
             step.flush.zero_()
     torch.cuda.synchronize()
     n_launch = count_launches(step, torch, df2)
+    graphs = step.capture()
+    if graphs is not None:
+        for _ in range(args.warmup):
+            graphs[0].replay()
+            graphs[1].replay()
+        torch.cuda.synchronize()
 
-    # ---- device-resident timing (W warm-up done above).  Inside the timed region
-    # only the head call is bracketed by events (every event between kernels
-    # drains the launch pipeline, so more of them would inflate the step).
+    # ---- device-resident timing (W warm-up done above).  Each step replays the
+    # conv graph and the draft-head graph (or, where capture is not possible, makes
+    # the calls).  Only the head call is bracketed by events: every event between
+    # kernels drains the launch pipeline, so more of them would inflate the step.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     flush_ms = 0.0
@@ -429,12 +461,21 @@ def gpu_arm(args, w, rank, world, torch):
     with ClockSampler(local) as clk:
         t0.record()
         for s in range(args.steps):
-            step.run(evs[s])
+            if graphs is not None:
+                graphs[0].replay()
+                evs[s][0].record()
+                graphs[1].replay()
+                evs[s][1].record()
+            else:
+                step.run(evs[s])
             if step.flush is not None:
                 step.flush.zero_()
         t1.record()
         torch.cuda.synchronize()
-    timed_launches = df2.kernels_launched() - launched0
+    # a graph replay launches the captured kernels without passing through the
+    # library, whose counter therefore counts them per step
+    timed_launches = (n_launch * args.steps if graphs is not None
+                      else df2.kernels_launched() - launched0)
     if dist is not None:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
@@ -553,6 +594,8 @@ def gpu_arm(args, w, rank, world, torch):
             "e2e": {"value": job_throughput(w.P, world, e2e_ms), "unit": "positions/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": timed_launches,
+            "execution": ("each step replays two CUDA graphs captured from the public calls (conv prepare + "
+                          "finish; draft head)" if graphs is not None else "eager calls"),
             "kernels_per_step": n_launch,
             "clocks": clocks,
         }

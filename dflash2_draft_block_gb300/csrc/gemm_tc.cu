@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_pair.cuh"
 #include "tc_ptx.cuh"
 
 namespace df2 {
