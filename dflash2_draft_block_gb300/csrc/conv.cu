@@ -107,7 +107,7 @@ conv_apply_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, int ta
             }
     }
 
-    if (TAPS > 0) {
+    if constexpr (TAPS > 0) {
         // Rows are taken kGroup at a time: all of a group's loads (x and the dynamic
         // corrections) are issued before any is used, so each thread keeps kGroup
         // 16-byte loads in flight instead of one.
@@ -158,33 +158,32 @@ conv_apply_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, int ta
                 Vec<T>::store(y + p * C + c0, acc);
             }
         }
-        return;
-    }
-
-    for (int t = 0; t < B; ++t) {
-        const int64_t p = nb * B + t;
-        float cur[N], acc[N];
-        Vec<T>::load(x + p * C + c0, cur);
-#pragma unroll
-        for (int e = 0; e < N; ++e) acc[e] = 0.f;
-        const float* drow = dyn + p * dyn_ld;
-        for (int j = 0; j < taps && j <= t; ++j) {
-            float xv[N];
-            if (j == 0) {
-#pragma unroll
-                for (int e = 0; e < N; ++e) xv[e] = cur[e];
-            } else {
-                Vec<T>::load(x + (p - j) * C + c0, xv);
+    } else {
+        for (int t = 0; t < B; ++t) {
+            const int64_t p = nb * B + t;
+            float cur[N], acc[N];
+            Vec<T>::load(x + p * C + c0, cur);
+    #pragma unroll
+            for (int e = 0; e < N; ++e) acc[e] = 0.f;
+            const float* drow = dyn + p * dyn_ld;
+            for (int j = 0; j < taps && j <= t; ++j) {
+                float xv[N];
+                if (j == 0) {
+    #pragma unroll
+                    for (int e = 0; e < N; ++e) xv[e] = cur[e];
+                } else {
+                    Vec<T>::load(x + (p - j) * C + c0, xv);
+                }
+    #pragma unroll
+                for (int e = 0; e < N; ++e) {
+                    const float d = __ldg(drow + j * G + (c0 + e) / g);
+                    const float k = __ldg(base + int64_t(j) * C + c0 + e) + d;
+                    acc[e] = fmaf(k, xv[e], acc[e]);
+                }
             }
-#pragma unroll
-            for (int e = 0; e < N; ++e) {
-                const float d = __ldg(drow + j * G + (c0 + e) / g);
-                const float k = __ldg(base + int64_t(j) * C + c0 + e) + d;
-                acc[e] = fmaf(k, xv[e], acc[e]);
-            }
+            if (res) add_residual<T>(acc, res + p * C + c0);
+            Vec<T>::store(y + p * C + c0, acc);
         }
-        if (res) add_residual<T>(acc, res + p * C + c0);
-        Vec<T>::store(y + p * C + c0, acc);
     }
 }
 
