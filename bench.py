@@ -604,6 +604,135 @@ def gpu_arm(args, w, rank, world, torch):
     return out
 
 
+# ------------------------------------------------------------- conv arm --
+
+def conv_config(w):
+    return {"workload": f"{w.name}: training-packed conv, {w.R} blocks of {w.B} rows (P={w.P} positions), "
+                        f"C={w.C}, taps={w.taps}, group={w.g} (G={w.G}), projection {w.C} -> {2 * w.taps * w.G}",
+            "positions_per_step": w.P,
+            "l2": "inputs larger than L2: x and z are 168 MB each; W_proj (13 MB) stays resident like any weight"}
+
+
+def conv_arm(args, w, rank, world, torch):
+    """The training-packed conv workload: one step is conv_prepare then conv_finish
+    over all P rows.  Events around each call give the live per-call durations: the
+    prepare call against the tensor peak (its projection is the contraction), the
+    finish call against HBM."""
+    import dflash2_draft_block_gb300 as df2
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    c = W.conv_inputs(w)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    x, z = bf(c["x"]), bf(c["z"])
+    W_proj, base = bf(c["W_proj"]), torch.from_numpy(c["base"]).to(device)
+    y, y2 = torch.empty_like(x), torch.empty_like(z)
+    dyn = torch.empty((w.P, w.taps, w.G), dtype=torch.float32, device=device)
+    ws = torch.empty(max(1, df2.conv_prepare_workspace_size(w.P, w.C, w.taps, w.g)), dtype=torch.uint8,
+                     device=device)
+
+    def run(ev=None):
+        if ev is not None:
+            ev[0].record()
+        df2.conv_prepare(x, w.B, w.taps, w.g, W_proj, base, workspace=ws, out=(y, dyn))
+        if ev is not None:
+            ev[1].record()
+        df2.conv_finish(z, w.B, w.taps, w.g, dyn, base, out=y2)
+        if ev is not None:
+            ev[2].record()
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    before = df2.kernels_launched()
+    run()
+    torch.cuda.synchronize()
+    n_launch = df2.kernels_launched() - before
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launched0 = df2.kernels_launched()
+    with ClockSampler(local) as clk:
+        t0.record()
+        for s in range(args.steps):
+            run(evs[s])
+        t1.record()
+        torch.cuda.synchronize()
+    timed_launches = df2.kernels_launched() - launched0
+    step_ms = slowest_rank_ms(t0.elapsed_time(t1) / args.steps, dist, device)
+    prep_us = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps * 1e3
+    fin_us = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps * 1e3
+
+    # end to end: x and z in from pinned host memory, y, dyn_out and the finish output back
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+    hx, hz = pin(x), pin(z)
+    hx.copy_(x)
+    hz.copy_(z)
+    outs = [y, dyn, y2]
+    houts = [pin(o) for o in outs]
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        z.copy_(hz, non_blocking=True)
+        run()
+        for o, ho in zip(outs, houts):
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(e0.elapsed_time(e1) / args.steps, dist, device)
+    h2d = (x.numel() + z.numel()) * 2
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    clocks = clk.summary()
+    out = None
+    if rank == 0:
+        peaks, src = load_peaks()
+        flops = 2.0 * w.P * w.C * (2 * w.taps * w.G)
+        pk = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        roof = {"kernel": "dflash2_conv_prepare call: the projection GEMM (gemm_wide_kernel, store epilogue) "
+                          "+ the conv apply", "bound": "tensor",
+                "achieved": flops / (prep_us * 1e-6) / 1e12, "peak": pk, "unit": "TFLOP/s",
+                "algorithmic_flops": flops, "peak_source": src, "traffic": None,
+                "traffic_note": "the call's time includes its apply kernel, so this understates the GEMM's rate"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        fb = conv_bytes(w, "finish")
+        roof_fin = {"kernel": "dflash2_conv_finish call: conv_apply_async_kernel", "bound": "hbm",
+                    "achieved": fb / (fin_us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "algorithmic_bytes": fb, "peak_source": src}
+        roof_fin["frac"] = roof_fin["achieved"] / roof_fin["peak"]
+        out = {
+            "metric": METRIC, "value": job_throughput(w.P, world, step_ms), "unit": "positions/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes and scales of the workload, no dataset or checkpoint)",
+            "config": conv_config(w),
+            "per_call_us": {"conv_prepare": prep_us, "conv_finish": fin_us},
+            "conv_gbs": {"prepare": conv_bytes(w, "prepare") / (prep_us * 1e-6) / 1e9,
+                         "finish": fb / (fin_us * 1e-6) / 1e9},
+            "roofline": roof, "roofline_finish": roof_fin,
+            "e2e": {"value": job_throughput(w.P, world, e2e_ms), "unit": "positions/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": timed_launches, "kernels_per_step": n_launch, "execution": "eager calls",
+            "clocks": clocks,
+        }
+    if dist is not None:
+        dist.destroy_process_group()
+    return out
+
+
 # ------------------------------------------------------------ oracle arm --
 
 def oracle_step(orc, w, inp, conv):
@@ -623,7 +752,33 @@ def oracle_sample(w):
     return w.scaled(R=R), R
 
 
+def cpu_arm_conv(w, steps, warmup):
+    """The oracle's conv pair on a bounded slice of the conv workload: 16 anchor
+    blocks per step."""
+    import oracle
+    orc = oracle.default()
+    nb = min(w.R, 16)
+    ws = w.scaled(R=nb)
+    conv = W.conv_inputs(ws)
+
+    def step():
+        _, dyn = orc.conv_prepare(conv["x"], ws.B, ws.taps, ws.g, conv["W_proj"], conv["base"])
+        orc.conv_finish(conv["z"], ws.B, ws.taps, ws.g, dyn, conv["base"])
+
+    for _ in range(warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t) / max(1, steps)
+    sample = (f"{nb} of {w.R} anchor blocks ({ws.P} positions) per step: conv prepare (projection "
+              f"{w.C} -> {2 * w.taps * w.G} in fp64) and conv finish on them")
+    return ws.P / dt, orc.num_threads(), sample, dt
+
+
 def cpu_arm(w, steps, warmup):
+    if w.conv_only:
+        return cpu_arm_conv(w, steps, warmup)
     import oracle
     orc = oracle.default()
     ws, R = oracle_sample(w)
@@ -648,7 +803,7 @@ def main():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="batch1", choices=[c.name for c in W.CONFIGS if not c.conv_only])
+    ap.add_argument("--workload", default="batch1", choices=[c.name for c in W.CONFIGS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.steps is None:
@@ -664,7 +819,8 @@ def main():
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w),
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": conv_config(w) if w.conv_only else config_of(w),
                 "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores,
                                  "kind": "oracle", "sample": sample},
                 "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
@@ -679,7 +835,7 @@ def main():
         cpu = {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
                "sample": sample}
     import torch
-    out = gpu_arm(args, w, rank, world, torch)
+    out = (conv_arm if w.conv_only else gpu_arm)(args, w, rank, world, torch)
     if rank == 0:
         out["cpu_baseline"] = cpu
         print(json.dumps(out), flush=True)

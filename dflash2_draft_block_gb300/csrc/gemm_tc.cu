@@ -44,6 +44,8 @@ struct WideArgs {
     int n_nt;               // N tiles
     int tiles_per_cta;      // consecutive N tiles per CTA
     int m_major;            // 1: consecutive CTAs share an M tile; 0: share an N range
+    int linear;             // 1 (store only): unit u takes tiles [u*tiles_per_cta, ...) of the
+                            // M-fastest order of all (M tile or pair, N tile)
     int nstages, kbox;
     // STORE
     float* out0;
@@ -153,6 +155,17 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     const int grp = args.m_major ? unit % n_groups : unit / n_mu;
     const int nt0 = grp * args.tiles_per_cta;
     const int nt1 = min(args.n_nt, nt0 + args.tiles_per_cta);
+    // this CTA's tiles k = 0 .. ntiles-1: a fixed M tile over N tiles nt0.., or (linear)
+    // a run of the M-fastest order, which lets one unit's store epilogue overlap its
+    // next tile's MMAs
+    const int tau0 = unit * args.tiles_per_cta;
+    const int ntiles = args.linear ? max(0, min(n_mu * args.n_nt, tau0 + args.tiles_per_cta) - tau0) : nt1 - nt0;
+    auto tile_nt = [&](int k) { return args.linear ? (tau0 + k) / n_mu : nt0 + k; };
+    auto tile_mt = [&](int k) {
+        if (!args.linear) return mt;
+        const int mu_k = (tau0 + k) % n_mu;
+        return PAIR ? 2 * mu_k + int(rank) : mu_k;
+    };
     const int nbox = (args.Kd + WK - 1) / WK;
     const int nk = (nbox + kbox - 1) / kbox;
 
@@ -202,7 +215,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             int8_t armed[kWideMaxStages];
             for (int s = 0; s < kWideMaxStages; ++s) armed[s] = -1;
             bool ok = true;
-            for (int nt = nt0; nt < nt1 && ok; ++nt) {
+            for (int k = 0; k < ntiles && ok; ++k) {
+                const int nt = tile_nt(k), mtk = tile_mt(k);
                 for (int kb = 0; kb < nk; ++kb) {
                     const int nb = min(kbox, nbox - kb * kbox);
                     if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
@@ -217,10 +231,10 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                         uint8_t* db = st + size_t(kbox) * kABox + size_t(j) * kBBox;
                         if (PAIR) {
                             const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
-                            tc::tma_load_2d_pair(da, &tm_a, fb, x, mt * WM, pol_a);
+                            tc::tma_load_2d_pair(da, &tm_a, fb, x, mtk * WM, pol_a);
                             tc::tma_load_2d_pair(db, &tm_b, fb, x, yb, pol_b);
                         } else {
-                            tc::tma_load_2d(da, &tm_a, &full[stage], x, mt * WM, pol_a);
+                            tc::tma_load_2d(da, &tm_a, &full[stage], x, mtk * WM, pol_a);
                             tc::tma_load_2d(db, &tm_b, &full[stage], x, yb, pol_b);
                         }
                     }
@@ -245,7 +259,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int nt = nt0; nt < nt1 && ok; ++nt, ++it) {
+            for (int k = 0; k < ntiles && ok; ++k, ++it) {
                 const int b = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
                 const bool drained = PAIR ? tc::mbar_wait_cluster(&tempty[b], tph ^ 1, abort_flag)
@@ -296,7 +310,11 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         // logit strictly below it cannot be in the global top-K.
         float gthr = -INFINITY;
         int it = 0;
-        for (int nt = nt0; nt < nt1; ++nt, ++it) {
+        for (int k = 0; k < ntiles; ++k, ++it) {
+            const int nt = tile_nt(k);
+            // the store epilogue's row for this tile (the top-K epilogue's is fixed)
+            const int ms = tile_mt(k) * WM + quarter * 32 + lane;
+            const bool ms_ok = ms < args.M;
             const int b = it & 1;
             const uint32_t tph = (it >> 1) & 1;
             const bool got = tc::mbar_wait(&tfull[b], tph, abort_flag);
@@ -308,12 +326,12 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                 tc::tmem_ld16(taddr + uint32_t(c0), v);
                 const int n0 = nt * WN + c0;
                 if (EPI == EPI_STORE) {
-                    if (row_ok) {
+                    if (ms_ok) {
                         const bool whole = n0 + 16 <= args.N;
                         const bool side0 = n0 + 16 <= args.n_split, side1 = n0 >= args.n_split;
                         float* dst = nullptr;
-                        if (side0) dst = args.out0 + int64_t(m) * args.ld0 + n0;
-                        else if (side1) dst = args.out1 + int64_t(m) * args.ld1 + (n0 - args.n_split);
+                        if (side0) dst = args.out0 + int64_t(ms) * args.ld0 + n0;
+                        else if (side1) dst = args.out1 + int64_t(ms) * args.ld1 + (n0 - args.n_split);
                         if (whole && dst && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
@@ -324,8 +342,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                             for (int e = 0; e < 16; ++e) {
                                 const int n = n0 + e;
                                 if (n >= args.N) break;
-                                if (n < args.n_split) args.out0[int64_t(m) * args.ld0 + n] = v[e];
-                                else args.out1[int64_t(m) * args.ld1 + (n - args.n_split)] = v[e];
+                                if (n < args.n_split) args.out0[int64_t(ms) * args.ld0 + n] = v[e];
+                                else args.out1[int64_t(ms) * args.ld1 + (n - args.n_split)] = v[e];
                             }
                         }
                     }
@@ -472,10 +490,12 @@ int wide_groups(int n_mt, int n_nt, int num_sms) {
 // its CTA still stages its half of every B tile).
 struct WidePlan {
     bool pair;
+    bool linear;        // store: units take runs of the M-fastest tile order
     int n_mt, n_nt;     // 128-row M tiles, 256-row N tiles
     int n_mu;           // work units along M: tiles, or pairs of tiles
-    int tiles_per_cta;  // consecutive N tiles per unit
-    int n_groups;       // N ranges per unit
+    int tiles_per_cta;  // tiles per unit (consecutive N tiles, or a run of the linear order)
+    int n_groups;       // N ranges per unit (top-K)
+    int units;          // units launched (each one CTA or one CTA pair)
     int nstages;
 };
 
@@ -487,13 +507,20 @@ WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persi
     p.pair = p.n_mt >= 2 && wide_stages(epi, K, true) >= 2;
     p.n_mu = p.pair ? (p.n_mt + 1) / 2 : p.n_mt;
     p.nstages = wide_stages(epi, K, p.pair);
+    const int slots = p.pair ? num_sms / 2 : num_sms;
     if (persistent) {
-        const int groups = wide_groups(p.n_mu, p.n_nt, p.pair ? num_sms / 2 : num_sms);
+        const int groups = wide_groups(p.n_mu, p.n_nt, slots);
         p.tiles_per_cta = (p.n_nt + groups - 1) / groups;
+        p.n_groups = (p.n_nt + p.tiles_per_cta - 1) / p.tiles_per_cta;
+        p.units = p.n_mu * p.n_groups;
     } else {
-        p.tiles_per_cta = 1;
+        // at most one wave of units, each a run of whole tiles
+        const int total = p.n_mu * p.n_nt;
+        p.linear = true;
+        p.tiles_per_cta = (total + slots - 1) / slots;
+        p.n_groups = p.n_nt;
+        p.units = (total + p.tiles_per_cta - 1) / p.tiles_per_cta;
     }
-    p.n_groups = (p.n_nt + p.tiles_per_cta - 1) / p.tiles_per_cta;
     return p;
 }
 
@@ -525,7 +552,7 @@ cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const Wide
 template <int EPI>
 cudaError_t launch_plan(const WidePlan& p, const CUtensorMap& ta, const CUtensorMap& tb, const WideArgs& a,
                         cudaStream_t stream) {
-    const int grid = (p.pair ? 2 : 1) * p.n_mu * p.n_groups;
+    const int grid = (p.pair ? 2 : 1) * p.units;
     return p.pair ? launch_wide<EPI, 256, true>(ta, tb, a, grid, stream)
                   : launch_wide<EPI, 256, false>(ta, tb, a, grid, stream);
 }
@@ -545,7 +572,11 @@ size_t wide_topk_workspace(int64_t M, int64_t N, int K, int num_sms) {
 cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd,
                               float* out0, int64_t ld0, int64_t n_split, float* out1, int64_t ld1,
                               int32_t* dev_status, cudaStream_t stream) {
-    const WidePlan p = wide_plan(EPI_STORE, M, N, 0, 0, false);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return cudaErrorInvalidValue;
+    const WidePlan p = wide_plan(EPI_STORE, M, N, 0, sms, false);
     CUtensorMap ta, tb;
     if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, p.pair ? 128 : 256))
         return cudaErrorInvalidValue;
@@ -555,6 +586,7 @@ cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, i
     a.n_nt = p.n_nt;
     a.tiles_per_cta = p.tiles_per_cta;
     a.m_major = 1;
+    a.linear = p.linear ? 1 : 0;
     a.nstages = p.nstages;
     a.kbox = 1;
     a.out0 = out0; a.ld0 = ld0; a.n_split = int(n_split); a.out1 = out1; a.ld1 = ld1;
