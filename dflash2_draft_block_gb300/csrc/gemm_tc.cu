@@ -44,8 +44,9 @@ struct WideArgs {
     int n_nt;               // N tiles
     int tiles_per_cta;      // consecutive N tiles per CTA
     int m_major;            // 1: consecutive CTAs share an M tile; 0: share an N range
-    int linear;             // 1 (store only): unit u takes tiles [u*tiles_per_cta, ...) of the
-                            // M-fastest order of all (M tile or pair, N tile)
+    int linear;             // 1 (store only): the tiles, numbered N-fastest over (M tile or
+                            // pair, N tile), dealt round-robin to n_units units
+    int n_units;
     int nstages, kbox;
     // STORE
     float* out0;
@@ -156,14 +157,16 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     const int nt0 = grp * args.tiles_per_cta;
     const int nt1 = min(args.n_nt, nt0 + args.tiles_per_cta);
     // this CTA's tiles k = 0 .. ntiles-1: a fixed M tile over N tiles nt0.., or (linear)
-    // a run of the M-fastest order, which lets one unit's store epilogue overlap its
-    // next tile's MMAs
-    const int tau0 = unit * args.tiles_per_cta;
-    const int ntiles = args.linear ? max(0, min(n_mu * args.n_nt, tau0 + args.tiles_per_cta) - tau0) : nt1 - nt0;
-    auto tile_nt = [&](int k) { return args.linear ? (tau0 + k) / n_mu : nt0 + k; };
+    // tiles unit, unit + n_units, ... of the N-fastest numbering.  In the linear walk a
+    // unit's store epilogue overlaps its next tile's MMAs, and at every step the units
+    // work on consecutive tiles, which share their A rows in L2.
+    const int total = n_mu * args.n_nt;
+    const int ntiles = args.linear ? (unit < total ? (total - unit + args.n_units - 1) / args.n_units : 0)
+                                   : nt1 - nt0;
+    auto tile_nt = [&](int k) { return args.linear ? (unit + k * args.n_units) % args.n_nt : nt0 + k; };
     auto tile_mt = [&](int k) {
         if (!args.linear) return mt;
-        const int mu_k = (tau0 + k) % n_mu;
+        const int mu_k = (unit + k * args.n_units) / args.n_nt;
         return PAIR ? 2 * mu_k + int(rank) : mu_k;
     };
     const int nbox = (args.Kd + WK - 1) / WK;
@@ -514,12 +517,12 @@ WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persi
         p.n_groups = (p.n_nt + p.tiles_per_cta - 1) / p.tiles_per_cta;
         p.units = p.n_mu * p.n_groups;
     } else {
-        // at most one wave of units, each a run of whole tiles
+        // one wave of units dealt the tiles round-robin
         const int total = p.n_mu * p.n_nt;
         p.linear = true;
-        p.tiles_per_cta = (total + slots - 1) / slots;
+        p.units = total < slots ? total : slots;
+        p.tiles_per_cta = (total + p.units - 1) / p.units;
         p.n_groups = p.n_nt;
-        p.units = (total + p.tiles_per_cta - 1) / p.tiles_per_cta;
     }
     return p;
 }
@@ -587,6 +590,7 @@ cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, i
     a.tiles_per_cta = p.tiles_per_cta;
     a.m_major = 1;
     a.linear = p.linear ? 1 : 0;
+    a.n_units = p.units;
     a.nstages = p.nstages;
     a.kbox = 1;
     a.out0 = out0; a.ld0 = ld0; a.n_split = int(n_split); a.out1 = out1; a.ld1 = ld1;
