@@ -55,6 +55,7 @@ PROFILES = {
     "batch1": ("head_skinny_kernel_batch1.md", ["head_tc.cu", "topk_warp.cuh", "tc_ptx.cuh", "common.cuh"]),
     "batched": ("gemm_wide_topk_batched.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
     "stress": ("gemm_wide_topk_stress.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
+    "conv": ("gemm_wide_store_conv.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
 }
 
 
@@ -705,8 +706,10 @@ def conv_arm(args, w, rank, world, torch):
         roof = {"kernel": "dflash2_conv_prepare call: the projection GEMM (gemm_wide_kernel, store epilogue) "
                           "+ the conv apply", "bound": "tensor",
                 "achieved": flops / (prep_us * 1e-6) / 1e12, "peak": pk, "unit": "TFLOP/s",
-                "algorithmic_flops": flops, "peak_source": src, "traffic": None,
-                "traffic_note": "the call's time includes its apply kernel, so this understates the GEMM's rate"}
+                "algorithmic_flops": flops, "peak_source": src,
+                "traffic_note": "the call's time includes its apply kernel, so this understates the GEMM's rate; "
+                                "traffic is the projection GEMM's DRAM bytes per launch (ncu)"}
+        roof["traffic"], roof["traffic_source"] = head_traffic(w.name)
         roof["frac"] = roof["achieved"] / roof["peak"]
         fb = conv_bytes(w, "finish")
         roof_fin = {"kernel": "dflash2_conv_finish call: conv_apply_async_kernel", "bound": "hbm",
