@@ -7,14 +7,13 @@
 // teacher-forced scorer takes the predecessor as given (PR #62, "Selector
 // training objective").
 //
-// The walk runs one CTA per request with its gathers staged in shared memory
-// (walk_request_cta, selector_dev.cuh) when they fit, else one warp per request;
-// the teacher-forced scores run one warp per (row, group of 8 candidates).  Lane
-// l owns rank elements [8l, 8l+8) of every 256-wide chunk: the gate
-// q = A[a] (.) G_t is formed once per position in registers, each candidate's B
-// row is read with one 16-byte load per lane per chunk, and a shuffle tree sums
-// the lanes.  The warp walk's candidate loop is unrolled by 4 so that four B-row
-// gathers are in flight.
+// The walk runs one CTA per request: with its gathers staged in shared memory
+// (walk_request_cta, selector_dev.cuh) when they fit, else reading them from L2
+// one step after they were prefetched (walk_l2_kernel).  The teacher-forced scores
+// run one warp per (row, group of 8 candidates).  Lane l owns rank elements
+// [8l, 8l+8) of every 256-wide chunk: the gate q = A[a] (.) G_t is formed once per
+// position in registers, each candidate's B row is read with one 16-byte load per
+// lane per chunk, and a shuffle tree sums the lanes.
 #include "common.cuh"
 #include "kernels.h"
 #include "selector_dev.cuh"
@@ -24,80 +23,6 @@ namespace df2 {
 namespace {
 
 using namespace sel;
-
-constexpr int kWarpsPerBlock = 4;
-
-// Scores of candidates [j0, j0+4) of one row against gate q; ids are in range.
-template <int NCH>
-__device__ __forceinline__ void score4(const int32_t* __restrict__ ids_row,
-                                       const float* __restrict__ vals_row, int K, int j0,
-                                       const uint16_t* __restrict__ Bc, int r, int lane,
-                                       const float q[NCH][8], float s[4], int b[4]) {
-    float part[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        b[u] = (j0 + u < K) ? __ldg(ids_row + j0 + u) : 0;
-        part[u] = (j0 + u < K) ? dot_lane<NCH>(Bc, b[u], r, lane, q) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const float d = warp_sum(part[u]);
-        s[u] = (j0 + u < K) ? __ldg(vals_row + j0 + u) + d : -INFINITY;
-    }
-}
-
-template <int NCH>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-walk_kernel(const int32_t* __restrict__ anchors, int R, int B, const int32_t* __restrict__ ids,
-            const float* __restrict__ vals, const float* __restrict__ G,
-            const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K, int r,
-            int32_t* __restrict__ path, float* __restrict__ path_scores,
-            int32_t* __restrict__ dev_status) {
-    const int lane = threadIdx.x & 31;
-    const int q = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    if (q >= R) return;
-    const int T = B - 1;
-
-    int32_t a = __ldg(anchors + q);
-    bool ok = a >= 0 && a < V;
-    for (int64_t e = lane; e < int64_t(T) * K; e += 32) {
-        const int32_t b = __ldg(ids + (int64_t(q) * B + 1) * K + e);
-        ok = ok && b >= 0 && b < V;
-    }
-    if (!__all_sync(kFull, ok)) {
-        for (int t = lane; t < T; t += 32) {
-            path[int64_t(q) * T + t] = -1;
-            path_scores[int64_t(q) * T + t] = __int_as_float(0x7fc00000);
-        }
-        if (lane == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
-        return;
-    }
-
-    for (int t = 1; t < B; ++t) {
-        const int64_t row = int64_t(q) * B + t;
-        float qv[NCH][8];
-        load_gate<NCH>(A, a, r, G + row * r, lane, qv);
-        float best = -INFINITY;
-        int best_id = -1;
-        for (int j0 = 0; j0 < K; j0 += 4) {
-            float s[4];
-            int b[4];
-            score4<NCH>(ids + row * K, vals + row * K, K, j0, Bc, r, lane, qv, s, b);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (j0 + u < K && (best_id < 0 || ranks_before(s[u], b[u], best, best_id))) {
-                    best = s[u];
-                    best_id = b[u];
-                }
-            }
-        }
-        if (lane == 0) {
-            path[int64_t(q) * T + (t - 1)] = best_id;
-            path_scores[int64_t(q) * T + (t - 1)] = best;
-        }
-        a = best_id;
-    }
-}
 
 // One warp per (row, group of kPairGroup candidates): the gate and the group's
 // B rows are independent loads, so a warp waits for about two memory latencies.
@@ -156,36 +81,33 @@ walk_cta_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __res
                                  dev_status, smem);
 }
 
-// Walk for requests whose gathers do not all fit in shared memory: one CTA per
-// request streams the steps.  The B rows and G row of step t+1 do not depend on
-// the choice at step t, so they are copied (cp.async, two buffers) while step t
-// runs, and the A rows of step t's candidates -- the possible predecessors at
-// step t+1 -- are prefetched into L2.  Warp w scores candidates w, w+8, ... with
-// the lane slicing and shuffle tree of the other walk kernels (bit-identical
-// scores); the warps' bests meet in shared memory.
 constexpr int kStreamThreads = 256;
 constexpr int kStreamWarps = kStreamThreads / 32;
 
-__host__ __device__ inline size_t walk_stream_smem(int K, int r) {
-    return 2 * (size_t(K) * r * 2 + size_t(r) * 4) + kStreamWarps * 16 + 64;
-}
+// Walk for requests whose gathers do not fit in shared memory, with nothing staged:
+// one CTA per request reads the candidates' B rows and the G row straight from L2,
+// where they were prefetched one step ahead (they do not depend on the choice), and
+// the first kPredPrefetch candidates' A rows -- the likeliest predecessors, the
+// candidates being sorted by unary value -- are prefetched too; any other
+// predecessor's A row is read on demand.  With a few hundred bytes of shared memory
+// every request is resident at once, so the steps' latencies overlap across
+// requests instead of running in waves.  Warp w scores candidates w, w+8, ... with
+// the lane slicing, fmaf chains and shuffle trees of the other walk kernels, and the
+// warps' bests meet in shared memory in a fixed order: bit-identical scores.
+constexpr int kPredPrefetch = 8;
 
 template <int NCH>
-__global__ void __launch_bounds__(kStreamThreads, 1)
-walk_stream_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __restrict__ ids,
-                   const float* __restrict__ vals, const float* __restrict__ G,
-                   const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K,
-                   int r, int32_t* __restrict__ path, float* __restrict__ path_scores,
-                   int32_t* __restrict__ dev_status) {
-    extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(kStreamThreads, NCH <= 8 ? 2 : 1)
+walk_l2_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __restrict__ ids,
+               const float* __restrict__ vals, const float* __restrict__ G, const uint16_t* __restrict__ A,
+               const uint16_t* __restrict__ Bc, int64_t V, int K, int r, int32_t* __restrict__ path,
+               float* __restrict__ path_scores, int32_t* __restrict__ dev_status) {
+    __shared__ float wv[kStreamWarps];
+    __shared__ int wi[kStreamWarps], wj[kStreamWarps];
     __shared__ int bad;
     const int T = B - 1;
     const int q = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const size_t stage_bytes = size_t(K) * r * 2 + size_t(r) * 4;
-    float* wv = reinterpret_cast<float*>(smem + 2 * stage_bytes);  // [warps] best value
-    int* wi = reinterpret_cast<int*>(wv + kStreamWarps);           // [warps] best id
-    int* wj = wi + kStreamWarps;                                   // [warps] best column
     const int64_t row1 = int64_t(q) * B + 1;
     const int32_t a0 = __ldg(anchors + q);
     if (tid == 0) bad = (a0 < 0 || a0 >= V) ? 1 : 0;
@@ -203,30 +125,30 @@ walk_stream_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __
         if (tid == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
         return;
     }
-    const int cpr = r / 8;
-    // stage t (1-based) into buffer t & 1: position t's B rows [K][r] and G row [r]
-    auto issue = [&](int t) {
-        uint16_t* Bs = reinterpret_cast<uint16_t*>(smem + (t & 1) * stage_bytes);
-        float* Gs = reinterpret_cast<float*>(Bs + size_t(K) * r);
+    const int lines = (r * 2 + 127) / 128;   // 128-byte lines of a codebook row
+    const int glines = (r * 4 + 127) / 128;  // of a G row
+    // position t's candidates' B rows and G row, and its likeliest candidates' A rows
+    // (the predecessors at step t+1), into L2
+    auto prefetch = [&](int t) {
         const int64_t row = row1 + t - 1;
-        for (int j = warp; j < K; j += kStreamWarps) {
-            const uint16_t* src = Bc + int64_t(__ldg(ids + row * K + j)) * r;
-            for (int c = lane; c < cpr; c += 32) cp_async16(Bs + size_t(j) * r + c * 8, src + c * 8);
-        }
-        for (int c = tid; c < r / 4; c += kStreamThreads) cp_async16(Gs + c * 4, G + row * r + c * 4);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        if (t < T) {  // position t's candidates are the predecessors at step t+1
-            const int lines = (r * 2 + 127) / 128;
-            for (int e = tid; e < K * lines; e += kStreamThreads)
+        for (int e = tid; e < K * lines; e += kStreamThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(Bc + int64_t(__ldg(ids + row * K + e / lines)) * r +
+                                                          (e % lines) * 64));
+        for (int e = tid; e < glines; e += kStreamThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(G + row * r + e * 32));
+        if (t < T) {
+            const int np = K < kPredPrefetch ? K : kPredPrefetch;
+            for (int e = tid; e < np * lines; e += kStreamThreads)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(A + int64_t(__ldg(ids + row * K + e / lines)) * r +
                                                               (e % lines) * 64));
         }
     };
-    issue(1);
+    prefetch(1);
     int32_t a = a0;
     for (int t = 1; t <= T; ++t) {
-        if (t < T) issue(t + 1);
-        // the gate A[a] (.) G_t: this warp's lane slices (A from L2, G once staged)
+        if (t < T) prefetch(t + 1);
+        const int64_t row = row1 + t - 1;
+        // the gate A[a] (.) G_t on this warp's lane slices
         float af[NCH][8];
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
@@ -236,20 +158,14 @@ walk_stream_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __
 #pragma unroll
                 for (int e = 0; e < 8; ++e) af[c][e] = 0.f;
         }
-        if (t < T) asm volatile("cp.async.wait_group 1;" ::: "memory");
-        else asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();
-        const uint16_t* Bs = reinterpret_cast<const uint16_t*>(smem + (t & 1) * stage_bytes);
-        const float* Gs = reinterpret_cast<const float*>(Bs + size_t(K) * r);
         float qv[NCH][8];
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             float gc[1][8];
-            load_gslice<1>(Gs + c * 256, r - c * 256, lane, gc);
+            load_gslice<1>(G + row * r + c * 256, r - c * 256, lane, gc);
 #pragma unroll
             for (int e = 0; e < 8; ++e) qv[c][e] = af[c][e] * gc[0][e];
         }
-        const int64_t row = row1 + t - 1;
         float bv = -INFINITY;
         int bid = INT_MAX, bj = -1;
         for (int j0 = warp; j0 < K; j0 += 4 * kStreamWarps) {
@@ -259,10 +175,11 @@ walk_stream_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __
                 const int j = j0 + u * kStreamWarps;
                 part[u] = 0.f;
                 if (j < K) {
+                    const uint16_t* brow = Bc + int64_t(__ldg(ids + row * K + j)) * r;
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
                         float bf[1][8];
-                        load_bslice<1>(Bs + size_t(j) * r + c * 256, r - c * 256, lane, true, bf);
+                        load_bslice<1>(brow + c * 256, r - c * 256, lane, true, bf);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) part[u] = fmaf(qv[c][e], bf[0][e], part[u]);
                     }
@@ -306,7 +223,7 @@ walk_stream_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __
             path_scores[int64_t(q) * T + (t - 1)] = best;
         }
         a = best_id;
-        __syncthreads();  // buffer t & 1 and the warps' bests are free again
+        __syncthreads();  // the warps' bests are free again
     }
 }
 
@@ -337,37 +254,15 @@ cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids
         note_launch();
         return cudaGetLastError();
     }
-    const size_t ssmem = walk_stream_smem(K, r);
-    if (ssmem <= 200 * 1024) {
-#define DF2_WALK_STREAM(N)                                                                          \
-    do {                                                                                            \
-        cudaError_t e = cudaFuncSetAttribute(walk_stream_kernel<N>,                                 \
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(ssmem)); \
-        if (e != cudaSuccess) return e;                                                             \
-        walk_stream_kernel<N><<<unsigned(R), kStreamThreads, ssmem, stream>>>(anchors, B, ids, vals, G, \
-                                                                              A, Bc, V, K, r, path,   \
-                                                                              scores, dev_status);    \
-    } while (0)
-        if (nch <= 1) DF2_WALK_STREAM(1);
-        else if (nch <= 2) DF2_WALK_STREAM(2);
-        else if (nch <= 4) DF2_WALK_STREAM(4);
-        else if (nch <= 8) DF2_WALK_STREAM(8);
-        else DF2_WALK_STREAM(16);
-#undef DF2_WALK_STREAM
-        note_launch();
-        return cudaGetLastError();
-    }
-    const unsigned grid = unsigned((R + kWarpsPerBlock - 1) / kWarpsPerBlock);
-#define DF2_WALK(N)                                                                            \
-    walk_kernel<N><<<grid, kWarpsPerBlock * 32, 0, stream>>>(anchors, R, B, ids, vals, G, A,  \
-                                                             Bc, V, K, r, path, scores,       \
-                                                             dev_status)
-    if (nch <= 1) DF2_WALK(1);
-    else if (nch <= 2) DF2_WALK(2);
-    else if (nch <= 4) DF2_WALK(4);
-    else if (nch <= 8) DF2_WALK(8);
-    else DF2_WALK(16);
-#undef DF2_WALK
+#define DF2_WALK_L2(N)                                                                                \
+    walk_l2_kernel<N><<<unsigned(R), kStreamThreads, 0, stream>>>(anchors, B, ids, vals, G, A, Bc, V, K, r, \
+                                                                  path, scores, dev_status)
+    if (nch <= 1) DF2_WALK_L2(1);
+    else if (nch <= 2) DF2_WALK_L2(2);
+    else if (nch <= 4) DF2_WALK_L2(4);
+    else if (nch <= 8) DF2_WALK_L2(8);
+    else DF2_WALK_L2(16);
+#undef DF2_WALK_L2
     note_launch();
     return cudaGetLastError();
 }
