@@ -369,6 +369,20 @@ class Step:
                      out=(self.ids, self.vals, self.Gt, self.path, self.pscore, self.scores))
         self._rec(ev[3])
 
+    IO_IN = ("h", "x", "z", "anchors", "pred")
+    IO_OUT = ("ids", "vals", "Gt", "path", "pscore", "scores", "y", "y2", "dyn")
+
+    def buffers(self):
+        """The step's per-step inputs and outputs (weights and workspaces are shared)."""
+        return {k: getattr(self, k) for k in self.IO_IN + self.IO_OUT}
+
+    def new_buffers(self):
+        return {k: self.torch.empty_like(v) for k, v in self.buffers().items()}
+
+    def use(self, bufs):
+        for k, v in bufs.items():
+            setattr(self, k, v)
+
     def capture(self):
         """The step as two CUDA graphs -- the conv calls, then the draft head call --
         so that replaying them launches the same kernels without the host's per-call
@@ -494,38 +508,74 @@ def gpu_arm(args, w, rank, world, torch):
     per_call_us = time_per_call(step, torch, min(args.steps, 50))
     next_us, next_how = time_next_rows(step, torch, df2)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step copies its
+    # inputs in from pinned host memory and its results out, with two steps in
+    # flight as a server runs them: step i+1's inputs go in and step i-1's results
+    # come out on copy streams while step i's kernels run; events keep each buffer
+    # set from being overwritten while a kernel or a copy still uses it.
+    out_names = [k for k in Step.IO_OUT if k != "Gt"]
     pinned_in = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v))
                  .pin_memory() for k, v in step.host.items()}
-    dev_in = {"h": step.h, "x": step.x, "z": step.z, "anchors": step.anchors, "pred": step.pred}
-    outs = step.outputs()
-    pinned_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    sets = [step.buffers(), step.new_buffers()]
+    pinned_out = [{k: torch.empty(sets[0][k].shape, dtype=sets[0][k].dtype).pin_memory() for k in out_names}
+                  for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pinned_in.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    d2h = sum(sets[0][k].numel() * sets[0][k].element_size() for k in out_names)
+    main = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k, v in pinned_in.items():
-            dst = dev_in[k]
-            dst.view(torch.uint8).reshape(-1).copy_(v.view(torch.uint8).reshape(-1), non_blocking=True)
+    def copy_in(i):
+        s = i % 2
+        s_in.wait_event(ev_done[s])  # step i-2's kernels have finished with set s
+        with torch.cuda.stream(s_in):
+            for k, v in pinned_in.items():
+                sets[s][k].view(torch.uint8).reshape(-1).copy_(v.view(torch.uint8).reshape(-1), non_blocking=True)
+        ev_in[s].record(s_in)
+
+    def compute(i):
+        s = i % 2
+        main.wait_event(ev_in[s])
+        main.wait_event(ev_out[s])  # step i-2's results in set s have been read out
+        step.use(sets[s])
         step.run()
-        for o, po in zip(outs, pinned_out):
-            po.copy_(o, non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+        ev_done[s].record(main)
         if step.flush is not None:
             step.flush.zero_()
+
+    def copy_out(i):
+        s = i % 2
+        s_out.wait_event(ev_done[s])
+        with torch.cuda.stream(s_out):
+            for k in out_names:
+                pinned_out[s][k].copy_(sets[s][k], non_blocking=True)
+        ev_out[s].record(s_out)
+
+    def e2e_steps(n):
+        for s in range(2):
+            ev_done[s].record(main)
+            ev_out[s].record(main)
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            compute(i)
+            copy_out(i)
+        for s in range(2):
+            main.wait_event(ev_out[s])
+
+    e2e_steps(max(1, args.warmup))
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
-        e2e_step()
-        if step.flush is not None:
-            step.flush.zero_()
+    e2e_steps(args.steps)
     e1.record()
     torch.cuda.synchronize()
+    step.use(sets[0])
     e2e_ms = slowest_rank_ms((e0.elapsed_time(e1) - flush_ms) / args.steps, dist, device)
 
     clocks = clk.summary()
@@ -593,7 +643,9 @@ def gpu_arm(args, w, rank, world, torch):
                 "lattice_tflops": lattice_flops(w) / (next_us[0] * 1e-6) / 1e12,
             },
             "e2e": {"value": job_throughput(w.P, world, e2e_ms), "unit": "positions/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "pipelining": "two steps in flight: step i+1's inputs in and step i-1's results out "
+                                  "overlap step i's calls"},
             "gpu_launches": timed_launches,
             "execution": ("each step replays two CUDA graphs captured from the public calls (conv prepare + "
                           "finish; draft head)" if graphs is not None else "eager calls"),
