@@ -214,13 +214,16 @@ def check_walk(orc, df2, anchors, ids, vals, G, A, Bc, B, what="walk"):
     (4, 8, 64, 10000, 512),
     (1, 5, 16, 2000, 1024),
     (37, 8, 16, 5000, 256),
+    (3, 6, 12, 1500, 2000),     # gathers past shared memory, 8 rank chunks, ragged
+    (2, 4, 8, 1000, 4096),      # the largest rank: 16 chunks
 ])
 def test_walk_shapes(orc, df2, R, B, K, V, r):
     rng = _rng(R * 1000 + B * 100 + K + r)
     check_walk(orc, df2, *lattice(rng, R, B, K, V, r), B, f"walk{R}x{B}k{K}r{r}")
 
 
-@pytest.mark.parametrize("P,K,V,r", [(16, 4, 4096, 32), (77, 16, 3000, 256), (9, 64, 900, 520)])
+@pytest.mark.parametrize("P,K,V,r", [(16, 4, 4096, 32), (77, 16, 3000, 256), (9, 64, 900, 520),
+                                     (5, 8, 700, 4096)])
 def test_pair_scores_shapes(orc, df2, P, K, V, r):
     rng = _rng(P + K + r)
     _, ids, vals, G, A, Bc = lattice(rng, P, 1, K, V, r)
