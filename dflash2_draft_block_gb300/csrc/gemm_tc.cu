@@ -124,7 +124,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const WideArgs args) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned, by pointer arithmetic on the shared array so that the
+    // compiler keeps every access derived from it in the shared address space
+    uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     constexpr int kBRows = PAIR ? WN / 2 : WN;  // B rows this CTA stages per tile
     constexpr uint32_t kBBox = kBRows * WK * 2;
     const int nstages = args.nstages, kbox = args.kbox;
