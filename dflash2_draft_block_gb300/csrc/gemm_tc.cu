@@ -100,6 +100,21 @@ __device__ __forceinline__ void heap_replace_root(uint2* hp, int K, int tt, floa
     hp[pos * 128 + tt] = make_uint2(__float_as_uint(v), unsigned(i));
 }
 
+// (v, i) added at position n of a heap of n entries (n < capacity), sifted up: while
+// the heap is filling, a new entry climbs ~1-2 levels on average, where replacing a
+// root above placeholder entries would sift it down through all of them.
+__device__ __forceinline__ void heap_push(uint2* hp, int n, int tt, float v, int i) {
+    int pos = n;
+    while (pos > 0) {
+        const int par = (pos - 1) >> 1;
+        const uint2 pe = hp[par * 128 + tt];
+        if (!ranks_before(__uint_as_float(pe.x), int(pe.y), v, i)) break;  // the parent is the worse
+        hp[pos * 128 + tt] = pe;
+        pos = par;
+    }
+    hp[pos * 128 + tt] = make_uint2(__float_as_uint(v), unsigned(i));
+}
+
 // Order-preserving map of finite floats to unsigned keys (0 = below everything).
 __device__ __forceinline__ unsigned order_key(float v) {
     const unsigned u = __float_as_uint(v);
@@ -311,6 +326,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         const bool row_ok = m < args.M;
         float tv = -INFINITY;                       // heap root: the K-th best so far
         int tid = INT_MAX;
+        int hn = 0;                                 // entries in the heap (K once it is full)
         // Best K-th value any vocabulary range has reached for this position: a
         // logit strictly below it cannot be in the global top-K.
         float gthr = -INFINITY;
@@ -372,10 +388,19 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                             for (int e = 1; e < 16; ++e) cv = (j == e) ? v[e] : cv;
                             const int n = n0 + j;
                             if (ranks_before(cv, n, tv, tid)) {
-                                heap_replace_root(hp, args.K, tt, cv, n);
-                                const uint2 root = hp[tt];
-                                tv = __uint_as_float(root.x);
-                                tid = int(root.y);
+                                if (hn < args.K) {
+                                    heap_push(hp, hn, tt, cv, n);
+                                    if (++hn == args.K) {  // full: its root is the K-th best
+                                        const uint2 root = hp[tt];
+                                        tv = __uint_as_float(root.x);
+                                        tid = int(root.y);
+                                    }
+                                } else {
+                                    heap_replace_root(hp, args.K, tt, cv, n);
+                                    const uint2 root = hp[tt];
+                                    tv = __uint_as_float(root.x);
+                                    tid = int(root.y);
+                                }
                             }
                         }
                     }
@@ -396,9 +421,10 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             }
         }
         if (EPI == EPI_TOPK && row_ok) {
-            // heap -> rank order (repeatedly move the worst to the end), then write
+            // heap -> rank order (repeatedly move the worst to the end), then write; the
+            // slots past the hn entries still hold their (-inf, no id) placeholders
             const int K = args.K;
-            for (int end = K - 1; end > 0; --end) {
+            for (int end = hn - 1; end > 0; --end) {
                 const uint2 root = hp[tt], last = hp[end * 128 + tt];
                 hp[end * 128 + tt] = root;
                 heap_replace_root(hp, end, tt, __uint_as_float(last.x), int(last.y));
