@@ -131,12 +131,9 @@ DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const ui
             if (rc != DF2_OK) return rc;
         } else {
             cudaError_t e = df2::wide_topk_launch(h, P, W_lm, V, D, K, topk_ids, topk_vals, workspace,
-                                                  dev_status, sms, st, &parts);
+                                                  dev_status, sms, st, &parts, nullptr, 0,
+                                                  has_wh ? W_H : nullptr, r, G);
             if (e != cudaSuccess) return DF2_ERR_CUDA;
-            if (has_wh) {
-                e = df2::wide_store_launch(h, P, W_H, r, D, G, r, r, G, r, dev_status, st);
-                if (e != cudaSuccess) return DF2_ERR_CUDA;
-            }
         }
         return from_cuda(df2::topk_merge_sorted_launch(parts.v, parts.id, parts.S, P, K, topk_ids, topk_vals,
                                                        st, lm));
@@ -228,9 +225,7 @@ DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const
         if (rc != DF2_OK) return rc;
     } else {
         cudaError_t e = df2::wide_topk_launch(h, P, W_lm, V, D, K, topk_ids, topk_vals, workspace,
-                                              dev_status, sms, st, &parts);
-        if (e != cudaSuccess) return DF2_ERR_CUDA;
-        e = df2::wide_store_launch(h, P, W_H, r, D, G, r, r, G, r, dev_status, st);
+                                              dev_status, sms, st, &parts, nullptr, 0, W_H, r, G);
         if (e != cudaSuccess) return DF2_ERR_CUDA;
     }
     return from_cuda(df2::draft_tail_launch(parts, P, K, topk_ids, topk_vals, anchors, B, G, A, Bc, V,

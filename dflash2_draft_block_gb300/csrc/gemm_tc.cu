@@ -59,6 +59,12 @@ struct WideArgs {
     float* part_v;          // [n_groups][M][K]
     int* part_id;
     unsigned* thr_g;        // [M] best K-th value so far over all ranges (ordered key), or null
+    // TOPK: G = A . W_H^T rides along as n_gt extra store tiles (B from the third
+    // tensor map), G tile j on vocabulary range g_grp0 + j of every M tile (ranges
+    // with fewer N tiles than the rest, so the longest unit stays as long)
+    int n_gt, g_grp0;
+    float* g_out;           // [M][g_n]
+    int g_n;
     int32_t* dev_status;
     unsigned* zero_words;   // [n_zero] zeroed by CTA 0 for the next kernel in the stream
     int n_zero;
@@ -134,10 +140,10 @@ namespace {
 // [WN/2 r, WN/2 (r + 1)) of the tile's WN; CTA 0's MMA thread computes the whole
 // tile, and each CTA's TMEM receives its own 128 rows x WN columns.  Each CTA thus
 // stages half the B bytes per flop of the one-CTA tile.
-template <int EPI, int WN, bool PAIR>
+template <int EPI, int WN, bool PAIR, bool GT>
 __global__ void __launch_bounds__(kWideThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                 const WideArgs args) {
+                 const __grid_constant__ CUtensorMap tm_g, const WideArgs args) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned, by pointer arithmetic on the shared array so that the
     // compiler keeps every access derived from it in the shared address space
@@ -178,9 +184,17 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     // unit's store epilogue overlaps its next tile's MMAs, and at every step the units
     // work on consecutive tiles, which share their A rows in L2.
     const int total = n_mu * args.n_nt;
+    const int n_rng = nt1 - nt0;
+    // this unit also computes G tile grp - g_grp0
+    // (GT: launches with G tiles; the others compile without them)
+    const bool has_g = GT && EPI == EPI_TOPK && grp >= args.g_grp0 && grp < args.g_grp0 + args.n_gt;
     const int ntiles = args.linear ? (unit < total ? (total - unit + args.n_units - 1) / args.n_units : 0)
-                                   : nt1 - nt0;
-    auto tile_nt = [&](int k) { return args.linear ? (unit + k * args.n_units) % args.n_nt : nt0 + k; };
+                                   : n_rng + (has_g ? 1 : 0);
+    auto tile_is_g = [&](int k) { return has_g && k == n_rng; };
+    auto tile_nt = [&](int k) {
+        if (tile_is_g(k)) return grp - args.g_grp0;
+        return args.linear ? (unit + k * args.n_units) % args.n_nt : nt0 + k;
+    };
     auto tile_mt = [&](int k) {
         if (!args.linear) return mt;
         const int mu_k = (unit + k * args.n_units) / args.n_nt;
@@ -218,6 +232,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tm_a);
         tc::prefetch_tmap(&tm_b);
+        if (GT) tc::prefetch_tmap(&tm_g);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -237,6 +252,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             bool ok = true;
             for (int k = 0; k < ntiles && ok; ++k) {
                 const int nt = tile_nt(k), mtk = tile_mt(k);
+                const bool gt = tile_is_g(k);
                 for (int kb = 0; kb < nk; ++kb) {
                     const int nb = min(kbox, nbox - kb * kbox);
                     if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
@@ -252,10 +268,12 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                         if (PAIR) {
                             const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
                             tc::tma_load_2d_pair(da, &tm_a, fb, x, mtk * WM, pol_a);
-                            tc::tma_load_2d_pair(db, &tm_b, fb, x, yb, pol_b);
+                            if (gt) tc::tma_load_2d_pair(db, &tm_g, fb, x, yb, pol_b);
+                            else tc::tma_load_2d_pair(db, &tm_b, fb, x, yb, pol_b);
                         } else {
                             tc::tma_load_2d(da, &tm_a, &full[stage], x, mtk * WM, pol_a);
-                            tc::tma_load_2d(db, &tm_b, &full[stage], x, yb, pol_b);
+                            if (gt) tc::tma_load_2d(db, &tm_g, &full[stage], x, yb, pol_b);
+                            else tc::tma_load_2d(db, &tm_b, &full[stage], x, yb, pol_b);
                         }
                     }
                     armed[stage] = int8_t(phase);
@@ -333,26 +351,34 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         int it = 0;
         for (int k = 0; k < ntiles; ++k, ++it) {
             const int nt = tile_nt(k);
-            // the store epilogue's row for this tile (the top-K epilogue's is fixed)
-            const int ms = tile_mt(k) * WM + quarter * 32 + lane;
-            const bool ms_ok = ms < args.M;
+            const bool gt = tile_is_g(k);
             const int b = it & 1;
             const uint32_t tph = (it >> 1) & 1;
             const bool got = tc::mbar_wait(&tfull[b], tph, abort_flag);
             if (!__all_sync(kFull, got)) break;
             tc::fence_after_sync();
             const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(b * WN);
-            for (int c0 = 0; c0 < WN; c0 += 16) {
-                float v[16];
-                tc::tmem_ld16(taddr + uint32_t(c0), v);
-                const int n0 = nt * WN + c0;
-                if (EPI == EPI_STORE) {
-                    if (ms_ok) {
-                        const bool whole = n0 + 16 <= args.N;
-                        const bool side0 = n0 + 16 <= args.n_split, side1 = n0 >= args.n_split;
+            if (EPI == EPI_STORE || gt) {
+                // the store epilogue's row for this tile (the top-K epilogue's is fixed)
+                const int ms = tile_mt(k) * WM + quarter * 32 + lane;
+                const bool ms_ok = ms < args.M;
+                // where a store tile goes: the store launch's outputs, or (top-K) G
+                float* so0 = EPI == EPI_STORE ? args.out0 : args.g_out;
+                float* so1 = EPI == EPI_STORE ? args.out1 : nullptr;
+                const int64_t sl0 = EPI == EPI_STORE ? args.ld0 : args.g_n;
+                const int64_t sl1 = EPI == EPI_STORE ? args.ld1 : 0;
+                const int sns = EPI == EPI_STORE ? args.n_split : args.g_n;
+                const int sN = EPI == EPI_STORE ? args.N : args.g_n;
+                for (int c0 = 0; c0 < WN; c0 += 16) {
+                    float v[16];
+                    tc::tmem_ld16(taddr + uint32_t(c0), v);
+                    const int n0 = nt * WN + c0;
+                    if (ms_ok && n0 < sN) {
+                        const bool whole = n0 + 16 <= sN;
+                        const bool side0 = n0 + 16 <= sns, side1 = n0 >= sns;
                         float* dst = nullptr;
-                        if (side0) dst = args.out0 + int64_t(ms) * args.ld0 + n0;
-                        else if (side1) dst = args.out1 + int64_t(ms) * args.ld1 + (n0 - args.n_split);
+                        if (side0) dst = so0 + int64_t(ms) * sl0 + n0;
+                        else if (side1) dst = so1 + int64_t(ms) * sl1 + (n0 - sns);
                         if (whole && dst && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
@@ -362,13 +388,18 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int n = n0 + e;
-                                if (n >= args.N) break;
-                                if (n < args.n_split) args.out0[int64_t(ms) * args.ld0 + n] = v[e];
-                                else args.out1[int64_t(ms) * args.ld1 + (n - args.n_split)] = v[e];
+                                if (n >= sN) break;
+                                if (n < sns) so0[int64_t(ms) * sl0 + n] = v[e];
+                                else so1[int64_t(ms) * sl1 + (n - sns)] = v[e];
                             }
                         }
                     }
-                } else {
+                }
+            } else {
+                for (int c0 = 0; c0 < WN; c0 += 16) {
+                    float v[16];
+                    tc::tmem_ld16(taddr + uint32_t(c0), v);
+                    const int n0 = nt * WN + c0;
                     // the chunk's candidates that beat the current K-th, as a bit mask;
                     // the warp then inserts them in rounds, one per lane per round, so
                     // the cost is the largest per-lane count, not one round per column
@@ -413,7 +444,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                 if (PAIR) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&tempty[b]), 0));
                 else tc::mbar_arrive(&tempty[b]);
             }
-            if (EPI == EPI_TOPK && args.thr_g && row_ok) {
+            if (EPI == EPI_TOPK && !gt && args.thr_g && row_ok) {
                 unsigned k = 0;
                 if (tid != INT_MAX) k = order_key(tv);  // heap full: publish its K-th value
                 const unsigned old = atomicMax(args.thr_g + m, k);
@@ -555,12 +586,12 @@ WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persi
     return p;
 }
 
-template <int EPI, int BN, bool PAIR>
-cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const WideArgs& a, int grid,
-                        cudaStream_t stream) {
+template <int EPI, int BN, bool PAIR, bool GT>
+cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg, const WideArgs& a,
+                        int grid, cudaStream_t stream) {
     const int brows = PAIR ? BN / 2 : BN;
     const size_t smem = wide_smem(a.nstages, a.kbox, EPI, a.K, brows) + 1024;
-    auto kernel = gemm_wide_kernel<EPI, BN, PAIR>;
+    auto kernel = gemm_wide_kernel<EPI, BN, PAIR, GT>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -575,17 +606,22 @@ cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const Wide
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = PAIR ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, a);
+    e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tg, a);
     note_launch();
     return e;
 }
 
 template <int EPI>
-cudaError_t launch_plan(const WidePlan& p, const CUtensorMap& ta, const CUtensorMap& tb, const WideArgs& a,
-                        cudaStream_t stream) {
+cudaError_t launch_plan(const WidePlan& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg,
+                        const WideArgs& a, cudaStream_t stream) {
     const int grid = (p.pair ? 2 : 1) * p.units;
-    return p.pair ? launch_wide<EPI, 256, true>(ta, tb, a, grid, stream)
-                  : launch_wide<EPI, 256, false>(ta, tb, a, grid, stream);
+    if constexpr (EPI == EPI_TOPK) {
+        if (a.n_gt > 0)
+            return p.pair ? launch_wide<EPI, 256, true, true>(ta, tb, tg, a, grid, stream)
+                          : launch_wide<EPI, 256, false, true>(ta, tb, tg, a, grid, stream);
+    }
+    return p.pair ? launch_wide<EPI, 256, true, false>(ta, tb, tg, a, grid, stream)
+                  : launch_wide<EPI, 256, false, false>(ta, tb, tg, a, grid, stream);
 }
 
 }  // namespace
@@ -624,17 +660,26 @@ cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, i
     a.out0 = out0; a.ld0 = ld0; a.n_split = int(n_split); a.out1 = out1; a.ld1 = ld1;
     a.K = 0;
     a.dev_status = dev_status;
-    return launch_plan<EPI_STORE>(p, ta, tb, a, stream);
+    return launch_plan<EPI_STORE>(p, ta, tb, tb, a, stream);
 }
 
 cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
                              int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
-                             cudaStream_t stream, TopkParts* parts_out, unsigned* zero_words, int n_zero) {
+                             cudaStream_t stream, TopkParts* parts_out, unsigned* zero_words, int n_zero,
+                             const uint16_t* W_H, int64_t r, float* G) {
     const WidePlan p = wide_plan(EPI_TOPK, M, N, K, num_sms, true);
     const int bn = wide_bn(EPI_TOPK, K);
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tg;
     if (!wide_map(&ta, A, M, Kd, WM) || !wide_map(&tb, B, N, Kd, p.pair ? bn / 2 : bn))
         return cudaErrorInvalidValue;
+    // G = A . W_H^T: inside this launch when it fits on the short last vocabulary
+    // range (one 256-column tile, and that range has fewer tiles than the others),
+    // else as a store launch of its own after it
+    const bool want_g = W_H && G && r > 0;
+    const int last_rng = p.n_nt - (p.n_groups - 1) * p.tiles_per_cta;
+    const bool fold_g = want_g && r <= 256 && last_rng < p.tiles_per_cta;
+    tg = tb;
+    if (fold_g && !wide_map(&tg, W_H, r, Kd, p.pair ? bn / 2 : bn)) return cudaErrorInvalidValue;
     WideArgs a{};
     a.M = int(M); a.N = int(N); a.Kd = int(Kd);
     a.n_mt = p.n_mt;
@@ -651,10 +696,20 @@ cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, in
     a.dev_status = dev_status;
     a.zero_words = zero_words;
     a.n_zero = n_zero;
+    if (fold_g) {
+        a.n_gt = 1;
+        a.g_grp0 = n_groups - 1;
+        a.g_out = G;
+        a.g_n = int(r);
+    }
     cudaError_t e = cudaMemsetAsync(a.thr_g, 0, size_t(M) * 4, stream);
     if (e != cudaSuccess) return e;
-    e = launch_plan<EPI_TOPK>(p, ta, tb, a, stream);
+    e = launch_plan<EPI_TOPK>(p, ta, tb, tg, a, stream);
     if (e != cudaSuccess) return e;
+    if (want_g && !fold_g) {
+        e = wide_store_launch(A, M, W_H, r, Kd, G, r, r, G, r, dev_status, stream);
+        if (e != cudaSuccess) return e;
+    }
     if (parts_out) {  // the caller folds the per-range lists itself
         *parts_out = TopkParts{a.part_v, a.part_id, n_groups};
         return cudaSuccess;

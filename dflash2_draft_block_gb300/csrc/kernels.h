@@ -62,11 +62,13 @@ cudaError_t wide_store_launch(const uint16_t* A, int64_t M, const uint16_t* B, i
                               int32_t* dev_status, cudaStream_t stream);
 // per-row top-K of A B^T (ids = B row indices), merged into ids/vals [M][K]; with
 // parts_out the sorted per-range lists are left for the caller to fold instead,
-// and zero_words[0 .. n_zero) are zeroed for the next kernel in the stream
+// and zero_words[0 .. n_zero) are zeroed for the next kernel in the stream.  With
+// W_H, also G = A W_H^T [M][r] (fp32), in the same launch where it fits
 cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, int64_t N, int64_t Kd, int K,
                              int32_t* ids, float* vals, void* ws, int32_t* dev_status, int num_sms,
                              cudaStream_t stream, TopkParts* parts_out = nullptr,
-                             unsigned* zero_words = nullptr, int n_zero = 0);
+                             unsigned* zero_words = nullptr, int n_zero = 0,
+                             const uint16_t* W_H = nullptr, int64_t r = 0, float* G = nullptr);
 
 // ---- selector
 cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,

@@ -105,6 +105,22 @@ def test_head_many_positions(orc, df2, P, D, V, K):
     check_head(orc, df2, h, Wlm, K, WH, f"wide{P}x{D}x{V}k{K}")
 
 
+@pytest.mark.parametrize("P,D,V,K,r", [
+    # on a 152-SM part the last vocabulary range holds one tile where the others
+    # hold two, so G = H(h) is computed there, inside the top-K launch
+    (200, 256, 19600, 16, 40),    # CTA pairs, ragged M tile, r not a multiple of 16
+    (256, 192, 19600, 8, 256),    # CTA pairs, G exactly one tile wide
+    (48, 128, 39000, 16, 24),     # one CTA per M tile
+    (200, 256, 19600, 16, 264),   # G wider than one tile: a store launch of its own
+])
+def test_head_many_positions_with_H(orc, df2, P, D, V, K, r):
+    rng = _rng(P * 17 + V + r)
+    h = rand_bf16(rng, (P, D))
+    Wlm = rand_bf16(rng, (V, D), 0.02)
+    WH = rand_bf16(rng, (r, D), 0.02)
+    check_head(orc, df2, h, Wlm, K, WH, f"wideH{P}x{D}x{V}k{K}r{r}")
+
+
 def test_head_many_positions_exact_ties(orc, df2):
     rng = _rng(77)
     P, D, V, K = 140, 128, 3000, 16
