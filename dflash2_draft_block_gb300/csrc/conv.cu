@@ -385,13 +385,16 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
 // Few rows (P <= 64): the projection and the apply in one kernel.  CTA (gx, gy)
 // owns channel groups [gx*gpc, gx*gpc + gpc) and rows [gy*PR, gy*PR + PR), PR a
 // multiple of the block size so that no tap reaches outside the CTA's rows.  It
-// stages its rows of x in shared memory, computes its groups' projection columns
-// -- (io*taps + j)*G + gi for both sides io -- one warp per column with the
-// arithmetic of gemm_rows_kernel (lane slices of 8 W elements, fmaf over the
-// rows, a shuffle tree), writes the output-side columns to dyn_out, keeps the
-// input-side ones in shared memory and applies the conv to its groups' channels
-// with the arithmetic of conv_apply_rows_kernel.  One launch instead of two, and
-// the input-side corrections never leave the chip.
+// stages its rows of x in shared memory and computes its groups' projection columns
+// -- (io*taps + j)*G + gi for both sides io -- NC at a time: the CTA's 256 lanes
+// split the C inputs into 8-element chunks, so each staged x element and each W
+// element is read and widened once per column group, and every lane keeps NC x PG
+// partial sums (64).  A reduce-scatter over the warp (recursive halving: 62
+// shuffles leave each lane two of the 64 warp sums) and a sum over the 8 warps in
+// shared memory finish the dot products.  The output-side columns go to dyn_out,
+// the input-side ones stay in shared memory for the apply, which uses the
+// arithmetic of conv_apply_rows_kernel.  One launch instead of two, and the
+// input-side corrections never leave the chip.
 __device__ __forceinline__ void cp_async16_p(void* smem_dst, const void* gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
                      static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
@@ -413,23 +416,46 @@ __device__ __forceinline__ void store1(uint16_t* p, float v) { *p = f32_to_bf16_
 __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 
 constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
+constexpr int kPrepSums = 64;  // partial sums per lane: columns x rows of one column group
+
+// Sum v[0..64) over the warp; lane l returns the sums of entries 2l and 2l + 1.
+// Each step halves the entries a lane holds: the lane keeps the half its bit of
+// the step selects and adds the partner's copy of that half.
+__device__ __forceinline__ float2 warp_reduce_scatter64(float (&v)[kPrepSums], int lane) {
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int half = kPrepSums >> (step + 1);  // 32, 16, 8, 4, 2
+        const int bit = 16 >> step;
+        const bool upper = (lane & bit) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+    }
+    return make_float2(v[0], v[1]);
+}
 
 template <int PG, typename T>
 __global__ void __launch_bounds__(kPrepThreads, 1)
 conv_prepare_rows_kernel(const T* __restrict__ x, int64_t P, int C, int B, int taps, int g, int G, int gpc,
                          int PR, const uint16_t* __restrict__ W, const float* __restrict__ base,
                          T* __restrict__ y, float* __restrict__ dyn_out) {
+    constexpr int NC = kPrepSums / PG;  // columns per group
     extern __shared__ __align__(16) uint8_t smem[];
     T* xs = reinterpret_cast<T*>(smem);                                          // [PR][C]
     float* ds = reinterpret_cast<float*>(smem + size_t(PR) * C * sizeof(T));     // [PR][taps][gpc]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = kPrepThreads / 32;
+    float* red = ds + size_t(PR) * taps * gpc;                                   // [warps][64]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g0 = int(blockIdx.x) * gpc;
     const int ng = gpc < G - g0 ? gpc : G - g0;
     const int64_t m0 = int64_t(blockIdx.y) * PR;
     const int nm = int(P - m0 < PR ? P - m0 : PR);
     constexpr int kPer16 = 16 / int(sizeof(T));
     const int cpr = C / kPer16;
-    for (int r = warp; r < nm; r += nwarps)
+    for (int r = warp; r < nm; r += kPrepWarps)
         for (int c = lane; c < cpr; c += 32)
             cp_async16_p(xs + size_t(r) * C + c * kPer16, x + (m0 + r) * C + c * kPer16);
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -440,61 +466,62 @@ conv_prepare_rows_kernel(const T* __restrict__ x, int64_t P, int C, int B, int t
         const int io = lc / (taps * ng), rem = lc % (taps * ng), j = rem / ng, gl = rem % ng;
         return int64_t(io * taps + j) * G + g0 + gl;
     };
-    // the first kPre chunks of each lane's slice of the warp's first W row are loaded
-    // while x is still being staged
-    constexpr int kPre = 16;
-    uint4 wpre[kPre];
-    if (warp < ncols) {
-        const uint4* wrow = reinterpret_cast<const uint4*>(W + column(warp) * C);
+    // this lane's chunks: c = c_first, c_first + 256, ...
+    const int c_first = warp * 32 + lane;
+    auto load_w = [&](uint4 (&w)[NC], int cg, int c) {
 #pragma unroll
-        for (int k = 0; k < kPre; ++k) {
-            const int c = lane + 32 * k;
-            wpre[k] = c < k8 ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+        for (int q = 0; q < NC; ++q) {
+            const int lc = cg * NC + q;
+            w[q] = (c < k8 && lc < ncols) ? __ldg(reinterpret_cast<const uint4*>(W + column(lc) * C) + c)
+                                          : make_uint4(0, 0, 0, 0);
         }
-    }
+    };
+    uint4 wn[NC];
+    load_w(wn, 0, c_first);  // the first chunk's W loads overlap the staging of x
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
 
-    for (int lc = warp; lc < ncols; lc += nwarps) {
-        const int io = lc / (taps * ng), rem = lc % (taps * ng), j = rem / ng, gl = rem % ng;
-        const int64_t n = column(lc);
-        float acc[PG];
+    for (int cg = 0; cg * NC < ncols; ++cg) {
+        float acc[kPrepSums];  // [q][p]
 #pragma unroll
-        for (int p = 0; p < PG; ++p) acc[p] = 0.f;
-        const uint4* wrow = reinterpret_cast<const uint4*>(W + n * C);
-        auto fold = [&](const uint4& wv, int c) {
-            float wf[8];
-            unpack8(wv, wf);
+        for (int i = 0; i < kPrepSums; ++i) acc[i] = 0.f;
+        for (int c = c_first; c < k8; c += kPrepThreads) {
+            float wf[NC][8];
+#pragma unroll
+            for (int q = 0; q < NC; ++q) unpack8(wn[q], wf[q]);
+            // the next chunk's W (this group's, else the next group's first) is in
+            // flight while this chunk is summed
+            if (c + kPrepThreads < k8) load_w(wn, cg, c + kPrepThreads);
+            else if ((cg + 1) * NC < ncols) load_w(wn, cg + 1, c_first);
 #pragma unroll
             for (int p = 0; p < PG; ++p) {
                 if (p < nm) {
                     float xf[8];
                     load8s(xs + size_t(p) * C + c * 8, xf);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[p] = fmaf(wf[e], xf[e], acc[p]);
+                    for (int q = 0; q < NC; ++q)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[q * PG + p] = fmaf(wf[q][e], xf[e], acc[q * PG + p]);
                 }
             }
-        };
-        const bool first = lc == warp;
+        }
+        const float2 s2 = warp_reduce_scatter64(acc, lane);
+        red[warp * kPrepSums + 2 * lane] = s2.x;
+        red[warp * kPrepSums + 2 * lane + 1] = s2.y;
+        __syncthreads();
+        if (threadIdx.x < kPrepSums) {
+            const int i = threadIdx.x, q = i / PG, p = i % PG, lc = cg * NC + q;
+            float sum = 0.f;
 #pragma unroll
-        for (int k = 0; k < kPre; ++k) {
-            const int c = lane + 32 * k;
-            if (c < k8) fold(first ? wpre[k] : __ldg(wrow + c), c);
+            for (int w = 0; w < kPrepWarps; ++w) sum += red[w * kPrepSums + i];
+            if (lc < ncols && p < nm) {
+                const int io = lc / (taps * ng), rem = lc % (taps * ng), j = rem / ng, gl = rem % ng;
+                if (io == 0) ds[(p * taps + j) * gpc + gl] = sum;
+                else dyn_out[(m0 + p) * (int64_t(taps) * G) + int64_t(j) * G + g0 + gl] = sum;
+            }
         }
-#pragma unroll 8
-        for (int c = lane + 32 * kPre; c < k8; c += 32) fold(__ldg(wrow + c), c);
-        float mine = 0.f;
-#pragma unroll
-        for (int p = 0; p < PG; ++p) {
-            const float sum = warp_sum(acc[p]);
-            if (lane == p) mine = sum;
-        }
-        if (lane < nm) {
-            if (io == 0) ds[(lane * taps + j) * gpc + gl] = mine;
-            else dyn_out[(m0 + lane) * (int64_t(taps) * G) + int64_t(j) * G + g0 + gl] = mine;
-        }
+        __syncthreads();  // red is reused by the next group
     }
-    __syncthreads();
 
     const int c_lo = g0 * g, nch = ng * g;
     for (int e = threadIdx.x; e < nm * nch; e += kPrepThreads) {
@@ -515,7 +542,8 @@ cudaError_t launch_prepare_rows(const T* x, int64_t P, int C, int B, int taps, i
                                 cudaStream_t stream) {
     const int G = C / g;
     const int gpc = 2 * taps >= 8 ? 1 : 8 / (2 * taps);
-    const size_t smem = size_t(PR) * C * sizeof(T) + size_t(PR) * taps * gpc * 4;
+    const size_t smem = size_t(PR) * C * sizeof(T) + size_t(PR) * taps * gpc * 4 +
+                        size_t(kPrepWarps) * kPrepSums * 4;
     cudaError_t e = cudaFuncSetAttribute(conv_prepare_rows_kernel<PG, T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
