@@ -334,7 +334,12 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
         note_launch();
         return cudaGetLastError();
     }
+    // threads per CTA: a multiple of 32 that divides the row's chunks, so that no
+    // strip of a block runs half empty (5120 channels: 640 chunks, 4 strips of 160)
+    const int chunks = C / Vec<T>::N;
     int nt = kAsyncThreads;
+    for (int cand = kAsyncThreads; cand >= 128; cand -= 32)
+        if (chunks % cand == 0) { nt = cand; break; }
     const size_t slot = size_t(B) * ((res ? 32 : 16) + size_t(taps) * 4);  // bytes per thread
     while (nt > 64 && slot * nt > kAsyncSmemMax) nt /= 2;
     const size_t async_smem = slot * nt;
