@@ -13,9 +13,12 @@
 //     bf16 boxes (so every W row contributes 64*kbox contiguous elements per
 //     stage), 128-byte swizzled, evict-first in L2, into a ring of `nstages`
 //     slots, together with the matching [N x 64] boxes of h (rows past P read 0);
-//   * warp 1 (one lane) issues tcgen05.mma M=128 (vocab rows) x N (positions,
-//     16 or 32) x K=16 into TMEM; two tile accumulators alternate so the next
-//     tile's MMAs overlap the epilogue of this one;
+//   * two issuing lanes (warps 1 and 6) issue tcgen05.mma M=128 (vocab rows) x N
+//     (positions, 16 or 32) x K=16 into TMEM, alternating k-steps, each into its
+//     own partial accumulator (one lane issues an MMA only every ~150 cycles,
+//     whatever its shape, so a single issuer could not keep up with the W
+//     stream at N = 16); two tile accumulators alternate so the next tile's MMAs
+//     overlap the epilogue of this one;
 //   * warps 2-5 read the accumulator (warp w owns TMEM lanes 32*(w%4)..+31, i.e.
 //     32 vocab rows) and keep, per position, a top-K list in registers across
 //     their 32 lanes (topk_warp.cuh): a ballot against the list's K-th entry
@@ -40,7 +43,9 @@ namespace {
 constexpr int BM = 128;          // vocab rows per tile (MMA M)
 constexpr int BK = 64;           // K elements per stage (one 128-byte swizzle row)
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kIssuers = 2;                        // MMA-issuing lanes: warps 1 and kIssuerWarp2
+constexpr int kIssuerWarp2 = 2 + kEpiWarps;
+constexpr int kThreads = 64 + 32 * kEpiWarps + 32;
 constexpr uint32_t kWBytes = BM * BK * 2;
 constexpr int kMaxK = 64;
 constexpr int kMaxStages = 16;
@@ -60,7 +65,7 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int R, int nstages, int
     L.w_off = 0;
     L.h_off = L.w_off + uint32_t(nstages) * L.stage_w;
     L.bar_off = L.h_off + uint32_t(nstages) * L.stage_h;               // 1024-aligned
-    L.misc_off = L.bar_off + uint32_t(2 * nstages + 5) * 8;
+    L.misc_off = L.bar_off + uint32_t(2 * nstages + 6) * 8;
     L.xch_off = 0;
     const uint32_t xch_bytes = uint32_t(kEpiWarps * N * R * 32) * 8;
     const uint32_t end = L.misc_off + 16;
@@ -78,8 +83,8 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                    int n_zero) {
     // TMEM: two tile buffers (the epilogue drains one while the MMAs fill the
     // other), each holding nacc partial accumulators of N columns.  Successive
-    // k-steps of a tile rotate over the partial accumulators, so consecutive MMAs
-    // do not depend on each other and the tensor core can overlap them; the
+    // k-steps of a tile rotate over the partial accumulators; partial a belongs to
+    // issuer a % kIssuers, so the issuers never write the same accumulator; the
     // epilogue adds the partials.
     const uint32_t buf_cols = uint32_t(nacc) * N;
     uint32_t tmem_cols = 32;
@@ -93,7 +98,7 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     uint64_t* empty = full + nstages;
     uint64_t* tfull = empty + nstages;
     uint64_t* tempty = tfull + 2;
-    uint64_t* mma_done = tempty + 2;
+    uint64_t* mma_done = tempty + 2;  // [kIssuers]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc_off);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
     float* xch_v = reinterpret_cast<float*>(smem + L.xch_off);                 // [4][N][R*32]
@@ -110,13 +115,13 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&empty[s], kIssuers);  // a commit from each issuer
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tfull[b], kIssuers);
             tc::mbar_init(&tempty[b], kEpiWarps);
         }
-        tc::mbar_init(mma_done, 1);
+        for (int i = 0; i < kIssuers; ++i) tc::mbar_init(&mma_done[i], 1);
         abort_flag[0] = 0;
         tc::fence_mbar_init();
     }
@@ -191,9 +196,10 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                     if (armed[s] >= 0) tc::mbar_wait(&full[s], uint32_t(armed[s]), &never);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kIssuerWarp2) {
         if (lane == 0) {
-            // ------------------------------------------------------ MMA issuer
+            // ----------------------------------------------------- MMA issuers
+            const int who = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, N);
             int stage = 0;
             uint32_t phase = 0;
@@ -216,6 +222,7 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k, ++ks) {
                             const int a = ks % nacc;
+                            if (a % kIssuers != who) continue;
                             tc::mma_bf16(d_tmem + uint32_t(a * N), tc::sw128_kmajor_desc(a0 + 32 * k),
                                          tc::sw128_kmajor_desc(b0 + 32 * k), idesc,
                                          ks >= nacc ? 1u : 0u);
@@ -227,11 +234,11 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 if (ok) tc::mma_commit(&tfull[b]);
             }
             // every MMA this thread issued is complete before TMEM is released
-            tc::mma_commit(mma_done);
+            tc::mma_commit(&mma_done[who]);
             volatile int never = 0;
-            tc::mbar_wait(mma_done, 0, &never);
+            tc::mbar_wait(&mma_done[who], 0, &never);
         }
-    } else {
+    } else if (warp < 2 + kEpiWarps) {
         // ---------------------------------------------------------- epilogue
         const int e = warp - 2;
         const int quarter = warp & 3;
@@ -362,8 +369,9 @@ int pick_n(int64_t P) { return P <= 16 ? 16 : 32; }
 #define DF2_HEAD_PF 0    // stages prefetched into L2 ahead of the TMA loads
 #endif
 #ifndef DF2_HEAD_NACC
-#define DF2_HEAD_NACC 1  // independent partial accumulators per tile
+#define DF2_HEAD_NACC 2  // partial accumulators per tile: a multiple of the issuers
 #endif
+static_assert(DF2_HEAD_NACC % kIssuers == 0, "every issuer owns whole partial accumulators");
 
 struct Plan {
     int N, R, nstages, kbox;
