@@ -7,8 +7,13 @@
 //
 // At this size the head is a stream of the whole LM head from HBM, so the
 // kernel is built around that stream:
-//   * the vocabulary is cut into 128-row tiles (plus ceil(r/128) tiles of W_H);
-//     one persistent CTA per SM walks tiles blockIdx.x, +gridDim.x, ...
+//   * the vocabulary is cut into tiles of at most 128 rows (plus ceil(r/128)
+//     tiles of W_H); one persistent CTA per SM walks tiles blockIdx.x,
+//     +gridDim.x, ...  The first n_hi vocabulary tiles have bm_hi rows and the
+//     rest bm_lo (both multiples of 8), chosen on the host so that every CTA
+//     walks the same number of tiles and the busiest streams as few rows as it
+//     can; a short tile's spare MMA rows hold stale shared memory and are never
+//     read out;
 //   * warp 0 (one lane) streams each tile with TMA in stages of `kbox` [128 x 64]
 //     bf16 boxes (so every W row contributes 64*kbox contiguous elements per
 //     stage), 128-byte swizzled, evict-first in L2, into a ring of `nstages`
@@ -75,9 +80,10 @@ __host__ __device__ inline SmemLayout smem_layout(int N, int R, int nstages, int
 
 template <int N, int R>
 __global__ void __launch_bounds__(kThreads, 1)
-head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
-                   const __grid_constant__ CUtensorMap tm_wh, int P, int D, int V, int K, int r,
-                   int n_vtiles, int n_tiles, int nstages, int kbox, int pf_stages, int nacc,
+head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w2,
+                   const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wh, int P,
+                   int D, int V, int K, int r, int n_vtiles, int n_hi, int bm_hi, int bm_lo, int n_tiles,
+                   int nstages, int kbox, int pf_stages, int nacc,
                    float* __restrict__ part_v, int* __restrict__ part_id, float* __restrict__ G,
                    int32_t* __restrict__ dev_status, int stall_stage, unsigned* __restrict__ zero_words,
                    int n_zero) {
@@ -111,6 +117,13 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0u;
     const int nk = (nbox + kbox - 1) / kbox;       // stages per tile
     const uint32_t h_box_bytes = uint32_t(N) * BK * 2;
+    // tile t: its first row, its row count, and the tensor map whose box it is
+    auto tile_row0 = [&](int t) {
+        if (t >= n_vtiles) return (t - n_vtiles) * BM;
+        return t < n_hi ? t * bm_hi : n_hi * bm_hi + (t - n_hi) * bm_lo;
+    };
+    auto tile_rows = [&](int t) { return t >= n_vtiles ? BM : (t < n_hi ? bm_hi : bm_lo); };
+    auto tile_map = [&](int t) { return t >= n_vtiles ? &tm_wh : (t < n_hi ? &tm_w : &tm_w2); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
@@ -131,6 +144,7 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tm_w);
+        if (n_hi < n_vtiles) tc::prefetch_tmap(&tm_w2);
         tc::prefetch_tmap(&tm_h);
         if (n_tiles > n_vtiles) tc::prefetch_tmap(&tm_wh);
     }
@@ -150,10 +164,8 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             for (int g = 0; g < pf_stages && g < total; ++g) {
                 const int t = int(blockIdx.x) + (g / nk) * int(gridDim.x);
                 const int kb = g % nk;
-                const bool is_wh = t >= n_vtiles;
-                const int row0 = (is_wh ? t - n_vtiles : t) * BM;
                 for (int j = 0; j < kbox && kb * kbox + j < nbox; ++j)
-                    tc::tma_prefetch_2d(is_wh ? &tm_wh : &tm_w, (kb * kbox + j) * BK, row0);
+                    tc::tma_prefetch_2d(tile_map(t), (kb * kbox + j) * BK, tile_row0(t));
             }
             int stage = 0;
             uint32_t phase = 0;
@@ -163,12 +175,12 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             for (int g = 0; g < total && ok; ++g) {
                 const int t = int(blockIdx.x) + (g / nk) * int(gridDim.x);
                 const int kb = g % nk;
-                const bool is_wh = t >= n_vtiles;
-                const CUtensorMap* mw = is_wh ? &tm_wh : &tm_w;
-                const int row0 = (is_wh ? t - n_vtiles : t) * BM;
+                const CUtensorMap* mw = tile_map(t);
+                const int row0 = tile_row0(t);
+                const uint32_t w_box_bytes = uint32_t(tile_rows(t)) * BK * 2;
                 const int nb = min(kbox, nbox - kb * kbox);
                 if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-                tc::mbar_arrive_expect_tx(&full[stage], uint32_t(nb) * (kWBytes + h_box_bytes));
+                tc::mbar_arrive_expect_tx(&full[stage], uint32_t(nb) * (w_box_bytes + h_box_bytes));
                 // self-test only: a stage whose copies are never issued, so the
                 // consumer's bounded wait must give up and report a timeout
                 for (int j = 0; j < nb && g != stall_stage; ++j) {
@@ -183,10 +195,8 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                 if (pf_stages > 0 && gp < total) {
                     const int tp = int(blockIdx.x) + (gp / nk) * int(gridDim.x);
                     const int kbp = gp % nk;
-                    const bool wh_p = tp >= n_vtiles;
-                    const int rowp = (wh_p ? tp - n_vtiles : tp) * BM;
                     for (int j = 0; j < kbox && kbp * kbox + j < nbox; ++j)
-                        tc::tma_prefetch_2d(wh_p ? &tm_wh : &tm_w, (kbp * kbox + j) * BK, rowp);
+                        tc::tma_prefetch_2d(tile_map(tp), (kbp * kbox + j) * BK, tile_row0(tp));
                 }
             }
             if (!ok) {
@@ -269,7 +279,8 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
             if (lane == 0) tc::mbar_arrive(&tempty[b]);
 
             const bool is_wh = t >= n_vtiles;
-            const int row = (is_wh ? t - n_vtiles : t) * BM + quarter * 32 + lane;
+            const int lr = quarter * 32 + lane;  // the tile's row of this lane
+            const int row = tile_row0(t) + lr;
             if (is_wh) {
                 if (row < r) {
 #pragma unroll
@@ -277,7 +288,7 @@ head_skinny_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
                         if (p < P) G[size_t(p) * r + row] = acc[p];
                 }
             } else {
-                const bool valid = row < V;
+                const bool valid = lr < tile_rows(t) && row < V;
 #pragma unroll
                 for (int p = 0; p < N; ++p)
                     if (p < P) lists[p].offer(acc[p], valid ? row : wtk::kEmptyId, K, lane);
@@ -390,6 +401,27 @@ Plan pick_plan(int64_t P, int K) {
     return pl;
 }
 
+// The vocabulary tiles: at 128 rows each CTA would walk `per` tiles (W_H's
+// included), and that stays so with n_vtiles = per * grid - n_wh tiles of the two
+// multiples of 8 around V / n_vtiles.  Round-robin then deals every CTA nearly the
+// same number of long tiles (V 151936, 152 CTAs: 782 of 128 rows, 432 of 120, so
+// the busiest CTA streams 1008 rows instead of 1024).
+struct VTiling {
+    int n_vtiles, n_hi, bm_hi, bm_lo;
+};
+VTiling v_tiling(int64_t V, int n_wh, int grid) {
+    const int64_t t128 = (V + BM - 1) / BM;
+    const VTiling uniform{int(t128), int(t128), BM, BM};
+    const int64_t per = (t128 + n_wh + grid - 1) / grid;
+    const int64_t slots = per * grid - n_wh;
+    if (slots < t128) return uniform;
+    const int64_t lo = V / slots / 8 * 8;
+    if (lo < 8 || lo >= BM) return uniform;
+    const int64_t n_hi = (V - slots * lo + 7) / 8;  // tiles of lo + 8 rows; the rest lo
+    if (n_hi < 0 || n_hi > slots) return uniform;
+    return VTiling{int(slots), int(n_hi), int(lo + 8), int(lo)};
+}
+
 }  // namespace
 
 bool head_tc_supported(int64_t P, int64_t D, int64_t V, int K) {
@@ -411,17 +443,25 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
                    TopkParts* parts_out, unsigned* zero_words, int n_zero) {
     const Plan pl = pick_plan(P, K);
     const int N = pl.N;
-    CUtensorMap tm_w, tm_h, tm_wh;
-    if (!make_map(&tm_w, W, V, D, BM) || !make_map(&tm_h, h, P, D, N)) return DF2_ERR_CUDA;
     const bool has_wh = W_H != nullptr;
+    const int n_v128 = int((V + BM - 1) / BM);
+    const int grid = n_v128 < num_sms ? n_v128 : num_sms;
+    const int n_wh = has_wh ? (r + BM - 1) / BM : 0;
+    const VTiling vt = v_tiling(V, n_wh, grid);
+    CUtensorMap tm_w, tm_w2, tm_h, tm_wh;
+    if (!make_map(&tm_w, W, V, D, vt.bm_hi) || !make_map(&tm_h, h, P, D, N)) return DF2_ERR_CUDA;
+    if (vt.n_hi < vt.n_vtiles) {
+        if (!make_map(&tm_w2, W, V, D, vt.bm_lo)) return DF2_ERR_CUDA;
+    } else {
+        tm_w2 = tm_w;
+    }
     if (has_wh) {
         if (!make_map(&tm_wh, W_H, r, D, BM)) return DF2_ERR_CUDA;
     } else {
         tm_wh = tm_w;
     }
-    const int n_vtiles = int((V + BM - 1) / BM);
-    const int n_tiles = n_vtiles + (has_wh ? (r + BM - 1) / BM : 0);
-    const int grid = n_vtiles < num_sms ? n_vtiles : num_sms;
+    const int n_vtiles = vt.n_vtiles;
+    const int n_tiles = n_vtiles + n_wh;
     const size_t parts = size_t(grid);
     float* part_v = static_cast<float*>(ws);
     int* part_id = reinterpret_cast<int*>(part_v + parts * P * K);
@@ -433,7 +473,8 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));         \
         if (e != cudaSuccess) return DF2_ERR_CUDA;                                                \
         head_skinny_kernel<NV, RV><<<grid, kThreads, smem, stream>>>(                             \
-            tm_w, tm_h, tm_wh, int(P), int(D), int(V), K, r, n_vtiles, n_tiles, pl.nstages,       \
+            tm_w, tm_w2, tm_h, tm_wh, int(P), int(D), int(V), K, r, n_vtiles, vt.n_hi, vt.bm_hi,   \
+            vt.bm_lo, n_tiles, pl.nstages,                                                        \
             pl.kbox, DF2_HEAD_PF, DF2_HEAD_NACC, part_v, part_id, G, dev_status, stall_stage,     \
             zero_words, n_zero);                                                                  \
     } while (0)
