@@ -20,9 +20,10 @@
 //     slots, together with the matching [N x 64] boxes of h (rows past P read 0);
 //   * two issuing lanes (warps 1 and 6) issue tcgen05.mma M=128 (vocab rows) x N
 //     (positions, 16 or 32) x K=16 into TMEM, alternating k-steps, each into its
-//     own partial accumulator (one lane issues an MMA only every ~150 cycles,
-//     whatever its shape, so a single issuer could not keep up with the W
-//     stream at N = 16); two tile accumulators alternate so the next tile's MMAs
+//     own partial accumulator (at N = 16 an MMA is a few cycles of tensor work,
+//     while this loop's per-MMA work in the issuing lane -- descriptors, the
+//     accumulator choice -- came to ~150 cycles, as long as the W stream; two
+//     lanes halve it); two tile accumulators alternate so the next tile's MMAs
 //     overlap the epilogue of this one;
 //   * warps 2-5 read the accumulator (warp w owns TMEM lanes 32*(w%4)..+31, i.e.
 //     32 vocab rows) and keep, per position, a top-K list in registers across
