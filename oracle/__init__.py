@@ -69,6 +69,8 @@ class Oracle:
         L = self.lib
         i64, i32, vp = ct.c_int64, ct.c_int32, ct.c_void_p
         L.df2o_num_threads.restype = ct.c_int
+        L.df2o_set_num_threads.argtypes = [ct.c_int]
+        L.df2o_set_num_threads.restype = None
         L.df2o_logits.argtypes = [vp, i64, i64, vp, i64, vp]
         L.df2o_unary_topk.argtypes = [vp, i64, i64, vp, i64, i32, ct.c_double, ct.c_double, vp, i32, vp, vp,
                                       vp, vp]
@@ -87,6 +89,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.df2o_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        """Host threads of the following calls (their results do not depend on it)."""
+        self.lib.df2o_set_num_threads(int(n))
 
     @staticmethod
     def _check(rc):

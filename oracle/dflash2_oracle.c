@@ -116,6 +116,16 @@ int df2o_num_threads(void)
 #endif
 }
 
+/* Host threads the following calls use (timing only; results do not depend on it). */
+void df2o_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ---------------------------------------------------------------- logits -- */
 
 /* U[p,v] = sum_d h[p,d] * W[v,d], rounded to fp32. */
