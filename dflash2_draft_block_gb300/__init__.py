@@ -22,6 +22,9 @@ DF2_DTYPE_BF16 = 0
 DF2_DTYPE_F32 = 1
 DF2_STATUS_ID_OUT_OF_RANGE = 0x1
 DF2_STATUS_WAIT_TIMEOUT = 0x2
+DF2_HEAD_PATH_STREAM = 0
+DF2_HEAD_PATH_GEMM = 1
+DF2_HEAD_PATH_CUDA_CORE = 2
 
 
 class DFlash2Error(RuntimeError):
@@ -37,6 +40,11 @@ def lib():
 def kernels_launched() -> int:
     """Kernels this library has launched in this process so far."""
     return int(lib().dflash2_kernels_launched())
+
+
+def unary_topk_path(P, D, V, K) -> int:
+    """DF2_HEAD_PATH_* of the head kernels for these shapes (-1: shapes rejected)."""
+    return int(lib().dflash2_unary_topk_path(P, D, V, K))
 
 
 def status_string(code: int) -> str:

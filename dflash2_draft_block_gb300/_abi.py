@@ -17,6 +17,7 @@ SIGNATURES = {
     "dflash2_status_string": (ct.c_char_p, [_int]),
     "dflash2_abi_version": (_int, []),
     "dflash2_kernels_launched": (ct.c_longlong, []),
+    "dflash2_unary_topk_path": (_int, [_i64, _i64, _i64, _int]),
     "dflash2_unary_topk_workspace_size": (_sz, [_i64, _i64, _i64, _int, _int]),
     "dflash2_unary_topk": (_int, [_vp, _i64, _i64, _vp, _i64, _int, _f32, _f32, _vp, _int, _vp, _vp, _vp,
                                   _vp, _sz, _vp, _vp]),

@@ -93,6 +93,15 @@ size_t head_workspace(HeadPath path, int64_t P, int64_t D, int64_t V, int K, int
 
 }  // namespace
 
+DF2_API int dflash2_unary_topk_path(int64_t P, int64_t D, int64_t V, int K) {
+    if (check_head(P, D, V, K, 0, false) != DF2_OK) return -1;
+    switch (pick_head(P, D, V, K)) {
+        case HeadPath::Skinny: return DF2_HEAD_PATH_STREAM;
+        case HeadPath::Wide: return DF2_HEAD_PATH_GEMM;
+        default: return DF2_HEAD_PATH_CUDA_CORE;
+    }
+}
+
 DF2_API size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V, int K, int r) {
     (void)r;
     if (check_head(P, D, V, K, 0, false) != DF2_OK || P == 0) return 0;
@@ -136,7 +145,7 @@ DF2_API int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const ui
             if (e != cudaSuccess) return DF2_ERR_CUDA;
         }
         return from_cuda(df2::topk_merge_sorted_launch(parts.v, parts.id, parts.S, P, K, topk_ids, topk_vals,
-                                                       st, lm));
+                                                       st, lm, df2::Refine{h, W_lm, D}));
     }
     cudaError_t e = df2::head_simple_launch(h, P, D, W_lm, V, K, topk_ids, topk_vals, workspace,
                                             sms, st, lm);
@@ -229,7 +238,8 @@ DF2_API int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const
         if (e != cudaSuccess) return DF2_ERR_CUDA;
     }
     return from_cuda(df2::draft_tail_launch(parts, P, K, topk_ids, topk_vals, anchors, B, G, A, Bc, V,
-                                            r, path, path_scores, pred, pair_scores, dev_status, st, lm));
+                                            r, path, path_scores, pred, pair_scores, dev_status, st, lm,
+                                            df2::Refine{h, W_lm, D}));
 }
 
 // -------------------------------------------------------------- selector --
@@ -350,6 +360,9 @@ DF2_API int dflash2_conv_prepare(const void* x, int dtype, int64_t P, int C, int
     if (df2::conv_prepare_rows_supported(P, C, B, dtype == DF2_DTYPE_F32))
         return from_cuda(df2::conv_prepare_rows_launch(x, dtype == DF2_DTYPE_F32, P, C, B, taps, g, W_proj,
                                                        base, y, dyn_out, st));
+    if (dtype == DF2_DTYPE_BF16 && P > 64 && df2::conv_prepare_tc_supported(P, C, B, taps, g))
+        return from_cuda(df2::conv_prepare_tc_launch(static_cast<const uint16_t*>(x), P, C, B, taps, g, W_proj,
+                                                     base, static_cast<uint16_t*>(y), dyn_out, nullptr, st));
     if (P <= 64) {
         const int sms = num_sms_current();
         if (sms <= 0) return DF2_ERR_CUDA;

@@ -120,19 +120,25 @@ struct WarpTopK {
 };
 
 // Writes the n entries of a list in rank order to out_ids/out_vals[0..K), each
-// value passed through map; slots past n get id -1 / -inf.  Called by `nthreads`
-// cooperating threads (index tid).
+// value passed through map and ranked by (mapped value, lower id): a map that
+// rounds neighbours to one value (a saturating cap) leaves them in id order.
+// Slots past n get id -1 / -inf.  Called by `nthreads` cooperating threads
+// (index tid).
 template <class Map>
 __device__ __forceinline__ void write_sorted(const float* v, const int* id, int n, int K,
                                              int32_t* out_ids, float* out_vals, int tid,
                                              int nthreads, Map map) {
+    const bool plain = map.identity();
     for (int i = tid; i < n; i += nthreads) {
-        const float vi = v[i];
         const int ii = id[i];
+        const float vi = plain ? v[i] : map(v[i]);
         int rank = 0;
-        for (int j = 0; j < n; ++j) rank += ranks_before(v[j], id[j], vi, ii);
+        if (plain)
+            for (int j = 0; j < n; ++j) rank += ranks_before(v[j], id[j], vi, ii);
+        else
+            for (int j = 0; j < n; ++j) rank += ranks_before(map(v[j]), id[j], vi, ii);
         out_ids[rank] = ii;
-        out_vals[rank] = map(vi);
+        out_vals[rank] = vi;
     }
     for (int i = n + tid; i < K; i += nthreads) {
         out_ids[i] = -1;

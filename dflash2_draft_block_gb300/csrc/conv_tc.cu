@@ -1,0 +1,536 @@
+// Conv prepare for many rows, fused on the tensor cores: the projection of x, the
+// output-side correction written out and the conv applied in the same kernel.
+//
+//   d[p, (io*taps + j)*G + gi] = sum_c x[p, c] * W_proj[(io*taps + j)*G + gi, c]
+//   y[p, c] = sum_{j < taps, t-j >= 0} (base[0, j, c] + d[p, (0*taps + j)*G + c/g]) * x[p-j, c]
+//   dyn_out[p, j, gi] = d[p, (1*taps + j)*G + gi]
+//
+// (verl-SpeCo PR #62, "What DFlash2 adds": one projection of the hidden state gives
+// the corrections of the conv before the sublayer and of the one after it; prepare
+// applies the first and emits the second.  "Two deltas", item 1: the taps stay
+// inside an anchor block.)
+//
+// A tile is 128 rows of x (a whole number of anchor blocks) times the projection
+// rows of `ng` consecutive groups: the input-side rows of every tap, then the
+// output-side ones (2*taps*ng columns, at most 256), gathered from 2*taps TMA boxes
+// of ng W_proj rows.  In a CTA pair (cta_group::2, 256 rows of x) CTA 0 stages the
+// input-side rows and CTA 1 the output-side ones; each CTA's TMEM receives all the
+// tile's columns for its own 128 rows.
+//
+// Epilogue (warps 2-5, thread = TMEM lane = row): the output-side columns go to
+// dyn_out; the input-side ones to shared memory; then the four warps apply the conv
+// to the tile's rows and its groups' ng*g channels, reading x again (from L2: the
+// units work on consecutive tiles, which share their x rows) and writing y.  The
+// input-side corrections never reach HBM and x is read from HBM once.
+//
+// Roles (192 threads): warp 0 lane 0 issues the TMA loads, warp 1 lane 0 (CTA 0 of
+// a pair) the MMAs into one of two TMEM accumulators, warps 2-5 the epilogue.  All
+// waits are bounded; the epilogue warps decide together, at a barrier that ORs
+// their wait results, whether to go on.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_pair.cuh"
+#include "tc_ptx.cuh"
+
+namespace df2 {
+
+namespace {
+
+constexpr int CM = 128;   // rows of x per CTA tile (MMA M per CTA, TMEM lanes)
+constexpr int CK = 64;    // reduction elements per box (one 128-byte swizzle row)
+constexpr int kCtcThreads = 192;
+constexpr int kCtcEpi = 128;                 // epilogue threads (warps 2-5)
+constexpr uint32_t kXBox = CM * CK * 2;      // 16 KB
+constexpr int kCtcMaxStages = 8;
+constexpr uint32_t kBufCols = 256;           // TMEM columns per accumulator buffer
+
+struct ConvTcArgs {
+    const uint16_t* x;      // [P][C] bf16
+    const float* base;      // [taps][C]: the input-side base kernel
+    uint16_t* y;            // [P][C] bf16
+    float* dyn_out;         // [P][taps][G]
+    int32_t* dev_status;
+    int P, C, B, g, G;
+    int ng;                 // groups per tile
+    int n_gt;               // group tiles (G / ng)
+    int n_mu;               // units along the rows: 128-row tiles, or pairs of them
+    int n_units;            // units launched (CTAs or CTA pairs)
+    int nstages;
+    int ds_ld;              // floats per row of the staged input-side corrections
+};
+
+// W_proj rows one CTA stages per tile: all 2*taps*ng, or (pair) its side's taps*ng.
+__host__ __device__ inline uint32_t ctc_b_rows(int taps, int ng, bool pair) {
+    return uint32_t((pair ? 1 : 2) * taps * ng);
+}
+__host__ __device__ inline uint32_t ctc_stage_bytes(int taps, int ng, bool pair) {
+    return kXBox + ctc_b_rows(taps, ng, pair) * CK * 2;
+}
+__host__ __device__ inline uint32_t ctc_ds_off(int nstages, int taps, int ng, bool pair) {
+    uint32_t off = uint32_t(nstages) * ctc_stage_bytes(taps, ng, pair);
+    off += uint32_t(2 * nstages + 5) * 8 + 16;  // barriers, TMEM address, abort flag
+    return (off + 15) / 16 * 16;
+}
+__host__ __device__ inline uint32_t ctc_smem(int nstages, int taps, int ng, bool pair, int ds_ld) {
+    return ctc_ds_off(nstages, taps, ng, pair) + uint32_t(CM) * uint32_t(ds_ld) * 4;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The conv of rows [m0, m0 + rows) (whole anchor blocks) on channels
+// [c_lo, c_lo + nch*8), with the input-side corrections ds[r][j*ng + gi - g0] of
+// the tile's groups.  Item = one 8-channel chunk of one block, walked row by row
+// with the last TAPS rows of x in registers (the arithmetic of the standalone
+// apply: acc = fma(base + d, x, acc) over the taps in order).  Consecutive threads
+// take consecutive chunks of the same block, so every load and store of a row is
+// coalesced.
+template <int TAPS>
+__device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, int64_t m0, int rows, int g0,
+                                          int etid) {
+    const int nch = a.ng * a.g / 8;
+    const int c_lo = g0 * a.g;
+    const int B = a.B, C = a.C;
+    const int nblk = rows / B;
+    const bool one_group = (a.g % 8) == 0;  // a chunk's 8 channels share one group
+    for (int item = etid; item < nblk * nch; item += kCtcEpi) {
+        const int blk = item / nch, ch = item - blk * nch;
+        const int c = c_lo + ch * 8;
+        const int r0 = blk * B;
+        float kb[TAPS][8], hist[TAPS][8];
+#pragma unroll
+        for (int j = 0; j < TAPS; ++j) {
+            const float4 lo = __ldg(reinterpret_cast<const float4*>(a.base + int64_t(j) * C + c));
+            const float4 hi = __ldg(reinterpret_cast<const float4*>(a.base + int64_t(j) * C + c + 4));
+            kb[j][0] = lo.x; kb[j][1] = lo.y; kb[j][2] = lo.z; kb[j][3] = lo.w;
+            kb[j][4] = hi.x; kb[j][5] = hi.y; kb[j][6] = hi.z; kb[j][7] = hi.w;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hist[j][e] = 0.f;
+        }
+        const int gl0 = c / a.g - g0;
+        for (int t0 = 0; t0 < B; t0 += 8) {
+            uint4 cur[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (t0 + u < B) cur[u] = __ldg(reinterpret_cast<const uint4*>(a.x + (m0 + r0 + t0 + u) * C + c));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int t = t0 + u;
+                if (t >= B) break;
+                const int r = r0 + t;
+#pragma unroll
+                for (int j = TAPS - 1; j > 0; --j)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hist[j][e] = hist[j - 1][e];
+                unpack8(cur[u], hist[0]);
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+                const float* drow = ds + size_t(r) * a.ds_ld;
+#pragma unroll
+                for (int j = 0; j < TAPS; ++j) {
+                    if (j > t) break;
+                    if (one_group) {
+                        const float d = drow[j * a.ng + gl0];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(kb[j][e] + d, hist[j][e], acc[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float d = drow[j * a.ng + (c + e) / a.g - g0];
+                            acc[e] = fmaf(kb[j][e] + d, hist[j][e], acc[e]);
+                        }
+                    }
+                }
+                uint4 w;
+                w.x = pack_bf16x2(acc[0], acc[1]);
+                w.y = pack_bf16x2(acc[2], acc[3]);
+                w.z = pack_bf16x2(acc[4], acc[5]);
+                w.w = pack_bf16x2(acc[6], acc[7]);
+                *reinterpret_cast<uint4*>(a.y + (m0 + r) * C + c) = w;
+            }
+        }
+    }
+}
+
+template <int TAPS, bool PAIR>
+__global__ void __launch_bounds__(kCtcThreads, 1)
+conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                       const ConvTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned by pointer arithmetic on the shared array (keeps every
+    // access derived from it in the shared address space)
+    uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int ng = a.ng, nstages = a.nstages;
+    const int half = TAPS * ng;          // input-side columns (= output-side columns)
+    const int N = 2 * half;              // MMA N
+    const uint32_t brows = ctc_b_rows(TAPS, ng, PAIR);
+    const uint32_t stage_bytes = kXBox + brows * CK * 2;
+    uint8_t* stages = smem;              // stage s: one x box, then the W_proj boxes
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(nstages) * stage_bytes);
+    uint64_t* empty = full + nstages;
+    uint64_t* tfull = empty + nstages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* mma_done = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    float* ds = reinterpret_cast<float*>(smem + ctc_ds_off(nstages, TAPS, ng, PAIR));  // [CM][ds_ld]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bid = int(blockIdx.x);
+    const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? bid >> 1 : bid;
+    // tiles numbered group-tile fastest, dealt round-robin to the units: at every
+    // step the units work on consecutive tiles, which share their x rows in L2
+    const int total = a.n_mu * a.n_gt;
+    const int ntiles = unit < total ? (total - unit + a.n_units - 1) / a.n_units : 0;
+    auto tile_mt = [&](int k) {
+        const int mu = (unit + k * a.n_units) / a.n_gt;
+        return PAIR ? 2 * mu + int(rank) : mu;
+    };
+    auto tile_gt = [&](int k) { return (unit + k * a.n_units) % a.n_gt; };
+    const int nbox = (a.C + CK - 1) / CK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nstages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tempty[b], PAIR ? 8 : 4);  // the epilogue warps of one CTA, or of both
+        }
+        tc::mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        if (PAIR) {
+            tc::tmem_alloc_pair(tmem_holder, 512);
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc(tmem_holder, 512);
+            tc::tmem_relinquish();
+        }
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tm_x);
+        tc::prefetch_tmap(&tm_w);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (PAIR) tc::cluster_sync_all();  // the peer's barriers are initialised before any remote use
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            // x: its rows are read by the group tiles of one row tile, then by the
+            // epilogue; W_proj (a few MB) is read by every row tile
+            const uint64_t pol_x = tc::l2_policy_evict_normal();
+            const uint64_t pol_w = tc::l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            int8_t armed[kCtcMaxStages];
+            for (int s = 0; s < kCtcMaxStages; ++s) armed[s] = -1;
+            bool ok = true;
+            for (int k = 0; k < ntiles && ok; ++k) {
+                const int mt = tile_mt(k), g0 = tile_gt(k) * ng;
+                for (int kb = 0; kb < nbox; ++kb) {
+                    if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                    // PAIR: CTA 0's full barrier counts the bytes both CTAs stage
+                    if (leader) tc::mbar_arrive_expect_tx(&full[stage], stage_bytes * (PAIR ? 2u : 1u));
+                    uint8_t* st = stages + size_t(stage) * stage_bytes;
+                    const int xk = kb * CK;
+                    if (PAIR) {
+                        const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
+                        tc::tma_load_2d_pair(st, &tm_x, fb, xk, mt * CM, pol_x);
+#pragma unroll
+                        for (int j = 0; j < TAPS; ++j)
+                            tc::tma_load_2d_pair(st + kXBox + size_t(j) * ng * CK * 2, &tm_w, fb, xk,
+                                                 (int(rank) * TAPS + j) * a.G + g0, pol_w);
+                    } else {
+                        tc::tma_load_2d(st, &tm_x, &full[stage], xk, mt * CM, pol_x);
+#pragma unroll
+                        for (int q = 0; q < 2 * TAPS; ++q)
+                            tc::tma_load_2d(st + kXBox + size_t(q) * ng * CK * 2, &tm_w, &full[stage], xk,
+                                            q * a.G + g0, pol_w);
+                    }
+                    armed[stage] = int8_t(phase);
+                    if (++stage == nstages) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok && leader) {
+                // wait (bounded) for the copies in flight; PAIR: CTA 1's copies complete on
+                // CTA 0's barriers, and CTA 1 leaves only after the closing cluster barrier
+                volatile int never = 0;
+                for (int s = 0; s < nstages; ++s)
+                    if (armed[s] >= 0) tc::mbar_wait(&full[s], uint32_t(armed[s]), &never);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // -------------------------------------------------------- MMA issuer
+            const uint32_t idesc = tc::idesc_bf16_f32(PAIR ? 2 * CM : CM, N);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int k = 0; k < ntiles && ok; ++k) {
+                const int b = k & 1;
+                const uint32_t tph = (k >> 1) & 1;
+                const bool drained = PAIR ? tc::mbar_wait_cluster(&tempty[b], tph ^ 1, abort_flag)
+                                          : tc::mbar_wait(&tempty[b], tph ^ 1, abort_flag);
+                if (!drained) break;
+                tc::fence_after_sync();
+                const uint32_t d_tmem = tmem_base + uint32_t(b) * kBufCols;
+                for (int kb = 0; kb < nbox; ++kb) {
+                    if (!tc::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    uint8_t* st = stages + size_t(stage) * stage_bytes;
+                    const uint32_t a0 = tc::smem_u32(st), b0 = tc::smem_u32(st + kXBox);
+#pragma unroll
+                    for (int kk = 0; kk < CK / 16; ++kk) {
+                        const uint64_t ad = tc::sw128_kmajor_desc(a0 + 32 * kk);
+                        const uint64_t bd = tc::sw128_kmajor_desc(b0 + 32 * kk);
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        if (PAIR) tc::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                        else tc::mma_bf16(d_tmem, ad, bd, idesc, acc);
+                    }
+                    if (PAIR) tc::mma_commit_pair(&empty[stage], 0x3);
+                    else tc::mma_commit(&empty[stage]);
+                    if (++stage == nstages) { stage = 0; phase ^= 1; }
+                }
+                if (ok) {
+                    if (PAIR) tc::mma_commit_pair(&tfull[b], 0x3);
+                    else tc::mma_commit(&tfull[b]);
+                }
+            }
+            if (PAIR) tc::mma_commit_pair(mma_done, 0x3);
+            else tc::mma_commit(mma_done);
+            volatile int never = 0;
+            tc::mbar_wait(mma_done, 0, &never);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;             // TMEM lane = the tile row of this thread
+        const int etid = (warp - 2) * 32 + lane;       // 0 .. 127 for the apply
+        const int64_t gld = int64_t(TAPS) * a.G;       // dyn_out row length
+        for (int k = 0; k < ntiles; ++k) {
+            const int mt = tile_mt(k), g0 = tile_gt(k) * ng;
+            const int b = k & 1;
+            const uint32_t tph = (k >> 1) & 1;
+            const bool got = tc::mbar_wait(&tfull[b], tph, abort_flag);
+            // one decision for the four warps; also orders the previous tile's reads
+            // of ds before this tile's writes
+            if (tc::named_barrier_or(1, kCtcEpi, !got)) break;
+            tc::fence_after_sync();
+            const int64_t m0 = int64_t(mt) * CM;
+            const int64_t m = m0 + r;
+            const bool row_ok = m < a.P;
+            const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(b) * kBufCols;
+            float* drow = ds + size_t(r) * a.ds_ld;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float v[16];
+                tc::tmem_ld16(taddr + uint32_t(c0), v);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int col = c0 + 4 * q;  // four columns of one side and one tap (ng % 4 == 0)
+                    if (col < half) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) drow[col + e] = v[4 * q + e];
+                    } else if (row_ok) {
+                        const int oc = col - half, j = oc / ng, gl = oc - j * ng;
+                        *reinterpret_cast<float4*>(a.dyn_out + m * gld + int64_t(j) * a.G + g0 + gl) =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                // the accumulator is free for the tile after next; PAIR: CTA 0's MMA
+                // thread waits for both CTAs' epilogues
+                if (PAIR) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&tempty[b]), 0));
+                else tc::mbar_arrive(&tempty[b]);
+            }
+            tc::named_barrier(1, kCtcEpi);  // every row's corrections are staged
+            const int64_t left = int64_t(a.P) - m0;
+            const int rows = left <= 0 ? 0 : (left < CM ? int(left) : CM);
+            ctc_apply<TAPS>(a, ds, m0, rows, g0, etid);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    // PAIR: CTA 0's MMAs read this CTA's shared memory and write its TMEM; neither
+    // CTA frees TMEM or exits before both are done
+    if (PAIR) tc::cluster_sync_all();
+    if (threadIdx.x == 0 && *abort_flag && a.dev_status) atomicOr(a.dev_status, DF2_STATUS_WAIT_TIMEOUT);
+    if (warp == 1) {
+        tc::fence_after_sync();
+        if (PAIR) tc::tmem_dealloc_pair(tmem_base, 512);
+        else tc::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------- host --
+
+PFN_cuTensorMapEncodeTiled_v12000 ctc_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool ctc_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = ctc_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    cuuint32_t box[2] = {cuuint32_t(CK), cuuint32_t(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct CtcPlan {
+    bool ok = false;
+    bool pair = false;
+    int ng = 0, n_gt = 0, n_mu = 0, units = 0, nstages = 0, ds_ld = 0;
+};
+
+// Groups per tile: a divisor of G that is a multiple of 8 (each W_proj box then
+// fills whole 1024-byte swizzle atoms) with 2*taps*ng <= 256 (the MMA's N and one
+// TMEM buffer), chosen by a model of the time: rounds of tiles over the units,
+// times a tile's MMA work plus a fixed cost per tile.
+CtcPlan ctc_plan(int64_t P, int C, int B, int taps, int g, int num_sms) {
+    CtcPlan best;
+    if (taps < 1 || taps > 4 || g < 1 || C % g != 0 || C % 8 != 0 || B < 1 || CM % B != 0 || P % B != 0)
+        return best;
+    if (P <= 0 || P > INT32_MAX || num_sms < 2) return best;
+    const int G = C / g;
+    const int n_mt = int((P + CM - 1) / CM);
+    const bool pair = n_mt >= 2;
+    const int n_mu = pair ? (n_mt + 1) / 2 : n_mt;
+    const int slots = pair ? num_sms / 2 : num_sms;
+    const uint32_t budget = 227 * 1024 - 1024;
+    double best_cost = 0;
+    for (int ng = 8; 2 * taps * ng <= 256; ng += 8) {
+        if (G % ng != 0 || (ng * g) % 8 != 0) continue;
+        const int ds_ld = (taps * ng) | 1;  // odd: a row's writes land in distinct banks
+        int st = 0;
+        for (int s = kCtcMaxStages; s >= 3; --s)
+            if (ctc_smem(s, taps, ng, pair, ds_ld) <= budget) { st = s; break; }
+        if (st == 0) continue;
+        const int n_gt = G / ng;
+        const int64_t total = int64_t(n_mu) * n_gt;
+        const int units = int(total < slots ? total : slots);
+        const int64_t rounds = (total + units - 1) / units;
+        const double cost = double(rounds) * (2.0 * taps * ng + 48.0);
+        if (!best.ok || cost < best_cost) {
+            best_cost = cost;
+            best.ok = true;
+            best.pair = pair;
+            best.ng = ng;
+            best.n_gt = n_gt;
+            best.n_mu = n_mu;
+            best.units = units;
+            best.nstages = st;
+            best.ds_ld = ds_ld;
+        }
+    }
+    return best;
+}
+
+template <int TAPS, bool PAIR>
+cudaError_t ctc_launch(const CUtensorMap& tx, const CUtensorMap& tw, const ConvTcArgs& a, cudaStream_t stream) {
+    const size_t smem = ctc_smem(a.nstages, TAPS, a.ng, PAIR, a.ds_ld) + 1024;
+    auto kernel = conv_prepare_tc_kernel<TAPS, PAIR>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned((PAIR ? 2 : 1) * a.n_units));
+    cfg.blockDim = dim3(kCtcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR ? 2u : 1u;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kernel, tx, tw, a);
+    note_launch();
+    return e;
+}
+
+int ctc_num_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
+}  // namespace
+
+bool conv_prepare_tc_supported(int64_t P, int C, int B, int taps, int g) {
+    return P > 0 && ctc_plan(P, C, B, taps, g, ctc_num_sms() > 0 ? ctc_num_sms() : 2).ok;
+}
+
+cudaError_t conv_prepare_tc_launch(const uint16_t* x, int64_t P, int C, int B, int taps, int g,
+                                   const uint16_t* W, const float* base, uint16_t* y, float* dyn_out,
+                                   int32_t* dev_status, cudaStream_t stream) {
+    const int sms = ctc_num_sms();
+    const CtcPlan p = ctc_plan(P, C, B, taps, g, sms);
+    if (!p.ok) return cudaErrorInvalidValue;
+    const int G = C / g;
+    CUtensorMap tx, tw;
+    if (!ctc_map(&tx, x, P, C, CM) || !ctc_map(&tw, W, int64_t(2) * taps * G, C, p.ng))
+        return cudaErrorInvalidValue;
+    ConvTcArgs a{};
+    a.x = x;
+    a.base = base;
+    a.y = y;
+    a.dyn_out = dyn_out;
+    a.dev_status = dev_status;
+    a.P = int(P);
+    a.C = C;
+    a.B = B;
+    a.g = g;
+    a.G = G;
+    a.ng = p.ng;
+    a.n_gt = p.n_gt;
+    a.n_mu = p.n_mu;
+    a.n_units = p.units;
+    a.nstages = p.nstages;
+    a.ds_ld = p.ds_ld;
+    switch (taps) {
+#define DF2_CTC(TP) \
+    case TP: return p.pair ? ctc_launch<TP, true>(tx, tw, a, stream) : ctc_launch<TP, false>(tx, tw, a, stream);
+        DF2_CTC(1)
+        DF2_CTC(2)
+        DF2_CTC(3)
+        DF2_CTC(4)
+#undef DF2_CTC
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace df2

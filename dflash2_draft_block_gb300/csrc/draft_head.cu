@@ -64,7 +64,7 @@ draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part
                   const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int r,
                   int32_t* __restrict__ path, float* __restrict__ path_scores,
                   const int32_t* __restrict__ pred, float* __restrict__ pair_scores,
-                  int32_t* __restrict__ dev_status, unsigned tab_off, LogitMap lm) {
+                  int32_t* __restrict__ dev_status, unsigned tab_off, LogitMap lm, Refine rf) {
     extern __shared__ __align__(16) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
     const int t = int(cluster.block_rank());
@@ -78,7 +78,7 @@ draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part
     float* tab_v = reinterpret_cast<float*>(tab_id + T * K);
     int* tab_bad = reinterpret_cast<int*>(tab_v + T * K);
 
-    mrg::merge_position<R>(part_v, part_id, S, P, K, p, ids, vals, smem, lm);
+    mrg::merge_position<R>(part_v, part_id, S, P, K, p, ids, vals, smem, lm, rf);
     __syncthreads();  // row p's list is written (by warp 0) and smem is free again
     const int32_t pid = pred ? __ldg(pred + p) : -1;
     const bool pred_ok = pid >= 0 && pid < V;
@@ -147,7 +147,7 @@ cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, cons
                         int32_t* ids, float* vals, const int32_t* anchors, const float* G,
                         const uint16_t* A, const uint16_t* Bc, int64_t V, int r, int32_t* path,
                         float* path_scores, const int32_t* pred, float* pair_scores, int32_t* dev_status,
-                        LogitMap lm, bool probe_only, bool* fits) {
+                        LogitMap lm, Refine rf, bool probe_only, bool* fits) {
     auto kernel = draft_tail_kernel<R, N>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
@@ -175,7 +175,7 @@ cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, cons
     }
     return cudaLaunchKernelEx(&cfg, kernel, parts.v, parts.id, parts.S, P, K, ids, vals, anchors, B, G, A,
                               Bc, V, r, path, path_scores, pred, pair_scores, dev_status,
-                              unsigned(tail_tab_off(K, r, parts.S)), lm);
+                              unsigned(tail_tab_off(K, r, parts.S)), lm, rf);
 }
 
 // Runs (or, probe_only, checks that the cluster shape can run) the right instance.
@@ -183,13 +183,13 @@ cudaError_t dispatch_tail(bool probe_only, bool* fits, const TopkParts& parts, i
                           float* vals, const int32_t* anchors, int B, const float* G, const uint16_t* A,
                           const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
                           const int32_t* pred, float* pair_scores, int32_t* dev_status, LogitMap lm,
-                          cudaStream_t stream) {
+                          Refine rf, cudaStream_t stream) {
     const size_t smem = tail_smem(B, K, r, parts.S);
     const int nch = (r + 255) / 256;
     cudaError_t e = cudaSuccess;
 #define DF2_TAIL(RV, N)                                                                                \
     e = launch_tail<RV, N>(P, B, smem, stream, parts, K, ids, vals, anchors, G, A, Bc, V, r, path,     \
-                           path_scores, pred, pair_scores, dev_status, lm, probe_only, fits)
+                           path_scores, pred, pair_scores, dev_status, lm, rf, probe_only, fits)
 #define DF2_TAIL_N(RV)                        \
     do {                                      \
         if (nch <= 1) DF2_TAIL(RV, 1);        \
@@ -221,8 +221,9 @@ bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const size_t smem = tail_smem(B, K, r, S);
-    const uint64_t key = (uint64_t(unsigned(dev)) << 48) ^ (uint64_t(B) << 40) ^ (uint64_t(K <= 32) << 39) ^
-                         (uint64_t((r + 255) / 256) << 32) ^ uint64_t(smem);
+    const uint64_t key = (uint64_t(unsigned(dev)) << 48) ^ (uint64_t(B) << 40) ^
+                         (uint64_t(K <= 32) << 37) ^ (uint64_t((r + 255) / 256) << 32) ^
+                         uint64_t(smem);
     {
         std::lock_guard<std::mutex> lock(g_fit_mu);
         auto it = g_fit.find(key);
@@ -230,8 +231,10 @@ bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
     }
     bool fits = false;
     const TopkParts probe{nullptr, nullptr, S};
+    static const uint16_t probe_row = 0;  // any non-null operand: the tail always refines
     if (dispatch_tail(true, &fits, probe, P, K, nullptr, nullptr, nullptr, B, nullptr, nullptr, nullptr, 1, r,
-                      nullptr, nullptr, nullptr, nullptr, nullptr, LogitMap{}, nullptr) != cudaSuccess)
+                      nullptr, nullptr, nullptr, nullptr, nullptr, LogitMap{}, Refine{&probe_row, nullptr, 0},
+                      nullptr) != cudaSuccess)
         fits = false;
     std::lock_guard<std::mutex> lock(g_fit_mu);
     g_fit[key] = fits;
@@ -242,10 +245,10 @@ cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t*
                               const int32_t* anchors, int B, const float* G, const uint16_t* A,
                               const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
                               const int32_t* pred, float* pair_scores, int32_t* dev_status,
-                              cudaStream_t stream, LogitMap lm) {
+                              cudaStream_t stream, LogitMap lm, Refine rf) {
     bool unused = false;
     const cudaError_t e = dispatch_tail(false, &unused, parts, P, K, ids, vals, anchors, B, G, A, Bc, V, r, path,
-                                        path_scores, pred, pair_scores, dev_status, lm, stream);
+                                        path_scores, pred, pair_scores, dev_status, lm, rf, stream);
     note_launch();
     return e;
 }

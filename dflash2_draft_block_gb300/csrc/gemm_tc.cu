@@ -714,7 +714,8 @@ cudaError_t wide_topk_launch(const uint16_t* A, int64_t M, const uint16_t* B, in
         *parts_out = TopkParts{a.part_v, a.part_id, n_groups};
         return cudaSuccess;
     }
-    return topk_merge_sorted_launch(a.part_v, a.part_id, n_groups, M, K, ids, vals, stream);
+    return topk_merge_sorted_launch(a.part_v, a.part_id, n_groups, M, K, ids, vals, stream, LogitMap{},
+                                    Refine{A, B, Kd});
 }
 
 }  // namespace df2

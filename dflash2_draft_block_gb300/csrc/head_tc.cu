@@ -489,7 +489,8 @@ int head_tc_launch(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W, i
         *parts_out = TopkParts{part_v, part_id, int(parts)};
         return DF2_OK;
     }
-    e = topk_merge_sorted_launch(part_v, part_id, int(parts), P, K, ids, vals, stream);
+    e = topk_merge_sorted_launch(part_v, part_id, int(parts), P, K, ids, vals, stream, LogitMap{},
+                                 Refine{h, W, D});
     return e == cudaSuccess ? DF2_OK : DF2_ERR_CUDA;
 }
 

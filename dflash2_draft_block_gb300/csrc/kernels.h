@@ -9,11 +9,13 @@ namespace df2 {
 
 // The unary logits' output multiplier and final softcap: u -> cap * tanh(mul * u / cap),
 // or mul * u when cap == 0 (the defaults leave every value bit for bit as it is).
-// With mul > 0 the map is increasing, so the kernels select on the raw logits
-// and map only the K values they keep.
+// With mul > 0 the map is non-decreasing, so the kernels select on the raw logits
+// and map only the K values they keep; where rounding maps neighbours to one
+// value (a saturating cap), the kept list is re-ranked by (mapped value, lower id).
 struct LogitMap {
     float mul = 1.f;
     float cap = 0.f;
+    __host__ __device__ __forceinline__ bool identity() const { return mul == 1.f && cap == 0.f; }
     __device__ __forceinline__ float operator()(float u) const {
         const float x = mul * u;
         return cap > 0.f ? cap * tanhf(x / cap) : x;
@@ -32,7 +34,16 @@ cudaError_t head_simple_launch(const uint16_t* h, int64_t P, int64_t D, const ui
 cudaError_t topk_merge_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
                               int32_t* ids, float* vals, cudaStream_t stream, LogitMap lm = LogitMap{});
 
-// ---- S partial lists [S][P][K], each in rank order (id -1 = empty), K <= 64 -> top-K [P][K]
+// Where the top-K merges find the logits' operands to recompute near-tied
+// neighbours exactly (h == null: no recompute).
+struct Refine {
+    const uint16_t* h;   // [P][D] bf16
+    const uint16_t* W;   // [V][D] bf16
+    int64_t D;           // D % 8 == 0, rows 16-byte aligned
+};
+
+// ---- S partial lists [S][P][K], each in rank order (id -1 = empty), K <= 64 -> top-K [P][K];
+//      with rf, near-tied neighbours (the K-th/(K+1)-th boundary included) recomputed exactly
 struct TopkParts {
     const float* v;
     const int* id;
@@ -40,7 +51,7 @@ struct TopkParts {
 };
 cudaError_t topk_merge_sorted_launch(const float* part_v, const int* part_id, int S, int64_t P, int K,
                                      int32_t* ids, float* vals, cudaStream_t stream,
-                                     LogitMap lm = LogitMap{});
+                                     LogitMap lm = LogitMap{}, Refine rf = Refine{nullptr, nullptr, 0});
 
 // ---- out = X . W^T on the CUDA cores, columns split between two outputs
 cudaError_t gemm_simple_launch(const void* X, bool x_f32, const uint16_t* W, int64_t M, int64_t N,
@@ -96,7 +107,8 @@ cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t*
                               const int32_t* anchors, int B, const float* G, const uint16_t* A,
                               const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
                               const int32_t* pred, float* pair_scores, int32_t* dev_status,
-                              cudaStream_t stream, LogitMap lm = LogitMap{});
+                              cudaStream_t stream, LogitMap lm = LogitMap{},
+                              Refine rf = Refine{nullptr, nullptr, 0});
 
 // ---- conv: y = sum_{j<taps, t-j>=0} (base[j] + dyn[p, j, c/g]) * x[p-j]
 // ---- conv prepare for few rows (P <= 64, B <= 16): projection and apply fused
@@ -104,6 +116,13 @@ bool conv_prepare_rows_supported(int64_t P, int C, int B, bool f32);
 cudaError_t conv_prepare_rows_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
                                      const uint16_t* W, const float* base, void* y, float* dyn_out,
                                      cudaStream_t stream);
+// ---- conv prepare for many bf16 rows, fused on the tensor cores (conv_tc.cu): the
+//      projection, dyn_out and the conv applied in one kernel; needs 128 % B == 0,
+//      taps <= 4 and a multiple of 8 groups dividing C / g
+bool conv_prepare_tc_supported(int64_t P, int C, int B, int taps, int g);
+cudaError_t conv_prepare_tc_launch(const uint16_t* x, int64_t P, int C, int B, int taps, int g,
+                                   const uint16_t* W, const float* base, uint16_t* y, float* dyn_out,
+                                   int32_t* dev_status, cudaStream_t stream);
 cudaError_t conv_apply_launch(const void* x, bool f32, int64_t P, int C, int B, int taps, int g,
                               const float* base_io, const float* dyn, int64_t dyn_ld, void* y,
                               cudaStream_t stream, const void* res = nullptr);

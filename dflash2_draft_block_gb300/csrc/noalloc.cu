@@ -54,6 +54,15 @@ DF2_API int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D,
     if (need > DF2_NOALLOC_SCRATCH_BYTES) return DF2_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     if (need > 0) {
+        // the scratch address is per device: a stream of another device would
+        // have its kernels read this device's address
+        if (stream != nullptr) {
+            int dev = 0, sdev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+                return DF2_ERR_CUDA;
+            if (sdev != dev) return DF2_ERR_INVALID_ARGUMENT;
+        }
         const int rc = scratch_for_current_device(&scratch);
         if (rc != DF2_OK) return rc;
     }

@@ -2,18 +2,31 @@
 // shared by the merge kernel and the fused draft-head kernel.
 //
 // One CTA per position.  All lists of the position are first copied to shared
-// memory in one round of independent loads.  Every list is sorted, so the K best
-// list heads are K entries that rank at or above the K-th best head t: the final
-// K entries all rank at or above t, and each list contributes only its prefix that
+// memory in one round of independent loads.  Every list is sorted, so the L best
+// list heads are L entries that rank at or above the L-th best head t: the best L
+// entries all rank at or above t, and each list contributes only its prefix that
 // does.  The threads rank the heads against each other to find t, compact the
 // qualifying prefixes into a candidate buffer (a few dozen entries on typical
 // data), and one warp folds the candidates into a register-resident list
-// (topk_warp.cuh) and writes the K best in rank order.  Without a threshold
-// (fewer than K non-empty lists) the 8 warps fold whole lists and warp 0 combines
-// their lists.
+// (topk_warp.cuh).  Without a threshold (fewer than L non-empty lists) the 8 warps
+// fold whole lists and warp 0 combines their lists.
+//
+// Exact decisions on near ties.  The head kernels sum the logits in fp32 on the
+// tensor cores, in another order than a plain sum; two logits closer than that
+// rounding (a few ulps of the accumulator over the reduction) may come out in the
+// wrong order.  With a Refine argument the merge also finds the (K+1)-th entry, and
+// wherever two neighbours of that list lie within 2^-14 of their magnitude (well
+// above the fp32 accumulation error of the tensor-core sum), it recomputes those
+// logits as correctly rounded fp32 values -- exact bf16 products, compensated
+// summation, one final rounding: the precision the ranking is defined in -- and
+// ranks the K + 1 entries again by (value, lower id).  The K-th/(K+1)-th boundary and the order inside the list are
+// then decided on correctly rounded logits.  (A candidate a head CTA dropped
+// because its own K entries were all better cannot be recovered: that needs the
+// whole top K + 1 in one CTA's vocabulary range.)
 #pragma once
 
 #include "common.cuh"
+#include "kernels.h"
 #include "topk_warp.cuh"
 
 namespace df2 {
@@ -25,24 +38,106 @@ constexpr int kOneWarpCands = 128;  // up to this many candidates one warp folds
 
 __host__ __device__ inline size_t merge_smem(int S, int K) { return size_t(S) * K * 16 + size_t(S) * 12; }
 
+// Two neighbouring fp32 logits this close may be ordered wrongly by the
+// tensor-core sum and are recomputed exactly.
+__device__ __forceinline__ bool near_tie(float a, float b) {
+    const float mag = fmaxf(fmaxf(fabsf(a), fabsf(b)), 1.f);
+    return a - b <= mag * (1.f / 16384.f);
+}
+
+// s + e = a + b exactly (Knuth's TwoSum; round-to-nearest adds, never contracted).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Adds p to the unevaluated sum s + c: s takes the rounded sum, c collects every
+// rounding error (compensated summation; the result carries about twice fp32's
+// precision).
+__device__ __forceinline__ void comp_add(float& s, float& c, float p) {
+    float e;
+    two_sum(s, p, s, e);
+    c = __fadd_rn(c, e);
+}
+
+// h . w over D elements, rounded once to fp32 from a sum whose error is of order
+// D * 2^-48 times the sum of |products| (a plain fp32 sum's is of order D * 2^-24):
+// every bf16 x bf16 product is exact in fp32, the products are added with
+// compensated summation in
+// four independent accumulators per lane (fixed order: lane chunks, then the
+// accumulators, then a shuffle tree), and s + c is rounded once.  All lanes of the
+// warp call; every lane returns the result.  (fp32 arithmetic: fp64 runs at a small
+// fraction of the fp32 rate on this GPU.)
+__device__ __forceinline__ float exact_logit(const uint16_t* __restrict__ h, const uint16_t* __restrict__ w,
+                                             int64_t D, int lane) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+    const int64_t nck = D / 8;  // 16-byte chunks of a row
+    // a lane takes chunks lane, lane + 32, ...; eight of them are loaded before any
+    // is used, so a row costs a few memory latencies, not one per chunk
+    for (int64_t k0 = lane; k0 < nck; k0 += 32 * 8) {
+        uint4 hv[8], wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t k = k0 + 32 * u;
+            if (k < nck) {
+                hv[u] = __ldg(reinterpret_cast<const uint4*>(h) + k);
+                wv[u] = __ldg(reinterpret_cast<const uint4*>(w) + k);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (k0 + 32 * u >= nck) break;
+            float hf[8], wf[8];
+            unpack8(hv[u], hf);
+            unpack8(wv[u], wf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) comp_add(s[e & 3], c[e & 3], __fmul_rn(hf[e], wf[e]));
+        }
+    }
+    float S = s[0], Cc = c[0];
+#pragma unroll
+    for (int a = 1; a < 4; ++a) {
+        comp_add(S, Cc, s[a]);
+        Cc = __fadd_rn(Cc, c[a]);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float S2 = __shfl_xor_sync(kFull, S, o), C2 = __shfl_xor_sync(kFull, Cc, o);
+        // the same (S, C) in both lanes of a pair: the lower lane's operand first
+        const bool lo = (lane & o) == 0;
+        float a = lo ? S : S2, b = lo ? S2 : S, e;
+        two_sum(a, b, S, e);
+        Cc = __fadd_rn(__fadd_rn(lo ? Cc : C2, lo ? C2 : Cc), e);
+    }
+    return __fadd_rn(S, Cc);
+}
+
 // The final top-K of position p from the S sorted lists part_[v|id][s][P][K], by
-// one CTA of kMergeThreads threads with merge_smem(S, K) bytes at smem.  Warp 0
-// writes out_ids/out_vals[p], each kept value passed through map; the other
-// warps return without touching them.
+// one CTA of kMergeThreads threads with merge_smem(S, K) bytes at smem (32 R >=
+// K).  Every thread of the CTA calls it.  Warp 0 writes
+// out_ids/out_vals[p] in rank order, each kept value passed through map and the
+// list ranked by (mapped value, lower id); the CTA's other warps write nothing.
 template <int R, class Map>
 __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
                                                const int* __restrict__ part_id, int S, int64_t P,
                                                int K, int64_t p, int32_t* __restrict__ out_ids,
-                                               float* __restrict__ out_vals, uint8_t* smem, Map map) {
+                                               float* __restrict__ out_vals, uint8_t* smem, Map map,
+                                               Refine rf = Refine{nullptr, nullptr, 0}) {
     float* cv = reinterpret_cast<float*>(smem);        // [S*K] this position's lists
     int* ci = reinterpret_cast<int*>(cv + S * K);
     float* bv = reinterpret_cast<float*>(ci + S * K);  // [S*K] candidates
     int* bi = reinterpret_cast<int*>(bv + S * K);
-    __shared__ float xv[kWarps][R * 32];
-    __shared__ int xi[kWarps][R * 32];
+    __shared__ float xv[kWarps][R * 32 + 1];  // row 0 also holds the (K+1)-th entry
+    __shared__ int xi[kWarps][R * 32 + 1];
+    __shared__ int re_idx[R * 32 + 1];
     __shared__ float t_v;
-    __shared__ int t_id, have_t, n_cand;
+    __shared__ int t_id, have_t, n_cand, n_re;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool refine = rf.h != nullptr;
+    // refining needs the (K+1)-th entry as well: the threshold is then the
+    // (K+1)-th best head, so that the candidates hold the best K + 1
+    const int L = refine ? K + 1 : K;
     if (tid == 0) {
         have_t = 0;
         n_cand = 0;
@@ -55,7 +150,7 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
         ci[i] = __ldg(part_id + at);
     }
     __syncthreads();
-    // the K-th best head: the head that exactly K-1 other heads rank before.  The
+    // the L-th best head: the head that exactly L-1 other heads rank before.  The
     // heads are packed as rank keys (larger = ranks before; 0 = empty list) into
     // the still unused candidate buffer, and two threads count each head's rank.
     unsigned long long* hk = reinterpret_cast<unsigned long long*>(smem + size_t(S) * K * 16);
@@ -78,7 +173,7 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
     }
     __syncthreads();
     for (int s = tid; s < S; s += kWarps * 32) {
-        if (hk[s] != 0ull && rk[s] == K - 1) {
+        if (hk[s] != 0ull && rk[s] == L - 1) {
             t_v = cv[s * K];
             t_id = ci[s * K];
             have_t = 1;
@@ -142,14 +237,113 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
 #pragma unroll
             for (int rr = 0; rr < R; ++rr) m.offer_sorted(xv[w][rr * 32 + lane], xi[w][rr * 32 + lane], K, lane);
     }
-    if (warp != 0) return;
+    if (!refine) {
+        if (warp != 0) return;
+        if (map.identity()) {
 #pragma unroll
-    for (int rr = 0; rr < R; ++rr) {
-        const int k = rr * 32 + lane;
-        if (k < K) {
-            const bool ok = m.id[rr] != wtk::kEmptyId;
-            out_ids[p * K + k] = ok ? m.id[rr] : -1;
-            out_vals[p * K + k] = ok ? map(m.v[rr]) : -INFINITY;
+            for (int rr = 0; rr < R; ++rr) {
+                const int k = rr * 32 + lane;
+                if (k < K) {
+                    const bool ok = m.id[rr] != wtk::kEmptyId;
+                    out_ids[p * K + k] = ok ? m.id[rr] : -1;
+                    out_vals[p * K + k] = ok ? m.v[rr] : -INFINITY;
+                }
+            }
+            return;
+        }
+        // warp 0 alone from here: its entries to shared memory for the ranking
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            xv[0][rr * 32 + lane] = m.v[rr];
+            xi[0][rr * 32 + lane] = m.id[rr];
+        }
+        __syncwarp();
+    } else {
+        // Warp 0's K entries to shared memory, and after them the (K+1)-th: the best
+        // entry that ranks after the K-th, found by a scan of the candidates (or,
+        // without a threshold, of every list).  Then the entries in runs of near
+        // ties get their exact logits, each recomputed by one warp of the CTA.
+        __syncthreads();  // any fold through xv is over
+        if (warp == 0) {
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                xv[0][rr * 32 + lane] = m.v[rr];
+                xi[0][rr * 32 + lane] = m.id[rr];
+            }
+            float kv;
+            int kid;
+            m.kth(K, kv, kid);
+            float nv = -INFINITY;
+            int nid = wtk::kEmptyId;
+            const int n_scan = have_t ? n_cand : S * K;
+            const float* sv = have_t ? bv : cv;
+            const int* si = have_t ? bi : ci;
+            for (int i = lane; i < n_scan; i += 32) {
+                const int id = si[i];
+                if (id < 0 || id == wtk::kEmptyId) continue;
+                const float v = sv[i];
+                if (kid != wtk::kEmptyId && !ranks_before(kv, kid, v, id)) continue;  // not after the K-th
+                if (nid == wtk::kEmptyId || ranks_before(v, id, nv, nid)) { nv = v; nid = id; }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float ov = __shfl_xor_sync(kFull, nv, o);
+                const int oid = __shfl_xor_sync(kFull, nid, o);
+                if (oid != wtk::kEmptyId && (nid == wtk::kEmptyId || ranks_before(ov, oid, nv, nid))) {
+                    nv = ov;
+                    nid = oid;
+                }
+            }
+            if (lane == 0) {
+                xv[0][K] = kid != wtk::kEmptyId ? nv : -INFINITY;
+                xi[0][K] = kid != wtk::kEmptyId ? nid : wtk::kEmptyId;
+                n_re = 0;
+            }
+            __syncwarp();
+            for (int k = lane; k < L; k += 32) {
+                const bool ok = xi[0][k] != wtk::kEmptyId;
+                const bool up = k > 0 && ok && near_tie(xv[0][k - 1], xv[0][k]);
+                const bool down =
+                    k + 1 < L && ok && xi[0][k + 1] != wtk::kEmptyId && near_tie(xv[0][k], xv[0][k + 1]);
+                if (up || down) re_idx[atomicAdd(&n_re, 1)] = k;
+            }
+        }
+        __syncthreads();
+        const int nre = n_re;
+        if (nre > 0) {
+            const uint16_t* hrow = rf.h + p * rf.D;
+            for (int f = warp; f < nre; f += kWarps) {
+                const int k = re_idx[f];
+                const float x = exact_logit(hrow, rf.W + int64_t(xi[0][k]) * rf.D, rf.D, lane);
+                if (lane == 0) xv[0][k] = x;
+            }
+            __syncthreads();
+        }
+        if (warp != 0) return;
+    }
+    // Rank the kept entries by (mapped value, id): the list is sorted by the fp32
+    // values the kernels computed; this settles the recomputed near ties and the
+    // neighbours a saturating map rounds to one value.  Empty slots stay at the end.
+    int nvalid = 0;
+    for (int k = 0; k < L; ++k) nvalid += xi[0][k] != wtk::kEmptyId ? 1 : 0;
+    for (int k = lane; k < L; k += 32) {
+        const int id = xi[0][k];
+        if (id == wtk::kEmptyId) {
+            if (k < K) {
+                out_ids[p * K + k] = -1;
+                out_vals[p * K + k] = -INFINITY;
+            }
+            continue;
+        }
+        const float mv = map(xv[0][k]);
+        int rank = 0;
+        for (int j = 0; j < L; ++j) {
+            const int oj = xi[0][j];
+            if (oj != wtk::kEmptyId && ranks_before(map(xv[0][j]), oj, mv, id)) ++rank;
+        }
+        if (rank < K && rank < nvalid) {
+            out_ids[p * K + rank] = id;
+            out_vals[p * K + rank] = mv;
         }
     }
 }

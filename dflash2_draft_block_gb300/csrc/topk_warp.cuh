@@ -1,4 +1,4 @@
-// Register-resident top-K for one warp, K <= 64.
+// Register-resident top-K for one warp, K <= 32 R (R = 1, 2 or 3 rows of 32).
 //
 // A list is R = ceil(K/32) "rows" of 32 entries, one entry per lane per row,
 // sorted in rank order (value descending, then token id ascending) across
@@ -9,7 +9,7 @@
 //   2. pair list row 0 lane i with batch lane 31-i: the better of each pair is the
 //      best 32 of the union (a bitonic sequence, sorted by a 5-step merge), the
 //      worse ones are the rest;
-//   3. for R = 2, the rest is sorted the same way and folded into row 1.
+//   3. for each further row, the rest is folded into it the same way.
 // Entries with id == INT_MAX are empty slots (value -inf) and rank last.
 #pragma once
 
@@ -87,7 +87,9 @@ struct List {
         const int r = (K - 1) >> 5, l = (K - 1) & 31;
         float sv = v[0];
         int sid = id[0];
-        if (R > 1 && r == 1) { sv = v[R - 1]; sid = id[R - 1]; }
+#pragma unroll
+        for (int rr = 1; rr < R; ++rr)
+            if (rr == r) { sv = v[rr]; sid = id[rr]; }
         tv = __shfl_sync(kFull, sv, l);
         tid = __shfl_sync(kFull, sid, l);
     }

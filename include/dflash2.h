@@ -87,6 +87,15 @@ int dflash2_abi_version(void);
  * before and after a region to count the region's kernels. */
 long long dflash2_kernels_launched(void);
 
+/* Diagnostics: which kernel path dflash2_unary_topk (and the head of
+ * dflash2_draft_head) takes for these shapes on the current device.  No
+ * counterpart in the pages.  Returns DF2_HEAD_PATH_* (>= 0), or -1 when the shapes
+ * break a rule of dflash2_unary_topk. */
+#define DF2_HEAD_PATH_STREAM 0     /* few positions: the HBM-streaming tensor-core head */
+#define DF2_HEAD_PATH_GEMM 1       /* many positions: the tensor-core GEMM with a top-K epilogue */
+#define DF2_HEAD_PATH_CUDA_CORE 2  /* K > 64 or shapes the tensor-core kernels do not take */
+int dflash2_unary_topk_path(int64_t P, int64_t D, int64_t V, int K);
+
 /* ------------------------------------------------------------------------
  * dflash2_unary_topk — unary logits, per-position top-K, hidden projection.
  *
@@ -148,10 +157,13 @@ int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* 
  * Allocates nothing: no cudaMalloc / cudaFree or allocating library call.
  * The first call on a device looks up that device's copy of the array
  * (cudaGetSymbolAddress, with the device current); make that first call before
- * any stream capture.  All calls share the one array: calls that may overlap on
- * the GPU (different streams, no ordering between them) race and give wrong
- * results.  The array keeps the last call's contents; none of it needs to start
- * at zero.
+ * any stream capture.  The address is kept for the life of the process: after a
+ * cudaDeviceReset of that device it is stale, so do not use this entry point on
+ * a device that has been reset.  `stream` must belong to the current device
+ * (DF2_ERR_INVALID_ARGUMENT otherwise).  All calls share the one array: calls
+ * that may overlap on the GPU (different streams, no ordering between them) race
+ * and give wrong results.  The array keeps the last call's contents; none of it
+ * needs to start at zero.
  * ---------------------------------------------------------------------- */
 #define DF2_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm,

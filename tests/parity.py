@@ -121,13 +121,16 @@ def compare_walk(gpu_path, gpu_score, ref_path, ref_score, ref_margin, what="wal
     rep = Report()
     R, T = ref_path.shape
     for q in range(R):
+        # the float rule's floor: the rms of the request's path scores
+        row = np.asarray(ref_score[q], np.float64)
+        rms = float(np.sqrt(np.mean(row * row))) if T else 0.0
         for t in range(T):
             rep.compared += 1
             if ref_margin[q, t] < MARGIN:
                 rep.flagged += 1
             if gpu_path[q, t] == ref_path[q, t]:
                 ref = float(ref_score[q, t])
-                if not abs(float(gpu_score[q, t]) - ref) <= FTOL * max(abs(ref), 1.0):
+                if not abs(float(gpu_score[q, t]) - ref) <= FTOL * max(abs(ref), rms) + 1e-30:
                     rep.unexplained.append((what, "score", q, t, float(gpu_score[q, t]), ref))
                 continue
             rep.mismatched += 1
@@ -159,3 +162,122 @@ def check_path_valid(orc, gpu_path, anchors, ids, vals, G, A, Bc, block):
             if scores[q, t, js[0]] < scores[q, t].max() - MARGIN:
                 bad.append((q, t, float(scores[q, t, js[0]]), float(scores[q, t].max())))
     assert not bad, f"GPU path not greedy under oracle scores: {bad[:5]}"
+
+
+# ------------------------------------------------------- one whole draft batch --
+
+def request_rows(requests, block):
+    """Row indices of whole requests (anchor blocks) in a [R*B, ...] tensor."""
+    requests = np.asarray(requests, np.int64)
+    return (requests[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+
+
+def oracle_rows_topk(orc, w, inp, rows):
+    """The oracle's top-K and G on the given rows: (rows, ids, vals, margin, G)."""
+    rows = np.asarray(rows, np.int64)
+    oi, ov, om, oG = orc.unary_topk(np.ascontiguousarray(inp["h"][rows]), inp["W_lm"], w.K, W_H=inp["W_H"])
+    return rows, oi, ov, om, oG
+
+
+def chain_rows(w, requests, extra_rows=()):
+    req = np.asarray(sorted(set(int(q) for q in requests)), np.int64)
+    return np.asarray(sorted(set(request_rows(req, w.B).tolist()) | set(int(e) for e in extra_rows)), np.int64)
+
+
+def compare_chain(orc, w, inp, gpu, requests, extra_rows=(), conv=None, check=True, ref_topk=None):
+    """The GPU outputs of one draft batch against the oracle's chain.
+
+    ``gpu`` holds full-size host arrays: ids/vals [P,K], G [P,r], path/pscore
+    [R,B-1], optionally scores [P,K] (teacher-forced) and, with ``conv``, y/dyn/y2.
+    Whole ``requests`` are compared through every step; ``extra_rows`` are single
+    rows compared for the top-K and G only.
+
+    Top-K: the oracle on the same rows (compare_topk's flagged-margin rule).  Walk:
+    the oracle's walk over its own candidate lists where a request's lists equal
+    the GPU's; where a flagged near-tie changed a list, over the GPU's lists (the
+    walk is then judged on the candidates it was given), and in both cases the GPU
+    path must be greedy under the oracle's scores of the GPU's lists.  Teacher-forced
+    scores: the oracle's scorer on the same lists.  Conv: the oracle on the
+    requests' anchor blocks (the conv never reads across a block), finish on the
+    oracle's own correction.
+
+    ``ref_topk`` may pass in oracle_rows_topk(...) of exactly these rows (the
+    expensive part), to compare several GPU runs against one oracle pass.
+
+    Returns a summary dict whose "failures" lists every rule broken; with
+    ``check`` the call asserts that there are none."""
+    B = w.B
+    failures = []
+
+    def rule(fn, *a, **k):
+        try:
+            fn(*a, **k)
+        except AssertionError as e:
+            failures.append(str(e)[:300])
+
+    req = np.asarray(sorted(set(int(q) for q in requests)), np.int64)
+    rrows = request_rows(req, B)
+    summary = {"requests_compared": int(req.size)}
+    if not w.conv_only:
+        K = w.K
+        rows = chain_rows(w, req, extra_rows)
+        gi, gv, gG = gpu["ids"], gpu["vals"], gpu["G"]
+        if ref_topk is None:
+            ref_topk = oracle_rows_topk(orc, w, inp, rows)
+        assert np.array_equal(ref_topk[0], rows), "ref_topk was computed on other rows"
+        _, oi, ov, om, oG = ref_topk
+        topk = compare_topk(gi[rows], gv[rows], oi, ov, om, w.name)
+        summary["topk"] = {"compared": topk.compared, "flagged": topk.flagged, "mismatched": topk.mismatched,
+                           "unexplained": len(topk.unexplained)}
+        rule(topk.check, w.name + " topk")
+        rule(compare_topk_values, gi[rows], gv[rows], oi, ov, w.name + " vals")
+        # the largest deviation of a kept logit from the oracle's, relative to
+        # max(|logit|, 1), where the ids agree
+        same = gi[rows] == oi
+        if same.any():
+            err = np.abs(gv[rows].astype(np.float64) - ov) / np.maximum(np.abs(ov.astype(np.float64)), 1.0)
+            summary["topk"]["max_val_rel_err"] = float(err[same].max())
+        rule(close, gG[rows], oG, what=w.name + " G")
+        if req.size:
+            # the lists the oracle's walk and scorer run on: the oracle's own where
+            # the request's lists match the GPU's, the GPU's otherwise
+            at = {int(p): k for k, p in enumerate(rows)}
+            k_of = np.asarray([at[int(p)] for p in rrows])
+            same_req = np.all((gi[rrows] == oi[k_of]).reshape(req.size, -1), axis=1)
+            same_rows = np.repeat(same_req, B)[:, None]
+            c_ids = np.ascontiguousarray(np.where(same_rows, oi[k_of], gi[rrows]), np.int32)
+            c_vals = np.ascontiguousarray(np.where(same_rows, ov[k_of], gv[rrows]), np.float32)
+            c_G = np.ascontiguousarray(np.where(same_rows, oG[k_of], gG[rrows]), np.float32)
+            anchors = np.ascontiguousarray(inp["anchors"][req])
+            op, os_, omg, st = orc.selector_walk(anchors, c_ids, c_vals, c_G, inp["A"], inp["Bc"], B)
+            gpath = np.ascontiguousarray(gpu["path"][req])
+            walk = compare_walk(gpath, gpu["pscore"][req], op, os_, omg, w.name + " walk")
+            summary["walk"] = {"compared": walk.compared, "flagged": walk.flagged, "mismatched": walk.mismatched,
+                               "unexplained": len(walk.unexplained),
+                               "requests_on_gpu_lists": int((~same_req).sum())}
+            if st != 0:
+                failures.append(f"oracle walk status {st}")
+            rule(walk.check, w.name + " walk")
+            rule(check_path_valid, orc, gpath, anchors, np.ascontiguousarray(gi[rrows]),
+                 np.ascontiguousarray(gv[rrows]), np.ascontiguousarray(gG[rrows]), inp["A"], inp["Bc"], B)
+            if gpu.get("scores") is not None:
+                osc, st = orc.pair_scores(np.ascontiguousarray(inp["pred"][rrows]), c_ids, c_vals, c_G,
+                                          inp["A"], inp["Bc"])
+                summary["teacher_forced_rows"] = int(rrows.size)
+                if st != 0:
+                    failures.append(f"oracle teacher-forced status {st}")
+                rule(close, gpu["scores"][rrows], osc, what=w.name + " teacher-forced scores")
+    if conv is not None and gpu.get("y") is not None and req.size:
+        x, z = np.ascontiguousarray(conv["x"][rrows]), np.ascontiguousarray(conv["z"][rrows])
+        oy, od = orc.conv_prepare(x, B, w.taps, w.g, conv["W_proj"], conv["base"])
+        oy2 = orc.conv_finish(z, B, w.taps, w.g, od, conv["base"])
+        summary["conv_rows"] = int(rrows.size)
+        rule(close, gpu["dyn"][rrows], od, what=w.name + " dyn_out")
+        cmp = close_bf16 if x.dtype == np.uint16 else close
+        rule(cmp, gpu["y"][rrows], oy, what=w.name + " conv y")
+        rule(cmp, gpu["y2"][rrows], oy2, what=w.name + " conv finish")
+    summary["failures"] = failures
+    summary["ok"] = not failures
+    if check:
+        assert not failures, failures
+    return summary

@@ -66,6 +66,18 @@ def test_head_validation(lib):
         assert f(fake, 4, 64, fake, 10, 2, m, c, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 1
 
 
+def test_head_path_query(lib):
+    """The head's kernel path is a host decision: few positions stream the LM head,
+    many positions run the GEMM with a top-K epilogue, K > 64 the CUDA cores."""
+    f = lib.dflash2_unary_topk_path
+    assert f(8, 4096, 151936, 16) == 0          # batch-1 shape
+    assert f(512, 5120, 248320, 16) == 1        # batched shape
+    assert f(4096, 4096, 151936, 64) == 1       # stress shape
+    assert f(20, 256, 3000, 100) == 2           # K > 64
+    assert f(8, 100, 1000, 16) == -1            # D % 8 != 0
+    assert f(8, 256, 10, 16) == -1              # K > V
+
+
 def test_selector_validation(lib):
     fake = VP(0x1000)
     w = lib.dflash2_selector_walk

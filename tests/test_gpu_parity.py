@@ -178,6 +178,56 @@ def test_head_logit_map(orc, df2, P, D, V, K, m, c):
         assert np.all(np.abs(gv) <= np.float32(c))
 
 
+def saturating_case(seed, P, D, V, K, n_sat=6):
+    """Exact logits with a saturating cap: h[p] is one-hot on column p % D, so
+    U[p, v] = W_lm[v, p % D] exactly.  Per column, n_sat tokens get logits 20, 20.5,
+    ... (tanh rounds every one of them to exactly 1 in fp32) with larger ids
+    holding larger raw logits, then K - n_sat tokens sit well apart in (0.3, 0.5),
+    and every other token below 0.2: the kept set is clear, but the saturated
+    entries tie and must come out in id order, not in raw-logit order."""
+    rng = _rng(seed)
+    Wf = rng.uniform(-0.2, 0.2, size=(V, D)).astype(np.float32)
+    for c in range(min(P, D)):
+        ids = np.sort(rng.choice(V, size=K, replace=False))
+        sat, mid = ids[:n_sat], rng.permutation(ids[n_sat:])
+        Wf[sat, c] = 20.0 + 0.5 * np.arange(n_sat)
+        Wf[mid, c] = 0.3 + 0.0125 * np.arange(K - n_sat)
+    h = np.zeros((P, D), np.float32)
+    h[np.arange(P), np.arange(P) % D] = 1.0
+    return W.f32_to_bf16_bits(h), W.f32_to_bf16_bits(Wf)
+
+
+@pytest.mark.parametrize("P,D,V,K", [
+    (8, 256, 5000, 16),      # the streaming head: merge of the per-CTA lists
+    (140, 256, 5000, 16),    # the tensor-core GEMM for many positions
+    (20, 256, 3000, 100),    # K > 64: the CUDA-core path
+])
+def test_head_saturating_cap_ties_break_to_lower_id(orc, df2, P, D, V, K):
+    h, Wlm = saturating_case(P + V + K, P, D, V, K)
+    ids, vals, _ = df2.unary_topk(bf_dev(h), bf_dev(Wlm), K, output_multiplier=1.0, final_logit_softcapping=1.0)
+    torch.cuda.synchronize()
+    oi, ov, om, _ = orc.unary_topk(h, Wlm, K, output_multiplier=1.0, final_logit_softcapping=1.0)
+    assert (ov[:, :6] == 1.0).all() and (om > 1e-3).all()
+    assert np.array_equal(host(ids), oi)
+    assert np.array_equal(host(vals)[:, :6], ov[:, :6])
+    close(host(vals), ov, what="saturating cap vals")
+
+
+def test_draft_head_saturating_cap_ties_break_to_lower_id(orc, df2):
+    R, B, D, V, K, r = 2, 8, 256, 5000, 16, 64
+    h, Wlm = saturating_case(7, R * B, D, V, K)
+    rng = _rng(8)
+    WH, A, Bc = rand_bf16(rng, (r, D), 0.02), rand_bf16(rng, (V, r), 0.3), rand_bf16(rng, (V, r), 0.3)
+    anchors = rng.integers(0, V, R).astype(np.int32)
+    out = df2.draft_head(bf_dev(h), bf_dev(Wlm), K, bf_dev(WH), bf_dev(A), bf_dev(Bc), dev(anchors), B,
+                         output_multiplier=1.0, final_logit_softcapping=1.0)
+    torch.cuda.synchronize()
+    oi, ov, om, oG = orc.unary_topk(h, Wlm, K, W_H=WH, output_multiplier=1.0, final_logit_softcapping=1.0)
+    assert np.array_equal(host(out[0]), oi)
+    op, os_, omg, _ = orc.selector_walk(anchors, oi, ov, oG, A, Bc, B)
+    compare_walk(host(out[3]), host(out[4]), op, os_, omg, "capped walk").check("capped walk")
+
+
 def test_head_logit_map_defaults_are_the_identity(df2):
     """m = 1, c = 0 leaves every value bit for bit as the call without the map."""
     rng = _rng(3)
@@ -366,6 +416,14 @@ def test_tiny_conv(orc, df2):
     (136, 264, 8, 3, 8, "bf16"),    # many rows: tensor-core projection, column split not /16
     (80, 512, 16, 4, 16, "bf16"),   # many rows, taps 4
     (72, 40, 9, 2, 4, "f32"),       # many fp32 rows: CUDA-core projection
+    # many bf16 rows: the fused tensor-core prepare (projection, dyn_out and apply in one kernel)
+    (200, 512, 8, 2, 16, "bf16"),   # CTA pairs, ragged last row tile
+    (72, 256, 8, 1, 8, "bf16"),     # one row tile, taps 1
+    (384, 1024, 8, 3, 32, "bf16"),  # taps 3, three row tiles (the last pair's second CTA idle)
+    (640, 512, 8, 2, 4, "bf16"),    # groups narrower than an 8-channel chunk
+    (1032, 256, 8, 2, 16, "bf16"),  # nine row tiles, the last one 8 rows
+    (256, 512, 32, 4, 16, "bf16"),  # blocks of 32, taps 4
+    (96, 256, 16, 3, 16, "bf16"),   # one partial row tile, blocks of 16
 ])
 def test_conv_shapes(orc, df2, P, C, B, taps, g, dt):
     rng = _rng(P * 13 + C + taps * 7 + g)
@@ -381,9 +439,26 @@ def test_conv_shapes(orc, df2, P, C, B, taps, g, dt):
     check_conv(orc, df2, x, z, B, taps, g, Wp, base, f"conv{P}x{C}b{B}t{taps}g{g}{dt}")
 
 
-def test_conv_identity_and_locality_gpu(df2):
+@pytest.mark.parametrize("P,C,B,taps,g", [(200, 512, 8, 2, 16), (1032, 256, 8, 2, 16), (256, 512, 32, 4, 16)])
+def test_conv_prepare_many_rows_is_one_kernel(df2, P, C, B, taps, g):
+    """Many bf16 rows: conv prepare is a single launch (the corrections for the
+    conv it applies never leave the chip)."""
+    rng = _rng(P + C)
+    x = bf_dev(rand_bf16(rng, (P, C)))
+    Wp = bf_dev(rand_bf16(rng, (2 * taps * (C // g), C), 0.05))
+    base = dev((rng.standard_normal((2, taps, C)) * 0.3).astype(np.float32))
+    df2.conv_prepare(x, B, taps, g, Wp, base)
+    torch.cuda.synchronize()
+    before = df2.kernels_launched()
+    df2.conv_prepare(x, B, taps, g, Wp, base)
+    torch.cuda.synchronize()
+    assert df2.kernels_launched() - before == 1
+
+
+@pytest.mark.parametrize("P", [32, 256])   # few rows; many rows (the fused tensor-core prepare)
+def test_conv_identity_and_locality_gpu(df2, P):
     rng = _rng(21)
-    P, C, B, taps, g = 32, 256, 8, 2, 16
+    C, B, taps, g = 256, 8, 2, 16
     x = rand_bf16(rng, (P, C))
     base = np.zeros((2, taps, C), np.float32)
     base[:, 0] = 1
@@ -406,25 +481,6 @@ def test_conv_identity_and_locality_gpu(df2):
 def _sample_rows(P, n, extra=()):
     rows = sorted(set(np.linspace(0, P - 1, n).astype(int).tolist()) | set(int(e) for e in extra))
     return np.asarray(rows)
-
-
-@pytest.mark.parametrize("name,nrows", [("batch1", 8), ("batched", 12), ("stress", 24)])
-def test_full_size_head(orc, df2, name, nrows):
-    w = W.BY_NAME[name]
-    inp = W.head_inputs(w)
-    gi, gv, gG = run_head(df2, inp["h"], inp["W_lm"], w.K, inp["W_H"])
-    spiked = inp["spiked_rows"][:8]
-    rows = _sample_rows(w.P, nrows, spiked)
-    oi, ov, om, oG = orc.unary_topk(np.ascontiguousarray(inp["h"][rows]), inp["W_lm"], w.K, W_H=inp["W_H"])
-    rep = compare_topk(gi[rows], gv[rows], oi, ov, om, name)
-    rep.check(name)
-    compare_topk_values(gi[rows], gv[rows], oi, ov, name + " vals")
-    close(gG[rows], oG, what=name + " G")
-    # properties over every row: sorted, distinct, in range
-    assert (gi >= 0).all() and (gi < w.V).all()
-    assert (np.diff(gv, axis=1) <= 0).all()
-    srt = np.sort(gi, axis=1)
-    assert (np.diff(srt, axis=1) > 0).all()
 
 
 @pytest.mark.parametrize("name", ["batch1", "batched", "stress"])

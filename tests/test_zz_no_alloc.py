@@ -65,14 +65,23 @@ def _no_alloc(lib, h, W, K, WH, stream):
     return ids, vals, G, status
 
 
+STREAM, GEMM, CUDA_CORE = 0, 1, 2   # DF2_HEAD_PATH_*
+
+
 @pytest.mark.parametrize("shape", [
-    [(8, 4096, 151936, 16, 256), (8, 4096, 151936, 16, 256)],   # batch-1 head, twice
-    [(8, 512, 30011, 16, 64), (24, 256, 5000, 64, 32)],         # different shapes back to back
-    [(40, 256, 3000, 8, 32), (5, 1024, 7777, 32, 128)],         # CUDA-core path, then tensor-core path
+    # (P, D, V, K, r, head path)
+    [(8, 4096, 151936, 16, 256, STREAM), (8, 4096, 151936, 16, 256, STREAM)],   # batch-1 head, twice
+    [(8, 512, 30011, 16, 64, STREAM), (24, 256, 5000, 64, 32, GEMM)],           # different shapes back to back
+    [(40, 256, 3000, 8, 32, GEMM), (5, 1024, 7777, 32, 128, STREAM)],           # GEMM path, then streaming
+    [(20, 256, 3000, 100, 32, CUDA_CORE), (9, 512, 20011, 64, 64, STREAM)],     # CUDA-core path (K > 64)
+    # the GEMM path keeps a per-position threshold in the scratch: a larger call,
+    # then a smaller one that must not see the first call's thresholds
+    [(256, 512, 40000, 16, 64, GEMM), (64, 512, 9000, 16, 64, GEMM)],
 ])
 def test_no_alloc_matches_workspace_entry_point(lib, shape):
     stream = ct.c_void_p(torch.cuda.current_stream().cuda_stream)
-    for i, (P, D, V, K, r) in enumerate(shape):
+    for i, (P, D, V, K, r, path) in enumerate(shape):
+        assert lib.dflash2_unary_topk_path(P, D, V, K) == path
         h, W, WH = _inputs(100 * i + P, P, D, V, r)
         ref_ids, ref_vals, ref_G = _with_workspace(lib, h, W, K, WH, stream)
         ids, vals, G, status = _no_alloc(lib, h, W, K, WH, stream)

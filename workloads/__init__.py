@@ -160,12 +160,12 @@ def head_inputs(w: Workload, selector_std: float | None = None, rows: int | None
     assert not w.conv_only
     s = w.seed
     P = w.P if rows is None else rows
-    cb_std = w.w_std if selector_std is None else selector_std
+    A, Bc = selector_codebooks(w, selector_std)
     out = {
         "W_lm": normal_bf16(s, "W_lm", (w.V, w.D), w.w_std),
         "W_H": normal_bf16(s, "W_H", (w.r, w.D), w.w_std),
-        "A": normal_bf16(s, "A", (w.V, w.r), cb_std),
-        "Bc": normal_bf16(s, "B", (w.V, w.r), cb_std),
+        "A": A,
+        "Bc": Bc,
         "anchors": uniform_ids(s, "anchors", w.R, w.V),
         "pred": uniform_ids(s, "pred", w.P, w.V),
     }
@@ -180,6 +180,13 @@ def head_inputs(w: Workload, selector_std: float | None = None, rows: int | None
         out["h"] = out["h"][:rows]
         out["pred"] = out["pred"][:rows]
     return out
+
+
+def selector_codebooks(w: Workload, selector_std: float | None = None):
+    """The predecessor and successor codebooks A, Bc [V, r] (bf16 bits), at the
+    workload's weight scale or at ``selector_std`` (the "strong selector")."""
+    cb_std = w.w_std if selector_std is None else selector_std
+    return (normal_bf16(w.seed, "A", (w.V, w.r), cb_std), normal_bf16(w.seed, "B", (w.V, w.r), cb_std))
 
 
 def conv_inputs(w: Workload) -> dict:
