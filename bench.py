@@ -1,6 +1,7 @@
 """Benchmark of the DFlash2 draft-block head on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                    [--no-records] [--no-cpu-baseline]
 
 One step = one pass of the whole head over one draft batch of the workload:
 conv_prepare -> conv_finish (one sublayer's conv pair) -> draft_head (unary
@@ -12,10 +13,14 @@ step streams the whole LM head (1.25 GB for the default batch-1 workload, larger
 than the 129 MB L2), so no separate L2 flush is needed for the default workload;
 other workloads flush L2 with a 256 MB write between steps.
 
-Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
-replica on its own GPU (the head shards by requests with no exchange: "weak"
-scaling); the time is the max over ranks.  --impl reference times the CPU oracle
-on the host cores on the same workload instead.
+Prints one JSON line (rank 0).  The headline is the batch-1 workload; a default run
+then appends a "workloads" object with one record each for the batched, stress and
+training-packed conv workloads (timing, roofline, cpu baseline, parity, e2e,
+clocks).  Each workload's "parity" block compares the timed step's outputs with the
+oracle on the first requests, the same slice its cpu baseline times.  Under
+torchrun each rank runs an independent replica on its own GPU (the head shards by
+requests with no exchange: "weak" scaling); the time is the max over ranks.
+--impl reference times the CPU oracle on the host cores on the same workload instead.
 """
 from __future__ import annotations
 
@@ -308,10 +313,10 @@ class ClockSampler:
 class Step:
     """Device-resident inputs/outputs of one workload and the five calls."""
 
-    def __init__(self, w, device, torch, df2):
+    def __init__(self, w, device, torch, df2, inp=None, conv=None):
         self.w, self.torch, self.df2 = w, torch, df2
-        inp = W.head_inputs(w)
-        conv = W.conv_inputs(w)
+        inp = W.head_inputs(w) if inp is None else inp
+        conv = W.conv_inputs(w) if conv is None else conv
 
         def bf(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
@@ -428,6 +433,20 @@ class Step:
     def outputs(self):
         return [self.ids, self.vals, self.path, self.pscore, self.scores, self.y, self.y2, self.dyn]
 
+    def host_outputs(self):
+        """The step's outputs on the host, named as the parity comparators expect
+        (bf16 tensors as uint16 bit patterns)."""
+        torch = self.torch
+        torch.cuda.synchronize()
+
+        def h(t):
+            if t.dtype == torch.bfloat16:
+                return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            return t.cpu().numpy()
+        return {"ids": h(self.ids), "vals": h(self.vals), "G": h(self.Gt), "path": h(self.path),
+                "pscore": h(self.pscore), "scores": h(self.scores), "y": h(self.y), "dyn": h(self.dyn),
+                "y2": h(self.y2)}
+
 
 def count_launches(step, torch, df2):
     """Kernels one step launches, from the library's own launch counter."""
@@ -438,18 +457,49 @@ def count_launches(step, torch, df2):
     return df2.kernels_launched() - before
 
 
-def gpu_arm(args, w, rank, world, torch):
-    import dflash2_draft_block_gb300 as df2
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 
-    step = Step(w, device, torch, df2)
-    for _ in range(args.warmup):
+
+def fractions(roof, peaks_src):
+    """frac against the measured peak (the roofline denominator) and against the
+    nominal figure (8 TB/s HBM, 2.25 PFLOP/s dense bf16)."""
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = peaks_src
+    nominal = NOMINAL["hbm_gbs"] if roof["bound"] == "hbm" else NOMINAL["bf16_tflops"]
+    roof["frac_of_nominal"] = roof["achieved"] / nominal
+    roof["nominal_peak"] = nominal
+    return roof
+
+
+def soak(fn, torch, seconds, chunk):
+    """Runs fn back to back for about `seconds` (untimed), so that the clock samples
+    taken over it and the timed region that follows see the GPU under this load."""
+    t_end = time.perf_counter() + seconds
+    n = 0
+    while time.perf_counter() < t_end:
+        for _ in range(chunk):
+            fn()
+        torch.cuda.synchronize()
+        n += chunk
+    return n
+
+
+def with_clock_product(clocks, ms):
+    if clocks.get("sm_mhz"):
+        clocks["ms_per_step_x_sm_mhz"] = ms * clocks["sm_mhz"]
+    clocks["window"] = ("nvidia-smi every 100 ms over a 1 s soak of the same step directly before the "
+                        "timed region, and over the timed region")
+    return clocks
+
+
+def gpu_arm(args, w, rank, world, torch, df2, dist, device, inp=None, conv=None, steps=None, warmup=None):
+    """The draft-block step of a head workload on this rank's GPU; returns the JSON
+    record (rank 0) and the step (for the parity comparison)."""
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
+    local = device.index
+    step = Step(w, device, torch, df2, inp, conv)
+    for _ in range(warmup):
         step.run()
         if step.flush is not None:
             step.flush.zero_()
@@ -457,25 +507,36 @@ def gpu_arm(args, w, rank, world, torch):
     n_launch = count_launches(step, torch, df2)
     graphs = step.capture()
     if graphs is not None:
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             graphs[0].replay()
             graphs[1].replay()
         torch.cuda.synchronize()
+
+    def one_step():
+        if graphs is not None:
+            graphs[0].replay()
+            graphs[1].replay()
+        else:
+            step.run()
+        if step.flush is not None:
+            step.flush.zero_()
 
     # ---- device-resident timing (W warm-up done above).  Each step replays the
     # conv graph and the draft-head graph (or, where capture is not possible, makes
     # the calls).  Only the head call is bracketed by events: every event between
     # kernels drains the launch pipeline, so more of them would inflate the step.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     flush_ms = 0.0
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launched0 = df2.kernels_launched()
+    chunk = 64 if w.P <= 32 else 8
     with ClockSampler(local) as clk:
+        soak(one_step, torch, 1.0, chunk)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        launched0 = df2.kernels_launched()
         t0.record()
-        for s in range(args.steps):
+        for s in range(steps):
             if graphs is not None:
                 graphs[0].replay()
                 evs[s][0].record()
@@ -489,12 +550,12 @@ def gpu_arm(args, w, rank, world, torch):
         torch.cuda.synchronize()
     # a graph replay launches the captured kernels without passing through the
     # library, whose counter therefore counts them per step
-    timed_launches = (n_launch * args.steps if graphs is not None
+    timed_launches = (n_launch * steps if graphs is not None
                       else df2.kernels_launched() - launched0)
     if dist is not None:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    head_us_live = sum(evs[s][0].elapsed_time(evs[s][1]) for s in range(args.steps)) / args.steps * 1e3
+    head_us_live = sum(evs[s][0].elapsed_time(evs[s][1]) for s in range(steps)) / steps * 1e3
     if step.flush is not None:
         # the flush runs between timed steps; its time is subtracted
         fe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -503,9 +564,9 @@ def gpu_arm(args, w, rank, world, torch):
             step.flush.zero_()
         fe[1].record()
         torch.cuda.synchronize()
-        flush_ms = fe[0].elapsed_time(fe[1]) / 5 * args.steps
-    step_ms = slowest_rank_ms((total_ms - flush_ms) / args.steps, dist, device)
-    per_call_us = time_per_call(step, torch, min(args.steps, 50))
+        flush_ms = fe[0].elapsed_time(fe[1]) / 5 * steps
+    step_ms = slowest_rank_ms((total_ms - flush_ms) / steps, dist, device)
+    per_call_us = time_per_call(step, torch, min(steps, 50))
     next_us, next_how = time_next_rows(step, torch, df2)
 
     # ---- end to end through the public API with host buffers.  Every step copies its
@@ -521,7 +582,7 @@ def gpu_arm(args, w, rank, world, torch):
                   for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pinned_in.values())
     d2h = sum(sets[0][k].numel() * sets[0][k].element_size() for k in out_names)
-    main = torch.cuda.current_stream()
+    main_s = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -537,11 +598,11 @@ def gpu_arm(args, w, rank, world, torch):
 
     def compute(i):
         s = i % 2
-        main.wait_event(ev_in[s])
-        main.wait_event(ev_out[s])  # step i-2's results in set s have been read out
+        main_s.wait_event(ev_in[s])
+        main_s.wait_event(ev_out[s])  # step i-2's results in set s have been read out
         step.use(sets[s])
         step.run()
-        ev_done[s].record(main)
+        ev_done[s].record(main_s)
         if step.flush is not None:
             step.flush.zero_()
 
@@ -555,8 +616,8 @@ def gpu_arm(args, w, rank, world, torch):
 
     def e2e_steps(n):
         for s in range(2):
-            ev_done[s].record(main)
-            ev_out[s].record(main)
+            ev_done[s].record(main_s)
+            ev_out[s].record(main_s)
         copy_in(0)
         for i in range(n):
             if i + 1 < n:
@@ -564,21 +625,21 @@ def gpu_arm(args, w, rank, world, torch):
             compute(i)
             copy_out(i)
         for s in range(2):
-            main.wait_event(ev_out[s])
+            main_s.wait_event(ev_out[s])
 
-    e2e_steps(max(1, args.warmup))
+    e2e_steps(max(1, warmup))
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    e2e_steps(args.steps)
+    e2e_steps(steps)
     e1.record()
     torch.cuda.synchronize()
     step.use(sets[0])
-    e2e_ms = slowest_rank_ms((e0.elapsed_time(e1) - flush_ms) / args.steps, dist, device)
+    e2e_ms = slowest_rank_ms((e0.elapsed_time(e1) - flush_ms) / steps, dist, device)
 
-    clocks = clk.summary()
+    clocks = with_clock_product(clk.summary(), step_ms)
     out = None
     if rank == 0:
         peaks, src = load_peaks()
@@ -600,8 +661,11 @@ def gpu_arm(args, w, rank, world, torch):
             roof = {"kernel": "dflash2_draft_head call: gemm_wide_kernel (top-K, G) + " + tail,
                     "bound": "tensor", "achieved": flops / (head_us * 1e-6) / 1e12, "peak": pk,
                     "unit": "TFLOP/s", "algorithmic_flops": flops}
-        roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["peak_source"] = src
+        fractions(roof, src)
+        if w.P <= 32:
+            roof["target"] = {"rule": ">= 0.70 of the HBM roofline for the batch-1 LM head + top-K + walk, "
+                                      "taken at the nominal 8 TB/s", "frac": roof["frac_of_nominal"],
+                              "met": roof["frac_of_nominal"] >= 0.70}
         roof["traffic"] = traffic
         roof["traffic_source"] = traffic_src
         roof["traffic_note"] = "DRAM bytes per launch of the head kernel (ncu); the other kernels of the call move < 1%"
@@ -610,8 +674,8 @@ def gpu_arm(args, w, rank, world, torch):
             "value": job_throughput(w.P, world, step_ms),
             "unit": "positions/s",
             "n_gpus": world,
-            "steps": args.steps,
-            "warmup": args.warmup,
+            "steps": steps,
+            "warmup": warmup,
             "ms_per_step": step_ms,
             "higher_is_better": True,
             "scaling": "weak",
@@ -652,9 +716,7 @@ def gpu_arm(args, w, rank, world, torch):
             "kernels_per_step": n_launch,
             "clocks": clocks,
         }
-    if dist is not None:
-        dist.destroy_process_group()
-    return out
+    return out, step
 
 
 # ------------------------------------------------------------- conv arm --
@@ -666,61 +728,73 @@ def conv_config(w):
             "l2": "inputs larger than L2: x and z are 168 MB each; W_proj (13 MB) stays resident like any weight"}
 
 
-def conv_arm(args, w, rank, world, torch):
+class ConvStep:
+    """The training-packed conv workload's device buffers and its step."""
+
+    def __init__(self, w, device, torch, df2, conv):
+        self.w, self.torch = w, torch
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+        self.x, self.z = bf(conv["x"]), bf(conv["z"])
+        self.W_proj, self.base = bf(conv["W_proj"]), torch.from_numpy(conv["base"]).to(device)
+        self.y, self.y2 = torch.empty_like(self.x), torch.empty_like(self.z)
+        self.dyn = torch.empty((w.P, w.taps, w.G), dtype=torch.float32, device=device)
+        self.ws = torch.empty(max(1, df2.conv_prepare_workspace_size(w.P, w.C, w.taps, w.g)), dtype=torch.uint8,
+                              device=device)
+        self.df2 = df2
+
+    def run(self, ev=None):
+        w, df2 = self.w, self.df2
+        if ev is not None:
+            ev[0].record()
+        df2.conv_prepare(self.x, w.B, w.taps, w.g, self.W_proj, self.base, workspace=self.ws,
+                         out=(self.y, self.dyn))
+        if ev is not None:
+            ev[1].record()
+        df2.conv_finish(self.z, w.B, w.taps, w.g, self.dyn, self.base, out=self.y2)
+        if ev is not None:
+            ev[2].record()
+
+    def host_outputs(self):
+        torch = self.torch
+        torch.cuda.synchronize()
+        bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        return {"y": bits(self.y), "dyn": self.dyn.cpu().numpy(), "y2": bits(self.y2)}
+
+
+def conv_arm(args, w, rank, world, torch, df2, dist, device, conv, steps=None, warmup=None):
     """The training-packed conv workload: one step is conv_prepare then conv_finish
     over all P rows.  Events around each call give the live per-call durations: the
     prepare call against the tensor peak (its projection is the contraction), the
     finish call against HBM."""
-    import dflash2_draft_block_gb300 as df2
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-    c = W.conv_inputs(w)
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
-    x, z = bf(c["x"]), bf(c["z"])
-    W_proj, base = bf(c["W_proj"]), torch.from_numpy(c["base"]).to(device)
-    y, y2 = torch.empty_like(x), torch.empty_like(z)
-    dyn = torch.empty((w.P, w.taps, w.G), dtype=torch.float32, device=device)
-    ws = torch.empty(max(1, df2.conv_prepare_workspace_size(w.P, w.C, w.taps, w.g)), dtype=torch.uint8,
-                     device=device)
-
-    def run(ev=None):
-        if ev is not None:
-            ev[0].record()
-        df2.conv_prepare(x, w.B, w.taps, w.g, W_proj, base, workspace=ws, out=(y, dyn))
-        if ev is not None:
-            ev[1].record()
-        df2.conv_finish(z, w.B, w.taps, w.g, dyn, base, out=y2)
-        if ev is not None:
-            ev[2].record()
-
-    for _ in range(args.warmup):
-        run()
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
+    local = device.index
+    cs = ConvStep(w, device, torch, df2, conv)
+    x, z, y, y2, dyn = cs.x, cs.z, cs.y, cs.y2, cs.dyn
+    for _ in range(warmup):
+        cs.run()
     torch.cuda.synchronize()
     before = df2.kernels_launched()
-    run()
+    cs.run()
     torch.cuda.synchronize()
     n_launch = df2.kernels_launched() - before
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launched0 = df2.kernels_launched()
     with ClockSampler(local) as clk:
+        soak(cs.run, torch, 1.0, 8)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        launched0 = df2.kernels_launched()
         t0.record()
-        for s in range(args.steps):
-            run(evs[s])
+        for s in range(steps):
+            cs.run(evs[s])
         t1.record()
         torch.cuda.synchronize()
     timed_launches = df2.kernels_launched() - launched0
-    step_ms = slowest_rank_ms(t0.elapsed_time(t1) / args.steps, dist, device)
-    prep_us = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps * 1e3
-    fin_us = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps * 1e3
+    step_ms = slowest_rank_ms(t0.elapsed_time(t1) / steps, dist, device)
+    prep_us = sum(e[0].elapsed_time(e[1]) for e in evs) / steps * 1e3
+    fin_us = sum(e[1].elapsed_time(e[2]) for e in evs) / steps * 1e3
 
     # end to end: x and z in from pinned host memory, y, dyn_out and the finish output back
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype).pin_memory()
@@ -733,23 +807,23 @@ def conv_arm(args, w, rank, world, torch):
     def e2e_step():
         x.copy_(hx, non_blocking=True)
         z.copy_(hz, non_blocking=True)
-        run()
+        cs.run()
         for o, ho in zip(outs, houts):
             ho.copy_(o, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
+    for _ in range(max(1, warmup)):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = slowest_rank_ms(e0.elapsed_time(e1) / args.steps, dist, device)
+    e2e_ms = slowest_rank_ms(e0.elapsed_time(e1) / steps, dist, device)
     h2d = (x.numel() + z.numel()) * 2
     d2h = sum(o.numel() * o.element_size() for o in outs)
-    clocks = clk.summary()
+    clocks = with_clock_product(clk.summary(), step_ms)
     out = None
     if rank == 0:
         peaks, src = load_peaks()
@@ -758,19 +832,19 @@ def conv_arm(args, w, rank, world, torch):
         roof = {"kernel": "dflash2_conv_prepare call: the projection GEMM (gemm_wide_kernel, store epilogue) "
                           "+ the conv apply", "bound": "tensor",
                 "achieved": flops / (prep_us * 1e-6) / 1e12, "peak": pk, "unit": "TFLOP/s",
-                "algorithmic_flops": flops, "peak_source": src,
+                "algorithmic_flops": flops,
                 "traffic_note": "the call's time includes its apply kernel, so this understates the GEMM's rate; "
                                 "traffic is the projection GEMM's DRAM bytes per launch (ncu)"}
+        fractions(roof, src)
         roof["traffic"], roof["traffic_source"] = head_traffic(w.name)
-        roof["frac"] = roof["achieved"] / roof["peak"]
         fb = conv_bytes(w, "finish")
         roof_fin = {"kernel": "dflash2_conv_finish call: conv_apply_async_kernel", "bound": "hbm",
                     "achieved": fb / (fin_us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "algorithmic_bytes": fb, "peak_source": src}
-        roof_fin["frac"] = roof_fin["achieved"] / roof_fin["peak"]
+                    "algorithmic_bytes": fb}
+        fractions(roof_fin, src)
         out = {
             "metric": METRIC, "value": job_throughput(w.P, world, step_ms), "unit": "positions/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; shapes and scales of the workload, no dataset or checkpoint)",
             "config": conv_config(w),
@@ -783,86 +857,161 @@ def conv_arm(args, w, rank, world, torch):
             "gpu_launches": timed_launches, "kernels_per_step": n_launch, "execution": "eager calls",
             "clocks": clocks,
         }
-    if dist is not None:
-        dist.destroy_process_group()
-    return out
+    return out, cs
 
 
 # ------------------------------------------------------------ oracle arm --
 
-def oracle_step(orc, w, inp, conv):
-    """The whole head on the CPU oracle for one draft batch (all P rows)."""
-    y, dyn = orc.conv_prepare(conv["x"], w.B, w.taps, w.g, conv["W_proj"], conv["base"])
-    orc.conv_finish(conv["z"], w.B, w.taps, w.g, dyn, conv["base"])
-    ids, vals, _, G = orc.unary_topk(inp["h"], inp["W_lm"], w.K, W_H=inp["W_H"])
-    orc.selector_walk(inp["anchors"], ids, vals, G, inp["A"], inp["Bc"], w.B)
-    orc.pair_scores(inp["pred"], ids, vals, G, inp["A"], inp["Bc"])
-
-
-def oracle_sample(w):
-    """A bounded slice of the workload for the CPU oracle: the first requests, so one
-    oracle step costs at most ~8 LM-head rows of work."""
-    rows_budget = 8
-    R = max(1, min(w.R, rows_budget // w.B if w.B <= rows_budget else 1))
-    return w.scaled(R=R), R
-
-
-def cpu_arm_conv(w, steps, warmup):
-    """The oracle's conv pair on a bounded slice of the conv workload: 16 anchor
-    blocks per step."""
-    import oracle
-    orc = oracle.default()
-    nb = min(w.R, 16)
-    ws = w.scaled(R=nb)
-    conv = W.conv_inputs(ws)
-
-    def step():
-        _, dyn = orc.conv_prepare(conv["x"], ws.B, ws.taps, ws.g, conv["W_proj"], conv["base"])
-        orc.conv_finish(conv["z"], ws.B, ws.taps, ws.g, dyn, conv["base"])
-
-    for _ in range(warmup):
-        step()
-    t = time.perf_counter()
-    for _ in range(steps):
-        step()
-    dt = (time.perf_counter() - t) / max(1, steps)
-    sample = (f"{nb} of {w.R} anchor blocks ({ws.P} positions) per step: conv prepare (projection "
-              f"{w.C} -> {2 * w.taps * w.G} in fp64) and conv finish on them")
-    return ws.P / dt, orc.num_threads(), sample, dt
-
-
-def cpu_arm(w, steps, warmup):
+def oracle_requests(w):
+    """Requests (anchor blocks for the conv workload) in the oracle's bounded
+    sample: the first ones, about 8 LM-head rows of work per step, or 16 conv blocks."""
     if w.conv_only:
-        return cpu_arm_conv(w, steps, warmup)
+        return min(w.R, 16)
+    rows_budget = 8
+    return max(1, min(w.R, rows_budget // w.B if w.B <= rows_budget else 1))
+
+
+def first_requests(w, inp, conv, n):
+    """The workload's inputs cut to its first n requests (rows 0 .. n*B)."""
+    rows = n * w.B
+    ws = w.scaled(R=n)
+    hi = None
+    if inp is not None:
+        hi = dict(inp)
+        hi["h"] = np.ascontiguousarray(inp["h"][:rows])
+        hi["pred"] = np.ascontiguousarray(inp["pred"][:rows])
+        hi["anchors"] = np.ascontiguousarray(inp["anchors"][:n])
+    ci = dict(conv)
+    ci["x"] = np.ascontiguousarray(conv["x"][:rows])
+    ci["z"] = np.ascontiguousarray(conv["z"][:rows])
+    return ws, hi, ci
+
+
+def oracle_step(orc, w, inp, conv):
+    """The whole step on the CPU oracle for one draft batch (all P rows of w):
+    conv prepare and finish, unary top-K with G, the walk and the teacher-forced
+    scores.  Returns the outputs by name."""
+    y, dyn = orc.conv_prepare(conv["x"], w.B, w.taps, w.g, conv["W_proj"], conv["base"])
+    y2 = orc.conv_finish(conv["z"], w.B, w.taps, w.g, dyn, conv["base"])
+    out = {"y": y, "dyn": dyn, "y2": y2}
+    if w.conv_only:
+        return out
+    ids, vals, _, G = orc.unary_topk(inp["h"], inp["W_lm"], w.K, W_H=inp["W_H"])
+    path, pscore, _, _ = orc.selector_walk(inp["anchors"], ids, vals, G, inp["A"], inp["Bc"], w.B)
+    scores, _ = orc.pair_scores(inp["pred"], ids, vals, G, inp["A"], inp["Bc"])
+    out.update(ids=ids, vals=vals, G=G, path=path, pscore=pscore, scores=scores)
+    return out
+
+
+def sample_text(w, n):
+    if w.conv_only:
+        return (f"{n} of {w.R} anchor blocks ({n * w.B} positions) per step: conv prepare (projection "
+                f"{w.C} -> {2 * w.taps * w.G} in fp64) and conv finish on them")
+    return (f"{n} of {w.R} requests ({n * w.B} positions) per step: the full step on them "
+            f"(conv pair, {n * w.B} x {w.V} logits, full-sort top-{w.K}, walk, teacher-forced scores)")
+
+
+def cpu_baseline(w, inp, conv, steps, warmup, one_thread_steps=1):
+    """The oracle, as it stands, timed on the host cores on the workload's first
+    requests: at every OpenMP thread (nproc) and, for one step, at one thread."""
     import oracle
     orc = oracle.default()
-    ws, R = oracle_sample(w)
-    inp = W.head_inputs(ws)
-    conv = W.conv_inputs(ws)
+    n = oracle_requests(w)
+    ws, hi, ci = first_requests(w, inp, conv, n)
     for _ in range(warmup):
-        oracle_step(orc, ws, inp, conv)
+        oracle_step(orc, ws, hi, ci)
     t = time.perf_counter()
     for _ in range(steps):
-        oracle_step(orc, ws, inp, conv)
+        oracle_step(orc, ws, hi, ci)
     dt = (time.perf_counter() - t) / max(1, steps)
-    sample = (f"{R} of {w.R} requests ({ws.P} positions) per step: the full head on them "
-              f"(conv pair, {ws.P} x {w.V} logits, full-sort top-{w.K}, walk, pair scores)")
-    return ws.P / dt, orc.num_threads(), sample, dt
+    cores = orc.num_threads()
+    rec = {"value": ws.P / dt, "unit": "positions/s", "cores": cores, "kind": "oracle",
+           "sample": sample_text(w, n), "ms_per_step": dt * 1e3}
+    if one_thread_steps:
+        orc.set_num_threads(1)
+        try:
+            t = time.perf_counter()
+            for _ in range(one_thread_steps):
+                oracle_step(orc, ws, hi, ci)
+            d1 = (time.perf_counter() - t) / one_thread_steps
+        finally:
+            orc.set_num_threads(cores)
+        rec["one_thread"] = {"value": ws.P / d1, "unit": "positions/s", "cores": 1, "ms_per_step": d1 * 1e3,
+                             "steps": one_thread_steps}
+    return rec
+
+
+def parity_block(w, inp, conv, gpu_out):
+    """The timed step's outputs against the oracle on the same first requests the
+    cpu baseline runs: compared / flagged / mismatched positions and every float
+    and bf16 output within the tolerances (tests/parity.py)."""
+    import oracle
+    from parity import compare_chain
+    orc = oracle.default()
+    n = oracle_requests(w)
+    s = compare_chain(orc, w, inp, gpu_out, range(n), conv=conv, check=False)
+    s["sample"] = sample_text(w, n)
+    s["rules"] = ("ids exact outside oracle margins < 1e-3 (flagged); mismatches flagged and <= 0.1% of "
+                  "compared; floats within 2e-3 of max(|ref|, row rms); bf16 within that or one step")
+    return s
+
+
+def reference_arm(args, w):
+    """--impl reference: the CPU oracle timed on the host cores on bounded samples of
+    the workload (the pages hold no runnable implementation of the method)."""
+    inp = None if w.conv_only else W.head_inputs(w)
+    conv = W.conv_inputs(w)
+    cpu = cpu_baseline(w, inp, conv, args.steps, max(0, args.warmup), one_thread_steps=0)
+    value = cpu["value"]
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": cpu["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": conv_config(w) if w.conv_only else config_of(w),
+            "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# The records that follow the headline in a default run: the other full-size
+# workloads, each with its own timing, roofline, cpu baseline, parity and clocks.
+RECORD_STEPS = {"batched": 200, "stress": 60, "conv": 500, "batch1": 2000}
+
+
+def run_workload(args, w, rank, world, torch, df2, dist, device, steps, warmup, cpu_ok):
+    inp = None if w.conv_only else W.head_inputs(w)
+    conv = W.conv_inputs(w)
+    cpu = cpu_baseline(w, inp, conv, steps=2, warmup=0) if cpu_ok else None
+    if w.conv_only:
+        out, st = conv_arm(args, w, rank, world, torch, df2, dist, device, conv, steps, warmup)
+    else:
+        out, st = gpu_arm(args, w, rank, world, torch, df2, dist, device, inp, conv, steps, warmup)
+    if rank == 0:
+        out["cpu_baseline"] = cpu
+        if cpu_ok:
+            out["parity"] = parity_block(w, inp, conv, st.host_outputs())
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    # default: 2000 device steps (about half a second timed, several clock samples);
-    # 5 steps for the reference arm, whose every step is a bounded CPU sample
+    # default: 2000 device steps for the headline (about half a second timed); 5
+    # steps for the reference arm, whose every step is a bounded CPU sample
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="batch1", choices=[c.name for c in W.CONFIGS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-records", action="store_true",
+                    help="only the headline workload (by default batch1 is followed by batched, stress, conv)")
     args = ap.parse_args()
+    steps_given = args.steps is not None
     if args.steps is None:
-        args.steps = 5 if args.impl == "reference" else 2000
+        args.steps = 5 if args.impl == "reference" else RECORD_STEPS.get(args.workload, 200)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     w = W.BY_NAME[args.workload]
@@ -870,29 +1019,34 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        value, cores, sample, dt = cpu_arm(w, args.steps, max(0, args.warmup))
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": conv_config(w) if w.conv_only else config_of(w),
-                "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores,
-                                 "kind": "oracle", "sample": sample},
-                "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
+        print(json.dumps(reference_arm(args, w)), flush=True)
         return
 
-    # the oracle runs before the first CUDA call (its threads, not a forked pool)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        value, cores, sample, dt = cpu_arm(w, steps=2, warmup=0)
-        cpu = {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
-               "sample": sample}
     import torch
-    out = (conv_arm if w.conv_only else gpu_arm)(args, w, rank, world, torch)
+    import dflash2_draft_block_gb300 as df2
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    cpu_ok = rank == 0 and world == 1 and not args.no_cpu_baseline
+    out = run_workload(args, w, rank, world, torch, df2, dist, device, args.steps, args.warmup, cpu_ok)
+    records = [] if (args.no_records or w.name != "batch1") else ["batched", "stress", "conv"]
+    if records and rank == 0:
+        out["workloads"] = {}
+    for name in records:
+        wr = W.BY_NAME[name]
+        steps = args.steps if steps_given else RECORD_STEPS[name]
+        rec = run_workload(args, wr, rank, world, torch, df2, dist, device, steps, args.warmup, cpu_ok)
+        if rank == 0:
+            for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data"):
+                rec.pop(k, None)
+            out["workloads"][name] = rec
+    if dist is not None:
+        dist.destroy_process_group()
     if rank == 0:
-        out["cpu_baseline"] = cpu
         print(json.dumps(out), flush=True)
 
 
