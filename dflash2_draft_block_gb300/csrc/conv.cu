@@ -14,6 +14,7 @@
 // eight loads in flight.  The base kernel for the thread's channels is loaded once.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace df2 {
 
@@ -288,6 +289,145 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
     }
 }
 
+// Pipelined apply for many rows.  An item is one anchor block times one strip of
+// nt 16-byte channel chunks (a chunk inside one group).  Persistent CTAs take items
+// blockIdx.x, + gridDim.x, ...; thread 0 fetches an item's B rows of x (and of the
+// residual) and the strip's corrections of every row and tap with 1-D bulk copies,
+// a few large copies per item that complete on the buffer's mbarrier, into one of
+// two shared buffers, while the CTA computes the item in the other.  The
+// arithmetic is conv_apply_async_kernel's.  Every wait is bounded: on a timeout the
+// CTA stops (all threads together) and waits, again bounded, for the copies it
+// still has in flight.
+struct BulkPlan {
+    int nt = 0;         // threads per CTA (chunks per strip)
+    int strips = 0;
+    uint32_t buf = 0;   // bytes per buffer
+    uint32_t smem = 0;  // two buffers and their barriers
+};
+
+template <typename T>
+BulkPlan bulk_plan(int C, int B, int taps, int g, int G, int64_t dyn_ld, bool res) {
+    BulkPlan pl;
+    constexpr int N = Vec<T>::N;
+    const int chunks = C / N;
+    if (taps > 4 || g % N != 0 || G % 4 != 0 || dyn_ld % 4 != 0) return pl;
+    for (int nt = 256; nt >= 64; nt -= 32) {
+        if (chunks % nt != 0) continue;
+        const int ngrp = nt * N / g;
+        if (ngrp % 4 != 0) continue;
+        const uint32_t row = uint32_t(nt) * 16;
+        const uint32_t buf = (uint32_t(B) * row * (res ? 2u : 1u) + uint32_t(B) * taps * ngrp * 4 + 127) / 128 * 128;
+        if (2 * buf + 64 > 112 * 1024) continue;  // at least two CTAs per SM
+        pl.nt = nt;
+        pl.strips = chunks / nt;
+        pl.buf = buf;
+        pl.smem = 2 * buf + 64;
+        return pl;
+    }
+    return pl;
+}
+
+template <typename T, int TAPS, bool RES>
+__global__ void __launch_bounds__(256)
+conv_apply_bulk_kernel(const T* __restrict__ x, int64_t n_items, int C, int B, int g, int G, int strips,
+                       uint32_t buf_bytes, const float* __restrict__ base, const float* __restrict__ dyn,
+                       int64_t dyn_ld, const T* __restrict__ res, T* __restrict__ y) {
+    constexpr int N = Vec<T>::N;
+    using Raw = typename Vec<T>::Raw;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nt = blockDim.x, tid = threadIdx.x;
+    const int ngrp = nt * N / g;
+    const uint32_t row = uint32_t(nt) * 16;
+    const uint32_t xbytes = uint32_t(B) * row;
+    const uint32_t rbytes = RES ? xbytes : 0u;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * size_t(buf_bytes));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2);
+    if (tid == 0) {
+        tc::mbar_init(&bars[0], 1);
+        tc::mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    const uint64_t pol = tc::l2_policy_evict_first();  // every byte is read once
+    auto issue = [&](int64_t item, int b) {
+        const int64_t nb = item / strips;
+        const int c0 = int(item - nb * strips) * nt * N;
+        const int grp0 = c0 / g;
+        uint8_t* buf = smem + size_t(b) * buf_bytes;
+        tc::mbar_arrive_expect_tx(&bars[b], xbytes + rbytes + uint32_t(B) * TAPS * ngrp * 4);
+        for (int t = 0; t < B; ++t) {
+            const int64_t p = nb * B + t;
+            tc::bulk_load(buf + size_t(t) * row, x + p * C + c0, row, &bars[b], pol);
+            if (RES) tc::bulk_load(buf + xbytes + size_t(t) * row, res + p * C + c0, row, &bars[b], pol);
+#pragma unroll
+            for (int j = 0; j < TAPS; ++j)
+                tc::bulk_load(buf + xbytes + rbytes + (size_t(t) * TAPS + j) * ngrp * 4, dyn + p * dyn_ld + j * G + grp0,
+                              uint32_t(ngrp) * 4, &bars[b], pol);
+        }
+    };
+    const int64_t stride = gridDim.x;
+    int64_t item = blockIdx.x;
+    int8_t armed[2] = {-1, -1};  // thread 0: the phase each buffer's copies complete
+    if (tid == 0) {
+        if (item < n_items) { issue(item, 0); armed[0] = 0; }
+        if (item + stride < n_items) { issue(item + stride, 1); armed[1] = 0; }
+    }
+    uint32_t phase[2] = {0u, 0u};
+    for (int b = 0; item < n_items; item += stride, b ^= 1) {
+        const bool got = tc::mbar_wait(&bars[b], phase[b], abort_flag);
+        if (__syncthreads_or(!got)) break;
+        phase[b] ^= 1u;
+        if (tid == 0) armed[b] = -1;
+        const int64_t nb = item / strips;
+        const int c0 = int(item - nb * strips) * nt * N + tid * N;
+        const uint8_t* buf = smem + size_t(b) * buf_bytes;
+        const float* ds = reinterpret_cast<const float*>(buf + xbytes + rbytes);
+        const int gl = (tid * N) / g;
+        float kb[TAPS][N], hist[TAPS][N];
+#pragma unroll
+        for (int j = 0; j < TAPS; ++j)
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                kb[j][e] = __ldg(base + int64_t(j) * C + c0 + e);
+                hist[j][e] = 0.f;
+            }
+        for (int t = 0; t < B; ++t) {
+            const int64_t p = nb * B + t;
+#pragma unroll
+            for (int j = TAPS - 1; j > 0; --j)
+#pragma unroll
+                for (int e = 0; e < N; ++e) hist[j][e] = hist[j - 1][e];
+            Vec<T>::widen(*reinterpret_cast<const Raw*>(buf + size_t(t) * row + size_t(tid) * 16), hist[0]);
+            float acc[N];
+#pragma unroll
+            for (int e = 0; e < N; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int j = 0; j < TAPS; ++j) {
+                if (j > t) break;
+                const float d = ds[(size_t(t) * TAPS + j) * ngrp + gl];
+#pragma unroll
+                for (int e = 0; e < N; ++e) acc[e] = fmaf(kb[j][e] + d, hist[j][e], acc[e]);
+            }
+            if (RES)
+                add_residual_raw<T>(acc, *reinterpret_cast<const Raw*>(buf + xbytes + size_t(t) * row +
+                                                                      size_t(tid) * 16));
+            Vec<T>::store(y + p * C + c0, acc);
+        }
+        __syncthreads();  // every thread is done with buffer b
+        if (tid == 0 && item + 2 * stride < n_items) {
+            issue(item + 2 * stride, b);
+            armed[b] = int8_t(phase[b]);
+        }
+    }
+    if (tid == 0 && *abort_flag) {
+        // a copy that timed out: wait (bounded) for the copies still in flight
+        volatile int never = 0;
+        for (int b = 0; b < 2; ++b)
+            if (armed[b] >= 0) tc::mbar_wait(&bars[b], uint32_t(armed[b]), &never);
+    }
+}
+
 // Few rows: one thread per (row, 16-byte channel chunk); the taps re-read the
 // previous rows (from L1/L2) so every thread has at most `taps` independent loads.
 template <typename T>
@@ -333,6 +473,42 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
             x, P, C, B, taps, g, G, base, dyn, dyn_ld, res, y);
         note_launch();
         return cudaGetLastError();
+    }
+    {
+        const BulkPlan bp = bulk_plan<T>(C, B, taps, g, G, dyn_ld, res != nullptr);
+        if (bp.nt > 0) {
+            const int64_t n_items = nblocks * bp.strips;
+            cudaError_t e = cudaSuccess;
+            int dev = 0, sms = 0, per_sm = 0;
+#define DF2_BULK(TP, R)                                                                                     \
+    do {                                                                                                    \
+        auto kern = conv_apply_bulk_kernel<T, TP, R>;                                                       \
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bp.smem));         \
+        if (e != cudaSuccess) return e;                                                                    \
+        e = cudaGetDevice(&dev);                                                                           \
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);        \
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, bp.nt, bp.smem); \
+        if (e != cudaSuccess) return e;                                                                    \
+        const int64_t grid = n_items < int64_t(sms) * per_sm ? n_items : int64_t(sms) * per_sm;           \
+        kern<<<unsigned(grid > 0 ? grid : 1), bp.nt, bp.smem, stream>>>(x, n_items, C, B, g, G, bp.strips, bp.buf, \
+                                                                     base, dyn, dyn_ld, res, y);            \
+    } while (0)
+#define DF2_BULK_T(TP)                 \
+    do {                               \
+        if (res) DF2_BULK(TP, true);   \
+        else DF2_BULK(TP, false);      \
+    } while (0)
+            switch (taps) {
+                case 1: DF2_BULK_T(1); break;
+                case 2: DF2_BULK_T(2); break;
+                case 3: DF2_BULK_T(3); break;
+                default: DF2_BULK_T(4); break;
+            }
+#undef DF2_BULK_T
+#undef DF2_BULK
+            note_launch();
+            return cudaGetLastError();
+        }
     }
     // threads per CTA: a multiple of 32 that divides the row's chunks, so that no
     // strip of a block runs half empty (5120 channels: 640 chunks, 4 strips of 160)

@@ -17,16 +17,18 @@
 // input-side rows and CTA 1 the output-side ones; each CTA's TMEM receives all the
 // tile's columns for its own 128 rows.
 //
-// Epilogue (warps 2-5, thread = TMEM lane = row): the output-side columns go to
-// dyn_out; the input-side ones to shared memory; then the four warps apply the conv
-// to the tile's rows and its groups' ng*g channels, reading x again (from L2: the
-// units work on consecutive tiles, which share their x rows) and writing y.  The
+// Epilogue (warps 2-9; thread = TMEM lane = row, the two warps of a lane quarter
+// taking alternate column chunks): the output-side columns go to dyn_out, the
+// input-side ones to shared memory; then the eight warps apply the conv to the
+// tile's rows and its groups' ng*g channels, reading x again (from L2: the units
+// work on consecutive tiles, which share their x rows) and writing y.  The
 // input-side corrections never reach HBM and x is read from HBM once.
 //
-// Roles (192 threads): warp 0 lane 0 issues the TMA loads, warp 1 lane 0 (CTA 0 of
-// a pair) the MMAs into one of two TMEM accumulators, warps 2-5 the epilogue.  All
-// waits are bounded; the epilogue warps decide together, at a barrier that ORs
-// their wait results, whether to go on.
+// Roles (320 threads): warp 0 lane 0 issues the TMA loads, warp 1 lane 0 (CTA 0 of
+// a pair) the MMAs into one of two TMEM accumulators, warps 2-9 the epilogue, which
+// releases an accumulator as soon as it has read it, so the apply of one tile runs
+// beside the MMAs of the next two.  All waits are bounded; the epilogue warps
+// decide together, at a barrier that ORs their wait results, whether to go on.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -40,8 +42,8 @@ namespace {
 
 constexpr int CM = 128;   // rows of x per CTA tile (MMA M per CTA, TMEM lanes)
 constexpr int CK = 64;    // reduction elements per box (one 128-byte swizzle row)
-constexpr int kCtcThreads = 192;
-constexpr int kCtcEpi = 128;                 // epilogue threads (warps 2-5)
+constexpr int kCtcThreads = 320;
+constexpr int kCtcEpi = 256;                 // epilogue threads (warps 2-9)
 constexpr uint32_t kXBox = CM * CK * 2;      // 16 KB
 constexpr int kCtcMaxStages = 8;
 constexpr uint32_t kBufCols = 256;           // TMEM columns per accumulator buffer
@@ -77,6 +79,22 @@ __host__ __device__ inline uint32_t ctc_smem(int nstages, int taps, int ng, bool
     return ctc_ds_off(nstages, taps, ng, pair) + uint32_t(CM) * uint32_t(ds_ld) * 4;
 }
 
+// 16-byte load / store with an L2 eviction-priority hint (the apply's last use of
+// x, and outputs no kernel reads soon: they should not push x out of L2 before the
+// other group tiles of its rows and their applies have read it).
+__device__ __forceinline__ uint4 ld16_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st16_hint(void* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -89,16 +107,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // with the last TAPS rows of x in registers (the arithmetic of the standalone
 // apply: acc = fma(base + d, x, acc) over the taps in order).  Consecutive threads
 // take consecutive chunks of the same block, so every load and store of a row is
-// coalesced.
-template <int TAPS>
+// coalesced.  Rows are loaded eight at a time; with PREF the next eight rows (of
+// this item or the thread's next one) are in flight while the current ones are
+// computed, so the epilogue keeps two groups of loads outstanding.
+template <int TAPS, bool PREF>
 __device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, int64_t m0, int rows, int g0,
                                           int etid) {
     const int nch = a.ng * a.g / 8;
     const int c_lo = g0 * a.g;
     const int B = a.B, C = a.C;
-    const int nblk = rows / B;
+    const int total = (rows / B) * nch;
     const bool one_group = (a.g % 8) == 0;  // a chunk's 8 channels share one group
-    for (int item = etid; item < nblk * nch; item += kCtcEpi) {
+    const uint64_t pol = tc::l2_policy_evict_first();
+    auto load_rows = [&](int item, int t0, uint4 (&buf)[8]) {
+        const int blk = item / nch, ch = item - blk * nch;
+        const uint16_t* src = a.x + (m0 + int64_t(blk) * B + t0) * C + c_lo + ch * 8;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (t0 + u < B) buf[u] = ld16_hint(src + int64_t(u) * C, pol);
+    };
+    uint4 cur[8], nxt[8];
+    if (etid < total) load_rows(etid, 0, cur);
+    for (int item = etid; item < total; item += kCtcEpi) {
         const int blk = item / nch, ch = item - blk * nch;
         const int c = c_lo + ch * 8;
         const int r0 = blk * B;
@@ -114,10 +144,11 @@ __device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, 
         }
         const int gl0 = c / a.g - g0;
         for (int t0 = 0; t0 < B; t0 += 8) {
-            uint4 cur[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (t0 + u < B) cur[u] = __ldg(reinterpret_cast<const uint4*>(a.x + (m0 + r0 + t0 + u) * C + c));
+            if (!PREF && t0 > 0) load_rows(item, t0, cur);
+            if (PREF) {
+                if (t0 + 8 < B) load_rows(item, t0 + 8, nxt);
+                else if (item + kCtcEpi < total) load_rows(item + kCtcEpi, 0, nxt);
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int t = t0 + u;
@@ -152,9 +183,14 @@ __device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, 
                 w.y = pack_bf16x2(acc[2], acc[3]);
                 w.z = pack_bf16x2(acc[4], acc[5]);
                 w.w = pack_bf16x2(acc[6], acc[7]);
-                *reinterpret_cast<uint4*>(a.y + (m0 + r) * C + c) = w;
+                st16_hint(a.y + (m0 + r) * C + c, w, pol);
+            }
+            if (PREF) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) cur[u] = nxt[u];
             }
         }
+        if (!PREF && item + kCtcEpi < total) load_rows(item + kCtcEpi, 0, cur);
     }
 }
 
@@ -204,7 +240,7 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], 1);
-            tc::mbar_init(&tempty[b], PAIR ? 8 : 4);  // the epilogue warps of one CTA, or of both
+            tc::mbar_init(&tempty[b], PAIR ? 16 : 8);  // the epilogue warps of one CTA, or of both
         }
         tc::mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -319,17 +355,21 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         }
     } else {
         // ---------------------------------------------------------- epilogue
+        // warps 2-9: a warp reads TMEM lanes 32 (warp % 4) ..; the two warps of a
+        // lane quarter take alternate 16-column chunks of the accumulator
         const int quarter = warp & 3;
+        const int half_grp = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;             // TMEM lane = the tile row of this thread
-        const int etid = (warp - 2) * 32 + lane;       // 0 .. 127 for the apply
+        const int etid = (warp - 2) * 32 + lane;       // 0 .. 255 for the apply
         const int64_t gld = int64_t(TAPS) * a.G;       // dyn_out row length
+        const uint64_t pol_out = tc::l2_policy_evict_first();
         for (int k = 0; k < ntiles; ++k) {
             const int mt = tile_mt(k), g0 = tile_gt(k) * ng;
             const int b = k & 1;
             const uint32_t tph = (k >> 1) & 1;
             const bool got = tc::mbar_wait(&tfull[b], tph, abort_flag);
-            // one decision for the four warps; also orders the previous tile's reads
-            // of ds before this tile's writes
+            // one decision for the epilogue warps; also orders the previous tile's
+            // reads of ds before this tile's writes
             if (tc::named_barrier_or(1, kCtcEpi, !got)) break;
             tc::fence_after_sync();
             const int64_t m0 = int64_t(mt) * CM;
@@ -337,7 +377,7 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             const bool row_ok = m < a.P;
             const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(b) * kBufCols;
             float* drow = ds + size_t(r) * a.ds_ld;
-            for (int c0 = 0; c0 < N; c0 += 16) {
+            for (int c0 = 16 * half_grp; c0 < N; c0 += 32) {
                 float v[16];
                 tc::tmem_ld16(taddr + uint32_t(c0), v);
 #pragma unroll
@@ -348,8 +388,10 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                         for (int e = 0; e < 4; ++e) drow[col + e] = v[4 * q + e];
                     } else if (row_ok) {
                         const int oc = col - half, j = oc / ng, gl = oc - j * ng;
-                        *reinterpret_cast<float4*>(a.dyn_out + m * gld + int64_t(j) * a.G + g0 + gl) =
-                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        st16_hint(a.dyn_out + m * gld + int64_t(j) * a.G + g0 + gl,
+                                  make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                                             __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])),
+                                  pol_out);
                     }
                 }
             }
@@ -364,7 +406,7 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             tc::named_barrier(1, kCtcEpi);  // every row's corrections are staged
             const int64_t left = int64_t(a.P) - m0;
             const int rows = left <= 0 ? 0 : (left < CM ? int(left) : CM);
-            ctc_apply<TAPS>(a, ds, m0, rows, g0, etid);
+            ctc_apply<TAPS, (TAPS <= 2)>(a, ds, m0, rows, g0, etid);
         }
     }
 
@@ -417,7 +459,9 @@ struct CtcPlan {
 // Groups per tile: a divisor of G that is a multiple of 8 (each W_proj box then
 // fills whole 1024-byte swizzle atoms) with 2*taps*ng <= 256 (the MMA's N and one
 // TMEM buffer), chosen by a model of the time: rounds of tiles over the units,
-// times a tile's MMA work plus a fixed cost per tile.
+// times the bytes a CTA stages per tile (its 128 x rows and its W_proj rows).
+// Measured at the training-packed shape, a tile's time follows those L2 bytes,
+// not its MMA work: N = 256 ran 136 us and N = 160 161 us without the apply.
 CtcPlan ctc_plan(int64_t P, int C, int B, int taps, int g, int num_sms) {
     CtcPlan best;
     if (taps < 1 || taps > 4 || g < 1 || C % g != 0 || C % 8 != 0 || B < 1 || CM % B != 0 || P % B != 0)
@@ -441,7 +485,7 @@ CtcPlan ctc_plan(int64_t P, int C, int B, int taps, int g, int num_sms) {
         const int64_t total = int64_t(n_mu) * n_gt;
         const int units = int(total < slots ? total : slots);
         const int64_t rounds = (total + units - 1) / units;
-        const double cost = double(rounds) * (2.0 * taps * ng + 48.0);
+        const double cost = double(rounds) * (CM + double(ctc_b_rows(taps, ng, pair)));
         if (!best.ok || cost < best_cost) {
             best_cost = cost;
             best.ok = true;

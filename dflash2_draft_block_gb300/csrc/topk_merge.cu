@@ -10,8 +10,11 @@ namespace {
 
 using namespace mrg;
 
+// Six CTAs per SM (40 registers): the merge runs one short CTA per position, so
+// occupancy hides its load latencies; the rare exact recomputes may spill a few
+// values to local memory instead.
 template <int R>
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeThreads, 6)
 topk_merge_sorted_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id, int S,
                          int64_t P, int K, int32_t* __restrict__ out_ids,
                          float* __restrict__ out_vals, LogitMap lm, Refine rf) {

@@ -61,41 +61,43 @@ __device__ __forceinline__ void comp_add(float& s, float& c, float p) {
     c = __fadd_rn(c, e);
 }
 
-// h . w over D elements, rounded once to fp32 from a sum whose error is of order
-// D * 2^-48 times the sum of |products| (a plain fp32 sum's is of order D * 2^-24):
-// every bf16 x bf16 product is exact in fp32, the products are added with
-// compensated summation in
-// four independent accumulators per lane (fixed order: lane chunks, then the
-// accumulators, then a shuffle tree), and s + c is rounded once.  All lanes of the
-// warp call; every lane returns the result.  (fp32 arithmetic: fp64 runs at a small
-// fraction of the fp32 rate on this GPU.)
-__device__ __forceinline__ float exact_logit(const uint16_t* __restrict__ h, const uint16_t* __restrict__ w,
-                                             int64_t D, int lane) {
+// Part of h . w over D elements: the 16-byte chunks k = k0, k0 + step, ... of the
+// row (step a multiple of 32; lane l starts at k0 + l), every bf16 x bf16 product
+// exact in fp32 and the products added with compensated summation in four
+// independent accumulators per lane, then the lanes combined by a shuffle tree
+// (fixed order).  All lanes of the warp call; every lane returns the warp's partial
+// as the unevaluated sum S + Cc.  h may be in shared or global memory.  (fp32
+// arithmetic: fp64 runs at a small fraction of the fp32 rate on this GPU.)
+template <bool HG>
+__device__ __forceinline__ void logit_partial(const uint16_t* h, const uint16_t* __restrict__ w, int64_t D,
+                                              int64_t k0, int64_t step, int lane, float& S, float& Cc) {
     float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
     const int64_t nck = D / 8;  // 16-byte chunks of a row
-    // a lane takes chunks lane, lane + 32, ...; eight of them are loaded before any
-    // is used, so a row costs a few memory latencies, not one per chunk
-    for (int64_t k0 = lane; k0 < nck; k0 += 32 * 8) {
-        uint4 hv[8], wv[8];
+    // four W chunks (and, HG: h in global memory, four h chunks) are loaded before
+    // any is used: a row costs a few memory latencies, not one per chunk
+    for (int64_t kb = k0 + lane; kb < nck; kb += 4 * step) {
+        uint4 wv[4], hv[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int64_t k = k0 + 32 * u;
+        for (int u = 0; u < 4; ++u) {
+            const int64_t k = kb + u * step;
             if (k < nck) {
-                hv[u] = __ldg(reinterpret_cast<const uint4*>(h) + k);
                 wv[u] = __ldg(reinterpret_cast<const uint4*>(w) + k);
+                if (HG) hv[u] = __ldg(reinterpret_cast<const uint4*>(h) + k);
             }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (k0 + 32 * u >= nck) break;
+        for (int u = 0; u < 4; ++u) {
+            const int64_t k = kb + u * step;
+            if (k >= nck) break;
             float hf[8], wf[8];
-            unpack8(hv[u], hf);
+            unpack8(HG ? hv[u] : reinterpret_cast<const uint4*>(h)[k], hf);
             unpack8(wv[u], wf);
 #pragma unroll
             for (int e = 0; e < 8; ++e) comp_add(s[e & 3], c[e & 3], __fmul_rn(hf[e], wf[e]));
         }
     }
-    float S = s[0], Cc = c[0];
+    S = s[0];
+    Cc = c[0];
 #pragma unroll
     for (int a = 1; a < 4; ++a) {
         comp_add(S, Cc, s[a]);
@@ -110,7 +112,6 @@ __device__ __forceinline__ float exact_logit(const uint16_t* __restrict__ h, con
         two_sum(a, b, S, e);
         Cc = __fadd_rn(__fadd_rn(lo ? Cc : C2, lo ? C2 : Cc), e);
     }
-    return __fadd_rn(S, Cc);
 }
 
 // The final top-K of position p from the S sorted lists part_[v|id][s][P][K], by
@@ -131,6 +132,8 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
     __shared__ float xv[kWarps][R * 32 + 1];  // row 0 also holds the (K+1)-th entry
     __shared__ int xi[kWarps][R * 32 + 1];
     __shared__ int re_idx[R * 32 + 1];
+    __shared__ int8_t link[R * 32 + 1];  // link[k]: entries k and k + 1 are near-tied
+    __shared__ float red_s[kWarps], red_c[kWarps];
     __shared__ float t_v;
     __shared__ int t_id, have_t, n_cand, n_re;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -305,21 +308,86 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
                 const bool up = k > 0 && ok && near_tie(xv[0][k - 1], xv[0][k]);
                 const bool down =
                     k + 1 < L && ok && xi[0][k + 1] != wtk::kEmptyId && near_tie(xv[0][k], xv[0][k + 1]);
+                link[k] = down ? 1 : 0;
                 if (up || down) re_idx[atomicAdd(&n_re, 1)] = k;
             }
         }
         __syncthreads();
         const int nre = n_re;
         if (nre > 0) {
+            // the row of h, read by every recompute: with more than two, into the
+            // lists' shared memory (free again: the scan above was its last use) when
+            // it fits; one or two read it from global memory beside their W rows
             const uint16_t* hrow = rf.h + p * rf.D;
-            for (int f = warp; f < nre; f += kWarps) {
-                const int k = re_idx[f];
-                const float x = exact_logit(hrow, rf.W + int64_t(xi[0][k]) * rf.D, rf.D, lane);
-                if (lane == 0) xv[0][k] = x;
+            const bool staged = nre > 2 && size_t(rf.D) * 2 <= size_t(S) * K * 16;
+            if (staged) {
+                uint4* hs = reinterpret_cast<uint4*>(smem);
+                for (int64_t i = tid; i < rf.D / 8; i += kWarps * 32)
+                    hs[i] = __ldg(reinterpret_cast<const uint4*>(hrow) + i);
+                __syncthreads();
+                hrow = reinterpret_cast<const uint16_t*>(smem);
             }
-            __syncthreads();
+            // gw warps per recompute (all eight for one): a recompute's loads are
+            // spread over gw * 32 lanes, so one or two rows cost about one memory
+            // latency; the warps' partials are added in warp order
+            const int gw = nre >= 8 ? 1 : (nre >= 4 ? 2 : (nre >= 2 ? 4 : 8));
+            const int per_round = kWarps / gw;
+            for (int f0 = 0; f0 < nre; f0 += per_round) {
+                const int f = f0 + warp / gw, sub = warp % gw;
+                float S = 0.f, Cc = 0.f;
+                if (f < nre) {
+                    const uint16_t* wrow = rf.W + int64_t(xi[0][re_idx[f]]) * rf.D;
+                    if (staged) logit_partial<false>(hrow, wrow, rf.D, int64_t(sub) * 32, int64_t(gw) * 32, lane, S, Cc);
+                    else logit_partial<true>(hrow, wrow, rf.D, int64_t(sub) * 32, int64_t(gw) * 32, lane, S, Cc);
+                }
+                if (lane == 0) {
+                    red_s[warp] = S;
+                    red_c[warp] = Cc;
+                }
+                __syncthreads();
+                if (sub == 0 && lane == 0 && f < nre) {
+                    float T = red_s[warp], Tc = red_c[warp];
+                    for (int q = 1; q < gw; ++q) {
+                        float e;
+                        two_sum(T, red_s[warp + q], T, e);
+                        Tc = __fadd_rn(__fadd_rn(Tc, red_c[warp + q]), e);
+                    }
+                    xv[0][re_idx[f]] = __fadd_rn(T, Tc);
+                }
+                __syncthreads();
+            }
         }
         if (warp != 0) return;
+    }
+    if (refine && map.identity()) {
+        // The list is sorted by the fp32 values the kernels computed; only the
+        // entries of a run of near ties (now holding exact values) may change places,
+        // and only among themselves: each entry's rank is its run's first index plus
+        // the run entries that rank before it.  Entries outside runs keep their
+        // place, and the ranks of a run are a permutation of its indices whatever the
+        // recomputed values are.
+        for (int k = lane; k < L; k += 32) {
+            const int id = xi[0][k];
+            if (id == wtk::kEmptyId) {
+                if (k < K) {
+                    out_ids[p * K + k] = -1;
+                    out_vals[p * K + k] = -INFINITY;
+                }
+                continue;
+            }
+            const float v = xv[0][k];
+            int s0 = k, s1 = k;
+            while (s0 > 0 && link[s0 - 1]) --s0;
+            while (s1 + 1 < L && link[s1]) ++s1;
+            int rank = s0;
+            for (int j = s0; j <= s1; ++j)
+                if (j != k && ranks_before(xv[0][j], xi[0][j], v, id)) ++rank;
+            if (rank < K) {
+                out_ids[p * K + rank] = id;
+                out_vals[p * K + rank] = v;
+            }
+        }
+        return;
     }
     // Rank the kept entries by (mapped value, id): the list is sorted by the fp32
     // values the kernels computed; this settles the recomputed near ties and the
