@@ -21,6 +21,7 @@
 // candidate-list order.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace df2 {
 
@@ -173,6 +174,208 @@ lattice_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __rest
     }
 }
 
+// ---------------------------------------------------------- tensor cores --
+// lattice_tc_kernel (32 < K <= 64): one CTA of 256 threads per (request, slot).  The
+// slot's table is a small GEMM, S = vals + X Y^T with X[i] = A[a_i] (.) G_t (fp32)
+// and Y[j] = Bc[b_j] (bf16).  X is split into bf16 halves, x = hi + lo with
+// lo = bf16(x - hi) (x - hi is exact in fp32; hi + lo is within 2^-17 of x), and
+// the halves are stacked as the 128 rows of one tcgen05 MMA: rows 0..63 hi, rows
+// 64..127 lo, N = K rounded up to 16 candidate rows, fp32 accumulation in TMEM.
+// Row i + 64 of the result is added to row i in the epilogue, so one M = 128 MMA
+// per 16-wide step covers both halves with no wasted rows.  The rank dimension
+// goes through shared memory in 64-wide slices (one 128-byte swizzle row per
+// operand row): the threads issue every gather of slice c + 1 before they wait for
+// the tensor core to finish slice c (an mbarrier), then form the slice (the
+// product with G, the split, the writes in the swizzled K-major layout).  One
+// 24 KB buffer lets eight CTAs share an SM, which is what hides the gathers'
+// latency.  Waits are bounded.
+constexpr int kLtcThreads = 256;
+constexpr int kLtcMaxK = 64;
+constexpr uint32_t kLtcA = 128 * 128;            // A slice: 128 rows x 128 bytes
+constexpr uint32_t kLtcB = kLtcMaxK * 128;       // B slice: up to 64 rows x 128 bytes
+constexpr uint32_t kLtcBuf = kLtcA + kLtcB;      // 24 KB, a multiple of 1024
+
+__device__ __forceinline__ uint32_t ltc_pack(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 16-byte chunk cc of operand row `row` in a 128-byte-swizzled K-major slice.
+__device__ __forceinline__ uint4* ltc_chunk(uint8_t* base, int row, int cc) {
+    return reinterpret_cast<uint4*>(base + size_t(row) * 128 + size_t((cc ^ (row & 7)) * 16));
+}
+
+__global__ void __launch_bounds__(kLtcThreads)
+lattice_tc_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __restrict__ ids,
+                  const float* __restrict__ vals, const float* __restrict__ G,
+                  const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K, int r,
+                  float* __restrict__ lattice, int32_t* __restrict__ dev_status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLtcBuf);  // [0] the slice's MMAs, [2] all MMAs
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    const int T = B - 1;
+    const int s = int(blockIdx.x % T);
+    const int64_t q = blockIdx.x / T;
+    const int t = s + 1;
+    const int64_t row = q * B + t;  // the successor row (position t)
+    const int tid = threadIdx.x, warp = tid >> 5;
+    float* out = lattice + ((q * T + s) * int64_t(K)) * K;
+    const int NP = (K + 15) / 16 * 16;
+    const int rows_here = (s == 0) ? 1 : K;
+
+    const bool valid = lattice_request_valid(anchors, q, B, ids, K, V);
+    if (!valid) {
+        for (int e = tid; e < K * K; e += kLtcThreads) out[e] = __int_as_float(0x7fc00000);
+        if (tid == 0 && s == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+        return;
+    }
+    if (tid == 0) {
+        tc::mbar_init(&bars[0], 1);
+        tc::mbar_init(&bars[1], 1);
+        tc::mbar_init(&bars[2], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_holder, 64);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    // thread roles while forming a slice: two threads per operand row, four 16-byte
+    // chunks each; tid < 128 predecessor row i = tid / 2 (hi row i, lo row i + 64),
+    // tid >= 128 candidate row j = (tid - 128) / 2
+    const bool is_a = tid < 128;
+    const int my = (is_a ? tid : tid - 128) >> 1;
+    const int cc0 = (tid & 1) * 4;
+    int64_t src = -1;
+    if (is_a) {
+        if (my < rows_here) src = s == 0 ? int64_t(__ldg(anchors + q)) : int64_t(__ldg(ids + (row - 1) * K + my));
+    } else if (my < K) {
+        src = int64_t(__ldg(ids + row * K + my));
+    }
+    const float* Grow = G + row * r;
+    // the whole gathered row into L2 at once (one contiguous stream per row), so the
+    // slices' 128-byte pieces of it hit L2 instead of being separate DRAM accesses
+    if (src >= 0 && (tid & 1) == 0) tc::bulk_prefetch_l2((is_a ? A : Bc) + src * r, uint32_t(r) * 2);
+    const uint32_t idesc = tc::idesc_bf16_f32(128, NP);
+    const int nsl = (r + 63) / 64;
+    uint32_t ph[1] = {0u};
+    bool ok = true;
+    for (int c = 0; c < nsl; ++c) {
+        const int k0 = c * 64;
+        // every load of this thread's part of the slice first, into registers
+        uint4 rv[4];
+        float4 gv[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + (cc0 + u) * 8;
+            const bool in = src >= 0 && k < r;
+            rv[u] = in ? __ldg(reinterpret_cast<const uint4*>((is_a ? A : Bc) + src * r + k)) : make_uint4(0, 0, 0, 0);
+            if (is_a) {
+                gv[2 * u] = in ? __ldg(reinterpret_cast<const float4*>(Grow + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                gv[2 * u + 1] = in ? __ldg(reinterpret_cast<const float4*>(Grow + k + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        if (c >= 1) {
+            // the MMAs that read the buffer for the previous slice are done (a slice's
+            // MMAs take a small fraction of the time its gathers do)
+            const bool got = tc::mbar_wait(&bars[0], ph[0], abort_flag);
+            ph[0] ^= 1u;
+            if (__syncthreads_or(!got)) { ok = false; break; }
+        }
+        uint8_t* bufA = smem;
+        uint8_t* bufB = bufA + kLtcA;
+        if (is_a) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float af[8];
+                unpack8(rv[u], af);
+                const float g8[8] = {gv[2 * u].x, gv[2 * u].y, gv[2 * u].z, gv[2 * u].w,
+                                     gv[2 * u + 1].x, gv[2 * u + 1].y, gv[2 * u + 1].z, gv[2 * u + 1].w};
+                float xh[8], xl[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float x = af[e] * g8[e];
+                    xh[e] = bf16_to_f32(f32_to_bf16_rn(x));
+                    xl[e] = x - xh[e];
+                }
+                *ltc_chunk(bufA, my, cc0 + u) = make_uint4(ltc_pack(xh[0], xh[1]), ltc_pack(xh[2], xh[3]),
+                                                           ltc_pack(xh[4], xh[5]), ltc_pack(xh[6], xh[7]));
+                *ltc_chunk(bufA, my + 64, cc0 + u) = make_uint4(ltc_pack(xl[0], xl[1]), ltc_pack(xl[2], xl[3]),
+                                                                ltc_pack(xl[4], xl[5]), ltc_pack(xl[6], xl[7]));
+            }
+        } else if (my < NP) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) *ltc_chunk(bufB, my, cc0 + u) = rv[u];
+        }
+        // the generic-proxy writes above become visible to the tensor core's reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t a0 = tc::smem_u32(bufA), b0 = tc::smem_u32(bufB);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc::mma_bf16(tmem, tc::sw128_kmajor_desc(a0 + 32 * kk), tc::sw128_kmajor_desc(b0 + 32 * kk), idesc,
+                             (c | kk) != 0 ? 1u : 0u);
+            tc::mma_commit(&bars[0]);
+        }
+    }
+    if (tid == 0) tc::mma_commit(&bars[2]);
+    {
+        volatile int never = 0;
+        const bool done = tc::mbar_wait(&bars[2], 0, ok ? abort_flag : &never);
+        if (!done) ok = false;
+    }
+    ok = !__syncthreads_or(!ok);
+    tc::fence_after_sync();
+    // the accumulator -> shared memory (the slice buffer is free): warps 2-3 (TMEM
+    // lanes 64..127, the lo rows) store theirs, then warps 0-1 add their hi rows in
+    // place, then every thread writes the table with consecutive threads on
+    // consecutive columns
+    float* red = reinterpret_cast<float*>(smem);  // [64][kLtcMaxK + 1]
+    constexpr int ld = kLtcMaxK + 1;
+    if (ok && (warp == 2 || warp == 3)) {
+        for (int c0 = 0; c0 < NP; c0 += 16) {
+            float v[16];
+            tc::tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) red[size_t(tid - 64) * ld + c0 + e] = v[e];
+        }
+    }
+    __syncthreads();
+    if (ok && warp < 2) {
+        for (int c0 = 0; c0 < NP; c0 += 16) {
+            float v[16];
+            tc::tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) red[size_t(tid) * ld + c0 + e] = v[e] + red[size_t(tid) * ld + c0 + e];
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (ok) {
+        for (int e = tid; e < K * K; e += kLtcThreads) {
+            const int i = e / K, j = e - i * K;
+            out[e] = i < rows_here ? __ldg(vals + row * K + j) + red[size_t(i) * ld + j] : __int_as_float(0x7fc00000);
+        }
+    } else if (tid == 0 && dev_status) {
+        atomicOr(dev_status, DF2_STATUS_WAIT_TIMEOUT);
+    }
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 64);
+    }
+}
+
 constexpr int kWalkWarps = 4;
 
 // Warp-wide best by (value desc, token id asc); returns the winning column.
@@ -283,6 +486,18 @@ cudaError_t lattice_launch(const int32_t* anchors, int R, int B, const int32_t* 
                            const float* G, const uint16_t* A, const uint16_t* Bc, int64_t V, int K,
                            int r, float* lattice, int32_t* dev_status, cudaStream_t stream) {
     const int T = B - 1;
+    if (K > 32 && K <= kLtcMaxK) {  // shorter lists: latency-bound, the CUDA-core tiles below
+        // one slice buffer (the accumulator is staged over it at the end), then the
+        // barriers, the TMEM address and the abort flag: eight CTAs fit on an SM
+        const size_t smem = size_t(kLtcBuf) + 64 + 1024;
+        cudaError_t e = cudaFuncSetAttribute(lattice_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+        lattice_tc_kernel<<<unsigned(int64_t(R) * T), kLtcThreads, smem, stream>>>(anchors, B, ids, vals, G, A, Bc,
+                                                                                   V, K, r, lattice, dev_status);
+        note_launch();
+        return cudaGetLastError();
+    }
 #define DF2_LAT(TM)                                                                                   \
     do {                                                                                              \
         const int tiles = (K + 16 * (TM) - 1) / (16 * (TM));                                          \
