@@ -291,19 +291,25 @@ conv_apply_async_kernel(const T* __restrict__ x, int64_t nblocks, int C, int B, 
 
 // Pipelined apply for many rows.  An item is one anchor block times one strip of
 // nt 16-byte channel chunks (a chunk inside one group).  Persistent CTAs take items
-// blockIdx.x, + gridDim.x, ...; thread 0 fetches an item's B rows of x (and of the
+// blockIdx.x, + gridDim.x, ... through a ring of `stages` shared buffers.  A
+// producer warp (the CTA's last) fetches an item's B rows of x (and of the
 // residual) and the strip's corrections of every row and tap with 1-D bulk copies,
-// a few large copies per item that complete on the buffer's mbarrier, into one of
-// two shared buffers, while the CTA computes the item in the other.  The
-// arithmetic is conv_apply_async_kernel's.  Every wait is bounded: on a timeout the
-// CTA stops (all threads together) and waits, again bounded, for the copies it
-// still has in flight.
+// a few large copies per item shared among its lanes and completing on the
+// buffer's full barrier; the nt compute threads wait only for that barrier,
+// compute the item with conv_apply_async_kernel's arithmetic, and release the
+// buffer on its empty barrier.  No barrier spans the CTA inside the loop, so a
+// slow thread holds up no other.  Every wait is bounded: a thread that gives up
+// raises the CTA's abort flag and stops; the producer then waits, again bounded,
+// for the copies it still has in flight.
 struct BulkPlan {
-    int nt = 0;         // threads per CTA (chunks per strip)
+    int nt = 0;         // compute threads per CTA (chunks per strip)
     int strips = 0;
+    int stages = 0;
     uint32_t buf = 0;   // bytes per buffer
-    uint32_t smem = 0;  // two buffers and their barriers
+    uint32_t smem = 0;  // the buffers and their barriers
 };
+
+constexpr int kBulkMaxStages = 4;
 
 template <typename T>
 BulkPlan bulk_plan(int C, int B, int taps, int g, int G, int64_t dyn_ld, bool res) {
@@ -311,79 +317,108 @@ BulkPlan bulk_plan(int C, int B, int taps, int g, int G, int64_t dyn_ld, bool re
     constexpr int N = Vec<T>::N;
     const int chunks = C / N;
     if (taps > 4 || g % N != 0 || G % 4 != 0 || dyn_ld % 4 != 0) return pl;
-    for (int nt = 256; nt >= 64; nt -= 32) {
-        if (chunks % nt != 0) continue;
-        const int ngrp = nt * N / g;
-        if (ngrp % 4 != 0) continue;
-        const uint32_t row = uint32_t(nt) * 16;
-        const uint32_t buf = (uint32_t(B) * row * (res ? 2u : 1u) + uint32_t(B) * taps * ngrp * 4 + 127) / 128 * 128;
-        if (2 * buf + 64 > 112 * 1024) continue;  // at least two CTAs per SM
-        pl.nt = nt;
-        pl.strips = chunks / nt;
-        pl.buf = buf;
-        pl.smem = 2 * buf + 64;
-        return pl;
-    }
+    // a strip of at least 128 chunks if one fits (up to 256, dividing the row), with
+    // a ring of four to two buffers that fits twice on an SM, preferring more
+    // buffers; narrower strips only when no such strip fits
+    for (int min_nt : {128, 64})
+    for (int stages = kBulkMaxStages; stages >= 2; --stages)
+        for (int nt = 256; nt >= min_nt; nt -= 32) {
+            if (chunks % nt != 0) continue;
+            const int ngrp = nt * N / g;
+            if (ngrp % 4 != 0) continue;
+            const uint32_t row = uint32_t(nt) * 16;
+            const uint32_t buf =
+                (uint32_t(B) * row * (res ? 2u : 1u) + uint32_t(B) * taps * ngrp * 4 + 127) / 128 * 128;
+            if (stages * buf + 128 > 110 * 1024) continue;
+            pl.nt = nt;
+            pl.strips = chunks / nt;
+            pl.stages = stages;
+            pl.buf = buf;
+            pl.smem = stages * buf + 128;
+            return pl;
+        }
     return pl;
 }
 
 template <typename T, int TAPS, bool RES>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(288)
 conv_apply_bulk_kernel(const T* __restrict__ x, int64_t n_items, int C, int B, int g, int G, int strips,
-                       uint32_t buf_bytes, const float* __restrict__ base, const float* __restrict__ dyn,
+                       int stages, uint32_t buf_bytes, const float* __restrict__ base, const float* __restrict__ dyn,
                        int64_t dyn_ld, const T* __restrict__ res, T* __restrict__ y) {
     constexpr int N = Vec<T>::N;
     using Raw = typename Vec<T>::Raw;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int nt = blockDim.x, tid = threadIdx.x;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int nt = blockDim.x - 32, tid = threadIdx.x;
     const int ngrp = nt * N / g;
     const uint32_t row = uint32_t(nt) * 16;
     const uint32_t xbytes = uint32_t(B) * row;
     const uint32_t rbytes = RES ? xbytes : 0u;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * size_t(buf_bytes));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(stages) * buf_bytes);
+    uint64_t* empty = full + kBulkMaxStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kBulkMaxStages);
     if (tid == 0) {
-        tc::mbar_init(&bars[0], 1);
-        tc::mbar_init(&bars[1], 1);
+        for (int s = 0; s < stages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], uint32_t(nt));
+        }
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
     __syncthreads();
-    const uint64_t pol = tc::l2_policy_evict_first();  // every byte is read once
-    auto issue = [&](int64_t item, int b) {
-        const int64_t nb = item / strips;
-        const int c0 = int(item - nb * strips) * nt * N;
-        const int grp0 = c0 / g;
-        uint8_t* buf = smem + size_t(b) * buf_bytes;
-        tc::mbar_arrive_expect_tx(&bars[b], xbytes + rbytes + uint32_t(B) * TAPS * ngrp * 4);
-        for (int t = 0; t < B; ++t) {
-            const int64_t p = nb * B + t;
-            tc::bulk_load(buf + size_t(t) * row, x + p * C + c0, row, &bars[b], pol);
-            if (RES) tc::bulk_load(buf + xbytes + size_t(t) * row, res + p * C + c0, row, &bars[b], pol);
-#pragma unroll
-            for (int j = 0; j < TAPS; ++j)
-                tc::bulk_load(buf + xbytes + rbytes + (size_t(t) * TAPS + j) * ngrp * 4, dyn + p * dyn_ld + j * G + grp0,
-                              uint32_t(ngrp) * 4, &bars[b], pol);
-        }
-    };
     const int64_t stride = gridDim.x;
-    int64_t item = blockIdx.x;
-    int8_t armed[2] = {-1, -1};  // thread 0: the phase each buffer's copies complete
-    if (tid == 0) {
-        if (item < n_items) { issue(item, 0); armed[0] = 0; }
-        if (item + stride < n_items) { issue(item + stride, 1); armed[1] = 0; }
+    const int64_t n_mine = blockIdx.x < n_items ? (n_items - blockIdx.x + stride - 1) / stride : 0;
+    if (tid >= nt) {
+        // ---------------------------------------------------------------- producer
+        const int lane = tid - nt;
+        const uint64_t pol = tc::l2_policy_evict_first();  // every byte is read once
+        const int per_row = (RES ? 2 : 1) + TAPS;
+        int64_t k = 0;
+        for (; k < n_mine; ++k) {
+            const int s = int(k % stages);
+            if (k >= stages) {
+                const bool got = tc::mbar_wait(&empty[s], uint32_t((k / stages - 1) & 1), abort_flag);
+                if (!__all_sync(kFull, got)) break;
+            }
+            const int64_t item = blockIdx.x + k * stride;
+            const int64_t nb = item / strips;
+            const int c0 = int(item - nb * strips) * nt * N;
+            const int grp0 = c0 / g;
+            uint8_t* buf = smem + size_t(s) * buf_bytes;
+            if (lane == 0) tc::mbar_arrive_expect_tx(&full[s], xbytes + rbytes + uint32_t(B) * TAPS * ngrp * 4);
+            __syncwarp();
+            for (int e = lane; e < B * per_row; e += 32) {
+                const int t = e / per_row, kind = e - t * per_row;
+                const int64_t p = nb * B + t;
+                if (kind == 0) {
+                    tc::bulk_load(buf + size_t(t) * row, x + p * C + c0, row, &full[s], pol);
+                } else if (RES && kind == 1) {
+                    tc::bulk_load(buf + xbytes + size_t(t) * row, res + p * C + c0, row, &full[s], pol);
+                } else {
+                    const int j = kind - (RES ? 2 : 1);
+                    tc::bulk_load(buf + xbytes + rbytes + (size_t(t) * TAPS + j) * ngrp * 4,
+                                  dyn + p * dyn_ld + j * G + grp0, uint32_t(ngrp) * 4, &full[s], pol);
+                }
+            }
+        }
+        if (lane == 0 && *abort_flag) {
+            // wait (bounded) for the copies issued but not consumed: the last
+            // `stages` items issued
+            volatile int never = 0;
+            for (int64_t kk = k - 1; kk >= 0 && kk >= k - stages; --kk)
+                tc::mbar_wait(&full[kk % stages], uint32_t((kk / stages) & 1), &never);
+        }
+        return;
     }
-    uint32_t phase[2] = {0u, 0u};
-    for (int b = 0; item < n_items; item += stride, b ^= 1) {
-        const bool got = tc::mbar_wait(&bars[b], phase[b], abort_flag);
-        if (__syncthreads_or(!got)) break;
-        phase[b] ^= 1u;
-        if (tid == 0) armed[b] = -1;
+    // -------------------------------------------------------------------- compute
+    const int gl = (tid * N) / g;
+    for (int64_t k = 0; k < n_mine; ++k) {
+        const int s = int(k % stages);
+        if (!tc::mbar_wait(&full[s], uint32_t((k / stages) & 1), abort_flag)) break;
+        const int64_t item = blockIdx.x + k * stride;
         const int64_t nb = item / strips;
         const int c0 = int(item - nb * strips) * nt * N + tid * N;
-        const uint8_t* buf = smem + size_t(b) * buf_bytes;
+        const uint8_t* buf = smem + size_t(s) * buf_bytes;
         const float* ds = reinterpret_cast<const float*>(buf + xbytes + rbytes);
-        const int gl = (tid * N) / g;
         float kb[TAPS][N], hist[TAPS][N];
 #pragma unroll
         for (int j = 0; j < TAPS; ++j)
@@ -414,17 +449,7 @@ conv_apply_bulk_kernel(const T* __restrict__ x, int64_t n_items, int C, int B, i
                                                                       size_t(tid) * 16));
             Vec<T>::store(y + p * C + c0, acc);
         }
-        __syncthreads();  // every thread is done with buffer b
-        if (tid == 0 && item + 2 * stride < n_items) {
-            issue(item + 2 * stride, b);
-            armed[b] = int8_t(phase[b]);
-        }
-    }
-    if (tid == 0 && *abort_flag) {
-        // a copy that timed out: wait (bounded) for the copies still in flight
-        volatile int never = 0;
-        for (int b = 0; b < 2; ++b)
-            if (armed[b] >= 0) tc::mbar_wait(&bars[b], uint32_t(armed[b]), &never);
+        tc::mbar_arrive(&empty[s]);  // this thread is done with the buffer
     }
 }
 
@@ -487,11 +512,12 @@ cudaError_t launch_t(const T* x, int64_t P, int C, int B, int taps, int g, const
         if (e != cudaSuccess) return e;                                                                    \
         e = cudaGetDevice(&dev);                                                                           \
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);        \
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, bp.nt, bp.smem); \
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, bp.nt + 32, bp.smem); \
         if (e != cudaSuccess) return e;                                                                    \
         const int64_t grid = n_items < int64_t(sms) * per_sm ? n_items : int64_t(sms) * per_sm;           \
-        kern<<<unsigned(grid > 0 ? grid : 1), bp.nt, bp.smem, stream>>>(x, n_items, C, B, g, G, bp.strips, bp.buf, \
-                                                                     base, dyn, dyn_ld, res, y);            \
+        kern<<<unsigned(grid > 0 ? grid : 1), bp.nt + 32, bp.smem, stream>>>(x, n_items, C, B, g, G, bp.strips, \
+                                                                          bp.stages, bp.buf, base, dyn, dyn_ld, \
+                                                                          res, y);                              \
     } while (0)
 #define DF2_BULK_T(TP)                 \
     do {                               \
