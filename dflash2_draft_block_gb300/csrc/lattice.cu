@@ -248,22 +248,20 @@ lattice_tc_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __r
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_holder;
 
-    // thread roles while forming a slice: two threads per operand row, four 16-byte
-    // chunks each; tid < 128 predecessor row i = tid / 2 (hi row i, lo row i + 64),
-    // tid >= 128 candidate row j = (tid - 128) / 2
-    const bool is_a = tid < 128;
-    const int my = (is_a ? tid : tid - 128) >> 1;
-    const int cc0 = (tid & 1) * 4;
-    int64_t src = -1;
-    if (is_a) {
-        if (my < rows_here) src = s == 0 ? int64_t(__ldg(anchors + q)) : int64_t(__ldg(ids + (row - 1) * K + my));
-    } else if (my < K) {
-        src = int64_t(__ldg(ids + row * K + my));
-    }
+    // every thread forms two 16-byte chunks of one predecessor row (hi row and lo
+    // row) and two of one candidate row: row tid / 4, chunks 2 (tid % 4) and + 1
+    const int my = tid >> 2;
+    const int cc0 = (tid & 3) * 2;
+    const int64_t src_a = my < rows_here ? (s == 0 ? int64_t(__ldg(anchors + q)) : int64_t(__ldg(ids + (row - 1) * K + my)))
+                                         : int64_t(-1);
+    const int64_t src_b = my < K ? int64_t(__ldg(ids + row * K + my)) : int64_t(-1);
     const float* Grow = G + row * r;
     // the whole gathered row into L2 at once (one contiguous stream per row), so the
     // slices' 128-byte pieces of it hit L2 instead of being separate DRAM accesses
-    if (src >= 0 && (tid & 1) == 0) tc::bulk_prefetch_l2((is_a ? A : Bc) + src * r, uint32_t(r) * 2);
+    if ((tid & 3) == 0) {
+        if (src_a >= 0) tc::bulk_prefetch_l2(A + src_a * r, uint32_t(r) * 2);
+        if (src_b >= 0) tc::bulk_prefetch_l2(Bc + src_b * r, uint32_t(r) * 2);
+    }
     const uint32_t idesc = tc::idesc_bf16_f32(128, NP);
     const int nsl = (r + 63) / 64;
     uint32_t ph[1] = {0u};
@@ -271,17 +269,16 @@ lattice_tc_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __r
     for (int c = 0; c < nsl; ++c) {
         const int k0 = c * 64;
         // every load of this thread's part of the slice first, into registers
-        uint4 rv[4];
-        float4 gv[8];
+        uint4 ra[2], rb[2];
+        float4 gv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 2; ++u) {
             const int k = k0 + (cc0 + u) * 8;
-            const bool in = src >= 0 && k < r;
-            rv[u] = in ? __ldg(reinterpret_cast<const uint4*>((is_a ? A : Bc) + src * r + k)) : make_uint4(0, 0, 0, 0);
-            if (is_a) {
-                gv[2 * u] = in ? __ldg(reinterpret_cast<const float4*>(Grow + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                gv[2 * u + 1] = in ? __ldg(reinterpret_cast<const float4*>(Grow + k + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            const bool in = k < r;
+            ra[u] = (in && src_a >= 0) ? __ldg(reinterpret_cast<const uint4*>(A + src_a * r + k)) : make_uint4(0, 0, 0, 0);
+            rb[u] = (in && src_b >= 0) ? __ldg(reinterpret_cast<const uint4*>(Bc + src_b * r + k)) : make_uint4(0, 0, 0, 0);
+            gv[2 * u] = in ? __ldg(reinterpret_cast<const float4*>(Grow + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[2 * u + 1] = in ? __ldg(reinterpret_cast<const float4*>(Grow + k + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         if (c >= 1) {
             // the MMAs that read the buffer for the previous slice are done (a slice's
@@ -292,28 +289,22 @@ lattice_tc_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __r
         }
         uint8_t* bufA = smem;
         uint8_t* bufB = bufA + kLtcA;
-        if (is_a) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float af[8];
-                unpack8(rv[u], af);
-                const float g8[8] = {gv[2 * u].x, gv[2 * u].y, gv[2 * u].z, gv[2 * u].w,
-                                     gv[2 * u + 1].x, gv[2 * u + 1].y, gv[2 * u + 1].z, gv[2 * u + 1].w};
-                float xh[8], xl[8];
+        for (int u = 0; u < 2; ++u) {
+            float af[8];
+            unpack8(ra[u], af);
+            const float g8[8] = {gv[2 * u].x, gv[2 * u].y, gv[2 * u].z, gv[2 * u].w,
+                                 gv[2 * u + 1].x, gv[2 * u + 1].y, gv[2 * u + 1].z, gv[2 * u + 1].w};
+            uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = af[e] * g8[e];
-                    xh[e] = bf16_to_f32(f32_to_bf16_rn(x));
-                    xl[e] = x - xh[e];
-                }
-                *ltc_chunk(bufA, my, cc0 + u) = make_uint4(ltc_pack(xh[0], xh[1]), ltc_pack(xh[2], xh[3]),
-                                                           ltc_pack(xh[4], xh[5]), ltc_pack(xh[6], xh[7]));
-                *ltc_chunk(bufA, my + 64, cc0 + u) = make_uint4(ltc_pack(xl[0], xl[1]), ltc_pack(xl[2], xl[3]),
-                                                                ltc_pack(xl[4], xl[5]), ltc_pack(xl[6], xl[7]));
+            for (int e = 0; e < 4; ++e) {
+                const float x0 = af[2 * e] * g8[2 * e], x1 = af[2 * e + 1] * g8[2 * e + 1];
+                hi[e] = ltc_pack(x0, x1);  // nearest-even, as the split needs
+                lo[e] = ltc_pack(x0 - bf16_lo(hi[e]), x1 - bf16_hi(hi[e]));
             }
-        } else if (my < NP) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) *ltc_chunk(bufB, my, cc0 + u) = rv[u];
+            *ltc_chunk(bufA, my, cc0 + u) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *ltc_chunk(bufA, my + 64, cc0 + u) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            if (my < NP) *ltc_chunk(bufB, my, cc0 + u) = rb[u];
         }
         // the generic-proxy writes above become visible to the tensor core's reads
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
