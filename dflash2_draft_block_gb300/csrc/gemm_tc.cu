@@ -20,6 +20,9 @@
 // 2-5 drain the other accumulator with tcgen05.ld.  All waits are bounded.
 #include <cudaTypedefs.h>
 
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_pair.cuh"
@@ -140,7 +143,12 @@ namespace {
 // [WN/2 r, WN/2 (r + 1)) of the tile's WN; CTA 0's MMA thread computes the whole
 // tile, and each CTA's TMEM receives its own 128 rows x WN columns.  Each CTA thus
 // stages half the B bytes per flop of the one-CTA tile.
-template <int EPI, int WN, bool PAIR, bool GT>
+// MC (with PAIR): a cluster of two pairs on consecutive M tiles of the same N
+// range.  The first pair's CTAs load the B halves once, multicast to the CTA of the
+// same pair rank in the other pair; a stage is free again when both pairs' MMAs
+// have read it (their commits arrive on every CTA's empty barrier).  A quarter less
+// data crosses from L2 to the SMs per flop.
+template <int EPI, int WN, bool PAIR, bool GT, bool MC = false>
 __global__ void __launch_bounds__(kWideThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_g, const WideArgs args) {
@@ -170,7 +178,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         for (int i = threadIdx.x; i < args.n_zero; i += blockDim.x) args.zero_words[i] = 0u;
     const int n_groups = (args.n_nt + args.tiles_per_cta - 1) / args.tiles_per_cta;
     // the work unit: one M tile, or (PAIR) one pair of M tiles, times a range of N tiles
-    const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+    const uint32_t crank = PAIR ? tc::cluster_ctarank() : 0u;
+    const uint32_t rank = crank & 1u;         // rank inside the CTA pair
+    const uint32_t lead_rank = crank & ~1u;   // cluster rank of this CTA's pair leader
     const bool leader = rank == 0;
     const int unit = PAIR ? bid >> 1 : bid;
     const int n_mu = PAIR ? (args.n_mt + 1) / 2 : args.n_mt;
@@ -206,7 +216,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&empty[s], MC ? 2 : 1);  // MC: both pairs' MMAs release a stage
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], 1);
@@ -266,10 +276,17 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                         uint8_t* da = st + size_t(j) * kABox;
                         uint8_t* db = st + size_t(kbox) * kABox + size_t(j) * kBBox;
                         if (PAIR) {
-                            const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
+                            const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), lead_rank);
                             tc::tma_load_2d_pair(da, &tm_a, fb, x, mtk * WM, pol_a);
-                            if (gt) tc::tma_load_2d_pair(db, &tm_g, fb, x, yb, pol_b);
-                            else tc::tma_load_2d_pair(db, &tm_b, fb, x, yb, pol_b);
+                            if (MC) {
+                                // the first pair loads the B halves for both pairs
+                                const uint16_t mask = uint16_t((1u << crank) | (1u << (crank + 2)));
+                                if (crank < 2) tc::tma_load_2d_pair_mc(db, gt ? &tm_g : &tm_b, fb, mask, x, yb, pol_b);
+                            } else if (gt) {
+                                tc::tma_load_2d_pair(db, &tm_g, fb, x, yb, pol_b);
+                            } else {
+                                tc::tma_load_2d_pair(db, &tm_b, fb, x, yb, pol_b);
+                            }
                         } else {
                             tc::tma_load_2d(da, &tm_a, &full[stage], x, mtk * WM, pol_a);
                             if (gt) tc::tma_load_2d(db, &tm_g, &full[stage], x, yb, pol_b);
@@ -322,16 +339,16 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                             else tc::mma_bf16(d_tmem, ad, bd, idesc, acc);
                         }
                     }
-                    if (PAIR) tc::mma_commit_pair(&empty[stage], 0x3);
+                    if (PAIR) tc::mma_commit_pair(&empty[stage], MC ? 0xF : 0x3);
                     else tc::mma_commit(&empty[stage]);
                     if (++stage == nstages) { stage = 0; phase ^= 1; }
                 }
                 if (ok) {
-                    if (PAIR) tc::mma_commit_pair(&tfull[b], 0x3);
+                    if (PAIR) tc::mma_commit_pair(&tfull[b], uint16_t(0x3u << lead_rank));
                     else tc::mma_commit(&tfull[b]);
                 }
             }
-            if (PAIR) tc::mma_commit_pair(mma_done, 0x3);
+            if (PAIR) tc::mma_commit_pair(mma_done, uint16_t(0x3u << lead_rank));
             else tc::mma_commit(mma_done);
             volatile int never = 0;
             tc::mbar_wait(mma_done, 0, &never);
@@ -441,7 +458,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             __syncwarp();
             if (lane == 0) {
                 // PAIR: CTA 0's MMA thread waits for both CTAs' epilogues
-                if (PAIR) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&tempty[b]), 0));
+                if (PAIR) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&tempty[b]), lead_rank));
                 else tc::mbar_arrive(&tempty[b]);
             }
             if (EPI == EPI_TOPK && !gt && args.thr_g && row_ok) {
@@ -552,6 +569,7 @@ int wide_groups(int n_mt, int n_nt, int num_sms) {
 // its CTA still stages its half of every B tile).
 struct WidePlan {
     bool pair;
+    bool mc;            // top-K: clusters of two pairs sharing the W_lm tiles
     bool linear;        // store: units take runs of the M-fastest tile order
     int n_mt, n_nt;     // 128-row M tiles, 256-row N tiles
     int n_mu;           // work units along M: tiles, or pairs of tiles
@@ -560,6 +578,11 @@ struct WidePlan {
     int units;          // units launched (each one CTA or one CTA pair)
     int nstages;
 };
+
+// Clusters of two CTA pairs (four SMs of one GPC) that can run at once with the
+// top-K kernel's shared memory, from the occupancy API, once per device and shape
+// class; 0 when the query fails.
+int mc_cluster_slots(int K, int nstages);
 
 WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persistent) {
     WidePlan p{};
@@ -575,6 +598,26 @@ WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persi
         p.tiles_per_cta = (p.n_nt + groups - 1) / groups;
         p.n_groups = (p.n_nt + p.tiles_per_cta - 1) / p.tiles_per_cta;
         p.units = p.n_mu * p.n_groups;
+        if (epi == EPI_TOPK && p.pair && p.n_mu % 2 == 0) {
+            // the same with clusters of two pairs: fewer of them fit at once (four SMs
+            // of one GPC each), but a tile moves a quarter fewer bytes from L2, which
+            // feeds this kernel.  Cost: waves x tiles per unit x relative tile time.
+            const int mc_slots = 2 * mc_cluster_slots(K, p.nstages);
+            if (mc_slots >= 2) {
+                const int g2 = wide_groups(p.n_mu, p.n_nt, mc_slots);
+                const int tpc2 = (p.n_nt + g2 - 1) / g2;
+                const int ng2 = (p.n_nt + tpc2 - 1) / tpc2;
+                const int units2 = p.n_mu * ng2;
+                const double cost_pair = double((p.units + slots - 1) / slots) * p.tiles_per_cta;
+                const double cost_mc = double((units2 + mc_slots - 1) / mc_slots) * tpc2 * 0.85;
+                if (cost_mc < cost_pair) {
+                    p.mc = true;
+                    p.tiles_per_cta = tpc2;
+                    p.n_groups = ng2;
+                    p.units = units2;
+                }
+            }
+        }
     } else {
         // one wave of units dealt the tiles round-robin
         const int total = p.n_mu * p.n_nt;
@@ -586,12 +629,12 @@ WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persi
     return p;
 }
 
-template <int EPI, int BN, bool PAIR, bool GT>
+template <int EPI, int BN, bool PAIR, bool GT, bool MC = false>
 cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tg, const WideArgs& a,
                         int grid, cudaStream_t stream) {
     const int brows = PAIR ? BN / 2 : BN;
     const size_t smem = wide_smem(a.nstages, a.kbox, EPI, a.K, brows) + 1024;
-    auto kernel = gemm_wide_kernel<EPI, BN, PAIR, GT>;
+    auto kernel = gemm_wide_kernel<EPI, BN, PAIR, GT, MC>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -601,7 +644,7 @@ cudaError_t launch_wide(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = PAIR ? 2u : 1u;
+    attr[0].val.clusterDim.x = MC ? 4u : (PAIR ? 2u : 1u);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -616,12 +659,52 @@ cudaError_t launch_plan(const WidePlan& p, const CUtensorMap& ta, const CUtensor
                         const WideArgs& a, cudaStream_t stream) {
     const int grid = (p.pair ? 2 : 1) * p.units;
     if constexpr (EPI == EPI_TOPK) {
-        if (a.n_gt > 0)
+        // clusters of two pairs on consecutive position tiles of one vocabulary range
+        // (the units of a range are consecutive: an even number of pairs keeps every
+        // cluster inside one range)
+        const bool mc = p.mc;
+        if (a.n_gt > 0) {
+            if (mc) return launch_wide<EPI, 256, true, true, true>(ta, tb, tg, a, grid, stream);
             return p.pair ? launch_wide<EPI, 256, true, true>(ta, tb, tg, a, grid, stream)
                           : launch_wide<EPI, 256, false, true>(ta, tb, tg, a, grid, stream);
+        }
+        if (mc) return launch_wide<EPI, 256, true, false, true>(ta, tb, tg, a, grid, stream);
     }
     return p.pair ? launch_wide<EPI, 256, true, false>(ta, tb, tg, a, grid, stream)
                   : launch_wide<EPI, 256, false, false>(ta, tb, tg, a, grid, stream);
+}
+
+int mc_cluster_slots(int K, int nstages) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const std::pair<int, int> key{dev, (K << 8) | nstages};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const size_t smem = wide_smem(nstages, 1, EPI_TOPK, K, 128) + 1024;
+    auto kernel = gemm_wide_kernel<EPI_TOPK, 256, true, false, true>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(4);
+        cfg.blockDim = dim3(kWideThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 4;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
+    return n;
 }
 
 }  // namespace

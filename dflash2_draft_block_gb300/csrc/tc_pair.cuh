@@ -73,6 +73,18 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
         : "memory");
 }
 
+// tma_load_2d_pair multicast to the CTAs of cta_mask (same shared-memory offset in
+// each): bar_cluster is the issuing CTA's pair-leader barrier, and every destination
+// CTA's bytes complete on the barrier at that offset in the leader of its own pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                    uint16_t cta_mask, int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster.L2::cache_hint [%0], [%1, {%4, %5}], [%2], %3, %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "h"(cta_mask), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 // TMEM allocation of a CTA pair: one warp of each CTA executes these together.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

@@ -96,6 +96,9 @@ def test_head_shapes(orc, df2, P, D, V, K):
     (130, 128, 513, 1),       # K = 1
     (257, 64, 300, 33),       # three M tiles, K just above one register row
     (48, 512, 5000, 16),      # just above the few-position path
+    # an even number of 256-position pairs: clusters of two pairs share the W_lm tiles
+    (512, 256, 7001, 16),     # two pairs, ragged V
+    (1000, 128, 4000, 64),    # four pairs, the last one ragged, K = 64
 ])
 def test_head_many_positions(orc, df2, P, D, V, K):
     rng = _rng(P * 131 + D + V * 7 + K)
@@ -112,6 +115,7 @@ def test_head_many_positions(orc, df2, P, D, V, K):
     (256, 192, 19600, 8, 256),    # CTA pairs, G exactly one tile wide
     (48, 128, 39000, 16, 24),     # one CTA per M tile
     (200, 256, 19600, 16, 264),   # G wider than one tile: a store launch of its own
+    (512, 256, 19600, 16, 40),    # two pairs sharing W_lm tiles, G in the top-K launch
 ])
 def test_head_many_positions_with_H(orc, df2, P, D, V, K, r):
     rng = _rng(P * 17 + V + r)
