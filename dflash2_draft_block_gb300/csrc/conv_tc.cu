@@ -31,6 +31,9 @@
 // decide together, at a barrier that ORs their wait results, whether to go on.
 #include <cudaTypedefs.h>
 
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_pair.cuh"
@@ -194,7 +197,12 @@ __device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, 
     }
 }
 
-template <int TAPS, bool PAIR>
+// MC (with PAIR): clusters of two pairs on consecutive 256-row tiles and one group
+// tile; the first pair loads the W_proj boxes once, multicast to the CTA of the same
+// pair rank in the other pair, and a stage is free again when both pairs' MMAs have
+// read it.  The units are then clusters: cluster step c + k * n_units covers row
+// tiles (pair units) 2 mg and 2 mg + 1 of group tile gt, numbered gt-fastest.
+template <int TAPS, bool PAIR, bool MC = false>
 __global__ void __launch_bounds__(kCtcThreads, 1)
 conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const ConvTcArgs a) {
@@ -219,15 +227,20 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bid = int(blockIdx.x);
-    const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+    const uint32_t crank = PAIR ? tc::cluster_ctarank() : 0u;
+    const uint32_t rank = crank & 1u;        // rank inside the CTA pair
+    const uint32_t lead_rank = crank & ~1u;  // cluster rank of this CTA's pair leader
+    const int pp = int(crank >> 1);          // MC: which pair of the cluster
     const bool leader = rank == 0;
-    const int unit = PAIR ? bid >> 1 : bid;
+    const int unit = MC ? bid >> 2 : (PAIR ? bid >> 1 : bid);
     // tiles numbered group-tile fastest, dealt round-robin to the units: at every
     // step the units work on consecutive tiles, which share their x rows in L2
-    const int total = a.n_mu * a.n_gt;
+    const int n_rows_units = MC ? (a.n_mu + 1) / 2 : a.n_mu;
+    const int total = n_rows_units * a.n_gt;
     const int ntiles = unit < total ? (total - unit + a.n_units - 1) / a.n_units : 0;
     auto tile_mt = [&](int k) {
-        const int mu = (unit + k * a.n_units) / a.n_gt;
+        const int mu0 = (unit + k * a.n_units) / a.n_gt;
+        const int mu = MC ? 2 * mu0 + pp : mu0;
         return PAIR ? 2 * mu + int(rank) : mu;
     };
     auto tile_gt = [&](int k) { return (unit + k * a.n_units) % a.n_gt; };
@@ -236,7 +249,7 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
+            tc::mbar_init(&empty[s], MC ? 2 : 1);  // MC: both pairs' MMAs release a stage
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&tfull[b], 1);
@@ -286,12 +299,22 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                     uint8_t* st = stages + size_t(stage) * stage_bytes;
                     const int xk = kb * CK;
                     if (PAIR) {
-                        const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), 0);
+                        const uint32_t fb = tc::mapa_shared(tc::smem_u32(&full[stage]), lead_rank);
                         tc::tma_load_2d_pair(st, &tm_x, fb, xk, mt * CM, pol_x);
+                        if (MC) {
+                            // the first pair loads the W_proj boxes for both pairs
+                            const uint16_t mask = uint16_t((1u << crank) | (1u << (crank + 2)));
+                            if (pp == 0)
 #pragma unroll
-                        for (int j = 0; j < TAPS; ++j)
-                            tc::tma_load_2d_pair(st + kXBox + size_t(j) * ng * CK * 2, &tm_w, fb, xk,
-                                                 (int(rank) * TAPS + j) * a.G + g0, pol_w);
+                                for (int j = 0; j < TAPS; ++j)
+                                    tc::tma_load_2d_pair_mc(st + kXBox + size_t(j) * ng * CK * 2, &tm_w, fb, mask, xk,
+                                                            (int(rank) * TAPS + j) * a.G + g0, pol_w);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < TAPS; ++j)
+                                tc::tma_load_2d_pair(st + kXBox + size_t(j) * ng * CK * 2, &tm_w, fb, xk,
+                                                     (int(rank) * TAPS + j) * a.G + g0, pol_w);
+                        }
                     } else {
                         tc::tma_load_2d(st, &tm_x, &full[stage], xk, mt * CM, pol_x);
 #pragma unroll
@@ -339,16 +362,16 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                         if (PAIR) tc::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
                         else tc::mma_bf16(d_tmem, ad, bd, idesc, acc);
                     }
-                    if (PAIR) tc::mma_commit_pair(&empty[stage], 0x3);
+                    if (PAIR) tc::mma_commit_pair(&empty[stage], MC ? 0xF : 0x3);
                     else tc::mma_commit(&empty[stage]);
                     if (++stage == nstages) { stage = 0; phase ^= 1; }
                 }
                 if (ok) {
-                    if (PAIR) tc::mma_commit_pair(&tfull[b], 0x3);
+                    if (PAIR) tc::mma_commit_pair(&tfull[b], uint16_t(0x3u << lead_rank));
                     else tc::mma_commit(&tfull[b]);
                 }
             }
-            if (PAIR) tc::mma_commit_pair(mma_done, 0x3);
+            if (PAIR) tc::mma_commit_pair(mma_done, uint16_t(0x3u << lead_rank));
             else tc::mma_commit(mma_done);
             volatile int never = 0;
             tc::mbar_wait(mma_done, 0, &never);
@@ -400,7 +423,7 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             if (lane == 0) {
                 // the accumulator is free for the tile after next; PAIR: CTA 0's MMA
                 // thread waits for both CTAs' epilogues
-                if (PAIR) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&tempty[b]), 0));
+                if (PAIR) tc::mbar_arrive_cluster(tc::mapa_shared(tc::smem_u32(&tempty[b]), lead_rank));
                 else tc::mbar_arrive(&tempty[b]);
             }
             tc::named_barrier(1, kCtcEpi);  // every row's corrections are staged
@@ -453,15 +476,22 @@ bool ctc_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int b
 struct CtcPlan {
     bool ok = false;
     bool pair = false;
+    bool mc = false;    // clusters of two pairs sharing the W_proj boxes
     int ng = 0, n_gt = 0, n_mu = 0, units = 0, nstages = 0, ds_ld = 0;
 };
+
+// Clusters of two pairs of this kernel that fit at once (occupancy API), cached per
+// device and launch shape; 0 when the query fails.
+int ctc_mc_slots(int taps, size_t smem);
 
 // Groups per tile: a divisor of G that is a multiple of 8 (each W_proj box then
 // fills whole 1024-byte swizzle atoms) with 2*taps*ng <= 256 (the MMA's N and one
 // TMEM buffer), chosen by a model of the time: rounds of tiles over the units,
-// times the bytes a CTA stages per tile (its 128 x rows and its W_proj rows).
-// Measured at the training-packed shape, a tile's time follows those L2 bytes,
-// not its MMA work: N = 256 ran 136 us and N = 160 161 us without the apply.
+// times the bytes a CTA stages per tile from L2 (its 128 x rows and its W_proj
+// rows; half the W_proj rows on average in clusters of two pairs, whose first pair
+// loads them for both).  Measured at the training-packed shape, a tile's time
+// follows those L2 bytes, not its MMA work: N = 256 ran 136 us and N = 160 161 us
+// without the apply.
 CtcPlan ctc_plan(int64_t P, int C, int B, int taps, int g, int num_sms) {
     CtcPlan best;
     if (taps < 1 || taps > 4 || g < 1 || C % g != 0 || C % 8 != 0 || B < 1 || CM % B != 0 || P % B != 0)
@@ -490,6 +520,7 @@ CtcPlan ctc_plan(int64_t P, int C, int B, int taps, int g, int num_sms) {
             best_cost = cost;
             best.ok = true;
             best.pair = pair;
+            best.mc = false;
             best.ng = ng;
             best.n_gt = n_gt;
             best.n_mu = n_mu;
@@ -497,24 +528,45 @@ CtcPlan ctc_plan(int64_t P, int C, int B, int taps, int g, int num_sms) {
             best.nstages = st;
             best.ds_ld = ds_ld;
         }
+        if (pair && n_mu % 2 == 0) {
+            const int mc_slots = ctc_mc_slots(taps, ctc_smem(st, taps, ng, true, ds_ld) + 1024);
+            if (mc_slots > 0) {
+                const int64_t total2 = int64_t(n_mu / 2) * n_gt;
+                const int units2 = int(total2 < mc_slots ? total2 : mc_slots);
+                const int64_t rounds2 = (total2 + units2 - 1) / units2;
+                const double cost2 = double(rounds2) * (CM + 0.5 * double(ctc_b_rows(taps, ng, true)));
+                if (cost2 < best_cost) {
+                    best_cost = cost2;
+                    best.ok = true;
+                    best.pair = true;
+                    best.mc = true;
+                    best.ng = ng;
+                    best.n_gt = n_gt;
+                    best.n_mu = n_mu;
+                    best.units = units2;
+                    best.nstages = st;
+                    best.ds_ld = ds_ld;
+                }
+            }
+        }
     }
     return best;
 }
 
-template <int TAPS, bool PAIR>
+template <int TAPS, bool PAIR, bool MC = false>
 cudaError_t ctc_launch(const CUtensorMap& tx, const CUtensorMap& tw, const ConvTcArgs& a, cudaStream_t stream) {
     const size_t smem = ctc_smem(a.nstages, TAPS, a.ng, PAIR, a.ds_ld) + 1024;
-    auto kernel = conv_prepare_tc_kernel<TAPS, PAIR>;
+    auto kernel = conv_prepare_tc_kernel<TAPS, PAIR, MC>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned((PAIR ? 2 : 1) * a.n_units));
+    cfg.gridDim = dim3(unsigned((MC ? 4 : (PAIR ? 2 : 1)) * a.n_units));
     cfg.blockDim = dim3(kCtcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = PAIR ? 2u : 1u;
+    attr[0].val.clusterDim.x = MC ? 4u : (PAIR ? 2u : 1u);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -522,6 +574,51 @@ cudaError_t ctc_launch(const CUtensorMap& tx, const CUtensorMap& tw, const ConvT
     e = cudaLaunchKernelEx(&cfg, kernel, tx, tw, a);
     note_launch();
     return e;
+}
+
+template <int TAPS>
+int ctc_mc_slots_t(size_t smem) {
+    auto kernel = conv_prepare_tc_kernel<TAPS, true, true>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(4);
+    cfg.blockDim = dim3(kCtcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 4;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+int ctc_mc_slots(int taps, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int64_t>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const std::pair<int, int64_t> key{dev, int64_t(taps) << 32 | int64_t(smem)};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    switch (taps) {
+        case 1: n = ctc_mc_slots_t<1>(smem); break;
+        case 2: n = ctc_mc_slots_t<2>(smem); break;
+        case 3: n = ctc_mc_slots_t<3>(smem); break;
+        case 4: n = ctc_mc_slots_t<4>(smem); break;
+        default: n = 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
+    return n;
 }
 
 int ctc_num_sms() {
@@ -566,8 +663,10 @@ cudaError_t conv_prepare_tc_launch(const uint16_t* x, int64_t P, int C, int B, i
     a.nstages = p.nstages;
     a.ds_ld = p.ds_ld;
     switch (taps) {
-#define DF2_CTC(TP) \
-    case TP: return p.pair ? ctc_launch<TP, true>(tx, tw, a, stream) : ctc_launch<TP, false>(tx, tw, a, stream);
+#define DF2_CTC(TP)                                                                    \
+    case TP:                                                                           \
+        if (p.mc) return ctc_launch<TP, true, true>(tx, tw, a, stream);                \
+        return p.pair ? ctc_launch<TP, true>(tx, tw, a, stream) : ctc_launch<TP, false>(tx, tw, a, stream);
         DF2_CTC(1)
         DF2_CTC(2)
         DF2_CTC(3)
