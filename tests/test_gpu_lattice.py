@@ -85,6 +85,8 @@ def compare_sampled(gpu_path, gpu_score, ref_path, ref_score, ref_margin, what):
     (3, 2, 1, 500, 8),
     (5, 16, 17, 3000, 264),
     (4, 8, 64, 10000, 512),
+    (3, 6, 40, 7000, 200),    # 32 < K < 64 (N = 48), a ragged last rank slice
+    (2, 5, 33, 3000, 72),
     (2, 4, 100, 3000, 64),
     (1, 3, 1024, 5000, 16),
     (37, 8, 16, 5000, 256),
