@@ -60,7 +60,8 @@ PROFILES = {
     "batch1": ("head_skinny_kernel_batch1.md", ["head_tc.cu", "topk_warp.cuh", "tc_ptx.cuh", "common.cuh"]),
     "batched": ("gemm_wide_topk_batched.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
     "stress": ("gemm_wide_topk_stress.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
-    "conv": ("gemm_wide_store_conv.md", ["gemm_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
+    "conv": ("conv_prepare_tc_conv.md", ["conv_tc.cu", "tc_pair.cuh", "tc_ptx.cuh", "common.cuh"]),
+    "conv_finish": ("conv_apply_bulk_conv.md", ["conv.cu", "tc_ptx.cuh", "common.cuh"]),
 }
 
 
@@ -829,19 +830,20 @@ def conv_arm(args, w, rank, world, torch, df2, dist, device, conv, steps=None, w
         peaks, src = load_peaks()
         flops = 2.0 * w.P * w.C * (2 * w.taps * w.G)
         pk = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-        roof = {"kernel": "dflash2_conv_prepare call: the projection GEMM (gemm_wide_kernel, store epilogue) "
-                          "+ the conv apply", "bound": "tensor",
+        roof = {"kernel": "dflash2_conv_prepare call: conv_prepare_tc_kernel (the projection on the tensor cores, "
+                          "dyn_out and the conv apply in its epilogue; one launch)", "bound": "tensor",
                 "achieved": flops / (prep_us * 1e-6) / 1e12, "peak": pk, "unit": "TFLOP/s",
                 "algorithmic_flops": flops,
-                "traffic_note": "the call's time includes its apply kernel, so this understates the GEMM's rate; "
-                                "traffic is the projection GEMM's DRAM bytes per launch (ncu)"}
+                "traffic_note": "the kernel also applies the conv (x read again, y written), so its MMA rate is "
+                                "below the contraction's own; traffic is the kernel's DRAM bytes per launch (ncu)"}
         fractions(roof, src)
         roof["traffic"], roof["traffic_source"] = head_traffic(w.name)
         fb = conv_bytes(w, "finish")
-        roof_fin = {"kernel": "dflash2_conv_finish call: conv_apply_async_kernel", "bound": "hbm",
+        roof_fin = {"kernel": "dflash2_conv_finish call: conv_apply_bulk_kernel", "bound": "hbm",
                     "achieved": fb / (fin_us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "algorithmic_bytes": fb}
         fractions(roof_fin, src)
+        roof_fin["traffic"], roof_fin["traffic_source"] = head_traffic("conv_finish")
         out = {
             "metric": METRIC, "value": job_throughput(w.P, world, step_ms), "unit": "positions/s",
             "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": step_ms,
