@@ -431,9 +431,164 @@ __device__ __forceinline__ void pair_row_staged(int64_t row, bool pred_ok, const
     }
 }
 
-// Finishes the slot started by slot_stage_begin: best_j/best_v/best_id[i] for each
-// predecessor i < rows (rows = 1 and the anchor when pred_row < 0).  Returns false
-// when a predecessor id is out of range (the outputs are untouched).
+// Row t's unary values and candidate ids into the slot layout (vs, cs).
+__device__ __forceinline__ void slot_load_row(int64_t row, const int32_t* __restrict__ ids,
+                                              const float* __restrict__ vals, int K, int r, uint8_t* smem) {
+    float* vs = reinterpret_cast<float*>(smem + size_t(K) * 2 * r * 2 + size_t(r) * 4 + size_t(K) * K * 4);
+    int* cs = reinterpret_cast<int*>(vs + K);
+    for (int i = threadIdx.x; i < K; i += blockDim.x) {
+        vs[i] = __ldcg(vals + row * K + i);
+        cs[i] = __ldcg(ids + row * K + i);
+    }
+}
+
+// Scores slot t-1 from staged rows: the candidates' B rows and G (slot_stage_begin,
+// landed), row t's values and ids (slot_load_row, or slot_finish's own loads), and
+// the predecessors' A rows [rows][r] at As; best_j/best_v/best_id[i] for each
+// predecessor i < rows.  Starts with a CTA barrier (the staged rows are visible).
+template <int NCH>
+__device__ __forceinline__ void slot_score(int rows, int K, int r, uint8_t* smem, const uint16_t* As,
+                                           int* best_j, float* best_v, int* best_id) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+    const uint16_t* Bs = reinterpret_cast<const uint16_t*>(smem);
+    const float* Gs = reinterpret_cast<const float*>(Bs + size_t(2) * K * r);
+    float* Ls = const_cast<float*>(Gs) + r;    // [K][K]
+    const float* vs = Ls + size_t(K) * K;      // [K] unary values of row t
+    const int* cs = reinterpret_cast<const int*>(vs + K);  // [K] candidate ids of row t
+    __syncthreads();
+    const int jblocks = (K + 15) / 16;
+    const int n_items = rows * jblocks;
+    // the predecessor's gate slices, A[i] (.) G, in the walk's lane slicing
+    auto gate = [&](int i, float (&qv)[NCH][8]) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int i0 = c * 256 + lane * 8;
+            float af[8], gc[1][8];
+            load_gslice<1>(Gs + c * 256, r - c * 256, lane, gc);
+            if (i0 < r) {
+                unpack8(*reinterpret_cast<const uint4*>(As + size_t(i) * r + i0), af);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) af[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qv[c][e] = af[e] * gc[0][e];
+        }
+    };
+    bool paired = false;
+    if constexpr (NCH <= 2) {
+        // a warp scores items `item` and `item + nwarps` together (the same 16
+        // candidates when nwarps is a multiple of jblocks): each candidate slice is
+        // loaded once for both, and the two sets of fmaf chains hide each other's
+        // latency.  Every sum is formed as in the one-item loop below.
+        paired = nwarps % jblocks == 0;
+        for (int item = warp; paired && item < n_items; item += 2 * nwarps) {
+            const int itemb = item + nwarps;
+            const bool hasb = itemb < n_items;
+            const int i = item / jblocks, j0 = (item % jblocks) * 16;
+            const int ib = hasb ? itemb / jblocks : i;
+            float qa[NCH][8], qb[NCH][8];
+            gate(i, qa);
+            gate(ib, qb);
+            float pa[16], pb[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                pa[u] = 0.f;
+                pb[u] = 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                const int i0 = c * 256 + lane * 8;
+                uint4 raw[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int j = j0 + u < K ? j0 + u : j0;  // rows past K: loaded, not used
+                    raw[u] = i0 < r ? *reinterpret_cast<const uint4*>(Bs + size_t(j) * r + i0)
+                                    : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (j0 + u < K) {
+                        float bf[8];
+                        unpack8(raw[u], bf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            pa[u] = fmaf(qa[c][e], bf[e], pa[u]);
+                            pb[u] = fmaf(qb[c][e], bf[e], pb[u]);
+                        }
+                    }
+                }
+            }
+            const int u = reduce16_transpose(pa, lane);
+            if ((lane & 1) == 0 && j0 + u < K) Ls[size_t(i) * K + j0 + u] = vs[j0 + u] + pa[0];
+            if (hasb) {
+                const int ub = reduce16_transpose(pb, lane);
+                if ((lane & 1) == 0 && j0 + ub < K) Ls[size_t(ib) * K + j0 + ub] = vs[j0 + ub] + pb[0];
+            }
+        }
+    }
+    if (!paired) {
+        for (int item = warp; item < n_items; item += nwarps) {
+            const int i = item / jblocks, j0 = (item % jblocks) * 16;
+            float qv[NCH][8];
+            gate(i, qv);
+            float part[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                part[u] = 0.f;
+                if (j0 + u < K) {
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        float bf[1][8];
+                        load_bslice<1>(Bs + size_t(j0 + u) * r + c * 256, r - c * 256, lane, true, bf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) part[u] = fmaf(qv[c][e], bf[0][e], part[u]);
+                    }
+                }
+            }
+            const int u = reduce16_transpose(part, lane);
+            if ((lane & 1) == 0 && j0 + u < K) Ls[size_t(i) * K + j0 + u] = vs[j0 + u] + part[0];
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < rows; i += blockDim.x) {
+        float bv = -INFINITY;
+        int bid = INT_MAX, bj = -1;
+        if (K % 4 == 0) {
+            // the row in 16-byte pieces (fewer shared-memory wavefronts), same scan order
+            for (int j4 = 0; j4 < K; j4 += 4) {
+                const float4 v4 = *reinterpret_cast<const float4*>(Ls + size_t(i) * K + j4);
+                const int4 c4 = *reinterpret_cast<const int4*>(cs + j4);
+                const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+                const int cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (bj < 0 || ranks_before(vv[e], cc[e], bv, bid)) {
+                        bv = vv[e];
+                        bid = cc[e];
+                        bj = j4 + e;
+                    }
+            }
+        } else {
+            for (int j = 0; j < K; ++j) {
+                const float v = Ls[size_t(i) * K + j];
+                if (bj < 0 || ranks_before(v, cs[j], bv, bid)) {
+                    bv = v;
+                    bid = cs[j];
+                    bj = j;
+                }
+            }
+        }
+        best_j[i] = bj;
+        best_v[i] = bv;
+        best_id[i] = bid;
+    }
+}
+
+// Finishes the slot started by slot_stage_begin: fetches the predecessors' A rows
+// itself, then slot_score.  best_j/best_v/best_id[i] for each predecessor i < rows
+// (rows = 1 and the anchor when pred_row < 0).  Returns false when a predecessor id
+// is out of range (the outputs are untouched).
 template <int NCH>
 __device__ __forceinline__ bool slot_finish(int64_t row, int64_t pred_row, int32_t anchor,
                                             const int32_t* __restrict__ ids,
@@ -470,58 +625,7 @@ __device__ __forceinline__ bool slot_finish(int64_t row, int64_t pred_row, int32
     for (int i = warp; i < rows; i += nwarps)
         for (int c = lane; c < cpr; c += 32) cp_async16(As + size_t(i) * r + c * 8, A + int64_t(ps[i]) * r + c * 8);
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    const int jblocks = (K + 15) / 16;
-    for (int item = warp; item < rows * jblocks; item += nwarps) {
-        const int i = item / jblocks, j0 = (item % jblocks) * 16;
-        float qv[NCH][8];
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int i0 = c * 256 + lane * 8;
-            float af[8], gc[1][8];
-            load_gslice<1>(Gs + c * 256, r - c * 256, lane, gc);
-            if (i0 < r) {
-                unpack8(*reinterpret_cast<const uint4*>(As + size_t(i) * r + i0), af);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) af[e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qv[c][e] = af[e] * gc[0][e];
-        }
-        float part[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            part[u] = 0.f;
-            if (j0 + u < K) {
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    float bf[1][8];
-                    load_bslice<1>(Bs + size_t(j0 + u) * r + c * 256, r - c * 256, lane, true, bf);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) part[u] = fmaf(qv[c][e], bf[0][e], part[u]);
-                }
-            }
-        }
-        const int u = reduce16_transpose(part, lane);
-        if ((lane & 1) == 0 && j0 + u < K) Ls[size_t(i) * K + j0 + u] = vs[j0 + u] + part[0];
-    }
-    __syncthreads();
-    for (int i = tid; i < rows; i += blockDim.x) {
-        float bv = -INFINITY;
-        int bid = INT_MAX, bj = -1;
-        for (int j = 0; j < K; ++j) {
-            const float v = Ls[size_t(i) * K + j];
-            if (bj < 0 || ranks_before(v, cs[j], bv, bid)) {
-                bv = v;
-                bid = cs[j];
-                bj = j;
-            }
-        }
-        best_j[i] = bj;
-        best_v[i] = bv;
-        best_id[i] = bid;
-    }
+    slot_score<NCH>(rows, K, r, smem, As, best_j, best_v, best_id);
     return true;
 }
 
