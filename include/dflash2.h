@@ -243,7 +243,10 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
  *   out; pair_scores [R*B, K] fp32 out (required iff pred != NULL).
  *   workspace: dflash2_draft_head_workspace_size(R, B, D, V, K, r) bytes, 256-byte
  *   aligned (it holds the head's partial lists).
- * Rules: the union of the three calls' rules; B >= 2.  Status bits as those calls.
+ * Rules: the union of the three calls' rules; B >= 2.  Status bits as those calls;
+ * in the fused launch each CTA of a cluster waits (bounded, about one second) for
+ * the predecessor rows the previous CTA sends it, and a wait that gives up ORs
+ * DF2_STATUS_WAIT_TIMEOUT and fails that request's path like a bad id (-1 / NaN).
  * ---------------------------------------------------------------------- */
 size_t dflash2_draft_head_workspace_size(int R, int B, int64_t D, int64_t V, int K, int r);
 int dflash2_draft_head(const uint16_t* h, int R, int B, int64_t D, const uint16_t* W_lm, int64_t V,
