@@ -64,6 +64,8 @@ def separate(df2, x, status=None):
     (1, 16, 512, 20000, 64, 512),    # K = 64: the separate calls
     (2, 16, 512, 20000, 32, 512),    # K = 32, a 16-CTA cluster
     (2, 8, 520, 9001, 17, 264),      # ragged K, D and r
+    (2, 8, 256, 9000, 13, 128),      # K < 16 and not a multiple of 4
+    (2, 8, 256, 20000, 32, 1280),    # a slot's predecessor rows too large to send: the L2 prefetch path
     (16, 8, 256, 30000, 16, 256),    # 128 positions: the tensor-core GEMM head + fused tail
     (64, 8, 256, 20000, 16, 256),    # 512 positions: 64 clusters
 ])
