@@ -90,8 +90,11 @@ __device__ __forceinline__ void cluster_arrive() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-template <int R, int NCH>
-__global__ void __launch_bounds__(kTailThreads)
+// MINB: CTAs per SM the registers must allow.  1: the fast instance (a warp scores
+// two predecessor rows at once); 4: for launches with more clusters than the fast
+// instance holds at once, which then run in one wave instead of two.
+template <int R, int NCH, int MINB>
+__global__ void __launch_bounds__(kTailThreads, MINB)
 draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id, int S, int64_t P,
                   int K, int32_t* __restrict__ ids, float* __restrict__ vals,
                   const int32_t* __restrict__ anchors, int B, const float* __restrict__ G,
@@ -202,9 +205,9 @@ draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part
             const bool ok_in = __syncthreads_and(got && *in_bad == 0) != 0;
             if (!got && threadIdx.x == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_WAIT_TIMEOUT);
             slot_ok = staged && ok_in;
-            if (slot_ok) sel::slot_score<NCH>(t == 1 ? 1 : K, K, r, smem, in_rows, rj, rv, rid);
+            if (slot_ok) sel::slot_score<NCH, (MINB < 4)>(t == 1 ? 1 : K, K, r, smem, in_rows, rj, rv, rid);
         } else {
-            slot_ok = staged && sel::slot_finish<NCH>(p, t == 1 ? -1 : p - 1, __ldg(anchors + q), ids, vals, A,
+            slot_ok = staged && sel::slot_finish<NCH, (MINB < 4)>(p, t == 1 ? -1 : p - 1, __ldg(anchors + q), ids, vals, A,
                                                       V, K, r, smem, rj, rv, rid);
         }
         if (!slot_ok && threadIdx.x == 0) *cluster.map_shared_rank(tab_bad, 0) = 1;
@@ -245,13 +248,13 @@ draft_tail_kernel(const float* __restrict__ part_v, const int* __restrict__ part
     }
 }
 
-template <int R, int N>
+template <int R, int N, int MINB>
 cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, const TopkParts& parts, int K,
                         int32_t* ids, float* vals, const int32_t* anchors, const float* G,
                         const uint16_t* A, const uint16_t* Bc, int64_t V, int r, int32_t* path,
                         float* path_scores, const int32_t* pred, float* pair_scores, int32_t* dev_status,
-                        LogitMap lm, Refine rf, bool probe_only, bool* fits) {
-    auto kernel = draft_tail_kernel<R, N>;
+                        LogitMap lm, Refine rf, bool probe_only, bool* fits, int* max_clusters) {
+    auto kernel = draft_tail_kernel<R, N, MINB>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     if (B > 8) {
@@ -274,6 +277,7 @@ cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, cons
         int clusters = 0;
         e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
         *fits = e == cudaSuccess && clusters > 0;
+        if (max_clusters) *max_clusters = e == cudaSuccess ? clusters : 0;
         return e;
     }
     const unsigned push_off = tail_push_fits(B, K, r, parts.S) ? unsigned(tail_push_off(B, K, r, parts.S)) : 0u;
@@ -283,25 +287,31 @@ cudaError_t launch_tail(int64_t P, int B, size_t smem, cudaStream_t stream, cons
 }
 
 // Runs (or, probe_only, checks that the cluster shape can run) the right instance.
+// many: the launch has more clusters than the fast instance holds at once.
 cudaError_t dispatch_tail(bool probe_only, bool* fits, const TopkParts& parts, int64_t P, int K, int32_t* ids,
                           float* vals, const int32_t* anchors, int B, const float* G, const uint16_t* A,
                           const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
                           const int32_t* pred, float* pair_scores, int32_t* dev_status, LogitMap lm,
-                          Refine rf, cudaStream_t stream) {
+                          Refine rf, cudaStream_t stream, bool many = false, int* max_clusters = nullptr) {
     const size_t smem = tail_push_fits(B, K, r, parts.S) ? tail_push_smem(B, K, r, parts.S)
                                                           : tail_smem(B, K, r, parts.S);
     const int nch = (r + 255) / 256;
     cudaError_t e = cudaSuccess;
-#define DF2_TAIL(RV, N)                                                                                \
-    e = launch_tail<RV, N>(P, B, smem, stream, parts, K, ids, vals, anchors, G, A, Bc, V, r, path,     \
-                           path_scores, pred, pair_scores, dev_status, lm, rf, probe_only, fits)
-#define DF2_TAIL_N(RV)                        \
-    do {                                      \
-        if (nch <= 1) DF2_TAIL(RV, 1);        \
-        else if (nch <= 2) DF2_TAIL(RV, 2);   \
-        else if (nch <= 4) DF2_TAIL(RV, 4);   \
-        else if (nch <= 8) DF2_TAIL(RV, 8);   \
-        else DF2_TAIL(RV, 16);                \
+#define DF2_TAIL(RV, N, MB)                                                                            \
+    e = launch_tail<RV, N, MB>(P, B, smem, stream, parts, K, ids, vals, anchors, G, A, Bc, V, r, path, \
+                               path_scores, pred, pair_scores, dev_status, lm, rf, probe_only, fits,    \
+                               max_clusters)
+#define DF2_TAIL_N(RV)                                         \
+    do {                                                       \
+        if (nch <= 1) {                                        \
+            if (many) DF2_TAIL(RV, 1, 4);                      \
+            else DF2_TAIL(RV, 1, 1);                           \
+        } else if (nch <= 2) {                                 \
+            if (many) DF2_TAIL(RV, 2, 4);                      \
+            else DF2_TAIL(RV, 2, 1);                           \
+        } else if (nch <= 4) DF2_TAIL(RV, 4, 1);               \
+        else if (nch <= 8) DF2_TAIL(RV, 8, 1);                 \
+        else DF2_TAIL(RV, 16, 1);                              \
     } while (0)
     if (K <= 32) DF2_TAIL_N(1);
     else DF2_TAIL_N(2);
@@ -312,6 +322,7 @@ cudaError_t dispatch_tail(bool probe_only, bool* fits, const TopkParts& parts, i
 
 std::mutex g_fit_mu;
 std::unordered_map<uint64_t, bool> g_fit;  // cluster-shape probe results
+std::unordered_map<uint64_t, int> g_clusters;  // clusters at once per instance (key | many)
 
 }  // namespace
 
@@ -346,14 +357,47 @@ bool draft_tail_supported(int64_t P, int B, int K, int r, int S, int num_sms) {
     return fits;
 }
 
+// Clusters of the fast (many = false) or the four-CTAs-per-SM instance that fit at
+// once for this shape, from the occupancy query, cached per device and shape.
+int tail_max_clusters(int S, int K, int B, int r, bool many) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const size_t smem = tail_push_fits(B, K, r, S) ? tail_push_smem(B, K, r, S) : tail_smem(B, K, r, S);
+    const uint64_t key = (uint64_t(unsigned(dev)) << 48) ^ (uint64_t(B) << 40) ^ (uint64_t(many) << 38) ^
+                         (uint64_t(K <= 32) << 37) ^ (uint64_t((r + 255) / 256) << 32) ^ uint64_t(smem);
+    {
+        std::lock_guard<std::mutex> lock(g_fit_mu);
+        auto it = g_clusters.find(key);
+        if (it != g_clusters.end()) return it->second;
+    }
+    bool fits = false;
+    int clusters = 0;
+    const TopkParts probe{nullptr, nullptr, S};
+    static const uint16_t probe_row = 0;
+    if (dispatch_tail(true, &fits, probe, B, K, nullptr, nullptr, nullptr, B, nullptr, nullptr, nullptr, 1, r,
+                      nullptr, nullptr, nullptr, nullptr, nullptr, LogitMap{}, Refine{&probe_row, nullptr, 0},
+                      nullptr, many, &clusters) != cudaSuccess)
+        clusters = 0;
+    std::lock_guard<std::mutex> lock(g_fit_mu);
+    g_clusters[key] = clusters;
+    return clusters;
+}
+
 cudaError_t draft_tail_launch(const TopkParts& parts, int64_t P, int K, int32_t* ids, float* vals,
                               const int32_t* anchors, int B, const float* G, const uint16_t* A,
                               const uint16_t* Bc, int64_t V, int r, int32_t* path, float* path_scores,
                               const int32_t* pred, float* pair_scores, int32_t* dev_status,
                               cudaStream_t stream, LogitMap lm, Refine rf) {
+    // more clusters than the fast instance holds at once: the instance that fits
+    // four CTAs per SM, if that holds more (one-row scoring, lower register count)
+    bool many = false;
+    if ((r + 255) / 256 <= 2) {
+        const int fast = tail_max_clusters(parts.S, K, B, r, false);
+        if (P / B > fast) many = tail_max_clusters(parts.S, K, B, r, true) > fast;
+    }
     bool unused = false;
     const cudaError_t e = dispatch_tail(false, &unused, parts, P, K, ids, vals, anchors, B, G, A, Bc, V, r, path,
-                                        path_scores, pred, pair_scores, dev_status, lm, rf, stream);
+                                        path_scores, pred, pair_scores, dev_status, lm, rf, stream, many);
     note_launch();
     return e;
 }

@@ -446,7 +446,8 @@ __device__ __forceinline__ void slot_load_row(int64_t row, const int32_t* __rest
 // landed), row t's values and ids (slot_load_row, or slot_finish's own loads), and
 // the predecessors' A rows [rows][r] at As; best_j/best_v/best_id[i] for each
 // predecessor i < rows.  Starts with a CTA barrier (the staged rows are visible).
-template <int NCH>
+// PAIRS: a warp may score two predecessor rows at once (more registers).
+template <int NCH, bool PAIRS = true>
 __device__ __forceinline__ void slot_score(int rows, int K, int r, uint8_t* smem, const uint16_t* As,
                                            int* best_j, float* best_v, int* best_id) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
@@ -476,7 +477,7 @@ __device__ __forceinline__ void slot_score(int rows, int K, int r, uint8_t* smem
         }
     };
     bool paired = false;
-    if constexpr (NCH <= 2) {
+    if constexpr (NCH <= 2 && PAIRS) {
         // a warp scores items `item` and `item + nwarps` together (the same 16
         // candidates when nwarps is a multiple of jblocks): each candidate slice is
         // loaded once for both, and the two sets of fmaf chains hide each other's
@@ -589,7 +590,7 @@ __device__ __forceinline__ void slot_score(int rows, int K, int r, uint8_t* smem
 // itself, then slot_score.  best_j/best_v/best_id[i] for each predecessor i < rows
 // (rows = 1 and the anchor when pred_row < 0).  Returns false when a predecessor id
 // is out of range (the outputs are untouched).
-template <int NCH>
+template <int NCH, bool PAIRS = true>
 __device__ __forceinline__ bool slot_finish(int64_t row, int64_t pred_row, int32_t anchor,
                                             const int32_t* __restrict__ ids,
                                             const float* __restrict__ vals,
@@ -625,7 +626,7 @@ __device__ __forceinline__ bool slot_finish(int64_t row, int64_t pred_row, int32
     for (int i = warp; i < rows; i += nwarps)
         for (int c = lane; c < cpr; c += 32) cp_async16(As + size_t(i) * r + c * 8, A + int64_t(ps[i]) * r + c * 8);
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-    slot_score<NCH>(rows, K, r, smem, As, best_j, best_v, best_id);
+    slot_score<NCH, PAIRS>(rows, K, r, smem, As, best_j, best_v, best_id);
     return true;
 }
 
