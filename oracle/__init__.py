@@ -77,6 +77,7 @@ class Oracle:
         L.df2o_selector_walk.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp, vp, vp]
         L.df2o_selector_pair_scores.argtypes = [vp, i64, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp]
         L.df2o_selector_lattice.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i64, i32, i32, vp, vp]
+        L.df2o_selector_ce.argtypes = [vp, vp, vp, i64, i32, i64, vp, vp, vp]
         L.df2o_lattice_walk.argtypes = [vp, vp, i32, i32, i32, i64, vp, ct.c_double, vp, vp, vp, vp]
         L.df2o_conv_prepare.argtypes = [vp, ct.c_int, i64, i32, i32, i32, i32, vp, vp, vp, vp]
         L.df2o_conv_finish.argtypes = [vp, ct.c_int, i64, i32, i32, i32, i32, vp, vp, vp]
@@ -84,7 +85,7 @@ class Oracle:
                                                vp, vp]
         for f in ("df2o_logits", "df2o_unary_topk", "df2o_selector_walk",
                   "df2o_selector_pair_scores", "df2o_conv_prepare", "df2o_conv_finish",
-                  "df2o_conv_finish_prepare"):
+                  "df2o_conv_finish_prepare", "df2o_selector_ce"):
             getattr(L, f).restype = ct.c_int
 
     def num_threads(self) -> int:
@@ -167,6 +168,19 @@ class Oracle:
         self._check(self.lib.df2o_selector_pair_scores(_p(pred), P, _p(ids), _p(vals), _p(G), _p(A),
                                                        _p(Bc), V, K, r, _p(scores), _p(status)))
         return scores, int(status[0])
+
+    def selector_ce(self, scores, ids, targets, V):
+        """scores/ids [P,K], targets [P]; returns (loss [P] f32, label_idx [P] int32, status)."""
+        scores, ids, targets = _c(scores, np.float32), _c(ids, np.int32), _c(targets, np.int32)
+        P = targets.shape[0]
+        K = ids.shape[-1]
+        assert ids.size == P * K and scores.size == P * K
+        loss = np.empty((P,), np.float32)
+        label = np.empty((P,), np.int32)
+        status = np.zeros((1,), np.int32)
+        self._check(self.lib.df2o_selector_ce(_p(scores), _p(ids), _p(targets), P, K, int(V), _p(loss),
+                                              _p(label), _p(status)))
+        return loss, label, int(status[0])
 
     def lattice(self, anchors, ids, vals, G, A, Bc, block_size):
         """ids/vals [R*B, K], G [R*B, r]; returns (lattice [R, B-1, K, K] f32, status)."""

@@ -21,6 +21,10 @@
  *                   PR #62, "Selector training objective")
  *   teacher-forced  the same score with the predecessor given, all positions at
  *                   once (PR #62, "Selector training objective")
+ *   selector loss   the K-way cross-entropy of the teacher-forced scores against
+ *                   the ground truth, on rows whose ground truth is a candidate
+ *                   (PR #62, "Selector training objective"; vLLM guide,
+ *                   "Training Objective")
  *   lattice         every adjacent candidate pair scored at once, then a greedy or
  *                   sampling walk over the finished table ("DFlash 2 Explanation",
  *                   "How It Works", Problem 1)
@@ -321,6 +325,53 @@ int df2o_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* ids
             }
             scores[p * K + j] = pair_score(vals[p * K + j], a, b, G + p * r, A, Bc, r);
         }
+    }
+    if (status) *status = bad;
+    return DF2O_OK;
+}
+
+/*
+ * The selector's training loss, forward (verl-SpeCo PR #62, "Selector training
+ * objective": a cross-entropy over the drafter's own top-K candidates with the
+ * predecessor teacher-forced, counted only on rows whose ground truth is among
+ * those candidates; vLLM Speculators "DFlash2" guide, "Training Objective": the
+ * K-way hard cross-entropy over the unary top-K candidates).  Row p holds the
+ * teacher-forced scores S[p, 0..K-1] of its candidates ids[p, .] and the ground
+ * truth y = targets[p]:
+ *     label_idx[p] = the column j with ids[p, j] == y, else -1
+ *     loss[p]      = log(sum_j exp(S[p, j])) - S[p, label_idx[p]]   (NaN when -1)
+ * in double; the sum is taken after subtracting the row's largest score, which
+ * leaves the value unchanged and keeps exp in range.  y < 0 means the row has no
+ * target; y >= V sets bit 1 of *status (label -1, loss NaN).
+ */
+int df2o_selector_ce(const float* scores, const int32_t* ids, const int32_t* targets, int64_t P, int32_t K,
+                     int64_t V, float* loss, int32_t* label_idx, int32_t* status)
+{
+    if (P < 0 || K < 1 || V < 1) return DF2O_INVALID;
+    int32_t bad = 0;
+    int64_t p;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (p = 0; p < P; ++p) {
+        const int32_t y = targets[p];
+        int32_t js = -1;
+        if (y >= V) bad |= 1;
+        if (y >= 0 && y < V)
+            for (int32_t j = 0; j < K; ++j)
+                if (ids[p * K + j] == y) {
+                    js = j;
+                    break;
+                }
+        label_idx[p] = js;
+        if (js < 0) {
+            loss[p] = NAN;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int32_t j = 0; j < K; ++j)
+            if ((double)scores[p * K + j] > m) m = (double)scores[p * K + j];
+        double sum = 0.0;
+        for (int32_t j = 0; j < K; ++j) sum += exp((double)scores[p * K + j] - m);
+        loss[p] = (float)(log(sum) + m - (double)scores[p * K + js]);
     }
     if (status) *status = bad;
     return DF2O_OK;

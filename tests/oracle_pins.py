@@ -287,6 +287,82 @@ def pin_pair_scores_golden(o):
     assert scores.tolist() == g["teacher_forced_scores"]
 
 
+# ---------------------------------------------------------------- selector CE --
+# The selector's K-way cross-entropy of teacher-forced scores against the ground
+# truth, on rows whose ground truth is a candidate (verl-SpeCo PR #62, "Selector
+# training objective"; vLLM Speculators "DFlash2" guide, "Training Objective").
+
+def pin_ce_single_candidate_is_zero(o):
+    """With one candidate that is the target, the cross-entropy is exactly 0."""
+    scores = np.array([[3.5], [-7.25], [0.0]], np.float32)
+    ids = np.array([[4], [9], [2]], np.int32)
+    loss, label, st = o.selector_ce(scores, ids, np.array([4, 9, 2], np.int32), 10)
+    assert st == 0 and label.tolist() == [0, 0, 0]
+    assert loss.tolist() == [0.0, 0.0, 0.0]
+
+
+def pin_ce_uniform_scores_is_log_k(o):
+    """Equal scores over K candidates: the softmax is uniform, the loss is ln K."""
+    for K in (2, 3, 16, 64, 1000):
+        for c in (-5.0, 0.0, 12.5):
+            scores = np.full((1, K), c, np.float32)
+            ids = np.arange(K, dtype=np.int32)[None] * 3
+            loss, label, _ = o.selector_ce(scores, ids, np.array([3 * (K // 2)], np.int32), 3 * K)
+            assert label[0] == K // 2
+            assert abs(float(loss[0]) - math.log(K)) <= 1e-6 * math.log(K), (K, c, loss[0])
+
+
+def pin_ce_two_candidates_is_softplus(o):
+    """K = 2: -log sigmoid(s_label - s_other) = softplus(s_other - s_label)."""
+    rng = _rng("ce_two")
+    for _ in range(50):
+        a, b = (rng.standard_normal(2) * 6).astype(np.float32)
+        loss, label, _ = o.selector_ce(np.array([[a, b]], np.float32), np.array([[7, 1]], np.int32),
+                                       np.array([1], np.int32), 8)
+        d = float(a) - float(b)
+        want = d + math.log1p(math.exp(-d)) if d > 0 else math.log1p(math.exp(d))
+        assert label[0] == 1 and abs(float(loss[0]) - want) <= 1e-6 * max(1.0, want), (a, b, loss[0], want)
+
+
+def pin_ce_hand_worked(o):
+    """Scores 1, 2, 3, 4 with the target in the second column:
+    log(e + e^2 + e^3 + e^4) - 2 = 2 + log(1 + e^-1 + e^-2 + e^-3)."""
+    loss, label, _ = o.selector_ce(np.array([[1, 2, 3, 4]], np.float32), np.array([[10, 20, 30, 40]], np.int32),
+                                   np.array([20], np.int32), 50)
+    want = 2.0 + math.log(1.0 + math.exp(-1.0) + math.exp(-2.0) + math.exp(-3.0))
+    assert label[0] == 1 and abs(float(loss[0]) - want) <= 1e-6
+
+
+def pin_ce_invariances(o):
+    """A constant added to a row's scores leaves its loss unchanged; permuting the
+    candidates (ids with their scores) leaves it unchanged and moves the label."""
+    rng = _rng("ce_inv")
+    P, K, V = 20, 16, 500
+    scores = rng.integers(-40, 40, size=(P, K)).astype(np.float32) / 4
+    ids = np.stack([rng.choice(V, size=K, replace=False) for _ in range(P)]).astype(np.int32)
+    targets = ids[np.arange(P), rng.integers(0, K, size=P)]
+    loss, label, _ = o.selector_ce(scores, ids, targets, V)
+    loss2, label2, _ = o.selector_ce(scores + 64.0, ids, targets, V)  # exact in fp32
+    assert np.array_equal(label, label2) and np.allclose(loss, loss2, rtol=1e-6, atol=1e-6)
+    perm = rng.permutation(K)
+    loss3, label3, _ = o.selector_ce(scores[:, perm], ids[:, perm], targets, V)
+    assert np.allclose(loss, loss3, rtol=1e-6, atol=1e-6)
+    assert np.array_equal(perm[label3], label)
+    assert np.all(loss >= 0)  # -log of a probability
+
+
+def pin_ce_rows_without_a_candidate_target(o):
+    """A target outside the row's candidates (or no target, < 0) contributes nothing:
+    label -1 and NaN loss, no status; a target id >= V is also flagged."""
+    scores = np.zeros((4, 3), np.float32)
+    ids = np.array([[1, 2, 3]] * 4, np.int32)
+    loss, label, st = o.selector_ce(scores, ids, np.array([5, -1, 2, 3], np.int32), 10)
+    assert label.tolist() == [-1, -1, 1, 2] and st == 0
+    assert np.isnan(loss[0]) and np.isnan(loss[1]) and loss[2] == loss[3]
+    loss, label, st = o.selector_ce(scores, ids, np.array([10, 1, 1, 1], np.int32), 10)
+    assert st & 1 and label[0] == -1 and np.isnan(loss[0]) and label[1] == 0
+
+
 def _random_lattice(tag, R, B, K, V, r, cb_std=1.0, G_std=1.0):
     rng = _rng(tag)
     ids = np.stack([np.stack([rng.choice(V, size=K, replace=False) for _ in range(B)]) for _ in range(R)])

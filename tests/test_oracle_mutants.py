@@ -86,6 +86,16 @@ MUTANTS = [
      "return df2o_conv_prepare(h, is_f32,", "return df2o_conv_prepare(z, is_f32,"),
     ("finish_prepare_next_uses_same_base",
      "W_proj, base_next, y_next, dyn_next);", "W_proj, base, y_next, dyn_next);"),
+    ("ce_sign_flip",
+     "loss[p] = (float)(log(sum) + m - (double)scores[p * K + js]);",
+     "loss[p] = (float)(log(sum) + m + (double)scores[p * K + js]);"),
+    ("ce_max_shift_not_restored",
+     "loss[p] = (float)(log(sum) + m - (double)scores[p * K + js]);",
+     "loss[p] = (float)(log(sum) - (double)scores[p * K + js]);"),
+    ("ce_label_is_the_best_column",
+     "                if (ids[p * K + j] == y) {", "                if (scores[p * K + j] >= scores[p * K] && ids[p * K + j] != -7) {"),
+    ("ce_uncovered_rows_count_zero", "            loss[p] = NAN;\n            continue;", "            loss[p] = 0.0f;\n            continue;"),
+    ("ce_sum_skips_last", "        for (int32_t j = 0; j < K; ++j) sum += exp(", "        for (int32_t j = 0; j + 1 < K; ++j) sum += exp("),
 ]
 
 

@@ -11,5 +11,5 @@ def test_pin(orc, pin):
 
 def test_every_oracle_function_is_pinned():
     names = {p.__name__ for p in oracle_pins.ALL_PINS}
-    for prefix in ("pin_logits", "pin_topk", "pin_walk", "pin_pair", "pin_conv"):
+    for prefix in ("pin_logits", "pin_topk", "pin_walk", "pin_pair", "pin_conv", "pin_ce"):
         assert any(n.startswith(prefix) for n in names), prefix
