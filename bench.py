@@ -205,7 +205,8 @@ def time_next_rows(step, torch, df2, iters=20):
     then the greedy and the sampling walk over it; then the draft head with capped
     logits (multiplier 1, softcap 30); then the conv finish fused with the next
     prepare (residual = the step's x), and the same as its separate calls with the
-    residual added by torch.  None of it is part of the timed step."""
+    residual added by torch; then the selector's K-way cross-entropy on the step's
+    teacher-forced scores.  None of it is part of the timed step."""
     w = step.w
     lat = torch.empty((w.R, w.B - 1, w.K, w.K), dtype=torch.float32, device=step.ids.device)
     gen = torch.Generator(device=step.ids.device)
@@ -215,6 +216,14 @@ def time_next_rows(step, torch, df2, iters=20):
     sc = torch.empty((w.R, w.B - 1), dtype=torch.float32, device=step.ids.device)
     h, y_next, dyn_next = torch.empty_like(step.z), torch.empty_like(step.z), torch.empty_like(step.dyn)
     ws_conv = step.ws_conv
+    # the selector loss's ground truth: a candidate of the row for three rows in four
+    # (a column chosen by the row index), a random token (mostly not a candidate) else
+    rows = torch.arange(w.P, device=step.ids.device)
+    pick = step.ids[rows, (rows * 7) % w.K]
+    other = torch.randint(0, w.V, (w.P,), generator=gen, device=step.ids.device, dtype=torch.int32)
+    targets = torch.where(rows % 4 == 3, other, pick).to(torch.int32).contiguous()
+    ce_out = (torch.empty((w.P,), dtype=torch.float32, device=step.ids.device),
+              torch.empty((w.P,), dtype=torch.int32, device=step.ids.device))
 
     def finish_add_prepare():
         hs = df2.conv_finish(step.z, w.B, w.taps, w.g, step.dyn, step.base, out=h)
@@ -231,6 +240,7 @@ def time_next_rows(step, torch, df2, iters=20):
         lambda: df2.conv_finish_prepare(step.z, w.B, w.taps, w.g, step.dyn, step.base, step.W_proj, step.base,
                                         step.x, workspace=ws_conv, out=(h, y_next, dyn_next)),
         finish_add_prepare,
+        lambda: df2.selector_ce(step.scores, step.ids, targets, w.V, out=ce_out),
     ]
     out, how = [], set()
     for c in calls:
@@ -695,7 +705,7 @@ def gpu_arm(args, w, rank, world, torch, df2, dist, device, inp=None, conv=None,
                          "finish": conv_bytes(w, "finish") / (per_call_us[1] * 1e-6) / 1e9},
             "roofline": roof,
             "next_rows": {
-                "note": "the lattice schedule, the capped-logit draft head and the fused conv finish -> prepare, timed on "
+                "note": "the lattice schedule, the capped-logit draft head, the fused conv finish -> prepare and the selector CE, timed on "
                         "the step's inputs outside the timed step",
                 "timed_by": next_how + " (graph: the calls captured in a CUDA graph and replayed, GPU time only)",
                 "selector_lattice_us": next_us[0],
@@ -704,6 +714,7 @@ def gpu_arm(args, w, rank, world, torch, df2, dist, device, inp=None, conv=None,
                 "draft_head_softcap_us": next_us[3],
                 "conv_finish_prepare_us": next_us[4],
                 "conv_finish_add_prepare_separate_us": next_us[5],
+                "selector_ce_us": next_us[6],
                 "lattice_gbs": lattice_bytes(w) / (next_us[0] * 1e-6) / 1e9,
                 "lattice_tflops": lattice_flops(w) / (next_us[0] * 1e-6) / 1e12,
             },

@@ -7,6 +7,7 @@ contiguous and row-major; calls are asynchronous on the current torch stream.
     ids, vals, G = unary_topk(h, W_lm, K, W_H)          # logits never leave the chip
     path, scores = selector_walk(anchors, ids, vals, G, A, Bc, block_size)
     s = selector_pair_scores(pred, ids, vals, G, A, Bc)  # teacher-forced
+    loss, label = selector_ce(s, ids, targets, V)      # the selector's K-way CE
     y, dyn = conv_prepare(x, block_size, taps, group, W_proj, base)
     y2 = conv_finish(z, block_size, taps, group, dyn, base)
 """
@@ -174,6 +175,27 @@ def selector_walk(anchors, topk_ids, topk_vals, G, A, Bc, block_size, *, dev_sta
                                      _stream(stream))
     _check("dflash2_selector_walk", rc)
     return path, scores
+
+
+def selector_ce(scores, topk_ids, targets, V, *, dev_status=None, out=None, stream=None):
+    """The selector's K-way cross-entropy per row of teacher-forced scores [P, K]:
+    (loss [P] fp32, label [P] int32); rows whose target is not a candidate give
+    label -1 and NaN loss."""
+    _need(scores, "scores", torch.float32)
+    _need(topk_ids, "topk_ids", torch.int32)
+    _need(targets, "targets", torch.int32, 1)
+    P = targets.shape[0]
+    K = topk_ids.shape[-1]
+    if topk_ids.numel() != P * K or scores.numel() != P * K:
+        raise ValueError("scores / topk_ids do not match [P, K]")
+    if out is None:
+        out = (torch.empty((P,), dtype=torch.float32, device=scores.device),
+               torch.empty((P,), dtype=torch.int32, device=scores.device))
+    loss, label = out
+    rc = lib().dflash2_selector_ce(_p(scores), _p(topk_ids), _p(targets), P, K, int(V), _p(loss), _p(label),
+                                   _p(dev_status), _stream(stream))
+    _check("dflash2_selector_ce", rc)
+    return loss, label
 
 
 def selector_pair_scores(pred, topk_ids, topk_vals, G, A, Bc, *, dev_status=None, out=None,

@@ -27,6 +27,7 @@ SIGNATURES = {
                                      _vp, _vp, _vp]),
     "dflash2_selector_pair_scores": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int,
                                             _vp, _vp, _vp]),
+    "dflash2_selector_ce": (_int, [_vp, _vp, _vp, _i64, _int, _i64, _vp, _vp, _vp, _vp]),
     "dflash2_draft_head_workspace_size": (_sz, [_int, _int, _i64, _i64, _int, _int]),
     "dflash2_draft_head": (_int, [_vp, _int, _int, _i64, _vp, _i64, _int, _f32, _f32, _vp, _int, _vp, _vp,
                                   _vp, _vp,

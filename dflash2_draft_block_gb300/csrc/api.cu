@@ -286,6 +286,18 @@ DF2_API int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const i
                                              static_cast<cudaStream_t>(stream)));
 }
 
+DF2_API int dflash2_selector_ce(const float* scores, const int32_t* topk_ids, const int32_t* targets,
+                                int64_t P, int K, int64_t V, float* loss, int32_t* label_idx,
+                                int32_t* dev_status, void* stream) {
+    if (P < 0 || K < 1 || V < 1) return DF2_ERR_INVALID_ARGUMENT;
+    if (K > DF2_MAX_TOPK || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (P == 0) return DF2_OK;
+    if (!scores || !topk_ids || !targets || !loss) return DF2_ERR_INVALID_ARGUMENT;
+    if ((P + 7) / 8 > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    return from_cuda(df2::selector_ce_launch(scores, topk_ids, targets, P, K, V, loss, label_idx, dev_status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 // --------------------------------------------------------------- lattice --
 
 DF2_API int dflash2_selector_lattice(const int32_t* anchors, int R, int B, const int32_t* topk_ids,

@@ -90,6 +90,9 @@ cudaError_t pair_scores_launch(const int32_t* pred, int64_t P, const int32_t* id
                                const float* vals, const float* G, const uint16_t* A,
                                const uint16_t* Bc, int64_t V, int K, int r, float* scores,
                                int32_t* dev_status, cudaStream_t stream);
+cudaError_t selector_ce_launch(const float* scores, const int32_t* ids, const int32_t* targets, int64_t P,
+                               int K, int64_t V, float* loss, int32_t* label_idx, int32_t* dev_status,
+                               cudaStream_t stream);
 
 // ---- lattice: L[q][t-1][i][j] = S_t(i-th predecessor, j-th candidate), then a walk over it
 cudaError_t lattice_launch(const int32_t* anchors, int R, int B, const int32_t* ids, const float* vals,

@@ -267,6 +267,67 @@ cudaError_t walk_launch(const int32_t* anchors, int R, int B, const int32_t* ids
     return cudaGetLastError();
 }
 
+namespace {
+
+// The selector's K-way cross-entropy ([PR62] "Selector training objective"): one
+// warp per row.  The lanes stride the row's K scores for its maximum and the first
+// column holding the target, then sum exp(score - maximum); lane 0 writes
+// loss = log(sum) + maximum - score[label].  Rows whose target is not a candidate
+// (or is negative) get label -1 and NaN.
+constexpr int kCeWarps = 8;
+
+__global__ void __launch_bounds__(kCeWarps * 32)
+selector_ce_kernel(const float* __restrict__ scores, const int32_t* __restrict__ ids,
+                   const int32_t* __restrict__ targets, int64_t P, int K, int64_t V, float* __restrict__ loss,
+                   int32_t* __restrict__ label_idx, int32_t* __restrict__ dev_status) {
+    const int64_t p = int64_t(blockIdx.x) * kCeWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (p >= P) return;
+    const int32_t y = __ldg(targets + p);
+    const bool has = y >= 0 && y < V;
+    if (y >= V && lane == 0 && dev_status) atomicOr(dev_status, DF2_STATUS_ID_OUT_OF_RANGE);
+    const float* s = scores + p * K;
+    const int32_t* id = ids + p * K;
+    float m = -INFINITY;
+    int js = INT_MAX;
+    for (int j = lane; j < K; j += 32) {
+        m = fmaxf(m, __ldg(s + j));
+        if (has && __ldg(id + j) == y && j < js) js = j;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        js = min(js, __shfl_xor_sync(kFull, js, o));
+    }
+    if (js == INT_MAX) {
+        if (lane == 0) {
+            loss[p] = __int_as_float(0x7fc00000);
+            if (label_idx) label_idx[p] = -1;
+        }
+        return;
+    }
+    float sum = 0.f;
+    for (int j = lane; j < K; j += 32) sum += expf(__ldg(s + j) - m);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    if (lane == 0) {
+        loss[p] = logf(sum) + m - __ldg(s + js);
+        if (label_idx) label_idx[p] = js;
+    }
+}
+
+}  // namespace
+
+cudaError_t selector_ce_launch(const float* scores, const int32_t* ids, const int32_t* targets, int64_t P,
+                               int K, int64_t V, float* loss, int32_t* label_idx, int32_t* dev_status,
+                               cudaStream_t stream) {
+    const unsigned grid = unsigned((P + kCeWarps - 1) / kCeWarps);
+    selector_ce_kernel<<<grid, kCeWarps * 32, 0, stream>>>(scores, ids, targets, P, K, V, loss, label_idx,
+                                                           dev_status);
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t pair_scores_launch(const int32_t* pred, int64_t P, const int32_t* ids,
                                const float* vals, const float* G, const uint16_t* A,
                                const uint16_t* Bc, int64_t V, int K, int r, float* scores,

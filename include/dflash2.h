@@ -7,6 +7,7 @@
  *                                 the per-position top-K, and the hidden projection H
  *   dflash2_selector_walk         the candidate selector's greedy walk
  *   dflash2_selector_pair_scores  the selector scores with teacher-forced predecessors
+ *   dflash2_selector_ce           the selector's K-way cross-entropy on those scores
  *   dflash2_draft_head            the four steps above for one draft block, fused
  *   dflash2_selector_lattice      every adjacent candidate pair scored at once
  *   dflash2_lattice_walk          the greedy or sampling walk over that table
@@ -220,6 +221,33 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
                                  const float* topk_vals, const float* G, const uint16_t* A,
                                  const uint16_t* Bc, int64_t V, int K, int r, float* scores,
                                  int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dflash2_selector_ce — the selector's training loss, forward.
+ *
+ * The K-way cross-entropy of the teacher-forced scores against the ground truth,
+ * on rows whose ground truth is among the row's candidates ([PR62] "Selector
+ * training objective": a cross-entropy over the drafter's own top-K, restricted to
+ * rows whose ground truth survived it; [vLLM] "Training Objective": the K-way
+ * hard cross-entropy over the unary top-K candidates).  For row p:
+ *
+ *   label_idx[p] = the column j with topk_ids[p, j] == targets[p], else -1
+ *   loss[p]      = log(sum_j exp(scores[p, j])) - scores[p, label_idx[p]]
+ *                  (NaN where label_idx[p] == -1: the row contributes nothing)
+ *
+ * The variant that swaps the target into the weakest candidate's slot when it is
+ * missing ([vLLM] "Training Objective") is the same call on the edited candidate
+ * list and scores.  Forward only; fp32 with the row maximum subtracted before exp.
+ *
+ *   scores [P, K] fp32 (dflash2_selector_pair_scores' output); topk_ids [P, K]
+ *   int32; targets [P] int32 (the ground-truth token of each row, < 0: none);
+ *   loss [P] fp32 out; label_idx [P] int32 out (nullable).
+ * Rules: P >= 0, 1 <= K <= DF2_MAX_TOPK, V >= 1.  A target >= V sets
+ * DF2_STATUS_ID_OUT_OF_RANGE (label -1, loss NaN).
+ * ---------------------------------------------------------------------- */
+int dflash2_selector_ce(const float* scores, const int32_t* topk_ids, const int32_t* targets, int64_t P,
+                        int K, int64_t V, float* loss, int32_t* label_idx, int32_t* dev_status,
+                        void* stream);
 
 /* ------------------------------------------------------------------------
  * dflash2_draft_head — unary top-K, H, greedy walk and teacher-forced scores of one
