@@ -3,7 +3,8 @@
 //   y[p, c] = sum_{j < taps, t-j >= 0} (base[j, c] + dyn[p, j, c/g]) * x[p-j, c],  t = p mod B
 //
 // (verl-SpeCo PR #62, "What DFlash2 adds": Conv_k(x)_t = k_{t,0} x_t + k_{t,1} x_{t-1},
-// static per-channel kernel plus a correction shared by conv_group_size channels;
+// a fixed kernel per channel with a correction common to a group of conv_group_size
+// channels added;
 // "Two deltas", item 1: no tap crosses an anchor-block boundary.)
 //
 // One thread owns 16 bytes of channels (8 bf16 or 4 fp32) of one anchor block and

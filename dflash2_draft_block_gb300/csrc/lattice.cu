@@ -1,8 +1,8 @@
 // The lattice schedule of the candidate selector: every adjacent candidate pair
 // scored in one parallel pass, then a sequential walk over the finished table
-// ("DFlash 2 Explanation", "How It Works", Problem 1: all pairs score at once,
-// only the final walk over the precomputed scores is sequential; greedy follows
-// the best successor, sampling draws from the same scores).
+// ("DFlash 2 Explanation", "How It Works", Problem 1: the pair scores are computed
+// together, and only the walk that reads them is serial, whether it takes the best
+// successor or samples one from those scores).
 //
 // Table slot s = t-1 of request q (drafted position t = 1 .. B-1) holds
 //   L[q][s][i][j] = vals[q,t,j] + sum_k A[a_i, k] * G[q,t,k] * Bc[ids[q,t,j], k]

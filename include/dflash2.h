@@ -103,7 +103,7 @@ int dflash2_unary_topk_path(int64_t P, int64_t D, int64_t V, int K);
  * For every row p of the draft hidden state (P = requests x block_size rows;
  * row 0 of each block is the anchor position):
  *   U[p, v] = sum_d h[p, d] * W_lm[v, d]        for all v in [0, V)   ([vLLM]
- *             "Candidate Selector": the unary draft logits; [KB] "Draft-Verify
+ *             "Candidate Selector": the drafter's per-token logits; [KB] "Draft-Verify
  *             Cycle": the shared lm_head gives logits and top-K per position;
  *             the full verifier vocabulary, [vLLM] "Candidate Selector")
  *   U'[p, v] = c * tanh(m * U[p, v] / c)          (m * U[p, v] when c = 0)
@@ -182,10 +182,10 @@ int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D, const ui
  *     s_j = topk_vals[row, j] + sum_i A[a_{t-1}, i] * G[row, i] * Bc[topk_ids[row, j], i]
  *     j*  = argmax_j s_j   (equal scores: the lower token id)
  *     a_t = topk_ids[row, j*];  path[q, t-1] = a_t;  path_scores[q, t-1] = s_{j*}
- * ([vLLM] "Candidate Selector": start at the anchor, condition each position on the
- * token selected at the one before; [PR62] "What DFlash2 adds": S_t(a, b) =
- * U_t(b) + <A(a) * H(h_t), B(b)>; [KB] "Problem 1": greedy follows the best
- * successor.)  Rows t = 0 (the anchor rows) are not read.  Scores are fp32.
+ * ([vLLM] "Candidate Selector": the walk begins at the anchor and each choice
+ * becomes the next position's predecessor; [PR62] "What DFlash2 adds": S_t(a, b) =
+ * U_t(b) + <A(a) * H(h_t), B(b)>; [KB] "Problem 1": the greedy walk takes the
+ * highest-scoring successor.)  Rows t = 0 (the anchor rows) are not read.  Scores are fp32.
  *
  *   anchors     [R]        int32   device
  *   topk_ids    [R*B, K]   int32   candidates (as written by dflash2_unary_topk)
@@ -225,11 +225,10 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
 /* ------------------------------------------------------------------------
  * dflash2_selector_ce — the selector's training loss, forward.
  *
- * The K-way cross-entropy of the teacher-forced scores against the ground truth,
- * on rows whose ground truth is among the row's candidates ([PR62] "Selector
- * training objective": a cross-entropy over the drafter's own top-K, restricted to
- * rows whose ground truth survived it; [vLLM] "Training Objective": the K-way
- * hard cross-entropy over the unary top-K candidates).  For row p:
+ * The K-way cross-entropy of the teacher-forced scores against the ground truth
+ * ([PR62] "Selector training objective"; [vLLM] "Training Objective"): a
+ * categorical loss over the K candidates the head kept, to which a row contributes
+ * only when its ground-truth token is one of them.  For row p:
  *
  *   label_idx[p] = the column j with topk_ids[p, j] == targets[p], else -1
  *   loss[p]      = log(sum_j exp(scores[p, j])) - scores[p, label_idx[p]]
@@ -318,8 +317,8 @@ int dflash2_selector_lattice(const int32_t* anchors, int R, int B, const int32_t
 /* ------------------------------------------------------------------------
  * dflash2_lattice_walk — the walk over a finished lattice.
  *
- * [KB] "How It Works", Problem 1: greedy follows the best successor; sampling
- * draws from the same scores.  Per request q the state is the row i of the
+ * [KB] "How It Works", Problem 1: the greedy walk takes the highest-scoring
+ * successor, and the sampled walk draws one from the same pair scores.  Per request q the state is the row i of the
  * current predecessor (i = 0, the anchor, at t = 1); step t reads row i of slot
  * t-1 and picks a column j, which becomes the next row:
  *   uniforms == NULL (greedy): the largest score, equal scores to the lower token id
@@ -357,10 +356,11 @@ int dflash2_lattice_walk(const float* lattice, const int32_t* topk_ids, int R, i
  *   d[p, io, j, gi] = sum_c W_proj[(io*taps + j)*G + gi, c] * x[p, c]
  *   y[p, c]         = sum_{j < taps, t-j >= 0} (base[0, j, c] + d[p, 0, j, c/g]) * x[p-j, c]
  *   dyn_out[p, j, gi] = d[p, 1, j, gi]
- * ([PR62] "What DFlash2 adds": Conv_k(x)_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}, a
- * static per-channel kernel plus a correction shared by conv_group_size channels;
- * prepare also emits the kernel finish applies; [vLLM] "Local Convolution": a
- * projection of the current hidden state gives both kernels.)  io = 0 is the
+ * ([PR62] "What DFlash2 adds": Conv_k(x)_t = k_{t,0} * x_t + k_{t,1} * x_{t-1}, where
+ * each k is a fixed kernel per channel with a correction common to a group of
+ * conv_group_size channels added, and prepare hands finish the kernel it will use;
+ * [vLLM] "Local Convolution": both kernels come from one projection of the hidden
+ * state at that position.)  io = 0 is the
  * kernel applied here, io = 1 the one dflash2_conv_finish applies.
  *
  *   x       [P, C]            dtype (DF2_DTYPE_BF16 or DF2_DTYPE_F32)
@@ -391,8 +391,8 @@ int dflash2_conv_finish(const void* z, int dtype, int64_t P, int C, int B, int t
 /* ------------------------------------------------------------------------
  * dflash2_conv_finish_prepare — the two convs between consecutive sublayers.
  *
- * ([vLLM] "Local Convolution": every attention and MLP sublayer is wrapped by a
- * conv before and after it.)  The finish of one sublayer, then the prepare of the
+ * ([vLLM] "Local Convolution": each attention and MLP sublayer has a conv on its
+ * input side and one on its output side.)  The finish of one sublayer, then the prepare of the
  * next, with the sum in between written out:
  *   h        = dflash2_conv_finish(z; dyn_out, base)  (+ residual)
  *   y_next, dyn_out_next = dflash2_conv_prepare(h; W_proj, base_next)

@@ -332,10 +332,10 @@ int df2o_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* ids
 
 /*
  * The selector's training loss, forward (verl-SpeCo PR #62, "Selector training
- * objective": a cross-entropy over the drafter's own top-K candidates with the
- * predecessor teacher-forced, counted only on rows whose ground truth is among
- * those candidates; vLLM Speculators "DFlash2" guide, "Training Objective": the
- * K-way hard cross-entropy over the unary top-K candidates).  Row p holds the
+ * objective"; vLLM Speculators "DFlash2" guide, "Training Objective"): a
+ * categorical cross-entropy of the teacher-forced scores over the K candidates the
+ * head kept, to which a row contributes only when its ground-truth token is one of
+ * those candidates.  Row p holds the
  * teacher-forced scores S[p, 0..K-1] of its candidates ids[p, .] and the ground
  * truth y = targets[p]:
  *     label_idx[p] = the column j with ids[p, j] == y, else -1
@@ -636,8 +636,8 @@ int df2o_conv_finish(const void* z, int z_is_f32, int64_t P, int32_t C, int32_t 
 /*
  * The two convs that meet between consecutive sublayers of a draft layer: the
  * finish of one sublayer, then the prepare of the next (vLLM Speculators "DFlash2"
- * guide, "Local Convolution": every attention and MLP sublayer is wrapped by a conv
- * before and after it).  The pages do not state the residual wiring between the
+ * guide, "Local Convolution": each attention and MLP sublayer has a conv on its
+ * input side and one on its output side).  The pages do not state the residual wiring between the
  * two.  Reading: h = finish(z), plus the residual stream when one is given (the sum
  * rounded to the activation dtype, as a separate elementwise add would round it),
  * then prepare(h) with the next sublayer's projection and base kernels.  Writes
