@@ -61,7 +61,9 @@ struct ConvTcArgs {
     int ng;                 // groups per tile
     int n_gt;               // group tiles (G / ng)
     int n_mu;               // units along the rows: 128-row tiles, or pairs of them
-    int n_units;            // units launched (CTAs or CTA pairs)
+    int n_units;            // units launched (CTAs, CTA pairs or clusters of two pairs)
+    int n_full_rounds;      // with n_half > 0: every unit's whole tiles, then its half tile
+    int n_half;             // the last round's tiles split in two along the groups (0: none)
     int nstages;
     int ds_ld;              // floats per row of the staged input-side corrections
 };
@@ -115,8 +117,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // computed, so the epilogue keeps two groups of loads outstanding.
 template <int TAPS, bool PREF>
 __device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, int64_t m0, int rows, int g0,
-                                          int etid) {
-    const int nch = a.ng * a.g / 8;
+                                          int ngt, int etid) {
+    const int nch = ngt * a.g / 8;
     const int c_lo = g0 * a.g;
     const int B = a.B, C = a.C;
     const int total = (rows / B) * nch;
@@ -170,13 +172,13 @@ __device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, 
                 for (int j = 0; j < TAPS; ++j) {
                     if (j > t) break;
                     if (one_group) {
-                        const float d = drow[j * a.ng + gl0];
+                        const float d = drow[j * ngt + gl0];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) acc[e] = fmaf(kb[j][e] + d, hist[j][e], acc[e]);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            const float d = drow[j * a.ng + (c + e) / a.g - g0];
+                            const float d = drow[j * ngt + (c + e) / a.g - g0];
                             acc[e] = fmaf(kb[j][e] + d, hist[j][e], acc[e]);
                         }
                     }
@@ -202,17 +204,19 @@ __device__ __forceinline__ void ctc_apply(const ConvTcArgs& a, const float* ds, 
 // pair rank in the other pair, and a stage is free again when both pairs' MMAs have
 // read it.  The units are then clusters: cluster step c + k * n_units covers row
 // tiles (pair units) 2 mg and 2 mg + 1 of group tile gt, numbered gt-fastest.
+//
+// Half tiles: when the last round would leave units idle (a.n_half > 0), its tiles
+// are split in two along the groups, ng/2 each (tm_wh: W_proj boxes of ng/2 rows,
+// an MMA of half the N), so that 2L units share the last round's L tiles.
 template <int TAPS, bool PAIR, bool MC = false>
 __global__ void __launch_bounds__(kCtcThreads, 1)
 conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                       const ConvTcArgs a) {
+                       const __grid_constant__ CUtensorMap tm_wh, const ConvTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned by pointer arithmetic on the shared array (keeps every
     // access derived from it in the shared address space)
     uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int ng = a.ng, nstages = a.nstages;
-    const int half = TAPS * ng;          // input-side columns (= output-side columns)
-    const int N = 2 * half;              // MMA N
     const uint32_t brows = ctc_b_rows(TAPS, ng, PAIR);
     const uint32_t stage_bytes = kXBox + brows * CK * 2;
     uint8_t* stages = smem;              // stage s: one x box, then the W_proj boxes
@@ -237,13 +241,27 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     // step the units work on consecutive tiles, which share their x rows in L2
     const int n_rows_units = MC ? (a.n_mu + 1) / 2 : a.n_mu;
     const int total = n_rows_units * a.n_gt;
-    const int ntiles = unit < total ? (total - unit + a.n_units - 1) / a.n_units : 0;
-    auto tile_mt = [&](int k) {
-        const int mu0 = (unit + k * a.n_units) / a.n_gt;
-        const int mu = MC ? 2 * mu0 + pp : mu0;
-        return PAIR ? 2 * mu + int(rank) : mu;
+    // the unit's tiles: unit, unit + n_units, ...; with half tiles, its whole rounds
+    // and then (unit < n_half) half `unit % 2` of whole tile F + unit / 2
+    const int ntiles = a.n_half > 0 ? a.n_full_rounds + (unit < a.n_half ? 1 : 0)
+                                    : (unit < total ? (total - unit + a.n_units - 1) / a.n_units : 0);
+    struct Tile {
+        int mt, g0, ngt;  // this CTA's 128-row tile, first group, groups
     };
-    auto tile_gt = [&](int k) { return (unit + k * a.n_units) % a.n_gt; };
+    auto tile = [&](int k) {
+        int T = unit + k * a.n_units, sub = -1;
+        if (a.n_half > 0 && k == a.n_full_rounds) {
+            T = a.n_full_rounds * a.n_units + unit / 2;
+            sub = unit % 2;
+        }
+        const int mu0 = T / a.n_gt, gt = T - mu0 * a.n_gt;
+        const int mu = MC ? 2 * mu0 + pp : mu0;
+        Tile tl;
+        tl.mt = PAIR ? 2 * mu + int(rank) : mu;
+        tl.ngt = sub < 0 ? ng : ng / 2;
+        tl.g0 = gt * ng + (sub > 0 ? ng / 2 : 0);
+        return tl;
+    };
     const int nbox = (a.C + CK - 1) / CK;
 
     if (threadIdx.x == 0) {
@@ -291,11 +309,14 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             for (int s = 0; s < kCtcMaxStages; ++s) armed[s] = -1;
             bool ok = true;
             for (int k = 0; k < ntiles && ok; ++k) {
-                const int mt = tile_mt(k), g0 = tile_gt(k) * ng;
+                const Tile tl = tile(k);
+                const int mt = tl.mt, g0 = tl.g0, ngt = tl.ngt;
+                const uint32_t tile_bytes = kXBox + ctc_b_rows(TAPS, ngt, PAIR) * CK * 2;
+                const CUtensorMap* wm = ngt == ng ? &tm_w : &tm_wh;
                 for (int kb = 0; kb < nbox; ++kb) {
                     if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
                     // PAIR: CTA 0's full barrier counts the bytes both CTAs stage
-                    if (leader) tc::mbar_arrive_expect_tx(&full[stage], stage_bytes * (PAIR ? 2u : 1u));
+                    if (leader) tc::mbar_arrive_expect_tx(&full[stage], tile_bytes * (PAIR ? 2u : 1u));
                     uint8_t* st = stages + size_t(stage) * stage_bytes;
                     const int xk = kb * CK;
                     if (PAIR) {
@@ -307,19 +328,19 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
                             if (pp == 0)
 #pragma unroll
                                 for (int j = 0; j < TAPS; ++j)
-                                    tc::tma_load_2d_pair_mc(st + kXBox + size_t(j) * ng * CK * 2, &tm_w, fb, mask, xk,
+                                    tc::tma_load_2d_pair_mc(st + kXBox + size_t(j) * ngt * CK * 2, wm, fb, mask, xk,
                                                             (int(rank) * TAPS + j) * a.G + g0, pol_w);
                         } else {
 #pragma unroll
                             for (int j = 0; j < TAPS; ++j)
-                                tc::tma_load_2d_pair(st + kXBox + size_t(j) * ng * CK * 2, &tm_w, fb, xk,
+                                tc::tma_load_2d_pair(st + kXBox + size_t(j) * ngt * CK * 2, wm, fb, xk,
                                                      (int(rank) * TAPS + j) * a.G + g0, pol_w);
                         }
                     } else {
                         tc::tma_load_2d(st, &tm_x, &full[stage], xk, mt * CM, pol_x);
 #pragma unroll
                         for (int q = 0; q < 2 * TAPS; ++q)
-                            tc::tma_load_2d(st + kXBox + size_t(q) * ng * CK * 2, &tm_w, &full[stage], xk,
+                            tc::tma_load_2d(st + kXBox + size_t(q) * ngt * CK * 2, wm, &full[stage], xk,
                                             q * a.G + g0, pol_w);
                     }
                     armed[stage] = int8_t(phase);
@@ -337,11 +358,11 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // -------------------------------------------------------- MMA issuer
-            const uint32_t idesc = tc::idesc_bf16_f32(PAIR ? 2 * CM : CM, N);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int k = 0; k < ntiles && ok; ++k) {
+                const uint32_t idesc = tc::idesc_bf16_f32(PAIR ? 2 * CM : CM, 2 * TAPS * tile(k).ngt);
                 const int b = k & 1;
                 const uint32_t tph = (k >> 1) & 1;
                 const bool drained = PAIR ? tc::mbar_wait_cluster(&tempty[b], tph ^ 1, abort_flag)
@@ -387,7 +408,9 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
         const int64_t gld = int64_t(TAPS) * a.G;       // dyn_out row length
         const uint64_t pol_out = tc::l2_policy_evict_first();
         for (int k = 0; k < ntiles; ++k) {
-            const int mt = tile_mt(k), g0 = tile_gt(k) * ng;
+            const Tile tl = tile(k);
+            const int mt = tl.mt, g0 = tl.g0, ngt = tl.ngt;
+            const int half_t = TAPS * ngt, N_t = 2 * half_t;  // this tile's columns
             const int b = k & 1;
             const uint32_t tph = (k >> 1) & 1;
             const bool got = tc::mbar_wait(&tfull[b], tph, abort_flag);
@@ -400,17 +423,17 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             const bool row_ok = m < a.P;
             const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(b) * kBufCols;
             float* drow = ds + size_t(r) * a.ds_ld;
-            for (int c0 = 16 * half_grp; c0 < N; c0 += 32) {
+            for (int c0 = 16 * half_grp; c0 < N_t; c0 += 32) {
                 float v[16];
                 tc::tmem_ld16(taddr + uint32_t(c0), v);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int col = c0 + 4 * q;  // four columns of one side and one tap (ng % 4 == 0)
-                    if (col < half) {
+                    const int col = c0 + 4 * q;  // four columns of one side and one tap (ngt % 4 == 0)
+                    if (col < half_t) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) drow[col + e] = v[4 * q + e];
                     } else if (row_ok) {
-                        const int oc = col - half, j = oc / ng, gl = oc - j * ng;
+                        const int oc = col - half_t, j = oc / ngt, gl = oc - j * ngt;
                         st16_hint(a.dyn_out + m * gld + int64_t(j) * a.G + g0 + gl,
                                   make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
                                              __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])),
@@ -429,7 +452,7 @@ conv_prepare_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_co
             tc::named_barrier(1, kCtcEpi);  // every row's corrections are staged
             const int64_t left = int64_t(a.P) - m0;
             const int rows = left <= 0 ? 0 : (left < CM ? int(left) : CM);
-            ctc_apply<TAPS, (TAPS <= 2)>(a, ds, m0, rows, g0, etid);
+            ctc_apply<TAPS, (TAPS <= 2)>(a, ds, m0, rows, g0, ngt, etid);
         }
     }
 
@@ -478,7 +501,22 @@ struct CtcPlan {
     bool pair = false;
     bool mc = false;    // clusters of two pairs sharing the W_proj boxes
     int ng = 0, n_gt = 0, n_mu = 0, units = 0, nstages = 0, ds_ld = 0;
+    int n_full_rounds = 0, n_half = 0;  // the last round in half tiles (n_half > 0)
 };
+
+// The last round split into half tiles when its L tiles would leave units idle and
+// 2L of them fit: the 2L units that take one then finish about as soon as a whole
+// tile would, with half the MMA work each.  A half tile has ng/2 groups, which must
+// still fill whole 1024-byte swizzle atoms (ng/2 a multiple of 8).
+void ctc_split_last_round(CtcPlan& p, int64_t total) {
+    p.n_full_rounds = 0;
+    p.n_half = 0;
+    if (p.units <= 0 || total <= p.units || p.ng % 16 != 0) return;
+    const int64_t full = total / p.units * p.units, left = total - full;
+    if (left == 0 || 2 * left > p.units) return;
+    p.n_full_rounds = int(total / p.units);
+    p.n_half = int(2 * left);
+}
 
 // Clusters of two pairs of this kernel that fit at once (occupancy API), cached per
 // device and launch shape; 0 when the query fails.
@@ -550,11 +588,16 @@ CtcPlan ctc_plan(int64_t P, int C, int B, int taps, int g, int num_sms) {
             }
         }
     }
+    if (best.ok) {
+        const int64_t total = int64_t(best.mc ? best.n_mu / 2 : best.n_mu) * best.n_gt;
+        ctc_split_last_round(best, total);
+    }
     return best;
 }
 
 template <int TAPS, bool PAIR, bool MC = false>
-cudaError_t ctc_launch(const CUtensorMap& tx, const CUtensorMap& tw, const ConvTcArgs& a, cudaStream_t stream) {
+cudaError_t ctc_launch(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& twh, const ConvTcArgs& a,
+                       cudaStream_t stream) {
     const size_t smem = ctc_smem(a.nstages, TAPS, a.ng, PAIR, a.ds_ld) + 1024;
     auto kernel = conv_prepare_tc_kernel<TAPS, PAIR, MC>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
@@ -571,7 +614,7 @@ cudaError_t ctc_launch(const CUtensorMap& tx, const CUtensorMap& tw, const ConvT
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = PAIR ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kernel, tx, tw, a);
+    e = cudaLaunchKernelEx(&cfg, kernel, tx, tw, twh, a);
     note_launch();
     return e;
 }
@@ -642,8 +685,9 @@ cudaError_t conv_prepare_tc_launch(const uint16_t* x, int64_t P, int C, int B, i
     const CtcPlan p = ctc_plan(P, C, B, taps, g, sms);
     if (!p.ok) return cudaErrorInvalidValue;
     const int G = C / g;
-    CUtensorMap tx, tw;
-    if (!ctc_map(&tx, x, P, C, CM) || !ctc_map(&tw, W, int64_t(2) * taps * G, C, p.ng))
+    CUtensorMap tx, tw, twh;
+    if (!ctc_map(&tx, x, P, C, CM) || !ctc_map(&tw, W, int64_t(2) * taps * G, C, p.ng) ||
+        !ctc_map(&twh, W, int64_t(2) * taps * G, C, p.n_half > 0 ? p.ng / 2 : p.ng))
         return cudaErrorInvalidValue;
     ConvTcArgs a{};
     a.x = x;
@@ -660,13 +704,16 @@ cudaError_t conv_prepare_tc_launch(const uint16_t* x, int64_t P, int C, int B, i
     a.n_gt = p.n_gt;
     a.n_mu = p.n_mu;
     a.n_units = p.units;
+    a.n_full_rounds = p.n_full_rounds;
+    a.n_half = p.n_half;
     a.nstages = p.nstages;
     a.ds_ld = p.ds_ld;
     switch (taps) {
 #define DF2_CTC(TP)                                                                    \
     case TP:                                                                           \
-        if (p.mc) return ctc_launch<TP, true, true>(tx, tw, a, stream);                \
-        return p.pair ? ctc_launch<TP, true>(tx, tw, a, stream) : ctc_launch<TP, false>(tx, tw, a, stream);
+        if (p.mc) return ctc_launch<TP, true, true>(tx, tw, twh, a, stream);           \
+        return p.pair ? ctc_launch<TP, true>(tx, tw, twh, a, stream)                   \
+                      : ctc_launch<TP, false>(tx, tw, twh, a, stream);
         DF2_CTC(1)
         DF2_CTC(2)
         DF2_CTC(3)

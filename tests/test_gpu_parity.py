@@ -428,6 +428,8 @@ def test_tiny_conv(orc, df2):
     (1032, 256, 8, 2, 16, "bf16"),  # nine row tiles, the last one 8 rows
     (256, 512, 32, 4, 16, "bf16"),  # blocks of 32, taps 4
     (96, 256, 16, 3, 16, "bf16"),   # one partial row tile, blocks of 16
+    (5120, 512, 8, 3, 4, "bf16"),   # a last round of half tiles (clusters of two pairs)
+    (5376, 512, 8, 3, 4, "bf16"),   # a last round of half tiles (CTA pairs)
 ])
 def test_conv_shapes(orc, df2, P, C, B, taps, g, dt):
     rng = _rng(P * 13 + C + taps * 7 + g)
