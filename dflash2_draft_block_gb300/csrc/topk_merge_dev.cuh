@@ -38,6 +38,11 @@ constexpr int kOneWarpCands = 128;  // up to this many candidates one warp folds
 
 __host__ __device__ inline size_t merge_smem(int S, int K) { return size_t(S) * K * 16 + size_t(S) * 12; }
 
+// Ask L2 for `bytes` (a multiple of 16) of global memory at p (16-byte aligned).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Two neighbouring fp32 logits this close may be ordered wrongly by the
 // tensor-core sum and are recomputed exactly.
 __device__ __forceinline__ bool near_tie(float a, float b) {
@@ -315,6 +320,12 @@ __device__ __forceinline__ void merge_position(const float* __restrict__ part_v,
         __syncthreads();
         const int nre = n_re;
         if (nre > 0) {
+            // every recomputed entry's W row asked into L2 at once: the rounds after
+            // the first then read it from there
+            for (int f = tid; f < nre; f += kWarps * 32) {
+                const int32_t id = xi[0][re_idx[f]];
+                prefetch_l2(rf.W + int64_t(id) * rf.D, uint32_t(rf.D) * 2u);
+            }
             // the row of h, read by every recompute: with more than two, into the
             // lists' shared memory (free again: the scan above was its last use) when
             // it fits; one or two read it from global memory beside their W rows
