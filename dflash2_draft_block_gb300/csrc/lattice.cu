@@ -186,10 +186,13 @@ lattice_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __rest
 // goes through shared memory in 64-wide slices (one 128-byte swizzle row per
 // operand row): the threads issue every gather of slice c + 1 before they wait for
 // the tensor core to finish slice c (an mbarrier), then form the slice (the
-// product with G, the split, the writes in the swizzled K-major layout).  One
-// 24 KB buffer lets eight CTAs share an SM, which is what hides the gathers'
-// latency.  Waits are bounded.
+// product with G, the split, the writes in the swizzled K-major layout).  What
+// hides the gathers' latency is the CTAs sharing an SM: the launch bound holds a
+// thread to 48 registers so that five fit (62 registers allowed four: 136.5 ->
+// 133.0 us at 256 requests x 15 slots, K 64, r 512; six, at 40 registers, spill
+// and took 141.7 us).  Waits are bounded.
 constexpr int kLtcThreads = 256;
+constexpr int kLtcCtasPerSm = 5;
 constexpr int kLtcMaxK = 64;
 constexpr uint32_t kLtcA = 128 * 128;            // A slice: 128 rows x 128 bytes
 constexpr uint32_t kLtcB = kLtcMaxK * 128;       // B slice: up to 64 rows x 128 bytes
@@ -206,7 +209,7 @@ __device__ __forceinline__ uint4* ltc_chunk(uint8_t* base, int row, int cc) {
     return reinterpret_cast<uint4*>(base + size_t(row) * 128 + size_t((cc ^ (row & 7)) * 16));
 }
 
-__global__ void __launch_bounds__(kLtcThreads)
+__global__ void __launch_bounds__(kLtcThreads, kLtcCtasPerSm)
 lattice_tc_kernel(const int32_t* __restrict__ anchors, int B, const int32_t* __restrict__ ids,
                   const float* __restrict__ vals, const float* __restrict__ G,
                   const uint16_t* __restrict__ A, const uint16_t* __restrict__ Bc, int64_t V, int K, int r,
