@@ -96,6 +96,52 @@ MUTANTS = [
      "                if (ids[p * K + j] == y) {", "                if (scores[p * K + j] >= scores[p * K] && ids[p * K + j] != -7) {"),
     ("ce_uncovered_rows_count_zero", "            loss[p] = NAN;\n            continue;", "            loss[p] = 0.0f;\n            continue;"),
     ("ce_sum_skips_last", "        for (int32_t j = 0; j < K; ++j) sum += exp(", "        for (int32_t j = 0; j + 1 < K; ++j) sum += exp("),
+    ("ce_no_status_for_large_target", "        if (y >= V) bad |= 1;\n", "        if (0) bad |= 1;\n"),
+    ("ce_label_off_by_one",
+     "loss[p] = (float)(log(sum) + m - (double)scores[p * K + js]);",
+     "loss[p] = (float)(log(sum) + m - (double)scores[p * K + (js + 1) % K]);"),
+    # transposed operands and off-by-one rows in the selector
+    ("pair_codebooks_swapped",
+     "bf16_value(A[(int64_t)a * r + i]) * (double)Grow[i] * bf16_value(Bc[(int64_t)b * r + i])",
+     "bf16_value(A[(int64_t)b * r + i]) * (double)Grow[i] * bf16_value(Bc[(int64_t)a * r + i])"),
+    ("pair_drops_unary", "    double s = (double)u;\n", "    double s = 0.0 * (double)u;\n"),
+    ("walk_reads_previous_row",
+     "            const int64_t row = (int64_t)q * Bsz + t;\n            float best = -INFINITY, second = -INFINITY;",
+     "            const int64_t row = (int64_t)q * Bsz + t - 1;\n            float best = -INFINITY, second = -INFINITY;"),
+    ("walk_margin_reversed",
+     "margin[q * T + (t - 1)] = (K > 1) ? (double)best - (double)second : INFINITY;",
+     "margin[q * T + (t - 1)] = (K > 1) ? (double)second - (double)best : INFINITY;"),
+    ("lattice_slot0_rows_zero",
+     "for (int32_t j = 0; j < K; ++j) Lt[(int64_t)i * K + j] = NAN;",
+     "for (int32_t j = 0; j < K; ++j) Lt[(int64_t)i * K + j] = 0.0f;"),
+    ("lattice_walk_row_stride", " + (int64_t)i * K;", " + (int64_t)i;"),
+    ("lattice_walk_path_is_column", "path[q * T + (t - 1)] = cand[pick];", "path[q * T + (t - 1)] = pick;"),
+    ("sampling_margin_counts_end_one", "if (pick < K - 1 && hi / total - u < mg)", "if (hi / total - u < mg)"),
+    ("sampling_margin_counts_end_zero", "if (pick > 0) mg = u - lo / total;", "mg = u - lo / total;"),
+    # the head: margin sign, a cap of 0, G from one row, fp32 accumulation
+    ("topk_margin_sign", "(double)c[K - 1].val - (double)c[K].val", "(double)c[K].val - (double)c[K - 1].val"),
+    ("softcap_zero_cap_applies",
+     "return cap > 0.0 ? cap * tanh(x / cap) : x;", "return cap >= 0.0 ? cap * tanh(x / cap) : x;"),
+    ("G_reads_first_row",
+     "acc += bf16_value(h[p * D + d]) * bf16_value(W_H[(int64_t)i * D + d]);",
+     "acc += bf16_value(h[d]) * bf16_value(W_H[(int64_t)i * D + d]);"),
+    ("logits_fp32_accumulate",
+     "            double acc = 0.0;\n            for (int64_t d = 0; d < D; ++d)\n"
+     "                acc += bf16_value(h[p * D + d]) * bf16_value(W[v * D + d]);",
+     "            float acc = 0.0f;\n            for (int64_t d = 0; d < D; ++d)\n"
+     "                acc += (float)(bf16_value(h[p * D + d]) * bf16_value(W[v * D + d]));"),
+    # the conv: reversed taps, one tap's correction, corrections of the wrong row
+    ("conv_base_taps_reversed",
+     "double k = (double)base[((int64_t)0 * taps + j) * C + c] +",
+     "double k = (double)base[((int64_t)0 * taps + (taps - 1 - j)) * C + c] +"),
+    ("conv_dyn_out_tap0_only",
+     "dyn_out[(p * taps + j) * G + gi] = (float)d[((int64_t)1 * taps + j) * G + gi];",
+     "dyn_out[(p * taps + j) * G + gi] = (float)d[((int64_t)1 * taps + 0) * G + gi];"),
+    ("conv_finish_dyn_from_source_row",
+     "(double)dyn_out[(p * taps + j) * G + c / g];", "(double)dyn_out[((p - j) * taps + j) * G + c / g];"),
+    ("conv_projection_reads_block_start",
+     "acc += bf16_value(W_proj[n * C + c]) * act_value(x, x_is_f32, p * C + c);",
+     "acc += bf16_value(W_proj[n * C + c]) * act_value(x, x_is_f32, (p - p % Bsz) * C + c);"),
 ]
 
 
