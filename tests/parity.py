@@ -69,7 +69,12 @@ def close_bf16(gpu_bits, ref_bits, ftol=FTOL, what=""):
     assert ok.all(), f"{what}: {(~ok).sum()} bf16 values outside tolerance"
 
 
-def compare_topk(gpu_ids, gpu_vals, ref_ids, ref_vals, ref_margin, what="topk") -> Report:
+def compare_topk(gpu_ids, gpu_vals, ref_ids, ref_vals, ref_margin, what="topk", logit_of=None) -> Report:
+    """Row by row under the flagged-margin rule.  ``logit_of(p, ids)``, when given,
+    returns the oracle's logits of those ids in row p: an id the GPU keeps and the
+    oracle does not must then have an oracle logit within MARGIN of the oracle's K-th
+    value (a real near-tie) and a GPU value within the float rule of that logit.
+    Without it, the GPU's own value for such an id is taken."""
     gpu_ids, ref_ids = np.asarray(gpu_ids), np.asarray(ref_ids)
     gpu_vals, ref_vals = np.asarray(gpu_vals), np.asarray(ref_vals)
     rep = Report()
@@ -98,9 +103,19 @@ def compare_topk(gpu_ids, gpu_vals, ref_ids, ref_vals, ref_margin, what="topk") 
             # for ids whose values sit within MARGIN of the oracle's K-th value
             if not boundary:
                 explained = False
-            for j, i in enumerate(gpu_ids[p].tolist()):
-                if i not in rs and abs(float(gpu_vals[p][j]) - rv[-1]) >= MARGIN:
-                    explained = False
+            foreign = [(j, i) for j, i in enumerate(gpu_ids[p].tolist()) if i not in rs]
+            if logit_of is not None and foreign:
+                true = np.asarray(logit_of(p, [i for _, i in foreign]), np.float64)
+                rms = float(np.sqrt(np.mean(rv * rv)))
+                for (j, _), u in zip(foreign, true):
+                    if not abs(u - rv[-1]) < MARGIN:
+                        explained = False
+                    if not abs(float(gpu_vals[p][j]) - u) <= FTOL * max(abs(u), rms) + 1e-30:
+                        explained = False
+            else:
+                for j, _ in foreign:
+                    if abs(float(gpu_vals[p][j]) - rv[-1]) >= MARGIN:
+                        explained = False
         if not explained:
             rep.unexplained.append((what, p, gpu_ids[p][:8].tolist(), ref_ids[p][:8].tolist()))
     return rep
@@ -226,7 +241,12 @@ def compare_chain(orc, w, inp, gpu, requests, extra_rows=(), conv=None, check=Tr
             ref_topk = oracle_rows_topk(orc, w, inp, rows)
         assert np.array_equal(ref_topk[0], rows), "ref_topk was computed on other rows"
         _, oi, ov, om, oG = ref_topk
-        topk = compare_topk(gi[rows], gv[rows], oi, ov, om, w.name)
+        def logit_of(k, ids):
+            # the oracle's logits of single ids in compared row k
+            h_row = np.ascontiguousarray(inp["h"][rows[k]][None, :])
+            return orc.logits(h_row, np.ascontiguousarray(inp["W_lm"][np.asarray(ids, np.int64)]))[0]
+
+        topk = compare_topk(gi[rows], gv[rows], oi, ov, om, w.name, logit_of=logit_of)
         summary["topk"] = {"compared": topk.compared, "flagged": topk.flagged, "mismatched": topk.mismatched,
                            "unexplained": len(topk.unexplained)}
         rule(topk.check, w.name + " topk")

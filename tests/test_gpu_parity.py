@@ -59,7 +59,8 @@ def run_head(df2, h, Wlm, K, WH=None):
 def check_head(orc, df2, h, Wlm, K, WH=None, what="head"):
     gi, gv, gG = run_head(df2, h, Wlm, K, WH)
     oi, ov, om, oG = orc.unary_topk(h, Wlm, K, W_H=WH)
-    rep = compare_topk(gi, gv, oi, ov, om, what)
+    rep = compare_topk(gi, gv, oi, ov, om, what,
+                       logit_of=lambda p, ids: orc.logits(h[p:p + 1], Wlm[np.asarray(ids, np.int64)])[0])
     rep.check(what)
     compare_topk_values(gi, gv, oi, ov, what + " vals")
     if WH is not None:

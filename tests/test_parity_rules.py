@@ -115,3 +115,77 @@ def test_conv_two_steps_off_fails_one_step_passes(orc, case):
     assert _run(orc, case, one)["ok"]
     s = _run(orc, case, far)
     assert not s["ok"] and any("finish" in f for f in s["failures"])
+
+
+# ------------------------------------------------ ids at a flagged K/K+1 boundary --
+
+def _lists():
+    """A row whose oracle K-th and (K+1)-th logits are 4e-4 apart (flagged)."""
+    ref_ids = np.array([[10, 11, 12, 13]], np.int32)
+    ref_vals = np.array([[4.0, 3.0, 2.0, 1.0]], np.float32)
+    return ref_ids, ref_vals, np.array([4e-4])
+
+
+def test_foreign_id_checked_against_the_oracle_logit():
+    """At a flagged boundary the GPU may keep the oracle's (K+1)-th token instead of
+    its K-th, but only if the oracle's own logit of that token is within MARGIN of the
+    K-th value and the GPU's value for it is right: a value the GPU reports is not
+    evidence."""
+    from parity import compare_topk
+    ref_ids, ref_vals, margin = _lists()
+    gpu_ids = np.array([[10, 11, 12, 99]], np.int32)
+    gpu_vals = np.array([[4.0, 3.0, 2.0, 0.9996]], np.float32)
+    near = {99: 0.9996}
+    far = {99: 0.5}
+    ok = compare_topk(gpu_ids, gpu_vals, ref_ids, ref_vals, margin, logit_of=lambda p, ids: [near[i] for i in ids])
+    assert ok.mismatched == 1 and not ok.unexplained
+    bad = compare_topk(gpu_ids, gpu_vals, ref_ids, ref_vals, margin, logit_of=lambda p, ids: [far[i] for i in ids])
+    assert len(bad.unexplained) == 1
+    # the right token with a wrong value
+    off = gpu_vals.copy()
+    off[0, 3] = 0.95
+    wrong = compare_topk(gpu_ids, off, ref_ids, ref_vals, margin, logit_of=lambda p, ids: [near[i] for i in ids])
+    assert len(wrong.unexplained) == 1
+
+
+def test_planted_tie_swap_passes_and_a_false_claim_fails(orc):
+    """The whole-batch comparator on a planted exact tie: token X gets the W_lm row
+    of row p's K-th token, so the two tie at rank K / K+1 and the oracle keeps the
+    lower id.  A GPU list holding X instead passes (a flagged near-tie); one holding
+    an unrelated token with the K-th value written beside it fails, because the
+    comparator asks the oracle for that token's logit."""
+    import bench
+    w = W.TINY.scaled(R=2)
+    inp = W.head_inputs(w, selector_std=0.3)
+    oi, _, _, _ = orc.unary_topk(inp["h"], inp["W_lm"], w.K + 1)
+    p = w.B + 1
+    a = int(oi[p, w.K - 1])
+    taken = set(int(i) for i in oi[p])
+    X = next(v for v in range(a + 1, w.V) if v not in taken)
+    Wl = inp["W_lm"].copy()
+    Wl[X] = Wl[a]
+    inp = dict(inp, W_lm=Wl)
+    conv = W.conv_inputs(w)
+    out = bench.oracle_step(orc, w, inp, conv)
+    assert int(out["ids"][p, w.K - 1]) == a
+    _, _, margin, _ = orc.unary_topk(inp["h"][p:p + 1], Wl, w.K)
+    assert margin[0] == 0.0
+
+    def run(mutate):
+        g = {k: np.array(v, copy=True) for k, v in out.items()}
+        mutate(g)
+        return compare_chain(orc, w, inp, g, range(w.R), conv=conv, check=False)
+
+    def swap(g):
+        g["ids"][p, w.K - 1] = X
+    s = run(swap)
+    assert s["topk"]["mismatched"] == 1 and s["topk"]["unexplained"] == 0, s["failures"]
+
+    U = orc.logits(inp["h"][p:p + 1], Wl)[0]
+    far = int(np.argmin(U))   # the token with the lowest logit of the row
+
+    def claim(g):
+        g["ids"][p, w.K - 1] = far
+    assert U[a] - U[far] >= MARGIN
+    s = run(claim)
+    assert s["topk"]["unexplained"] == 1 and not s["ok"]
