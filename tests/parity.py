@@ -207,11 +207,13 @@ def compare_chain(orc, w, inp, gpu, requests, extra_rows=(), conv=None, check=Tr
     Whole ``requests`` are compared through every step; ``extra_rows`` are single
     rows compared for the top-K and G only.
 
-    Top-K: the oracle on the same rows (compare_topk's flagged-margin rule).  Walk:
-    the oracle's walk over its own candidate lists where a request's lists equal
-    the GPU's; where a flagged near-tie changed a list, over the GPU's lists (the
-    walk is then judged on the candidates it was given), and in both cases the GPU
-    path must be greedy under the oracle's scores of the GPU's lists.  Teacher-forced
+    Top-K: the oracle on the same rows (compare_topk's flagged-margin rule, with the
+    oracle's logit of every token only the GPU kept).  Walk: the oracle's walk over
+    its own candidate lists where a request's lists equal the GPU's; where a flagged
+    near-tie changed a list, over the GPU's candidate ids with the oracle's logits of
+    them (the walk is then judged on the candidates it was given), and in both cases
+    the GPU path must be greedy under the oracle's scores of those lists.  No GPU
+    value is an input of the oracle: its G, logits and scores are its own.  Teacher-forced
     scores: the oracle's scorer on the same lists.  Conv: the oracle on the
     requests' anchor blocks (the conv never reads across a block), finish on the
     oracle's own correction.
@@ -260,14 +262,19 @@ def compare_chain(orc, w, inp, gpu, requests, extra_rows=(), conv=None, check=Tr
         rule(close, gG[rows], oG, what=w.name + " G")
         if req.size:
             # the lists the oracle's walk and scorer run on: the oracle's own where
-            # the request's lists match the GPU's, the GPU's otherwise
+            # the request's lists match the GPU's, the GPU's ids otherwise (a flagged
+            # near-tie changed them), always with the oracle's logits of those ids
+            # and the oracle's G, so no GPU value enters the oracle
             at = {int(p): k for k, p in enumerate(rows)}
             k_of = np.asarray([at[int(p)] for p in rrows])
             same_req = np.all((gi[rrows] == oi[k_of]).reshape(req.size, -1), axis=1)
             same_rows = np.repeat(same_req, B)[:, None]
             c_ids = np.ascontiguousarray(np.where(same_rows, oi[k_of], gi[rrows]), np.int32)
-            c_vals = np.ascontiguousarray(np.where(same_rows, ov[k_of], gv[rrows]), np.float32)
-            c_G = np.ascontiguousarray(np.where(same_rows, oG[k_of], gG[rrows]), np.float32)
+            c_vals = np.array(ov[k_of], np.float32)
+            for n in np.nonzero(~same_rows[:, 0])[0]:
+                c_vals[n] = logit_of(k_of[n], c_ids[n])
+            c_vals = np.ascontiguousarray(c_vals)
+            c_G = np.ascontiguousarray(oG[k_of], np.float32)
             anchors = np.ascontiguousarray(inp["anchors"][req])
             op, os_, omg, st = orc.selector_walk(anchors, c_ids, c_vals, c_G, inp["A"], inp["Bc"], B)
             gpath = np.ascontiguousarray(gpu["path"][req])
@@ -278,8 +285,7 @@ def compare_chain(orc, w, inp, gpu, requests, extra_rows=(), conv=None, check=Tr
             if st != 0:
                 failures.append(f"oracle walk status {st}")
             rule(walk.check, w.name + " walk")
-            rule(check_path_valid, orc, gpath, anchors, np.ascontiguousarray(gi[rrows]),
-                 np.ascontiguousarray(gv[rrows]), np.ascontiguousarray(gG[rrows]), inp["A"], inp["Bc"], B)
+            rule(check_path_valid, orc, gpath, anchors, c_ids, c_vals, c_G, inp["A"], inp["Bc"], B)
             if gpu.get("scores") is not None:
                 osc, st = orc.pair_scores(np.ascontiguousarray(inp["pred"][rrows]), c_ids, c_vals, c_G,
                                           inp["A"], inp["Bc"])

@@ -177,9 +177,18 @@ def test_planted_tie_swap_passes_and_a_false_claim_fails(orc):
         return compare_chain(orc, w, inp, g, range(w.R), conv=conv, check=False)
 
     def swap(g):
+        # a GPU that kept X: the same logit, and its walk and teacher-forced scores
+        # computed on the list it kept
         g["ids"][p, w.K - 1] = X
+        g["path"], g["pscore"], _, _ = orc.selector_walk(inp["anchors"], g["ids"], g["vals"], g["G"], inp["A"],
+                                                         inp["Bc"], w.B)
+        g["scores"], _ = orc.pair_scores(inp["pred"], g["ids"], g["vals"], g["G"], inp["A"], inp["Bc"])
     s = run(swap)
     assert s["topk"]["mismatched"] == 1 and s["topk"]["unexplained"] == 0, s["failures"]
+    assert s["walk"]["requests_on_gpu_lists"] == 1 and s["walk"]["unexplained"] == 0
+    # the walk and scores over the GPU's list agree; what fails is only the fraction
+    # rule (one mismatch in 16 compared rows is above 0.1%)
+    assert len(s["failures"]) == 1 and "mismatched positions" in s["failures"][0], s["failures"]
 
     U = orc.logits(inp["h"][p:p + 1], Wl)[0]
     far = int(np.argmin(U))   # the token with the lowest logit of the row
