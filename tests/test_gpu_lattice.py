@@ -224,23 +224,28 @@ def test_lattice_empty(df2):
     assert tuple(path.shape) == (0, 3)
 
 
-@pytest.mark.parametrize("name,nreq", [("batch1", 1), ("batched", 6), ("stress", 4)])
-def test_full_size_lattice(orc, df2, name, nreq):
-    """The workload's shapes in the launch configuration the benchmark uses: the whole
-    table on the GPU, the oracle on a few requests; greedy and sampled walks over the
-    full GPU table against the oracle's walks over that same table."""
+@pytest.mark.parametrize("name", ["batch1", "batched", "stress"])
+def test_full_size_lattice(orc, df2, name):
+    """The workload's shapes in the launch configuration the benchmark uses, every
+    request compared: the GPU table against the oracle's; the GPU walks over the
+    oracle's table against the oracle's walks over it (greedy exactly, sampled under
+    the probability margin); and the GPU walks over the GPU table against the
+    oracle's walks over its own table (the flagged-margin rule).  The oracle only
+    ever reads its own table."""
     w = W.BY_NAME[name]
     rng = np.random.default_rng(w.seed + 200)
     anchors, ids, vals, G, A, Bc = candidates(rng, w.R, w.B, w.K, w.V, w.r)
     gl = gpu_lattice(df2, anchors, ids, vals, G, A, Bc, w.B)
-    reqs = np.unique(np.linspace(0, w.R - 1, nreq).astype(int))
-    rows = (reqs[:, None] * w.B + np.arange(w.B)[None, :]).reshape(-1)
-    ol, _ = orc.lattice(anchors[reqs], ids[rows], vals[rows], G[rows], A, Bc, w.B)
-    check_table(gl[reqs], ol, name + " lattice")
+    ol, st = orc.lattice(anchors, ids, vals, G, A, Bc, w.B)
+    assert st == 0
+    check_table(gl, ol, name + " lattice")
+    op, os_, om, _ = orc.lattice_walk(ol, ids, w.B, w.V)
+    gp, gs = gpu_walk(df2, ol, ids, w.B, w.V)
+    assert np.array_equal(gp, op) and np.array_equal(gs, os_), name + " greedy walk over the oracle table"
     gp, gs = gpu_walk(df2, gl, ids, w.B, w.V)
-    op, os_, _, _ = orc.lattice_walk(gl, ids, w.B, w.V)
-    assert np.array_equal(gp, op) and np.array_equal(gs, os_)
+    compare_walk(gp, gs, op, os_, om, name + " greedy").check(name + " greedy")
     u = rng.random((w.R, w.B - 1)).astype(np.float32)
-    sp, ss = gpu_walk(df2, gl, ids, w.B, w.V, uniforms=u, temperature=1.0)
-    op2, os2, om2, _ = orc.lattice_walk(gl, ids, w.B, w.V, uniforms=u, temperature=1.0)
-    compare_sampled(sp, ss, op2, os2, om2, name + " sampling").check(name + " sampling")
+    op2, os2, om2, _ = orc.lattice_walk(ol, ids, w.B, w.V, uniforms=u, temperature=1.0)
+    for table, what in ((ol, " sampling over the oracle table"), (gl, " sampling")):
+        sp, ss = gpu_walk(df2, table, ids, w.B, w.V, uniforms=u, temperature=1.0)
+        compare_sampled(sp, ss, op2, os2, om2, name + what).check(name + what)
