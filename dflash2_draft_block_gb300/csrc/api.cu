@@ -66,7 +66,7 @@ namespace {
 int check_head(int64_t P, int64_t D, int64_t V, int K, int r, bool has_wh) {
     if (P < 0 || D < 1 || V < 1 || K < 1 || K > V) return DF2_ERR_INVALID_ARGUMENT;
     if (has_wh && r < 1) return DF2_ERR_INVALID_ARGUMENT;
-    if (D % 8 != 0 || K > DF2_MAX_TOPK || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (D % 8 != 0 || K > DF2_MAX_TOPK || V > DF2_MAX_VOCAB) return DF2_ERR_UNSUPPORTED;
     if (has_wh && (r > DF2_MAX_RANK || r % 8 != 0)) return DF2_ERR_UNSUPPORTED;
     if (!df2::head_simple_supported(D, K)) return DF2_ERR_UNSUPPORTED;
     return DF2_OK;
@@ -248,7 +248,7 @@ namespace {
 
 int check_selector(int64_t V, int K, int r) {
     if (V < 1 || K < 1 || r < 1) return DF2_ERR_INVALID_ARGUMENT;
-    if (K > DF2_MAX_TOPK || r > DF2_MAX_RANK || r % 8 != 0 || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (K > DF2_MAX_TOPK || r > DF2_MAX_RANK || r % 8 != 0 || V > DF2_MAX_VOCAB) return DF2_ERR_UNSUPPORTED;
     return DF2_OK;
 }
 
@@ -290,7 +290,7 @@ DF2_API int dflash2_selector_ce(const float* scores, const int32_t* topk_ids, co
                                 int64_t P, int K, int64_t V, float* loss, int32_t* label_idx,
                                 int32_t* dev_status, void* stream) {
     if (P < 0 || K < 1 || V < 1) return DF2_ERR_INVALID_ARGUMENT;
-    if (K > DF2_MAX_TOPK || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (K > DF2_MAX_TOPK || V > DF2_MAX_VOCAB) return DF2_ERR_UNSUPPORTED;
     if (P == 0) return DF2_OK;
     if (!scores || !topk_ids || !targets || !loss) return DF2_ERR_INVALID_ARGUMENT;
     if ((P + 7) / 8 > INT32_MAX) return DF2_ERR_UNSUPPORTED;
@@ -322,7 +322,7 @@ DF2_API int dflash2_lattice_walk(const float* lattice, const int32_t* topk_ids, 
                                  int64_t V, const float* uniforms, float temperature, int32_t* path,
                                  float* path_scores, int32_t* dev_status, void* stream) {
     if (R < 0 || B < 2 || K < 1 || V < 1 || K > V) return DF2_ERR_INVALID_ARGUMENT;
-    if (K > DF2_MAX_TOPK || V > INT32_MAX) return DF2_ERR_UNSUPPORTED;
+    if (K > DF2_MAX_TOPK || V > DF2_MAX_VOCAB) return DF2_ERR_UNSUPPORTED;
     if (uniforms && !(temperature > 0.f && temperature <= FLT_MAX)) return DF2_ERR_INVALID_ARGUMENT;
     if (R == 0) return DF2_OK;
     if (!lattice || !topk_ids || !path || !path_scores) return DF2_ERR_INVALID_ARGUMENT;

@@ -73,9 +73,12 @@ extern "C" {
 #define DF2_STATUS_ID_OUT_OF_RANGE 0x1  /* a token id outside [0, V) was read */
 #define DF2_STATUS_WAIT_TIMEOUT 0x2     /* a bounded in-kernel wait gave up; outputs invalid */
 
-/* Limits of this build (DF2_ERR_UNSUPPORTED beyond them). */
+/* Limits of this build (DF2_ERR_UNSUPPORTED beyond them).  DF2_MAX_VOCAB bounds V
+ * (token ids, rows of W_lm, A and Bc) so that a row index plus a tile's rows stays
+ * inside int32 in every kernel. */
 #define DF2_MAX_TOPK 1024
 #define DF2_MAX_RANK 4096
+#define DF2_MAX_VOCAB (1 << 30)
 
 /* Name of a return code ("DF2_OK", ...); never NULL. */
 const char* dflash2_status_string(int status);
@@ -132,7 +135,7 @@ int dflash2_unary_topk_path(int64_t P, int64_t D, int64_t V, int K);
  *   topk_ids  [P, K]  int32       out
  *   topk_vals [P, K]  fp32        out
  *   workspace                      >= dflash2_unary_topk_workspace_size(P, D, V, K, r)
- * Rules: P >= 0 (P = 0 launches nothing), D >= 1, D % 8 == 0, V >= 1.
+ * Rules: P >= 0 (P = 0 launches nothing), D >= 1, D % 8 == 0, 1 <= V <= DF2_MAX_VOCAB.
  * ---------------------------------------------------------------------- */
 size_t dflash2_unary_topk_workspace_size(int64_t P, int64_t D, int64_t V, int K, int r);
 int dflash2_unary_topk(const uint16_t* h, int64_t P, int64_t D, const uint16_t* W_lm, int64_t V,
@@ -194,7 +197,8 @@ int dflash2_unary_topk_noalloc(const uint16_t* h, int64_t P, int64_t D, const ui
  *   A, Bc       [V, r]     bf16    predecessor / successor codebooks
  *   path        [R, B-1]   int32   out
  *   path_scores [R, B-1]   fp32    out
- * Rules: R >= 0, B >= 2, 1 <= K <= min(V, DF2_MAX_TOPK), 1 <= r <= DF2_MAX_RANK.
+ * Rules: R >= 0, B >= 2, 1 <= K <= min(V, DF2_MAX_TOPK), 1 <= r <= DF2_MAX_RANK,
+ * V <= DF2_MAX_VOCAB.
  * An anchor or candidate id outside [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and
  * writes -1 / NaN over that request's whole path.
  * ---------------------------------------------------------------------- */
@@ -213,7 +217,7 @@ int dflash2_selector_walk(const int32_t* anchors, int R, int B, const int32_t* t
  *
  *   pred [P] int32; topk_ids/topk_vals [P, K]; G [P, r]; A, Bc [V, r] bf16;
  *   scores [P, K] fp32 out.
- * Rules: P >= 0, 1 <= K <= DF2_MAX_TOPK, 1 <= r <= DF2_MAX_RANK, V >= 1.
+ * Rules: P >= 0, 1 <= K <= DF2_MAX_TOPK, 1 <= r <= DF2_MAX_RANK, 1 <= V <= DF2_MAX_VOCAB.
  * A pred or candidate id outside [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and
  * writes NaN for the affected scores.
  * ---------------------------------------------------------------------- */
@@ -241,7 +245,7 @@ int dflash2_selector_pair_scores(const int32_t* pred, int64_t P, const int32_t* 
  *   scores [P, K] fp32 (dflash2_selector_pair_scores' output); topk_ids [P, K]
  *   int32; targets [P] int32 (the ground-truth token of each row, < 0: none);
  *   loss [P] fp32 out; label_idx [P] int32 out (nullable).
- * Rules: P >= 0, 1 <= K <= DF2_MAX_TOPK, V >= 1.  A target >= V sets
+ * Rules: P >= 0, 1 <= K <= DF2_MAX_TOPK, 1 <= V <= DF2_MAX_VOCAB.  A target >= V sets
  * DF2_STATUS_ID_OUT_OF_RANGE (label -1, loss NaN).
  * ---------------------------------------------------------------------- */
 int dflash2_selector_ce(const float* scores, const int32_t* topk_ids, const int32_t* targets, int64_t P,
@@ -338,9 +342,9 @@ int dflash2_selector_lattice(const int32_t* anchors, int R, int B, const int32_t
  *   temperature                 host float, > 0 and finite when uniforms is given
  *   path        [R, B-1]        int32  out
  *   path_scores [R, B-1]        fp32   out
- * Rules: R >= 0, B >= 2, 1 <= K <= min(V, DF2_MAX_TOPK).  A candidate id outside
- * [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and writes -1 / NaN over that request's
- * path.  The sampling draw computes its weights and running sums in fp32, so a u
+ * Rules: R >= 0, B >= 2, 1 <= K <= min(V, DF2_MAX_TOPK), V <= DF2_MAX_VOCAB.  A
+ * candidate id outside [0, V) sets DF2_STATUS_ID_OUT_OF_RANGE and writes -1 / NaN
+ * over that request's path.  The sampling draw computes its weights and running sums in fp32, so a u
  * that lies within rounding of an interval end may pick the neighbouring column.
  * ---------------------------------------------------------------------- */
 int dflash2_lattice_walk(const float* lattice, const int32_t* topk_ids, int R, int B, int K,

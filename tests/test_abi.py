@@ -58,6 +58,11 @@ def test_head_validation(lib):
     assert f(fake, 4, 64, fake, 5000, 2000, 1.0, 0.0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 2
     # W_H given with r < 1
     assert f(fake, 4, 64, fake, 10, 2, 1.0, 0.0, fake, 0, fake, fake, fake, fake, 1 << 20, None, None) == 1
+    # V above the build limit (DF2_MAX_VOCAB = 2^30), and at the int32 edge
+    for V in ((1 << 30) + 1, (1 << 31) - 1):
+        assert f(fake, 4, 64, fake, V, 16, 1.0, 0.0, None, 0, None, fake, fake, fake, 1 << 20, None, None) == 2
+        assert lib.dflash2_unary_topk_path(8, 4096, V, 16) == -1
+    assert lib.dflash2_unary_topk_path(8, 4096, 1 << 30, 16) == 0
     # P == 0 is a no-op
     assert f(fake, 0, 64, fake, 10, 2, 1.0, 0.0, None, 0, None, fake, fake, fake, 0, None, None) == 0
     # output multiplier finite and > 0, final softcap finite and >= 0
@@ -85,6 +90,9 @@ def test_selector_validation(lib):
     assert w(fake, 2, 8, fake, fake, fake, fake, fake, 100, 101, 32, fake, fake, None, None) == 1  # K > V
     assert w(fake, 2, 8, fake, fake, fake, fake, fake, 100, 4, 12, fake, fake, None, None) == 2  # r % 8
     assert w(fake, 0, 8, fake, fake, fake, fake, fake, 100, 4, 32, fake, fake, None, None) == 0
+    assert w(fake, 2, 8, fake, fake, fake, fake, fake, (1 << 30) + 1, 4, 32, fake, fake, None, None) == 2
+    assert lib.dflash2_lattice_walk(fake, fake, 2, 8, 4, (1 << 30) + 1, None, 1.0, fake, fake, None, None) == 2
+    assert lib.dflash2_selector_ce(fake, fake, fake, 4, 4, (1 << 30) + 1, fake, fake, None, None) == 2
     dh = lib.dflash2_draft_head
     f8 = [fake] * 8
     # B < 2, K > V, r % 8, W_H missing, workspace too small
