@@ -15,7 +15,14 @@ wide sweep:
   `tile(k)`), for single CTAs, CTA pairs and clusters of two pairs, with and without
   the last round in half tiles: every (128-row tile, channel group) pair of the
   problem is computed by exactly one CTA, and nothing past the padded last pair
-  tile or the last group is touched.
+  tile or the last group is touched;
+- the many-position GEMM's plan (`wide_plan`) and the kernel's tile walk, for the
+  top-K epilogue (CTAs, pairs, clusters of two pairs, with G riding on the short
+  last vocabulary range) and the store epilogue (the linear round-robin walk):
+  every (M tile, N tile) is computed once, every row gets exactly the partial lists
+  the workspace holds, the G tile once per M tile, and the two pairs of a cluster
+  share their vocabulary range.  The occupancy queries the plan makes on a GPU
+  (pipeline stages, clusters that fit) are parameters of the sweep.
 """
 import ctypes
 import os
@@ -65,7 +72,13 @@ def _harness():
     frag_start = kernel.index("    const int n_rows_units")
     frag = kernel[frag_start:kernel.index(_block(kernel, "auto tile = [&](int k) {"))] + \
         _block(kernel, "auto tile = [&](int k) {")
+    gemm = _read("gemm_tc.cu")
+    wk = gemm[gemm.index("gemm_wide_kernel(const __grid_constant__"):]
+    w_start = wk.index("    const int n_groups = (args.n_nt + args.tiles_per_cta - 1) / args.tiles_per_cta;")
+    w_last = _block(wk, "auto tile_mt = [&](int k) {")
+    frag_w = wk[w_start:wk.index(w_last)] + w_last
     return f"""
+#include <algorithm>
 #include <cstdint>
 #include <vector>
 
@@ -152,6 +165,113 @@ int cover(int n_mt, int n_gt, int ng, int slots, int* n_half_out) {{
 }}
 }}  // namespace conv
 
+namespace wide {{
+using std::min;
+{_line(gemm, "constexpr int WM = ")}
+{_line(gemm, "enum { EPI_STORE = 0, EPI_TOPK = 1 };")}
+{_block(gemm, "struct WideArgs {")}
+// the plan's two occupancy queries, as sweep parameters
+int g_stages = 3, g_mc_slots = 0;
+int wide_stages(int, int, bool) {{ return g_stages; }}
+int mc_cluster_slots(int, int) {{ return g_mc_slots; }}
+{_block(gemm, "int wide_bn(int epi, int K) {")}
+{_block(gemm, "int wide_groups(int n_mt, int n_nt, int num_sms) {")}
+{_block(gemm, "struct WidePlan {")}
+{_block(gemm, "WidePlan wide_plan(int epi, int64_t M, int64_t N, int K, int num_sms, bool persistent) {")}
+namespace tc {{
+uint32_t g_crank = 0;
+inline uint32_t cluster_ctarank() {{ return g_crank; }}
+}}
+
+template <int EPI, bool PAIR, bool GT, bool MC>
+int cover(const WidePlan& p, const WideArgs& args) {{
+    const int grid = (p.pair ? 2 : 1) * p.units;
+    const int pad_mt = PAIR ? 2 * ((args.n_mt + 1) / 2) : args.n_mt;
+    std::vector<int> cnt(size_t(pad_mt) * args.n_nt, 0), gcnt(pad_mt, 0), lists(size_t(pad_mt) * p.n_groups, 0);
+    std::vector<int> grp_of(grid, -1), mu_of(grid, -1);
+    for (int bid = 0; bid < grid; ++bid) {{
+        tc::g_crank = MC ? bid % 4 : (PAIR ? bid % 2 : 0);
+{frag_w}
+        grp_of[bid] = grp;
+        mu_of[bid] = mu;
+        for (int k = 0; k < ntiles; ++k) {{
+            const int nt = tile_nt(k), mtk = tile_mt(k);
+            if (mtk < 0 || mtk >= pad_mt) return 1;
+            if (tile_is_g(k)) {{
+                if (nt != 0) return 2;
+                ++gcnt[mtk];
+            }} else {{
+                if (nt < 0 || nt >= args.n_nt) return 3;
+                ++cnt[size_t(mtk) * args.n_nt + nt];
+            }}
+        }}
+        if (EPI == EPI_TOPK) {{
+            if (grp < 0 || grp >= p.n_groups) return 4;   // a list slot the workspace lacks
+            ++lists[size_t(mt) * p.n_groups + grp];
+        }}
+    }}
+    for (int m = 0; m < pad_mt; ++m) {{
+        for (int n = 0; n < args.n_nt; ++n) {{
+            const int v = cnt[size_t(m) * args.n_nt + n];
+            if (v > 1 || (v == 0 && m < args.n_mt)) return 5;
+        }}
+        if (m < args.n_mt && gcnt[m] != (GT ? 1 : 0)) return 6;
+        if (EPI == EPI_TOPK && m < args.n_mt)
+            for (int g = 0; g < p.n_groups; ++g)
+                if (lists[size_t(m) * p.n_groups + g] != 1) return 7;
+    }}
+    if (MC)
+        for (int bid = 0; bid < grid; bid += 4)
+            if (grp_of[bid] != grp_of[bid + 2] || mu_of[bid + 2] != mu_of[bid] + 1) return 8;
+    return 0;
+}}
+}}  // namespace wide
+
+// 0 when the plan of this shape covers it (see cover), else the broken rule's code;
+// plan_out: pair, mc, units, n_groups, G folded
+extern "C" int wide_cover(int epi, int64_t M, int64_t N, int K, int sms, int stages, int mc_slots, int64_t r,
+                          int* plan_out) {{
+    using namespace wide;
+    g_stages = stages;
+    g_mc_slots = mc_slots;
+    const WidePlan p = wide_plan(epi, M, N, K, sms, epi == EPI_TOPK);
+    WideArgs a{{}};
+    a.M = int(M);
+    a.N = int(N);
+    a.n_mt = p.n_mt;
+    a.n_nt = p.n_nt;
+    a.tiles_per_cta = p.tiles_per_cta;
+    a.K = K;
+    bool fold = false;
+    if (epi == EPI_STORE) {{
+        a.m_major = 1;
+        a.linear = p.linear ? 1 : 0;
+        a.n_units = p.units;
+    }} else {{
+        const bool want_g = r > 0;
+        float* G = nullptr;
+        const int n_groups = p.n_groups;
+        {_line(gemm, "    const int last_rng = p.n_nt - (p.n_groups - 1) * p.tiles_per_cta;").strip()}
+        {_line(gemm, "    const bool fold_g = want_g && r <= 256 && last_rng < p.tiles_per_cta;").strip()}
+        {_block(gemm, "if (fold_g) {")}
+        fold = fold_g;
+        (void)n_groups;
+    }}
+    plan_out[0] = p.pair;
+    plan_out[1] = p.mc;
+    plan_out[2] = p.units;
+    plan_out[3] = p.n_groups;
+    plan_out[4] = fold;
+    if (epi == EPI_STORE)
+        return p.pair ? cover<EPI_STORE, true, false, false>(p, a) : cover<EPI_STORE, false, false, false>(p, a);
+    if (a.n_gt > 0) {{
+        if (p.mc) return cover<EPI_TOPK, true, true, true>(p, a);
+        return p.pair ? cover<EPI_TOPK, true, true, false>(p, a) : cover<EPI_TOPK, false, true, false>(p, a);
+    }}
+    if (p.mc) return cover<EPI_TOPK, true, false, true>(p, a);
+    return p.pair ? cover<EPI_TOPK, true, false, false>(p, a) : cover<EPI_TOPK, false, false, false>(p, a);
+}}
+
 // kind: 0 single CTAs, 1 CTA pairs, 2 clusters of two pairs
 extern "C" int conv_cover(int kind, int n_mt, int n_gt, int ng, int slots, int* n_half) {{
     if (kind == 0) return conv::cover<false, false>(n_mt, n_gt, ng, slots, n_half);
@@ -174,6 +294,9 @@ def plans(tmp_path_factory):
     so = ctypes.CDLL(str(lib))
     so.head_sweep.restype = ctypes.c_int64
     so.head_sweep.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    so.wide_cover.restype = ctypes.c_int
+    so.wide_cover.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_int] * 4 + [
+        ctypes.c_int64, ctypes.POINTER(ctypes.c_int)]
     so.conv_cover.restype = ctypes.c_int
     so.conv_cover.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
     return so
@@ -210,3 +333,32 @@ def test_conv_prepare_schedule_at_the_workloads(plans):
         for ng, kind, slots in ((40, 1, 76), (32, 2, 36), (40, 2, 36), (64, 0, 152)):
             if 320 % ng == 0:
                 assert plans.conv_cover(kind, n_mt, 320 // ng, ng, slots, ctypes.byref(n_half)) == 0
+
+
+_M = list(range(1, 65)) + [100, 127, 128, 129, 255, 256, 257, 384, 511, 512, 513, 1000, 1024, 2048, 4096, 4097]
+
+
+@pytest.mark.parametrize("N", [151936, 248320, 40000, 9000, 3000, 257, 256, 100])
+def test_wide_gemm_topk_schedule(plans, N):
+    out = (ctypes.c_int * 5)()
+    seen = set()
+    for M in _M:
+        for K in (16, 64):
+            for sms in (152, 148):
+                for stages, mc in ((3, 0), (2, 0), (3, 18), (3, 36), (4, 19)):
+                    for r in (0, 64, 256, 512):
+                        rc = plans.wide_cover(1, M, N, K, sms, stages, mc, r, out)
+                        assert rc == 0, (M, N, K, sms, stages, mc, r, rc, list(out))
+                        seen.add((out[0], out[1], out[4]))
+    if N >= 40000:
+        # CTAs and pairs, clusters of two pairs, with and without G on the last range
+        assert {(0, 0), (1, 0), (1, 1)} <= {(p, m) for p, m, _ in seen}, seen
+        assert {0, 1} <= {f for _, _, f in seen}, seen
+
+
+@pytest.mark.parametrize("N", [256, 512, 1280, 2560, 10240, 100, 300])
+def test_wide_gemm_store_schedule(plans, N):
+    out = (ctypes.c_int * 5)()
+    for M in _M + [16384]:
+        for sms in (152, 148):
+            assert plans.wide_cover(0, M, N, 0, sms, 3, 0, 0, out) == 0, (M, N, sms)
