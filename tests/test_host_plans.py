@@ -22,7 +22,12 @@ wide sweep:
   every (M tile, N tile) is computed once, every row gets exactly the partial lists
   the workspace holds, the G tile once per M tile, and the two pairs of a cluster
   share their vocabulary range.  The occupancy queries the plan makes on a GPU
-  (pipeline stages, clusters that fit) are parameters of the sweep.
+  (pipeline stages, clusters that fit) are parameters of the sweep;
+- the conv apply ring (`bulk_plan` and the producer warp's copy loop): every 1-D
+  bulk copy starts and ends on a 16-byte boundary on both sides (the instruction
+  faults otherwise), stays inside its tensor and inside its ring buffer, the copies
+  of one item tile the buffer's bytes without overlap, and they add up to the byte
+  count the buffer's barrier is told to expect (a mismatch would stall it).
 """
 import ctypes
 import os
@@ -77,8 +82,21 @@ def _harness():
     w_start = wk.index("    const int n_groups = (args.n_nt + args.tiles_per_cta - 1) / args.tiles_per_cta;")
     w_last = _block(wk, "auto tile_mt = [&](int k) {")
     frag_w = wk[w_start:wk.index(w_last)] + w_last
+    capp = _read("conv.cu")
+    ck = capp[capp.index("conv_apply_bulk_kernel(const T* __restrict__ x"):]
+    ck = ck[:ck.index("// Few rows: one thread per (row")]
+    c_start = ck.index("            const int64_t item = blockIdx.x + k * stride;")
+    c_loop = _block(ck[c_start:], "for (int e = lane; e < B * per_row; e += 32) {")
+    frag_c = ck[c_start:ck.index(c_loop, c_start)] + c_loop
+    ln_ngrp = _line(ck, "    const int ngrp = nt * N / g;")
+    ln_row = _line(ck, "    const uint32_t row = uint32_t(nt) * 16;")
+    ln_xbytes = _line(ck, "    const uint32_t xbytes = uint32_t(B) * row;")
+    ln_rbytes = _line(ck, "    const uint32_t rbytes = RES ? xbytes : 0u;")
+    ln_per_row = _line(ck, "        const int per_row = (RES ? 2 : 1) + TAPS;")
+    ln_n_mine = _line(ck, "    const int64_t n_mine = blockIdx.x < n_items ?")
     return f"""
 #include <algorithm>
+#include <utility>
 #include <cstdint>
 #include <vector>
 
@@ -272,6 +290,112 @@ extern "C" int wide_cover(int epi, int64_t M, int64_t N, int K, int sms, int sta
     return p.pair ? cover<EPI_TOPK, true, false, false>(p, a) : cover<EPI_TOPK, false, false, false>(p, a);
 }}
 
+namespace capply {{
+template <typename T>
+struct Vec {{
+    static constexpr int N = 16 / int(sizeof(T));
+}};
+{_line(capp, "constexpr int kBulkMaxStages = ")}
+{_block(capp, "struct BulkPlan {")}
+{_block(capp, "template <typename T>" + chr(10) + "BulkPlan bulk_plan(")}
+
+struct Copy {{
+    uint64_t dst, src, bytes;
+}};
+std::vector<Copy> g_copies;
+uint64_t g_expect = 0;
+namespace tc {{
+inline void mbar_arrive_expect_tx(uint64_t*, uint32_t bytes) {{ g_expect += bytes; }}
+inline void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t*, uint64_t) {{
+    g_copies.push_back(Copy{{uint64_t(reinterpret_cast<uintptr_t>(dst)), uint64_t(reinterpret_cast<uintptr_t>(src)), bytes}});
+}}
+}}  // namespace tc
+inline void __syncwarp() {{}}
+
+// The launch's copies, CTA by CTA and item by item, for one shape; the tensors sit
+// at 16-byte-aligned addresses that are never dereferenced.  0, -1 (no ring plan:
+// the launch takes another kernel), or the code of the broken rule.
+template <typename T, int TAPS, bool RES>
+int check(int64_t nblocks, int C, int B, int g, int dyn_mult, int grid) {{
+    const int G = C / g;
+    const int64_t dyn_ld = int64_t(dyn_mult) * TAPS * G;
+    const int64_t P = nblocks * B;
+    const BulkPlan bp = bulk_plan<T>(C, B, TAPS, g, G, dyn_ld, RES);
+    if (bp.nt == 0) return -1;
+    if (bp.smem > 227u * 1024u || bp.stages < 2 || bp.stages > kBulkMaxStages) return 10;
+    if (bp.buf % 128 != 0 || bp.smem < uint32_t(bp.stages) * bp.buf + 2 * kBulkMaxStages * 8 + 4) return 11;
+    constexpr int N = Vec<T>::N;
+    const int nt = bp.nt, strips = bp.strips, stages = bp.stages;
+    const uint32_t buf_bytes = bp.buf;
+{ln_ngrp}
+{ln_row}
+{ln_xbytes}
+{ln_rbytes}
+{ln_per_row}
+    if (int64_t(strips) * nt * N != C) return 12;
+    const T* x = reinterpret_cast<const T*>(uintptr_t(1) << 40);
+    const T* res = reinterpret_cast<const T*>(uintptr_t(2) << 40);
+    const float* dyn = reinterpret_cast<const float*>(uintptr_t(3) << 40);
+    uint8_t* smem = reinterpret_cast<uint8_t*>(uintptr_t(4) << 40);
+    uint64_t full[kBulkMaxStages] = {{}};
+    const uint64_t pol = 0;
+    const int64_t n_items = nblocks * strips;
+    const int64_t stride = grid;
+    for (int64_t bx = 0; bx < grid; ++bx) {{
+        const struct {{
+            int64_t x;
+        }} blockIdx = {{bx}};
+{ln_n_mine}
+        for (int64_t k = 0; k < n_mine; ++k) {{
+            const int s = int(k % stages);
+            g_copies.clear();
+            g_expect = 0;
+            for (int lane = 0; lane < 32; ++lane) {{
+{frag_c}
+            }}
+            // every copy: 16-byte aligned at both ends, inside its tensor or buffer
+            uint64_t sum = 0;
+            const uint64_t b0 = (uintptr_t(4) << 40) + uint64_t(s) * buf_bytes;
+            std::vector<std::pair<uint64_t, uint64_t>> spans;
+            for (const Copy& c : g_copies) {{
+                if (c.bytes == 0 || c.bytes % 16 || c.src % 16 || c.dst % 16) return 1;
+                const uint64_t base = c.src >> 40 << 40;
+                const uint64_t size = base == (uintptr_t(3) << 40) ? uint64_t(P) * dyn_ld * 4 : uint64_t(P) * C * sizeof(T);
+                if (c.src + c.bytes > base + size) return 2;
+                if (base == (uintptr_t(2) << 40) && !RES) return 3;
+                if (c.dst < b0 || c.dst + c.bytes > b0 + buf_bytes) return 4;
+                spans.push_back({{c.dst - b0, c.dst - b0 + c.bytes}});
+                sum += c.bytes;
+            }}
+            if (sum != g_expect) return 5;
+            std::sort(spans.begin(), spans.end());
+            uint64_t at = 0;
+            for (const auto& sp : spans) {{
+                if (sp.first != at) return 6;   // a gap or an overlap
+                at = sp.second;
+            }}
+            if (at != xbytes + rbytes + uint64_t(B) * TAPS * ngrp * 4) return 7;
+        }}
+    }}
+    return 0;
+}}
+}}  // namespace capply
+
+extern "C" int conv_apply_copies(int f32, int taps, int res, int64_t nblocks, int C, int B, int g, int dyn_mult,
+                                 int grid) {{
+    using namespace capply;
+#define DF2T_CASE(TP)                                                                           \
+    if (taps == TP) {{                                                                            \
+        if (f32) return res ? check<float, TP, true>(nblocks, C, B, g, dyn_mult, grid)            \
+                            : check<float, TP, false>(nblocks, C, B, g, dyn_mult, grid);          \
+        return res ? check<uint16_t, TP, true>(nblocks, C, B, g, dyn_mult, grid)                  \
+                   : check<uint16_t, TP, false>(nblocks, C, B, g, dyn_mult, grid);                \
+    }}
+    DF2T_CASE(1) DF2T_CASE(2) DF2T_CASE(3) DF2T_CASE(4)
+#undef DF2T_CASE
+    return 99;
+}}
+
 // kind: 0 single CTAs, 1 CTA pairs, 2 clusters of two pairs
 extern "C" int conv_cover(int kind, int n_mt, int n_gt, int ng, int slots, int* n_half) {{
     if (kind == 0) return conv::cover<false, false>(n_mt, n_gt, ng, slots, n_half);
@@ -297,6 +421,8 @@ def plans(tmp_path_factory):
     so.wide_cover.restype = ctypes.c_int
     so.wide_cover.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64] + [ctypes.c_int] * 4 + [
         ctypes.c_int64, ctypes.POINTER(ctypes.c_int)]
+    so.conv_apply_copies.restype = ctypes.c_int
+    so.conv_apply_copies.argtypes = [ctypes.c_int] * 3 + [ctypes.c_int64] + [ctypes.c_int] * 5
     so.conv_cover.restype = ctypes.c_int
     so.conv_cover.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
     return so
@@ -362,3 +488,21 @@ def test_wide_gemm_store_schedule(plans, N):
     for M in _M + [16384]:
         for sms in (152, 148):
             assert plans.wide_cover(0, M, N, 0, sms, 3, 0, 0, out) == 0, (M, N, sms)
+
+
+@pytest.mark.parametrize("f32", [0, 1])
+@pytest.mark.parametrize("taps", [1, 2, 3, 4])
+def test_conv_apply_bulk_copies(plans, f32, taps):
+    planned = 0
+    for res in (0, 1):
+        for C in (512, 640, 2048, 4096, 5120, 8192):
+            for B in (1, 2, 4, 8, 16, 32):
+                if taps > B:
+                    continue
+                for g in (8, 16, 64):
+                    for dyn_mult in (1, 2):
+                        for nblocks, grid in ((5, 3), (2, 152)):
+                            rc = plans.conv_apply_copies(f32, taps, res, nblocks, C, B, g, dyn_mult, grid)
+                            assert rc in (0, -1), (f32, taps, res, C, B, g, dyn_mult, nblocks, grid, rc)
+                            planned += rc == 0
+    assert planned > 50   # shapes the ring takes, not only the fallbacks
