@@ -56,13 +56,21 @@ def _p(t):
     return ct.c_void_p(t.data_ptr() if t is not None else 0)
 
 
-def _stream(stream):
+def _on_device(t):
+    return t.is_cuda
+
+
+def _stream(stream, device):
+    """The CUDA stream handle of `stream` (default: the current one), which must
+    belong to the device of the call's tensors."""
     s = stream if stream is not None else torch.cuda.current_stream()
+    if s.device != device:
+        raise ValueError(f"the stream is on {s.device}, the call's tensors on {device}")
     return ct.c_void_p(s.cuda_stream)
 
 
 def _need(t, name, dtype, ndim=None):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+    if not isinstance(t, torch.Tensor) or not _on_device(t):
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -72,19 +80,59 @@ def _need(t, name, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
 
 
+def _device(first, **others):
+    """The device of the call: `first`'s, which every other given tensor shares and
+    which is the current CUDA device (the library launches on the current device)."""
+    dev = first.device
+    for name, t in others.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the call's tensors on {dev}")
+    if dev.type == "cuda" and dev.index is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"the tensors are on {dev} but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()} (torch.cuda.set_device first)")
+    return dev
+
+
+def _out(t, name, dtype, numel, dev):
+    """A caller-given output: a contiguous tensor of the call's device, dtype and
+    element count (the kernels write numel elements through its pointer)."""
+    _need(t, name, dtype)
+    if t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got shape {tuple(t.shape)}")
+    if t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, the call's tensors on {dev}")
+    return t
+
+
+def _status(st, dev):
+    """dev_status: None, or one int32 word (at least) on the call's device."""
+    if st is not None:
+        _need(st, "dev_status", torch.int32)
+        if st.numel() < 1 or st.device != dev:
+            raise ValueError("dev_status must hold an int32 word on the call's device")
+    return st
+
+
 def _check(call, rc):
     if rc != 0:
         raise DFlash2Error(call, rc)
 
 
 def _workspace(nbytes, workspace, device):
-    if nbytes == 0:
+    if nbytes == 0 and workspace is None:
         return None
     if workspace is None:
         return torch.empty(nbytes, dtype=torch.uint8, device=device)
-    if workspace.numel() * workspace.element_size() < nbytes:
+    _need(workspace, "workspace", workspace.dtype)
+    if workspace.device != device:
+        raise ValueError(f"workspace is on {workspace.device}, the call's tensors on {device}")
+    if _nbytes(workspace) < nbytes:
         raise ValueError(f"workspace too small: need {nbytes} bytes")
     return workspace
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
 
 
 def unary_topk_workspace_size(P, D, V, K, r=0) -> int:
@@ -109,18 +157,23 @@ def unary_topk(h, W_lm, K, W_H=None, *, output_multiplier=1.0, final_logit_softc
         r = W_H.shape[0]
         if W_H.shape[1] != D:
             raise ValueError("W_H must be [r, D]")
-    dev = h.device
+    dev = _device(h, W_lm=W_lm, W_H=W_H)
     if out is None:
         ids = torch.empty((P, K), dtype=torch.int32, device=dev)
         vals = torch.empty((P, K), dtype=torch.float32, device=dev)
         G = torch.empty((P, r), dtype=torch.float32, device=dev) if r else None
     else:
         ids, vals, G = out
+        _out(ids, "ids", torch.int32, P * K, dev)
+        _out(vals, "vals", torch.float32, P * K, dev)
+        if r:
+            _out(G, "G", torch.float32, P * r, dev)
+    _status(dev_status, dev)
     ws = _workspace(unary_topk_workspace_size(P, D, V, K, r), workspace, dev)
     rc = lib().dflash2_unary_topk(_p(h), P, D, _p(W_lm), V, int(K), float(output_multiplier),
                                   float(final_logit_softcapping), _p(W_H), r, _p(G), _p(ids),
-                                  _p(vals), _p(ws), 0 if ws is None else ws.numel(),
-                                  _p(dev_status), _stream(stream))
+                                  _p(vals), _p(ws), _nbytes(ws),
+                                  _p(dev_status), _stream(stream, dev))
     _check("dflash2_unary_topk", rc)
     return ids, vals, G
 
@@ -134,16 +187,29 @@ def unary_topk_noalloc(h, W_lm, K, W_H=None, *, output_multiplier=1.0, final_log
     _need(h, "h", torch.bfloat16, 2)
     _need(W_lm, "W_lm", torch.bfloat16, 2)
     P, D = h.shape
-    r = 0 if W_H is None else W_H.shape[0]
+    if W_lm.shape[1] != D:
+        raise ValueError("W_lm must be [V, D]")
+    r = 0
+    if W_H is not None:
+        _need(W_H, "W_H", torch.bfloat16, 2)
+        r = W_H.shape[0]
+        if W_H.shape[1] != D:
+            raise ValueError("W_H must be [r, D]")
+    dev = _device(h, W_lm=W_lm, W_H=W_H)
     if out is None:
-        ids = torch.empty((P, K), dtype=torch.int32, device=h.device)
-        vals = torch.empty((P, K), dtype=torch.float32, device=h.device)
-        G = torch.empty((P, r), dtype=torch.float32, device=h.device) if r else None
+        ids = torch.empty((P, K), dtype=torch.int32, device=dev)
+        vals = torch.empty((P, K), dtype=torch.float32, device=dev)
+        G = torch.empty((P, r), dtype=torch.float32, device=dev) if r else None
     else:
         ids, vals, G = out
+        _out(ids, "ids", torch.int32, P * K, dev)
+        _out(vals, "vals", torch.float32, P * K, dev)
+        if r:
+            _out(G, "G", torch.float32, P * r, dev)
+    _status(dev_status, dev)
     rc = lib().dflash2_unary_topk_noalloc(_p(h), P, D, _p(W_lm), W_lm.shape[0], int(K),
                                           float(output_multiplier), float(final_logit_softcapping), _p(W_H), r,
-                                          _p(G), _p(ids), _p(vals), _p(dev_status), _stream(stream))
+                                          _p(G), _p(ids), _p(vals), _p(dev_status), _stream(stream, dev))
     _check("dflash2_unary_topk_noalloc", rc)
     return ids, vals, G
 
@@ -165,14 +231,19 @@ def selector_walk(anchors, topk_ids, topk_vals, G, A, Bc, block_size, *, dev_sta
         raise ValueError("candidate / gate shapes do not match [R*B, K] / [R*B, r]")
     if tuple(Bc.shape) != (V, r):
         raise ValueError("Bc must be [V, r] like A")
+    dev = _device(anchors, topk_ids=topk_ids, topk_vals=topk_vals, G=G, A=A, Bc=Bc)
+    T = max(B - 1, 0)
     if out is None:
-        path = torch.empty((R, B - 1), dtype=torch.int32, device=anchors.device)
-        scores = torch.empty((R, B - 1), dtype=torch.float32, device=anchors.device)
+        path = torch.empty((R, T), dtype=torch.int32, device=dev)
+        scores = torch.empty((R, T), dtype=torch.float32, device=dev)
     else:
         path, scores = out
+        _out(path, "path", torch.int32, R * T, dev)
+        _out(scores, "path_scores", torch.float32, R * T, dev)
+    _status(dev_status, dev)
     rc = lib().dflash2_selector_walk(_p(anchors), R, B, _p(topk_ids), _p(topk_vals), _p(G), _p(A),
                                      _p(Bc), V, K, r, _p(path), _p(scores), _p(dev_status),
-                                     _stream(stream))
+                                     _stream(stream, dev))
     _check("dflash2_selector_walk", rc)
     return path, scores
 
@@ -188,12 +259,16 @@ def selector_ce(scores, topk_ids, targets, V, *, dev_status=None, out=None, stre
     K = topk_ids.shape[-1]
     if topk_ids.numel() != P * K or scores.numel() != P * K:
         raise ValueError("scores / topk_ids do not match [P, K]")
+    dev = _device(scores, topk_ids=topk_ids, targets=targets)
     if out is None:
-        out = (torch.empty((P,), dtype=torch.float32, device=scores.device),
-               torch.empty((P,), dtype=torch.int32, device=scores.device))
+        out = (torch.empty((P,), dtype=torch.float32, device=dev),
+               torch.empty((P,), dtype=torch.int32, device=dev))
     loss, label = out
+    _out(loss, "loss", torch.float32, P, dev)
+    _out(label, "label", torch.int32, P, dev)
+    _status(dev_status, dev)
     rc = lib().dflash2_selector_ce(_p(scores), _p(topk_ids), _p(targets), P, K, int(V), _p(loss), _p(label),
-                                   _p(dev_status), _stream(stream))
+                                   _p(dev_status), _stream(stream, dev))
     _check("dflash2_selector_ce", rc)
     return loss, label
 
@@ -212,10 +287,17 @@ def selector_pair_scores(pred, topk_ids, topk_vals, G, A, Bc, *, dev_status=None
     V, r = A.shape
     if topk_ids.numel() != P * K or topk_vals.numel() != P * K or G.numel() != P * r:
         raise ValueError("candidate / gate shapes do not match [P, K] / [P, r]")
-    scores = out if out is not None else torch.empty((P, K), dtype=torch.float32, device=pred.device)
+    if tuple(Bc.shape) != (V, r):
+        raise ValueError("Bc must be [V, r] like A")
+    dev = _device(pred, topk_ids=topk_ids, topk_vals=topk_vals, G=G, A=A, Bc=Bc)
+    if out is None:
+        scores = torch.empty((P, K), dtype=torch.float32, device=dev)
+    else:
+        scores = _out(out, "scores", torch.float32, P * K, dev)
+    _status(dev_status, dev)
     rc = lib().dflash2_selector_pair_scores(_p(pred), P, _p(topk_ids), _p(topk_vals), _p(G), _p(A),
                                             _p(Bc), V, K, r, _p(scores), _p(dev_status),
-                                            _stream(stream))
+                                            _stream(stream, dev))
     _check("dflash2_selector_pair_scores", rc)
     return scores
 
@@ -248,21 +330,30 @@ def draft_head(h, W_lm, K, W_H, A, Bc, anchors, block_size, pred=None, *, output
         _need(pred, "pred", torch.int32, 1)
         if pred.shape[0] != P:
             raise ValueError("pred must be [R*B]")
-    dev = h.device
+    dev = _device(h, W_lm=W_lm, W_H=W_H, A=A, Bc=Bc, anchors=anchors, pred=pred)
+    T = max(B - 1, 0)
     if out is None:
         e = torch.empty
         out = (e((P, K), dtype=torch.int32, device=dev), e((P, K), dtype=torch.float32, device=dev),
-               e((P, r), dtype=torch.float32, device=dev), e((R, B - 1), dtype=torch.int32, device=dev),
-               e((R, B - 1), dtype=torch.float32, device=dev),
+               e((P, r), dtype=torch.float32, device=dev), e((R, T), dtype=torch.int32, device=dev),
+               e((R, T), dtype=torch.float32, device=dev),
                e((P, K), dtype=torch.float32, device=dev) if pred is not None else None)
     ids, vals, G, path, ps, pair = out
-    need = draft_head_workspace_size(R, B, D, V, K, r)
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _out(ids, "ids", torch.int32, P * K, dev)
+    _out(vals, "vals", torch.float32, P * K, dev)
+    _out(G, "G", torch.float32, P * r, dev)
+    _out(path, "path", torch.int32, R * T, dev)
+    _out(ps, "path_scores", torch.float32, R * T, dev)
+    if pred is not None:
+        _out(pair, "pair_scores", torch.float32, P * K, dev)
+    _status(dev_status, dev)
+    workspace = _workspace(draft_head_workspace_size(R, B, D, V, K, r), workspace, dev)
+    if workspace is None:  # nothing to hold (R = 0): the call still takes a buffer
+        workspace = torch.empty(1, dtype=torch.uint8, device=dev)
     rc = lib().dflash2_draft_head(_p(h), R, B, D, _p(W_lm), V, K, float(output_multiplier),
                                   float(final_logit_softcapping), _p(W_H), r, _p(A), _p(Bc), _p(anchors),
                                   _p(pred), _p(ids), _p(vals), _p(G), _p(path), _p(ps), _p(pair),
-                                  _p(workspace), workspace.numel(), _p(dev_status), _stream(stream))
+                                  _p(workspace), _nbytes(workspace), _p(dev_status), _stream(stream, dev))
     _check("dflash2_draft_head", rc)
     return ids, vals, G, path, ps, pair
 
@@ -284,13 +375,13 @@ def selector_lattice(anchors, topk_ids, topk_vals, G, A, Bc, block_size, *, dev_
         raise ValueError("candidate / gate shapes do not match [R*B, K] / [R*B, r]")
     if tuple(Bc.shape) != (V, r):
         raise ValueError("Bc must be [V, r] like A")
-    lat = out if out is not None else torch.empty((R, B - 1, K, K), dtype=torch.float32,
-                                                  device=anchors.device)
-    _need(lat, "lattice", torch.float32)
-    if lat.numel() != R * (B - 1) * K * K:
-        raise ValueError("lattice must hold [R, B-1, K, K]")
+    dev = _device(anchors, topk_ids=topk_ids, topk_vals=topk_vals, G=G, A=A, Bc=Bc)
+    T = max(B - 1, 0)
+    lat = out if out is not None else torch.empty((R, T, K, K), dtype=torch.float32, device=dev)
+    _out(lat, "lattice", torch.float32, R * T * K * K, dev)
+    _status(dev_status, dev)
     rc = lib().dflash2_selector_lattice(_p(anchors), R, B, _p(topk_ids), _p(topk_vals), _p(G), _p(A),
-                                        _p(Bc), V, K, r, _p(lat), _p(dev_status), _stream(stream))
+                                        _p(Bc), V, K, r, _p(lat), _p(dev_status), _stream(stream, dev))
     _check("dflash2_selector_lattice", rc)
     return lat
 
@@ -309,14 +400,18 @@ def lattice_walk(lattice, topk_ids, block_size, vocab_size, *, uniforms=None, te
         _need(uniforms, "uniforms", torch.float32)
         if uniforms.numel() != R * T:
             raise ValueError("uniforms must be [R, B-1]")
+    dev = _device(lattice, topk_ids=topk_ids, uniforms=uniforms)
     if out is None:
-        path = torch.empty((R, T), dtype=torch.int32, device=lattice.device)
-        scores = torch.empty((R, T), dtype=torch.float32, device=lattice.device)
+        path = torch.empty((R, T), dtype=torch.int32, device=dev)
+        scores = torch.empty((R, T), dtype=torch.float32, device=dev)
     else:
         path, scores = out
+        _out(path, "path", torch.int32, R * T, dev)
+        _out(scores, "path_scores", torch.float32, R * T, dev)
+    _status(dev_status, dev)
     rc = lib().dflash2_lattice_walk(_p(lattice), _p(topk_ids), R, B, K, int(vocab_size), _p(uniforms),
                                     float(temperature), _p(path), _p(scores), _p(dev_status),
-                                    _stream(stream))
+                                    _stream(stream, dev))
     _check("dflash2_lattice_walk", rc)
     return path, scores
 
@@ -327,6 +422,19 @@ def _act_dtype(x):
     if x.dtype == torch.float32:
         return DF2_DTYPE_F32
     raise TypeError("conv activations must be bfloat16 or float32")
+
+
+def _conv_shapes(C, taps, group, **named):
+    """The conv's weight and correction shapes (skipped when taps or group are
+    themselves invalid: the library rejects those with a status)."""
+    if not (taps >= 1 and group >= 1 and C % group == 0):
+        return
+    G = C // group
+    want = {"W_proj": (2 * taps * G, C), "base": (2, taps, C), "base_next": (2, taps, C)}
+    for name, (t, P) in named.items():
+        shape = (P, taps, G) if name == "dyn_out" else want[name]
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}, got {list(t.shape)}")
 
 
 def conv_prepare_workspace_size(P, C, taps, group, dtype=DF2_DTYPE_BF16) -> int:
@@ -340,16 +448,21 @@ def conv_prepare(x, block_size, taps, group, W_proj, base, *, workspace=None, ou
     _need(W_proj, "W_proj", torch.bfloat16, 2)
     _need(base, "base", torch.float32, 3)
     P, C = x.shape
-    G = C // group
+    taps, group = int(taps), int(group)
+    _conv_shapes(C, taps, group, W_proj=(W_proj, P), base=(base, P))
+    G = C // group if group >= 1 else 0
+    dev = _device(x, W_proj=W_proj, base=base)
     if out is None:
         y = torch.empty_like(x)
-        dyn = torch.empty((P, taps, G), dtype=torch.float32, device=x.device)
+        dyn = torch.empty((P, taps, G), dtype=torch.float32, device=dev)
     else:
         y, dyn = out
-    ws = _workspace(conv_prepare_workspace_size(P, C, taps, group, dt), workspace, x.device)
-    rc = lib().dflash2_conv_prepare(_p(x), dt, P, C, int(block_size), int(taps), int(group),
+        _out(y, "y", x.dtype, P * C, dev)
+        _out(dyn, "dyn_out", torch.float32, P * max(taps, 0) * G, dev)
+    ws = _workspace(conv_prepare_workspace_size(P, C, taps, group, dt), workspace, dev)
+    rc = lib().dflash2_conv_prepare(_p(x), dt, P, C, int(block_size), taps, group,
                                     _p(W_proj), _p(base), _p(y), _p(dyn), _p(ws),
-                                    0 if ws is None else ws.numel(), _stream(stream))
+                                    _nbytes(ws), _stream(stream, dev))
     _check("dflash2_conv_prepare", rc)
     return y, dyn
 
@@ -361,9 +474,12 @@ def conv_finish(z, block_size, taps, group, dyn_out, base, *, out=None, stream=N
     _need(dyn_out, "dyn_out", torch.float32, 3)
     _need(base, "base", torch.float32, 3)
     P, C = z.shape
-    y = out if out is not None else torch.empty_like(z)
-    rc = lib().dflash2_conv_finish(_p(z), dt, P, C, int(block_size), int(taps), int(group),
-                                   _p(dyn_out), _p(base), _p(y), _stream(stream))
+    taps, group = int(taps), int(group)
+    _conv_shapes(C, taps, group, dyn_out=(dyn_out, P), base=(base, P))
+    dev = _device(z, dyn_out=dyn_out, base=base)
+    y = _out(out, "y", z.dtype, P * C, dev) if out is not None else torch.empty_like(z)
+    rc = lib().dflash2_conv_finish(_p(z), dt, P, C, int(block_size), taps, group,
+                                   _p(dyn_out), _p(base), _p(y), _stream(stream, dev))
     _check("dflash2_conv_finish", rc)
     return y
 
@@ -384,16 +500,22 @@ def conv_finish_prepare(z, block_size, taps, group, dyn_out, base, W_proj, base_
         if residual.shape != z.shape:
             raise ValueError("residual must have z's shape")
     P, C = z.shape
-    G = C // group
+    taps, group = int(taps), int(group)
+    _conv_shapes(C, taps, group, dyn_out=(dyn_out, P), base=(base, P), W_proj=(W_proj, P),
+                 base_next=(base_next, P))
+    G = C // group if group >= 1 else 0
+    dev = _device(z, dyn_out=dyn_out, base=base, W_proj=W_proj, base_next=base_next, residual=residual)
     if out is None:
         h, y = torch.empty_like(z), torch.empty_like(z)
-        dyn = torch.empty((P, taps, G), dtype=torch.float32, device=z.device)
+        dyn = torch.empty((P, taps, G), dtype=torch.float32, device=dev)
     else:
         h, y, dyn = out
-    ws = _workspace(int(lib().dflash2_conv_finish_prepare_workspace_size(P, C, taps, group, dt)), workspace,
-                    z.device)
-    rc = lib().dflash2_conv_finish_prepare(_p(z), dt, P, C, int(block_size), int(taps), int(group), _p(dyn_out),
+        _out(h, "h", z.dtype, P * C, dev)
+        _out(y, "y_next", z.dtype, P * C, dev)
+        _out(dyn, "dyn_out_next", torch.float32, P * max(taps, 0) * G, dev)
+    ws = _workspace(int(lib().dflash2_conv_finish_prepare_workspace_size(P, C, taps, group, dt)), workspace, dev)
+    rc = lib().dflash2_conv_finish_prepare(_p(z), dt, P, C, int(block_size), taps, group, _p(dyn_out),
                                            _p(base), _p(residual), _p(h), _p(W_proj), _p(base_next), _p(y),
-                                           _p(dyn), _p(ws), 0 if ws is None else ws.numel(), _stream(stream))
+                                           _p(dyn), _p(ws), _nbytes(ws), _stream(stream, dev))
     _check("dflash2_conv_finish_prepare", rc)
     return h, y, dyn
