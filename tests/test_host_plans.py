@@ -11,6 +11,11 @@ wide sweep:
   `tile_rows`): the tiles cover rows 0 .. V-1 once each, in order, none of them
   empty, none taller than the MMA's 128 rows, the W_H tiles after them, and every
   CTA streams the same number of tiles whenever the tiling is not the plain one;
+- the batch-1 head's plan and shared-memory layout (`pick_plan`, `smem_layout`) for
+  every supported (positions, K): it fits the 227 KB a CTA may have, the stages
+  start on 1024-byte swizzle boundaries, and the end-of-kernel list exchange, which
+  reuses the start of the W stage ring, stays inside that ring (clear of the h
+  stages and the barriers other warps may still be waiting on);
 - the many-row conv prepare's schedule (`ctc_split_last_round` and the kernel's
   `tile(k)`), for single CTAs, CTA pairs and clusters of two pairs, with and without
   the last round in half tiles: every (128-row tile, channel group) pair of the
@@ -105,6 +110,44 @@ namespace head {{
 {_block(head, "struct VTiling {")}
 {_block(head, "VTiling v_tiling(int64_t V, int n_wh, int grid) {")}
 }}  // namespace head
+
+namespace headplan {{
+{_line(head, "constexpr int BM = ")}
+{_line(head, "constexpr int BK = ")}
+{_line(head, "constexpr int kEpiWarps = ")}
+{_line(head, "constexpr uint32_t kWBytes = ")}
+{_line(head, "constexpr int kMaxStages = ")}
+{_line(head, "constexpr int kMaxK = ")}
+{_line(head, "#define DF2_HEAD_KBOX ")}
+#define __host__
+#define __device__
+{_block(head, "struct SmemLayout {")}
+{_block(head, "__host__ __device__ inline SmemLayout smem_layout(int N, int R, int nstages, int kbox) {")}
+#undef __host__
+#undef __device__
+{_line(head, "int pick_n(int64_t P) {")}
+{_block(head, "struct Plan {")}
+{_block(head, "Plan pick_plan(int64_t P, int K) {")}
+}}  // namespace headplan
+
+// 0 when every supported (P, K) gets a plan that fits and keeps its regions apart;
+// else 1000 * P + K of the first that does not
+extern "C" int head_plans() {{
+    using namespace headplan;
+    for (int P = 1; P <= 32; ++P)
+        for (int K = 1; K <= kMaxK; ++K) {{
+            if (!(P <= 16 || K <= 32)) continue;   // not taken by this kernel
+            const Plan pl = pick_plan(P, K);
+            if (pl.nstages < 2) return 1000 * P + K;
+            const SmemLayout L = smem_layout(pl.N, pl.R, pl.nstages, pl.kbox);
+            const uint32_t xch = uint32_t(kEpiWarps * pl.N * pl.R * 32) * 8;
+            if (L.total + 1024 > 227u * 1024u) return 1000 * P + K;
+            if (L.stage_w % 1024 || L.h_off % 1024 || L.stage_h % 1024 || L.bar_off % 8) return 1000 * P + K;
+            if (xch > L.h_off) return 1000 * P + K;   // the exchange would reach the h stages or barriers
+            if (pl.N < P || (K > 32 && pl.R < 2)) return 1000 * P + K;
+        }}
+    return 0;
+}}
 
 // 0, or the first V of [V0, V1) (step) whose tiling breaks a rule
 extern "C" int64_t head_sweep(int64_t V0, int64_t V1, int64_t step, int sms, int n_wh) {{
@@ -416,6 +459,7 @@ def plans(tmp_path_factory):
     lib = d / "libplans.so"
     subprocess.run([cxx, "-std=c++17", "-O2", "-shared", "-fPIC", "-o", str(lib), str(src)], check=True)
     so = ctypes.CDLL(str(lib))
+    so.head_plans.restype = ctypes.c_int
     so.head_sweep.restype = ctypes.c_int64
     so.head_sweep.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
     so.wide_cover.restype = ctypes.c_int
@@ -426,6 +470,10 @@ def plans(tmp_path_factory):
     so.conv_cover.restype = ctypes.c_int
     so.conv_cover.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
     return so
+
+
+def test_head_plan_and_shared_memory(plans):
+    assert plans.head_plans() == 0
 
 
 @pytest.mark.parametrize("n_wh", [0, 1, 2, 32])   # no W_H; r = 128, 256, 4096
