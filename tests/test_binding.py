@@ -98,6 +98,20 @@ def test_valid_calls_reach_the_library_with_their_outputs(fake):
                      "dflash2_conv_finish_prepare"]
 
 
+def test_no_alloc_call_checks_its_inputs_and_outputs(fake):
+    ids, vals, G = df2.unary_topk_noalloc(*head_args())
+    assert ids.shape == (P, K) and G.shape == (P, r)
+    assert fake.calls[-1][0] == "dflash2_unary_topk_noalloc"
+    n = len(fake.calls)
+    with pytest.raises(ValueError):
+        df2.unary_topk_noalloc(bf(P, D), bf(V, D + 8), K)                  # W_lm not [V, D]
+    with pytest.raises(ValueError):
+        df2.unary_topk_noalloc(bf(P, D), bf(V, D), K, bf(r, D - 8))         # W_H not [r, D]
+    with pytest.raises(ValueError):
+        df2.unary_topk_noalloc(*head_args(), out=(i32(P, K), f32(P, K), f32(P, r - 1)))
+    assert len(fake.calls) == n
+
+
 def test_workspace_sizes_are_passed_in_bytes(fake):
     ws = torch.zeros(64, dtype=torch.float32)   # 256 bytes in 64 elements
     df2.unary_topk(*head_args(), workspace=ws)
